@@ -1,0 +1,352 @@
+// KATA oracle: a plain, slow, fp64 CPU restatement of the causal normalised
+// linear-attention forward of "Kernelized Linear Attention: Breaking the
+// Capacity Wall with Symmetric Cones" (arXiv 2607.17419).
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+// load this file; only the test suite, the smoke check and the benchmark's
+// CPU-baseline leg use it.  It shares no code, header or constant with the
+// CUDA library.
+//
+// Every function works on fp64 arrays in the layout the library documents:
+//   q, k : [B, H, T, p]      v, o : [B, H, T, dv]
+//   packed state S : [n, dv] with n = p(p+1)/2, z : [n]
+//   packed index of (i, j), i <= j : row-major upper triangle
+//        idx(i, j) = i*p - i*(i-1)/2 + (j - i)
+// Plain loops, no BLAS, no blocking; threads only split independent heads.
+//
+// Citations are to the arXiv HTML page of the paper (section / equation):
+//   * unit-sphere projection and the rank-one lift psi(u) = u u^T with
+//     ||u u^T||_F = 1 and <u u^T, v v^T>_F = (u.v)^2: the "rank-one lift"
+//     paragraph after Eq. 8;
+//   * packed width n = p(p+1)/2: Eq. 8 and the state-size paragraph
+//     ("n = d(d+1)/2 unique coordinates after symmetry packing");
+//   * state S_t = Psi(K_{1:t})^T V_{1:t}: state-size paragraph;
+//   * normalised readout psi(q_t)^T S_t / psi(q_t)^T Z_t: the discussion of
+//     Assumption 1 (denominator psi(q_t)^T Z_t) and the convex output gate;
+//   * chunked form: per-chunk local states, an associative prefix over the
+//     N_C chunks (sequential, or a scan in ceil(log2 N_C) rounds of
+//     N_C-wide work) and a per-chunk output that adds the local C x C
+//     causal part: the chunked-scan paragraph (the one introducing the
+//     three kernels and the wall-clock model).
+//
+// Readings where the pages are silent (each is listed in the design doc):
+//   * off-diagonal packed coordinates carry a factor sqrt(2), diagonal 1, so
+//     the packed dot product is the Frobenius product;
+//   * q and k are normalised inside the forward; a zero vector stays zero;
+//   * causality is inclusive (s <= t, "K_{1:t}");
+//   * a zero denominator gives a zero output row (no epsilon);
+//   * the chunk output uses the exclusive prefix of earlier chunks plus the
+//     inclusive causal part of its own chunk; a ragged last chunk is shorter.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+#include <algorithm>
+
+namespace {
+
+inline int64_t packed_dim_i(int p) { return (int64_t)p * (p + 1) / 2; }
+
+inline int64_t pidx(int p, int i, int j) {  // requires i <= j
+    return (int64_t)i * p - (int64_t)i * (i - 1) / 2 + (j - i);
+}
+
+// u = x / ||x||; the zero vector maps to zero.
+void normalize(const double* x, int p, double* u) {
+    double ss = 0.0;
+    for (int i = 0; i < p; ++i) ss += x[i] * x[i];
+    double nrm = std::sqrt(ss);
+    for (int i = 0; i < p; ++i) u[i] = nrm > 0.0 ? x[i] / nrm : 0.0;
+}
+
+// psi(u) = u u^T packed: diagonal u_i^2, off-diagonal sqrt(2) u_i u_j.
+void lift(const double* u, int p, double* psi) {
+    const double r2 = std::sqrt(2.0);
+    for (int i = 0; i < p; ++i)
+        for (int j = i; j < p; ++j)
+            psi[pidx(p, i, j)] = (i == j) ? u[i] * u[i] : r2 * u[i] * u[j];
+}
+
+double dot(const double* a, const double* b, int64_t n) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+// Run f(head) for head in [0, heads) on up to nthreads threads.
+template <class F>
+void for_heads(int64_t heads, int nthreads, F f) {
+    if (nthreads <= 0) nthreads = (int)std::max(1u, std::thread::hardware_concurrency());
+    nthreads = (int)std::min<int64_t>(nthreads, std::max<int64_t>(heads, 1));
+    if (nthreads <= 1) {
+        for (int64_t h = 0; h < heads; ++h) f(h);
+        return;
+    }
+    std::vector<std::thread> pool;
+    for (int w = 0; w < nthreads; ++w)
+        pool.emplace_back([&, w] {
+            for (int64_t h = w; h < heads; h += nthreads) f(h);
+        });
+    for (auto& th : pool) th.join();
+}
+
+// Normalise every row of a [rows, p] block.
+std::vector<double> normalized_rows(const double* x, int64_t rows, int p) {
+    std::vector<double> u((size_t)(rows * p));
+    for (int64_t r = 0; r < rows; ++r) normalize(x + r * p, p, u.data() + r * p);
+    return u;
+}
+
+// Exclusive prefix over `nc` items of width `w`, sequential: one step per item.
+void exclusive_sequential(const double* x, int64_t nc, int64_t w, double* out) {
+    std::vector<double> run((size_t)w, 0.0);
+    for (int64_t c = 0; c < nc; ++c) {
+        for (int64_t e = 0; e < w; ++e) out[c * w + e] = run[e];
+        for (int64_t e = 0; e < w; ++e) run[e] += x[c * w + e];
+    }
+}
+
+// Exclusive prefix by a log-depth scan: ceil(log2 nc) rounds, each round adds
+// to every item the item 2^d places earlier (read from the previous round),
+// giving the inclusive prefix; the exclusive prefix is that shifted by one.
+// Returns the number of rounds.
+int exclusive_tree(const double* x, int64_t nc, int64_t w, double* out) {
+    std::vector<double> cur(x, x + nc * w), nxt((size_t)(nc * w));
+    int rounds = 0;
+    for (int64_t d = 1; d < nc; d <<= 1) {
+        for (int64_t c = 0; c < nc; ++c)
+            for (int64_t e = 0; e < w; ++e)
+                nxt[c * w + e] = cur[c * w + e] + (c >= d ? cur[(c - d) * w + e] : 0.0);
+        cur.swap(nxt);
+        ++rounds;
+    }
+    for (int64_t e = 0; e < w; ++e) out[e] = 0.0;
+    for (int64_t c = 1; c < nc; ++c)
+        for (int64_t e = 0; e < w; ++e) out[c * w + e] = cur[(c - 1) * w + e];
+    return rounds;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kor_packed_dim(int p) { return (int)packed_dim_i(p); }
+
+void kor_normalize(const double* x, int p, double* u) { normalize(x, p, u); }
+
+void kor_lift(const double* u, int p, double* psi) { lift(u, p, psi); }
+
+// The plain definition, every row:
+//   o_t = sum_{s<=t} (qh_t . kh_s)^2 v_s / sum_{s<=t} (qh_t . kh_s)^2.
+int kor_forward_plain(const double* q, const double* k, const double* v, int B, int H, int T,
+                      int p, int dv, double* o, int nthreads) {
+    const int64_t heads = (int64_t)B * H;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const double* qh = q + bh * T * p;
+        const double* kh = k + bh * T * p;
+        const double* vh = v + bh * T * dv;
+        double* oh = o + bh * T * dv;
+        std::vector<double> qu = normalized_rows(qh, T, p), ku = normalized_rows(kh, T, p);
+        std::vector<double> num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            std::fill(num.begin(), num.end(), 0.0);
+            double den = 0.0;
+            for (int s = 0; s <= t; ++s) {
+                double c = dot(&qu[(size_t)t * p], &ku[(size_t)s * p], p);
+                double w = c * c;
+                den += w;
+                for (int j = 0; j < dv; ++j) num[j] += w * vh[(int64_t)s * dv + j];
+            }
+            for (int j = 0; j < dv; ++j) oh[(int64_t)t * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+    });
+    return 0;
+}
+
+// The plain definition for selected rows only: row r is head bh[r] (= b*H + h),
+// position t[r]; its dv outputs go to out[r*dv ...].  Cost O(t (p + dv)) per row.
+int kor_forward_plain_rows(const double* q, const double* k, const double* v, int B, int H,
+                           int T, int p, int dv, const int64_t* bh, const int64_t* t, int64_t nrows,
+                           double* out, int nthreads) {
+    for_heads(nrows, nthreads, [&](int64_t r) {
+        const double* qh = q + bh[r] * T * p;
+        const double* kh = k + bh[r] * T * p;
+        const double* vh = v + bh[r] * T * dv;
+        std::vector<double> qu((size_t)p), ku((size_t)p), num((size_t)dv, 0.0);
+        normalize(qh + t[r] * p, p, qu.data());
+        double den = 0.0;
+        for (int64_t s = 0; s <= t[r]; ++s) {
+            normalize(kh + s * p, p, ku.data());
+            double c = dot(qu.data(), ku.data(), p);
+            double w = c * c;
+            den += w;
+            for (int j = 0; j < dv; ++j) num[j] += w * vh[s * dv + j];
+        }
+        for (int j = 0; j < dv; ++j) out[r * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+    });
+    (void)B;
+    (void)H;
+    return 0;
+}
+
+// Token-recurrent form in the explicit packed lift:
+//   S += psi(kh_t) v_t^T,  z += psi(kh_t),  o_t = psi(qh_t)^T S / psi(qh_t)^T z.
+// S0 [B,H,n,dv] / z0 [B,H,n] are the optional initial state (NULL = zero);
+// S_final / z_final receive the state after the last token (NULL = skipped).
+int kor_forward_recurrent(const double* q, const double* k, const double* v, int B, int H, int T,
+                          int p, int dv, const double* S0, const double* z0, double* o,
+                          double* S_final, double* z_final, int nthreads) {
+    const int64_t heads = (int64_t)B * H, n = packed_dim_i(p);
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        std::vector<double> S((size_t)(n * dv), 0.0), z((size_t)n, 0.0);
+        if (S0) std::copy(S0 + bh * n * dv, S0 + (bh + 1) * n * dv, S.begin());
+        if (z0) std::copy(z0 + bh * n, z0 + (bh + 1) * n, z.begin());
+        std::vector<double> u((size_t)p), pk((size_t)n), pq((size_t)n), num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            const double* kt = k + (bh * T + t) * p;
+            const double* qt = q + (bh * T + t) * p;
+            const double* vt = v + (bh * T + t) * dv;
+            normalize(kt, p, u.data());
+            lift(u.data(), p, pk.data());
+            for (int64_t a = 0; a < n; ++a) {
+                for (int j = 0; j < dv; ++j) S[a * dv + j] += pk[a] * vt[j];
+                z[a] += pk[a];
+            }
+            normalize(qt, p, u.data());
+            lift(u.data(), p, pq.data());
+            std::fill(num.begin(), num.end(), 0.0);
+            for (int64_t a = 0; a < n; ++a)
+                for (int j = 0; j < dv; ++j) num[j] += pq[a] * S[a * dv + j];
+            double den = dot(pq.data(), z.data(), n);
+            double* ot = o + (bh * T + t) * dv;
+            for (int j = 0; j < dv; ++j) ot[j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+        if (S_final) std::copy(S.begin(), S.end(), S_final + bh * n * dv);
+        if (z_final) std::copy(z.begin(), z.end(), z_final + bh * n);
+    });
+    return 0;
+}
+
+// Per-chunk local states of chunk length C (the last chunk may be shorter):
+//   S_loc[c] = sum_{s in chunk c} psi(kh_s) v_s^T,  z_loc[c] = sum psi(kh_s).
+// Outputs S_loc [B,H,NC,n,dv], z_loc [B,H,NC,n], NC = ceil(T / C).
+int kor_chunk_states(const double* k, const double* v, int B, int H, int T, int p, int dv, int C,
+                     double* S_loc, double* z_loc, int nthreads) {
+    const int64_t heads = (int64_t)B * H, n = packed_dim_i(p);
+    const int64_t NC = (T + C - 1) / C;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        std::vector<double> u((size_t)p), pk((size_t)n);
+        for (int64_t c = 0; c < NC; ++c) {
+            double* S = S_loc + (bh * NC + c) * n * dv;
+            double* z = z_loc + (bh * NC + c) * n;
+            std::fill(S, S + n * dv, 0.0);
+            std::fill(z, z + n, 0.0);
+            for (int64_t s = c * C; s < std::min<int64_t>((c + 1) * C, T); ++s) {
+                normalize(k + (bh * T + s) * p, p, u.data());
+                lift(u.data(), p, pk.data());
+                const double* vs = v + (bh * T + s) * dv;
+                for (int64_t a = 0; a < n; ++a) {
+                    for (int j = 0; j < dv; ++j) S[a * dv + j] += pk[a] * vs[j];
+                    z[a] += pk[a];
+                }
+            }
+        }
+    });
+    return 0;
+}
+
+// Exclusive prefix of chunk states over the chunk axis, mode 0 = sequential
+// (N_C steps), mode 1 = log-depth scan (ceil(log2 N_C) rounds).
+// Returns the number of rounds (steps) taken for one head.
+int kor_scan_exclusive(const double* S_loc, const double* z_loc, int B, int H, int NC, int n,
+                       int dv, int mode, double* S_prefix, double* z_prefix, int nthreads) {
+    const int64_t heads = (int64_t)B * H;
+    std::vector<int> rounds((size_t)std::max<int64_t>(heads, 1), 0);
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const int64_t ws = (int64_t)n * dv;
+        if (mode == 0) {
+            exclusive_sequential(S_loc + bh * NC * ws, NC, ws, S_prefix + bh * NC * ws);
+            exclusive_sequential(z_loc + bh * NC * n, NC, n, z_prefix + bh * NC * n);
+            rounds[bh] = NC;
+        } else {
+            rounds[bh] = exclusive_tree(S_loc + bh * NC * ws, NC, ws, S_prefix + bh * NC * ws);
+            exclusive_tree(z_loc + bh * NC * n, NC, n, z_prefix + bh * NC * n);
+        }
+    });
+    return heads > 0 ? rounds[0] : 0;
+}
+
+// Chunked form: local chunk states, exclusive prefix over chunks (mode as in
+// kor_scan_exclusive) seeded with the optional initial state, then for each
+// token t of chunk c
+//   num = psi(qh_t)^T P_c + sum_{s in c, s<=t} <psi(qh_t), psi(kh_s)> v_s
+//   den = psi(qh_t)^T Pz_c + sum_{s in c, s<=t} <psi(qh_t), psi(kh_s)>
+//   o_t = num / den.
+// The intra-chunk scores use the lifted features, as the chunk output
+// combines the prefix with the local C x C causal pattern.
+int kor_forward_chunked(const double* q, const double* k, const double* v, int B, int H, int T,
+                        int p, int dv, int C, int mode, const double* S0, const double* z0,
+                        double* o, double* S_final, double* z_final, int nthreads) {
+    const int64_t heads = (int64_t)B * H, n = packed_dim_i(p);
+    const int64_t NC = (T + C - 1) / C, ws = n * dv;
+    if (T <= 0) {
+        for (int64_t bh = 0; bh < heads; ++bh) {
+            if (S_final)
+                for (int64_t e = 0; e < ws; ++e) S_final[bh * ws + e] = S0 ? S0[bh * ws + e] : 0.0;
+            if (z_final)
+                for (int64_t e = 0; e < n; ++e) z_final[bh * n + e] = z0 ? z0[bh * n + e] : 0.0;
+        }
+        return 0;
+    }
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        // 1. local chunk states
+        std::vector<double> Sl((size_t)(NC * ws)), zl((size_t)(NC * n));
+        kor_chunk_states(k + bh * T * p, v + bh * T * dv, 1, 1, T, p, dv, C, Sl.data(), zl.data(), 1);
+        // 2. exclusive prefix, then add the initial state
+        std::vector<double> P((size_t)(NC * ws)), Pz((size_t)(NC * n));
+        kor_scan_exclusive(Sl.data(), zl.data(), 1, 1, (int)NC, (int)n, dv, mode, P.data(), Pz.data(), 1);
+        if (S0)
+            for (int64_t c = 0; c < NC; ++c)
+                for (int64_t e = 0; e < ws; ++e) P[c * ws + e] += S0[bh * ws + e];
+        if (z0)
+            for (int64_t c = 0; c < NC; ++c)
+                for (int64_t e = 0; e < n; ++e) Pz[c * n + e] += z0[bh * n + e];
+        // 3. per-chunk output: prefix readout + local causal part
+        std::vector<double> u((size_t)p), pq((size_t)n), num((size_t)dv);
+        std::vector<double> pk((size_t)(C * n));
+        for (int64_t c = 0; c < NC; ++c) {
+            const int64_t t0 = c * C, t1 = std::min<int64_t>(t0 + C, T);
+            for (int64_t s = t0; s < t1; ++s) {
+                normalize(k + (bh * T + s) * p, p, u.data());
+                lift(u.data(), p, &pk[(size_t)((s - t0) * n)]);
+            }
+            for (int64_t t = t0; t < t1; ++t) {
+                normalize(q + (bh * T + t) * p, p, u.data());
+                lift(u.data(), p, pq.data());
+                std::fill(num.begin(), num.end(), 0.0);
+                for (int64_t a = 0; a < n; ++a)
+                    for (int j = 0; j < dv; ++j) num[j] += pq[a] * P[c * ws + a * dv + j];
+                double den = dot(pq.data(), &Pz[(size_t)(c * n)], n);
+                for (int64_t s = t0; s <= t; ++s) {
+                    double w = dot(pq.data(), &pk[(size_t)((s - t0) * n)], n);
+                    den += w;
+                    for (int j = 0; j < dv; ++j) num[j] += w * v[(bh * T + s) * dv + j];
+                }
+                double* ot = o + (bh * T + t) * dv;
+                for (int j = 0; j < dv; ++j) ot[j] = den > 0.0 ? num[j] / den : 0.0;
+            }
+        }
+        // 4. final state = last prefix + last local state (+ initial state, already in P)
+        if (S_final)
+            for (int64_t e = 0; e < ws; ++e)
+                S_final[bh * ws + e] = P[(NC - 1) * ws + e] + Sl[(NC - 1) * ws + e];
+        if (z_final)
+            for (int64_t e = 0; e < n; ++e)
+                z_final[bh * n + e] = Pz[(NC - 1) * n + e] + zl[(NC - 1) * n + e];
+    });
+    return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+"""ctypes front end of the fp64 CPU oracle (``kata_oracle.cpp``).
+
+TEST INFRASTRUCTURE ONLY: the oracle restates, slowly and in fp64, what the
+KATA causal normalised linear-attention forward computes, so that the CUDA
+library can be checked against it.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this module; the product path never
+does.  It shares no code with the CUDA library.
+
+All arrays are numpy float64, C-contiguous, in the documented layouts:
+q, k [B,H,T,p]; v, o [B,H,T,dv]; S [B,H,n,dv]; z [B,H,n]; n = p(p+1)/2.
+Anything that is not already float64 (e.g. bf16 values held in float32) is
+widened exactly before the call.
+
+Parity status of each function (pins live in tests/test_oracle_pins.py):
+  packed_dim, normalize, lift       pinned (closed forms, lift identities)
+  forward_plain, forward_plain_rows pinned (special cases, pSNR closed form,
+                                     rotation/scale invariance, convexity)
+  forward_recurrent                 pinned (agrees with plain; split calls)
+  forward_chunked, chunk_states     pinned (agrees with plain for every C,
+                                     ragged T; split calls; state identity)
+  scan_exclusive                    pinned (tree == sequential; depth)
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+SCAN_SEQUENTIAL = 0
+SCAN_TREE = 1
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    i = ctypes.c_int
+    lib.kor_packed_dim.argtypes = [i]
+    lib.kor_packed_dim.restype = i
+    lib.kor_normalize.argtypes = [_D, i, _D]
+    lib.kor_normalize.restype = None
+    lib.kor_lift.argtypes = [_D, i, _D]
+    lib.kor_lift.restype = None
+    lib.kor_forward_plain.argtypes = [_D, _D, _D, i, i, i, i, i, _D, i]
+    lib.kor_forward_plain.restype = i
+    lib.kor_forward_plain_rows.argtypes = [_D, _D, _D, i, i, i, i, i, _I64, _I64,
+                                           ctypes.c_int64, _D, i]
+    lib.kor_forward_plain_rows.restype = i
+    lib.kor_forward_recurrent.argtypes = [_D, _D, _D, i, i, i, i, i, _D, _D, _D, _D, _D, i]
+    lib.kor_forward_recurrent.restype = i
+    lib.kor_chunk_states.argtypes = [_D, _D, i, i, i, i, i, i, _D, _D, i]
+    lib.kor_chunk_states.restype = i
+    lib.kor_scan_exclusive.argtypes = [_D, _D, i, i, i, i, i, i, _D, _D, i]
+    lib.kor_scan_exclusive.restype = i
+    lib.kor_forward_chunked.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
+    lib.kor_forward_chunked.restype = i
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_D)
+
+
+def _shape4(q, k, v):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k [B,H,T,p] and v [B,H,T,dv]")
+    return q, k, v
+
+
+def packed_dim(p: int) -> int:
+    return _load().kor_packed_dim(p)
+
+
+def normalize(x):
+    """Row-wise unit-sphere projection of an [..., p] array."""
+    x = _f64(x)
+    p = x.shape[-1]
+    flat = x.reshape(-1, p)
+    u = np.empty_like(flat)
+    for r in range(flat.shape[0]):
+        _load().kor_normalize(_ptr(flat[r]), p, _ptr(u[r]))
+    return u.reshape(x.shape)
+
+
+def lift(u):
+    u = _f64(u)
+    p = u.shape[-1]
+    out = np.empty(packed_dim(p))
+    _load().kor_lift(_ptr(u), p, _ptr(out))
+    return out
+
+
+def forward_plain(q, k, v, nthreads=0):
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    o = np.empty((B, H, T, dv))
+    _load().kor_forward_plain(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, _ptr(o), nthreads)
+    return o
+
+
+def forward_plain_rows(q, k, v, bh, t, nthreads=0):
+    """Plain-definition outputs for rows (bh[r], t[r]); bh = b*H + h. Returns [R, dv]."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    bh = np.ascontiguousarray(np.asarray(bh, dtype=np.int64))
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int64))
+    if bh.shape != t.shape or (bh.size and (bh.min() < 0 or bh.max() >= B * H or t.min() < 0
+                                            or t.max() >= T)):
+        raise ValueError("row index out of range")
+    out = np.empty((bh.size, dv))
+    _load().kor_forward_plain_rows(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv,
+                                   bh.ctypes.data_as(_I64), t.ctypes.data_as(_I64), bh.size,
+                                   _ptr(out), nthreads)
+    return out
+
+
+def forward_recurrent(q, k, v, S0=None, z0=None, nthreads=0):
+    """Token-recurrent form. Returns (o, S_final, z_final)."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    n = packed_dim(p)
+    S0 = None if S0 is None else _f64(S0).reshape(B, H, n, dv)
+    z0 = None if z0 is None else _f64(z0).reshape(B, H, n)
+    o = np.empty((B, H, T, dv))
+    S = np.empty((B, H, n, dv))
+    z = np.empty((B, H, n))
+    _load().kor_forward_recurrent(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, _ptr(S0), _ptr(z0),
+                                  _ptr(o), _ptr(S), _ptr(z), nthreads)
+    return o, S, z
+
+
+def chunk_states(k, v, C, nthreads=0):
+    """Per-chunk local states. Returns (S_loc [B,H,NC,n,dv], z_loc [B,H,NC,n])."""
+    k, v = _f64(k), _f64(v)
+    B, H, T, p = k.shape
+    dv = v.shape[-1]
+    n = packed_dim(p)
+    NC = (T + C - 1) // C
+    S = np.empty((B, H, NC, n, dv))
+    z = np.empty((B, H, NC, n))
+    _load().kor_chunk_states(_ptr(k), _ptr(v), B, H, T, p, dv, C, _ptr(S), _ptr(z), nthreads)
+    return S, z
+
+
+def scan_exclusive(S_loc, z_loc, mode=SCAN_SEQUENTIAL, nthreads=0):
+    """Exclusive prefix over the chunk axis. Returns (S_prefix, z_prefix, rounds)."""
+    S_loc, z_loc = _f64(S_loc), _f64(z_loc)
+    B, H, NC, n, dv = S_loc.shape
+    Sp = np.empty_like(S_loc)
+    zp = np.empty_like(z_loc)
+    rounds = _load().kor_scan_exclusive(_ptr(S_loc), _ptr(z_loc), B, H, NC, n, dv, mode,
+                                        _ptr(Sp), _ptr(zp), nthreads)
+    return Sp, zp, rounds
+
+
+def forward_chunked(q, k, v, C, mode=SCAN_SEQUENTIAL, S0=None, z0=None, nthreads=0):
+    """Chunked form. Returns (o, S_final, z_final)."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    n = packed_dim(p)
+    S0 = None if S0 is None else _f64(S0).reshape(B, H, n, dv)
+    z0 = None if z0 is None else _f64(z0).reshape(B, H, n)
+    o = np.empty((B, H, T, dv))
+    S = np.empty((B, H, n, dv))
+    z = np.empty((B, H, n))
+    _load().kor_forward_chunked(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, C, mode, _ptr(S0),
+                                _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
+    return o, S, z
+
+
+def library_path() -> str:
+    return _build.LIB
+
