@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Throughput of the KATA chunked-state forward at the long-context workload
+(B=1, H=8, T=131072, p=64, d_v=64, C=128, bf16, associative-scan prefix).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one kata_forward_chunked call over the whole workload (every
+step of the path: normalise, lift, intra-chunk scores, state build, inter-
+chunk prefix, readout, normalisation).  Inputs are resident in HBM and
+larger than L2 (403 MB), so no L2 flush is needed between steps.  Prints one
+JSON line on rank 0.  Under torchrun every rank runs its own replica of the
+workload (independent sequences, no collective on the data path): weak
+scaling, value = all ranks' tokens / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from kernelized_linear_attention_03_b300 import binding as kb  # noqa: E402
+from kernelized_linear_attention_03_b300 import inputs  # noqa: E402
+
+METRIC = "KATA chunked fwd tokens/s at T=131072 (1 B300); % tensor-core peak"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                  "sm_max_mhz": 2032.0}
+SMS = 148
+FP32_LANES_PER_SM = 128
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+# ---------------------------------------------------------------- work model
+def flops_forward(w):
+    """Algorithmic flops of one chunked forward: per head-token
+    4 n (dv+1) (state build + readout, normaliser column included) plus
+    (C+1)(p+dv) (causal intra-chunk scores and their value product)."""
+    return w.B * w.H * w.T * (4 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
+
+
+def kernel_work(name, w):
+    """(kind, algorithmic amount per forward call) of a library kernel."""
+    bht = w.B * w.H * w.T
+    if name in ("chunk_states_simt",):
+        return "flop", bht * 2 * w.n * (w.dv + 1)
+    if name in ("chunk_output_simt",):
+        return "flop", bht * (2 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
+    if name in ("scan_tree", "scan_sequential"):
+        return "byte", 2 * w.B * w.H * w.NC * w.n * (w.dv + 1) * 4
+    return None, 0
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1] or [s for (_, s) in self.samples]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        smax = [num(s[1]) for s in inside if num(s[1]) is not None]
+        reasons = set()
+        for s in inside:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), s[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        power = [num(s[2]) for s in inside if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(w, q, k, v, T_s, nthreads):
+    """Run the fp64 oracle's chunked form on the first T_s tokens of every
+    head; return seconds."""
+    import oracle
+    qs, ks, vs = (t[:, :, :T_s].double().cpu().numpy() for t in (q, k, v))
+    t0 = time.perf_counter()
+    oracle.forward_chunked(qs, ks, vs, w.C, oracle.SCAN_TREE, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def oracle_threads(w):
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    return max(1, min(cores, w.B * w.H))
+
+
+def sample_len(w, q, k, v, seconds, nthreads):
+    """Tokens per head for an oracle sample of about `seconds` (multiple of C)."""
+    t_cal = max(oracle_sample(w, q, k, v, w.C, nthreads), 1e-3)
+    T_s = int(w.C * seconds / t_cal)
+    return max(w.C, min(w.T, T_s // w.C * w.C))
+
+
+def cpu_baseline(w, q, k, v, seconds=15.0):
+    nthreads = oracle_threads(w)
+    T_s = sample_len(w, q, k, v, seconds, nthreads)
+    dt = oracle_sample(w, q, k, v, T_s, nthreads)
+    return {"value": w.B * T_s / dt, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"fp64 oracle chunked form (C={w.C}, tree prefix) on the first {T_s} tokens "
+                      f"of all {w.B * w.H} heads of {w.name}; {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- main arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = inputs.HEADLINE
+    q, k, v = inputs.make(w, "cpu")
+    nthreads = oracle_threads(w)
+    budget = 150.0
+    per_step = max(1.0, budget / max(1, args.steps + args.warmup))
+    T_s = sample_len(w, q, k, v, per_step, nthreads)
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, w.C, nthreads)
+    times = [oracle_sample(w, q, k, v, T_s, nthreads) for _ in range(args.steps)]
+    total = sum(times)
+    value = args.steps * w.B * T_s / total
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "p": w.p, "dv": w.dv, "C": w.C,
+                   "scan_mode": "tree", "sample_tokens_per_head": T_s},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle chunked form on the first {T_s} tokens of "
+                                   f"all {w.B * w.H} heads of {w.name}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w0 = {x.name.split("_")[0]: x for x in inputs.WORKLOADS}[args.workload]
+    w = inputs.Workload(w0.name, w0.B, w0.H, w0.T, w0.p, w0.dv, w0.C, w0.dtype, w0.kind, seed=rank)
+    mode = kb.KATA_SCAN_TREE if args.scan == "tree" else kb.KATA_SCAN_SEQUENTIAL
+    q, k, v = inputs.make(w, dev)
+    o = torch.empty_like(v)
+    ws_bytes = kb.kata_chunked_workspace_bytes(q.dtype, w.B, w.H, w.T, w.p, w.dv, w.C)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kb.kata_forward_chunked(q, k, v, w.C, mode, o=o, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    kb.kata_get_device_status(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    kb.kata_trace_start(args.steps * 16 + 16)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    trace = kb.kata_trace_stop()
+    barrier(world)
+    clocks.stop()
+    kb.kata_get_device_status(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    tokens = w.B * w.T
+    value = world * tokens / (ms_max / 1e3)
+
+    # dominant kernel from the live trace
+    peaks = load_peaks()
+    per = {}
+    for name, t in trace:
+        per.setdefault(name, []).append(t)
+    dom = max(per, key=lambda n: sum(per[n]))
+    kind, amount = kernel_work(dom, w)
+    calls_per_step = len(per[dom]) / args.steps
+    dom_ms_per_call = sum(per[dom]) / args.steps  # all launches of it in one forward
+    if kind == "flop":
+        achieved = amount / (dom_ms_per_call / 1e3) / 1e12
+        if dom.endswith("_simt"):
+            peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+            bound, unit = "alu", "TFLOP/s"
+        else:
+            peak = peaks["bf16_tflops"]
+            bound, unit = "tensor", "TFLOP/s"
+    else:
+        achieved = amount / (dom_ms_per_call / 1e3) / 1e9
+        peak, bound, unit = peaks["hbm_gbs"], "hbm", "GB/s"
+    roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": args.traffic, "peak_source": peaks["source"],
+            "launches_per_step": calls_per_step,
+            "ms_per_step_in_kernel": dom_ms_per_call,
+            "share_of_step": dom_ms_per_call / ms}
+    kernels = {n: {"launches": len(t), "ms_total": sum(t), "share": sum(t) / max(1e-9, sum(x for _, x in trace))}
+               for n, t in per.items()}
+    alg_tflops = flops_forward(w) / (ms / 1e3) / 1e12
+
+    # end to end through the C ABI with host buffers
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        kb.kata_forward_chunked(qd, kd, vd, w.C, mode, o=o, workspace=ws, stream=stream)
+        oh.copy_(o, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e = {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if not dom.endswith("_simt") else "f32",
+        "data": "synthetic: seeded N(0,1) draws, q/k put on the unit sphere",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "p": w.p, "dv": w.dv, "C": w.C,
+                   "n": w.n, "scan_mode": args.scan, "inputs": "bf16",
+                   "l2": f"inputs larger than L2 ({(h2d) / 1e6:.0f} MB), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "algorithmic_tflops": alg_tflops,
+        "pct_bf16_peak": 100.0 * alg_tflops / peaks["bf16_tflops"],
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": len(trace),
+        "e2e": e2e,
+        "clocks": clocks.summary(wall0, wall1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c4", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--scan", default="tree", choices=["tree", "sequential"])
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per call of the dominant kernel from an ncu capture")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * kata.h -- C ABI of libkata.so: the KATA causal normalised linear-attention
+ * forward ("Kernelized Linear Attention: Breaking the Capacity Wall with
+ * Symmetric Cones", arXiv 2607.17419) on NVIDIA B300 (sm_103a).
+ *
+ * What every forward computes, per batch b, head h, position t (0-based):
+ *   qh_t = q_t / ||q_t||, kh_s = k_s / ||k_s||      (unit-sphere projection,
+ *        rank-one lift paragraph after Eq. 8; a zero vector stays zero)
+ *   psi(u) = u u^T packed into n = p(p+1)/2 coordinates (Eq. 8), diagonal
+ *        u_i^2, off-diagonal sqrt(2) u_i u_j, so <psi(a), psi(b)> = (a.b)^2
+ *   S_t = S0 + sum_{s<=t} psi(kh_s) v_s^T,  z_t = z0 + sum_{s<=t} psi(kh_s)
+ *        (state-size paragraph: S_t = Psi(K_{1:t})^T V_{1:t})
+ *   o_t = psi(qh_t)^T S_t / psi(qh_t)^T z_t   (normalised readout with the
+ *        denominator psi(q_t)^T Z_t of the Assumption 1 discussion; a zero
+ *        denominator gives a zero row).  With S0 = z0 = 0 this equals
+ *        o_t = sum_{s<=t} (qh_t.kh_s)^2 v_s / sum_{s<=t} (qh_t.kh_s)^2.
+ *
+ * Conventions shared by all calls
+ *   Layouts   q, k: [B][H][T][p]; v, o: [B][H][T][dv]; all dense row-major.
+ *             Packed state S: [B][H][n][dv] fp32, z: [B][H][n] fp32, with
+ *             packed index idx(i,j) = i*p - i*(i-1)/2 + (j-i) for i <= j.
+ *   Dtypes    KATA_FP32: q, k, v, o are float.  KATA_BF16: q, k, v, o are
+ *             bfloat16 (o has the input dtype); accumulation is fp32.
+ *   Shapes    p in {16, 32, 64}; dv in {16, 32, 64}; C in {32, 64, 128}
+ *             (chunk length; quadratic form also accepts 0 = automatic);
+ *             B, H, T >= 0 with B*H <= 65535; T <= 2^30.  Empty inputs
+ *             (B*H*T == 0) launch nothing and return KATA_OK (pointers may
+ *             then be NULL), except that a forward with T == 0 still writes
+ *             S_final = S0 and z_final = z0 when asked.
+ *   Pointers  Device pointers (or managed), 16-byte aligned; violations give
+ *             KATA_ERR_INVALID_ARG before anything is launched.  The caller
+ *             owns all memory; the library allocates no device memory.
+ *   Streams   Every call is asynchronous on `stream` (0 = legacy default).
+ *             Launch failures return KATA_ERR_CUDA.  Kernels never trap:
+ *             a bounded device wait that expires records KATA_ERR_TIMEOUT in
+ *             a device status word read by kata_get_device_status().
+ *   Threads   Calls on different streams may run concurrently as long as
+ *             their output and workspace buffers do not overlap.
+ */
+#ifndef KATA_H
+#define KATA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KATA_API __attribute__((visibility("default")))
+#else
+#define KATA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KATA_OK = 0,
+    KATA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad enum */
+    KATA_ERR_UNSUPPORTED = 2,  /* p, dv or C outside the supported set, too large */
+    KATA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    KATA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    KATA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired */
+} kata_status;
+
+typedef enum { KATA_FP32 = 0, KATA_BF16 = 1 } kata_dtype;
+
+/* Inter-chunk prefix: one step per chunk, or a log-depth scan taking
+ * ceil(log2 N_C) rounds of N_C-wide work (chunked-scan paragraph). */
+typedef enum { KATA_SCAN_SEQUENTIAL = 0, KATA_SCAN_TREE = 1 } kata_scan_mode;
+
+/* n = p(p+1)/2, the packed width of the rank-one lift (Eq. 8); -1 if p < 0. */
+KATA_API int kata_packed_dim(int p);
+
+/* Static, human-readable name of a status code; never NULL. */
+KATA_API const char* kata_status_string(kata_status status);
+
+/*
+ * Flash-style O(T^2) form (the flash-attention-style forward of the
+ * abstract): for each query tile, over key tiles up to the diagonal,
+ * scores (qh.kh)^2 with the causal mask s <= t, accumulated against [V | 1]
+ * and divided by the accumulated row sum.  Needs no workspace.
+ *   q, k [B,H,T,p], v [B,H,T,dv] in; o [B,H,T,dv] out (input dtype).
+ *   C: query/key tile hint (0, 32, 64 or 128); it does not change results.
+ */
+KATA_API kata_status kata_forward_quadratic(const void* q, const void* k, const void* v, void* o,
+                                   kata_dtype dtype, int B, int H, int T, int p, int dv, int C,
+                                   cudaStream_t stream);
+
+/* Bytes of workspace kata_forward_chunked needs for these sizes (0 if none). */
+KATA_API size_t kata_chunked_workspace_bytes(kata_dtype dtype, int B, int H, int T, int p, int dv, int C);
+
+/*
+ * Exact O(T) chunked-state form (chunked-scan paragraph): local chunk
+ * states psi(K_c)^T [V_c | 1], an exclusive prefix over chunks (`mode`),
+ * and per chunk the prefix readout psi(Q_c) [S | z] plus the local C x C
+ * causal part (Q_c K_c^T)^2 masked times [V_c | 1], then the division.
+ *   S0 [B,H,n,dv], z0 [B,H,n]: optional initial state (NULL = zero; give
+ *     both or neither).
+ *   S_final, z_final: optional state after the last token (NULL = not
+ *     written; give both or neither).  May alias S0 / z0.
+ *   workspace: device scratch of at least kata_chunked_workspace_bytes(),
+ *     256-byte aligned; contents on entry are ignored.  The call owns it
+ *     until the stream reaches the end of the call.
+ * Results do not depend on C or mode beyond fp32 rounding.
+ */
+KATA_API kata_status kata_forward_chunked(const void* q, const void* k, const void* v, void* o,
+                                 kata_dtype dtype, int B, int H, int T, int p, int dv, int C,
+                                 kata_scan_mode mode, const float* S0, const float* z0,
+                                 float* S_final, float* z_final, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Chunk states and their inter-chunk scan (the state kernel and the
+ * cumulative pass of the chunked-scan paragraph): with N_C = ceil(T/C),
+ *   S_prefix[b,h,c] = sum_{c' < c} psi(K_c')^T V_c'   [B,H,N_C,n,dv] fp32
+ *   z_prefix[b,h,c] = sum_{c' < c} psi(K_c')^T 1       [B,H,N_C,n]    fp32
+ * (exclusive prefixes: chunk 0 gets zeros).  The per-chunk states are built
+ * in the output buffers and scanned in place, so no workspace is needed.
+ */
+KATA_API kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dtype, int B, int H,
+                                  int T, int p, int dv, int C, kata_scan_mode mode,
+                                  float* S_prefix, float* z_prefix, cudaStream_t stream);
+
+/*
+ * Exclusive prefix over the chunk axis of given chunk states (the
+ * cumulative pass alone):
+ *   S_prefix[b,h,c] = sum_{c'<c} S_loc[b,h,c'],  z likewise.
+ *   S_loc/S_prefix [B,H,NC,n,dv], z_loc/z_prefix [B,H,NC,n], fp32.  Any
+ *   n, dv >= 1.  In place (S_prefix == S_loc, z_prefix == z_loc) is allowed;
+ *   partial overlap is not.
+ */
+KATA_API kata_status kata_scan_states(const float* S_loc, const float* z_loc, float* S_prefix,
+                             float* z_prefix, int B, int H, int NC, int n, int dv,
+                             kata_scan_mode mode, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: KATA_OK, or KATA_ERR_TIMEOUT if a bounded device-side
+ * wait expired in an earlier call (that call's outputs are then invalid).
+ * KATA_ERR_CUDA if the synchronisation itself fails.
+ */
+KATA_API kata_status kata_get_device_status(cudaStream_t stream);
+
+/*
+ * Launch tracing (instrumentation for benchmarks; not part of the method).
+ * kata_trace_start(capacity) creates 2*capacity CUDA events and, until
+ * kata_trace_stop(), brackets each kernel the library launches (from any
+ * thread, on the call's stream) with an event pair.  Launches beyond the
+ * capacity are not recorded.  kata_trace_stop() synchronises the recorded
+ * events and returns how many launches were recorded (negative on a CUDA
+ * error); kata_trace_get(i, &name, &ms) then gives the i-th launch's kernel
+ * name (static string) and its device duration in milliseconds.  Starting a
+ * new trace discards the previous one.  KATA_ERR_INVALID_ARG for a bad index
+ * or capacity.
+ */
+KATA_API kata_status kata_trace_start(int capacity);
+KATA_API int kata_trace_stop(void);
+KATA_API kata_status kata_trace_get(int index, const char** name, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KATA_H */

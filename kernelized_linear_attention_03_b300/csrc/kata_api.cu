@@ -1,0 +1,226 @@
+// C ABI of libkata (declared in include/kata.h): argument checks, workspace
+// sizing and dispatch to the kernels.  No device memory is allocated here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/kata.h"
+#include "kata_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxT = int64_t(1) << 30;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool p_ok(int p) { return p == 16 || p == 32 || p == 64; }
+bool dv_ok(int dv) { return dv == 16 || dv == 32 || dv == 64; }
+bool c_ok(int C) { return C == 32 || C == 64 || C == 128; }
+int64_t packed(int p) { return (int64_t)p * (p + 1) / 2; }
+kata_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KATA_OK : KATA_ERR_CUDA; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shape checks shared by the forwards.  Returns KATA_OK or the error.
+kata_status check_shapes(kata_dtype dt, int B, int H, int T, int p, int dv) {
+    if (dt != KATA_FP32 && dt != KATA_BF16) return KATA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || T < 0) return KATA_ERR_INVALID_ARG;
+    if (!p_ok(p) || !dv_ok(dv)) return KATA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535 || T > kMaxT) return KATA_ERR_UNSUPPORTED;
+    return KATA_OK;
+}
+
+// cuMemGetAddressRange through the runtime's driver entry point (no link
+// dependency on libcuda); null if unavailable.
+PFN_cuMemGetAddressRange_v3020 mem_range_fn() {
+    static PFN_cuMemGetAddressRange_v3020 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// A buffer the kernels may touch: non-null, 16-byte aligned, device memory of
+// the current device (or managed memory), and -- where the driver can tell
+// the allocation's extent -- at least `bytes` long from `ptr`.
+kata_status check_buffer(const void* ptr, size_t bytes) {
+    if (ptr == nullptr || !aligned16(ptr)) return KATA_ERR_INVALID_ARG;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_INVALID_ARG;
+    }
+    if (a.type == cudaMemoryTypeDevice) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || a.device != dev) return KATA_ERR_INVALID_ARG;
+        if (PFN_cuMemGetAddressRange_v3020 fn = mem_range_fn()) {
+            CUdeviceptr base = 0;
+            size_t size = 0;
+            if (fn(&base, &size, reinterpret_cast<CUdeviceptr>(ptr)) == CUDA_SUCCESS &&
+                reinterpret_cast<uintptr_t>(ptr) + bytes > (uintptr_t)base + size)
+                return KATA_ERR_INVALID_ARG;
+        }
+        return KATA_OK;
+    }
+    return a.type == cudaMemoryTypeManaged ? KATA_OK : KATA_ERR_INVALID_ARG;
+}
+
+size_t elem_bytes(kata_dtype dt) { return dt == KATA_FP32 ? 4 : 2; }
+
+// Workspace of the chunked forward: per-chunk states [BH, NC, n, dv] and
+// [BH, NC, n] in fp32, each 256-byte aligned.
+struct ChunkedWs {
+    size_t s_off, z_off, total;
+};
+
+ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C) {
+    const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C, n = packed(p);
+    ChunkedWs w;
+    w.s_off = 0;
+    w.z_off = round_up(sizeof(float) * (size_t)(BH * NC * n * dv), 256);
+    w.total = w.z_off + round_up(sizeof(float) * (size_t)(BH * NC * n), 256);
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kata_packed_dim(int p) { return p < 0 ? -1 : (int)packed(p); }
+
+const char* kata_status_string(kata_status s) {
+    switch (s) {
+        case KATA_OK: return "KATA_OK";
+        case KATA_ERR_INVALID_ARG: return "KATA_ERR_INVALID_ARG: null or misaligned pointer, negative size or bad enum";
+        case KATA_ERR_UNSUPPORTED: return "KATA_ERR_UNSUPPORTED: p, dv or C outside the supported set, or sizes too large";
+        case KATA_ERR_WORKSPACE: return "KATA_ERR_WORKSPACE: workspace missing or too small";
+        case KATA_ERR_CUDA: return "KATA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KATA_ERR_TIMEOUT: return "KATA_ERR_TIMEOUT: a bounded device-side wait expired";
+    }
+    return "KATA_ERR_UNKNOWN";
+}
+
+kata_status kata_forward_quadratic(const void* q, const void* k, const void* v, void* o,
+                                   kata_dtype dt, int B, int H, int T, int p, int dv, int C,
+                                   cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if (C != 0 && !c_ok(C)) return KATA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
+        return st;
+    return cuda_status(kata::launch_quadratic_simt(dt, q, k, v, o, B * H, T, p, dv, stream));
+}
+
+size_t kata_chunked_workspace_bytes(kata_dtype dt, int B, int H, int T, int p, int dv, int C) {
+    if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C)) return 0;
+    if ((int64_t)B * H * T == 0) return 0;
+    return chunked_ws(B, H, T, p, dv, C).total;
+}
+
+kata_status kata_forward_chunked(const void* q, const void* k, const void* v, void* o,
+                                 kata_dtype dt, int B, int H, int T, int p, int dv, int C,
+                                 kata_scan_mode mode, const float* S0, const float* z0,
+                                 float* S_final, float* z_final, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if (!c_ok(C)) return KATA_ERR_UNSUPPORTED;
+    if (mode != KATA_SCAN_SEQUENTIAL && mode != KATA_SCAN_TREE) return KATA_ERR_INVALID_ARG;
+    if ((S0 == nullptr) != (z0 == nullptr)) return KATA_ERR_INVALID_ARG;
+    if ((S_final == nullptr) != (z_final == nullptr)) return KATA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H, n = packed(p);
+    if (BH == 0) return KATA_OK;
+    const size_t s_bytes = sizeof(float) * BH * n * dv, z_bytes = sizeof(float) * BH * n;
+    if (S0 && ((st = check_buffer(S0, s_bytes)) != KATA_OK || (st = check_buffer(z0, z_bytes)) != KATA_OK))
+        return st;
+    if (S_final &&
+        ((st = check_buffer(S_final, s_bytes)) != KATA_OK || (st = check_buffer(z_final, z_bytes)) != KATA_OK))
+        return st;
+    if (T == 0) {
+        if (S_final == nullptr) return KATA_OK;
+        cudaError_t e = kata::launch_copy_or_zero(S0, S_final, BH * n * dv, stream);
+        if (e == cudaSuccess) e = kata::launch_copy_or_zero(z0, z_final, BH * n, stream);
+        return cuda_status(e);
+    }
+    const size_t qk_bytes = elem_bytes(dt) * BH * T * p, v_bytes = elem_bytes(dt) * BH * T * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
+        return st;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C);
+    if (ws == nullptr || ws_bytes < w.total) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
+
+    const int64_t NC = (T + C - 1) / C;
+    float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
+    float* z_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
+    cudaError_t e = kata::launch_chunk_states_simt(dt, k, v, S_loc, z_loc, (int)BH, T, p, dv, C, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, S_loc, S_loc, S0, S_final, BH, NC, n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, z_loc, z_loc, z0, z_final, BH, NC, n, stream);
+    if (e == cudaSuccess)
+        e = kata::launch_chunk_output_simt(dt, q, k, v, S_loc, z_loc, o, (int)BH, T, p, dv, C, stream);
+    return cuda_status(e);
+}
+
+kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dt, int B, int H, int T,
+                                  int p, int dv, int C, kata_scan_mode mode, float* S_prefix,
+                                  float* z_prefix, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if (!c_ok(C)) return KATA_ERR_UNSUPPORTED;
+    if (mode != KATA_SCAN_SEQUENTIAL && mode != KATA_SCAN_TREE) return KATA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H, n = packed(p), NC = (T + C - 1) / C;
+    if (BH * T == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * BH * T * p, v_bytes = elem_bytes(dt) * BH * T * dv;
+    if ((st = check_buffer(k, qk_bytes)) != KATA_OK || (st = check_buffer(v, v_bytes)) != KATA_OK ||
+        (st = check_buffer(S_prefix, sizeof(float) * BH * NC * n * dv)) != KATA_OK ||
+        (st = check_buffer(z_prefix, sizeof(float) * BH * NC * n)) != KATA_OK)
+        return st;
+    cudaError_t e = kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, S_prefix, S_prefix, nullptr, nullptr, BH, NC, n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, z_prefix, z_prefix, nullptr, nullptr, BH, NC, n, stream);
+    return cuda_status(e);
+}
+
+kata_status kata_scan_states(const float* S_loc, const float* z_loc, float* S_prefix,
+                             float* z_prefix, int B, int H, int NC, int n, int dv,
+                             kata_scan_mode mode, cudaStream_t stream) {
+    if (B < 0 || H < 0 || NC < 0 || n < 0 || dv < 0) return KATA_ERR_INVALID_ARG;
+    if (mode != KATA_SCAN_SEQUENTIAL && mode != KATA_SCAN_TREE) return KATA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H;
+    if (BH * NC * n * dv == 0 && BH * NC * n == 0) return KATA_OK;
+    const size_t sb = sizeof(float) * (size_t)(BH * NC * n * dv), zb = sizeof(float) * (size_t)(BH * NC * n);
+    kata_status st;
+    if ((st = check_buffer(S_loc, sb)) != KATA_OK || (st = check_buffer(z_loc, zb)) != KATA_OK ||
+        (st = check_buffer(S_prefix, sb)) != KATA_OK || (st = check_buffer(z_prefix, zb)) != KATA_OK)
+        return st;
+    // Partial overlap of input and output would race; exact aliasing is fine.
+    auto overlaps = [](const void* a, const void* b, size_t bytes) {
+        const char* x = static_cast<const char*>(a);
+        const char* y = static_cast<const char*>(b);
+        return x != y && x < y + bytes && y < x + bytes;
+    };
+    if (overlaps(S_loc, S_prefix, sb) || overlaps(z_loc, z_prefix, zb)) return KATA_ERR_INVALID_ARG;
+    cudaError_t e = kata::launch_scan(mode, S_loc, S_prefix, nullptr, nullptr, BH, NC, (int64_t)n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, z_loc, z_prefix, nullptr, nullptr, BH, NC, n, stream);
+    return cuda_status(e);
+}
+
+kata_status kata_get_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
+    return KATA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal launchers of libkata (host side).  Every launcher enqueues work on
+// `stream` and returns cudaGetLastError() of its launches; argument checking
+// happens before, in kata_api.cu.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace kata {
+
+// SIMT flash-style quadratic form, any dtype: o = causal sum (qh.kh)^2 v / sum.
+cudaError_t launch_quadratic_simt(int dtype, const void* q, const void* k, const void* v, void* o,
+                                  int BH, int T, int p, int dv, cudaStream_t s);
+
+// Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).
+cudaError_t launch_chunk_states_simt(int dtype, const void* k, const void* v, float* S_loc,
+                                     float* z_loc, int BH, int T, int p, int dv, int C,
+                                     cudaStream_t s);
+
+// Per-chunk output from exclusive prefixes P [BH,NC,n,dv], Pz [BH,NC,n] (SIMT).
+cudaError_t launch_chunk_output_simt(int dtype, const void* q, const void* k, const void* v,
+                                     const float* P, const float* Pz, void* o, int BH, int T,
+                                     int p, int dv, int C, cudaStream_t s);
+
+// Exclusive prefix over the chunk axis of x [heads, NC, W] into y (y may be
+// x).  init [heads, W] (or null) seeds the prefix; fin [heads, W] (or null)
+// receives init + total.  mode 0: one step per chunk; 1: log-depth scan.
+cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, float* fin,
+                        int64_t heads, int64_t NC, int64_t W, cudaStream_t s);
+
+// dst[i] = src ? src[i] : 0 for i < count (fp32), used for pass-through states.
+cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s);
+
+// Launch tracing (trace.cu): trace_begin returns a slot (or -1 when no trace
+// is active) and records its start event; trace_end records the stop event.
+int trace_begin(const char* name, cudaStream_t s);
+void trace_end(int slot, cudaStream_t s);
+
+// Brackets one kernel launch statement with trace events.
+#define KATA_TRACED(name, stream, ...)                            \
+    do {                                                          \
+        const int kata_slot_ = ::kata::trace_begin(name, stream); \
+        __VA_ARGS__;                                              \
+        ::kata::trace_end(kata_slot_, stream);                    \
+    } while (0)
+
+}  // namespace kata
