@@ -142,6 +142,33 @@ KATA_API kata_status kata_scan_states(const float* S_loc, const float* z_loc, fl
 KATA_API kata_status kata_get_device_status(cudaStream_t stream);
 
 /*
+ * Chunked forward that allocates nothing (no counterpart in the paper; it
+ * exists for callers that cannot call cudaMalloc: a plugin inside a runtime
+ * that owns all device allocations, code under a fixed start-up memory
+ * budget, or a real-time loop that must not enter the allocator).  Same
+ * arguments, results and errors as kata_forward_chunked except that the
+ * workspace is a fixed array of KATA_NOALLOC_SCRATCH_BYTES compiled into
+ * the library, held by every GPU that loads it until the process exits.
+ *   Sizes whose kata_chunked_workspace_bytes() exceeds that limit are
+ *   refused with KATA_ERR_UNSUPPORTED before anything is launched.
+ *   The first call on a device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress); make that first call before
+ *   any stream capture on the device.
+ *   Every call shares the one array (its contents are overwritten and need
+ *   no clearing): calls that may overlap on the GPU -- on different streams,
+ *   or from different threads -- race on it and must be serialised by the
+ *   caller, e.g. by issuing them on one stream.
+ *   Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define KATA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+KATA_API kata_status kata_forward_chunked_noalloc(const void* q, const void* k, const void* v,
+                                                  void* o, kata_dtype dtype, int B, int H, int T,
+                                                  int p, int dv, int C, kata_scan_mode mode,
+                                                  const float* S0, const float* z0,
+                                                  float* S_final, float* z_final,
+                                                  cudaStream_t stream);
+
+/*
  * Launch tracing (instrumentation for benchmarks; not part of the method).
  * kata_trace_start(capacity) creates 2*capacity CUDA events and, until
  * kata_trace_stop(), brackets each kernel the library launches (from any

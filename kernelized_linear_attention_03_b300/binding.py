@@ -27,7 +27,7 @@ KATA_SCAN_TREE = 1
 SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_chunked_workspace_bytes", "kata_forward_chunked", "kata_chunk_state_scan",
            "kata_scan_states", "kata_get_device_status", "kata_trace_start", "kata_trace_stop",
-           "kata_trace_get")
+           "kata_trace_get", "kata_forward_chunked_noalloc")
 
 
 class KataError(RuntimeError):
@@ -65,6 +65,8 @@ def load():
     lib.kata_scan_states.restype = I
     lib.kata_get_device_status.argtypes = [P]
     lib.kata_get_device_status.restype = I
+    lib.kata_forward_chunked_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P]
+    lib.kata_forward_chunked_noalloc.restype = I
     lib.kata_trace_start.argtypes = [I]
     lib.kata_trace_start.restype = I
     lib.kata_trace_stop.argtypes = []
@@ -153,6 +155,22 @@ def kata_forward_chunked(q, k, v, C, mode=KATA_SCAN_TREE, S0=None, z0=None, o=No
                                        p, dv, int(C), int(mode), _ptr(S0), _ptr(z0), _ptr(S_final),
                                        _ptr(z_final), _ptr(workspace), ws_bytes, _stream(stream)),
            "kata_forward_chunked")
+    return o if S_final is None else (o, S_final, z_final)
+
+
+def kata_forward_chunked_noalloc(q, k, v, C, mode=KATA_SCAN_TREE, S0=None, z0=None, o=None,
+                                 S_final=None, z_final=None, stream=None):
+    """Chunked forward using the library's fixed device scratch instead of a
+    workspace, for callers that must not allocate device memory.  The caller
+    passes every input and output (pass `o` to avoid the torch allocation made
+    here for convenience).  Returns o, or (o, S_final, z_final)."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_forward_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B,
+                                               H, T, p, dv, int(C), int(mode), _ptr(S0), _ptr(z0),
+                                               _ptr(S_final), _ptr(z_final), _stream(stream)),
+           "kata_forward_chunked_noalloc")
     return o if S_final is None else (o, S_final, z_final)
 
 
