@@ -120,6 +120,7 @@ kata_status kata_forward_quadratic(const void* q, const void* k, const void* v, 
     if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
         (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
         return st;
+    if (dt == KATA_BF16) return cuda_status(kata::launch_quadratic_tc(q, k, v, o, B * H, T, p, dv, stream));
     return cuda_status(kata::launch_quadratic_simt(dt, q, k, v, o, B * H, T, p, dv, stream));
 }
 
@@ -220,7 +221,8 @@ kata_status kata_scan_states(const float* S_loc, const float* z_loc, float* S_pr
 
 kata_status kata_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
-    return KATA_OK;
+    unsigned int word = kata::quadratic_tc_take_status();
+    return word ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 
 }  // extern "C"

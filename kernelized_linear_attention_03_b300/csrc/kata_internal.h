@@ -13,6 +13,12 @@ namespace kata {
 cudaError_t launch_quadratic_simt(int dtype, const void* q, const void* k, const void* v, void* o,
                                   int BH, int T, int p, int dv, cudaStream_t s);
 
+// tcgen05 flash-style quadratic form, bf16 inputs and output.
+cudaError_t launch_quadratic_tc(const void* q, const void* k, const void* v, void* o, int BH, int T,
+                                int p, int dv, cudaStream_t s);
+// Read and clear the device status word of the tensor-core quadratic kernel.
+unsigned int quadratic_tc_take_status();
+
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).
 cudaError_t launch_chunk_states_simt(int dtype, const void* k, const void* v, float* S_loc,
                                      float* z_loc, int BH, int T, int p, int dv, int C,
