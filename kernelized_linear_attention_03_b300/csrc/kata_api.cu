@@ -189,7 +189,9 @@ kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dt, i
         (st = check_buffer(S_prefix, sizeof(float) * BH * NC * n * dv)) != KATA_OK ||
         (st = check_buffer(z_prefix, sizeof(float) * BH * NC * n)) != KATA_OK)
         return st;
-    cudaError_t e = kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
+    cudaError_t e = dt == KATA_BF16
+                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream)
+                        : kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, S_prefix, S_prefix, nullptr, nullptr, BH, NC, n * dv, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, z_prefix, z_prefix, nullptr, nullptr, BH, NC, n, stream);
     return cuda_status(e);
@@ -222,6 +224,7 @@ kata_status kata_scan_states(const float* S_loc, const float* z_loc, float* S_pr
 kata_status kata_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
     unsigned int word = kata::quadratic_tc_take_status();
+    word |= kata::states_tc_take_status();
     return word ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 

@@ -19,6 +19,13 @@ cudaError_t launch_quadratic_tc(const void* q, const void* k, const void* v, voi
 // Read and clear the device status word of the tensor-core quadratic kernel.
 unsigned int quadratic_tc_take_status();
 
+// Segment states on the tensor cores (bf16 k, v): for each head and each
+// segment of L tokens, S_out [BH, NS, n, dv] and z_out [BH, NS, n] (fp32,
+// sqrt(2)-packed order), NS = ceil(T / L).
+cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
+                             int p, int dv, int L, cudaStream_t s);
+unsigned int states_tc_take_status();
+
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).
 cudaError_t launch_chunk_states_simt(int dtype, const void* k, const void* v, float* S_loc,
                                      float* z_loc, int BH, int T, int p, int dv, int C,

@@ -1,0 +1,90 @@
+// The rank-one lift psi(u) = u u^T of the tensor-core kernels, in the slot
+// order they keep internally (the rank-one lift paragraph after Eq. 8; the
+// packed width n = p(p+1)/2 of Eq. 8).
+//
+// Internal slot order.  With h = p/2, the n coordinates (i <= j) of the
+// upper triangle are laid out as
+//   slots [0, h*h)   "rectangle":  s = r*h + l            -> (i, j) = (r, h + l)
+//   slots [h*h, n)   "triangles":  s = h*h + r*h + l, r in [0, h]:
+//                       l >= r -> (r, l)          (upper-left triangle)
+//                       l <  r -> (h + l, h-1+r)  (lower-right triangle)
+// so that two consecutive slots (l even) nearly always share one factor and
+// take the other from an aligned pair of u: one bf16x2 multiply per pair.
+//
+// Internal scaling.  Keys are lifted without the sqrt(2) of the packed
+// Frobenius form: psiK(k)_(i,j) = k_i k_j.  Queries carry the whole factor 2
+// of the off-diagonal terms: psiQ(q)_(i,j) = q_i q_j (i = j), 2 q_i q_j
+// (i < j).  Then <psiQ(q), psiK(k)> = (q.k)^2 exactly as in the lift
+// identity, every scaling is a power of two (exact in bf16), and a state
+// built from psiK differs from the sqrt(2)-packed state of the C ABI only by
+// a factor sqrt(2) on its off-diagonal rows.
+#pragma once
+
+#include <cstdint>
+
+namespace kata {
+namespace lift {
+
+__host__ __device__ constexpr int packed_n(int P) { return P * (P + 1) / 2; }
+__host__ __device__ constexpr int tiles_of(int P) { return (packed_n(P) + 127) / 128; }
+
+// Coordinates (i, j), i <= j, of internal slot s < n.
+__host__ __device__ constexpr void slot_coord(int P, int s, int& i, int& j) {
+    const int h = P / 2;
+    if (s < h * h) {
+        i = s / h;
+        j = h + s % h;
+    } else {
+        const int q = s - h * h, r = q / h, l = q % h;
+        if (l >= r) {
+            i = r;
+            j = l;
+        } else {
+            i = h + l;
+            j = h - 1 + r;
+        }
+    }
+}
+
+// Row of (i, j) in the C ABI's packed order idx(i,j) = i*P - i(i-1)/2 + (j-i).
+__host__ __device__ constexpr int canonical_index(int P, int i, int j) { return i * P - i * (i - 1) / 2 + (j - i); }
+
+// bf16 pair with element a of ua in the low half and element b of ub in the
+// high half (arrays of packed bf16x2 words; a, b compile-time after unrolling).
+__device__ __forceinline__ uint32_t bf16_pair(const uint32_t* ua, int a, const uint32_t* ub, int b) {
+    const uint32_t sel = ((a & 1) ? 0x32u : 0x10u) | ((b & 1) ? 0x7600u : 0x5400u);
+    return __byte_perm(ua[a >> 1], ub[b >> 1], sel);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Packed bf16x2 word holding the lift at slots (2w, 2w+1) of the vector u
+// (u: P/2 packed words; u2: the same vector doubled, used for the query's
+// off-diagonal factor 2 when QUERY).  Slots at or past n give 0.
+template <int P, bool QUERY>
+__device__ __forceinline__ uint32_t lift_word(const uint32_t* u, const uint32_t* u2, int w) {
+    constexpr int n = packed_n(P);
+    const int s0 = 2 * w, s1 = 2 * w + 1;
+    if (s0 >= n) return 0u;
+    int i0 = 0, j0 = 0, i1 = 0, j1 = 0;
+    slot_coord(P, s0, i0, j0);
+    if (s1 < n) {
+        slot_coord(P, s1, i1, j1);
+    } else {
+        i1 = i0;
+        j1 = j0;
+    }
+    const uint32_t* a0 = (QUERY && i0 < j0) ? u2 : u;
+    const uint32_t* a1 = (QUERY && i1 < j1) ? u2 : u;
+    const uint32_t x = bf16_pair(a0, i0, a1, i1);
+    const uint32_t y = bf16_pair(u, j0, u, j1);
+    const uint32_t r = bf16x2_mul(x, y);
+    return s1 < n ? r : (r & 0xFFFFu);
+}
+
+}  // namespace lift
+}  // namespace kata

@@ -161,6 +161,43 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Instruction descriptor as above with the operand majorness given: bit 15
+// set = A is MN-major (M contiguous), bit 16 set = B is MN-major (N
+// contiguous).  An A operand read from tensor memory is always K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+    return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+}
+
+// Shared-memory descriptor of an MN-major 128-byte-swizzled operand: the
+// tile is stored as atoms of 64 MN-elements; inside an atom, K-row k takes
+// 128 bytes at (k / 8) * 1024 + (k % 8) * 128 with its 16-byte chunks
+// swizzled by k % 8.  `atom_stride` (leading byte offset) is the distance
+// between consecutive 64-element MN atoms; 8-row K groups are 1024 bytes
+// apart (stride byte offset).  A step of 16 K-rows starts 2048 bytes later.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t atom_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Byte offset of element (mn, k) inside an MN-major 128B-swizzled tile
+// whose 64-element MN atoms are `atom_stride` bytes apart.
+__host__ __device__ __forceinline__ uint32_t mn_sw128_offset(uint32_t mn, uint32_t k, uint32_t atom_stride) {
+    const uint32_t a = mn >> 6, m = mn & 63;
+    return a * atom_stride + (k >> 3) * 1024u + (k & 7u) * 128u + ((((m >> 3) ^ (k & 7u))) << 4) + ((m & 7u) << 1);
+}
+
+// Byte offset of the 16-byte chunk holding MN-elements mn..mn+7 (mn % 8 == 0)
+// of K-row k.
+__host__ __device__ __forceinline__ uint32_t mn_sw128_chunk(uint32_t mn, uint32_t k, uint32_t atom_stride) {
+    const uint32_t a = mn >> 6, c = (mn & 63) >> 3;
+    return a * atom_stride + (k >> 3) * 1024u + (k & 7u) * 128u + ((c ^ (k & 7u)) << 4);
+}
+
 // Byte offset of element (row r, k) inside a K-major 128B-swizzled tile of
 // `rows` rows (rows a multiple of 8).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k, uint32_t rows) {

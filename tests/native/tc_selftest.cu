@@ -1,8 +1,8 @@
 // Self-test of libkata's tcgen05 building blocks (test infrastructure): one
 // CTA computes D[128 x N] = A[128 x K] * B[N x K]^T with bf16 operands and an
-// fp32 TMEM accumulator, A taken from shared memory (mode 0) or from tensor
-// memory (mode 1), B from shared memory, both in the K-major 128B-swizzled
-// layout.  The test compares D with a host matmul.
+// fp32 TMEM accumulator, A taken from shared memory or from tensor memory,
+// B from shared memory, shared-memory operands in the K-major or MN-major
+// 128B-swizzled layouts.  The test compares D with a host matmul.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -12,6 +12,11 @@ using namespace kata::tc;
 
 namespace {
 
+// mode 0: A smem K-major,  B smem K-major
+// mode 1: A tmem,           B smem K-major
+// mode 2: A smem MN-major,  B smem K-major
+// mode 3: A tmem,           B smem MN-major
+// mode 4: A smem MN-major,  B smem MN-major
 __global__ void __launch_bounds__(128) gemm_probe(const __nv_bfloat16* __restrict__ A,
                                                   const __nv_bfloat16* __restrict__ B,
                                                   float* __restrict__ D, int K, int N, int mode,
@@ -21,25 +26,27 @@ __global__ void __launch_bounds__(128) gemm_probe(const __nv_bfloat16* __restric
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int kblocks = (K + 63) / 64;     // 128-byte rows, 64 elements per column block
-    uint8_t* As = smem;                    // 128 rows x kblocks blocks
-    uint8_t* Bs = smem + 128 * 128 * kblocks;  // N rows x kblocks blocks (N multiple of 8)
+    const bool a_mn = (mode == 2 || mode == 4), b_mn = (mode == 3 || mode == 4);
+    const uint32_t a_atom = (uint32_t)K * 128u;  // MN-major atom: K rows of 128 bytes
+    const uint32_t b_atom = (uint32_t)K * 128u;
+    uint8_t* As = smem;                                        // 32 KB at most
+    uint8_t* Bs = smem + 128 * 128 * 2;                        // up to 128 x 128 elements
     const int t = threadIdx.x, warp = t >> 5;
     if (t == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
-    // operands into the swizzled layout, 8 elements (16 B) at a time
-    for (int e = t; e < 128 * (K / 8); e += 128) {
-        const int r = e / (K / 8), k = (e % (K / 8)) * 8;
-        *reinterpret_cast<uint4*>(As + sw128_chunk(r, k, 128)) =
-            *reinterpret_cast<const uint4*>(A + (size_t)r * K + k);
+    // operands into the swizzled layouts, one element at a time
+    for (int e = t; e < 128 * K; e += 128) {
+        const int m = e / K, k = e % K;
+        const uint32_t off = a_mn ? mn_sw128_offset(m, k, a_atom) : sw128_offset(m, k, 128);
+        *reinterpret_cast<__nv_bfloat16*>(As + off) = A[(size_t)m * K + k];
     }
-    for (int e = t; e < N * (K / 8); e += 128) {
-        const int r = e / (K / 8), k = (e % (K / 8)) * 8;
-        *reinterpret_cast<uint4*>(Bs + sw128_chunk(r, k, N)) =
-            *reinterpret_cast<const uint4*>(B + (size_t)r * K + k);
+    for (int e = t; e < N * K; e += 128) {
+        const int n = e / K, k = e % K;
+        const uint32_t off = b_mn ? mn_sw128_offset(n, k, b_atom) : sw128_offset(n, k, N);
+        *reinterpret_cast<__nv_bfloat16*>(Bs + off) = B[(size_t)n * K + k];
     }
     fence_proxy_async_smem();
     if (warp == 0) {
@@ -51,7 +58,8 @@ __global__ void __launch_bounds__(128) gemm_probe(const __nv_bfloat16* __restric
     tc_fence_after();
     const uint32_t tb = tmem_base;
     const uint32_t d_tmem = tb, a_tmem = tb + 128;  // D: cols 0..N-1, A: cols 128..128+K/2-1
-    if (mode == 1) {
+    const bool a_tm = (mode == 1 || mode == 3);
+    if (a_tm) {
         // row t of A into lane t, column c holding elements (2c, 2c+1)
         const uint32_t lane0 = (uint32_t)(warp * 32);
         for (int c0 = 0; c0 < K / 2; c0 += 16) {
@@ -69,15 +77,17 @@ __global__ void __launch_bounds__(128) gemm_probe(const __nv_bfloat16* __restric
     __syncthreads();
     tc_fence_after();
     if (t == 0) {
-        const uint32_t idesc = idesc_bf16_f32(128, N);
+        const uint32_t idesc = idesc_bf16_f32_major(128, N, a_mn, b_mn);
         for (int ks = 0; ks < K / 16; ++ks) {
             const uint32_t koff = (ks & 3) * 32;
-            const uint64_t ad = sdesc_kmajor_sw128(smem_u32(As) + (ks >> 2) * 128 * 128 + koff);
-            const uint64_t bd = sdesc_kmajor_sw128(smem_u32(Bs) + (ks >> 2) * N * 128 + koff);
-            if (mode == 0)
-                mma_ss(d_tmem, ad, bd, idesc, ks > 0);
-            else
+            const uint64_t ad = a_mn ? sdesc_mnmajor_sw128(smem_u32(As) + ks * 2048, a_atom)
+                                     : sdesc_kmajor_sw128(smem_u32(As) + (ks >> 2) * 128 * 128 + koff);
+            const uint64_t bd = b_mn ? sdesc_mnmajor_sw128(smem_u32(Bs) + ks * 2048, b_atom)
+                                     : sdesc_kmajor_sw128(smem_u32(Bs) + (ks >> 2) * N * 128 + koff);
+            if (a_tm)
                 mma_ts(d_tmem, a_tmem + ks * 8, bd, idesc, ks > 0);
+            else
+                mma_ss(d_tmem, ad, bd, idesc, ks > 0);
         }
         mma_commit(&bar);
     }
@@ -106,8 +116,8 @@ __global__ void __launch_bounds__(128) gemm_probe(const __nv_bfloat16* __restric
 extern "C" __attribute__((visibility("default"))) int kata_tc_selftest(const void* A, const void* B,
                                                                      float* D, int K, int N, int mode,
                                                                      int* status, cudaStream_t s) {
-    if (K < 16 || K > 128 || K % 16 || N < 16 || N > 128 || N % 16 || (mode != 0 && mode != 1)) return 1;
-    const int smem = 1024 + (128 + N) * 128 * ((K + 63) / 64);
+    if (K < 16 || K > 128 || K % 16 || N < 16 || N > 128 || N % 16 || mode < 0 || mode > 4) return 1;
+    const int smem = 1024 + 2 * 128 * 128 * 2;
     if (cudaFuncSetAttribute(gemm_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 2;
     gemm_probe<<<1, 128, smem, s>>>(static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B),

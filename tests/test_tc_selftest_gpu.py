@@ -20,7 +20,7 @@ def lib():
     return lib
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("K", [16, 32, 64, 128])
 @pytest.mark.parametrize("N", [16, 64, 80, 128])
 def test_gemm_probe(lib, mode, K, N):
