@@ -70,6 +70,12 @@ def kernel_work(name, w):
         return "flop", bht * (2 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
     if name in ("scan_tree", "scan_sequential"):
         return "byte", 2 * w.B * w.H * w.NC * w.n * (w.dv + 1) * 4
+    if name == "chunked_tc":
+        # the fused forward does all of the forward's algorithmic work
+        return "flop", flops_forward(w)
+    if name == "states_tc":
+        # segment start states: recomputed work, no algorithmic share
+        return "flop", 0
     return None, 0
 
 

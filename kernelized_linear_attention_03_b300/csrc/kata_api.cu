@@ -90,6 +90,31 @@ ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C) {
     return w;
 }
 
+// bf16 inputs take the fused tensor-core forward when its cluster can be
+// scheduled on the current device; its workspace holds one start state per
+// segment when the sequence is cut into G > 1 segments.
+struct TcPlan {
+    bool use = false;
+    int G = 1;
+    ChunkedWs ws{0, 0, 0};
+};
+
+TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
+    TcPlan pl;
+    if (dt != KATA_BF16) return pl;
+    const int64_t BH = (int64_t)B * H, n = packed(p);
+    const int G = kata::chunked_tc_segments(p, dv, (int)BH, T);
+    if (G <= 0) return pl;
+    pl.use = true;
+    pl.G = G;
+    if (G > 1) {
+        pl.ws.s_off = 0;
+        pl.ws.z_off = round_up(sizeof(float) * (size_t)(BH * G * n * dv), 256);
+        pl.ws.total = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * G * n), 256);
+    }
+    return pl;
+}
+
 }  // namespace
 
 extern "C" {
@@ -127,7 +152,8 @@ kata_status kata_forward_quadratic(const void* q, const void* k, const void* v, 
 size_t kata_chunked_workspace_bytes(kata_dtype dt, int B, int H, int T, int p, int dv, int C) {
     if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C)) return 0;
     if ((int64_t)B * H * T == 0) return 0;
-    return chunked_ws(B, H, T, p, dv, C).total;
+    const TcPlan pl = tc_plan(dt, B, H, T, p, dv);
+    return pl.use ? pl.ws.total : chunked_ws(B, H, T, p, dv, C).total;
 }
 
 kata_status kata_forward_chunked(const void* q, const void* k, const void* v, void* o,
@@ -159,10 +185,36 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
     if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
         (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
         return st;
-    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C);
-    if (ws == nullptr || ws_bytes < w.total) return KATA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
-    if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
+    const TcPlan pl = tc_plan(dt, B, H, T, p, dv);
+    const ChunkedWs w = pl.use ? pl.ws : chunked_ws(B, H, T, p, dv, C);
+    if (w.total > 0) {
+        if (ws == nullptr || ws_bytes < w.total) return KATA_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+        if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
+    }
+    if (pl.use) {
+        if (pl.G == 1)
+            return cuda_status(kata::launch_chunked_tc(q, k, v, o, S0, z0, 1, S_final, z_final, (int)BH, T, p,
+                                                       dv, 1, stream));
+        // segment totals of segments 0..G-2, then exclusive prefixes seeded
+        // with the initial state: the start state of every segment
+        const int G = pl.G, n32 = (int)n;
+        const int L = kata::chunked_tc_segment_chunks(T, G) * 128;
+        float* Sg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
+        float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
+        cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, stream);
+        if (e == cudaSuccess)
+            e = cudaMemset2DAsync(Sg + (size_t)(G - 1) * n32 * dv, sizeof(float) * (size_t)G * n32 * dv, 0,
+                                  sizeof(float) * (size_t)n32 * dv, (size_t)BH, stream);
+        if (e == cudaSuccess)
+            e = cudaMemset2DAsync(zg + (size_t)(G - 1) * n32, sizeof(float) * (size_t)G * n32, 0,
+                                  sizeof(float) * (size_t)n32, (size_t)BH, stream);
+        if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
+        if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
+        if (e == cudaSuccess)
+            e = kata::launch_chunked_tc(q, k, v, o, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, G, stream);
+        return cuda_status(e);
+    }
 
     const int64_t NC = (T + C - 1) / C;
     float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
@@ -190,7 +242,7 @@ kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dt, i
         (st = check_buffer(z_prefix, sizeof(float) * BH * NC * n)) != KATA_OK)
         return st;
     cudaError_t e = dt == KATA_BF16
-                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream)
+                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, stream)
                         : kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, S_prefix, S_prefix, nullptr, nullptr, BH, NC, n * dv, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, z_prefix, z_prefix, nullptr, nullptr, BH, NC, n, stream);
@@ -225,6 +277,7 @@ kata_status kata_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
     unsigned int word = kata::quadratic_tc_take_status();
     word |= kata::states_tc_take_status();
+    word |= kata::chunked_tc_take_status();
     return word ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 

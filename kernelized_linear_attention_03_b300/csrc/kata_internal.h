@@ -20,11 +20,25 @@ cudaError_t launch_quadratic_tc(const void* q, const void* k, const void* v, voi
 unsigned int quadratic_tc_take_status();
 
 // Segment states on the tensor cores (bf16 k, v): for each head and each
-// segment of L tokens, S_out [BH, NS, n, dv] and z_out [BH, NS, n] (fp32,
-// sqrt(2)-packed order), NS = ceil(T / L).
+// of the first NS segments of L tokens, into S_out [BH, NS_out, n, dv] and
+// z_out [BH, NS_out, n] (fp32, sqrt(2)-packed order).  NS <= NS_out and
+// NS <= ceil(T / L).
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, cudaStream_t s);
+                             int p, int dv, int L, int NS, int NS_out, cudaStream_t s);
 unsigned int states_tc_take_status();
+
+// Fused chunked forward on the tensor cores (bf16), one cluster per (head,
+// segment).  chunked_tc_segments() gives the number of segments G the
+// sequence is cut into on the current device (0 if the kernel's cluster
+// cannot be scheduled there); chunked_tc_segment_chunks() the 128-token
+// chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
+// start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
+int chunked_tc_segments(int p, int dv, int BH, int T);
+int chunked_tc_segment_chunks(int T, int G);
+cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, const float* S_start,
+                              const float* z_start, int start_groups, float* S_final, float* z_final, int BH,
+                              int T, int p, int dv, int G, cudaStream_t s);
+unsigned int chunked_tc_take_status();
 
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).
 cudaError_t launch_chunk_states_simt(int dtype, const void* k, const void* v, float* S_loc,

@@ -71,7 +71,10 @@ template <int P, int DV>
 __global__ void __launch_bounds__(kThreads)
 states_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                  float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS,
-                 int segs_per_cta) {
+                 int NS_out, int segs_per_cta) {
+    // T: tokens per head (row stride and bound); segments 0..NS-1 of L tokens
+    // are computed (NS may cover fewer than all T tokens) into rows of a
+    // [BH, NS_out, n] layout.
     using Lay = StatesLayout<DV>;
     constexpr int NB = Lay::NB;
     constexpr int n = lift::packed_n(P);
@@ -192,7 +195,7 @@ states_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __res
             int i = 0, j = 0;
             lift::slot_coord(P, slot, i, j);
             const float f = i < j ? kSqrt2f : 1.f;
-            const int64_t row = (bh * NS + seg) * (int64_t)n + lift::canonical_index(P, i, j);
+            const int64_t row = (bh * NS_out + seg) * (int64_t)n + lift::canonical_index(P, i, j);
             float4* dst = reinterpret_cast<float4*>(S_out + row * DV);
 #pragma unroll
             for (int c = 0; c < DV / 4; ++c)
@@ -215,12 +218,11 @@ states_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __res
 
 template <int P, int DV>
 cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_out, int BH, int T, int L,
-                         cudaStream_t s) {
+                         int NS, int NS_out, cudaStream_t s) {
     constexpr size_t smem = StatesLayout<DV>::smem;
     auto kern = states_tc_kernel<P, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int NS = (T + L - 1) / L;
     const int tiles = lift::tiles_of(P);
     // a few segments per CTA, enough CTAs for several waves
     const int64_t work = (int64_t)tiles * NS * BH;
@@ -231,16 +233,17 @@ cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_ou
     KATA_TRACED("states_tc", s,
                 kern<<<grid, kThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(k),
                                                   static_cast<const __nv_bfloat16*>(v), S_out, z_out, T,
-                                                  L, NS, per));
+                                                  L, NS, NS_out, per));
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, cudaStream_t s) {
+                             int p, int dv, int L, int NS, int NS_out, cudaStream_t s) {
+    if (NS <= 0) return cudaSuccess;
 #define KATA_CASE(P_, DV_) \
-    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(k, v, S_out, z_out, BH, T, L, s);
+    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, s);
     KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
     KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
     KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)

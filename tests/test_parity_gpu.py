@@ -186,7 +186,8 @@ def test_host_and_short_buffers_rejected():
         assert st == kb.KATA_ERR_INVALID_ARG
     finally:
         cudart.cudaFree(ptr)
-    q, k, v = _inputs(1, 1, 64, 16, 16, torch.bfloat16)
+    q, k, v = _inputs(1, 1, 64, 16, 16, torch.float32)  # the fp32 path keeps per-chunk states
+    assert kb.kata_chunked_workspace_bytes(torch.float32, 1, 1, 64, 16, 16, 32) > 16
     with pytest.raises(kb.KataError) as ei:
         kb.kata_forward_chunked(q, k, v, 32, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert ei.value.status == kb.KATA_ERR_WORKSPACE
