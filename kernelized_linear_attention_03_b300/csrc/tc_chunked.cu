@@ -39,7 +39,12 @@ namespace cg = cooperative_groups;
 
 __device__ unsigned int g_chunked_tc_status = 0;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 384;  // warpgroups: lift, epilogue, MMA (one issuing thread)
+// Register split between the warpgroups after launch (setmaxnreg): the MMA
+// warpgroup gives back registers the two working warpgroups take.  Their sum,
+// 128 * (2 * kRegsWork + kRegsMma), must not exceed 384 * (registers per thread
+// at launch); the launcher checks that before every launch.
+constexpr uint32_t kRegsWork = 192, kRegsMma = 88;
 constexpr int kChunk = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes
@@ -57,30 +62,33 @@ struct Cfg {
     static constexpr int NTC = NT / TPC;               // tile CTAs
     static constexpr int CS = NTC + 1;                 // cluster size
     static constexpr int R = (kChunk + CS - 1) / CS;   // output rows owned per CTA
-    // shared memory (offsets from a 1024-byte aligned base)
-    static constexpr uint32_t ak_off = 0;              // key lift, TPC tiles x 2 atoms
-    static constexpr uint32_t q_off = 2 * kAtom;       // extra CTA: queries (K-major)
-    static constexpr uint32_t kh_off = 3 * kAtom;      // extra CTA: unit keys (K-major)
-    static constexpr uint32_t bv_off = 4 * kAtom;      // values (MN-major, N = dv)
-    static constexpr uint32_t s16_off = 5 * kAtom;     // bf16 state rows, TPC tiles
-    static constexpr uint32_t z16_off = 6 * kAtom;     // extra CTA: bf16 Z (K-major, P rows)
-    static constexpr uint32_t recv_off = 7 * kAtom;
+    // shared memory, in 16 KB atoms from a 1024-byte aligned base
+    //   tile CTA : key lift [0, 2 TPC), V, bf16 state [TPC], query/key staging [2]
+    //   extra CTA: tail key lift, Q, unit keys, bf16 Z, V, bf16 tail state, staging [2]
+    static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 1) * kAtom,
+                              t_stage = (3 * TPC + 1) * kAtom;
+    static constexpr uint32_t x_ak = 0, x_q = 1 * kAtom, x_kh = 2 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
+                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom;
+    static constexpr uint32_t atoms = (3 * TPC + 3) > 8 ? (3 * TPC + 3) : 8;
+    static constexpr uint32_t recv_off = atoms * kAtom;
     static constexpr uint32_t recv_part = R * DV * 4;  // one CTA's partial rows
     static constexpr uint32_t recv_den = CS * recv_part;
     static constexpr uint32_t recv_buf = round16(recv_den + R * 4);
     static constexpr uint32_t total = recv_off + 2 * recv_buf;
     static constexpr size_t smem = total + 1024;
-    // tensor memory columns
-    static constexpr uint32_t tm_s = 0;                // tile CTA: TPC x 64 state columns
-    static constexpr uint32_t tm_aq = 128;             // tile CTA: TPC x 64 query-lift columns
-    static constexpr uint32_t tm_y = 256;              // tile CTA: partial Y
-    static constexpr uint32_t tx_s = 0;                // extra CTA: tail state
-    static constexpr uint32_t tx_aq = 64;              // extra CTA: tail query lift
-    static constexpr uint32_t tx_y = 128;              // extra CTA: partial Y
-    static constexpr uint32_t tx_sc = 192;             // extra CTA: scores (128 cols), P in place
-    static constexpr uint32_t tx_w = 320;              // extra CTA: Q Z
-    static constexpr uint32_t tx_z = 384;              // extra CTA: Z
+    // tensor memory columns, tile CTA
+    static constexpr uint32_t tm_s = 0;      // TPC x 64: fp32 state
+    static constexpr uint32_t tm_aq = 128;   // 2 slots x 128: query lift
+    static constexpr uint32_t tm_y = 384;    // 2 slots x 64: partial readout
+    // tensor memory columns, extra CTA
+    static constexpr uint32_t tx_s = 0;      // tail state
+    static constexpr uint32_t tx_aq = 64;    // 2 slots x 32: tail query lift
+    static constexpr uint32_t tx_y = 128;    // 2 slots x 64: partial readout
+    static constexpr uint32_t tx_sc = 256;   // 128: intra scores, P in place
+    static constexpr uint32_t tx_w = 384;    // Q Z
+    static constexpr uint32_t tx_z = 448;    // Z
     static_assert(NT % TPC == 0, "tiles must split evenly");
+    static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(total + 1024 <= 232448, "shared memory");
 };
 
@@ -90,37 +98,71 @@ __device__ __forceinline__ void key_tile(const uint32_t (&u)[P / 2], uint8_t* As
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         uint4 val;
-        val.x = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 0);
-        val.y = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 1);
-        val.z = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 2);
-        val.w = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 3);
+        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
+        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
+        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
+        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
         *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
     }
 }
 
 template <int P, int TAU>
-__device__ __forceinline__ void query_tile(const uint32_t (&u)[P / 2], const uint32_t (&u2)[P / 2],
-                                           uint32_t taddr) {
+__device__ __forceinline__ void query_tile(const uint32_t (&u)[P / 2], uint32_t taddr) {
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = lift::lift_word<P, true>(u, u2, 64 * TAU + c0 + i);
+        for (int i = 0; i < 16; ++i) w[i] = lift::lift_word<P, true>(u, 64 * TAU + c0 + i);
         tmem_st16(taddr + c0, w);
     }
 }
 
 template <int P, int TAU = 0>
-__device__ __forceinline__ void lift_tile(int tau, const uint32_t (&uk)[P / 2], const uint32_t (&uq)[P / 2],
-                                          const uint32_t (&uq2)[P / 2], uint8_t* As, int row, uint32_t taddr) {
+__device__ __forceinline__ void query_dispatch(int tau, const uint32_t (&uq)[P / 2], uint32_t taddr) {
     if constexpr (TAU < lift::tiles_of(P)) {
-        if (tau == TAU) {
-            key_tile<P, TAU>(uk, As, row);
-            query_tile<P, TAU>(uq, uq2, taddr);
-        } else {
-            lift_tile<P, TAU + 1>(tau, uk, uq, uq2, As, row, taddr);
-        }
+        if (tau == TAU)
+            query_tile<P, TAU>(uq, taddr);
+        else
+            query_dispatch<P, TAU + 1>(tau, uq, taddr);
     }
+}
+
+template <int P, int TAU = 0>
+__device__ __forceinline__ void key_dispatch(int tau, const uint32_t (&uk)[P / 2], uint8_t* As, int row) {
+    if constexpr (TAU < lift::tiles_of(P)) {
+        if (tau == TAU)
+            key_tile<P, TAU>(uk, As, row);
+        else
+            key_dispatch<P, TAU + 1>(tau, uk, As, row);
+    }
+}
+
+// Key lift of the last (partly filled) tile into its first 64-slot atom, up
+// to the next multiple of 16 slots (slots past n are written as zeros).
+template <int P>
+__device__ __forceinline__ void key_tail(const uint32_t (&u)[P / 2], uint8_t* As, int row) {
+    constexpr int TAU = lift::tiles_of(P) - 1;
+    constexpr int tail = lift::packed_n(P) - 128 * TAU;
+    constexpr int chunks = 2 * ((tail + 15) / 16);
+#pragma unroll
+    for (int c = 0; c < chunks; ++c) {
+        uint4 val;
+        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
+        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
+        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
+        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
+        *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
+    }
+}
+
+// Query lift of the last (partly filled) tile: its first 16 words (32 slots).
+template <int P>
+__device__ __forceinline__ void query_tail(const uint32_t (&uq)[P / 2], uint32_t taddr) {
+    constexpr int TAU = lift::tiles_of(P) - 1;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = lift::lift_word<P, true>(uq, 64 * TAU + i);
+    tmem_st16(taddr, w);
 }
 
 // ---------------------------------------------------------------- state rows
@@ -215,6 +257,19 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 }
 
 // ---------------------------------------------------------------- kernel
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3  lift:     thread t = token t of the chunk; stages its query
+//                        and key rows one chunk ahead (cp.async), puts the key
+//                        on the unit sphere, writes the query lift (tensor
+//                        memory) and key lift (shared memory), the value row
+//   warps 4-7  epilogue: thread e = tensor-memory lane e; reads the state after
+//                        each update, refreshes its bf16 copy, sends the partial
+//                        readout to the row owners, reduces its owned rows one
+//                        chunk later
+//   warps 8-11 MMA:      one thread issues every tcgen05.mma
+// Per chunk the MMAs run update (state += lift(K)^T V) then readout
+// (Y = lift(Q) S), so the next update starts as soon as the epilogue has read
+// the state.
 template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -225,7 +280,8 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     constexpr int n = K::n;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], y_full[2], recv_full[2], peer_free[2];
+    __shared__ uint64_t v_free, ak_free, qk_free, upd_done, state_read, s16_ready, p_ready, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,15 +293,42 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int G = gridDim.x / K::CS;
     const int64_t bh = blockIdx.y;
     const int NCH = (T + kChunk - 1) / kChunk;
-    const int c_begin = g * seg_chunks, c_end = min(NCH, c_begin + seg_chunks);
-    const __nv_bfloat16* qh = q + bh * (int64_t)T * P;
-    const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
-    const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
-    __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
+    const int c0 = g * seg_chunks, c1 = min(NCH, c0 + seg_chunks);
+    const int nk = c1 - c0;
+    const int my_rows = min(K::R, kChunk - rank * K::R);
+    // bytes of partial rows (and denominators) other CTAs deliver per chunk
+    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 4 + (extra ? 0 : my_rows * 4);
+    // shared memory of this CTA's role
+    uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
+    uint8_t* const s_v = sm + (extra ? K::x_v : K::t_v);
+    uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
+    uint8_t* const s_stage = sm + (extra ? K::x_stage : K::t_stage);
+    uint8_t* const s_q = sm + K::x_q;
+    uint8_t* const s_kh = sm + K::x_kh;
+    uint8_t* const s_z16 = sm + K::x_z16;
+    uint8_t* const s_recv = sm + K::recv_off;
 
     if (t == 0) {
-        mbar_init(&bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&lift_full[b], 128);
+            mbar_init(&aq_free[b], 1);
+            mbar_init(&y_part[b], 1);
+            mbar_init(&y_free[b], 128);
+            mbar_init(&y_full[b], 1);
+            mbar_init(&recv_full[b], 1);
+            mbar_init(&peer_free[b], K::CS);
+        }
+        mbar_init(&v_free, 1);
+        mbar_init(&ak_free, 1);
+        mbar_init(&qk_free, 128);
+        mbar_init(&upd_done, 1);
+        mbar_init(&state_read, 128);
+        mbar_init(&s16_ready, 128);
+        mbar_init(&p_ready, 128);
+        mbar_init(&drain, 1);
         fence_mbar_init();
+        // the first two chunks' partial rows may arrive as soon as the cluster starts
+        for (int b = 0; b < 2 && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
         abort_flag = 0;
     }
     if (warp == 0) {
@@ -256,288 +339,179 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t lane0 = (uint32_t)(warp * 32);
+    const uint32_t lane0 = (uint32_t)((warp & 3) * 32);
     auto tm = [&](uint32_t col) { return tmem_addr(tb, lane0, col); };
+    auto fail = [&]() {
+        abort_flag = 1;
+        atomicOr(&g_chunked_tc_status, kStatusTimeout);
+    };
 
-    // ---- start state of this segment
-    const int sg = start_groups > 1 ? g : 0;
-    const float* S0 = S_start ? S_start + (bh * start_groups + sg) * (int64_t)n * DV : nullptr;
-    const float* z0 = z_start ? z_start + (bh * start_groups + sg) * (int64_t)n : nullptr;
-    if (!extra) {
-#pragma unroll
-        for (int tl = 0; tl < K::TPC; ++tl)
-            load_state_tile<P, DV>(S0, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), sm + K::s16_off + tl * kAtom, t);
-    } else {
-        load_state_tile<P, DV>(S0, K::NT, tm(K::tx_s), sm + K::s16_off, t);
-        // Z row t (t < P) from the packed normaliser: Z_ij = z_idx(i,j) / (sqrt2 if i != j)
-        float zr[P];
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            float val = 0.f;
-            if (z0 != nullptr && t < P) {
-                const int a = t < j ? t : j, b = t < j ? j : t;
-                val = z0[lift::canonical_index(P, a, b)] * (a == b ? 1.f : kInvSqrt2f);
-            }
-            zr[j] = val;
-        }
-#pragma unroll
-        for (int c0 = 0; c0 < P; c0 += 16) {
-            uint32_t r[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(zr[c0 + i]);
-            tmem_st16(tm(K::tx_z + c0), r);
-        }
-        if (t < P) {
-#pragma unroll
-            for (int c = 0; c < P / 8; ++c) {
-                uint4 w;
-                w.x = pack_bf16x2(zr[8 * c], zr[8 * c + 1]);
-                w.y = pack_bf16x2(zr[8 * c + 2], zr[8 * c + 3]);
-                w.z = pack_bf16x2(zr[8 * c + 4], zr[8 * c + 5]);
-                w.w = pack_bf16x2(zr[8 * c + 6], zr[8 * c + 7]);
-                *reinterpret_cast<uint4*>(sm + K::z16_off + sw128_chunk(t, 8 * c, P)) = w;
-            }
-        }
-    }
-    tmem_wait_st();
-
-    uint32_t phase = 0;
-    bool ok = true;
-    const int owner = t / K::R, orow = t % K::R;
-
-    for (int c = c_begin; c < c_end; ++c) {
-        const int tok = c * kChunk + t;
-        const bool valid = tok < T;
-        const int buf = (c - c_begin) & 1;
-        uint8_t* recv = sm + K::recv_off + buf * K::recv_buf;
-        // ---- this token's rows
-        uint4 qraw[P / 8], kraw[P / 8];
-        uint32_t uq[P / 2], uq2[P / 2], uk[P / 2];
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < P / 8; ++i) {
-            qraw[i] = valid ? *reinterpret_cast<const uint4*>(qh + (int64_t)tok * P + 8 * i) : make_uint4(0, 0, 0, 0);
-            kraw[i] = valid ? *reinterpret_cast<const uint4*>(kh + (int64_t)tok * P + 8 * i) : make_uint4(0, 0, 0, 0);
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(&qraw[i]);
-            const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uq[4 * i + j] = qw[j];
-                uq2[4 * i + j] = lift::bf16x2_mul(qw[j], 0x40004000u);  // 2q, exact
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float x = __bfloat162float(ke[j]);
-                ss = fmaf(x, x, ss);
-            }
-        }
-        const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
-#pragma unroll
-        for (int i = 0; i < P / 8; ++i) {
-            const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                uk[4 * i + j] = pack_bf16x2(__bfloat162float(ke[2 * j]) * kinv, __bfloat162float(ke[2 * j + 1]) * kinv);
-        }
-        // ---- lifts (query -> tensor memory, key -> shared memory)
+    // ---- start state of this segment (epilogue warps: lane = slot / dim)
+    if (warp >= 4 && warp < 8) {
+        const int e = t - 128;
+        const int sg = start_groups > 1 ? g : 0;
+        const float* S0 = S_start ? S_start + (bh * start_groups + sg) * (int64_t)n * DV : nullptr;
+        const float* z0 = z_start ? z_start + (bh * start_groups + sg) * (int64_t)n : nullptr;
         if (!extra) {
 #pragma unroll
             for (int tl = 0; tl < K::TPC; ++tl)
-                lift_tile<P>(rank * K::TPC + tl, uk, uq, uq2, sm + K::ak_off + 2 * tl * kAtom, t,
-                             tm(K::tm_aq + 64 * tl));
+                load_state_tile<P, DV>(S0, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), s_s16 + tl * kAtom, e);
         } else {
-            lift_tile<P>(K::NT, uk, uq, uq2, sm + K::ak_off, t, tm(K::tx_aq));
+            load_state_tile<P, DV>(S0, K::NT, tm(K::tx_s), s_s16, e);
+            float zr[P];
 #pragma unroll
-            for (int i = 0; i < P / 8; ++i) {
-                *reinterpret_cast<uint4*>(sm + K::q_off + sw128_chunk(t, 8 * i, kChunk)) = qraw[i];
-                *reinterpret_cast<uint4*>(sm + K::kh_off + sw128_chunk(t, 8 * i, kChunk)) =
-                    make_uint4(uk[4 * i], uk[4 * i + 1], uk[4 * i + 2], uk[4 * i + 3]);
+            for (int j = 0; j < P; ++j) {
+                float val = 0.f;
+                if (z0 != nullptr && e < P) {
+                    const int a = e < j ? e : j, b = e < j ? j : e;
+                    val = z0[lift::canonical_index(P, a, b)] * (a == b ? 1.f : kInvSqrt2f);
+                }
+                zr[j] = val;
             }
-        }
 #pragma unroll
-        for (int i = 0; i < DV / 8; ++i) {
-            const uint4 val = valid ? *reinterpret_cast<const uint4*>(vh + (int64_t)tok * DV + 8 * i)
-                                    : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + K::bv_off + mn_sw128_chunk(8 * i, t, kAtom)) = val;
+            for (int c = 0; c < P; c += 16) {
+                uint32_t r[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(zr[c + i]);
+                tmem_st16(tm(K::tx_z + c), r);
+            }
+            if (e < P) {
+#pragma unroll
+                for (int c = 0; c < P / 8; ++c)
+                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c, P)) =
+                        make_uint4(pack_bf16x2(zr[8 * c], zr[8 * c + 1]), pack_bf16x2(zr[8 * c + 2], zr[8 * c + 3]),
+                                   pack_bf16x2(zr[8 * c + 4], zr[8 * c + 5]), pack_bf16x2(zr[8 * c + 6], zr[8 * c + 7]));
+            }
         }
         tmem_wait_st();
         fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+    }
+    tc_fence_before();
+    cluster.sync();  // barriers initialised and start state in place cluster-wide
+    tc_fence_after();
 
-        // ---- MMA group 1
-        if (t == 0 && ok) {
-            tc_fence_after();
-            const uint32_t sb = smem_u32(sm);
-            constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
-            constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, true, true);
-            const uint64_t bv0 = sdesc_mnmajor_sw128(sb + K::bv_off, kAtom);
-            if (!extra) {
-#pragma unroll 1
-                for (int tl = 0; tl < K::TPC; ++tl)
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + K::tm_y, tb + K::tm_aq + 64 * tl + 8 * ks,
-                               sdesc_mnmajor_sw128(sb + K::s16_off + tl * kAtom + ks * 2048, kAtom), id_read,
-                               (tl > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll 1
-                for (int tl = 0; tl < K::TPC; ++tl)
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tb + K::tm_s + 64 * tl,
-                               sdesc_mnmajor_sw128(sb + K::ak_off + 2 * tl * kAtom + ks * 2048, kAtom),
-                               bv0 + (uint64_t)((ks * 2048) >> 4), id_upd, 1u);
-            } else {
-                // tail tile: readout over its TAIL slots, update
-                for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
-                    mma_ts(tb + K::tx_y, tb + K::tx_aq + 8 * ks,
-                           sdesc_mnmajor_sw128(sb + K::s16_off + ks * 2048, kAtom), id_read, ks > 0 ? 1u : 0u);
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb + K::ak_off + ks * 2048, kAtom),
-                           bv0 + (uint64_t)((ks * 2048) >> 4), id_upd, 1u);
-                // intra scores Q Kh^T and Q Z
-                constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
-                constexpr uint32_t id_w = idesc_bf16_f32(128, P);
-                for (int ks = 0; ks < P / 16; ++ks) {
-                    const uint64_t qd = sdesc_kmajor_sw128(sb + K::q_off + ks * 32);
-                    mma_ss(tb + K::tx_sc, qd, sdesc_kmajor_sw128(sb + K::kh_off + ks * 32), id_sc, ks > 0 ? 1u : 0u);
-                    mma_ss(tb + K::tx_w, qd, sdesc_kmajor_sw128(sb + K::z16_off + ks * 32), id_w, ks > 0 ? 1u : 0u);
-                }
-                // Z += Kh^T Kh (A: unit keys viewed MN-major, both M atoms on the same data)
-                constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_z, sdesc_mnmajor_sw128(sb + K::kh_off + ks * 2048, 0),
-                           sdesc_mnmajor_sw128(sb + K::kh_off + ks * 2048, kAtom), id_z, 1u);
+    if (warp < 4) {
+        // =============================================================== lift warps
+        regs_inc<kRegsWork>();
+        const __nv_bfloat16* qh = q + bh * (int64_t)T * P;
+        const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
+        const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
+        uint8_t* my_q = s_stage + t * 128;           // this token's staged rows (128-byte swizzled)
+        uint8_t* my_k = s_stage + kAtom + t * 128;
+        auto stage_qk = [&](int c) {
+            const int tok = c * kChunk + t;
+            const bool valid = tok < T;
+            const __nv_bfloat16* qs = valid ? qh + (int64_t)tok * P : qh;
+            const __nv_bfloat16* ks = valid ? kh + (int64_t)tok * P : kh;
+#pragma unroll
+            for (int i = 0; i < P / 8; ++i) {
+                cp_async16(my_q + ((i ^ (t & 7)) << 4), qs + 8 * i, valid ? 16u : 0u);
+                cp_async16(my_k + ((i ^ (t & 7)) << 4), ks + 8 * i, valid ? 16u : 0u);
             }
-            mma_commit(&bar);
-        }
-        if (ok) {
-            ok = mbar_wait(&bar, phase, &abort_flag, kWaitNs);
-            phase ^= 1;
-            if (!ok) abort_flag = 1;
-        }
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-
-        float den = 0.f;
-        if (extra) {
-            // ---- P = (Q Kh^T)^2 masked, in place as bf16; intra denominator
-            float dsum = 0.f;
-            if (ok) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < kChunk; c0 += 32) {
-                    uint32_t s0[16], s1[16], pk[16];
-                    tmem_ld16(tm(K::tx_sc + c0), s0);
-                    tmem_ld16(tm(K::tx_sc + c0 + 16), s1);
-                    tmem_wait_ld();
+            cp_async_commit();
+        };
+        uint4 vraw[DV / 8];
+        auto load_v = [&](int c) {
+            const int tok = c * kChunk + t;
+            const bool valid = tok < T;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float a = __uint_as_float(s0[2 * i]), b = __uint_as_float(s0[2 * i + 1]);
-                        float cc = __uint_as_float(s1[2 * i]), d = __uint_as_float(s1[2 * i + 1]);
-                        a = (c0 + 2 * i <= t) ? a * a : 0.f;
-                        b = (c0 + 2 * i + 1 <= t) ? b * b : 0.f;
-                        cc = (c0 + 16 + 2 * i <= t) ? cc * cc : 0.f;
-                        d = (c0 + 16 + 2 * i + 1 <= t) ? d * d : 0.f;
-                        pk[i] = pack_bf16x2(a, b);
-                        pk[8 + i] = pack_bf16x2(cc, d);
-                        const __nv_bfloat162 h0 = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
-                        const __nv_bfloat162 h1 = *reinterpret_cast<const __nv_bfloat162*>(&pk[8 + i]);
-                        dsum += (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+            for (int i = 0; i < DV / 8; ++i)
+                vraw[i] = valid ? __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)tok * DV) + i) : make_uint4(0, 0, 0, 0);
+        };
+        if (nk > 0) {
+            stage_qk(c0);
+            load_v(c0);
+        }
+        for (int kk = 0; kk < nk; ++kk) {
+            const int slot = kk & 1, use = kk >> 1;
+            cp_async_wait<0>();
+            uint32_t uq[P / 2];
+            uint4 kraw[P / 8];
+#pragma unroll
+            for (int i = 0; i < P / 8; ++i) {
+                const uint4 a = *reinterpret_cast<const uint4*>(my_q + ((i ^ (t & 7)) << 4));
+                uq[4 * i] = a.x;
+                uq[4 * i + 1] = a.y;
+                uq[4 * i + 2] = a.z;
+                uq[4 * i + 3] = a.w;
+                kraw[i] = *reinterpret_cast<const uint4*>(my_k + ((i ^ (t & 7)) << 4));
+            }
+            if (kk + 1 < nk) stage_qk(c0 + kk + 1);
+            // unit key
+            uint32_t uk[P / 2];
+            {
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < P / 8; ++i) {
+                    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float x = __bfloat162float(ke[j]);
+                        ss = fmaf(x, x, ss);
                     }
-                    tmem_st16(tm(K::tx_sc + c0 / 2), pk);
                 }
-                // inter denominator q^T Z q from W = Q Z
-                float dint = 0.f;
+                const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
 #pragma unroll
-                for (int c0 = 0; c0 < P; c0 += 16) {
-                    uint32_t w[16];
-                    tmem_ld16(tm(K::tx_w + c0), w);
-                    tmem_wait_ld();
-                    const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(qraw) + c0;
+                for (int i = 0; i < P / 8; ++i) {
+                    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dint = fmaf(__bfloat162float(qe[i]), __uint_as_float(w[i]), dint);
+                    for (int j = 0; j < 4; ++j)
+                        uk[4 * i + j] = pack_bf16x2(__bfloat162float(ke[2 * j]) * kinv, __bfloat162float(ke[2 * j + 1]) * kinv);
                 }
-                den = dsum + dint;
+            }
+            // value row (loaded during the previous chunk) -> shared memory (single buffer)
+            if (kk >= 1 && !mbar_wait(&v_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+#pragma unroll
+            for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(s_v + mn_sw128_chunk(8 * i, t, kAtom)) = vraw[i];
+            // query lift -> tensor memory slot
+            if (kk >= 2 && !mbar_wait(&aq_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            if (!extra) {
+#pragma unroll
+                for (int tl = 0; tl < K::TPC; ++tl)
+                    query_dispatch<P>(rank * K::TPC + tl, uq, tm(K::tm_aq + 128 * slot + 64 * tl));
+            } else {
+                query_tail<P>(uq, tm(K::tx_aq + 32 * slot));
+            }
+            // key lift -> shared memory (single buffer)
+            if (kk >= 1 && !mbar_wait(&ak_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!extra) {
+#pragma unroll
+                for (int tl = 0; tl < K::TPC; ++tl)
+                    key_dispatch<P>(rank * K::TPC + tl, uk, s_ak + 2 * tl * kAtom, t);
+            } else {
+                key_tail<P>(uk, s_ak, t);
+                if (kk >= 1 && !mbar_wait(&qk_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+#pragma unroll
+                for (int i = 0; i < P / 8; ++i) {
+                    *reinterpret_cast<uint4*>(s_q + sw128_chunk(t, 8 * i, kChunk)) =
+                        make_uint4(uq[4 * i], uq[4 * i + 1], uq[4 * i + 2], uq[4 * i + 3]);
+                    *reinterpret_cast<uint4*>(s_kh + sw128_chunk(t, 8 * i, kChunk)) =
+                        make_uint4(uk[4 * i], uk[4 * i + 1], uk[4 * i + 2], uk[4 * i + 3]);
+                }
             }
             tmem_wait_st();
+            fence_proxy_async_smem();
             tc_fence_before();
-            __syncthreads();
-            // ---- MMA group 2: Y += P V
-            if (t == 0 && ok) {
-                tc_fence_after();
-                const uint32_t sb = smem_u32(sm);
-                constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tb + K::tx_y, tb + K::tx_sc + 8 * ks,
-                           sdesc_mnmajor_sw128(sb + K::bv_off + ks * 2048, kAtom), id_pv, 1u);
-                mma_commit(&bar);
-            }
-            // ---- meanwhile: bf16 copies of Z and of the tail state
-            {
-                uint32_t zr[P];
-#pragma unroll
-                for (int c0 = 0; c0 < P; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tm(K::tx_z + c0), r);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) zr[c0 + i] = r[i];
-                }
-                tmem_wait_ld();
-                if (t < P) {
-#pragma unroll
-                    for (int c8 = 0; c8 < P / 8; ++c8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(zr[8 * c8]), __uint_as_float(zr[8 * c8 + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(zr[8 * c8 + 2]), __uint_as_float(zr[8 * c8 + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(zr[8 * c8 + 4]), __uint_as_float(zr[8 * c8 + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(zr[8 * c8 + 6]), __uint_as_float(zr[8 * c8 + 7]));
-                        *reinterpret_cast<uint4*>(sm + K::z16_off + sw128_chunk(t, 8 * c8, P)) = w;
-                    }
-                }
-            }
-            refresh_state_tile<DV>(tm(K::tx_s), sm + K::s16_off, t);
-            if (ok) {
-                ok = mbar_wait(&bar, phase, &abort_flag, kWaitNs);
-                phase ^= 1;
-                if (!ok) abort_flag = 1;
-            }
-            ok = __syncthreads_and(ok);
-            tc_fence_after();
-        } else {
-#pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl)
-                refresh_state_tile<DV>(tm(K::tm_s + 64 * tl), sm + K::s16_off + tl * kAtom, t);
+            mbar_arrive(&lift_full[slot]);
+            if (kk + 1 < nk) load_v(c0 + kk + 1);
         }
-
-        // ---- partial Y (and d) to the owner of this row
-        {
-            const uint32_t ycol = extra ? K::tx_y : K::tm_y;
-            float* dst = cluster.map_shared_rank(
-                reinterpret_cast<float*>(recv + rank * K::recv_part + orow * DV * 4), owner);
-#pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tm(ycol + c0), r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    reinterpret_cast<float4*>(dst + c0)[i] =
-                        make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-            }
-            if (extra) {
-                float* ddst = cluster.map_shared_rank(reinterpret_cast<float*>(recv + K::recv_den + orow * 4), owner);
-                *ddst = den;
-            }
-        }
-        tc_fence_before();
-        cluster.sync();
-        tc_fence_after();
-
-        // ---- owned rows: sum the partials, divide, store
-        {
+        cp_async_wait<0>();
+    } else if (warp < 8) {
+        // =============================================================== epilogue warps
+        regs_inc<kRegsWork>();
+        const int e = t - 128;
+        const int owner = e / K::R, orow = e % K::R;
+        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
+        // owner side: sum the partial rows of chunk c0 + kr, divide, store; then
+        // hand the receive slot back to every sender
+        auto reduce = [&](int kr) -> bool {
+            const int r = kr & 1;
+            if (!mbar_wait_cluster(&recv_full[r], (kr >> 1) & 1, &abort_flag, kWaitNs)) return false;
+            const uint8_t* recv = s_recv + r * K::recv_buf;
             const int r0 = rank * K::R;
-            const int rows = min(K::R, kChunk - r0);
-            for (int e = t; e < rows * (DV / 2); e += kThreads) {
-                const int lr = e / (DV / 2), col = 2 * (e % (DV / 2));
+            for (int idx = e; idx < my_rows * (DV / 2); idx += 128) {
+                const int lr = idx / (DV / 2), col = 2 * (idx % (DV / 2));
                 float a = 0.f, b = 0.f;
 #pragma unroll
                 for (int src = 0; src < K::CS; ++src) {
@@ -547,49 +521,286 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 }
                 const float d = *reinterpret_cast<const float*>(recv + K::recv_den + lr * 4);
                 const float inv = d > 0.f ? 1.f / d : 0.f;
-                const int otok = c * kChunk + r0 + lr;
+                const int otok = (c0 + kr) * kChunk + r0 + lr;
                 if (otok < T)
-                    *reinterpret_cast<__nv_bfloat162*>(oh + (int64_t)otok * DV + col) =
-                        __floats2bfloat162_rn(a * inv, b * inv);
+                    *reinterpret_cast<__nv_bfloat162*>(oh + (int64_t)otok * DV + col) = __floats2bfloat162_rn(a * inv, b * inv);
             }
-        }
-    }
-
-    // ---- final state of the last segment
-    if (S_final != nullptr && g == G - 1) {
-        const int64_t head_s = bh * (int64_t)n * DV, head_z = bh * (int64_t)n;
-        if (!extra) {
+            named_sync(1, 128);
+            if (e == 0 && kr + 2 < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
+            if (e < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], e));
+            return true;
+        };
+        bool ok = true;
+        for (int kk = 0; kk < nk && ok; ++kk) {
+            const int slot = kk & 1, use = kk >> 1;
+            // state after this chunk's update
+            if (!mbar_wait(&upd_done, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            uint32_t sreg[K::TPC][DV / 2];  // bf16 pairs of this lane's state rows
+            uint32_t zreg[P / 2];           // extra CTA: bf16 pairs of this lane's Z row
+            float den = 0.f;
+            if (!extra) {
 #pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl)
-                store_state_tile<P, DV>(S_final + head_s, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), t);
-        } else {
-            store_state_tile<P, DV>(S_final + head_s, K::NT, tm(K::tx_s), t);
-            uint32_t zr[P];
+                for (int tl = 0; tl < K::TPC; ++tl)
 #pragma unroll
-            for (int c0 = 0; c0 < P; c0 += 16) {
+                    for (int c16 = 0; c16 < DV; c16 += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(tm(K::tm_s + 64 * tl + c16), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            sreg[tl][c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    }
+                tc_fence_before();
+                mbar_arrive(&state_read);
+            } else {
+#pragma unroll
+                for (int c16 = 0; c16 < DV; c16 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tm(K::tx_s + c16), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        sreg[0][c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                }
+#pragma unroll
+                for (int c16 = 0; c16 < P; c16 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tm(K::tx_z + c16), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        zreg[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                }
+                tc_fence_before();
+                mbar_arrive(&state_read);
+                // P = (Q Kh^T)^2 masked (s <= t), bf16, in place; its row sum
+#pragma unroll 1
+                for (int c32 = 0; c32 < kChunk; c32 += 32) {
+                    uint32_t s0[16], s1[16], pk[16];
+                    tmem_ld16(tm(K::tx_sc + c32), s0);
+                    tmem_ld16(tm(K::tx_sc + c32 + 16), s1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float a = __uint_as_float(s0[2 * i]), b = __uint_as_float(s0[2 * i + 1]);
+                        float cc = __uint_as_float(s1[2 * i]), d = __uint_as_float(s1[2 * i + 1]);
+                        a = (c32 + 2 * i <= e) ? a * a : 0.f;
+                        b = (c32 + 2 * i + 1 <= e) ? b * b : 0.f;
+                        cc = (c32 + 16 + 2 * i <= e) ? cc * cc : 0.f;
+                        d = (c32 + 16 + 2 * i + 1 <= e) ? d * d : 0.f;
+                        pk[i] = pack_bf16x2(a, b);
+                        pk[8 + i] = pack_bf16x2(cc, d);
+                        const __nv_bfloat162 h0 = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+                        const __nv_bfloat162 h1 = *reinterpret_cast<const __nv_bfloat162*>(&pk[8 + i]);
+                        den += (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+                    }
+                    tmem_st16(tm(K::tx_sc + c32 / 2), pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_ready);
+            }
+            // this chunk's readout is done: its bf16 state copy may be replaced
+            if (!mbar_wait(&y_part[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            if (extra) {
+                // inter-chunk denominator q^T Z q from W = Q Z (Z before this chunk)
+                uint4 qrow[P / 8];
+#pragma unroll
+                for (int i = 0; i < P / 8; ++i) qrow[i] = *reinterpret_cast<const uint4*>(s_q + sw128_chunk(e, 8 * i, kChunk));
+                const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(qrow);
+                float dint = 0.f;
+#pragma unroll
+                for (int c16 = 0; c16 < P; c16 += 16) {
+                    uint32_t w[16];
+                    tmem_ld16(tm(K::tx_w + c16), w);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dint = fmaf(__bfloat162float(qe[c16 + i]), __uint_as_float(w[i]), dint);
+                }
+                den += dint;
+                tc_fence_before();
+                mbar_arrive(&qk_free);  // Q and W of this chunk have been read
+            }
+            auto write_s16 = [&](const uint32_t (&x)[DV / 2], int tl) {
+#pragma unroll
+                for (int c8 = 0; c8 < DV / 8; ++c8)
+                    *reinterpret_cast<uint4*>(s_s16 + tl * kAtom + mn_sw128_chunk(8 * c8, e, kAtom)) =
+                        make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
+            };
+            if (!extra) {
+#pragma unroll
+                for (int tl = 0; tl < K::TPC; ++tl) write_s16(sreg[tl], tl);
+            } else {
+                write_s16(sreg[0], 0);
+                if (e < P) {
+#pragma unroll
+                    for (int c8 = 0; c8 < P / 8; ++c8)
+                        *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, P)) =
+                            make_uint4(zreg[4 * c8], zreg[4 * c8 + 1], zreg[4 * c8 + 2], zreg[4 * c8 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s16_ready);
+            if (extra) {
+                if (!mbar_wait(&y_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                tc_fence_after();
+            }
+            // partial readout of this lane's row -> its owner
+            float yrow[DV];
+            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
+#pragma unroll
+            for (int c16 = 0; c16 < DV; c16 += 16) {
                 uint32_t r[16];
-                tmem_ld16(tm(K::tx_z + c0), r);
+                tmem_ld16(tm(ycol + c16), r);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) zr[c0 + i] = r[i];
+                for (int i = 0; i < 16; ++i) yrow[c16 + i] = __uint_as_float(r[i]);
             }
             tmem_wait_ld();
-            if (t < P) {
+            tc_fence_before();
+            mbar_arrive(&y_free[slot]);
+            if (kk >= 2 && !mbar_wait_cluster(&peer_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            uint8_t* recv = s_recv + slot * K::recv_buf;
+            uint8_t* dst = recv + rank * K::recv_part + orow * DV * 4;
+            if (owner == rank) {
 #pragma unroll
-                for (int j = 0; j < P; ++j)
-                    if (j >= t)
-                        z_final[head_z + lift::canonical_index(P, t, j)] =
-                            __uint_as_float(zr[j]) * (j == t ? 1.f : kSqrt2f);
+                for (int i = 0; i < DV / 4; ++i)
+                    *reinterpret_cast<float4*>(dst + 16 * i) = make_float4(yrow[4 * i], yrow[4 * i + 1], yrow[4 * i + 2], yrow[4 * i + 3]);
+                if (extra) *reinterpret_cast<float*>(recv + K::recv_den + orow * 4) = den;
+            } else {
+                const uint32_t rdst = cluster_addr(dst, owner);
+                const uint32_t rbar = cluster_addr(&recv_full[slot], owner);
+#pragma unroll
+                for (int i = 0; i < DV / 4; ++i)
+                    st_async_v4(rdst + 16 * i, yrow[4 * i], yrow[4 * i + 1], yrow[4 * i + 2], yrow[4 * i + 3], rbar);
+                if (extra) st_async_f32(cluster_addr(recv + K::recv_den + orow * 4, owner), den, rbar);
+            }
+            // owned rows of the previous chunk
+            if (kk >= 1 && !reduce(kk - 1)) { fail(); ok = false; }
+        }
+        if (ok && !abort_flag && nk >= 1 && !reduce(nk - 1)) fail();
+        // final state of the last segment
+        if (S_final != nullptr && g == G - 1 && !abort_flag) {
+            const int64_t head_s = bh * (int64_t)n * DV, head_z = bh * (int64_t)n;
+            if (!extra) {
+#pragma unroll
+                for (int tl = 0; tl < K::TPC; ++tl)
+                    store_state_tile<P, DV>(S_final + head_s, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), e);
+            } else {
+                store_state_tile<P, DV>(S_final + head_s, K::NT, tm(K::tx_s), e);
+                uint32_t zr[P];
+#pragma unroll
+                for (int c16 = 0; c16 < P; c16 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tm(K::tx_z + c16), r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zr[c16 + i] = r[i];
+                }
+                tmem_wait_ld();
+                if (e < P) {
+#pragma unroll
+                    for (int j = 0; j < P; ++j)
+                        if (j >= e)
+                            z_final[head_z + lift::canonical_index(P, e, j)] = __uint_as_float(zr[j]) * (j == e ? 1.f : kSqrt2f);
+                }
             }
         }
+    } else {
+        regs_dec<kRegsMma>();
     }
-    if (!ok && t == 0) atomicOr(&g_chunked_tc_status, kStatusTimeout);
-    if (!ok) mbar_wait_quiet(&bar, phase ^ 1, kWaitNs / 4);
+    if (t == 256) {
+        // =============================================================== MMA issuer
+        const uint32_t sb_ak = smem_u32(s_ak), sb_v = smem_u32(s_v), sb_s16 = smem_u32(s_s16);
+        constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
+        constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, true, true);
+        for (int kk = 0; kk < nk; ++kk) {
+            const int slot = kk & 1, use = kk >> 1;
+            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            // ---- group U: state updates (and, extra CTA: Z update, intra scores)
+            if (!extra) {
+#pragma unroll 1
+                for (int tl = 0; tl < K::TPC; ++tl)
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ss(tb + K::tm_s + 64 * tl, sdesc_mnmajor_sw128(sb_ak + 2 * tl * kAtom + ks * 2048, kAtom),
+                               sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom), id_upd, 1u);
+                mma_commit(&upd_done);
+                mma_commit(&ak_free);
+                mma_commit(&v_free);
+            } else {
+                // tail tile: one 64-slot atom, the second M atom aliases it (rows past the tail are never read)
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb_ak + ks * 2048, 0), sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom),
+                           id_upd, 1u);
+                const uint32_t sb_kh = smem_u32(s_kh), sb_q = smem_u32(s_q);
+                constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tb + K::tx_z, sdesc_mnmajor_sw128(sb_kh + ks * 2048, 0),
+                           sdesc_mnmajor_sw128(sb_kh + ks * 2048, kAtom), id_z, 1u);
+                constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
+                for (int ks = 0; ks < P / 16; ++ks)
+                    mma_ss(tb + K::tx_sc, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_kh + ks * 32), id_sc,
+                           ks > 0 ? 1u : 0u);
+                mma_commit(&upd_done);
+                mma_commit(&ak_free);
+            }
+            // ---- group R: readout of the state before this chunk
+            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            if (!extra) {
+#pragma unroll 1
+                for (int tl = 0; tl < K::TPC; ++tl)
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(tb + K::tm_y + 64 * slot, tb + K::tm_aq + 128 * slot + 64 * tl + 8 * ks,
+                               sdesc_mnmajor_sw128(sb_s16 + tl * kAtom + ks * 2048, kAtom), id_read, (tl > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&y_part[slot]);
+                mma_commit(&aq_free[slot]);
+            } else {
+                for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
+                    mma_ts(tb + K::tx_y + 64 * slot, tb + K::tx_aq + 32 * slot + 8 * ks,
+                           sdesc_mnmajor_sw128(sb_s16 + ks * 2048, kAtom), id_read, ks > 0 ? 1u : 0u);
+                const uint32_t sb_q = smem_u32(s_q), sb_z16 = smem_u32(s_z16);
+                constexpr uint32_t id_w = idesc_bf16_f32(128, P);
+                for (int ks = 0; ks < P / 16; ++ks)
+                    mma_ss(tb + K::tx_w, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_z16 + ks * 32), id_w,
+                           ks > 0 ? 1u : 0u);
+                mma_commit(&y_part[slot]);
+                mma_commit(&aq_free[slot]);
+                // ---- group PV: intra-chunk part
+                if (!mbar_wait(&p_ready, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                tc_fence_after();
+                constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(tb + K::tx_y + 64 * slot, tb + K::tx_sc + 8 * ks, sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom), id_pv, 1u);
+                mma_commit(&y_full[slot]);
+                mma_commit(&v_free);
+            }
+        }
+        // every issued MMA has completed before tensor memory is released
+        mma_commit(&drain);
+        mbar_wait_quiet(&drain, 0, kWaitNs);
+    }
+
     tc_fence_before();
+    __syncwarp();
     cluster.sync();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 // ---------------------------------------------------------------- host side
+// The register split of the kernel fits in its launch allocation.
+template <int P, int DV>
+bool register_split_fits() {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, chunked_tc_kernel<P, DV>) != cudaSuccess) return false;
+    return (uint32_t)kThreads * (uint32_t)fa.numRegs >= 128u * (2u * kRegsWork + kRegsMma);
+}
+
 template <int P, int DV>
 cudaError_t configure(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int G, int BH, cudaStream_t s) {
     using K = Cfg<P, DV>;
@@ -620,7 +831,7 @@ int max_clusters() {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         int m = 0;
-        if (configure<P, DV>(cfg, attr, 1, 1, 0) != cudaSuccess ||
+        if (!register_split_fits<P, DV>() || configure<P, DV>(cfg, attr, 1, 1, 0) != cudaSuccess ||
             cudaOccupancyMaxActiveClusters(&m, chunked_tc_kernel<P, DV>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             return 0;
@@ -634,6 +845,7 @@ template <int P, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, const float* S_start,
                          const float* z_start, int start_groups, float* S_final, float* z_final, int BH, int T,
                          int seg_chunks, int G, cudaStream_t s) {
+    if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     cudaError_t e = configure<P, DV>(cfg, attr, G, BH, s);

@@ -63,10 +63,10 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 }
 
 // Packed bf16x2 word holding the lift at slots (2w, 2w+1) of the vector u
-// (u: P/2 packed words; u2: the same vector doubled, used for the query's
-// off-diagonal factor 2 when QUERY).  Slots at or past n give 0.
+// (P/2 packed words).  QUERY applies the query's factor 2 to off-diagonal
+// slots (exact in bf16).  Slots at or past n give 0.
 template <int P, bool QUERY>
-__device__ __forceinline__ uint32_t lift_word(const uint32_t* u, const uint32_t* u2, int w) {
+__device__ __forceinline__ uint32_t lift_word(const uint32_t* u, int w) {
     constexpr int n = packed_n(P);
     const int s0 = 2 * w, s1 = 2 * w + 1;
     if (s0 >= n) return 0u;
@@ -78,9 +78,11 @@ __device__ __forceinline__ uint32_t lift_word(const uint32_t* u, const uint32_t*
         i1 = i0;
         j1 = j0;
     }
-    const uint32_t* a0 = (QUERY && i0 < j0) ? u2 : u;
-    const uint32_t* a1 = (QUERY && i1 < j1) ? u2 : u;
-    const uint32_t x = bf16_pair(a0, i0, a1, i1);
+    uint32_t x = bf16_pair(u, i0, u, i1);
+    if (QUERY) {
+        const uint32_t f = (i0 < j0 ? 0x4000u : 0x3F80u) | ((i1 < j1 ? 0x4000u : 0x3F80u) << 16);  // (2|1, 2|1)
+        if (f != 0x3F803F80u) x = bf16x2_mul(x, f);
+    }
     const uint32_t y = bf16_pair(u, j0, u, j1);
     const uint32_t r = bf16x2_mul(x, y);
     return s1 < n ? r : (r & 0xFFFFu);

@@ -49,10 +49,10 @@ __device__ __forceinline__ void key_tile_to_smem(const uint32_t (&u)[P / 2], uin
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         uint4 val;
-        val.x = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 0);
-        val.y = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 1);
-        val.z = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 2);
-        val.w = lift::lift_word<P, false>(u, u, 64 * TAU + 4 * c + 3);
+        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
+        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
+        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
+        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
         *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
     }
 }
