@@ -39,12 +39,13 @@ namespace cg = cooperative_groups;
 
 __device__ unsigned int g_chunked_tc_status = 0;
 
-constexpr int kThreads = 384;  // warpgroups: lift, epilogue, MMA (one issuing thread)
+
+constexpr int kThreads = 512;  // warpgroups: lift, state epilogue, readout epilogue, MMA
 // Register split between the warpgroups after launch (setmaxnreg): the MMA
-// warpgroup gives back registers the two working warpgroups take.  Their sum,
-// 128 * (2 * kRegsWork + kRegsMma), must not exceed 384 * (registers per thread
-// at launch); the launcher checks that before every launch.
-constexpr uint32_t kRegsWork = 192, kRegsMma = 88;
+// warpgroup gives back registers that the lift and state warpgroups take.
+// 128 * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma) must not exceed
+// 512 * (registers per thread at launch); the launcher checks that.
+constexpr uint32_t kRegsLift = 168, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 88;
 constexpr int kChunk = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes
@@ -64,17 +65,21 @@ struct Cfg {
     static constexpr int R = (kChunk + CS - 1) / CS;   // output rows owned per CTA
     // shared memory, in 16 KB atoms from a 1024-byte aligned base
     //   tile CTA : key lift [0, 2 TPC), V, bf16 state [TPC], query/key staging [2]
-    //   extra CTA: tail key lift, Q, unit keys, bf16 Z, V, bf16 tail state, staging [2]
+    //   extra CTA: tail key lift, Q, unit keys, bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
     static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 1) * kAtom,
                               t_stage = (3 * TPC + 1) * kAtom;
     static constexpr uint32_t x_ak = 0, x_q = 1 * kAtom, x_kh = 2 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
-                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom;
-    static constexpr uint32_t atoms = (3 * TPC + 3) > 8 ? (3 * TPC + 3) : 8;
+                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom, x_v2 = 8 * kAtom;  // extra: V slots x_v, x_v2
+    static constexpr uint32_t atoms = (3 * TPC + 3) > 9 ? (3 * TPC + 3) : 9;
+    // partial readouts: one part per (source CTA, receive slot) = R rows of bf16
+    // laid out [DV/8][R] x 16 bytes (a warp's store of one column group is
+    // contiguous per owner), then R fp32 denominators (extra CTA's part only)
+    static constexpr uint32_t part_y = R * DV * 2;
+    static constexpr uint32_t recv_part = part_y + round16(R * 4);
+    static constexpr uint32_t recv_buf = CS * recv_part;
+    static constexpr int RS = 4;                        // receive slots (chunks in flight)
     static constexpr uint32_t recv_off = atoms * kAtom;
-    static constexpr uint32_t recv_part = R * DV * 4;  // one CTA's partial rows
-    static constexpr uint32_t recv_den = CS * recv_part;
-    static constexpr uint32_t recv_buf = round16(recv_den + R * 4);
-    static constexpr uint32_t total = recv_off + 2 * recv_buf;
+    static constexpr uint32_t total = recv_off + RS * recv_buf;
     static constexpr size_t smem = total + 1024;
     // tensor memory columns, tile CTA
     static constexpr uint32_t tm_s = 0;      // TPC x 64: fp32 state
@@ -257,19 +262,22 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 }
 
 // ---------------------------------------------------------------- kernel
-// Warp roles (384 threads, three warpgroups):
-//   warps 0-3  lift:     thread t = token t of the chunk; stages its query
-//                        and key rows one chunk ahead (cp.async), puts the key
-//                        on the unit sphere, writes the query lift (tensor
-//                        memory) and key lift (shared memory), the value row
-//   warps 4-7  epilogue: thread e = tensor-memory lane e; reads the state after
-//                        each update, refreshes its bf16 copy, sends the partial
-//                        readout to the row owners, reduces its owned rows one
-//                        chunk later
-//   warps 8-11 MMA:      one thread issues every tcgen05.mma
+// Warp roles (512 threads, four warpgroups):
+//   warps 0-3   lift:     thread t = token t of the chunk; stages its query
+//                         and key rows one chunk ahead (cp.async), puts the key
+//                         on the unit sphere, writes the query lift (tensor
+//                         memory), the key lift (shared memory), the value row
+//   warps 4-7   state:    thread e = tensor-memory lane e; reads the state
+//                         after each update and releases it to the next update,
+//                         refreshes the bf16 copy for the next readout (extra
+//                         CTA: also P = scores^2 and the denominators)
+//   warps 8-11  readout:  thread e = lane e; reads the partial readout, sends
+//                         it to the row owners, reduces its owned rows one
+//                         chunk later and stores o
+//   warps 12-15 MMA:      one thread issues every tcgen05.mma
 // Per chunk the MMAs run update (state += lift(K)^T V) then readout
-// (Y = lift(Q) S), so the next update starts as soon as the epilogue has read
-// the state.
+// (Y = lift(Q) S), so the next update starts as soon as the state warps have
+// read the state.
 template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -280,8 +288,10 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     constexpr int n = K::n;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], y_full[2], recv_full[2], peer_free[2];
-    __shared__ uint64_t v_free, ak_free, qk_free, upd_done, state_read, s16_ready, p_ready, drain;
+    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], y_full[2], den_ready[2], v_free[2];
+    __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
+    __shared__ float dens[2][kChunk];  // extra CTA: denominators of the chunk rows
+    __shared__ uint64_t ak_free, qk_free, upd_done, state_read, s16_ready, p_ready, sc_done, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -297,10 +307,13 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int nk = c1 - c0;
     const int my_rows = min(K::R, kChunk - rank * K::R);
     // bytes of partial rows (and denominators) other CTAs deliver per chunk
-    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 4 + (extra ? 0 : my_rows * 4);
+    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + (extra ? 0 : my_rows * 4);
     // shared memory of this CTA's role
     uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
     uint8_t* const s_v = sm + (extra ? K::x_v : K::t_v);
+    // value buffer of chunk kk: the extra CTA keeps two (its intra-chunk MMA
+    // reads V one chunk later), a tile CTA one
+    auto v_buf = [&](int kk) { return (extra && (kk & 1)) ? sm + K::x_v2 : s_v; };
     uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
     uint8_t* const s_stage = sm + (extra ? K::x_stage : K::t_stage);
     uint8_t* const s_q = sm + K::x_q;
@@ -315,10 +328,11 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             mbar_init(&y_part[b], 1);
             mbar_init(&y_free[b], 128);
             mbar_init(&y_full[b], 1);
-            mbar_init(&recv_full[b], 1);
-            mbar_init(&peer_free[b], K::CS);
+
+            mbar_init(&den_ready[b], 128);
+            mbar_init(&v_free[b], 1);
         }
-        mbar_init(&v_free, 1);
+        mbar_init(&sc_done, 1);
         mbar_init(&ak_free, 1);
         mbar_init(&qk_free, 128);
         mbar_init(&upd_done, 1);
@@ -327,8 +341,13 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         mbar_init(&p_ready, 128);
         mbar_init(&drain, 1);
         fence_mbar_init();
-        // the first two chunks' partial rows may arrive as soon as the cluster starts
-        for (int b = 0; b < 2 && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
+        for (int b = 0; b < K::RS; ++b) {
+            mbar_init(&recv_full[b], 1);
+            mbar_init(&peer_free[b], K::CS);
+        }
+        fence_mbar_init();
+        // the first RS chunks' partial rows may arrive as soon as the cluster starts
+        for (int b = 0; b < K::RS && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
         abort_flag = 0;
     }
     if (warp == 0) {
@@ -392,7 +411,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
     if (warp < 4) {
         // =============================================================== lift warps
-        regs_inc<kRegsWork>();
+        regs_inc<kRegsLift>();
         const __nv_bfloat16* qh = q + bh * (int64_t)T * P;
         const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
         const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
@@ -459,11 +478,8 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                         uk[4 * i + j] = pack_bf16x2(__bfloat162float(ke[2 * j]) * kinv, __bfloat162float(ke[2 * j + 1]) * kinv);
                 }
             }
-            // value row (loaded during the previous chunk) -> shared memory (single buffer)
-            if (kk >= 1 && !mbar_wait(&v_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-#pragma unroll
-            for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(s_v + mn_sw128_chunk(8 * i, t, kAtom)) = vraw[i];
-            // query lift -> tensor memory slot
+            // query lift -> tensor memory slot (double-buffered: overlaps the
+            // previous chunk's update)
             if (kk >= 2 && !mbar_wait(&aq_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
@@ -472,6 +488,17 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                     query_dispatch<P>(rank * K::TPC + tl, uq, tm(K::tm_aq + 128 * slot + 64 * tl));
             } else {
                 query_tail<P>(uq, tm(K::tx_aq + 32 * slot));
+            }
+            // value row (loaded during the previous chunk) -> its buffer
+            if (!extra) {
+                if (kk >= 1 && !mbar_wait(&v_free[0], (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            } else {
+                if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            }
+            {
+                uint8_t* vb = v_buf(kk);
+#pragma unroll
+                for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(vb + mn_sw128_chunk(8 * i, t, kAtom)) = vraw[i];
             }
             // key lift -> shared memory (single buffer)
             if (kk >= 1 && !mbar_wait(&ak_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
@@ -498,38 +525,9 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
         cp_async_wait<0>();
     } else if (warp < 8) {
-        // =============================================================== epilogue warps
-        regs_inc<kRegsWork>();
+        // =============================================================== state warps
+        regs_inc<kRegsState>();
         const int e = t - 128;
-        const int owner = e / K::R, orow = e % K::R;
-        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
-        // owner side: sum the partial rows of chunk c0 + kr, divide, store; then
-        // hand the receive slot back to every sender
-        auto reduce = [&](int kr) -> bool {
-            const int r = kr & 1;
-            if (!mbar_wait_cluster(&recv_full[r], (kr >> 1) & 1, &abort_flag, kWaitNs)) return false;
-            const uint8_t* recv = s_recv + r * K::recv_buf;
-            const int r0 = rank * K::R;
-            for (int idx = e; idx < my_rows * (DV / 2); idx += 128) {
-                const int lr = idx / (DV / 2), col = 2 * (idx % (DV / 2));
-                float a = 0.f, b = 0.f;
-#pragma unroll
-                for (int src = 0; src < K::CS; ++src) {
-                    const float2 x = *reinterpret_cast<const float2*>(recv + src * K::recv_part + (lr * DV + col) * 4);
-                    a += x.x;
-                    b += x.y;
-                }
-                const float d = *reinterpret_cast<const float*>(recv + K::recv_den + lr * 4);
-                const float inv = d > 0.f ? 1.f / d : 0.f;
-                const int otok = (c0 + kr) * kChunk + r0 + lr;
-                if (otok < T)
-                    *reinterpret_cast<__nv_bfloat162*>(oh + (int64_t)otok * DV + col) = __floats2bfloat162_rn(a * inv, b * inv);
-            }
-            named_sync(1, 128);
-            if (e == 0 && kr + 2 < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
-            if (e < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], e));
-            return true;
-        };
         bool ok = true;
         for (int kk = 0; kk < nk && ok; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
@@ -575,27 +573,29 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 tc_fence_before();
                 mbar_arrive(&state_read);
                 // P = (Q Kh^T)^2 masked (s <= t), bf16, in place; its row sum
-#pragma unroll 1
-                for (int c32 = 0; c32 < kChunk; c32 += 32) {
-                    uint32_t s0[16], s1[16], pk[16];
-                    tmem_ld16(tm(K::tx_sc + c32), s0);
-                    tmem_ld16(tm(K::tx_sc + c32 + 16), s1);
-                    tmem_wait_ld();
+                if (!mbar_wait(&sc_done, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                tc_fence_after();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float a = __uint_as_float(s0[2 * i]), b = __uint_as_float(s0[2 * i + 1]);
-                        float cc = __uint_as_float(s1[2 * i]), d = __uint_as_float(s1[2 * i + 1]);
-                        a = (c32 + 2 * i <= e) ? a * a : 0.f;
-                        b = (c32 + 2 * i + 1 <= e) ? b * b : 0.f;
-                        cc = (c32 + 16 + 2 * i <= e) ? cc * cc : 0.f;
-                        d = (c32 + 16 + 2 * i + 1 <= e) ? d * d : 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sc[64];
+#pragma unroll
+                    for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld16(tm(K::tx_sc + 64 * h + c16), *reinterpret_cast<uint32_t(*)[16]>(sc + c16));
+                    tmem_wait_ld();
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = 64 * h + 2 * i;
+                        float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
+                        a = col <= e ? a * a : 0.f;
+                        b = col + 1 <= e ? b * b : 0.f;
                         pk[i] = pack_bf16x2(a, b);
-                        pk[8 + i] = pack_bf16x2(cc, d);
-                        const __nv_bfloat162 h0 = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
-                        const __nv_bfloat162 h1 = *reinterpret_cast<const __nv_bfloat162*>(&pk[8 + i]);
-                        den += (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+                        // the row sum of the rounded weights, so the intra-chunk
+                        // weights stay an exact convex combination
+                        const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+                        den += __low2float(hp) + __high2float(hp);
                     }
-                    tmem_st16(tm(K::tx_sc + c32 / 2), pk);
+                    tmem_st16(tm(K::tx_sc + 32 * h), *reinterpret_cast<uint32_t(*)[16]>(pk));
+                    tmem_st16(tm(K::tx_sc + 32 * h + 16), *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -645,42 +645,10 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             tc_fence_before();
             mbar_arrive(&s16_ready);
             if (extra) {
-                if (!mbar_wait(&y_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
-                tc_fence_after();
+                dens[slot][e] = den;
+                mbar_arrive(&den_ready[slot]);
             }
-            // partial readout of this lane's row -> its owner
-            float yrow[DV];
-            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
-#pragma unroll
-            for (int c16 = 0; c16 < DV; c16 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tm(ycol + c16), r);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) yrow[c16 + i] = __uint_as_float(r[i]);
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&y_free[slot]);
-            if (kk >= 2 && !mbar_wait_cluster(&peer_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            uint8_t* recv = s_recv + slot * K::recv_buf;
-            uint8_t* dst = recv + rank * K::recv_part + orow * DV * 4;
-            if (owner == rank) {
-#pragma unroll
-                for (int i = 0; i < DV / 4; ++i)
-                    *reinterpret_cast<float4*>(dst + 16 * i) = make_float4(yrow[4 * i], yrow[4 * i + 1], yrow[4 * i + 2], yrow[4 * i + 3]);
-                if (extra) *reinterpret_cast<float*>(recv + K::recv_den + orow * 4) = den;
-            } else {
-                const uint32_t rdst = cluster_addr(dst, owner);
-                const uint32_t rbar = cluster_addr(&recv_full[slot], owner);
-#pragma unroll
-                for (int i = 0; i < DV / 4; ++i)
-                    st_async_v4(rdst + 16 * i, yrow[4 * i], yrow[4 * i + 1], yrow[4 * i + 2], yrow[4 * i + 3], rbar);
-                if (extra) st_async_f32(cluster_addr(recv + K::recv_den + orow * 4, owner), den, rbar);
-            }
-            // owned rows of the previous chunk
-            if (kk >= 1 && !reduce(kk - 1)) { fail(); ok = false; }
         }
-        if (ok && !abort_flag && nk >= 1 && !reduce(nk - 1)) fail();
         // final state of the last segment
         if (S_final != nullptr && g == G - 1 && !abort_flag) {
             const int64_t head_s = bh * (int64_t)n * DV, head_z = bh * (int64_t)n;
@@ -707,49 +675,169 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 }
             }
         }
+    } else if (warp < 12) {
+        // =============================================================== readout warps
+        const int e = t - 256;
+        const int owner = e / K::R, orow = e % K::R;
+        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
+        // owner side: sum the partial rows of chunk c0 + kr, hand the receive
+        // slot back to every sender, then divide and store
+        auto reduce = [&](int kr) -> bool {
+            const int r = kr % K::RS;
+            if (!mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs)) return false;
+            const uint8_t* recv = s_recv + r * K::recv_buf;
+            const int r0 = rank * K::R;
+            const int items = my_rows * (DV / 8);
+            // 8-column groups of owned rows, at most MAXIT per lane
+            constexpr int MAXIT = (K::R * (DV / 8) + 127) / 128;
+            float acc[MAXIT][8];
+            float dd[MAXIT];
+#pragma unroll
+            for (int it = 0; it < MAXIT; ++it) {
+                const int idx = e + 128 * it;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[it][j] = 0.f;
+                dd[it] = 0.f;
+                if (idx < items) {
+                    const int lr = idx % my_rows, i = idx / my_rows;
+#pragma unroll
+                    for (int src = 0; src < K::CS; ++src) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
+                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[it][2 * j] += __low2float(h[j]);
+                            acc[it][2 * j + 1] += __high2float(h[j]);
+                        }
+                    }
+                    dd[it] = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
+                }
+            }
+            named_sync(1, 128);
+            if (e == 0 && kr + K::RS < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
+            if (e < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], e));
+#pragma unroll
+            for (int it = 0; it < MAXIT; ++it) {
+                const int idx = e + 128 * it;
+                if (idx < items) {
+                    const int lr = idx % my_rows, i = idx / my_rows;
+                    const float inv = dd[it] > 0.f ? 1.f / dd[it] : 0.f;
+                    const int otok = (c0 + kr) * kChunk + r0 + lr;
+                    if (otok < T)
+                        *reinterpret_cast<uint4*>(oh + (int64_t)otok * DV + 8 * i) = make_uint4(
+                            pack_bf16x2(acc[it][0] * inv, acc[it][1] * inv), pack_bf16x2(acc[it][2] * inv, acc[it][3] * inv),
+                            pack_bf16x2(acc[it][4] * inv, acc[it][5] * inv), pack_bf16x2(acc[it][6] * inv, acc[it][7] * inv));
+                }
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int kk = 0; kk < nk && ok; ++kk) {
+            const int slot = kk & 1, use = kk >> 1;
+            const int rs = kk % K::RS, ruse = kk / K::RS;
+            // partial readout of this lane's row -> its owner
+            if (!mbar_wait(extra ? &y_full[slot] : &y_part[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            tc_fence_after();
+            float den = 0.f;
+            if (extra) {
+                if (!mbar_wait(&den_ready[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                den = dens[slot][e];
+            }
+            uint32_t ypk[DV / 2];
+            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
+#pragma unroll
+            for (int c16 = 0; c16 < DV; c16 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tm(ycol + c16), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ypk[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            }
+            tc_fence_before();
+            mbar_arrive(&y_free[slot]);
+            // the owners have consumed what this receive slot held RS chunks ago
+            if (kk >= K::RS && !mbar_wait_cluster(&peer_free[rs], (ruse - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            uint8_t* recv = s_recv + rs * K::recv_buf;
+            uint8_t* dst = recv + rank * K::recv_part + orow * 16;
+            if (owner == rank) {
+#pragma unroll
+                for (int i = 0; i < DV / 8; ++i)
+                    *reinterpret_cast<uint4*>(dst + i * K::R * 16) = make_uint4(ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3]);
+                if (extra) *reinterpret_cast<float*>(recv + rank * K::recv_part + K::part_y + orow * 4) = den;
+            } else {
+                const uint32_t rdst = cluster_addr(dst, owner);
+                const uint32_t rbar = cluster_addr(&recv_full[rs], owner);
+#pragma unroll
+                for (int i = 0; i < DV / 8; ++i)
+                    st_async_v4_b32(rdst + i * K::R * 16, ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3], rbar);
+                if (extra) st_async_f32(cluster_addr(recv + rank * K::recv_part + K::part_y + orow * 4, owner), den, rbar);
+            }
+            // owned rows two chunks back
+            if (kk >= 2 && !reduce(kk - 2)) { fail(); ok = false; }
+        }
+        for (int kr = nk >= 2 ? nk - 2 : 0; kr < nk && ok && !abort_flag; ++kr)
+            if (!reduce(kr)) fail();
     } else {
         regs_dec<kRegsMma>();
     }
-    if (t == 256) {
+    if (t == 384) {
         // =============================================================== MMA issuer
         const uint32_t sb_ak = smem_u32(s_ak), sb_v = smem_u32(s_v), sb_s16 = smem_u32(s_s16);
         constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
         constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, true, true);
+        constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
+        // intra-chunk part of chunk kp (extra CTA), issued one chunk late
+        auto issue_pv = [&](int kp) -> bool {
+            const int sp = kp & 1;
+            if (!mbar_wait(&p_ready, kp & 1, &abort_flag, kWaitNs)) return false;
+            tc_fence_after();
+            const uint32_t vb = smem_u32(v_buf(kp));
+            for (int ks = 0; ks < 8; ++ks)
+                mma_ts(tb + K::tx_y + 64 * sp, tb + K::tx_sc + 8 * ks, sdesc_mnmajor_sw128(vb + ks * 2048, kAtom), id_pv, 1u);
+            mma_commit(&y_full[sp]);
+            mma_commit(&v_free[sp]);
+            return true;
+        };
+        bool mok = true;
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
+            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
             tc_fence_after();
-            // ---- group U: state updates (and, extra CTA: Z update, intra scores)
+            const uint32_t sb_vk = smem_u32(v_buf(kk));
+            // ---- group U: state updates (extra CTA: tail state and Z)
             if (!extra) {
 #pragma unroll 1
                 for (int tl = 0; tl < K::TPC; ++tl)
                     for (int ks = 0; ks < 8; ++ks)
                         mma_ss(tb + K::tm_s + 64 * tl, sdesc_mnmajor_sw128(sb_ak + 2 * tl * kAtom + ks * 2048, kAtom),
-                               sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom), id_upd, 1u);
+                               sdesc_mnmajor_sw128(sb_vk + ks * 2048, kAtom), id_upd, 1u);
                 mma_commit(&upd_done);
                 mma_commit(&ak_free);
-                mma_commit(&v_free);
+                mma_commit(&v_free[0]);
             } else {
                 // tail tile: one 64-slot atom, the second M atom aliases it (rows past the tail are never read)
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb_ak + ks * 2048, 0), sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom),
+                    mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb_ak + ks * 2048, 0), sdesc_mnmajor_sw128(sb_vk + ks * 2048, kAtom),
                            id_upd, 1u);
                 const uint32_t sb_kh = smem_u32(s_kh), sb_q = smem_u32(s_q);
                 constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tb + K::tx_z, sdesc_mnmajor_sw128(sb_kh + ks * 2048, 0),
                            sdesc_mnmajor_sw128(sb_kh + ks * 2048, kAtom), id_z, 1u);
+                mma_commit(&upd_done);
+                mma_commit(&ak_free);
+                // previous chunk's intra part, then this chunk's scores (same tensor columns)
+                if (kk >= 1 && !issue_pv(kk - 1)) { fail(); mok = false; break; }
                 constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
                 for (int ks = 0; ks < P / 16; ++ks)
                     mma_ss(tb + K::tx_sc, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_kh + ks * 32), id_sc,
                            ks > 0 ? 1u : 0u);
-                mma_commit(&upd_done);
-                mma_commit(&ak_free);
+                mma_commit(&sc_done);
             }
             // ---- group R: readout of the state before this chunk
-            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
+            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
             tc_fence_after();
             if (!extra) {
 #pragma unroll 1
@@ -770,16 +858,9 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                            ks > 0 ? 1u : 0u);
                 mma_commit(&y_part[slot]);
                 mma_commit(&aq_free[slot]);
-                // ---- group PV: intra-chunk part
-                if (!mbar_wait(&p_ready, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
-                tc_fence_after();
-                constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tb + K::tx_y + 64 * slot, tb + K::tx_sc + 8 * ks, sdesc_mnmajor_sw128(sb_v + ks * 2048, kAtom), id_pv, 1u);
-                mma_commit(&y_full[slot]);
-                mma_commit(&v_free);
             }
         }
+        if (extra && mok && nk >= 1 && !issue_pv(nk - 1)) fail();
         // every issued MMA has completed before tensor memory is released
         mma_commit(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
@@ -798,7 +879,7 @@ template <int P, int DV>
 bool register_split_fits() {
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, chunked_tc_kernel<P, DV>) != cudaSuccess) return false;
-    return (uint32_t)kThreads * (uint32_t)fa.numRegs >= 128u * (2u * kRegsWork + kRegsMma);
+    return (uint32_t)kThreads * (uint32_t)fa.numRegs >= 128u * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma);
 }
 
 template <int P, int DV>
@@ -909,3 +990,4 @@ unsigned int chunked_tc_take_status() {
 }
 
 }  // namespace kata
+

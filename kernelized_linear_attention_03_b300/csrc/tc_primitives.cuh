@@ -147,6 +147,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
         : "memory");
 }
 
+__device__ __forceinline__ void st_async_v4_b32(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            cluster_addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float a, uint32_t cluster_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
                  "r"(__float_as_uint(a)), "r"(cluster_bar)
