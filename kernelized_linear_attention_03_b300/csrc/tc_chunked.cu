@@ -23,7 +23,11 @@
 // of those rows from every CTA of the cluster (double-buffered by chunk
 // parity), adds them, divides by d and stores o.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include <cstdint>
 
@@ -68,16 +72,18 @@ struct Cfg {
     //   extra CTA: tail key lift, Q, unit keys, bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
     static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 1) * kAtom,
                               t_stage = (3 * TPC + 1) * kAtom;
-    static constexpr uint32_t x_ak = 0, x_q = 1 * kAtom, x_kh = 2 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
-                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom, x_v2 = 8 * kAtom;  // extra: V slots x_v, x_v2
-    static constexpr uint32_t atoms = (3 * TPC + 3) > 9 ? (3 * TPC + 3) : 9;
+    static constexpr uint32_t x_ak = 0, x_kh = 1 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
+                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom, x_v2 = 10 * kAtom;  // extra: V slots x_v, x_v2,
+                                                                                           // unit-key slots x_kh, x_kh + 1
+    // query / key row staging: two stages of (Q tile, K tile), each filled by TMA
+    static constexpr uint32_t atoms = 11;
     // partial readouts: one part per (source CTA, receive slot) = R rows of bf16
     // laid out [DV/8][R] x 16 bytes (a warp's store of one column group is
     // contiguous per owner), then R fp32 denominators (extra CTA's part only)
     static constexpr uint32_t part_y = R * DV * 2;
     static constexpr uint32_t recv_part = part_y + round16(R * 4);
     static constexpr uint32_t recv_buf = CS * recv_part;
-    static constexpr int RS = 4;                        // receive slots (chunks in flight)
+    static constexpr int RS = 2;                        // receive slots (chunks in flight)
     static constexpr uint32_t recv_off = atoms * kAtom;
     static constexpr uint32_t total = recv_off + RS * recv_buf;
     static constexpr size_t smem = total + 1024;
@@ -95,6 +101,7 @@ struct Cfg {
     static_assert(NT % TPC == 0, "tiles must split evenly");
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(total + 1024 <= 232448, "shared memory");
+    static_assert(3 * TPC + 5 <= atoms, "tile CTA layout");
 };
 
 // ---------------------------------------------------------------- lifts per tile
@@ -280,8 +287,8 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 // read the state.
 template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ o,
+chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
                   float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV>;
@@ -290,8 +297,11 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], y_full[2], den_ready[2], v_free[2];
     __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
+    __shared__ uint64_t local_full[K::RS];  // this CTA's own partial rows written (one arrival per row)
     __shared__ float dens[2][kChunk];  // extra CTA: denominators of the chunk rows
-    __shared__ uint64_t ak_free, qk_free, upd_done, state_read, s16_ready, p_ready, sc_done, drain;
+    __shared__ uint64_t ak_free, upd_done, state_read, s16_ready, p_ready, sc_done, drain;
+    __shared__ uint64_t rd_sync;  // bounded group barrier of the reduce warps
+    __shared__ uint64_t stage_full[2], stage_free[2], v_full[2], kh_free[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -316,8 +326,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     auto v_buf = [&](int kk) { return (extra && (kk & 1)) ? sm + K::x_v2 : s_v; };
     uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
     uint8_t* const s_stage = sm + (extra ? K::x_stage : K::t_stage);
-    uint8_t* const s_q = sm + K::x_q;
-    uint8_t* const s_kh = sm + K::x_kh;
+    auto s_kh = [&](int kk) { return sm + K::x_kh + (kk & 1) * kAtom; };
     uint8_t* const s_z16 = sm + K::x_z16;
     uint8_t* const s_recv = sm + K::recv_off;
 
@@ -333,8 +342,16 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             mbar_init(&v_free[b], 1);
         }
         mbar_init(&sc_done, 1);
+        mbar_init(&rd_sync, 64);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&stage_full[b], 1);
+            // the staged rows are read by the lift warps and, in the extra CTA,
+            // also by the state warps (its Q operand lives there)
+            mbar_init(&stage_free[b], extra ? 256 : 128);
+            mbar_init(&kh_free[b], 1);
+            mbar_init(&v_full[b], 1);
+        }
         mbar_init(&ak_free, 1);
-        mbar_init(&qk_free, 128);
         mbar_init(&upd_done, 1);
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
@@ -344,6 +361,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         for (int b = 0; b < K::RS; ++b) {
             mbar_init(&recv_full[b], 1);
             mbar_init(&peer_free[b], K::CS);
+            mbar_init(&local_full[b], my_rows);
         }
         fence_mbar_init();
         // the first RS chunks' partial rows may arrive as soon as the cluster starts
@@ -363,6 +381,20 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     auto fail = [&]() {
         abort_flag = 1;
         atomicOr(&g_chunked_tc_status, kStatusTimeout);
+    };
+    // Bounded waits whose outcome is the same for every lane of the warp (the
+    // warp-collective tensor-memory instructions that follow need that).
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag, kWaitNs));
+    };
+    auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, &abort_flag, kWaitNs));
+    };
+    // Group barrier of 128 threads on an mbarrier (bounded, unlike bar.sync):
+    // every thread arrives, then waits for the phase of use number `n`.
+    auto group_sync = [&](uint64_t* bar, uint32_t n) {
+        mbar_arrive(bar);
+        return wait(bar, n & 1);
     };
 
     // ---- start state of this segment (epilogue warps: lane = slot / dim)
@@ -412,38 +444,12 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     if (warp < 4) {
         // =============================================================== lift warps
         regs_inc<kRegsLift>();
-        const __nv_bfloat16* qh = q + bh * (int64_t)T * P;
-        const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
-        const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
-        uint8_t* my_q = s_stage + t * 128;           // this token's staged rows (128-byte swizzled)
-        uint8_t* my_k = s_stage + kAtom + t * 128;
-        auto stage_qk = [&](int c) {
-            const int tok = c * kChunk + t;
-            const bool valid = tok < T;
-            const __nv_bfloat16* qs = valid ? qh + (int64_t)tok * P : qh;
-            const __nv_bfloat16* ks = valid ? kh + (int64_t)tok * P : kh;
-#pragma unroll
-            for (int i = 0; i < P / 8; ++i) {
-                cp_async16(my_q + ((i ^ (t & 7)) << 4), qs + 8 * i, valid ? 16u : 0u);
-                cp_async16(my_k + ((i ^ (t & 7)) << 4), ks + 8 * i, valid ? 16u : 0u);
-            }
-            cp_async_commit();
-        };
-        uint4 vraw[DV / 8];
-        auto load_v = [&](int c) {
-            const int tok = c * kChunk + t;
-            const bool valid = tok < T;
-#pragma unroll
-            for (int i = 0; i < DV / 8; ++i)
-                vraw[i] = valid ? __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)tok * DV) + i) : make_uint4(0, 0, 0, 0);
-        };
-        if (nk > 0) {
-            stage_qk(c0);
-            load_v(c0);
-        }
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            cp_async_wait<0>();
+            // this token's query and key rows (128-byte swizzled, staged by TMA)
+            if (!wait(&stage_full[slot], use & 1)) { fail(); break; }
+            const uint8_t* my_q = s_stage + slot * 2 * kAtom + t * 128;
+            const uint8_t* my_k = my_q + kAtom;
             uint32_t uq[P / 2];
             uint4 kraw[P / 8];
 #pragma unroll
@@ -455,7 +461,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 uq[4 * i + 3] = a.w;
                 kraw[i] = *reinterpret_cast<const uint4*>(my_k + ((i ^ (t & 7)) << 4));
             }
-            if (kk + 1 < nk) stage_qk(c0 + kk + 1);
+            mbar_arrive(&stage_free[slot]);
             // unit key
             uint32_t uk[P / 2];
             {
@@ -480,7 +486,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             }
             // query lift -> tensor memory slot (double-buffered: overlaps the
             // previous chunk's update)
-            if (kk >= 2 && !mbar_wait(&aq_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 2 && !wait(&aq_free[slot], (use - 1) & 1)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
 #pragma unroll
@@ -489,41 +495,25 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             } else {
                 query_tail<P>(uq, tm(K::tx_aq + 32 * slot));
             }
-            // value row (loaded during the previous chunk) -> its buffer
-            if (!extra) {
-                if (kk >= 1 && !mbar_wait(&v_free[0], (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            } else {
-                if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            }
-            {
-                uint8_t* vb = v_buf(kk);
-#pragma unroll
-                for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(vb + mn_sw128_chunk(8 * i, t, kAtom)) = vraw[i];
-            }
             // key lift -> shared memory (single buffer)
-            if (kk >= 1 && !mbar_wait(&ak_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 1 && !wait(&ak_free, (kk - 1) & 1)) { fail(); break; }
             if (!extra) {
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
                     key_dispatch<P>(rank * K::TPC + tl, uk, s_ak + 2 * tl * kAtom, t);
             } else {
                 key_tail<P>(uk, s_ak, t);
-                if (kk >= 1 && !mbar_wait(&qk_free, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                if (kk >= 2 && !wait(&kh_free[slot], (use - 1) & 1)) { fail(); break; }
 #pragma unroll
-                for (int i = 0; i < P / 8; ++i) {
-                    *reinterpret_cast<uint4*>(s_q + sw128_chunk(t, 8 * i, kChunk)) =
-                        make_uint4(uq[4 * i], uq[4 * i + 1], uq[4 * i + 2], uq[4 * i + 3]);
-                    *reinterpret_cast<uint4*>(s_kh + sw128_chunk(t, 8 * i, kChunk)) =
+                for (int i = 0; i < P / 8; ++i)
+                    *reinterpret_cast<uint4*>(s_kh(kk) + sw128_chunk(t, 8 * i, kChunk)) =
                         make_uint4(uk[4 * i], uk[4 * i + 1], uk[4 * i + 2], uk[4 * i + 3]);
-                }
             }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&lift_full[slot]);
-            if (kk + 1 < nk) load_v(c0 + kk + 1);
         }
-        cp_async_wait<0>();
     } else if (warp < 8) {
         // =============================================================== state warps
         regs_inc<kRegsState>();
@@ -532,7 +522,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         for (int kk = 0; kk < nk && ok; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
             // state after this chunk's update
-            if (!mbar_wait(&upd_done, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!wait(&upd_done, kk & 1)) { fail(); break; }
             tc_fence_after();
             uint32_t sreg[K::TPC][DV / 2];  // bf16 pairs of this lane's state rows
             uint32_t zreg[P / 2];           // extra CTA: bf16 pairs of this lane's Z row
@@ -572,43 +562,16 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 }
                 tc_fence_before();
                 mbar_arrive(&state_read);
-                // P = (Q Kh^T)^2 masked (s <= t), bf16, in place; its row sum
-                if (!mbar_wait(&sc_done, kk & 1, &abort_flag, kWaitNs)) { fail(); break; }
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sc[64];
-#pragma unroll
-                    for (int c16 = 0; c16 < 64; c16 += 16) tmem_ld16(tm(K::tx_sc + 64 * h + c16), *reinterpret_cast<uint32_t(*)[16]>(sc + c16));
-                    tmem_wait_ld();
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = 64 * h + 2 * i;
-                        float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
-                        a = col <= e ? a * a : 0.f;
-                        b = col + 1 <= e ? b * b : 0.f;
-                        pk[i] = pack_bf16x2(a, b);
-                        // the row sum of the rounded weights, so the intra-chunk
-                        // weights stay an exact convex combination
-                        const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
-                        den += __low2float(hp) + __high2float(hp);
-                    }
-                    tmem_st16(tm(K::tx_sc + 32 * h), *reinterpret_cast<uint32_t(*)[16]>(pk));
-                    tmem_st16(tm(K::tx_sc + 32 * h + 16), *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&p_ready);
             }
             // this chunk's readout is done: its bf16 state copy may be replaced
-            if (!mbar_wait(&y_part[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!wait(&y_part[slot], use & 1)) { fail(); break; }
             tc_fence_after();
             if (extra) {
                 // inter-chunk denominator q^T Z q from W = Q Z (Z before this chunk)
                 uint4 qrow[P / 8];
+                const uint8_t* sq = s_stage + slot * 2 * kAtom;  // this chunk's staged queries
 #pragma unroll
-                for (int i = 0; i < P / 8; ++i) qrow[i] = *reinterpret_cast<const uint4*>(s_q + sw128_chunk(e, 8 * i, kChunk));
+                for (int i = 0; i < P / 8; ++i) qrow[i] = *reinterpret_cast<const uint4*>(sq + sw128_chunk(e, 8 * i, kChunk));
                 const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(qrow);
                 float dint = 0.f;
 #pragma unroll
@@ -621,7 +584,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 }
                 den += dint;
                 tc_fence_before();
-                mbar_arrive(&qk_free);  // Q and W of this chunk have been read
+                mbar_arrive(&stage_free[slot]);  // this chunk's staged queries and W have been read
             }
             auto write_s16 = [&](const uint32_t (&x)[DV / 2], int tl) {
 #pragma unroll
@@ -679,69 +642,17 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         // =============================================================== readout warps
         const int e = t - 256;
         const int owner = e / K::R, orow = e % K::R;
-        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
-        // owner side: sum the partial rows of chunk c0 + kr, hand the receive
-        // slot back to every sender, then divide and store
-        auto reduce = [&](int kr) -> bool {
-            const int r = kr % K::RS;
-            if (!mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs)) return false;
-            const uint8_t* recv = s_recv + r * K::recv_buf;
-            const int r0 = rank * K::R;
-            const int items = my_rows * (DV / 8);
-            // 8-column groups of owned rows, at most MAXIT per lane
-            constexpr int MAXIT = (K::R * (DV / 8) + 127) / 128;
-            float acc[MAXIT][8];
-            float dd[MAXIT];
-#pragma unroll
-            for (int it = 0; it < MAXIT; ++it) {
-                const int idx = e + 128 * it;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[it][j] = 0.f;
-                dd[it] = 0.f;
-                if (idx < items) {
-                    const int lr = idx % my_rows, i = idx / my_rows;
-#pragma unroll
-                    for (int src = 0; src < K::CS; ++src) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
-                        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc[it][2 * j] += __low2float(h[j]);
-                            acc[it][2 * j + 1] += __high2float(h[j]);
-                        }
-                    }
-                    dd[it] = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
-                }
-            }
-            named_sync(1, 128);
-            if (e == 0 && kr + K::RS < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
-            if (e < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], e));
-#pragma unroll
-            for (int it = 0; it < MAXIT; ++it) {
-                const int idx = e + 128 * it;
-                if (idx < items) {
-                    const int lr = idx % my_rows, i = idx / my_rows;
-                    const float inv = dd[it] > 0.f ? 1.f / dd[it] : 0.f;
-                    const int otok = (c0 + kr) * kChunk + r0 + lr;
-                    if (otok < T)
-                        *reinterpret_cast<uint4*>(oh + (int64_t)otok * DV + 8 * i) = make_uint4(
-                            pack_bf16x2(acc[it][0] * inv, acc[it][1] * inv), pack_bf16x2(acc[it][2] * inv, acc[it][3] * inv),
-                            pack_bf16x2(acc[it][4] * inv, acc[it][5] * inv), pack_bf16x2(acc[it][6] * inv, acc[it][7] * inv));
-                }
-            }
-            return true;
-        };
-        bool ok = true;
-        for (int kk = 0; kk < nk && ok; ++kk) {
-            const int slot = kk & 1, use = kk >> 1;
-            const int rs = kk % K::RS, ruse = kk / K::RS;
-            // partial readout of this lane's row -> its owner
-            if (!mbar_wait(extra ? &y_full[slot] : &y_part[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+        // this lane's partial readout of chunk c0 + kc -> its owner (den: the
+        // denominator of the row, extra CTA only)
+        auto send = [&](int kc, float den_intra) -> bool {
+            const int slot = kc & 1, use = kc >> 1;
+            const int rs = kc % K::RS, ruse = kc / K::RS;
+            if (!wait(extra ? &y_full[slot] : &y_part[slot], use & 1)) return false;
             tc_fence_after();
-            float den = 0.f;
+            float den = den_intra;
             if (extra) {
-                if (!mbar_wait(&den_ready[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
-                den = dens[slot][e];
+                if (!wait(&den_ready[slot], use & 1)) return false;
+                den += dens[slot][e];
             }
             uint32_t ypk[DV / 2];
             const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
@@ -756,7 +667,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             tc_fence_before();
             mbar_arrive(&y_free[slot]);
             // the owners have consumed what this receive slot held RS chunks ago
-            if (kk >= K::RS && !mbar_wait_cluster(&peer_free[rs], (ruse - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kc >= K::RS && !wait_cluster(&peer_free[rs], (ruse - 1) & 1)) return false;
             uint8_t* recv = s_recv + rs * K::recv_buf;
             uint8_t* dst = recv + rank * K::recv_part + orow * 16;
             if (owner == rank) {
@@ -764,6 +675,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 for (int i = 0; i < DV / 8; ++i)
                     *reinterpret_cast<uint4*>(dst + i * K::R * 16) = make_uint4(ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3]);
                 if (extra) *reinterpret_cast<float*>(recv + rank * K::recv_part + K::part_y + orow * 4) = den;
+                mbar_arrive(&local_full[rs]);
             } else {
                 const uint32_t rdst = cluster_addr(dst, owner);
                 const uint32_t rbar = cluster_addr(&recv_full[rs], owner);
@@ -772,13 +684,120 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                     st_async_v4_b32(rdst + i * K::R * 16, ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3], rbar);
                 if (extra) st_async_f32(cluster_addr(recv + rank * K::recv_part + K::part_y + orow * 4, owner), den, rbar);
             }
-            // owned rows two chunks back
-            if (kk >= 2 && !reduce(kk - 2)) { fail(); ok = false; }
+            return true;
+        };
+        if (!extra) {
+            for (int kk = 0; kk < nk; ++kk)
+                if (!send(kk, 0.f)) { fail(); break; }
+        } else {
+            // extra CTA: P = (Q Kh^T)^2 masked (s <= t) of chunk kk, bf16 in place,
+            // and its row sum; then the previous chunk's partial readout
+            float den_prev = 0.f;
+            for (int kk = 0; kk <= nk; ++kk) {
+                float den_cur = 0.f;
+                if (kk < nk) {
+                    if (!wait(&sc_done, kk & 1)) { fail(); break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t sc[32], pk[16];
+                        tmem_ld16(tm(K::tx_sc + 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                        tmem_ld16(tm(K::tx_sc + 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int col = 32 * q4 + 2 * i;
+                            float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
+                            a = col <= e ? a * a : 0.f;
+                            b = col + 1 <= e ? b * b : 0.f;
+                            pk[i] = pack_bf16x2(a, b);
+                            // the row sum of the rounded weights keeps the
+                            // intra-chunk weights an exact convex combination
+                            const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+                            den_cur += __low2float(hp) + __high2float(hp);
+                        }
+                        tmem_st16(tm(K::tx_sc + 16 * q4), pk);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&p_ready);
+                }
+                if (kk >= 1 && !send(kk - 1, den_prev)) { fail(); break; }
+                den_prev = den_cur;
+            }
         }
-        for (int kr = nk >= 2 ? nk - 2 : 0; kr < nk && ok && !abort_flag; ++kr)
-            if (!reduce(kr)) fail();
     } else {
         regs_dec<kRegsMma>();
+    }
+    if (warp >= 14) {
+        // =============================================================== reduce warps
+        // owner side, chunk by chunk as the partial rows land: sum them, divide
+        // by the denominator, store o, then hand the receive slot back to every
+        // sender (its next use is RS chunks later)
+        const int er = t - 448;
+        const int r0 = rank * K::R;
+        const int items = my_rows * (DV / 8);
+        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
+        for (int kr = 0; kr < nk; ++kr) {
+            const int r = kr % K::RS;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs) &&
+                                             mbar_wait(&local_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs))) {
+                fail();
+                break;
+            }
+            const uint8_t* recv = s_recv + r * K::recv_buf;
+            for (int idx = er; idx < items; idx += 64) {
+                const int lr = idx % my_rows, i = idx / my_rows;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int src = 0; src < K::CS; ++src) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[2 * j] += __low2float(h[j]);
+                        acc[2 * j + 1] += __high2float(h[j]);
+                    }
+                }
+                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
+                const float inv = d > 0.f ? 1.f / d : 0.f;
+                const int otok = (c0 + kr) * kChunk + r0 + lr;
+                if (otok < T)
+                    *reinterpret_cast<uint4*>(oh + (int64_t)otok * DV + 8 * i) =
+                        make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                                   pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+            }
+            mbar_arrive(&rd_sync);
+            if (!__all_sync(0xffffffffu, mbar_wait(&rd_sync, kr & 1, &abort_flag, kWaitNs))) {
+                fail();
+                break;
+            }
+            if (er == 0 && kr + K::RS < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
+            if (er < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], er));
+        }
+    }
+    if (t == 416) {
+        // =============================================================== TMA producer
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        for (int kk = 0; kk < nk; ++kk) {
+            const int slot = kk & 1, use = kk >> 1;
+            const int row = (c0 + kk) * kChunk;
+            // query and key rows of chunk kk into staging slot kk % 2
+            if (kk >= 2 && !mbar_wait(&stage_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&stage_full[slot], 2 * kAtom);
+            tma_load_3d(s_stage + slot * 2 * kAtom, &tmq, 0, row, (int)bh, &stage_full[slot]);
+            tma_load_3d(s_stage + slot * 2 * kAtom + kAtom, &tmk, 0, row, (int)bh, &stage_full[slot]);
+            // value tile of chunk kk into its buffer (tile CTA: one; extra CTA: two)
+            const int vs = extra ? slot : 0;
+            if (extra ? kk >= 2 : kk >= 1) {
+                const uint32_t par = extra ? ((use - 1) & 1) : ((kk - 1) & 1);
+                if (!mbar_wait(&v_free[vs], par, &abort_flag, kWaitNs)) { fail(); break; }
+            }
+            mbar_arrive_expect_tx(&v_full[vs], kAtom);
+            tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[vs]);
+        }
     }
     if (t == 384) {
         // =============================================================== MMA issuer
@@ -802,6 +821,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
             if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
+            if (!mbar_wait(&v_full[extra ? slot : 0], extra ? (use & 1) : (kk & 1), &abort_flag, kWaitNs)) { fail(); mok = false; break; }
             if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
             tc_fence_after();
             const uint32_t sb_vk = smem_u32(v_buf(kk));
@@ -820,7 +840,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb_ak + ks * 2048, 0), sdesc_mnmajor_sw128(sb_vk + ks * 2048, kAtom),
                            id_upd, 1u);
-                const uint32_t sb_kh = smem_u32(s_kh), sb_q = smem_u32(s_q);
+                const uint32_t sb_kh = smem_u32(s_kh(kk)), sb_q = smem_u32(s_stage + slot * 2 * kAtom);
                 constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tb + K::tx_z, sdesc_mnmajor_sw128(sb_kh + ks * 2048, 0),
@@ -834,6 +854,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                     mma_ss(tb + K::tx_sc, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_kh + ks * 32), id_sc,
                            ks > 0 ? 1u : 0u);
                 mma_commit(&sc_done);
+                mma_commit(&kh_free[slot]);
             }
             // ---- group R: readout of the state before this chunk
             if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
@@ -851,7 +872,7 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
                     mma_ts(tb + K::tx_y + 64 * slot, tb + K::tx_aq + 32 * slot + 8 * ks,
                            sdesc_mnmajor_sw128(sb_s16 + ks * 2048, kAtom), id_read, ks > 0 ? 1u : 0u);
-                const uint32_t sb_q = smem_u32(s_q), sb_z16 = smem_u32(s_z16);
+                const uint32_t sb_q = smem_u32(s_stage + slot * 2 * kAtom), sb_z16 = smem_u32(s_z16);
                 constexpr uint32_t id_w = idesc_bf16_f32(128, P);
                 for (int ks = 0; ks < P / 16; ++ks)
                     mma_ss(tb + K::tx_w, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_z16 + ks * 32), id_w,
@@ -874,6 +895,38 @@ chunked_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 }
 
 // ---------------------------------------------------------------- host side
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess && qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of a bf16 [BH][T][cols] array read as 128-row x 64-column boxes
+// (128-byte rows, 128-byte swizzle: the layout the kernel's operand tiles
+// use; columns past `cols` and rows past T are filled with zeros).
+bool rows_map(CUtensorMap* m, const void* base, int cols, int T, int BH) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)T * cols * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kChunk, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The register split of the kernel fits in its launch allocation.
 template <int P, int DV>
 bool register_split_fits() {
@@ -931,11 +984,12 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, c
     cudaLaunchAttribute attr[1];
     cudaError_t e = configure<P, DV>(cfg, attr, G, BH, s);
     if (e != cudaSuccess) return e;
+    CUtensorMap tq, tk, tv;
+    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
+        return cudaErrorInvalidValue;
     KATA_TRACED("chunked_tc", s,
-                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, static_cast<const __nv_bfloat16*>(q),
-                                       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-                                       static_cast<__nv_bfloat16*>(o), S_start, z_start, start_groups, S_final,
-                                       z_final, T, seg_chunks));
+                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tk, tv, static_cast<__nv_bfloat16*>(o),
+                                       S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -60,6 +60,24 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_test, but the thread may sleep in hardware (issuing nothing) for up
+// to `hint_ns` while the phase is still open.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Per-try sleep of the bounded waits: long enough that waiting warps leave
+// the issue slots to working warps, short against the overall budget.
+constexpr uint32_t kSleepHintNs = 20000;
+
 // Wait for the phase with the given parity to complete, for at most
 // `budget_ns` of wall time; also gives up as soon as *abort is non-zero.
 // Returns true when the phase completed.
@@ -68,7 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_test(bar, parity)) return true;
+        if (mbar_test_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
     }
@@ -98,13 +116,25 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_cluster_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                   uint64_t budget_ns) {
     if (*abort) return false;
     if (mbar_test_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_test_cluster(bar, parity)) return true;
+        if (mbar_test_cluster_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
     }
@@ -184,6 +214,20 @@ template <uint32_t N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// TMA: 3-D tiled tensor load (coordinates innermost first) into this CTA's
+// shared memory; the barrier counts the box bytes when they land.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
 
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
