@@ -61,7 +61,7 @@ def flops_forward(w):
     return w.B * w.H * w.T * (4 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
 
 
-def kernel_work(name, w):
+def kernel_work(name, w, form="chunked"):
     """(kind, algorithmic amount per forward call) of a library kernel."""
     bht = w.B * w.H * w.T
     if name in ("chunk_states_simt",):
@@ -70,6 +70,11 @@ def kernel_work(name, w):
         return "flop", bht * (2 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
     if name in ("scan_tree", "scan_sequential"):
         return "byte", 2 * w.B * w.H * w.NC * w.n * (w.dv + 1) * 4
+    if name == "quadratic_tc" or name == "quadratic_simt":
+        # causal half of the flash-style form: (T+1)(p+dv) per head-token
+        return "flop", bht * (w.T + 1) * (w.p + w.dv)
+    if name == "states_tc" and form == "chunk_state_scan":
+        return "flop", bht * 2 * w.n * (w.dv + 1)
     if name == "chunked_tc":
         # the fused forward does all of the forward's algorithmic work
         return "flop", flops_forward(w)
@@ -259,8 +264,26 @@ def run_ours(args, world, rank, local):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        kb.kata_forward_chunked(q, k, v, w.C, mode, o=o, workspace=ws, stream=stream)
+    if args.form == "chunked":
+        def step():
+            kb.kata_forward_chunked(q, k, v, w.C, mode, o=o, workspace=ws, stream=stream)
+    elif args.form == "quadratic":
+        def step():
+            kb.kata_forward_quadratic(q, k, v, o=o, C=w.C, stream=stream)
+    elif args.form == "chunk_state_scan":
+        Sp = torch.empty((w.B, w.H, w.NC, w.n, w.dv), dtype=torch.float32, device=dev)
+        zp = torch.empty((w.B, w.H, w.NC, w.n), dtype=torch.float32, device=dev)
+
+        def step():
+            kb.kata_chunk_state_scan(k, v, w.C, mode, S_prefix=Sp, z_prefix=zp, stream=stream)
+    else:  # scan of given chunk states
+        g = torch.Generator(device=dev).manual_seed(rank)
+        S_loc = torch.randn((w.B, w.H, w.NC, w.n, w.dv), generator=g, device=dev)
+        z_loc = torch.rand((w.B, w.H, w.NC, w.n), generator=g, device=dev)
+        Sp, zp = torch.empty_like(S_loc), torch.empty_like(z_loc)
+
+        def step():
+            kb.kata_scan_states(S_loc, z_loc, mode, S_prefix=Sp, z_prefix=zp, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -295,7 +318,7 @@ def run_ours(args, world, rank, local):
     for name, t in trace:
         per.setdefault(name, []).append(t)
     dom = max(per, key=lambda n: sum(per[n]))
-    kind, amount = kernel_work(dom, w)
+    kind, amount = kernel_work(dom, w, args.form)
     calls_per_step = len(per[dom]) / args.steps
     dom_ms_per_call = sum(per[dom]) / args.steps  # all launches of it in one forward
     if kind == "flop":
@@ -317,6 +340,17 @@ def run_ours(args, world, rank, local):
     kernels = {n: {"launches": len(t), "ms_total": sum(t), "share": sum(t) / max(1e-9, sum(x for _, x in trace))}
                for n, t in per.items()}
     alg_tflops = flops_forward(w) / (ms / 1e3) / 1e12
+
+    if args.form != "chunked":
+        if rank == 0:
+            line = {"metric": f"KATA {args.form} {w.name}: tokens/s (1 B300)", "value": value, "unit": "tokens/s",
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                    "higher_is_better": True, "form": args.form, "roofline": roof, "kernels": kernels,
+                    "gpu_launches": len(trace), "clocks": clocks.summary(wall0, wall1),
+                    "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "p": w.p, "dv": w.dv, "C": w.C,
+                               "n": w.n, "scan_mode": args.scan}}
+            print(json.dumps(line), flush=True)
+        return
 
     # end to end through the C ABI with host buffers
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
@@ -381,6 +415,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per call of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--form", default="chunked", choices=["chunked", "quadratic", "scan", "chunk_state_scan"],
+                    help="entry point timed (the contract's line is the chunked forward)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
