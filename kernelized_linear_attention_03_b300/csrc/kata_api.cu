@@ -79,12 +79,14 @@ size_t elem_bytes(kata_dtype dt) { return dt == KATA_FP32 ? 4 : 2; }
 // [BH, NC, n] in fp32, each 256-byte aligned.
 struct ChunkedWs {
     size_t s_off, z_off, total;
+    size_t i_off;  // tensor-core path: intra-chunk rows
 };
 
 ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C) {
     const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C, n = packed(p);
     ChunkedWs w;
     w.s_off = 0;
+    w.i_off = 0;
     w.z_off = round_up(sizeof(float) * (size_t)(BH * NC * n * dv), 256);
     w.total = w.z_off + round_up(sizeof(float) * (size_t)(BH * NC * n), 256);
     return w;
@@ -96,7 +98,7 @@ ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C) {
 struct TcPlan {
     bool use = false;
     int G = 1;
-    ChunkedWs ws{0, 0, 0};
+    ChunkedWs ws{0, 0, 0, 0};
 };
 
 TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
@@ -107,11 +109,14 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
     if (G <= 0) return pl;
     pl.use = true;
     pl.G = G;
+    size_t off = 0;
     if (G > 1) {
         pl.ws.s_off = 0;
         pl.ws.z_off = round_up(sizeof(float) * (size_t)(BH * G * n * dv), 256);
-        pl.ws.total = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * G * n), 256);
+        off = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * G * n), 256);
     }
+    pl.ws.i_off = off;
+    pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, dv), 256);
     return pl;
 }
 
@@ -193,9 +198,10 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
     }
     if (pl.use) {
+        void* intra = static_cast<char*>(ws) + w.i_off;
         if (pl.G == 1)
-            return cuda_status(kata::launch_chunked_tc(q, k, v, o, S0, z0, 1, S_final, z_final, (int)BH, T, p,
-                                                       dv, 1, stream));
+            return cuda_status(kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, S_final, z_final, (int)BH, T,
+                                                       p, dv, 1, stream));
         // segment totals of segments 0..G-2, then exclusive prefixes seeded
         // with the initial state: the start state of every segment
         const int G = pl.G, n32 = (int)n;
@@ -212,7 +218,8 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
         if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
         if (e == cudaSuccess)
-            e = kata::launch_chunked_tc(q, k, v, o, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, G, stream);
+            e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, G,
+                                        stream);
         return cuda_status(e);
     }
 

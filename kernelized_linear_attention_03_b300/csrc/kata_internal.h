@@ -33,11 +33,14 @@ unsigned int states_tc_take_status();
 // cannot be scheduled there); chunked_tc_segment_chunks() the 128-token
 // chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
 // start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
+// `intra` is chunked_tc_intra_bytes() of device scratch (16-byte aligned)
+// for the intra-chunk rows a first kernel computes for every chunk at once.
 int chunked_tc_segments(int p, int dv, int BH, int T);
 int chunked_tc_segment_chunks(int T, int G);
-cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, const float* S_start,
-                              const float* z_start, int start_groups, float* S_final, float* z_final, int BH,
-                              int T, int p, int dv, int G, cudaStream_t s);
+size_t chunked_tc_intra_bytes(int BH, int T, int dv);
+cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
+                              const float* S_start, const float* z_start, int start_groups, float* S_final,
+                              float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s);
 unsigned int chunked_tc_take_status();
 
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).

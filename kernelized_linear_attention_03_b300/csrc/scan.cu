@@ -3,11 +3,10 @@
 // prefix over the chunk axis can be taken
 //   * sequentially: one thread per 4 state elements walks the N_C chunks
 //     (depth N_C, every element's walk independent), or
-//   * as a log-depth scan: a block stages an [N_C x 16] slab of one head's
-//     state in shared memory and runs ceil(log2 N_C) rounds in which every
-//     chunk adds the chunk 2^d before it (N_C-wide work per round), then
-//     writes the exclusive prefix.  Chunk counts above the slab window are
-//     walked window by window with a carry.
+//   * as a log-depth tree: per 16-byte column vector, a work-efficient
+//     up-sweep / down-sweep over runs of 8 chunks held in registers around
+//     a Kogge-Stone scan of the run totals in shared memory.  Chunk counts
+//     above the 1024-chunk window continue window by window from a carry.
 // Both read every element once and write it once: the pass is HBM-bound.
 #include <cstdint>
 
@@ -72,54 +71,98 @@ scan_sequential_kernel(const float* x, float* y, const float* init, float* fin, 
     if (fin) *reinterpret_cast<T*>(fin + h * W + e) = run;
 }
 
-constexpr int kTreeThreads = 256;
-constexpr int kTreeE = 16;       // state elements per slab column group
-constexpr int kTreeWin = 1024;   // chunks per shared-memory window
-constexpr int kTreePer = kTreeWin * kTreeE / kTreeThreads;
+// Log-depth scan.  A block owns a tile of kTreeTPR x VEC state columns of
+// one head and a window of GROUPS x kTreeCPT consecutive chunks; thread
+// (g, cc) holds the kTreeCPT chunks 8g..8g+7 of column group cc in registers.
+//   1. up-sweep inside the thread: pairwise partial sums, 3 levels;
+//   2. inclusive Kogge-Stone over the GROUPS group totals in shared memory,
+//      log2(GROUPS) rounds, each GROUPS-wide;
+//   3. down-sweep inside the thread, giving each chunk its exclusive prefix
+//      within the group, then the group's offset is added.
+// Depth 3 + log2(GROUPS) + 3 = log2(window) + 3.  Windows beyond the first
+// (N_C above 1024) continue from a carry.  Loads and stores are full 16-byte
+// vectors along the columns, all kTreeCPT of a thread in flight at once.
+constexpr int kTreeTPR = 4;  // threads across a tile row
+constexpr int kTreeCPT = 8;  // chunks per thread
 
-// Block = (element group g of head h).  Slab sx[c][e] for the current window.
-__global__ void __launch_bounds__(kTreeThreads)
+template <int VEC, int GROUPS>
+__global__ void __launch_bounds__(GROUPS * kTreeTPR)
 scan_tree_kernel(const float* x, float* y, const float* init, float* fin, int64_t NC, int64_t W,
-                 int64_t groups) {
-    extern __shared__ float sx[];  // [kTreeWin][kTreeE]
-    __shared__ float carry[kTreeE];
-    const int64_t h = blockIdx.x / groups, g = blockIdx.x - h * groups;
-    const int64_t e0 = g * kTreeE;
-    const int tid = threadIdx.x;
-    if (tid < kTreeE) carry[tid] = (init && e0 + tid < W) ? init[h * W + e0 + tid] : 0.f;
-    for (int64_t w0 = 0; w0 < NC; w0 += kTreeWin) {
-        const int len = (int)((NC - w0) < kTreeWin ? (NC - w0) : kTreeWin);
-        __syncthreads();
-        for (int idx = tid; idx < len * kTreeE; idx += kTreeThreads) {
-            const int c = idx / kTreeE, e = idx - c * kTreeE;
-            sx[idx] = (e0 + e < W) ? x[(h * NC + w0 + c) * W + e0 + e] : 0.f;
-        }
-        __syncthreads();
-        for (int d = 1; d < len; d <<= 1) {
-            float tmp[kTreePer];
+                 int64_t tiles) {
+    using V = Vec<VEC>;
+    using T = typename V::T;
+    constexpr int kWin = GROUPS * kTreeCPT;
+    __shared__ T part[2][GROUPS][kTreeTPR];
+    const int64_t h = blockIdx.x / tiles, tile = blockIdx.x - h * tiles;
+    const int g = threadIdx.x / kTreeTPR, cc = threadIdx.x % kTreeTPR;
+    const int64_t e = (tile * kTreeTPR + cc) * VEC;
+    const bool col_ok = e < W;  // VEC = 4 only when W % 4 == 0
+    T carry = (init && col_ok) ? *reinterpret_cast<const T*>(init + h * W + e) : V::zero();
+    const float* src = x + h * NC * W + e;
+    float* dst = y + h * NC * W + e;
+    for (int64_t w0 = 0; w0 < NC; w0 += kWin) {
+        const int64_t c0 = w0 + (int64_t)g * kTreeCPT;
+        T a[kTreeCPT];
 #pragma unroll
-            for (int m = 0; m < kTreePer; ++m) {
-                const int idx = tid + m * kTreeThreads;
-                tmp[m] = (idx < len * kTreeE && idx / kTreeE >= d) ? sx[idx - d * kTreeE] : 0.f;
-            }
-            __syncthreads();
+        for (int m = 0; m < kTreeCPT; ++m)
+            a[m] = (col_ok && c0 + m < NC) ? *reinterpret_cast<const T*>(src + (c0 + m) * W) : V::zero();
+        // up-sweep
 #pragma unroll
-            for (int m = 0; m < kTreePer; ++m) {
-                const int idx = tid + m * kTreeThreads;
-                if (idx < len * kTreeE) sx[idx] += tmp[m];
-            }
+        for (int st = 1; st < kTreeCPT; st <<= 1)
+#pragma unroll
+            for (int i = 2 * st - 1; i < kTreeCPT; i += 2 * st) a[i] = V::add(a[i - st], a[i]);
+        // group totals
+        int buf = 0;
+        part[0][g][cc] = a[kTreeCPT - 1];
+        __syncthreads();
+#pragma unroll
+        for (int d = 1; d < GROUPS; d <<= 1) {
+            T v = part[buf][g][cc];
+            if (g >= d) v = V::add(part[buf][g - d][cc], v);
+            part[buf ^ 1][g][cc] = v;
+            buf ^= 1;
             __syncthreads();
         }
-        for (int idx = tid; idx < len * kTreeE; idx += kTreeThreads) {
-            const int c = idx / kTreeE, e = idx - c * kTreeE;
-            if (e0 + e < W) y[(h * NC + w0 + c) * W + e0 + e] = carry[e] + (c > 0 ? sx[idx - kTreeE] : 0.f);
-        }
-        __syncthreads();
-        if (tid < kTreeE) carry[tid] += sx[(len - 1) * kTreeE + tid];
+        const T offset = V::add(carry, g > 0 ? part[buf][g - 1][cc] : V::zero());
+        const T wtotal = part[buf][GROUPS - 1][cc];
+        // down-sweep: exclusive prefixes within the thread
+        a[kTreeCPT - 1] = V::zero();
+#pragma unroll
+        for (int st = kTreeCPT / 2; st >= 1; st >>= 1)
+#pragma unroll
+            for (int i = 2 * st - 1; i < kTreeCPT; i += 2 * st) {
+                const T left = a[i - st];
+                a[i - st] = a[i];
+                a[i] = V::add(a[i], left);
+            }
+#pragma unroll
+        for (int m = 0; m < kTreeCPT; ++m)
+            if (col_ok && c0 + m < NC) *reinterpret_cast<T*>(dst + (c0 + m) * W) = V::add(offset, a[m]);
+        carry = V::add(carry, wtotal);
+        __syncthreads();  // part[] is rewritten by the next window
     }
-    __syncthreads();
-    if (fin && tid < kTreeE && e0 + tid < W) fin[h * W + e0 + tid] = carry[tid];
+    if (fin && col_ok) *reinterpret_cast<T*>(fin + h * W + e) = carry;
 }
+
+template <int VEC, int GROUPS>
+cudaError_t launch_tree(const float* x, float* y, const float* init, float* fin, int64_t heads, int64_t NC,
+                        int64_t W, cudaStream_t s) {
+    const int64_t tiles = (W + kTreeTPR * VEC - 1) / (kTreeTPR * VEC);
+    KATA_TRACED("scan_tree", s,
+                (scan_tree_kernel<VEC, GROUPS><<<(unsigned)(heads * tiles), GROUPS * kTreeTPR, 0, s>>>(
+                    x, y, init, fin, NC, W, tiles)));
+    return cudaGetLastError();
+}
+
+template <int VEC>
+cudaError_t launch_tree_vec(const float* x, float* y, const float* init, float* fin, int64_t heads, int64_t NC,
+                            int64_t W, cudaStream_t s) {
+    if (NC <= 8 * kTreeCPT) return launch_tree<VEC, 8>(x, y, init, fin, heads, NC, W, s);
+    if (NC <= 32 * kTreeCPT) return launch_tree<VEC, 32>(x, y, init, fin, heads, NC, W, s);
+    return launch_tree<VEC, 128>(x, y, init, fin, heads, NC, W, s);
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 __global__ void copy_or_zero_kernel(const float* src, float* dst, int64_t count) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -145,15 +188,9 @@ cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, f
                                                                                           heads, NC, W));
         return cudaGetLastError();
     }
-    const size_t smem = sizeof(float) * kTreeWin * kTreeE;
-    cudaError_t e = cudaFuncSetAttribute(scan_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    const int64_t groups = (W + kTreeE - 1) / kTreeE;
-    KATA_TRACED("scan_tree", s,
-                scan_tree_kernel<<<(unsigned)(heads * groups), kTreeThreads, smem, s>>>(x, y, init, fin, NC, W,
-                                                                                         groups));
-    return cudaGetLastError();
+    const bool vec4 = W % 4 == 0 && aligned16(x) && aligned16(y) && aligned16(init) && aligned16(fin);
+    if (vec4) return launch_tree_vec<4>(x, y, init, fin, heads, NC, W, s);
+    return launch_tree_vec<1>(x, y, init, fin, heads, NC, W, s);
 }
 
 cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s) {

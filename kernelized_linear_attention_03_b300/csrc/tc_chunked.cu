@@ -68,14 +68,16 @@ struct Cfg {
     static constexpr int CS = NTC + 1;                 // cluster size
     static constexpr int R = (kChunk + CS - 1) / CS;   // output rows owned per CTA
     // shared memory, in 16 KB atoms from a 1024-byte aligned base
-    //   tile CTA : key lift [0, 2 TPC), V, bf16 state [TPC], query/key staging [2]
-    //   extra CTA: tail key lift, Q, unit keys, bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
+    //   tile CTA : key lift [0, 2 TPC), V (slot 0), bf16 state [TPC], query/key staging, V (slot 1)
+    //   extra CTA: tail key lift, unit keys [2], bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
     static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 1) * kAtom,
-                              t_stage = (3 * TPC + 1) * kAtom;
+                              t_stage = (3 * TPC + 1) * kAtom, t_v2 = (3 * TPC + 3) * kAtom;
     static constexpr uint32_t x_ak = 0, x_kh = 1 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
                               x_s16 = 5 * kAtom, x_stage = 6 * kAtom, x_v2 = 10 * kAtom;  // extra: V slots x_v, x_v2,
                                                                                            // unit-key slots x_kh, x_kh + 1
-    // query / key row staging: two stages of (Q tile, K tile), each filled by TMA
+    // query / key row staging, (Q tile, K tile) per stage, filled by TMA: one
+    // stage in a tile CTA (its lift warps copy the rows out at once), two in
+    // the extra CTA (its MMAs read the queries in place)
     static constexpr uint32_t atoms = 11;
     // partial readouts: one part per (source CTA, receive slot) = R rows of bf16
     // laid out [DV/8][R] x 16 bytes (a warp's store of one column group is
@@ -95,13 +97,12 @@ struct Cfg {
     static constexpr uint32_t tx_s = 0;      // tail state
     static constexpr uint32_t tx_aq = 64;    // 2 slots x 32: tail query lift
     static constexpr uint32_t tx_y = 128;    // 2 slots x 64: partial readout
-    static constexpr uint32_t tx_sc = 256;   // 128: intra scores, P in place
     static constexpr uint32_t tx_w = 384;    // Q Z
     static constexpr uint32_t tx_z = 448;    // Z
     static_assert(NT % TPC == 0, "tiles must split evenly");
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(total + 1024 <= 232448, "shared memory");
-    static_assert(3 * TPC + 5 <= atoms, "tile CTA layout");
+    static_assert(3 * TPC + 4 <= atoms, "tile CTA layout");
 };
 
 // ---------------------------------------------------------------- lifts per tile
@@ -289,17 +290,18 @@ template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
+                  const __nv_bfloat16* __restrict__ y_intra, const float* __restrict__ d_intra,
                   const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
                   float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV>;
     constexpr int n = K::n;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], y_full[2], den_ready[2], v_free[2];
+    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], den_ready[2], v_free[2];
     __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
     __shared__ uint64_t local_full[K::RS];  // this CTA's own partial rows written (one arrival per row)
     __shared__ float dens[2][kChunk];  // extra CTA: denominators of the chunk rows
-    __shared__ uint64_t ak_free, upd_done, state_read, s16_ready, p_ready, sc_done, drain;
+    __shared__ uint64_t ak_free, upd_done, state_read, s16_ready, drain;
     __shared__ uint64_t rd_sync;  // bounded group barrier of the reduce warps
     __shared__ uint64_t stage_full[2], stage_free[2], v_full[2], kh_free[2];
     __shared__ uint32_t tmem_base;
@@ -320,10 +322,11 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + (extra ? 0 : my_rows * 4);
     // shared memory of this CTA's role
     uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
-    uint8_t* const s_v = sm + (extra ? K::x_v : K::t_v);
-    // value buffer of chunk kk: the extra CTA keeps two (its intra-chunk MMA
-    // reads V one chunk later), a tile CTA one
-    auto v_buf = [&](int kk) { return (extra && (kk & 1)) ? sm + K::x_v2 : s_v; };
+    // value buffer of chunk kk (two, so the next chunk's values load while the
+    // update, or in the extra CTA the one-chunk-late intra part, reads these)
+    auto v_buf = [&](int kk) { return sm + ((kk & 1) ? (extra ? K::x_v2 : K::t_v2) : (extra ? K::x_v : K::t_v)); };
+    // staging stages and the stage of chunk kk
+    const int nstg = extra ? 2 : 1;
     uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
     uint8_t* const s_stage = sm + (extra ? K::x_stage : K::t_stage);
     auto s_kh = [&](int kk) { return sm + K::x_kh + (kk & 1) * kAtom; };
@@ -336,12 +339,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             mbar_init(&aq_free[b], 1);
             mbar_init(&y_part[b], 1);
             mbar_init(&y_free[b], 128);
-            mbar_init(&y_full[b], 1);
 
             mbar_init(&den_ready[b], 128);
             mbar_init(&v_free[b], 1);
         }
-        mbar_init(&sc_done, 1);
         mbar_init(&rd_sync, 64);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&stage_full[b], 1);
@@ -355,7 +356,6 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         mbar_init(&upd_done, 1);
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
-        mbar_init(&p_ready, 128);
         mbar_init(&drain, 1);
         fence_mbar_init();
         for (int b = 0; b < K::RS; ++b) {
@@ -446,9 +446,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         regs_inc<kRegsLift>();
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
+            const int stg = kk % nstg, stg_use = kk / nstg;
             // this token's query and key rows (128-byte swizzled, staged by TMA)
-            if (!wait(&stage_full[slot], use & 1)) { fail(); break; }
-            const uint8_t* my_q = s_stage + slot * 2 * kAtom + t * 128;
+            if (!wait(&stage_full[stg], stg_use & 1)) { fail(); break; }
+            const uint8_t* my_q = s_stage + stg * 2 * kAtom + t * 128;
             const uint8_t* my_k = my_q + kAtom;
             uint32_t uq[P / 2];
             uint4 kraw[P / 8];
@@ -461,7 +462,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 uq[4 * i + 3] = a.w;
                 kraw[i] = *reinterpret_cast<const uint4*>(my_k + ((i ^ (t & 7)) << 4));
             }
-            mbar_arrive(&stage_free[slot]);
+            mbar_arrive(&stage_free[stg]);
             // unit key
             uint32_t uk[P / 2];
             {
@@ -642,17 +643,17 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         // =============================================================== readout warps
         const int e = t - 256;
         const int owner = e / K::R, orow = e % K::R;
-        // this lane's partial readout of chunk c0 + kc -> its owner (den: the
-        // denominator of the row, extra CTA only)
-        auto send = [&](int kc, float den_intra) -> bool {
+        // this lane's partial readout of chunk c0 + kc -> its owner (the extra
+        // CTA adds the row's inter-chunk denominator)
+        auto send = [&](int kc) -> bool {
             const int slot = kc & 1, use = kc >> 1;
             const int rs = kc % K::RS, ruse = kc / K::RS;
-            if (!wait(extra ? &y_full[slot] : &y_part[slot], use & 1)) return false;
+            if (!wait(&y_part[slot], use & 1)) return false;
             tc_fence_after();
-            float den = den_intra;
+            float den = 0.f;
             if (extra) {
                 if (!wait(&den_ready[slot], use & 1)) return false;
-                den += dens[slot][e];
+                den = dens[slot][e];
             }
             uint32_t ypk[DV / 2];
             const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
@@ -686,69 +687,57 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
             return true;
         };
-        if (!extra) {
-            for (int kk = 0; kk < nk; ++kk)
-                if (!send(kk, 0.f)) { fail(); break; }
-        } else {
-            // extra CTA: P = (Q Kh^T)^2 masked (s <= t) of chunk kk, bf16 in place,
-            // and its row sum; then the previous chunk's partial readout
-            float den_prev = 0.f;
-            for (int kk = 0; kk <= nk; ++kk) {
-                float den_cur = 0.f;
-                if (kk < nk) {
-                    if (!wait(&sc_done, kk & 1)) { fail(); break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t sc[32], pk[16];
-                        tmem_ld16(tm(K::tx_sc + 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
-                        tmem_ld16(tm(K::tx_sc + 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int col = 32 * q4 + 2 * i;
-                            float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
-                            a = col <= e ? a * a : 0.f;
-                            b = col + 1 <= e ? b * b : 0.f;
-                            pk[i] = pack_bf16x2(a, b);
-                            // the row sum of the rounded weights keeps the
-                            // intra-chunk weights an exact convex combination
-                            const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
-                            den_cur += __low2float(hp) + __high2float(hp);
-                        }
-                        tmem_st16(tm(K::tx_sc + 16 * q4), pk);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&p_ready);
-                }
-                if (kk >= 1 && !send(kk - 1, den_prev)) { fail(); break; }
-                den_prev = den_cur;
-            }
-        }
+        for (int kk = 0; kk < nk; ++kk)
+            if (!send(kk)) { fail(); break; }
     } else {
         regs_dec<kRegsMma>();
     }
     if (warp >= 14) {
         // =============================================================== reduce warps
-        // owner side, chunk by chunk as the partial rows land: sum them, divide
-        // by the denominator, store o, then hand the receive slot back to every
-        // sender (its next use is RS chunks later)
+        // owner side, chunk by chunk as the partial rows land: sum them and the
+        // rows' intra-chunk part, divide by the denominator, store o, then hand
+        // the receive slot back to every sender (its next use is RS chunks later)
+        constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
         const int er = t - 448;
         const int r0 = rank * K::R;
         const int items = my_rows * (DV / 8);
         __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
+        const __nv_bfloat16* yih = y_intra + bh * (int64_t)T * DV;
+        const float* dih = d_intra + bh * (int64_t)T;
         for (int kr = 0; kr < nk; ++kr) {
             const int r = kr % K::RS;
+            // this chunk's intra-chunk rows do not depend on the partials: load first
+            uint4 yi[kRedIt];
+            float di[kRedIt];
+#pragma unroll
+            for (int it = 0; it < kRedIt; ++it) {
+                const int idx = er + 64 * it;
+                const int lr = idx % my_rows, i = idx / my_rows;
+                const int otok = (c0 + kr) * kChunk + r0 + lr;
+                const bool have = idx < items && otok < T;
+                yi[it] = have ? *reinterpret_cast<const uint4*>(yih + (int64_t)otok * DV + 8 * i) : make_uint4(0, 0, 0, 0);
+                di[it] = have ? dih[otok] : 0.f;
+            }
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs) &&
                                              mbar_wait(&local_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs))) {
                 fail();
                 break;
             }
             const uint8_t* recv = s_recv + r * K::recv_buf;
-            for (int idx = er; idx < items; idx += 64) {
+#pragma unroll
+            for (int it = 0; it < kRedIt; ++it) {
+                const int idx = er + 64 * it;
+                if (idx >= items) break;
                 const int lr = idx % my_rows, i = idx / my_rows;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float acc[8];
+                {
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yi[it]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[2 * j] = __low2float(h[j]);
+                        acc[2 * j + 1] = __high2float(h[j]);
+                    }
+                }
 #pragma unroll
                 for (int src = 0; src < K::CS; ++src) {
                     const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
@@ -759,7 +748,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         acc[2 * j + 1] += __high2float(h[j]);
                     }
                 }
-                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
+                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + di[it];
                 const float inv = d > 0.f ? 1.f / d : 0.f;
                 const int otok = (c0 + kr) * kChunk + r0 + lr;
                 if (otok < T)
@@ -783,105 +772,96 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         tma_prefetch_desc(&tmv);
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
+            const int stg = kk % nstg, stg_use = kk / nstg;
             const int row = (c0 + kk) * kChunk;
-            // query and key rows of chunk kk into staging slot kk % 2
-            if (kk >= 2 && !mbar_wait(&stage_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            mbar_arrive_expect_tx(&stage_full[slot], 2 * kAtom);
-            tma_load_3d(s_stage + slot * 2 * kAtom, &tmq, 0, row, (int)bh, &stage_full[slot]);
-            tma_load_3d(s_stage + slot * 2 * kAtom + kAtom, &tmk, 0, row, (int)bh, &stage_full[slot]);
-            // value tile of chunk kk into its buffer (tile CTA: one; extra CTA: two)
-            const int vs = extra ? slot : 0;
-            if (extra ? kk >= 2 : kk >= 1) {
-                const uint32_t par = extra ? ((use - 1) & 1) : ((kk - 1) & 1);
-                if (!mbar_wait(&v_free[vs], par, &abort_flag, kWaitNs)) { fail(); break; }
-            }
-            mbar_arrive_expect_tx(&v_full[vs], kAtom);
-            tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[vs]);
+            // query and key rows of chunk kk into its stage
+            if (kk >= nstg && !mbar_wait(&stage_free[stg], (stg_use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&stage_full[stg], 2 * kAtom);
+            tma_load_3d(s_stage + stg * 2 * kAtom, &tmq, 0, row, (int)bh, &stage_full[stg]);
+            tma_load_3d(s_stage + stg * 2 * kAtom + kAtom, &tmk, 0, row, (int)bh, &stage_full[stg]);
+            // value tile of chunk kk into its buffer
+            if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&v_full[slot], kAtom);
+            tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[slot]);
         }
     }
     if (t == 384) {
         // =============================================================== MMA issuer
-        const uint32_t sb_ak = smem_u32(s_ak), sb_v = smem_u32(s_v), sb_s16 = smem_u32(s_s16);
+        // Every descriptor is built once: one thread issues all MMAs, so the
+        // issue loop carries no descriptor arithmetic beyond one add per
+        // K step (a step moves the start-address field, in 16-byte units).
         constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
         constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, true, true);
-        constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
-        // intra-chunk part of chunk kp (extra CTA), issued one chunk late
-        auto issue_pv = [&](int kp) -> bool {
-            const int sp = kp & 1;
-            if (!mbar_wait(&p_ready, kp & 1, &abort_flag, kWaitNs)) return false;
-            tc_fence_after();
-            const uint32_t vb = smem_u32(v_buf(kp));
-            for (int ks = 0; ks < 8; ++ks)
-                mma_ts(tb + K::tx_y + 64 * sp, tb + K::tx_sc + 8 * ks, sdesc_mnmajor_sw128(vb + ks * 2048, kAtom), id_pv, 1u);
-            mma_commit(&y_full[sp]);
-            mma_commit(&v_free[sp]);
-            return true;
-        };
-        bool mok = true;
+        constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
+        constexpr uint32_t id_w = idesc_bf16_f32(128, P);
+        constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kAtomD = kAtom >> 4;
+        // key lift (A of the update): tile CTA two 64-slot atoms per tile; the
+        // extra CTA's tail tile one atom that the second M atom aliases (its
+        // rows past the tail are never read)
+        const uint64_t d_ak = sdesc_mnmajor_sw128(smem_u32(s_ak), extra ? 0u : kAtom);
+        const uint64_t d_s16 = sdesc_mnmajor_sw128(smem_u32(s_s16), kAtom);
+        const uint64_t d_v[2] = {sdesc_mnmajor_sw128(smem_u32(v_buf(0)), kAtom),
+                                 sdesc_mnmajor_sw128(smem_u32(v_buf(1)), kAtom)};
+        // extra CTA: unit keys as M (aliased atoms) and as N; staged Q; Z
+        const uint64_t d_khm[2] = {sdesc_mnmajor_sw128(smem_u32(s_kh(0)), 0), sdesc_mnmajor_sw128(smem_u32(s_kh(1)), 0)};
+        const uint64_t d_khn[2] = {sdesc_mnmajor_sw128(smem_u32(s_kh(0)), kAtom),
+                                   sdesc_mnmajor_sw128(smem_u32(s_kh(1)), kAtom)};
+        const uint64_t d_q[2] = {sdesc_kmajor_sw128(smem_u32(s_stage)), sdesc_kmajor_sw128(smem_u32(s_stage + 2 * kAtom))};
+        const uint64_t d_z16 = sdesc_kmajor_sw128(smem_u32(s_z16));
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
-            if (!mbar_wait(&v_full[extra ? slot : 0], extra ? (use & 1) : (kk & 1), &abort_flag, kWaitNs)) { fail(); mok = false; break; }
-            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
+            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!mbar_wait(&v_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             tc_fence_after();
-            const uint32_t sb_vk = smem_u32(v_buf(kk));
+            const uint64_t dv = d_v[slot];
             // ---- group U: state updates (extra CTA: tail state and Z)
             if (!extra) {
-#pragma unroll 1
+#pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
+#pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tb + K::tm_s + 64 * tl, sdesc_mnmajor_sw128(sb_ak + 2 * tl * kAtom + ks * 2048, kAtom),
-                               sdesc_mnmajor_sw128(sb_vk + ks * 2048, kAtom), id_upd, 1u);
+                        mma_ss(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + ks * kStepMN, dv + ks * kStepMN, id_upd, 1u);
                 mma_commit(&upd_done);
                 mma_commit(&ak_free);
-                mma_commit(&v_free[0]);
+                mma_commit(&v_free[slot]);
             } else {
-                // tail tile: one 64-slot atom, the second M atom aliases it (rows past the tail are never read)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) mma_ss(tb + K::tx_s, d_ak + ks * kStepMN, dv + ks * kStepMN, id_upd, 1u);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_s, sdesc_mnmajor_sw128(sb_ak + ks * 2048, 0), sdesc_mnmajor_sw128(sb_vk + ks * 2048, kAtom),
-                           id_upd, 1u);
-                const uint32_t sb_kh = smem_u32(s_kh(kk)), sb_q = smem_u32(s_stage + slot * 2 * kAtom);
-                constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_z, sdesc_mnmajor_sw128(sb_kh + ks * 2048, 0),
-                           sdesc_mnmajor_sw128(sb_kh + ks * 2048, kAtom), id_z, 1u);
+                    mma_ss(tb + K::tx_z, d_khm[slot] + ks * kStepMN, d_khn[slot] + ks * kStepMN, id_z, 1u);
                 mma_commit(&upd_done);
                 mma_commit(&ak_free);
-                // previous chunk's intra part, then this chunk's scores (same tensor columns)
-                if (kk >= 1 && !issue_pv(kk - 1)) { fail(); mok = false; break; }
-                constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
-                for (int ks = 0; ks < P / 16; ++ks)
-                    mma_ss(tb + K::tx_sc, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_kh + ks * 32), id_sc,
-                           ks > 0 ? 1u : 0u);
-                mma_commit(&sc_done);
+                mma_commit(&v_free[slot]);
                 mma_commit(&kh_free[slot]);
             }
             // ---- group R: readout of the state before this chunk
-            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
-            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); mok = false; break; }
+            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
-#pragma unroll 1
+                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 128 * slot;
+#pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
+#pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + K::tm_y + 64 * slot, tb + K::tm_aq + 128 * slot + 64 * tl + 8 * ks,
-                               sdesc_mnmajor_sw128(sb_s16 + tl * kAtom + ks * 2048, kAtom), id_read, (tl > 0 || ks > 0) ? 1u : 0u);
+                        mma_ts(dy, aq + 64 * tl + 8 * ks, d_s16 + tl * kAtomD + ks * kStepMN, id_read,
+                               (tl > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(&y_part[slot]);
                 mma_commit(&aq_free[slot]);
             } else {
+                const uint32_t dy = tb + K::tx_y + 64 * slot, aq = tb + K::tx_aq + 32 * slot;
+#pragma unroll
                 for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
-                    mma_ts(tb + K::tx_y + 64 * slot, tb + K::tx_aq + 32 * slot + 8 * ks,
-                           sdesc_mnmajor_sw128(sb_s16 + ks * 2048, kAtom), id_read, ks > 0 ? 1u : 0u);
-                const uint32_t sb_q = smem_u32(s_stage + slot * 2 * kAtom), sb_z16 = smem_u32(s_z16);
-                constexpr uint32_t id_w = idesc_bf16_f32(128, P);
+                    mma_ts(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
+#pragma unroll
                 for (int ks = 0; ks < P / 16; ++ks)
-                    mma_ss(tb + K::tx_w, sdesc_kmajor_sw128(sb_q + ks * 32), sdesc_kmajor_sw128(sb_z16 + ks * 32), id_w,
-                           ks > 0 ? 1u : 0u);
+                    mma_ss(tb + K::tx_w, d_q[slot] + ks * kStepK, d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
                 mma_commit(&y_part[slot]);
                 mma_commit(&aq_free[slot]);
             }
         }
-        if (extra && mok && nk >= 1 && !issue_pv(nk - 1)) fail();
         // every issued MMA has completed before tensor memory is released
         mma_commit(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
@@ -892,6 +872,164 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     cluster.sync();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// ---------------------------------------------------------------- intra-chunk part
+// Every chunk on its own (no state): for the 128 queries of a chunk,
+//   P = (Q Kh^T) o (Q Kh^T) o M   (bf16, M the causal mask s <= t)
+//   [Y | d] = P [V | 1]           (fp32 accumulation)
+// Y goes out as bf16 rows [BH][T][DV] and d, the rows' intra-chunk
+// normaliser, as fp32 [BH][T]; the fused forward adds both when it combines
+// a chunk's rows.  The normaliser comes out of the same MMA as Y (the ones
+// column of B), so it sums exactly the rounded weights Y is built from.
+// One CTA per (chunk, head); thread t owns query / key / value row t.
+template <int P, int DV>
+__global__ void __launch_bounds__(128)
+intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ y_out, float* __restrict__ d_out,
+                int T) {
+    constexpr int NV = DV + 16;  // values, ones, zero padding
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar, drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* Qs = sm;              // K-major, 128 rows x 128 B
+    uint8_t* Ks = sm + kAtom;      // unit keys, K-major
+    uint8_t* Vs = sm + 2 * kAtom;  // [V | 1 | 0], MN-major, two 64-column atoms
+    const int t = threadIdx.x, warp = t >> 5;
+    const int64_t bh = blockIdx.y;
+    const int row = blockIdx.x * kChunk + t;
+    const bool valid = row < T;
+    const int64_t grow = bh * T + (valid ? row : 0);
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        mbar_init(&drain, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    // rows -> shared memory (zeros past T)
+    {
+        const uint4* gq = reinterpret_cast<const uint4*>(q + grow * P);
+        const uint4* gk = reinterpret_cast<const uint4*>(k + grow * P);
+        const uint4* gv = reinterpret_cast<const uint4*>(v + grow * DV);
+        uint4 kr[P / 8];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < P / 8; ++i) {
+            const uint4 a = valid ? gq[i] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(Qs + sw128_chunk(t, 8 * i, kChunk)) = a;
+            kr[i] = valid ? gk[i] : make_uint4(0, 0, 0, 0);
+            const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float x = __bfloat162float(ke[j]);
+                ss = fmaf(x, x, ss);
+            }
+        }
+        const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+        for (int i = 0; i < P / 8; ++i) {
+            const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
+            uint4 w;
+            w.x = pack_bf16x2(__bfloat162float(ke[0]) * kinv, __bfloat162float(ke[1]) * kinv);
+            w.y = pack_bf16x2(__bfloat162float(ke[2]) * kinv, __bfloat162float(ke[3]) * kinv);
+            w.z = pack_bf16x2(__bfloat162float(ke[4]) * kinv, __bfloat162float(ke[5]) * kinv);
+            w.w = pack_bf16x2(__bfloat162float(ke[6]) * kinv, __bfloat162float(ke[7]) * kinv);
+            *reinterpret_cast<uint4*>(Ks + sw128_chunk(t, 8 * i, kChunk)) = w;
+        }
+#pragma unroll
+        for (int i = 0; i < DV / 8; ++i)
+            *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(8 * i, t, kAtom)) = valid ? gv[i] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(DV, t, kAtom)) = make_uint4(0x3F80u, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(DV + 8, t, kAtom)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    const uint32_t lane0 = (uint32_t)(warp * 32);
+    if (t == 0) {
+        const uint64_t dq = sdesc_kmajor_sw128(smem_u32(Qs)), dk = sdesc_kmajor_sw128(smem_u32(Ks));
+        constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
+#pragma unroll
+        for (int ks = 0; ks < P / 16; ++ks) mma_ss(tb, dq + 2 * ks, dk + 2 * ks, id_sc, ks > 0 ? 1u : 0u);
+        mma_commit(&bar);
+    }
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, kWaitNs));
+    if (!ok) abort_flag = 1;
+    tc_fence_after();
+    // P = scores^2 masked, bf16, in place (columns 0..63); quarters past this
+    // warp's rows are all masked
+    if (ok) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
+            if (q4 <= warp) {
+                uint32_t sc[32];
+                tmem_ld16(tmem_addr(tb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                tmem_ld16(tmem_addr(tb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int col = 32 * q4 + 2 * i;
+                    float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
+                    a = col <= t ? a * a : 0.f;
+                    b = col + 1 <= t ? b * b : 0.f;
+                    pk[i] = pack_bf16x2(a, b);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = 0u;
+            }
+            tmem_st16(tmem_addr(tb, lane0, 16 * q4), pk);
+        }
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (t == 0 && !abort_flag) {
+        const uint64_t dv = sdesc_mnmajor_sw128(smem_u32(Vs), kAtom);
+        constexpr uint32_t id_pv = idesc_bf16_f32_major(128, NV, false, true);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_ts(tb + 128, tb + 8 * ks, dv + ks * (2048 >> 4), id_pv, ks > 0 ? 1u : 0u);
+        mma_commit(&bar);
+    }
+    ok = !abort_flag && __all_sync(0xffffffffu, mbar_wait(&bar, 1, &abort_flag, kWaitNs));
+    tc_fence_after();
+    if (ok) {
+        uint32_t y[DV + 16];
+#pragma unroll
+        for (int c = 0; c < NV; c += 16) tmem_ld16(tmem_addr(tb, lane0, 128 + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
+        tmem_wait_ld();
+        if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(y_out + grow * DV);
+#pragma unroll
+            for (int i = 0; i < DV / 8; ++i)
+                dst[i] = make_uint4(pack_bf16x2(__uint_as_float(y[8 * i]), __uint_as_float(y[8 * i + 1])),
+                                    pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
+                                    pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
+                                    pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
+            d_out[grow] = __uint_as_float(y[DV]);
+        }
+    } else if (t == 0) {
+        atomicOr(&g_chunked_tc_status, kStatusTimeout);
+    }
+    // every issued MMA has completed before the tensor memory is released
+    if (t == 0) {
+        mma_commit(&drain);
+        mbar_wait_quiet(&drain, 0, kWaitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 256);
 }
 
 // ---------------------------------------------------------------- host side
@@ -976,20 +1114,33 @@ int max_clusters() {
 }
 
 template <int P, int DV>
-cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, const float* S_start,
-                         const float* z_start, int start_groups, float* S_final, float* z_final, int BH, int T,
-                         int seg_chunks, int G, cudaStream_t s) {
+cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* y_intra, float* d_intra,
+                         const float* S_start, const float* z_start, int start_groups, float* S_final,
+                         float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
     if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
+    // intra-chunk rows first: every chunk at once, over the whole device
+    constexpr size_t intra_smem = 4 * kAtom + 1024;
+    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)intra_smem);
+    if (e != cudaSuccess) return e;
+    const dim3 igrid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)BH);
+    KATA_TRACED("intra_tc", s,
+                (intra_tc_kernel<P, DV><<<igrid, 128, intra_smem, s>>>(
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                    static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(y_intra), d_intra, T)));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    cudaError_t e = configure<P, DV>(cfg, attr, G, BH, s);
+    e = configure<P, DV>(cfg, attr, G, BH, s);
     if (e != cudaSuccess) return e;
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
     KATA_TRACED("chunked_tc", s,
                 e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tk, tv, static_cast<__nv_bfloat16*>(o),
-                                       S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
+                                       static_cast<const __nv_bfloat16*>(y_intra),
+                                       static_cast<const float*>(d_intra), S_start, z_start, start_groups, S_final,
+                                       z_final, T, seg_chunks));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1027,12 +1178,19 @@ int chunked_tc_segment_chunks(int T, int G) {
     return (nch + G - 1) / G;
 }
 
-cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, const float* S_start,
-                              const float* z_start, int start_groups, float* S_final, float* z_final, int BH,
-                              int T, int p, int dv, int G, cudaStream_t s) {
+size_t chunked_tc_intra_bytes(int BH, int T, int dv) {
+    return (size_t)BH * (size_t)T * ((size_t)dv * 2 + 4);
+}
+
+cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
+                              const float* S_start, const float* z_start, int start_groups, float* S_final,
+                              float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s) {
     const int seg_chunks = chunked_tc_segment_chunks(T, G);
-    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, S_start, z_start, start_groups, S_final, z_final, BH, T,
-                                             seg_chunks, G, s));
+    // intra-chunk rows: bf16 [BH][T][dv], then fp32 normalisers [BH][T]
+    void* y_intra = intra;
+    float* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + (size_t)BH * T * dv * 2);
+    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, y_intra, d_intra, S_start, z_start, start_groups, S_final,
+                                             z_final, BH, T, seg_chunks, G, s));
     return cudaErrorInvalidValue;
 }
 
