@@ -17,11 +17,13 @@
 // by the update MMA) and a bf16 copy in shared memory (B operand of the
 // readout MMA).  Its query lift goes to tensor memory (A operand of the
 // readout), its key lift to shared memory (A operand of the update).  The
-// "extra CTA" owns the last, partly filled tile, the intra-chunk part and Z.
-// Each CTA's partial Y (128 x dv fp32) is summed in distributed shared
-// memory: CTA r owns rows [r*R, r*R + R) of the chunk, receives the partials
-// of those rows from every CTA of the cluster (double-buffered by chunk
-// parity), adds them, divides by d and stores o.
+// "extra CTA" owns the last, partly filled tile and Z (the inter-chunk
+// denominator).  The intra-chunk part of every chunk is computed beforehand
+// by a separate kernel (all chunks at once).  Each CTA's partial Y (128 x dv,
+// sent as bf16) is summed in distributed shared memory: tile CTA r owns rows
+// [r*R, r*R + R) of the chunk, receives the partials of those rows from
+// every CTA of the cluster (a ring of RS chunks), adds them and the rows'
+// intra-chunk part, divides by d and stores o.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -66,7 +68,7 @@ struct Cfg {
     static constexpr int TPC = NT >= 2 ? 2 : 1;        // tiles per tile CTA
     static constexpr int NTC = NT / TPC;               // tile CTAs
     static constexpr int CS = NTC + 1;                 // cluster size
-    static constexpr int R = (kChunk + CS - 1) / CS;   // output rows owned per CTA
+    static constexpr int R = kChunk / NTC;             // output rows owned per tile CTA (the extra CTA owns none)
     // shared memory, in 16 KB atoms from a 1024-byte aligned base
     //   tile CTA : key lift [0, 2 TPC), V (slot 0), bf16 state [TPC], query/key staging, V (slot 1)
     //   extra CTA: tail key lift, unit keys [2], bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
@@ -78,16 +80,18 @@ struct Cfg {
     // query / key row staging, (Q tile, K tile) per stage, filled by TMA: one
     // stage in a tile CTA (its lift warps copy the rows out at once), two in
     // the extra CTA (its MMAs read the queries in place)
-    static constexpr uint32_t atoms = 11;
-    // partial readouts: one part per (source CTA, receive slot) = R rows of bf16
-    // laid out [DV/8][R] x 16 bytes (a warp's store of one column group is
-    // contiguous per owner), then R fp32 denominators (extra CTA's part only)
+    static constexpr uint32_t atoms = 11, atoms_tile = 3 * TPC + 4;
+    // partial readouts received by a tile CTA: one part per (source CTA,
+    // receive slot) = R rows of bf16 laid out [DV/8][R] x 16 bytes (a warp's
+    // store of one column group is contiguous per owner), then R fp32
+    // denominators (extra CTA's part only)
     static constexpr uint32_t part_y = R * DV * 2;
     static constexpr uint32_t recv_part = part_y + round16(R * 4);
     static constexpr uint32_t recv_buf = CS * recv_part;
-    static constexpr int RS = 2;                        // receive slots (chunks in flight)
-    static constexpr uint32_t recv_off = atoms * kAtom;
-    static constexpr uint32_t total = recv_off + RS * recv_buf;
+    static constexpr uint32_t recv_off = atoms_tile * kAtom;
+    // receive slots (chunks in flight): three where they fit
+    static constexpr int RS = recv_off + 3 * recv_buf + 1024 + 4096 <= 232448 ? 3 : 2;
+    static constexpr uint32_t total = (recv_off + RS * recv_buf) > atoms * kAtom ? recv_off + RS * recv_buf : atoms * kAtom;
     static constexpr size_t smem = total + 1024;
     // tensor memory columns, tile CTA
     static constexpr uint32_t tm_s = 0;      // TPC x 64: fp32 state
@@ -102,7 +106,8 @@ struct Cfg {
     static_assert(NT % TPC == 0, "tiles must split evenly");
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(total + 1024 <= 232448, "shared memory");
-    static_assert(3 * TPC + 4 <= atoms, "tile CTA layout");
+    static_assert(atoms_tile <= atoms, "tile CTA layout");
+    static_assert(R * NTC == kChunk, "owned rows");
 };
 
 // ---------------------------------------------------------------- lifts per tile
@@ -317,9 +322,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const int NCH = (T + kChunk - 1) / kChunk;
     const int c0 = g * seg_chunks, c1 = min(NCH, c0 + seg_chunks);
     const int nk = c1 - c0;
-    const int my_rows = min(K::R, kChunk - rank * K::R);
-    // bytes of partial rows (and denominators) other CTAs deliver per chunk
-    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + (extra ? 0 : my_rows * 4);
+    const int my_rows = extra ? 0 : K::R;
+    // bytes of partial rows (and the extra CTA's denominators) other CTAs
+    // deliver per chunk
+    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + my_rows * 4;
     // shared memory of this CTA's role
     uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
     // value buffer of chunk kk (two, so the next chunk's values load while the
@@ -360,12 +366,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         fence_mbar_init();
         for (int b = 0; b < K::RS; ++b) {
             mbar_init(&recv_full[b], 1);
-            mbar_init(&peer_free[b], K::CS);
-            mbar_init(&local_full[b], my_rows);
+            mbar_init(&peer_free[b], K::NTC);  // one arrival per owner
+            mbar_init(&local_full[b], my_rows > 0 ? my_rows : 1);
         }
         fence_mbar_init();
         // the first RS chunks' partial rows may arrive as soon as the cluster starts
-        for (int b = 0; b < K::RS && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
+        if (my_rows > 0)
+            for (int b = 0; b < K::RS && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
         abort_flag = 0;
     }
     if (warp == 0) {
@@ -692,12 +699,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     } else {
         regs_dec<kRegsMma>();
     }
-    if (warp >= 14) {
+    if (warp >= 14 && my_rows > 0) {
         // =============================================================== reduce warps
         // owner side, chunk by chunk as the partial rows land: sum them and the
         // rows' intra-chunk part, divide by the denominator, store o, then hand
         // the receive slot back to every sender (its next use is RS chunks later)
         constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
+        constexpr int kPre = kRedIt < 2 ? kRedIt : 2;  // items whose intra rows are loaded ahead
         const int er = t - 448;
         const int r0 = rank * K::R;
         const int items = my_rows * (DV / 8);
@@ -707,10 +715,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         for (int kr = 0; kr < nk; ++kr) {
             const int r = kr % K::RS;
             // this chunk's intra-chunk rows do not depend on the partials: load first
-            uint4 yi[kRedIt];
-            float di[kRedIt];
+            uint4 yi[kPre];
+            float di[kPre];
 #pragma unroll
-            for (int it = 0; it < kRedIt; ++it) {
+            for (int it = 0; it < kPre; ++it) {
                 const int idx = er + 64 * it;
                 const int lr = idx % my_rows, i = idx / my_rows;
                 const int otok = (c0 + kr) * kChunk + r0 + lr;
@@ -729,9 +737,19 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 const int idx = er + 64 * it;
                 if (idx >= items) break;
                 const int lr = idx % my_rows, i = idx / my_rows;
+                uint4 yrow;
+                float drow;
+                if (it < kPre) {
+                    yrow = yi[it];
+                    drow = di[it];
+                } else {
+                    const int otok = (c0 + kr) * kChunk + r0 + lr;
+                    yrow = otok < T ? *reinterpret_cast<const uint4*>(yih + (int64_t)otok * DV + 8 * i) : make_uint4(0, 0, 0, 0);
+                    drow = otok < T ? dih[otok] : 0.f;
+                }
                 float acc[8];
                 {
-                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yi[it]);
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yrow);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         acc[2 * j] = __low2float(h[j]);
@@ -748,7 +766,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         acc[2 * j + 1] += __high2float(h[j]);
                     }
                 }
-                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + di[it];
+                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + drow;
                 const float inv = d > 0.f ? 1.f / d : 0.f;
                 const int otok = (c0 + kr) * kChunk + r0 + lr;
                 if (otok < T)
