@@ -5,18 +5,29 @@
 //   S = Q Kh^T            (tcgen05, A = raw queries, B = unit keys, D in TMEM)
 //   P = S o S, masked     (CUDA cores: squared scores, causal mask s <= t,
 //                          packed to bf16 in place in TMEM)
-//   O += P [V | 1]        (tcgen05, A = P from TMEM, B = V^T with an extra
-//                          ones row, D in TMEM)
-//   o = O[:, :dv] / O[:, dv]
+//   O += P [V | 1]        (tcgen05, A = P from TMEM, B = the value tile and a
+//                          constant ones column, D in TMEM)
+//   o = O[:, :dv] / O[:, 64]
 // Only keys are put on the unit sphere: a query's norm scales numerator and
 // denominator alike and cancels.  Scores of unit keys with a fixed query are
 // bounded, so no running maximum or rescale is needed.
+//
+// Pipeline (one CTA per query tile, 384 threads):
+//   warp 0 lane 0   TMA: the query tile once, key and value tiles into a ring
+//                   of kStages stages
+//   warp 1 lane 0   issues every MMA: S(j+1) before O(j), so the squaring of
+//                   tile j overlaps the score product of tile j+1
+//   warps 2-3       put the keys of each staged tile on the unit sphere, in
+//                   place (thread = two key rows)
+//   warps 4-7, 8-11 two squaring groups, one per score buffer (tiles of even
+//                   and odd index); warps 4-7 also write o at the end
 #include <cuda_bf16.h>
 
 #include <cstdint>
 
 #include "kata_internal.h"
 #include "tc_primitives.cuh"
+#include "tc_tma.cuh"
 
 namespace kata {
 namespace {
@@ -26,239 +37,264 @@ using namespace tc;
 __device__ unsigned int g_quad_tc_status = 0;
 
 constexpr int kTile = 128;        // queries per CTA, keys per tile
-constexpr int kThreads = 128;     // thread t owns query row t (TMEM lane t)
-constexpr uint32_t kTmemCols = 256;
+constexpr int kThreads = 384;
+constexpr int kStages = 3;        // key / value ring
+constexpr uint32_t kAtom = 128 * 128;
+constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value slots, the ones column, pad
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every device-side wait
 
-template <int DV>
-struct QuadLayout {
-    static constexpr int NV = DV + 16;                  // V^T rows: values, ones, zero pad
-    static constexpr uint32_t q_bytes = kTile * 128;    // 128 rows x 128 B
-    static constexpr uint32_t k_bytes = kTile * 128;
-    static constexpr uint32_t v_bytes = 2 * NV * 128;   // two 64-key column blocks
-    static constexpr uint32_t q_off = 0, k_off = q_bytes, v_off = q_bytes + k_bytes;
-    static constexpr uint32_t total = v_off + v_bytes;
-    static constexpr size_t smem = total + 1024;        // slack for 1024-byte alignment
-};
+// shared memory, 16 KB atoms from a 1024-byte aligned base: Q, K[kStages],
+// V[kStages], the ones atom (last, so every value stage reaches it with a
+// positive atom stride)
+constexpr uint32_t kQOff = 0, kKOff = kAtom, kVOff = (1 + kStages) * kAtom, kOnesOff = (1 + 2 * kStages) * kAtom;
+constexpr size_t kSmem = (2 + 2 * kStages) * kAtom + 1024;
+// tensor memory: two score buffers, O
+constexpr uint32_t kTmS = 0, kTmO = 256;
 
 template <int P, int DV>
-__global__ void __launch_bounds__(kThreads)
-quadratic_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                    const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ o, int T) {
-    using L = QuadLayout<DV>;
-    constexpr int NV = L::NV;
+__global__ void __launch_bounds__(kThreads, 1)
+quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int T) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_s, bar_o;
+    __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_ready[kStages], kv_free[kStages];
+    __shared__ uint64_t s_full[2], p_full[2], s_free[2], o_done, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* Qs = sm + L::q_off;
-    uint8_t* Ks = sm + L::k_off;
-    uint8_t* Vs = sm + L::v_off;
 
     const int t = threadIdx.x, warp = t >> 5;
     const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest query tiles first
     const int64_t bh = blockIdx.y;
-    const int qi = qt * kTile + t;
-    const __nv_bfloat16* qh = q + bh * (int64_t)T * P;
-    const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
-    const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
+    const int nj = qt + 1;                      // key tiles up to the diagonal
 
     if (t == 0) {
-        mbar_init(&bar_s, 1);
-        mbar_init(&bar_o, 1);
+        mbar_init(&q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&k_ready[s], 64);
+            mbar_init(&kv_free[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 128);
+            mbar_init(&s_free[b], 1);
+        }
+        mbar_init(&o_done, 1);
+        mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_base, kTmemCols);
+        tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
-    // query row t, raw bf16, into the swizzled tile (rows past T are zero)
+    // the ones atom: B rows = keys, column 64 of the value product = 1
+    for (int r = t; r < kTile; r += kThreads)
 #pragma unroll
-    for (int c = 0; c < P / 8; ++c) {
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (qi < T) val = *reinterpret_cast<const uint4*>(qh + (int64_t)qi * P + 8 * c);
-        *reinterpret_cast<uint4*>(Qs + sw128_chunk(t, 8 * c, kTile)) = val;
-    }
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sm + kOnesOff + mn_sw128_chunk(8 * c, r, kAtom)) =
+                make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    const uint32_t d_s = tb;          // S (fp32, 128 cols); P overwrites cols 0..63 in place
-    const uint32_t d_o = tb + kTile;  // O (fp32, NV cols)
-    const uint32_t lane0 = (uint32_t)(warp * 32);
-    bool ok = true;
-    uint64_t* pending_bar = nullptr;  // barrier of the last commit not yet observed
-    uint32_t pending_parity = 0;
+    auto fail = [&]() {
+        abort_flag = 1;
+        atomicOr(&g_quad_tc_status, kStatusTimeout);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag, kWaitNs));
+    };
 
-    for (int j = 0; j <= qt; ++j) {
-        // ---- key tile j: unit keys (row t) and V^T with the ones row
-        const int kj = j * kTile + t;
-        {
-            uint4 raw[P / 8];
-            float ss = 0.f;
-#pragma unroll
-            for (int c = 0; c < P / 8; ++c) {
-                raw[c] = make_uint4(0, 0, 0, 0);
-                if (kj < T) raw[c] = *reinterpret_cast<const uint4*>(kh + (int64_t)kj * P + 8 * c);
-                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float x = __bfloat162float(e[i]);
-                    ss = fmaf(x, x, ss);
-                }
-            }
-            const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-#pragma unroll
-            for (int c = 0; c < P / 8; ++c) {
-                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
-                uint4 out;
-                uint32_t* w = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = pack_bf16x2(__bfloat162float(e[2 * i]) * inv, __bfloat162float(e[2 * i + 1]) * inv);
-                *reinterpret_cast<uint4*>(Ks + sw128_chunk(t, 8 * c, kTile)) = out;
-            }
+    if (t == 0) {
+        // =============================================================== TMA producer
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        mbar_arrive_expect_tx(&q_full, kAtom);
+        tma_load_3d(sm + kQOff, &tmq, 0, qt * kTile, (int)bh, &q_full);
+        int issued = 0;
+        for (int j = 0; j < nj; ++j) {
+            const int st = j % kStages, use = j / kStages;
+            if (j >= kStages && !mbar_wait(&kv_free[st], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&k_full[st], kAtom);
+            tma_load_3d(sm + kKOff + st * kAtom, &tmk, 0, j * kTile, (int)bh, &k_full[st]);
+            mbar_arrive_expect_tx(&v_full[st], kAtom);
+            tma_load_3d(sm + kVOff + st * kAtom, &tmv, 0, j * kTile, (int)bh, &v_full[st]);
+            issued = j + 1;
         }
-        {
-            // thread t: key pair (2*(t%64), +1), value columns [half*DV/2, (half+1)*DV/2)
-            const int pr = t & 63, half = t >> 6;
-            const int k0 = j * kTile + 2 * pr;
-            const bool v0 = k0 < T, v1 = k0 + 1 < T;
-            for (int c = half * (DV / 2); c < (half + 1) * (DV / 2); ++c) {
-                const float a = v0 ? __bfloat162float(vh[(int64_t)k0 * DV + c]) : 0.f;
-                const float b = v1 ? __bfloat162float(vh[(int64_t)(k0 + 1) * DV + c]) : 0.f;
-                *reinterpret_cast<uint32_t*>(Vs + sw128_offset(c, 2 * pr, NV)) = pack_bf16x2(a, b);
-            }
-            for (int c = DV + half * 8; c < DV + (half + 1) * 8; ++c) {
-                const uint32_t one = (c == DV) ? pack_bf16x2(v0 ? 1.f : 0.f, v1 ? 1.f : 0.f) : 0u;
-                *reinterpret_cast<uint32_t*>(Vs + sw128_offset(c, 2 * pr, NV)) = one;
-            }
+        // no copy may still be landing in shared memory when the CTA exits
+        mbar_wait_quiet(&q_full, 0, kWaitNs);
+        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+            mbar_wait_quiet(&k_full[j % kStages], (j / kStages) & 1, kWaitNs);
+            mbar_wait_quiet(&v_full[j % kStages], (j / kStages) & 1, kWaitNs);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- S = Q Kh^T
-        if (t == 0) {
+    } else if (t == 32) {
+        // =============================================================== MMA issuer
+        constexpr uint32_t id_s = idesc_bf16_f32(kTile, kTile);
+        constexpr uint32_t id_o = idesc_bf16_f32_major(kTile, kNV, false, true);
+        const uint64_t d_q = sdesc_kmajor_sw128(smem_u32(sm + kQOff));
+        auto issue_s = [&](int j) -> bool {
+            const int st = j % kStages, b = j & 1;
+            if (!mbar_wait(&k_ready[st], (j / kStages) & 1, &abort_flag, kWaitNs)) return false;
+            if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1, &abort_flag, kWaitNs)) return false;
             tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16_f32(kTile, kTile);
+            const uint64_t d_k = sdesc_kmajor_sw128(smem_u32(sm + kKOff + st * kAtom));
 #pragma unroll
-            for (int ks = 0; ks < P / 16; ++ks)
-                mma_ss(d_s, sdesc_kmajor_sw128(smem_u32(Qs) + ks * 32), sdesc_kmajor_sw128(smem_u32(Ks) + ks * 32),
-                       idesc, ks > 0);
-            mma_commit(&bar_s);
-        }
-        pending_bar = &bar_s;
-        pending_parity = j & 1;
-        ok = mbar_wait(&bar_s, j & 1, &abort_flag, kWaitNs);
-        if (!ok) abort_flag = 1;
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        // ---- P = S o S with the causal mask, bf16 pairs written over S cols [0, 64)
-        const bool diag = (j == qt);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-            uint32_t s0[16], s1[16], pk[16];
-            tmem_ld16(tmem_addr(d_s, lane0, c0), s0);
-            tmem_ld16(tmem_addr(d_s, lane0, c0 + 16), s1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float a = __uint_as_float(s0[2 * i]), b = __uint_as_float(s0[2 * i + 1]);
-                a *= a;
-                b *= b;
-                if (diag) {
-                    const int key = j * kTile + c0 + 2 * i;
-                    if (key > qi) a = 0.f;
-                    if (key + 1 > qi) b = 0.f;
-                }
-                pk[i] = pack_bf16x2(a, b);
-                float c = __uint_as_float(s1[2 * i]), d = __uint_as_float(s1[2 * i + 1]);
-                c *= c;
-                d *= d;
-                if (diag) {
-                    const int key = j * kTile + c0 + 16 + 2 * i;
-                    if (key > qi) c = 0.f;
-                    if (key + 1 > qi) d = 0.f;
-                }
-                pk[8 + i] = pack_bf16x2(c, d);
+            for (int ks = 0; ks < P / 16; ++ks) mma_ss(tb + kTmS + 128 * b, d_q + 2 * ks, d_k + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+            mma_commit(&s_full[b]);
+            return true;
+        };
+        bool ok = mbar_wait(&q_full, 0, &abort_flag, kWaitNs) && issue_s(0);
+        for (int j = 0; ok && j < nj; ++j) {
+            const int st = j % kStages, b = j & 1;
+            if (j + 1 < nj && !issue_s(j + 1)) { ok = false; break; }
+            if (!mbar_wait(&p_full[b], (j >> 1) & 1, &abort_flag, kWaitNs) ||
+                !mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag, kWaitNs)) {
+                ok = false;
+                break;
             }
-            tmem_st16(tmem_addr(d_s, lane0, c0 / 2), pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncthreads();
-        // ---- O += P [V | 1]
-        if (t == 0) {
             tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16_f32(kTile, NV);
+            // B = [value tile | ones]: two MN atoms, the ones atom kOnesOff - value stage bytes away
+            const uint32_t vaddr = smem_u32(sm + kVOff + st * kAtom);
+            const uint64_t d_v = sdesc_mnmajor_sw128(vaddr, (uint32_t)(kOnesOff - (kVOff + st * kAtom)));
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ts(d_o, d_s + ks * 8,
-                       sdesc_kmajor_sw128(smem_u32(Vs) + (ks >> 2) * NV * 128 + (ks & 3) * 32), idesc,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&bar_o);
+                mma_ts(tb + kTmO, tb + kTmS + 128 * b + 8 * ks, d_v + ks * (2048 >> 4), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&kv_free[st]);
+            mma_commit(&s_free[b]);
         }
-        pending_bar = &bar_o;
-        pending_parity = j & 1;
-        ok = mbar_wait(&bar_o, j & 1, &abort_flag, kWaitNs);
-        if (!ok) abort_flag = 1;
-        if (!__syncthreads_and(ok)) {
-            ok = false;
-            break;
+        if (!ok) fail();
+        mma_commit(&o_done);
+        mma_commit(&drain);
+        mbar_wait_quiet(&drain, 0, kWaitNs);
+    } else if (warp == 2 || warp == 3) {
+        // =============================================================== key normalisation
+        const int lt = t - 64;
+        for (int j = 0; j < nj; ++j) {
+            const int st = j % kStages;
+            if (!wait(&k_full[st], (j / kStages) & 1)) { fail(); break; }
+            uint8_t* kb = sm + kKOff + st * kAtom;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = 2 * lt + rr;
+                uint4 raw[P / 8];
+                float ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < P / 8; ++c) {
+                    raw[c] = *reinterpret_cast<const uint4*>(kb + sw128_chunk(r, 8 * c, kTile));
+                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float x = __bfloat162float(e[i]);
+                        ss = fmaf(x, x, ss);
+                    }
+                }
+                const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+                for (int c = 0; c < P / 8; ++c) {
+                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
+                    uint4 w;
+                    w.x = pack_bf16x2(__bfloat162float(e[0]) * inv, __bfloat162float(e[1]) * inv);
+                    w.y = pack_bf16x2(__bfloat162float(e[2]) * inv, __bfloat162float(e[3]) * inv);
+                    w.z = pack_bf16x2(__bfloat162float(e[4]) * inv, __bfloat162float(e[5]) * inv);
+                    w.w = pack_bf16x2(__bfloat162float(e[6]) * inv, __bfloat162float(e[7]) * inv);
+                    *reinterpret_cast<uint4*>(kb + sw128_chunk(r, 8 * c, kTile)) = w;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&k_ready[st]);
         }
-        tc_fence_after();
-    }
-
-    if (ok) {
-        // ---- o = O[:, :DV] / O[:, DV]
-        uint32_t r[16];
-        tmem_ld16(tmem_addr(d_o, lane0, DV), r);
-        tmem_wait_ld();
-        const float den = __uint_as_float(r[0]);
-        const float inv = den > 0.f ? 1.f / den : 0.f;
+    } else if (warp >= 4) {
+        // =============================================================== squaring groups
+        const int b = warp >= 8 ? 1 : 0;
+        const int e = t & 127;          // query row = tensor-memory lane
+        const int wq = (warp & 3);      // this warp's rows are 32 wq .. 32 wq + 31
+        const uint32_t lane0 = (uint32_t)(wq * 32);
+        const uint32_t sb = tb + kTmS + 128 * b;
+        for (int j = b; j < nj; j += 2) {
+            if (!wait(&s_full[b], (j >> 1) & 1)) { fail(); break; }
+            tc_fence_after();
+            const bool diag = j == qt;  // keys past the query are masked only on the diagonal tile
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
-            tmem_ld16(tmem_addr(d_o, lane0, c0), r);
-            tmem_wait_ld();
-            if (qi < T) {
-                uint4 out[2];
-                uint32_t* w = reinterpret_cast<uint32_t*>(out);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
+                if (!diag || q4 <= wq) {
+                    uint32_t sc[32];
+                    tmem_ld16(tmem_addr(sb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                    tmem_ld16(tmem_addr(sb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-                __nv_bfloat16* dst = o + (bh * T + qi) * (int64_t)DV + c0;
-                reinterpret_cast<uint4*>(dst)[0] = out[0];
-                reinterpret_cast<uint4*>(dst)[1] = out[1];
+                    for (int i = 0; i < 16; ++i) {
+                        const int col = 32 * q4 + 2 * i;
+                        float a = __uint_as_float(sc[2 * i]), c = __uint_as_float(sc[2 * i + 1]);
+                        a *= a;
+                        c *= c;
+                        if (diag) {
+                            a = col <= e ? a : 0.f;
+                            c = col + 1 <= e ? c : 0.f;
+                        }
+                        pk[i] = pack_bf16x2(a, c);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                }
+                tmem_st16(tmem_addr(sb, lane0, 16 * q4), pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[b]);
+        }
+        if (b == 0) {
+            // ---- o = O[:, :DV] / O[:, 64]
+            const bool ok = wait(&o_done, 0) && !abort_flag;
+            tc_fence_after();
+            if (ok) {
+                const int qi = qt * kTile + e;
+                uint32_t r[16];
+                tmem_ld16(tmem_addr(tb + kTmO, lane0, 64), r);
+                tmem_wait_ld();
+                const float den = __uint_as_float(r[0]);
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < DV; c0 += 16) {
+                    tmem_ld16(tmem_addr(tb + kTmO, lane0, c0), r);
+                    tmem_wait_ld();
+                    if (qi < T) {
+                        uint4 out[2];
+                        uint32_t* w = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                        __nv_bfloat16* dst = o + (bh * T + qi) * (int64_t)DV + c0;
+                        reinterpret_cast<uint4*>(dst)[0] = out[0];
+                        reinterpret_cast<uint4*>(dst)[1] = out[1];
+                    }
+                }
             }
         }
-    } else {
-        if (t == 0) atomicOr(&g_quad_tc_status, kStatusTimeout);
-        // let this CTA's last MMA drain (bounded) before its columns are freed
-        if (pending_bar) mbar_wait_quiet(pending_bar, pending_parity, kWaitNs / 4);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, kTmemCols);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 template <int P, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, int BH, int T,
                          cudaStream_t s) {
-    constexpr size_t smem = QuadLayout<DV>::smem;
     auto kern = quadratic_tc_kernel<P, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
+    CUtensorMap tq, tk, tv;
+    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
+        return cudaErrorInvalidValue;
     dim3 grid((T + kTile - 1) / kTile, BH);
     KATA_TRACED("quadratic_tc", s,
-                kern<<<grid, kThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q),
-                                                  static_cast<const __nv_bfloat16*>(k),
-                                                  static_cast<const __nv_bfloat16*>(v),
-                                                  static_cast<__nv_bfloat16*>(o), T));
+                kern<<<grid, kThreads, kSmem, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), T));
     return cudaGetLastError();
 }
 
