@@ -12,13 +12,13 @@
 // denominator alike and cancels.  Scores of unit keys with a fixed query are
 // bounded, so no running maximum or rescale is needed.
 //
-// Pipeline (one CTA per query tile, 384 threads):
+// Pipeline (one CTA per query tile, 512 threads):
 //   warp 0 lane 0   TMA: the query tile once, key and value tiles into a ring
 //                   of kStages stages
 //   warp 1 lane 0   issues every MMA: S(j+1) before O(j), so the squaring of
 //                   tile j overlaps the score product of tile j+1
-//   warps 2-3       put the keys of each staged tile on the unit sphere, in
-//                   place (thread = two key rows)
+//   warps 12-15     put the keys of each staged tile on the unit sphere, in
+//                   place (thread = key row)
 //   warps 4-7, 8-11 two squaring groups, one per score buffer (tiles of even
 //                   and odd index); warps 4-7 also write o at the end
 #include <cuda_bf16.h>
@@ -37,7 +37,7 @@ using namespace tc;
 __device__ unsigned int g_quad_tc_status = 0;
 
 constexpr int kTile = 128;        // queries per CTA, keys per tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kStages = 3;        // key / value ring
 constexpr uint32_t kAtom = 128 * 128;
 constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value slots, the ones column, pad
@@ -72,7 +72,7 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&v_full[s], 1);
-            mbar_init(&k_ready[s], 64);
+            mbar_init(&k_ready[s], 128);
             mbar_init(&kv_free[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -170,16 +170,14 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         mma_commit(&o_done);
         mma_commit(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp >= 12) {
         // =============================================================== key normalisation
-        const int lt = t - 64;
+        const int r = t - 384;
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages;
             if (!wait(&k_full[st], (j / kStages) & 1)) { fail(); break; }
             uint8_t* kb = sm + kKOff + st * kAtom;
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = 2 * lt + rr;
+            {
                 uint4 raw[P / 8];
                 float ss = 0.f;
 #pragma unroll
@@ -207,7 +205,7 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             fence_proxy_async_smem();
             mbar_arrive(&k_ready[st]);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // =============================================================== squaring groups
         const int b = warp >= 8 ? 1 : 0;
         const int e = t & 127;          // query row = tensor-memory lane
