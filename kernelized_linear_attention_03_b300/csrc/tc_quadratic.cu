@@ -12,15 +12,18 @@
 // denominator alike and cancels.  Scores of unit keys with a fixed query are
 // bounded, so no running maximum or rescale is needed.
 //
-// Pipeline (one CTA per query tile, 512 threads):
-//   warp 0 lane 0   TMA: the query tile once, key and value tiles into a ring
-//                   of kStages stages
-//   warp 1 lane 0   issues every MMA: S(j+1) before O(j), so the squaring of
-//                   tile j overlaps the score product of tile j+1
+// Pipeline (one CTA per pair of query tiles A = 2m, B = 2m + 1, sharing
+// every key / value tile they both need; 512 threads):
+//   warp 0 lane 0   TMA: both query tiles once, key and value tiles into a
+//                   ring of kStages stages
+//   warp 1 lane 0   issues every MMA, alternating the two query tiles:
+//                   O_A(j), S_A(j+1), O_B(j), S_B(j+1), ... so that the
+//                   squaring of one tile's scores overlaps the other tile's
+//                   products
+//   warps 4-7       squaring group of query tile A (and its o at the end)
+//   warps 8-11      squaring group of query tile B (and its o at the end)
 //   warps 12-15     put the keys of each staged tile on the unit sphere, in
 //                   place (thread = key row)
-//   warps 4-7, 8-11 two squaring groups, one per score buffer (tiles of even
-//                   and odd index); warps 4-7 also write o at the end
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -36,20 +39,20 @@ using namespace tc;
 
 __device__ unsigned int g_quad_tc_status = 0;
 
-constexpr int kTile = 128;        // queries per CTA, keys per tile
+constexpr int kTile = 128;        // queries per tile, keys per tile
 constexpr int kThreads = 512;
 constexpr int kStages = 3;        // key / value ring
 constexpr uint32_t kAtom = 128 * 128;
 constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value slots, the ones column, pad
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every device-side wait
 
-// shared memory, 16 KB atoms from a 1024-byte aligned base: Q, K[kStages],
-// V[kStages], the ones atom (last, so every value stage reaches it with a
-// positive atom stride)
-constexpr uint32_t kQOff = 0, kKOff = kAtom, kVOff = (1 + kStages) * kAtom, kOnesOff = (1 + 2 * kStages) * kAtom;
-constexpr size_t kSmem = (2 + 2 * kStages) * kAtom + 1024;
-// tensor memory: two score buffers, O
-constexpr uint32_t kTmS = 0, kTmO = 256;
+// shared memory, 16 KB atoms from a 1024-byte aligned base: Q_A, Q_B,
+// K[kStages], V[kStages], the ones atom (last, so every value stage reaches
+// it with a positive atom stride)
+constexpr uint32_t kQOff = 0, kKOff = 2 * kAtom, kVOff = (2 + kStages) * kAtom, kOnesOff = (2 + 2 * kStages) * kAtom;
+constexpr size_t kSmem = (3 + 2 * kStages) * kAtom + 1024;
+// tensor memory: scores (then squared weights, in place) and O per query tile
+constexpr uint32_t kTmS = 0, kTmO = 256;  // tile g: S at 128 g, O at 256 + 128 g
 
 template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -57,15 +60,19 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int T) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_ready[kStages], kv_free[kStages];
-    __shared__ uint64_t s_full[2], p_full[2], s_free[2], o_done, drain;
+    __shared__ uint64_t s_full[2], p_full[2], o_done, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int t = threadIdx.x, warp = t >> 5;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest query tiles first
+    const int m = gridDim.x - 1 - blockIdx.x;  // heaviest pairs first
     const int64_t bh = blockIdx.y;
-    const int nj = qt + 1;                      // key tiles up to the diagonal
+    const int ntiles = (T + kTile - 1) / kTile;
+    const int qa = 2 * m, qb = 2 * m + 1;
+    const bool has_b = qb < ntiles;
+    const int last[2] = {qa, has_b ? qb : -1};  // last key tile of each query tile
+    const int nj = has_b ? qb + 1 : qa + 1;     // key tiles loaded
 
     if (t == 0) {
         mbar_init(&q_full, 1);
@@ -75,10 +82,9 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_init(&k_ready[s], 128);
             mbar_init(&kv_free[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128);
-            mbar_init(&s_free[b], 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&s_full[g], 1);
+            mbar_init(&p_full[g], 128);
         }
         mbar_init(&o_done, 1);
         mbar_init(&drain, 1);
@@ -113,8 +119,9 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
-        mbar_arrive_expect_tx(&q_full, kAtom);
-        tma_load_3d(sm + kQOff, &tmq, 0, qt * kTile, (int)bh, &q_full);
+        mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * kAtom);
+        tma_load_3d(sm + kQOff, &tmq, 0, qa * kTile, (int)bh, &q_full);
+        if (has_b) tma_load_3d(sm + kQOff + kAtom, &tmq, 0, qb * kTile, (int)bh, &q_full);
         int issued = 0;
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages, use = j / kStages;
@@ -135,36 +142,41 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // =============================================================== MMA issuer
         constexpr uint32_t id_s = idesc_bf16_f32(kTile, kTile);
         constexpr uint32_t id_o = idesc_bf16_f32_major(kTile, kNV, false, true);
-        const uint64_t d_q = sdesc_kmajor_sw128(smem_u32(sm + kQOff));
-        auto issue_s = [&](int j) -> bool {
-            const int st = j % kStages, b = j & 1;
+        // scores of query tile g against key tile j (P in place of S afterwards)
+        auto issue_s = [&](int g, int j) -> bool {
+            const int st = j % kStages;
             if (!mbar_wait(&k_ready[st], (j / kStages) & 1, &abort_flag, kWaitNs)) return false;
-            if (j >= 2 && !mbar_wait(&s_free[b], ((j - 2) >> 1) & 1, &abort_flag, kWaitNs)) return false;
             tc_fence_after();
+            const uint64_t d_q = sdesc_kmajor_sw128(smem_u32(sm + kQOff + g * kAtom));
             const uint64_t d_k = sdesc_kmajor_sw128(smem_u32(sm + kKOff + st * kAtom));
 #pragma unroll
-            for (int ks = 0; ks < P / 16; ++ks) mma_ss(tb + kTmS + 128 * b, d_q + 2 * ks, d_k + 2 * ks, id_s, ks > 0 ? 1u : 0u);
-            mma_commit(&s_full[b]);
+            for (int ks = 0; ks < P / 16; ++ks)
+                mma_ss(tb + kTmS + 128 * g, d_q + 2 * ks, d_k + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+            mma_commit(&s_full[g]);
             return true;
         };
-        bool ok = mbar_wait(&q_full, 0, &abort_flag, kWaitNs) && issue_s(0);
-        for (int j = 0; ok && j < nj; ++j) {
-            const int st = j % kStages, b = j & 1;
-            if (j + 1 < nj && !issue_s(j + 1)) { ok = false; break; }
-            if (!mbar_wait(&p_full[b], (j >> 1) & 1, &abort_flag, kWaitNs) ||
-                !mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag, kWaitNs)) {
-                ok = false;
-                break;
-            }
+        // O_g += P_g [V_j | 1]; then the next scores of tile g (they overwrite P_g)
+        auto issue_o = [&](int g, int j) -> bool {
+            const int st = j % kStages;
+            if (!mbar_wait(&p_full[g], j & 1, &abort_flag, kWaitNs) ||
+                !mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag, kWaitNs))
+                return false;
             tc_fence_after();
             // B = [value tile | ones]: two MN atoms, the ones atom kOnesOff - value stage bytes away
             const uint32_t vaddr = smem_u32(sm + kVOff + st * kAtom);
             const uint64_t d_v = sdesc_mnmajor_sw128(vaddr, (uint32_t)(kOnesOff - (kVOff + st * kAtom)));
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ts(tb + kTmO, tb + kTmS + 128 * b + 8 * ks, d_v + ks * (2048 >> 4), id_o, (j > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&kv_free[st]);
-            mma_commit(&s_free[b]);
+                mma_ts(tb + kTmO + 128 * g, tb + kTmS + 128 * g + 8 * ks, d_v + ks * (2048 >> 4), id_o,
+                       (j > 0 || ks > 0) ? 1u : 0u);
+            if (j + 1 <= last[g]) return issue_s(g, j + 1);
+            return true;
+        };
+        bool ok = mbar_wait(&q_full, 0, &abort_flag, kWaitNs) && issue_s(0, 0) && (!has_b || issue_s(1, 0));
+        for (int j = 0; ok && j < nj; ++j) {
+            if (j <= last[0] && !issue_o(0, j)) { ok = false; break; }
+            if (j <= last[1] && !issue_o(1, j)) { ok = false; break; }
+            mma_commit(&kv_free[j % kStages]);  // both tiles' products with key / value tile j are issued
         }
         if (!ok) fail();
         mma_commit(&o_done);
@@ -177,45 +189,43 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int st = j % kStages;
             if (!wait(&k_full[st], (j / kStages) & 1)) { fail(); break; }
             uint8_t* kb = sm + kKOff + st * kAtom;
-            {
-                uint4 raw[P / 8];
-                float ss = 0.f;
+            uint4 raw[P / 8];
+            float ss = 0.f;
 #pragma unroll
-                for (int c = 0; c < P / 8; ++c) {
-                    raw[c] = *reinterpret_cast<const uint4*>(kb + sw128_chunk(r, 8 * c, kTile));
-                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
+            for (int c = 0; c < P / 8; ++c) {
+                raw[c] = *reinterpret_cast<const uint4*>(kb + sw128_chunk(r, 8 * c, kTile));
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float x = __bfloat162float(e[i]);
-                        ss = fmaf(x, x, ss);
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const float x = __bfloat162float(e[i]);
+                    ss = fmaf(x, x, ss);
                 }
-                const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            }
+            const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
 #pragma unroll
-                for (int c = 0; c < P / 8; ++c) {
-                    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
-                    uint4 w;
-                    w.x = pack_bf16x2(__bfloat162float(e[0]) * inv, __bfloat162float(e[1]) * inv);
-                    w.y = pack_bf16x2(__bfloat162float(e[2]) * inv, __bfloat162float(e[3]) * inv);
-                    w.z = pack_bf16x2(__bfloat162float(e[4]) * inv, __bfloat162float(e[5]) * inv);
-                    w.w = pack_bf16x2(__bfloat162float(e[6]) * inv, __bfloat162float(e[7]) * inv);
-                    *reinterpret_cast<uint4*>(kb + sw128_chunk(r, 8 * c, kTile)) = w;
-                }
+            for (int c = 0; c < P / 8; ++c) {
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
+                uint4 w;
+                w.x = pack_bf16x2(__bfloat162float(e[0]) * inv, __bfloat162float(e[1]) * inv);
+                w.y = pack_bf16x2(__bfloat162float(e[2]) * inv, __bfloat162float(e[3]) * inv);
+                w.z = pack_bf16x2(__bfloat162float(e[4]) * inv, __bfloat162float(e[5]) * inv);
+                w.w = pack_bf16x2(__bfloat162float(e[6]) * inv, __bfloat162float(e[7]) * inv);
+                *reinterpret_cast<uint4*>(kb + sw128_chunk(r, 8 * c, kTile)) = w;
             }
             fence_proxy_async_smem();
             mbar_arrive(&k_ready[st]);
         }
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp >= 4) {
         // =============================================================== squaring groups
-        const int b = warp >= 8 ? 1 : 0;
-        const int e = t & 127;          // query row = tensor-memory lane
-        const int wq = (warp & 3);      // this warp's rows are 32 wq .. 32 wq + 31
+        const int g = warp >= 8 ? 1 : 0;  // query tile A or B
+        const int e = t & 127;            // query row = tensor-memory lane
+        const int wq = (warp & 3);        // this warp's rows are 32 wq .. 32 wq + 31
         const uint32_t lane0 = (uint32_t)(wq * 32);
-        const uint32_t sb = tb + kTmS + 128 * b;
-        for (int j = b; j < nj; j += 2) {
-            if (!wait(&s_full[b], (j >> 1) & 1)) { fail(); break; }
+        const uint32_t sb = tb + kTmS + 128 * g;
+        for (int j = 0; j <= last[g]; ++j) {
+            if (!wait(&s_full[g], j & 1)) { fail(); break; }
             tc_fence_after();
-            const bool diag = j == qt;  // keys past the query are masked only on the diagonal tile
+            const bool diag = j == last[g];  // keys past the query are masked only on the diagonal tile
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t pk[16];
@@ -244,33 +254,32 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            mbar_arrive(&p_full[g]);
         }
-        if (b == 0) {
-            // ---- o = O[:, :DV] / O[:, 64]
-            const bool ok = wait(&o_done, 0) && !abort_flag;
-            tc_fence_after();
-            if (ok) {
-                const int qi = qt * kTile + e;
-                uint32_t r[16];
-                tmem_ld16(tmem_addr(tb + kTmO, lane0, 64), r);
+        // ---- o = O[:, :DV] / O[:, 64]
+        const bool ok = wait(&o_done, 0) && !abort_flag;
+        tc_fence_after();
+        const int qi = (g == 0 ? qa : qb) * kTile + e;
+        if (ok && last[g] >= 0) {
+            const uint32_t ob = tb + kTmO + 128 * g;
+            uint32_t r[16];
+            tmem_ld16(tmem_addr(ob, lane0, 64), r);
+            tmem_wait_ld();
+            const float den = __uint_as_float(r[0]);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 16) {
+                tmem_ld16(tmem_addr(ob, lane0, c0), r);
                 tmem_wait_ld();
-                const float den = __uint_as_float(r[0]);
-                const float inv = den > 0.f ? 1.f / den : 0.f;
+                if (qi < T) {
+                    uint4 out[2];
+                    uint32_t* w = reinterpret_cast<uint32_t*>(out);
 #pragma unroll
-                for (int c0 = 0; c0 < DV; c0 += 16) {
-                    tmem_ld16(tmem_addr(tb + kTmO, lane0, c0), r);
-                    tmem_wait_ld();
-                    if (qi < T) {
-                        uint4 out[2];
-                        uint32_t* w = reinterpret_cast<uint32_t*>(out);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-                        __nv_bfloat16* dst = o + (bh * T + qi) * (int64_t)DV + c0;
-                        reinterpret_cast<uint4*>(dst)[0] = out[0];
-                        reinterpret_cast<uint4*>(dst)[1] = out[1];
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                    __nv_bfloat16* dst = o + (bh * T + qi) * (int64_t)DV + c0;
+                    reinterpret_cast<uint4*>(dst)[0] = out[0];
+                    reinterpret_cast<uint4*>(dst)[1] = out[1];
                 }
             }
         }
@@ -290,7 +299,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, i
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
-    dim3 grid((T + kTile - 1) / kTile, BH);
+    dim3 grid(((T + kTile - 1) / kTile + 1) / 2, BH);
     KATA_TRACED("quadratic_tc", s,
                 kern<<<grid, kThreads, kSmem, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), T));
     return cudaGetLastError();
