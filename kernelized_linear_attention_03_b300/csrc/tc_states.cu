@@ -6,13 +6,18 @@
 // the chunked-scan paragraph's state kernel).
 //
 // One CTA owns one 128-slot tile of the packed lift for a run of segments
-// of one head.  Per block of up to 128 tokens: every thread puts its key on
-// the unit sphere, writes its 128 lifted coordinates of the tile into a
-// token-major (MN-major for the MMA) swizzled tile, and its value row with a
-// trailing ones column into a token-major [V | 1] tile; one thread issues
-//   D[slots x (dv+16)] += psiK(K)^T [V | 1]     (tcgen05, D in TMEM)
-// with K = tokens.  At the end of a segment the tile's rows are written out
-// in the C ABI's sqrt(2)-packed order.
+// of one head; blocks of up to 128 tokens stream through a pipeline
+// (384 threads):
+//   warp 0 lane 0   TMA: key and value rows of each block into a ring of
+//                   kStages stages
+//   warp 1 lane 0   issues D[slots x 80] += psiK(K)^T [V | 1] per block (K =
+//                   tokens; B = the value tile and a constant ones atom), two
+//                   accumulators in tensor memory alternating by segment
+//   warps 4-7       thread = token: unit key, the tile's lifted coordinates
+//                   into a token-major (MN-major for the MMA) swizzled tile,
+//                   double-buffered
+//   warps 8-11      at each segment end, thread = slot: the accumulator row
+//                   out in the C ABI's sqrt(2)-packed order
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -20,6 +25,7 @@
 #include "kata_internal.h"
 #include "tc_lift.cuh"
 #include "tc_primitives.cuh"
+#include "tc_tma.cuh"
 
 namespace kata {
 namespace {
@@ -28,19 +34,20 @@ using namespace tc;
 
 __device__ unsigned int g_states_tc_status = 0;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 384;
+constexpr int kStages = 2;
 constexpr float kSqrt2f = 1.41421356237309504880f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // one MN atom: 128 K-rows (tokens) x 128 bytes
-
-template <int DV>
-struct StatesLayout {
-    static constexpr int NB = DV + 16;                       // [V | 1 | 0 pad] columns
-    static constexpr int b_atoms = (NB + 63) / 64;
-    static constexpr uint32_t a_off = 0, b_off = 2 * kAtom;  // A: two 64-slot atoms
-    static constexpr uint32_t total = b_off + b_atoms * kAtom;
-    static constexpr size_t smem = total + 1024;
-};
+constexpr uint32_t kNB = 80;           // B columns: 64 value slots, the ones column, pad
+// shared memory from a 1024-byte aligned base: A[2] (two 64-slot atoms
+// each), K[kStages], V[kStages], the ones atom (last: every value stage
+// reaches it with a positive atom stride), then the output staging (128
+// rows of 64 fp32, each row padded by 16 bytes)
+constexpr uint32_t kAOff = 0, kKOff = 4 * kAtom, kVOff = (4 + kStages) * kAtom,
+                   kOnesOff = (4 + 2 * kStages) * kAtom, kOutOff = (5 + 2 * kStages) * kAtom;
+constexpr uint32_t kOutRow = 64 * 4 + 16;
+constexpr size_t kSmem = kOutOff + 128 * kOutRow + 1024;
 
 // Lifted key coordinates of tile TAU for this thread's token into row `row`
 // of the token-major A tile.
@@ -68,69 +75,147 @@ __device__ __forceinline__ void key_tile_dispatch(int tau, const uint32_t (&u)[P
 }
 
 template <int P, int DV>
-__global__ void __launch_bounds__(kThreads)
-states_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                 float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS,
-                 int NS_out, int segs_per_cta) {
-    // T: tokens per head (row stride and bound); segments 0..NS-1 of L tokens
-    // are computed (NS may cover fewer than all T tokens) into rows of a
-    // [BH, NS_out, n] layout.
-    using Lay = StatesLayout<DV>;
-    constexpr int NB = Lay::NB;
+__global__ void __launch_bounds__(kThreads, 1)
+states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                 float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS, int NS_out,
+                 int segs_per_cta) {
+    // T: tokens per head; segments 0..NS-1 of L tokens (L a multiple of 128,
+    // or L <= 128) are computed into rows of a [BH, NS_out, n] layout.
     constexpr int n = lift::packed_n(P);
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t k_full[kStages], v_full[kStages], kv_free[kStages], a_full[2], a_free[2];
+    __shared__ uint64_t acc_full[2], acc_free[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* As = sm + Lay::a_off;
-    uint8_t* Bs = sm + Lay::b_off;
 
     const int t = threadIdx.x, warp = t >> 5;
     const int tau = blockIdx.x;
     const int64_t bh = blockIdx.z;
     const int seg0 = blockIdx.y * segs_per_cta;
     const int seg1 = min(NS, seg0 + segs_per_cta);
-    const __nv_bfloat16* kh = k + bh * (int64_t)T * P;
-    const __nv_bfloat16* vh = v + bh * (int64_t)T * DV;
+    const int bl = L < 128 ? L : 128;  // tokens per block
+    const int tok0 = seg0 * L, tok1 = min(T, seg1 * L);
+    const int nblk = tok1 > tok0 ? (tok1 - tok0 + bl - 1) / bl : 0;
+    // block i: tokens [b0, b1) of segment seg
+    auto block = [&](int i, int& b0, int& b1, int& seg) {
+        b0 = tok0 + i * bl;
+        seg = b0 / L;
+        b1 = min(min(T, (seg + 1) * L), b0 + bl);
+    };
 
     if (t == 0) {
-        mbar_init(&bar, 1);
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&k_full[st], 1);
+            mbar_init(&v_full[st], 1);
+            mbar_init(&kv_free[st], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&a_full[b], 128);
+            mbar_init(&a_free[b], 1);
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_free[b], 128);
+        }
+        mbar_init(&drain, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 128);
+        tmem_alloc(&tmem_base, 256);
         tmem_relinquish();
     }
+    for (int r = t; r < 128; r += kThreads)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sm + kOnesOff + mn_sw128_chunk(8 * c, r, kAtom)) =
+                make_uint4(c == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t d_tm = tmem_base;
-    const uint32_t lane0 = (uint32_t)(warp * 32);
-    uint32_t phase = 0;
-    bool ok = true;
+    const uint32_t tb = tmem_base;
+    auto fail = [&]() {
+        abort_flag = 1;
+        atomicOr(&g_states_tc_status, kStatusTimeout);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag, kWaitNs));
+    };
 
-    for (int seg = seg0; seg < seg1 && ok; ++seg) {
-        const int s_begin = seg * L, s_end = min(T, s_begin + L);
-        bool first = true;
-        for (int b0 = s_begin; b0 < s_end; b0 += 128) {
-            const int b1 = min(s_end, b0 + 128);
-            const int tok = b0 + t;
-            const bool valid = tok < b1;
-            // ---- unit key, lifted tile coordinates -> A (token-major)
+    if (t == 0) {
+        // =============================================================== TMA producer
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        int issued = 0;
+        for (int i = 0; i < nblk; ++i) {
+            const int st = i % kStages, use = i / kStages;
+            int b0, b1, seg;
+            block(i, b0, b1, seg);
+            if (i >= kStages && !mbar_wait(&kv_free[st], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&k_full[st], kAtom);
+            tma_load_3d(sm + kKOff + st * kAtom, &tmk, 0, b0, (int)bh, &k_full[st]);
+            mbar_arrive_expect_tx(&v_full[st], kAtom);
+            tma_load_3d(sm + kVOff + st * kAtom, &tmv, 0, b0, (int)bh, &v_full[st]);
+            issued = i + 1;
+        }
+        // no copy may still be landing in shared memory when the CTA exits
+        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+            mbar_wait_quiet(&k_full[i % kStages], (i / kStages) & 1, kWaitNs);
+            mbar_wait_quiet(&v_full[i % kStages], (i / kStages) & 1, kWaitNs);
+        }
+    } else if (t == 32) {
+        // =============================================================== MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32_major(128, kNB, true, true);
+        bool ok = true;
+        for (int i = 0; i < nblk; ++i) {
+            const int st = i % kStages, ab = i & 1;
+            int b0, b1, seg;
+            block(i, b0, b1, seg);
+            const int sl = seg - seg0, acb = sl & 1;
+            const bool first = b0 == seg * L, last = b1 == min(T, (seg + 1) * L);
+            if (!mbar_wait(&a_full[ab], (i >> 1) & 1, &abort_flag, kWaitNs) ||
+                !mbar_wait(&v_full[st], (i / kStages) & 1, &abort_flag, kWaitNs) ||
+                (first && sl >= 2 && !mbar_wait(&acc_free[acb], ((sl - 2) >> 1) & 1, &abort_flag, kWaitNs))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t d_a = sdesc_mnmajor_sw128(smem_u32(sm + kAOff + 2 * ab * kAtom), kAtom);
+            const uint64_t d_b = sdesc_mnmajor_sw128(smem_u32(sm + kVOff + st * kAtom),
+                                                     (uint32_t)(kOnesOff - (kVOff + st * kAtom)));
+            const int steps = (b1 - b0 + 15) / 16;
+            for (int ks = 0; ks < steps; ++ks)
+                mma_ss(tb + 128 * acb, d_a + ks * (2048 >> 4), d_b + ks * (2048 >> 4), idesc,
+                       (first && ks == 0) ? 0u : 1u);
+            mma_commit(&a_free[ab]);
+            mma_commit(&kv_free[st]);
+            if (last) mma_commit(&acc_full[acb]);
+        }
+        if (!ok) fail();
+        mma_commit(&drain);
+        mbar_wait_quiet(&drain, 0, kWaitNs);
+    } else if (warp >= 4 && warp < 8) {
+        // =============================================================== lift warps
+        const int lt = t - 128;
+        for (int i = 0; i < nblk; ++i) {
+            const int st = i % kStages, ab = i & 1;
+            int b0, b1, seg;
+            block(i, b0, b1, seg);
+            const bool valid = b0 + lt < b1;
+            if (!wait(&k_full[st], (i / kStages) & 1)) { fail(); break; }
+            if (i >= 2 && !wait(&a_free[ab], ((i - 2) >> 1) & 1)) { fail(); break; }
+            const uint8_t* kb = sm + kKOff + st * kAtom;
             uint32_t u[P / 2];
             {
                 uint4 raw[P / 8];
                 float ss = 0.f;
 #pragma unroll
                 for (int c = 0; c < P / 8; ++c) {
-                    raw[c] = valid ? *reinterpret_cast<const uint4*>(kh + (int64_t)tok * P + 8 * c)
-                                   : make_uint4(0, 0, 0, 0);
+                    raw[c] = valid ? *reinterpret_cast<const uint4*>(kb + sw128_chunk(lt, 8 * c, 128)) : make_uint4(0, 0, 0, 0);
                     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float x = __bfloat162float(e[i]);
+                    for (int j = 0; j < 8; ++j) {
+                        const float x = __bfloat162float(e[j]);
                         ss = fmaf(x, x, ss);
                     }
                 }
@@ -139,101 +224,84 @@ states_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __res
                 for (int c = 0; c < P / 8; ++c) {
                     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        u[4 * c + i] = pack_bf16x2(__bfloat162float(e[2 * i]) * inv,
-                                                   __bfloat162float(e[2 * i + 1]) * inv);
+                    for (int j = 0; j < 4; ++j)
+                        u[4 * c + j] = pack_bf16x2(__bfloat162float(e[2 * j]) * inv, __bfloat162float(e[2 * j + 1]) * inv);
                 }
             }
-            key_tile_dispatch<P>(tau, u, As, t);
-            // ---- [V | 1 | 0] row -> B (token-major)
-#pragma unroll
-            for (int c = 0; c < DV / 8; ++c) {
-                const uint4 val = valid ? *reinterpret_cast<const uint4*>(vh + (int64_t)tok * DV + 8 * c)
-                                        : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(Bs + mn_sw128_chunk(8 * c, t, kAtom)) = val;
-            }
-            *reinterpret_cast<uint4*>(Bs + mn_sw128_chunk(DV, t, kAtom)) =
-                make_uint4(valid ? pack_bf16x2(1.f, 0.f) : 0u, 0, 0, 0);
-            *reinterpret_cast<uint4*>(Bs + mn_sw128_chunk(DV + 8, t, kAtom)) = make_uint4(0, 0, 0, 0);
+            key_tile_dispatch<P>(tau, u, sm + kAOff + 2 * ab * kAtom, lt);
             fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            // ---- D += psiK^T [V | 1] over this block's tokens
-            if (t == 0) {
-                tc_fence_after();
-                constexpr uint32_t idesc = idesc_bf16_f32_major(128, NB, true, true);
-                const int steps = (b1 - b0 + 15) / 16;
-                for (int ks = 0; ks < steps; ++ks)
-                    mma_ss(d_tm, sdesc_mnmajor_sw128(smem_u32(As) + ks * 2048, kAtom),
-                           sdesc_mnmajor_sw128(smem_u32(Bs) + ks * 2048, kAtom), idesc,
-                           (first && ks == 0) ? 0u : 1u);
-                mma_commit(&bar);
-            }
-            first = false;
-            ok = mbar_wait(&bar, phase, &abort_flag, kWaitNs);
-            phase ^= 1;
-            if (!ok) abort_flag = 1;
-            if (!__syncthreads_and(ok)) {
-                ok = false;
-                break;
-            }
+            mbar_arrive(&a_full[ab]);
+        }
+    } else if (warp >= 8) {
+        // =============================================================== epilogue warps
+        // thread e reads accumulator row e (slot tau*128 + e); the rows go out
+        // through shared memory so that each canonical row (DV contiguous
+        // floats) is written by one warp store
+        const int e = t - 256, ew = e >> 5, lane = e & 31;
+        const uint32_t lane0 = (uint32_t)((warp & 3) * 32);
+        const int slot = tau * 128 + e;
+        int ci = 0, cj = 0;
+        if (slot < n) lift::slot_coord(P, slot, ci, cj);
+        const float f = ci < cj ? kSqrt2f : 1.f;
+        const int my_canon = slot < n ? lift::canonical_index(P, ci, cj) : -1;
+        uint8_t* stage = sm + kOutOff;
+        for (int seg = seg0; seg < seg1; ++seg) {
+            if (seg * L >= T) break;
+            const int sl = seg - seg0, acb = sl & 1;
+            if (!wait(&acc_full[acb], (sl >> 1) & 1)) { fail(); break; }
             tc_fence_after();
-        }
-        if (!ok) break;
-        // ---- write the segment's tile rows in the sqrt(2)-packed order
-        const int slot = tau * 128 + t;
-        uint32_t r[NB];
+            uint32_t r[80];
 #pragma unroll
-        for (int c0 = 0; c0 < NB; c0 += 16) {
-            uint32_t q[16];
-            tmem_ld16(tmem_addr(d_tm, lane0, c0), q);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[c0 + i] = q[i];
-        }
-        tmem_wait_ld();
-        if (slot < n) {
-            int i = 0, j = 0;
-            lift::slot_coord(P, slot, i, j);
-            const float f = i < j ? kSqrt2f : 1.f;
-            const int64_t row = (bh * NS_out + seg) * (int64_t)n + lift::canonical_index(P, i, j);
-            float4* dst = reinterpret_cast<float4*>(S_out + row * DV);
+            for (int c0 = 0; c0 < 80; c0 += 16) tmem_ld16(tmem_addr(tb + 128 * acb, lane0, c0), *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&acc_free[acb]);
+            const int64_t base = (bh * NS_out + seg) * (int64_t)n;
+            if (slot < n) z_out[base + my_canon] = f * __uint_as_float(r[64]);
+            // this warp's 32 rows: stage, then one 8-byte-per-lane store per row
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < DV / 4; ++c)
-                dst[c] = make_float4(f * __uint_as_float(r[4 * c]), f * __uint_as_float(r[4 * c + 1]),
-                                     f * __uint_as_float(r[4 * c + 2]), f * __uint_as_float(r[4 * c + 3]));
-            z_out[row] = f * __uint_as_float(r[DV]);
+                *reinterpret_cast<float4*>(stage + e * kOutRow + 16 * c) =
+                    make_float4(f * __uint_as_float(r[4 * c]), f * __uint_as_float(r[4 * c + 1]),
+                                f * __uint_as_float(r[4 * c + 2]), f * __uint_as_float(r[4 * c + 3]));
+            __syncwarp();
+            for (int rr = 0; rr < 32; ++rr) {
+                const int canon = __shfl_sync(0xffffffffu, my_canon, rr);
+                if (canon < 0) continue;
+                const uint8_t* src = stage + (32 * ew + rr) * kOutRow;
+                float* dst = S_out + (base + canon) * DV;
+                if (DV == 64) {
+                    reinterpret_cast<float2*>(dst)[lane] = *reinterpret_cast<const float2*>(src + 8 * lane);
+                } else if (lane < DV) {
+                    dst[lane] = *reinterpret_cast<const float*>(src + 4 * lane);
+                }
+            }
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
-    if (!ok) {
-        if (t == 0) atomicOr(&g_states_tc_status, kStatusTimeout);
-        mbar_wait_quiet(&bar, phase ^ 1, kWaitNs / 4);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(d_tm, 128);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tb, 256);
 }
 
 template <int P, int DV>
 cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_out, int BH, int T, int L,
                          int NS, int NS_out, cudaStream_t s) {
-    constexpr size_t smem = StatesLayout<DV>::smem;
     auto kern = states_tc_kernel<P, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
+    CUtensorMap tk, tv;
+    if (!rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH)) return cudaErrorInvalidValue;
     const int tiles = lift::tiles_of(P);
-    // a few segments per CTA, enough CTAs for several waves
-    const int64_t work = (int64_t)tiles * NS * BH;
-    int per = (int)((work + 148 * 8 - 1) / (148 * 8));
-    per = per < 1 ? 1 : (per > 64 ? 64 : per);
-    const int groups = (NS + per - 1) / per;
+    // about two CTAs per SM in total, each a run of segments
+    const int64_t units = (int64_t)tiles * BH;
+    int groups = (int)((2 * 148) / (units > 0 ? units : 1));
+    groups = groups < 1 ? 1 : (groups > NS ? NS : groups);
+    const int per = (NS + groups - 1) / groups;
+    groups = (NS + per - 1) / per;
     dim3 grid(tiles, groups, BH);
-    KATA_TRACED("states_tc", s,
-                kern<<<grid, kThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(k),
-                                                  static_cast<const __nv_bfloat16*>(v), S_out, z_out, T,
-                                                  L, NS, NS_out, per));
+    KATA_TRACED("states_tc", s, kern<<<grid, kThreads, kSmem, s>>>(tk, tv, S_out, z_out, T, L, NS, NS_out, per));
     return cudaGetLastError();
 }
 
