@@ -76,8 +76,11 @@ def kernel_work(name, w, form="chunked"):
     if name == "states_tc" and form == "chunk_state_scan":
         return "flop", bht * 2 * w.n * (w.dv + 1)
     if name == "chunked_tc":
-        # the fused forward does all of the forward's algorithmic work
-        return "flop", flops_forward(w)
+        # the fused forward: state build and readout with the normaliser column
+        return "flop", bht * 4 * w.n * (w.dv + 1)
+    if name == "intra_tc":
+        # the causal intra-chunk half of the forward
+        return "flop", bht * (w.C + 1) * (w.p + w.dv)
     if name == "states_tc":
         # segment start states: recomputed work, no algorithmic share
         return "flop", 0
