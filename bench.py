@@ -74,7 +74,8 @@ def kernel_work(name, w, form="chunked"):
         # causal half of the flash-style form: (T+1)(p+dv) per head-token
         return "flop", bht * (w.T + 1) * (w.p + w.dv)
     if name == "states_tc" and form == "chunk_state_scan":
-        return "flop", bht * 2 * w.n * (w.dv + 1)
+        # every chunk state is written once (fp32), the keys and values read once
+        return "byte", w.B * w.H * w.NC * w.n * (w.dv + 1) * 4 + bht * (w.p + w.dv) * 2
     if name == "chunked_tc":
         # the fused forward: state build and readout with the normaliser column
         return "flop", bht * 4 * w.n * (w.dv + 1)

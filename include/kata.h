@@ -64,8 +64,10 @@ typedef enum {
 
 typedef enum { KATA_FP32 = 0, KATA_BF16 = 1 } kata_dtype;
 
-/* Inter-chunk prefix: one step per chunk, or a log-depth scan taking
- * ceil(log2 N_C) rounds of N_C-wide work (chunked-scan paragraph). */
+/* Inter-chunk prefix: one step per chunk, or a log-depth tree scan
+ * (chunked-scan paragraph): ceil(log2 N_C) levels for N_C up to 256 chunks;
+ * longer sequences run one such tree per 256-chunk window, each window
+ * starting from the previous one's total. */
 typedef enum { KATA_SCAN_SEQUENTIAL = 0, KATA_SCAN_TREE = 1 } kata_scan_mode;
 
 /* n = p(p+1)/2, the packed width of the rank-one lift (Eq. 8); -1 if p < 0. */

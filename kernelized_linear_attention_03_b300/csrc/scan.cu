@@ -4,9 +4,10 @@
 //   * sequentially: one thread per 4 state elements walks the N_C chunks
 //     (depth N_C, every element's walk independent), or
 //   * as a log-depth tree: per 16-byte column vector, a work-efficient
-//     up-sweep / down-sweep over runs of 8 chunks held in registers around
-//     a Kogge-Stone scan of the run totals in shared memory.  Chunk counts
-//     above the 1024-chunk window continue window by window from a carry.
+//     up-sweep / down-sweep over runs of 8 or 16 chunks held in registers around
+//     a Kogge-Stone scan of the run totals in shared memory (depth log2 of
+//     the 256-chunk window plus log2 of the run).  Longer sequences continue
+//     window by window from a carry.
 // Both read every element once and write it once: the pass is HBM-bound.
 #include <cstdint>
 
@@ -72,26 +73,27 @@ scan_sequential_kernel(const float* x, float* y, const float* init, float* fin, 
 }
 
 // Log-depth scan.  A block owns a tile of kTreeTPR x VEC state columns of
-// one head and a window of GROUPS x kTreeCPT consecutive chunks; thread
-// (g, cc) holds the kTreeCPT chunks 8g..8g+7 of column group cc in registers.
-//   1. up-sweep inside the thread: pairwise partial sums, 3 levels;
+// one head and a window of GROUPS x CPT consecutive chunks; thread (g, cc)
+// holds the CPT chunks CPT g .. CPT g + CPT - 1 of column group cc in
+// registers.
+//   1. up-sweep inside the thread: pairwise partial sums, log2 CPT levels;
 //   2. inclusive Kogge-Stone over the GROUPS group totals in shared memory,
 //      log2(GROUPS) rounds, each GROUPS-wide;
 //   3. down-sweep inside the thread, giving each chunk its exclusive prefix
 //      within the group, then the group's offset is added.
-// Depth 3 + log2(GROUPS) + 3 = log2(window) + 3.  Windows beyond the first
-// (N_C above 1024) continue from a carry.  Loads and stores are full 16-byte
-// vectors along the columns, all kTreeCPT of a thread in flight at once.
+// Depth log2(CPT) + log2(GROUPS) + log2(CPT) = log2(window) + log2(CPT).
+// Windows beyond the first continue from a carry.  Loads
+// and stores are full 16-byte vectors along the columns, all CPT of a thread
+// in flight at once.
 constexpr int kTreeTPR = 4;  // threads across a tile row
-constexpr int kTreeCPT = 8;  // chunks per thread
 
-template <int VEC, int GROUPS>
+template <int VEC, int GROUPS, int CPT>
 __global__ void __launch_bounds__(GROUPS * kTreeTPR)
 scan_tree_kernel(const float* x, float* y, const float* init, float* fin, int64_t NC, int64_t W,
                  int64_t tiles) {
     using V = Vec<VEC>;
     using T = typename V::T;
-    constexpr int kWin = GROUPS * kTreeCPT;
+    constexpr int kWin = GROUPS * CPT;
     __shared__ T part[2][GROUPS][kTreeTPR];
     const int64_t h = blockIdx.x / tiles, tile = blockIdx.x - h * tiles;
     const int g = threadIdx.x / kTreeTPR, cc = threadIdx.x % kTreeTPR;
@@ -101,19 +103,19 @@ scan_tree_kernel(const float* x, float* y, const float* init, float* fin, int64_
     const float* src = x + h * NC * W + e;
     float* dst = y + h * NC * W + e;
     for (int64_t w0 = 0; w0 < NC; w0 += kWin) {
-        const int64_t c0 = w0 + (int64_t)g * kTreeCPT;
-        T a[kTreeCPT];
+        const int64_t c0 = w0 + (int64_t)g * CPT;
+        T a[CPT];
 #pragma unroll
-        for (int m = 0; m < kTreeCPT; ++m)
+        for (int m = 0; m < CPT; ++m)
             a[m] = (col_ok && c0 + m < NC) ? *reinterpret_cast<const T*>(src + (c0 + m) * W) : V::zero();
         // up-sweep
 #pragma unroll
-        for (int st = 1; st < kTreeCPT; st <<= 1)
+        for (int st = 1; st < CPT; st <<= 1)
 #pragma unroll
-            for (int i = 2 * st - 1; i < kTreeCPT; i += 2 * st) a[i] = V::add(a[i - st], a[i]);
+            for (int i = 2 * st - 1; i < CPT; i += 2 * st) a[i] = V::add(a[i - st], a[i]);
         // group totals
         int buf = 0;
-        part[0][g][cc] = a[kTreeCPT - 1];
+        part[0][g][cc] = a[CPT - 1];
         __syncthreads();
 #pragma unroll
         for (int d = 1; d < GROUPS; d <<= 1) {
@@ -126,17 +128,17 @@ scan_tree_kernel(const float* x, float* y, const float* init, float* fin, int64_
         const T offset = V::add(carry, g > 0 ? part[buf][g - 1][cc] : V::zero());
         const T wtotal = part[buf][GROUPS - 1][cc];
         // down-sweep: exclusive prefixes within the thread
-        a[kTreeCPT - 1] = V::zero();
+        a[CPT - 1] = V::zero();
 #pragma unroll
-        for (int st = kTreeCPT / 2; st >= 1; st >>= 1)
+        for (int st = CPT / 2; st >= 1; st >>= 1)
 #pragma unroll
-            for (int i = 2 * st - 1; i < kTreeCPT; i += 2 * st) {
+            for (int i = 2 * st - 1; i < CPT; i += 2 * st) {
                 const T left = a[i - st];
                 a[i - st] = a[i];
                 a[i] = V::add(a[i], left);
             }
 #pragma unroll
-        for (int m = 0; m < kTreeCPT; ++m)
+        for (int m = 0; m < CPT; ++m)
             if (col_ok && c0 + m < NC) *reinterpret_cast<T*>(dst + (c0 + m) * W) = V::add(offset, a[m]);
         carry = V::add(carry, wtotal);
         __syncthreads();  // part[] is rewritten by the next window
@@ -144,12 +146,12 @@ scan_tree_kernel(const float* x, float* y, const float* init, float* fin, int64_
     if (fin && col_ok) *reinterpret_cast<T*>(fin + h * W + e) = carry;
 }
 
-template <int VEC, int GROUPS>
+template <int VEC, int GROUPS, int CPT>
 cudaError_t launch_tree(const float* x, float* y, const float* init, float* fin, int64_t heads, int64_t NC,
                         int64_t W, cudaStream_t s) {
     const int64_t tiles = (W + kTreeTPR * VEC - 1) / (kTreeTPR * VEC);
     KATA_TRACED("scan_tree", s,
-                (scan_tree_kernel<VEC, GROUPS><<<(unsigned)(heads * tiles), GROUPS * kTreeTPR, 0, s>>>(
+                (scan_tree_kernel<VEC, GROUPS, CPT><<<(unsigned)(heads * tiles), GROUPS * kTreeTPR, 0, s>>>(
                     x, y, init, fin, NC, W, tiles)));
     return cudaGetLastError();
 }
@@ -157,9 +159,11 @@ cudaError_t launch_tree(const float* x, float* y, const float* init, float* fin,
 template <int VEC>
 cudaError_t launch_tree_vec(const float* x, float* y, const float* init, float* fin, int64_t heads, int64_t NC,
                             int64_t W, cudaStream_t s) {
-    if (NC <= 8 * kTreeCPT) return launch_tree<VEC, 8>(x, y, init, fin, heads, NC, W, s);
-    if (NC <= 32 * kTreeCPT) return launch_tree<VEC, 32>(x, y, init, fin, heads, NC, W, s);
-    return launch_tree<VEC, 128>(x, y, init, fin, heads, NC, W, s);
+    // small blocks keep the most copies in flight per SM; sequences past 256
+    // chunks chain 256-chunk windows
+    if (NC <= 64) return launch_tree<VEC, 8, 8>(x, y, init, fin, heads, NC, W, s);
+    if (NC <= 256) return launch_tree<VEC, 32, 8>(x, y, init, fin, heads, NC, W, s);
+    return launch_tree<VEC, 16, 16>(x, y, init, fin, heads, NC, W, s);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }

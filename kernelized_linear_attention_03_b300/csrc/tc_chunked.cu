@@ -894,18 +894,18 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 // ---------------------------------------------------------------- intra-chunk part
 // Every chunk on its own (no state): for the 128 queries of a chunk,
 //   P = (Q Kh^T) o (Q Kh^T) o M   (bf16, M the causal mask s <= t)
-//   [Y | d] = P [V | 1]           (fp32 accumulation)
+//   Y = P V,  d = rowsum(P)       (fp32 accumulation)
 // Y goes out as bf16 rows [BH][T][DV] and d, the rows' intra-chunk
 // normaliser, as fp32 [BH][T]; the fused forward adds both when it combines
-// a chunk's rows.  The normaliser comes out of the same MMA as Y (the ones
-// column of B), so it sums exactly the rounded weights Y is built from.
-// One CTA per (chunk, head); thread t owns query / key / value row t.
+// a chunk's rows.  d sums exactly the rounded weights Y is built from, which
+// keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
+// head), 128 columns of tensor memory and 48 KB of shared memory, so several
+// chunks are in flight per SM; thread t owns query / key / value row t.
 template <int P, int DV>
 __global__ void __launch_bounds__(128)
 intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ y_out, float* __restrict__ d_out,
                 int T) {
-    constexpr int NV = DV + 16;  // values, ones, zero padding
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar, drain;
     __shared__ uint32_t tmem_base;
@@ -913,7 +913,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* Qs = sm;              // K-major, 128 rows x 128 B
     uint8_t* Ks = sm + kAtom;      // unit keys, K-major
-    uint8_t* Vs = sm + 2 * kAtom;  // [V | 1 | 0], MN-major, two 64-column atoms
+    uint8_t* Vs = sm + 2 * kAtom;  // V, MN-major
     const int t = threadIdx.x, warp = t >> 5;
     const int64_t bh = blockIdx.y;
     const int row = blockIdx.x * kChunk + t;
@@ -926,7 +926,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         abort_flag = 0;
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_base, 256);
+        tmem_alloc(&tmem_base, 128);
         tmem_relinquish();
     }
     // rows -> shared memory (zeros past T)
@@ -962,8 +962,6 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 #pragma unroll
         for (int i = 0; i < DV / 8; ++i)
             *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(8 * i, t, kAtom)) = valid ? gv[i] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(DV, t, kAtom)) = make_uint4(0x3F80u, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(DV + 8, t, kAtom)) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -981,8 +979,9 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, kWaitNs));
     if (!ok) abort_flag = 1;
     tc_fence_after();
-    // P = scores^2 masked, bf16, in place (columns 0..63); quarters past this
-    // warp's rows are all masked
+    // P = scores^2 masked, bf16, in place (columns 0..63), and its row sum;
+    // quarters past this warp's rows are all masked
+    float den = 0.f;
     if (ok) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -999,6 +998,8 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                     a = col <= t ? a * a : 0.f;
                     b = col + 1 <= t ? b * b : 0.f;
                     pk[i] = pack_bf16x2(a, b);
+                    const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+                    den += __low2float(hp) + __high2float(hp);
                 }
             } else {
 #pragma unroll
@@ -1011,19 +1012,20 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Y into columns 64.. (the scores there have been read)
     if (t == 0 && !abort_flag) {
         const uint64_t dv = sdesc_mnmajor_sw128(smem_u32(Vs), kAtom);
-        constexpr uint32_t id_pv = idesc_bf16_f32_major(128, NV, false, true);
+        constexpr uint32_t id_pv = idesc_bf16_f32_major(128, DV, false, true);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_ts(tb + 128, tb + 8 * ks, dv + ks * (2048 >> 4), id_pv, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks) mma_ts(tb + 64, tb + 8 * ks, dv + ks * (2048 >> 4), id_pv, ks > 0 ? 1u : 0u);
         mma_commit(&bar);
     }
     ok = !abort_flag && __all_sync(0xffffffffu, mbar_wait(&bar, 1, &abort_flag, kWaitNs));
     tc_fence_after();
     if (ok) {
-        uint32_t y[DV + 16];
+        uint32_t y[DV];
 #pragma unroll
-        for (int c = 0; c < NV; c += 16) tmem_ld16(tmem_addr(tb, lane0, 128 + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
+        for (int c = 0; c < DV; c += 16) tmem_ld16(tmem_addr(tb, lane0, 64 + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
         tmem_wait_ld();
         if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(y_out + grow * DV);
@@ -1033,7 +1035,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                                     pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
                                     pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
                                     pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
-            d_out[grow] = __uint_as_float(y[DV]);
+            d_out[grow] = den;
         }
     } else if (t == 0) {
         atomicOr(&g_chunked_tc_status, kStatusTimeout);
@@ -1046,7 +1048,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (warp == 0) tmem_dealloc(tb, 128);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1104,7 +1106,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
                          float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
     if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
     // intra-chunk rows first: every chunk at once, over the whole device
-    constexpr size_t intra_smem = 4 * kAtom + 1024;
+    constexpr size_t intra_smem = 3 * kAtom + 1024;
     cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)intra_smem);
     if (e != cudaSuccess) return e;
