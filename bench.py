@@ -79,6 +79,9 @@ def kernel_work(name, w, form="chunked"):
     if name == "chunked_tc":
         # the fused forward: state build and readout with the normaliser column
         return "flop", bht * 4 * w.n * (w.dv + 1)
+    if name == "combine":
+        # numerators, intra rows and both normalisers read, o written
+        return "byte", bht * (w.dv * 2 * 3 + 8)
     if name == "intra_tc":
         # the causal intra-chunk half of the forward
         return "flop", bht * (w.C + 1) * (w.p + w.dv)

@@ -34,7 +34,9 @@ unsigned int states_tc_take_status();
 // chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
 // start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
 // `intra` is chunked_tc_intra_bytes() of device scratch (16-byte aligned)
-// for the intra-chunk rows a first kernel computes for every chunk at once.
+// for the intra-chunk rows, their normalisers and the inter-chunk
+// denominators; the intra-chunk kernel runs on a second stream of the device
+// that is joined back into `s` before the combine pass.
 int chunked_tc_segments(int p, int dv, int BH, int T);
 int chunked_tc_segment_chunks(int T, int G);
 size_t chunked_tc_intra_bytes(int BH, int T, int dv);

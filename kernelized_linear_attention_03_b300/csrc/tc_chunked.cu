@@ -18,18 +18,21 @@
 // readout MMA).  Its query lift goes to tensor memory (A operand of the
 // readout), its key lift to shared memory (A operand of the update).  The
 // "extra CTA" owns the last, partly filled tile and Z (the inter-chunk
-// denominator).  The intra-chunk part of every chunk is computed beforehand
-// by a separate kernel (all chunks at once).  Each CTA's partial Y (128 x dv,
-// sent as bf16) is summed in distributed shared memory: tile CTA r owns rows
-// [r*R, r*R + R) of the chunk, receives the partials of those rows from
-// every CTA of the cluster (a ring of RS chunks), adds them and the rows'
-// intra-chunk part, divides by d and stores o.
+// denominator).  Each CTA's partial Y (128 x dv, sent as bf16) is summed in
+// distributed shared memory: tile CTA r owns rows [r*R, r*R + R) of the
+// chunk, receives the partials of those rows from every CTA of the cluster
+// (a ring of RS chunks) and stores their sum and the rows' inter-chunk
+// denominator.  The intra-chunk part of every chunk is computed by a separate
+// kernel on a second stream, beside the clusters (which leave SMs free); a
+// combine pass then adds it and divides.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "kata_internal.h"
 #include "tc_lift.cuh"
@@ -294,8 +297,7 @@ template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
-                  const __nv_bfloat16* __restrict__ y_intra, const float* __restrict__ d_intra,
-                  const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
+                  float* __restrict__ den_out, const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
                   float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV>;
     constexpr int n = K::n;
@@ -704,27 +706,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         // rows' intra-chunk part, divide by the denominator, store o, then hand
         // the receive slot back to every sender (its next use is RS chunks later)
         constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
-        constexpr int kPre = kRedIt < 2 ? kRedIt : 2;  // items whose intra rows are loaded ahead
         const int er = t - 448;
         const int r0 = rank * K::R;
         const int items = my_rows * (DV / 8);
         __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
-        const __nv_bfloat16* yih = y_intra + bh * (int64_t)T * DV;
-        const float* dih = d_intra + bh * (int64_t)T;
+        float* dh = den_out + bh * (int64_t)T;
         for (int kr = 0; kr < nk; ++kr) {
             const int r = kr % K::RS;
-            // this chunk's intra-chunk rows do not depend on the partials: load first
-            uint4 yi[kPre];
-            float di[kPre];
-#pragma unroll
-            for (int it = 0; it < kPre; ++it) {
-                const int idx = er + 64 * it;
-                const int lr = idx % my_rows, i = idx / my_rows;
-                const int otok = (c0 + kr) * kChunk + r0 + lr;
-                const bool have = idx < items && otok < T;
-                yi[it] = have ? *reinterpret_cast<const uint4*>(yih + (int64_t)otok * DV + 8 * i) : make_uint4(0, 0, 0, 0);
-                di[it] = have ? dih[otok] : 0.f;
-            }
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs) &&
                                              mbar_wait(&local_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs))) {
                 fail();
@@ -736,25 +724,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 const int idx = er + 64 * it;
                 if (idx >= items) break;
                 const int lr = idx % my_rows, i = idx / my_rows;
-                uint4 yrow;
-                float drow;
-                if (it < kPre) {
-                    yrow = yi[it];
-                    drow = di[it];
-                } else {
-                    const int otok = (c0 + kr) * kChunk + r0 + lr;
-                    yrow = otok < T ? *reinterpret_cast<const uint4*>(yih + (int64_t)otok * DV + 8 * i) : make_uint4(0, 0, 0, 0);
-                    drow = otok < T ? dih[otok] : 0.f;
-                }
-                float acc[8];
-                {
-                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yrow);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[2 * j] = __low2float(h[j]);
-                        acc[2 * j + 1] = __high2float(h[j]);
-                    }
-                }
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int src = 0; src < K::CS; ++src) {
                     const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
@@ -765,13 +735,15 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         acc[2 * j + 1] += __high2float(h[j]);
                     }
                 }
-                const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + drow;
-                const float inv = d > 0.f ? 1.f / d : 0.f;
                 const int otok = (c0 + kr) * kChunk + r0 + lr;
-                if (otok < T)
+                if (otok < T) {
+                    // the inter-chunk numerator and denominator of the row; the
+                    // combine pass adds the intra-chunk part and divides
                     *reinterpret_cast<uint4*>(oh + (int64_t)otok * DV + 8 * i) =
-                        make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
-                                   pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+                        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                                   pack_bf16x2(acc[6], acc[7]));
+                    if (i == 0) dh[otok] = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
+                }
             }
             mbar_arrive(&rd_sync);
             if (!__all_sync(0xffffffffu, mbar_wait(&rd_sync, kr & 1, &abort_flag, kWaitNs))) {
@@ -1051,6 +1023,32 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (warp == 0) tmem_dealloc(tb, 128);
 }
 
+// o = (numerator + intra rows) / (denominator + intra normaliser), in place
+// over the fused kernel's bf16 numerators; thread = 8 columns of one row.
+template <int DV>
+__global__ void __launch_bounds__(256)
+combine_kernel(__nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ y_intra,
+               const float* __restrict__ d_intra, const float* __restrict__ d_inter, int64_t rows) {
+    const int64_t total = rows * (DV / 8);
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = idx / (DV / 8);
+        const uint4 a = reinterpret_cast<const uint4*>(o)[idx];
+        const uint4 b = reinterpret_cast<const uint4*>(y_intra)[idx];
+        const float d = d_inter[row] + d_intra[row];
+        const float inv = d > 0.f ? 1.f / d : 0.f;
+        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
+        uint4 r;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = pack_bf16x2((__low2float(ha[j]) + __low2float(hb[j])) * inv,
+                               (__high2float(ha[j]) + __high2float(hb[j])) * inv);
+        reinterpret_cast<uint4*>(o)[idx] = r;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 // The register split of the kernel fits in its launch allocation.
 template <int P, int DV>
@@ -1100,35 +1098,72 @@ int max_clusters() {
     return cached[dev] > 0 ? cached[dev] : 0;
 }
 
+// A second stream of the current device, and two events, for running the
+// intra-chunk kernel beside the fused kernel (created once per device).
+struct AuxStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t aux_stream(AuxStream** out) {
+    static AuxStream aux[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    AuxStream& a = aux[dev];
+    if (a.s == nullptr) {
+        if ((e = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &a;
+    return cudaSuccess;
+}
+
 template <int P, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* y_intra, float* d_intra,
-                         const float* S_start, const float* z_start, int start_groups, float* S_final,
-                         float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
+                         float* d_inter, const float* S_start, const float* z_start, int start_groups,
+                         float* S_final, float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
     if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
-    // intra-chunk rows first: every chunk at once, over the whole device
-    constexpr size_t intra_smem = 3 * kAtom + 1024;
-    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)intra_smem);
+    AuxStream* aux = nullptr;
+    cudaError_t e = aux_stream(&aux);
     if (e != cudaSuccess) return e;
-    const dim3 igrid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)BH);
-    KATA_TRACED("intra_tc", s,
-                (intra_tc_kernel<P, DV><<<igrid, 128, intra_smem, s>>>(
-                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                    static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(y_intra), d_intra, T)));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the intra-chunk rows of every chunk, on a second stream: the fused
+    // kernel's clusters leave SMs free, and it does not read these rows
+    constexpr size_t intra_smem = 3 * kAtom + 1024;
+    if ((e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)intra_smem)) != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    e = configure<P, DV>(cfg, attr, G, BH, s);
-    if (e != cudaSuccess) return e;
+    if ((e = configure<P, DV>(cfg, attr, G, BH, s)) != cudaSuccess) return e;
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
+    if ((e = cudaEventRecord(aux->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(aux->s, aux->fork, 0)) != cudaSuccess)
+        return e;
+    // the fused kernel first, so its clusters are placed before the intra CTAs fill the device
     KATA_TRACED("chunked_tc", s,
                 e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tk, tv, static_cast<__nv_bfloat16*>(o),
-                                       static_cast<const __nv_bfloat16*>(y_intra),
-                                       static_cast<const float*>(d_intra), S_start, z_start, start_groups, S_final,
-                                       z_final, T, seg_chunks));
+                                       d_inter, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
     if (e != cudaSuccess) return e;
+    const dim3 igrid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)BH);
+    KATA_TRACED("intra_tc", aux->s,
+                (intra_tc_kernel<P, DV><<<igrid, 128, intra_smem, aux->s>>>(
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                    static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(y_intra), d_intra, T)));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(aux->join, aux->s)) != cudaSuccess || (e = cudaStreamWaitEvent(s, aux->join, 0)) != cudaSuccess)
+        return e;
+    const int64_t rows = (int64_t)BH * T;
+    const int64_t work = rows * (DV / 8);
+    const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 148 * 16);
+    KATA_TRACED("combine", s,
+                (combine_kernel<DV><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(o),
+                                                             static_cast<const __nv_bfloat16*>(y_intra), d_intra,
+                                                             d_inter, rows)));
     return cudaGetLastError();
 }
 
@@ -1166,18 +1201,20 @@ int chunked_tc_segment_chunks(int T, int G) {
 }
 
 size_t chunked_tc_intra_bytes(int BH, int T, int dv) {
-    return (size_t)BH * (size_t)T * ((size_t)dv * 2 + 4);
+    return (size_t)BH * (size_t)T * ((size_t)dv * 2 + 8);
 }
 
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
                               const float* S_start, const float* z_start, int start_groups, float* S_final,
                               float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s) {
     const int seg_chunks = chunked_tc_segment_chunks(T, G);
-    // intra-chunk rows: bf16 [BH][T][dv], then fp32 normalisers [BH][T]
+    // intra-chunk rows: bf16 [BH][T][dv], then fp32 intra-chunk normalisers
+    // [BH][T], then the fused kernel's inter-chunk denominators [BH][T]
     void* y_intra = intra;
     float* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + (size_t)BH * T * dv * 2);
-    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, y_intra, d_intra, S_start, z_start, start_groups, S_final,
-                                             z_final, BH, T, seg_chunks, G, s));
+    float* d_inter = d_intra + (size_t)BH * T;
+    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, y_intra, d_intra, d_inter, S_start, z_start, start_groups,
+                                             S_final, z_final, BH, T, seg_chunks, G, s));
     return cudaErrorInvalidValue;
 }
 
