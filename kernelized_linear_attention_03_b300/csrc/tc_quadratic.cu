@@ -41,7 +41,7 @@ __device__ unsigned int g_quad_tc_status = 0;
 
 constexpr int kTile = 128;        // queries per tile, keys per tile
 constexpr int kThreads = 512;
-constexpr int kStages = 3;        // key / value ring
+constexpr int kStages = 4;        // key / value ring
 constexpr uint32_t kAtom = 128 * 128;
 constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value slots, the ones column, pad
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every device-side wait
