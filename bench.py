@@ -359,19 +359,42 @@ def run_ours(args, world, rank, local):
             print(json.dumps(line), flush=True)
         return
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers.  The heads stream
+    # through: one copy stream brings each head's rows in, in order, and each
+    # head's forward (its own call, on its own stream) starts as soon as its
+    # rows have landed, its output going back on the same stream.
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
     oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size()
+    nh = w.B * w.H
+    heads = lambda t: t.view(nh, 1, 1, w.T, t.shape[-1])
+    qh_, kh_, vh_, oh_ = heads(qh), heads(kh), heads(vh), heads(oh)
+    qd_, kd_, vd_, od_ = heads(qd), heads(kd), heads(vd), heads(o)
+    copy_in = torch.cuda.Stream(device=dev)
+    hstreams = [torch.cuda.Stream(device=dev) for _ in range(nh)]
+    landed = [torch.cuda.Event() for _ in range(nh)]
+    ws1 = kb.kata_chunked_workspace_bytes(q.dtype, 1, 1, w.T, w.p, w.dv, w.C)
+    wsh = [torch.empty(max(ws1, 1), dtype=torch.uint8, device=dev) for _ in range(nh)]
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        kb.kata_forward_chunked(qd, kd, vd, w.C, mode, o=o, workspace=ws, stream=stream)
-        oh.copy_(o, non_blocking=True)
+        copy_in.wait_stream(stream)
+        for h in range(nh):
+            with torch.cuda.stream(copy_in):
+                qd_[h].copy_(qh_[h], non_blocking=True)
+                kd_[h].copy_(kh_[h], non_blocking=True)
+                vd_[h].copy_(vh_[h], non_blocking=True)
+                landed[h].record(copy_in)
+        for h in range(nh):
+            sh = hstreams[h]
+            sh.wait_stream(stream)
+            sh.wait_event(landed[h])
+            kb.kata_forward_chunked(qd_[h], kd_[h], vd_[h], w.C, mode, o=od_[h], workspace=wsh[h], stream=sh)
+            with torch.cuda.stream(sh):
+                oh_[h].copy_(od_[h], non_blocking=True)
+        for sh in hstreams:
+            stream.wait_stream(sh)
 
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
