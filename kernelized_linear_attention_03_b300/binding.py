@@ -90,6 +90,16 @@ def _stream(stream):
     return int(stream)
 
 
+def _used_on(t, stream):
+    """Tell torch's caching allocator that `t`, allocated here, is used on
+    `stream` (so its memory is not handed out again before that stream has
+    passed this call)."""
+    if t is None or stream is None:
+        return
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+    t.record_stream(s)
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -150,6 +160,7 @@ def kata_forward_chunked(q, k, v, C, mode=KATA_SCAN_TREE, S0=None, z0=None, o=No
     need = kata_chunked_workspace_bytes(_dtype_code(q), B, H, T, p, dv, C)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().kata_forward_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, T,
                                        p, dv, int(C), int(mode), _ptr(S0), _ptr(z0), _ptr(S_final),

@@ -278,18 +278,19 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 
 // ---------------------------------------------------------------- kernel
 // Warp roles (512 threads, four warpgroups):
-//   warps 0-3   lift:     thread t = token t of the chunk; stages its query
-//                         and key rows one chunk ahead (cp.async), puts the key
-//                         on the unit sphere, writes the query lift (tensor
-//                         memory), the key lift (shared memory), the value row
+//   warps 0-3   lift:     thread t = token t of the chunk; reads its staged
+//                         query and key rows, puts the key on the unit sphere,
+//                         writes the query lift (tensor memory) and the key
+//                         lift (shared memory; extra CTA: also the unit keys)
 //   warps 4-7   state:    thread e = tensor-memory lane e; reads the state
 //                         after each update and releases it to the next update,
 //                         refreshes the bf16 copy for the next readout (extra
-//                         CTA: also P = scores^2 and the denominators)
-//   warps 8-11  readout:  thread e = lane e; reads the partial readout, sends
-//                         it to the row owners, reduces its owned rows one
-//                         chunk later and stores o
-//   warps 12-15 MMA:      one thread issues every tcgen05.mma
+//                         CTA: also Z and the rows' inter-chunk denominators)
+//   warps 8-11  readout:  thread e = lane e; reads the partial readout and
+//                         sends each row to the tile CTA that owns it
+//   warps 12-15 warp 12 lane 0 issues every tcgen05.mma, warp 13 lane 0 the
+//                         TMA loads; warps 14-15 reduce the owned rows and
+//                         store their numerators and denominators
 // Per chunk the MMAs run update (state += lift(K)^T V) then readout
 // (Y = lift(Q) S), so the next update starts as soon as the state warps have
 // read the state.
@@ -702,9 +703,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     }
     if (warp >= 14 && my_rows > 0) {
         // =============================================================== reduce warps
-        // owner side, chunk by chunk as the partial rows land: sum them and the
-        // rows' intra-chunk part, divide by the denominator, store o, then hand
-        // the receive slot back to every sender (its next use is RS chunks later)
+        // owner side, chunk by chunk as the partial rows land: sum them, store
+        // the rows' inter-chunk numerator and denominator, then hand the
+        // receive slot back to every sender (its next use is RS chunks later)
         constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
         const int er = t - 448;
         const int r0 = rank * K::R;

@@ -284,3 +284,24 @@ def test_workload_c3_chunk_state_scan_modes():
     _, S_ref, z_ref = oracle.forward_recurrent(kk, kk, vv)
     assert _state_err(Sa[:, :1, -1], S_ref) <= TOL[torch.bfloat16]
     assert _state_err(za[:, :1, -1], z_ref) <= TOL[torch.bfloat16]
+
+
+def test_chunked_calls_on_concurrent_streams():
+    # single-head calls issued back to back on separate streams (the library's
+    # second stream and its events are shared by all of them) match one call
+    # over all heads and the plain definition
+    q, k, v = _inputs(1, 4, 1000, 64, 64, torch.bfloat16, seed=11)
+    whole = kb.kata_forward_chunked(q, k, v, 128, kb.KATA_SCAN_TREE)
+    o = torch.empty_like(v)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    cur = torch.cuda.current_stream()
+    for h, s in enumerate(streams):
+        s.wait_stream(cur)
+        kb.kata_forward_chunked(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], 128, kb.KATA_SCAN_TREE,
+                                o=o[:, h:h + 1], stream=s)
+    for s in streams:
+        cur.wait_stream(s)
+    torch.cuda.synchronize()
+    ref = oracle.forward_plain(f64(q), f64(k), f64(v))
+    assert_close(f64(o), ref, torch.bfloat16, "per-head calls")
+    assert_close(f64(whole), ref, torch.bfloat16, "one call")
