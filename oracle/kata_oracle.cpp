@@ -29,7 +29,7 @@
 //     causal part: the chunked-scan paragraph (the one introducing the
 //     three kernels and the wall-clock model).
 //
-// Readings where the pages are silent (each is listed in the design doc):
+// Readings where the pages are silent:
 //   * off-diagonal packed coordinates carry a factor sqrt(2), diagonal 1, so
 //     the packed dot product is the Frobenius product;
 //   * q and k are normalised inside the forward; a zero vector stays zero;
