@@ -215,9 +215,12 @@ def oracle_threads(w):
 
 
 def sample_len(w, q, k, v, seconds, nthreads):
-    """Tokens per head for an oracle sample of about `seconds` (multiple of C)."""
-    t_cal = max(oracle_sample(w, q, k, v, w.C, nthreads), 1e-3)
-    T_s = int(w.C * seconds / t_cal)
+    """Tokens per head for an oracle sample of about `seconds` (multiple of C),
+    calibrated on a short sample long enough that the per-call overhead does
+    not dominate."""
+    T_c = min(w.T, 8 * w.C)
+    t_cal = max(oracle_sample(w, q, k, v, T_c, nthreads), 1e-3)
+    T_s = int(T_c * seconds / t_cal)
     return max(w.C, min(w.T, T_s // w.C * w.C))
 
 
