@@ -1104,6 +1104,7 @@ int max_clusters() {
 struct AuxStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;  // held across one call's fork ... join, so calls from several host threads do not interleave
 };
 cudaError_t aux_stream(AuxStream** out) {
     static AuxStream aux[64];
@@ -1143,6 +1144,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
+    std::lock_guard<std::mutex> lk(aux->mu);
     if ((e = cudaEventRecord(aux->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(aux->s, aux->fork, 0)) != cudaSuccess)
         return e;
     // the fused kernel first, so its clusters are placed before the intra CTAs fill the device

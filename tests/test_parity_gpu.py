@@ -305,3 +305,32 @@ def test_chunked_calls_on_concurrent_streams():
     ref = oracle.forward_plain(f64(q), f64(k), f64(v))
     assert_close(f64(o), ref, torch.bfloat16, "per-head calls")
     assert_close(f64(whole), ref, torch.bfloat16, "one call")
+
+
+def test_chunked_calls_from_host_threads():
+    # the same single-head calls issued from four host threads at once
+    import threading
+    q, k, v = _inputs(1, 4, 700, 64, 64, torch.bfloat16, seed=12)
+    ref = oracle.forward_plain(f64(q), f64(k), f64(v))
+    o = torch.empty_like(v)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(h):
+        try:
+            for _ in range(3):
+                kb.kata_forward_chunked(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], 128, kb.KATA_SCAN_TREE,
+                                        o=o[:, h:h + 1], stream=streams[h])
+            streams[h].synchronize()
+        except Exception as exc:  # noqa: BLE001 - reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(h,)) for h in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert_close(f64(o), ref, torch.bfloat16, "calls from host threads")
