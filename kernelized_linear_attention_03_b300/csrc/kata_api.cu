@@ -208,7 +208,7 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         const int L = kata::chunked_tc_segment_chunks(T, G) * 128;
         float* Sg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
         float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
-        cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, stream);
+        cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, 0, stream);
         if (e == cudaSuccess)
             e = cudaMemset2DAsync(Sg + (size_t)(G - 1) * n32 * dv, sizeof(float) * (size_t)G * n32 * dv, 0,
                                   sizeof(float) * (size_t)n32 * dv, (size_t)BH, stream);
@@ -248,8 +248,13 @@ kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dt, i
         (st = check_buffer(S_prefix, sizeof(float) * BH * NC * n * dv)) != KATA_OK ||
         (st = check_buffer(z_prefix, sizeof(float) * BH * NC * n)) != KATA_OK)
         return st;
+    // bf16, sequential prefix: the state kernel sums the chunk states in chunk
+    // order as it goes and writes the exclusive prefixes directly (one pass)
+    if (dt == KATA_BF16 && mode == KATA_SCAN_SEQUENTIAL)
+        return cuda_status(
+            kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 1, stream));
     cudaError_t e = dt == KATA_BF16
-                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, stream)
+                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 0, stream)
                         : kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, S_prefix, S_prefix, nullptr, nullptr, BH, NC, n * dv, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, z_prefix, z_prefix, nullptr, nullptr, BH, NC, n, stream);

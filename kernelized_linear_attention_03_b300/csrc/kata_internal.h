@@ -24,7 +24,7 @@ unsigned int quadratic_tc_take_status();
 // z_out [BH, NS_out, n] (fp32, sqrt(2)-packed order).  NS <= NS_out and
 // NS <= ceil(T / L).
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, cudaStream_t s);
+                             int p, int dv, int L, int NS, int NS_out, int prefix, cudaStream_t s);
 unsigned int states_tc_take_status();
 
 // Fused chunked forward on the tensor cores (bf16), one cluster per (head,

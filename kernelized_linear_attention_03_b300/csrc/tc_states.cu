@@ -78,7 +78,10 @@ template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS, int NS_out,
-                 int segs_per_cta) {
+                 int segs_per_cta, int prefix) {
+    // prefix != 0 (one CTA per tile and head, all segments): each segment's
+    // row is the exclusive running sum of the segments before it, summed in
+    // segment order in the epilogue's registers, instead of the segment's own total
     // T: tokens per head; segments 0..NS-1 of L tokens (L a multiple of 128,
     // or L <= 128) are computed into rows of a [BH, NS_out, n] layout.
     constexpr int n = lift::packed_n(P);
@@ -245,26 +248,46 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const float f = ci < cj ? kSqrt2f : 1.f;
         const int my_canon = slot < n ? lift::canonical_index(P, ci, cj) : -1;
         uint8_t* stage = sm + kOutOff;
+        float run[DV + 1];  // running sum of the segment totals (prefix mode)
+#pragma unroll
+        for (int c = 0; c <= DV; ++c) run[c] = 0.f;
         for (int seg = seg0; seg < seg1; ++seg) {
             if (seg * L >= T) break;
             const int sl = seg - seg0, acb = sl & 1;
             if (!wait(&acc_full[acb], (sl >> 1) & 1)) { fail(); break; }
             tc_fence_after();
-            uint32_t r[80];
+            const int64_t base = (bh * NS_out + seg) * (int64_t)n;
+            // 16 columns at a time: out = the segment's total, or (prefix mode)
+            // the sum before it, into the staging row
+            __syncwarp();  // this warp's previous rows have left the staging
 #pragma unroll
-            for (int c0 = 0; c0 < 80; c0 += 16) tmem_ld16(tmem_addr(tb + 128 * acb, lane0, c0), *reinterpret_cast<uint32_t(*)[16]>(r + c0));
-            tmem_wait_ld();
+            for (int c0 = 0; c0 < DV; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tmem_addr(tb + 128 * acb, lane0, c0), r);
+                tmem_wait_ld();
+                float out[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float tot = __uint_as_float(r[i]);
+                    out[i] = prefix ? run[c0 + i] : tot;
+                    run[c0 + i] += tot;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4*>(stage + e * kOutRow + 4 * (c0 + 4 * c)) =
+                        make_float4(f * out[4 * c], f * out[4 * c + 1], f * out[4 * c + 2], f * out[4 * c + 3]);
+            }
+            {
+                uint32_t r[16];
+                tmem_ld16(tmem_addr(tb + 128 * acb, lane0, 64), r);  // the ones column: z
+                tmem_wait_ld();
+                const float tot = __uint_as_float(r[0]);
+                const float zo = prefix ? run[DV] : tot;
+                run[DV] += tot;
+                if (slot < n) z_out[base + my_canon] = f * zo;
+            }
             tc_fence_before();
             mbar_arrive(&acc_free[acb]);
-            const int64_t base = (bh * NS_out + seg) * (int64_t)n;
-            if (slot < n) z_out[base + my_canon] = f * __uint_as_float(r[64]);
-            // this warp's 32 rows: stage, then one 8-byte-per-lane store per row
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < DV / 4; ++c)
-                *reinterpret_cast<float4*>(stage + e * kOutRow + 16 * c) =
-                    make_float4(f * __uint_as_float(r[4 * c]), f * __uint_as_float(r[4 * c + 1]),
-                                f * __uint_as_float(r[4 * c + 2]), f * __uint_as_float(r[4 * c + 3]));
             __syncwarp();
             for (int rr = 0; rr < 32; ++rr) {
                 const int canon = __shfl_sync(0xffffffffu, my_canon, rr);
@@ -287,7 +310,7 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 
 template <int P, int DV>
 cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_out, int BH, int T, int L,
-                         int NS, int NS_out, cudaStream_t s) {
+                         int NS, int NS_out, int prefix, cudaStream_t s) {
     auto kern = states_tc_kernel<P, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
@@ -296,22 +319,22 @@ cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_ou
     const int tiles = lift::tiles_of(P);
     // about two CTAs per SM in total, each a run of segments
     const int64_t units = (int64_t)tiles * BH;
-    int groups = (int)((2 * 148) / (units > 0 ? units : 1));
+    int groups = prefix ? 1 : (int)((2 * 148) / (units > 0 ? units : 1));
     groups = groups < 1 ? 1 : (groups > NS ? NS : groups);
     const int per = (NS + groups - 1) / groups;
     groups = (NS + per - 1) / per;
     dim3 grid(tiles, groups, BH);
-    KATA_TRACED("states_tc", s, kern<<<grid, kThreads, kSmem, s>>>(tk, tv, S_out, z_out, T, L, NS, NS_out, per));
+    KATA_TRACED("states_tc", s, kern<<<grid, kThreads, kSmem, s>>>(tk, tv, S_out, z_out, T, L, NS, NS_out, per, prefix));
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, cudaStream_t s) {
+                             int p, int dv, int L, int NS, int NS_out, int prefix, cudaStream_t s) {
     if (NS <= 0) return cudaSuccess;
 #define KATA_CASE(P_, DV_) \
-    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, s);
+    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, prefix, s);
     KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
     KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
     KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)
