@@ -124,3 +124,42 @@ extern "C" __attribute__((visibility("default"))) int kata_tc_selftest(const voi
                                     D, K, N, mode, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
+
+// ---------------------------------------------------------------- bounded waits
+// A warp waits on an mbarrier that nothing ever arrives on, with a budget of
+// `budget_ns`; the wait must give up, and the kernel must report it and return
+// (the same bounded wait every tensor-core kernel of the library uses).
+namespace {
+
+__global__ void wait_probe(int* status, unsigned long long* elapsed_ns, unsigned long long budget_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        kata::tc::mbar_init(&bar, 1);
+        kata::tc::fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    const unsigned long long t0 = kata::tc::globaltimer_ns();
+    const bool ok = kata::tc::mbar_wait(&bar, 0, &abort_flag, budget_ns);
+    const unsigned long long t1 = kata::tc::globaltimer_ns();
+    if (threadIdx.x == 0) {
+        status[0] = ok ? 0 : 1;  // 1: the wait gave up, as it must
+        elapsed_ns[0] = t1 - t0;
+    }
+}
+
+__global__ void after_probe(int* status) {
+    if (threadIdx.x == 0) status[1] = 42;
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int kata_wait_selftest(int* status,
+                                                                       unsigned long long* elapsed_ns,
+                                                                       unsigned long long budget_ns,
+                                                                       cudaStream_t s) {
+    wait_probe<<<1, 32, 0, s>>>(status, elapsed_ns, budget_ns);
+    after_probe<<<1, 32, 0, s>>>(status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}

@@ -37,3 +37,21 @@ def test_gemm_probe(lib, mode, K, N):
     assert rc == 0 and int(status.item()) == 0
     err = (D.double().cpu() - ref).abs().max().item()
     assert err <= 1e-3 * max(1.0, ref.abs().max().item()), err
+
+
+def test_bounded_wait_gives_up_and_context_stays_usable(lib):
+    # an mbarrier nothing arrives on: the library's bounded wait returns after
+    # its budget, the kernel reports it, and the next kernel still runs
+    P = ctypes.c_void_p
+    lib.kata_wait_selftest.argtypes = [P, P, ctypes.c_ulonglong, P]
+    lib.kata_wait_selftest.restype = ctypes.c_int
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    budget = 5_000_000  # 5 ms
+    rc = lib.kata_wait_selftest(status.data_ptr(), elapsed.data_ptr(), budget,
+                                torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(status[0].item()) == 1, "the wait did not give up"
+    assert budget <= int(elapsed.item()) < 1_000_000_000
+    assert int(status[1].item()) == 42, "the context did not survive the timeout"
