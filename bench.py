@@ -40,6 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
                   "sm_max_mhz": 2032.0}
 SMS = 148
 FP32_LANES_PER_SM = 128
+DECODE_B, DECODE_H = 64, 16  # decode batch: sequences x heads, one new token each
 
 
 def load_peaks():
@@ -88,6 +89,10 @@ def kernel_work(name, w, form="chunked"):
     if name == "states_tc":
         # segment start states: recomputed work, no algorithmic share
         return "flop", 0
+    if name == "decode_step":
+        # state and normaliser read and written once, the token's q, k, v read, o written
+        elem = 4 if w.dtype == "fp32" else 2
+        return "byte", w.B * w.H * (2 * w.n * (w.dv + 1) * 4 + (2 * w.p + 2 * w.dv) * elem)
     return None, 0
 
 
@@ -267,6 +272,11 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     w0 = {x.name.split("_")[0]: x for x in inputs.WORKLOADS}[args.workload]
     w = inputs.Workload(w0.name, w0.B, w0.H, w0.T, w0.p, w0.dv, w0.C, w0.dtype, w0.kind, seed=rank)
+    if args.form == "decode":
+        # a serving batch of one-token steps with the workload's head shape:
+        # 64 sequences x 16 heads, each head's state n x (dv+1) fp32 (above L2 at p >= 32)
+        w = inputs.Workload(f"decode_B{DECODE_B}_H{DECODE_H}_p{w0.p}_dv{w0.dv}_{w0.dtype}", DECODE_B, DECODE_H, 1,
+                            w0.p, w0.dv, w0.C, w0.dtype, w0.kind, seed=rank)
     mode = kb.KATA_SCAN_TREE if args.scan == "tree" else kb.KATA_SCAN_SEQUENTIAL
     q, k, v = inputs.make(w, dev)
     o = torch.empty_like(v)
@@ -286,6 +296,14 @@ def run_ours(args, world, rank, local):
 
         def step():
             kb.kata_chunk_state_scan(k, v, w.C, mode, S_prefix=Sp, z_prefix=zp, stream=stream)
+    elif args.form == "decode":
+        qt, kt, vt = (x[:, :, 0].contiguous() for x in (q, k, v))
+        S = torch.zeros((w.B, w.H, w.n, w.dv), dtype=torch.float32, device=dev)
+        z = torch.zeros((w.B, w.H, w.n), dtype=torch.float32, device=dev)
+        ot = torch.empty_like(vt)
+
+        def step():
+            kb.kata_decode_step(qt, kt, vt, S, z, o=ot, stream=stream)
     else:  # scan of given chunk states
         g = torch.Generator(device=dev).manual_seed(rank)
         S_loc = torch.randn((w.B, w.H, w.NC, w.n, w.dv), generator=g, device=dev)
@@ -448,7 +466,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per call of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--form", default="chunked", choices=["chunked", "quadratic", "scan", "chunk_state_scan"],
+    ap.add_argument("--form", default="chunked",
+                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode"],
                     help="entry point timed (the contract's line is the chunked forward)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

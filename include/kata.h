@@ -141,6 +141,25 @@ KATA_API kata_status kata_scan_states(const float* S_loc, const float* z_loc, fl
                              kata_scan_mode mode, cudaStream_t stream);
 
 /*
+ * Recurrent decode step (the constant-time recurrent inference of the
+ * abstract: the state recurrence of the state-size paragraph taken one
+ * token at a time).  For each b, h, with the new token's q, k [B,H,p] and
+ * v [B,H,dv]:
+ *   S += psi(kh) v^T,  z += psi(kh)    S [B,H,n,dv], z [B,H,n] fp32, in the
+ *                                      packed order above, updated in place
+ *   o = psi(qh)^T S / psi(qh)^T z      o [B,H,dv] in the input dtype, read
+ *                                      from the updated state (s <= t), a
+ *                                      zero denominator giving a zero row.
+ * Stepping from S = z = 0 through tokens 0..T-1 gives the forward's rows; a
+ * forward's S_final, z_final continue as decode states, and a decode state
+ * seeds a forward as S0, z0.  S and z must not overlap each other or q, k,
+ * v, o (KATA_ERR_INVALID_ARG if S and z overlap).  Needs no workspace.
+ */
+KATA_API kata_status kata_decode_step(const void* q, const void* k, const void* v, void* o,
+                                      kata_dtype dtype, int B, int H, int p, int dv, float* S,
+                                      float* z, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: KATA_OK, or KATA_ERR_TIMEOUT if a bounded device-side
  * wait expired in an earlier call (that call's outputs are then invalid).

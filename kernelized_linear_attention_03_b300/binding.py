@@ -27,7 +27,7 @@ KATA_SCAN_TREE = 1
 SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_chunked_workspace_bytes", "kata_forward_chunked", "kata_chunk_state_scan",
            "kata_scan_states", "kata_get_device_status", "kata_trace_start", "kata_trace_stop",
-           "kata_trace_get", "kata_forward_chunked_noalloc")
+           "kata_trace_get", "kata_forward_chunked_noalloc", "kata_decode_step")
 
 
 class KataError(RuntimeError):
@@ -67,6 +67,8 @@ def load():
     lib.kata_get_device_status.restype = I
     lib.kata_forward_chunked_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P]
     lib.kata_forward_chunked_noalloc.restype = I
+    lib.kata_decode_step.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
+    lib.kata_decode_step.restype = I
     lib.kata_trace_start.argtypes = [I]
     lib.kata_trace_start.restype = I
     lib.kata_trace_stop.argtypes = []
@@ -215,6 +217,26 @@ def kata_scan_states(S_loc, z_loc, mode=KATA_SCAN_TREE, S_prefix=None, z_prefix=
                                    NC, n, dv, int(mode), _stream(stream)),
            "kata_scan_states")
     return S_prefix, z_prefix
+
+
+def kata_decode_step(q, k, v, S, z, o=None, stream=None):
+    """One recurrent decode step: q, k [B,H,p], v [B,H,dv] (one dtype); S
+    [B,H,n,dv] and z [B,H,n] float32, updated in place.  Returns o [B,H,dv]."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,p] and v [B,H,dv]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share one dtype")
+    B, H, p = q.shape
+    dv = v.shape[-1]
+    n = kata_packed_dim(p)
+    if S.shape != (B, H, n, dv) or z.shape != (B, H, n) or S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise ValueError("expected float32 S [B,H,n,dv] and z [B,H,n]")
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, p, dv,
+                                   _ptr(S), _ptr(z), _stream(stream)),
+           "kata_decode_step")
+    return o
 
 
 def kata_get_device_status(stream=None):

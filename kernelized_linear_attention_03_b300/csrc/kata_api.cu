@@ -285,6 +285,25 @@ kata_status kata_scan_states(const float* S_loc, const float* z_loc, float* S_pr
     return cuda_status(e);
 }
 
+kata_status kata_decode_step(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B, int H,
+                             int p, int dv, float* S, float* z, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, 1, p, dv);
+    if (st != KATA_OK) return st;
+    const int64_t BH = (int64_t)B * H, n = packed(p);
+    if (BH == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * BH * p, v_bytes = elem_bytes(dt) * BH * dv;
+    const size_t sb = sizeof(float) * (size_t)(BH * n * dv), zb = sizeof(float) * (size_t)(BH * n);
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
+        (st = check_buffer(S, sb)) != KATA_OK || (st = check_buffer(z, zb)) != KATA_OK)
+        return st;
+    // S and z are updated in place by different threads: they must not overlap.
+    const char* sp = reinterpret_cast<const char*>(S);
+    const char* zp = reinterpret_cast<const char*>(z);
+    if (sp < zp + zb && zp < sp + sb) return KATA_ERR_INVALID_ARG;
+    return cuda_status(kata::launch_decode_step(dt, q, k, v, o, S, z, (int)BH, p, dv, stream));
+}
+
 kata_status kata_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
     unsigned int word = kata::quadratic_tc_take_status();

@@ -61,6 +61,11 @@ cudaError_t launch_chunk_output_simt(int dtype, const void* q, const void* k, co
 cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, float* fin,
                         int64_t heads, int64_t NC, int64_t W, cudaStream_t s);
 
+// Recurrent decode step, any dtype: S += psi(kh) v^T, z += psi(kh) in place
+// (S [BH,n,dv], z [BH,n] fp32), o = psi(qh)^T S / psi(qh)^T z [BH,dv].
+cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
+                               float* z, int BH, int p, int dv, cudaStream_t s);
+
 // dst[i] = src ? src[i] : 0 for i < count (fp32), used for pass-through states.
 cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s);
 

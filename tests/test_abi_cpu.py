@@ -121,3 +121,19 @@ def test_binding_rejects_cpu_tensors(lib):
     v = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         kb.kata_forward_quadratic(q, q, v, o=v.clone())
+
+
+def _dec(lib, dt=kb.KATA_BF16, B=1, H=1, p=16, dv=16, ptr=NULL):
+    return lib.kata_decode_step(ptr, ptr, ptr, ptr, dt, B, H, p, dv, ptr, ptr, None)
+
+
+def test_decode_argument_errors(lib):
+    assert _dec(lib, dt=3) == kb.KATA_ERR_INVALID_ARG
+    assert _dec(lib, B=-1) == kb.KATA_ERR_INVALID_ARG
+    assert _dec(lib, p=48) == kb.KATA_ERR_UNSUPPORTED
+    assert _dec(lib, dv=8) == kb.KATA_ERR_UNSUPPORTED
+    assert _dec(lib, B=256, H=512) == kb.KATA_ERR_UNSUPPORTED
+    assert _dec(lib, ptr=NULL) == kb.KATA_ERR_INVALID_ARG
+    assert _dec(lib, ptr=MISALIGNED) == kb.KATA_ERR_INVALID_ARG
+    # no heads: nothing to do, pointers unused
+    assert _dec(lib, B=0) == kb.KATA_OK
