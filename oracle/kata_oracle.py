@@ -15,7 +15,8 @@ Parity status of each function (pins live in tests/test_oracle_pins.py):
   packed_dim, normalize, lift       pinned (closed forms, lift identities)
   forward_plain, forward_plain_rows pinned (special cases, pSNR closed form,
                                      rotation/scale invariance, convexity)
-  forward_recurrent                 pinned (agrees with plain; split calls)
+  forward_recurrent                 pinned (agrees with plain; split calls; one-token
+                                     decode steps chained through their states)
   forward_chunked, chunk_states     pinned (agrees with plain for every C,
                                      ragged T; split calls; state identity)
   scan_exclusive                    pinned (tree == sequential; depth)

@@ -379,3 +379,23 @@ def test_empty_sequence_passes_state_through():
     assert o.shape == (1, 1, 0, 2)
     np.testing.assert_array_equal(S, S0)
     np.testing.assert_array_equal(z, z0)
+
+
+def test_decode_steps_from_carried_states_equal_the_definition():
+    """The decode step is the recurrence taken one token at a time (constant-
+    time recurrent inference, abstract): T one-token calls, each seeded with the
+    previous call's state, give the definition's rows, and one step adds exactly
+    psi(kh) v^T, read back through any unit u as (u.kh)^2 v."""
+    B, H, T, p, dv = 2, 1, 19, 5, 4
+    q, k, v = _rand_qkv(B, H, T, p, dv, seed=111)
+    n = p * (p + 1) // 2
+    S, z = np.zeros((B, H, n, dv)), np.zeros((B, H, n))
+    rows = []
+    for t in range(T):
+        S_prev = S
+        o, S, z = oracle.forward_recurrent(q[:, :, t:t + 1], k[:, :, t:t + 1], v[:, :, t:t + 1], S0=S, z0=z)
+        rows.append(o)
+        u = _unit(_rng(200 + t).standard_normal(p))
+        kh = _unit(k[0, 0, t])
+        np.testing.assert_allclose(oracle.lift(u) @ (S - S_prev)[0, 0], (u @ kh) ** 2 * v[0, 0, t], atol=1e-13)
+    np.testing.assert_allclose(np.concatenate(rows, axis=2), oracle.forward_plain(q, k, v), atol=1e-12)
