@@ -350,3 +350,136 @@ int kor_forward_chunked(const double* q, const double* k, const double* v, int B
 }
 
 }  // extern "C"
+
+namespace {
+
+// ---------------------------------------------------------------- block lifts
+// The two reduced PSD families ("two reduced PSD families" paragraph, after
+// the state-size discussion): g divides p, m = p/g, and each unit vector u
+// (the projected query or key) is cut into g blocks u_1..u_g of length m,
+// u_a = (u[a m], ..., u[a m + m - 1]).
+//   family 1, KATA-Sigma-g: psi(u) = sum_a u_a u_a^T, one m x m PSD matrix
+//     packed in m(m+1)/2 coordinates; <psi(q), psi(k)>_F = sum_{a,b} (q_a.k_b)^2.
+//   family 2, KATA-M-g: psi(u) = (u_1 u_1^T, ..., u_g u_g^T), g packed m x m
+//     matrices one after another, g m(m+1)/2 coordinates;
+//     <psi(q), psi(k)> = sum_a (q_a.k_a)^2.
+//   family 0: the full rank-one lift (g must be 1).
+// Packing inside an m x m block as for the full lift (upper triangle row by
+// row, off-diagonal coordinates times sqrt 2).
+
+// Width of the lift, or -1 if (family, g) does not fit p.
+int block_dim_i(int p, int family, int g) {
+    if (p <= 0 || g <= 0 || p % g != 0) return -1;
+    const int m = p / g;
+    if (family == 0) return g == 1 ? (int)packed_dim_i(p) : -1;
+    if (family == 1) return (int)packed_dim_i(m);
+    if (family == 2) return g * (int)packed_dim_i(m);
+    return -1;
+}
+
+void lift_block(const double* u, int p, int family, int g, double* psi) {
+    const int m = p / g;
+    const double r2 = std::sqrt(2.0);
+    if (family == 2) {
+        for (int a = 0; a < g; ++a) lift(u + a * m, m, psi + a * packed_dim_i(m));
+        return;
+    }
+    // family 0 (g = 1) and family 1: the block outer products summed
+    for (int i = 0; i < m; ++i)
+        for (int j = i; j < m; ++j) {
+            double sum = 0.0;
+            for (int a = 0; a < g; ++a) sum += u[a * m + i] * u[a * m + j];
+            psi[pidx(m, i, j)] = (i == j) ? sum : r2 * sum;
+        }
+}
+
+// The kernel of two unit vectors written from its definition (block dot
+// products squared), not through the lift.
+double block_kernel(const double* qu, const double* ku, int p, int family, int g) {
+    const int m = p / g;
+    double w = 0.0;
+    for (int a = 0; a < g; ++a)
+        for (int b = 0; b < g; ++b) {
+            if (family != 1 && a != b) continue;
+            const double c = dot(qu + a * m, ku + b * m, m);
+            w += c * c;
+        }
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kor_block_dim(int p, int family, int g) { return block_dim_i(p, family, g); }
+
+void kor_lift_block(const double* u, int p, int family, int g, double* psi) {
+    lift_block(u, p, family, g, psi);
+}
+
+// The plain definition with a block lift, every row:
+//   o_t = sum_{s<=t} w(qh_t, kh_s) v_s / sum_{s<=t} w(qh_t, kh_s),
+//   w = sum_{a,b} (q_a.k_b)^2 (Sigma-g) or sum_a (q_a.k_a)^2 (M-g).
+// Returns -1 if (family, g) does not fit p.
+int kor_forward_plain_block(const double* q, const double* k, const double* v, int B, int H, int T,
+                            int p, int dv, int family, int g, double* o, int nthreads) {
+    if (block_dim_i(p, family, g) < 0) return -1;
+    const int64_t heads = (int64_t)B * H;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const double* vh = v + bh * T * dv;
+        double* oh = o + bh * T * dv;
+        std::vector<double> qu = normalized_rows(q + bh * T * p, T, p), ku = normalized_rows(k + bh * T * p, T, p);
+        std::vector<double> num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            std::fill(num.begin(), num.end(), 0.0);
+            double den = 0.0;
+            for (int s = 0; s <= t; ++s) {
+                const double w = block_kernel(&qu[(size_t)t * p], &ku[(size_t)s * p], p, family, g);
+                den += w;
+                for (int j = 0; j < dv; ++j) num[j] += w * vh[(int64_t)s * dv + j];
+            }
+            for (int j = 0; j < dv; ++j) oh[(int64_t)t * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+    });
+    return 0;
+}
+
+// Token recurrence in the packed block lift (state [n_psi, dv], z [n_psi]):
+//   S += psi(kh_t) v_t^T,  z += psi(kh_t),  o_t = psi(qh_t)^T S / psi(qh_t)^T z,
+// optional initial / final state as in kor_forward_recurrent.  Returns -1 if
+// (family, g) does not fit p.
+int kor_forward_recurrent_block(const double* q, const double* k, const double* v, int B, int H, int T,
+                                int p, int dv, int family, int g, const double* S0, const double* z0,
+                                double* o, double* S_final, double* z_final, int nthreads) {
+    const int64_t n = block_dim_i(p, family, g);
+    if (n < 0) return -1;
+    const int64_t heads = (int64_t)B * H;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        std::vector<double> S((size_t)(n * dv), 0.0), z((size_t)n, 0.0);
+        if (S0) std::copy(S0 + bh * n * dv, S0 + (bh + 1) * n * dv, S.begin());
+        if (z0) std::copy(z0 + bh * n, z0 + (bh + 1) * n, z.begin());
+        std::vector<double> u((size_t)p), pk((size_t)n), pq((size_t)n), num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            const double* vt = v + (bh * T + t) * dv;
+            normalize(k + (bh * T + t) * p, p, u.data());
+            lift_block(u.data(), p, family, g, pk.data());
+            for (int64_t a = 0; a < n; ++a) {
+                for (int j = 0; j < dv; ++j) S[a * dv + j] += pk[a] * vt[j];
+                z[a] += pk[a];
+            }
+            normalize(q + (bh * T + t) * p, p, u.data());
+            lift_block(u.data(), p, family, g, pq.data());
+            std::fill(num.begin(), num.end(), 0.0);
+            for (int64_t a = 0; a < n; ++a)
+                for (int j = 0; j < dv; ++j) num[j] += pq[a] * S[a * dv + j];
+            const double den = dot(pq.data(), z.data(), n);
+            double* ot = o + (bh * T + t) * dv;
+            for (int j = 0; j < dv; ++j) ot[j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+        if (S_final) std::copy(S.begin(), S.end(), S_final + bh * n * dv);
+        if (z_final) std::copy(z.begin(), z.end(), z_final + bh * n);
+    });
+    return 0;
+}
+
+}  // extern "C"

@@ -20,6 +20,11 @@ Parity status of each function (pins live in tests/test_oracle_pins.py):
   forward_chunked, chunk_states     pinned (agrees with plain for every C,
                                      ragged T; split calls; state identity)
   scan_exclusive                    pinned (tree == sequential; depth)
+  block_dim, lift_block             pinned (page's state sizes, block outer products,
+                                     kernel identities, g = 1 is the full lift)
+  forward_plain_block,              pinned (agree with each other; g = 1 is the full
+  forward_recurrent_block            forward; Sigma-p running mean; disjoint blocks;
+                                     block-permutation behaviour; split calls)
 """
 import ctypes
 
@@ -32,6 +37,9 @@ _D = ctypes.POINTER(ctypes.c_double)
 _I64 = ctypes.POINTER(ctypes.c_int64)
 SCAN_SEQUENTIAL = 0
 SCAN_TREE = 1
+LIFT_FULL = 0
+LIFT_SIGMA = 1
+LIFT_MULTI = 2
 
 
 def _bind(lib):
@@ -56,6 +64,14 @@ def _bind(lib):
     lib.kor_scan_exclusive.restype = i
     lib.kor_forward_chunked.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
     lib.kor_forward_chunked.restype = i
+    lib.kor_block_dim.argtypes = [i, i, i]
+    lib.kor_block_dim.restype = i
+    lib.kor_lift_block.argtypes = [_D, i, i, i, _D]
+    lib.kor_lift_block.restype = None
+    lib.kor_forward_plain_block.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _D, i]
+    lib.kor_forward_plain_block.restype = i
+    lib.kor_forward_recurrent_block.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
+    lib.kor_forward_recurrent_block.restype = i
     return lib
 
 
@@ -183,6 +199,58 @@ def forward_chunked(q, k, v, C, mode=SCAN_SEQUENTIAL, S0=None, z0=None, nthreads
     z = np.empty((B, H, n))
     _load().kor_forward_chunked(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, C, mode, _ptr(S0),
                                 _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
+    return o, S, z
+
+
+# ---------------------------------------------------------------- block lifts
+
+def block_dim(p: int, family: int, g: int) -> int:
+    """Width of the lift: full p(p+1)/2 (g = 1), Sigma-g m(m+1)/2, M-g g m(m+1)/2
+    with m = p/g; -1 if (family, g) does not fit p."""
+    return _load().kor_block_dim(int(p), int(family), int(g))
+
+
+def _check_block(p, family, g):
+    n = block_dim(p, family, g)
+    if n < 0:
+        raise ValueError(f"lift family {family} with g={g} does not fit p={p}")
+    return n
+
+
+def lift_block(u, family, g):
+    """Packed block lift of one vector (used as given, not normalised)."""
+    u = _f64(u)
+    n = _check_block(u.shape[-1], family, g)
+    out = np.empty(n)
+    _load().kor_lift_block(_ptr(u), u.shape[-1], int(family), int(g), _ptr(out))
+    return out
+
+
+def forward_plain_block(q, k, v, family, g, nthreads=0):
+    """The definition with a block-lift kernel (block dot products squared)."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    _check_block(p, family, g)
+    o = np.empty((B, H, T, dv))
+    _load().kor_forward_plain_block(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, int(family), int(g), _ptr(o),
+                                    nthreads)
+    return o
+
+
+def forward_recurrent_block(q, k, v, family, g, S0=None, z0=None, nthreads=0):
+    """Token recurrence in the packed block lift. Returns (o, S_final, z_final)."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    n = _check_block(p, family, g)
+    S0 = None if S0 is None else _f64(S0).reshape(B, H, n, dv)
+    z0 = None if z0 is None else _f64(z0).reshape(B, H, n)
+    o = np.empty((B, H, T, dv))
+    S = np.empty((B, H, n, dv))
+    z = np.empty((B, H, n))
+    _load().kor_forward_recurrent_block(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, int(family), int(g),
+                                        _ptr(S0), _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
     return o, S, z
 
 

@@ -42,6 +42,34 @@ MUTATIONS = {
         "                for (int j = 0; j < dv; ++j) S[a * dv + j] += pk[a] * vt[(j + 1) % dv];"),
 }
 
+# Slips in the block lifts (KATA-Sigma-g / KATA-M-g), caught by the block pins.
+BLOCK_MUTATIONS = {
+    "block_drop_sqrt2": ("psi[pidx(m, i, j)] = (i == j) ? sum : r2 * sum;",
+                         "psi[pidx(m, i, j)] = (i == j) ? sum : sum;"),
+    "block_sigma_without_cross_terms": ("if (family != 1 && a != b) continue;", "if (a != b) continue;"),
+    "block_multi_with_cross_terms": ("if (family != 1 && a != b) continue;", "if (family == 0 && a != b) continue;"),
+    "block_multi_wrong_block_start": ("lift(u + a * m, m, psi + a * packed_dim_i(m));",
+                                      "lift(u + a, m, psi + a * packed_dim_i(m));"),
+    "block_interleaved_blocks": ("sum += u[a * m + i] * u[a * m + j];", "sum += u[a + i * g] * u[a + j * g];"),
+    "block_kernel_diagonal_pairs": ("dot(qu + a * m, ku + b * m, m)", "dot(qu + a * m, ku + a * m, m)"),
+    "block_state_skips_normalise": ("normalize(k + (bh * T + t) * p, p, u.data());\n            lift_block(",
+                                    "std::copy(k + (bh * T + t) * p, k + (bh * T + t) * p + p, u.begin());\n"
+                                    "            lift_block("),
+}
+
+
+def _block_battery():
+    import tests.test_oracle_block_pins as bp
+    yield lambda: bp.test_state_sizes_at_d64()
+    yield lambda: bp.test_lifts_are_the_block_outer_products(12, 3)
+    yield lambda: bp.test_inner_product_identities(12, 3)
+    yield lambda: bp.test_g1_is_the_full_lift(4)
+    yield lambda: bp.test_definition_and_lifted_recurrence_agree(bp.SIGMA, 12, 3, 9)
+    yield lambda: bp.test_definition_and_lifted_recurrence_agree(bp.MULTI, 12, 4, 30)
+    yield lambda: bp.test_sigma_with_scalar_blocks_is_the_running_mean()
+    yield lambda: bp.test_disjoint_blocks_separate_the_families()
+    yield lambda: bp.test_block_permutations()
+
 
 def _battery():
     """Pins that run in well under a second each."""
@@ -61,9 +89,10 @@ def _battery():
         yield lambda case=case: pins.test_quadratic_recurrent_chunked_agree(*case)
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
+@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(BLOCK_MUTATIONS))
 def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
-    old, new = MUTATIONS[name]
+    block = name in BLOCK_MUTATIONS
+    old, new = (BLOCK_MUTATIONS if block else MUTATIONS)[name]
     src = open(obuild.SRC).read()
     assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mutated = tmp_path / "mut.cpp"
@@ -74,7 +103,7 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     subprocess.run(cmd, check=True)
     monkeypatch.setattr(km, "_lib", km._bind(ctypes.CDLL(os.fspath(lib))))
     failures = 0
-    for pin in _battery():
+    for pin in (_block_battery() if block else _battery()):
         try:
             pin()
         except AssertionError:
@@ -84,4 +113,6 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
 
 def test_unmutated_battery_passes():
     for pin in _battery():
+        pin()
+    for pin in _block_battery():
         pin()
