@@ -160,6 +160,62 @@ KATA_API kata_status kata_decode_step(const void* q, const void* k, const void* 
                                       float* z, cudaStream_t stream);
 
 /*
+ * Block lifts: the two reduced PSD families of the paragraph that follows
+ * the state-size discussion.  g divides p, m = p/g, and each unit query or
+ * key u is cut into g contiguous blocks u_a = (u[a m], ..., u[a m + m - 1]):
+ *   KATA_LIFT_SIGMA (KATA-Sigma-g): psi(u) = sum_a u_a u_a^T, one m x m PSD
+ *     matrix, n = m(m+1)/2; kernel <psi(q), psi(k)> = sum_{a,b} (q_a.k_b)^2.
+ *   KATA_LIFT_MULTI (KATA-M-g): psi(u) = (u_1 u_1^T, ..., u_g u_g^T), the g
+ *     packed blocks one after another, n = g m(m+1)/2; kernel
+ *     sum_a (q_a.k_a)^2.
+ *   KATA_LIFT_FULL: the rank-one lift of Eq. 8 (g must be 1).
+ * Inside a block the packing above (idx with m for p, off-diagonals times
+ * sqrt 2).  Both families are the full lift at g = 1.  The *_block calls
+ * compute the forwards above with this kernel in place of (qh.kh)^2 and
+ * this lift in place of psi; states are [B,H,n,dv] / [B,H,n] with the
+ * lift's n.  They run on CUDA cores in fp32 for either dtype.
+ */
+typedef enum { KATA_LIFT_FULL = 0, KATA_LIFT_SIGMA = 1, KATA_LIFT_MULTI = 2 } kata_lift_family;
+
+/* n of a lift for head dimension p; -1 if g < 1, g does not divide p, the
+ * family is unknown, or family is KATA_LIFT_FULL with g != 1. */
+KATA_API int kata_lift_dim(kata_lift_family family, int p, int g);
+
+/* Bytes of workspace kata_forward_chunked_block needs (0 if none or invalid). */
+KATA_API size_t kata_chunked_block_workspace_bytes(kata_dtype dtype, kata_lift_family family, int g, int B,
+                                                   int H, int T, int p, int dv, int C);
+
+/*
+ * Chunked-state form with a block lift: the three phases of
+ * kata_forward_chunked (local chunk states in the lift, exclusive prefix
+ * over chunks by `mode`, per chunk the prefix readout plus the local causal
+ * part, here from block dot products).  Arguments, state and workspace
+ * rules as for kata_forward_chunked, with n = kata_lift_dim(family, p, g).
+ * KATA_ERR_INVALID_ARG for an unknown family or g < 1, KATA_ERR_UNSUPPORTED
+ * if g does not fit p.
+ */
+KATA_API kata_status kata_forward_chunked_block(const void* q, const void* k, const void* v, void* o,
+                                                kata_dtype dtype, int B, int H, int T, int p, int dv,
+                                                int C, kata_lift_family family, int g,
+                                                kata_scan_mode mode, const float* S0, const float* z0,
+                                                float* S_final, float* z_final, void* workspace,
+                                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Flash-style form with a block lift's kernel; as kata_forward_quadratic
+ * (no tile hint), errors as kata_forward_chunked_block. */
+KATA_API kata_status kata_forward_quadratic_block(const void* q, const void* k, const void* v, void* o,
+                                                  kata_dtype dtype, int B, int H, int T, int p,
+                                                  int dv, kata_lift_family family, int g,
+                                                  cudaStream_t stream);
+
+/* Decode step with a block lift; as kata_decode_step, with S [B,H,n,dv] and
+ * z [B,H,n] for n = kata_lift_dim(family, p, g). */
+KATA_API kata_status kata_decode_step_block(const void* q, const void* k, const void* v, void* o,
+                                            kata_dtype dtype, int B, int H, int p, int dv,
+                                            kata_lift_family family, int g, float* S, float* z,
+                                            cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: KATA_OK, or KATA_ERR_TIMEOUT if a bounded device-side
  * wait expired in an earlier call (that call's outputs are then invalid).

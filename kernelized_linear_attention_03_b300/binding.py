@@ -23,11 +23,16 @@ KATA_FP32 = 0
 KATA_BF16 = 1
 KATA_SCAN_SEQUENTIAL = 0
 KATA_SCAN_TREE = 1
+KATA_LIFT_FULL = 0
+KATA_LIFT_SIGMA = 1
+KATA_LIFT_MULTI = 2
 
 SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_chunked_workspace_bytes", "kata_forward_chunked", "kata_chunk_state_scan",
            "kata_scan_states", "kata_get_device_status", "kata_trace_start", "kata_trace_stop",
-           "kata_trace_get", "kata_forward_chunked_noalloc", "kata_decode_step")
+           "kata_trace_get", "kata_forward_chunked_noalloc", "kata_decode_step", "kata_lift_dim",
+           "kata_chunked_block_workspace_bytes", "kata_forward_chunked_block", "kata_forward_quadratic_block",
+           "kata_decode_step_block")
 
 
 class KataError(RuntimeError):
@@ -69,6 +74,16 @@ def load():
     lib.kata_forward_chunked_noalloc.restype = I
     lib.kata_decode_step.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     lib.kata_decode_step.restype = I
+    lib.kata_lift_dim.argtypes = [I, I, I]
+    lib.kata_lift_dim.restype = I
+    lib.kata_chunked_block_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
+    lib.kata_chunked_block_workspace_bytes.restype = Z
+    lib.kata_forward_chunked_block.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P, P, Z, P]
+    lib.kata_forward_chunked_block.restype = I
+    lib.kata_forward_quadratic_block.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, P]
+    lib.kata_forward_quadratic_block.restype = I
+    lib.kata_decode_step_block.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P]
+    lib.kata_decode_step_block.restype = I
     lib.kata_trace_start.argtypes = [I]
     lib.kata_trace_start.restype = I
     lib.kata_trace_stop.argtypes = []
@@ -236,6 +251,66 @@ def kata_decode_step(q, k, v, S, z, o=None, stream=None):
     _check(load().kata_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, p, dv,
                                    _ptr(S), _ptr(z), _stream(stream)),
            "kata_decode_step")
+    return o
+
+
+def kata_lift_dim(family, p, g):
+    return load().kata_lift_dim(int(family), int(p), int(g))
+
+
+def kata_chunked_block_workspace_bytes(dtype, family, g, B, H, T, p, dv, C):
+    code = dtype if isinstance(dtype, int) else (KATA_FP32 if dtype == torch.float32 else KATA_BF16)
+    return int(load().kata_chunked_block_workspace_bytes(code, int(family), int(g), B, H, T, p, dv, C))
+
+
+def kata_forward_chunked_block(q, k, v, C, family, g, mode=KATA_SCAN_TREE, S0=None, z0=None, o=None,
+                               S_final=None, z_final=None, workspace=None, stream=None):
+    """Chunked forward with a block lift (KATA-Sigma-g / KATA-M-g); returns o,
+    or (o, S_final, z_final) when state buffers are given."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    need = kata_chunked_block_workspace_bytes(_dtype_code(q), family, g, B, H, T, p, dv, C)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kata_forward_chunked_block(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, T, p, dv,
+                                             int(C), int(family), int(g), int(mode), _ptr(S0), _ptr(z0),
+                                             _ptr(S_final), _ptr(z_final), _ptr(workspace), ws_bytes,
+                                             _stream(stream)),
+           "kata_forward_chunked_block")
+    return o if S_final is None else (o, S_final, z_final)
+
+
+def kata_forward_quadratic_block(q, k, v, family, g, o=None, stream=None):
+    """Flash-style forward with a block lift's kernel; returns o."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_forward_quadratic_block(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, T, p, dv,
+                                               int(family), int(g), _stream(stream)),
+           "kata_forward_quadratic_block")
+    return o
+
+
+def kata_decode_step_block(q, k, v, S, z, family, g, o=None, stream=None):
+    """Decode step with a block lift: S [B,H,n,dv], z [B,H,n] float32 with
+    n = kata_lift_dim(family, p, g), updated in place.  Returns o [B,H,dv]."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,p] and v [B,H,dv]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share one dtype")
+    B, H, p = q.shape
+    dv = v.shape[-1]
+    n = kata_lift_dim(family, p, g)
+    if S.shape != (B, H, n, dv) or z.shape != (B, H, n) or S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise ValueError("expected float32 S [B,H,n,dv] and z [B,H,n] for the lift")
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_decode_step_block(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, p, dv,
+                                         int(family), int(g), _ptr(S), _ptr(z), _stream(stream)),
+           "kata_decode_step_block")
     return o
 
 

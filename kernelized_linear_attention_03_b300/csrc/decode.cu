@@ -9,13 +9,14 @@
 // each CTA updates its rows with 16-byte loads and stores (a state row of dv
 // floats is dv/4 threads wide) and forms a partial readout [num | den].  The
 // cluster's rank-0 CTA sums the NSPLIT partials out of the other CTAs' shared
-// memory, in rank order, and divides.
+// memory, in rank order, and divides.  The same kernel serves the block lifts
+// (KATA-Sigma-g, KATA-M-g; BLOCK = true) with the lift's packed rows.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <cstdint>
 
-#include "kata_device.cuh"
+#include "block_lift.cuh"
 #include "kata_internal.h"
 
 namespace kata {
@@ -27,11 +28,14 @@ constexpr int kDecThreads = 256;
 constexpr int kDecUnroll = 4;  // state rows of a thread in flight at once
 constexpr int kDecMaxSplit = 8;
 
-template <typename Tin, int P, int DV>
+template <typename Tin, int P, int DV, bool BLOCK>
 __global__ void __launch_bounds__(kDecThreads)
 decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-                   Tin* __restrict__ o, float* __restrict__ S, float* __restrict__ z) {
-    constexpr int N = P * (P + 1) / 2;
+                   Tin* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int family, int g,
+                   int n_block) {
+    // full lift: N = p(p+1)/2; block lift (family, g): N = n_block
+    const int N = BLOCK ? n_block : P * (P + 1) / 2;
+    const int m = BLOCK ? P / g : P, nm = m * (m + 1) / 2;
     constexpr int CPR = DV / 4;            // 16-byte columns of a state row
     constexpr int RP = kDecThreads / CPR;  // state rows per pass of the block
     constexpr int NW = kDecThreads / 32;
@@ -64,9 +68,10 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    // (i, start): the lift row i holding packed row r, start = idx(i, i);
-    // r only grows along a thread's walk, so i only moves forward.
-    int i = 0, start = 0;
+    // (i, start): the lift row i holding packed row r, start = idx(i, i)
+    // (inside block blk, whose first packed row is bstart, for M-g); r only
+    // grows along a thread's walk, so i and blk only move forward.
+    int i = 0, start = 0, blk = 0, bstart = 0;
     for (int rb = r0 + rr; rb < r1; rb += RP * kDecUnroll) {
         float4 s[kDecUnroll];
         float zr[kDecUnroll];
@@ -84,13 +89,44 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
         for (int u = 0; u < kDecUnroll; ++u) {
             const int r = rb + u * RP;
             if (r < r1) {
-                while (r >= start + (P - i)) {
-                    start += P - i;
-                    ++i;
+                float fk, fq;
+                if constexpr (!BLOCK) {
+                    while (r >= start + (P - i)) {
+                        start += P - i;
+                        ++i;
+                    }
+                    const int j = i + (r - start);
+                    const float w = i == j ? 1.f : kSqrt2;
+                    fk = w * kh[i] * kh[j];
+                    fq = w * qh[i] * qh[j];
+                } else {
+                    if (family == kLiftMulti)
+                        while (r >= bstart + nm) {
+                            bstart += nm;
+                            ++blk;
+                            i = 0;
+                            start = 0;
+                        }
+                    const int rl = r - bstart;
+                    while (rl >= start + (m - i)) {
+                        start += m - i;
+                        ++i;
+                    }
+                    const int j = i + (rl - start);
+                    const float w = i == j ? 1.f : kSqrt2;
+                    if (family == kLiftMulti) {
+                        fk = w * kh[blk * m + i] * kh[blk * m + j];
+                        fq = w * qh[blk * m + i] * qh[blk * m + j];
+                    } else {
+                        float sk = 0.f, sq = 0.f;
+                        for (int a = 0; a < g; ++a) {
+                            sk = fmaf(kh[a * m + i], kh[a * m + j], sk);
+                            sq = fmaf(qh[a * m + i], qh[a * m + j], sq);
+                        }
+                        fk = w * sk;
+                        fq = w * sq;
+                    }
                 }
-                const int j = i + (r - start);
-                const float w = i == j ? 1.f : kSqrt2;
-                const float fk = w * kh[i] * kh[j], fq = w * qh[i] * qh[j];
                 float4 t = s[u];
                 t.x = fmaf(fk, v4.x, t.x);
                 t.y = fmaf(fk, v4.y, t.y);
@@ -153,8 +189,10 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
 
 template <typename Tin, int P, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH,
-                         cudaStream_t s) {
-    constexpr int N = P * (P + 1) / 2;
+                         int family, int g, cudaStream_t s) {
+    const bool block = family != kLiftFull;
+    const int N = block ? block_lift_dim(family, P, g) : P * (P + 1) / 2;
+    if (N <= 0) return cudaErrorInvalidValue;
     constexpr int RP = kDecThreads / (DV / 4);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -175,31 +213,37 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, f
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    KATA_TRACED("decode_step", s,
-                e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV>, static_cast<const Tin*>(q),
-                                       static_cast<const Tin*>(k), static_cast<const Tin*>(v), static_cast<Tin*>(o),
-                                       S, z));
+    if (block)
+        KATA_TRACED("decode_step_block", s,
+                    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV, true>, static_cast<const Tin*>(q),
+                                           static_cast<const Tin*>(k), static_cast<const Tin*>(v),
+                                           static_cast<Tin*>(o), S, z, family, g, N));
+    else
+        KATA_TRACED("decode_step", s,
+                    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV, false>, static_cast<const Tin*>(q),
+                                           static_cast<const Tin*>(k), static_cast<const Tin*>(v),
+                                           static_cast<Tin*>(o), S, z, family, g, N));
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, int P>
 cudaError_t by_dv(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH, int dv,
-                  cudaStream_t s) {
+                  int family, int g, cudaStream_t s) {
     switch (dv) {
-        case 16: return launch_typed<Tin, P, 16>(q, k, v, o, S, z, BH, s);
-        case 32: return launch_typed<Tin, P, 32>(q, k, v, o, S, z, BH, s);
-        case 64: return launch_typed<Tin, P, 64>(q, k, v, o, S, z, BH, s);
+        case 16: return launch_typed<Tin, P, 16>(q, k, v, o, S, z, BH, family, g, s);
+        case 32: return launch_typed<Tin, P, 32>(q, k, v, o, S, z, BH, family, g, s);
+        case 64: return launch_typed<Tin, P, 64>(q, k, v, o, S, z, BH, family, g, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <typename Tin>
 cudaError_t by_p(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH, int p, int dv,
-                 cudaStream_t s) {
+                 int family, int g, cudaStream_t s) {
     switch (p) {
-        case 16: return by_dv<Tin, 16>(q, k, v, o, S, z, BH, dv, s);
-        case 32: return by_dv<Tin, 32>(q, k, v, o, S, z, BH, dv, s);
-        case 64: return by_dv<Tin, 64>(q, k, v, o, S, z, BH, dv, s);
+        case 16: return by_dv<Tin, 16>(q, k, v, o, S, z, BH, dv, family, g, s);
+        case 32: return by_dv<Tin, 32>(q, k, v, o, S, z, BH, dv, family, g, s);
+        case 64: return by_dv<Tin, 64>(q, k, v, o, S, z, BH, dv, family, g, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -207,9 +251,9 @@ cudaError_t by_p(const void* q, const void* k, const void* v, void* o, float* S,
 }  // namespace
 
 cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
-                               float* z, int BH, int p, int dv, cudaStream_t s) {
-    return dtype == 0 ? by_p<float>(q, k, v, o, S, z, BH, p, dv, s)
-                      : by_p<__nv_bfloat16>(q, k, v, o, S, z, BH, p, dv, s);
+                               float* z, int BH, int p, int dv, int family, int g, cudaStream_t s) {
+    return dtype == 0 ? by_p<float>(q, k, v, o, S, z, BH, p, dv, family, g, s)
+                      : by_p<__nv_bfloat16>(q, k, v, o, S, z, BH, p, dv, family, g, s);
 }
 
 }  // namespace kata

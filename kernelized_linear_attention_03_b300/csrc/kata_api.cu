@@ -82,8 +82,8 @@ struct ChunkedWs {
     size_t i_off;  // tensor-core path: intra-chunk rows
 };
 
-ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C) {
-    const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C, n = packed(p);
+ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C, int64_t n_lift = 0) {
+    const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C, n = n_lift > 0 ? n_lift : packed(p);
     ChunkedWs w;
     w.s_off = 0;
     w.i_off = 0;
@@ -118,6 +118,41 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
     pl.ws.i_off = off;
     pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, dv), 256);
     return pl;
+}
+
+// Width of a lift (full, Sigma-g, M-g); -1 if (family, g) does not fit p.
+int lift_dim(int family, int p, int g) {
+    if (p <= 0 || g <= 0 || p % g != 0) return -1;
+    const int64_t m = p / g, nm = m * (m + 1) / 2;
+    if (family == KATA_LIFT_FULL) return g == 1 ? (int)nm : -1;
+    if (family == KATA_LIFT_SIGMA) return (int)nm;
+    if (family == KATA_LIFT_MULTI) return (int)(g * nm);
+    return -1;
+}
+
+kata_status check_lift(kata_lift_family family, int p, int g) {
+    if (family != KATA_LIFT_FULL && family != KATA_LIFT_SIGMA && family != KATA_LIFT_MULTI) return KATA_ERR_INVALID_ARG;
+    if (g < 1) return KATA_ERR_INVALID_ARG;
+    return lift_dim(family, p, g) > 0 ? KATA_OK : KATA_ERR_UNSUPPORTED;
+}
+
+// Shared body of the decode steps (shapes and lift already checked).
+kata_status decode_common(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B, int H, int p,
+                          int dv, int family, int g, float* S, float* z, cudaStream_t stream) {
+    kata_status st = KATA_OK;
+    const int64_t BH = (int64_t)B * H, n = lift_dim(family, p, g);
+    if (BH == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * BH * p, v_bytes = elem_bytes(dt) * BH * dv;
+    const size_t sb = sizeof(float) * (size_t)(BH * n * dv), zb = sizeof(float) * (size_t)(BH * n);
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
+        (st = check_buffer(S, sb)) != KATA_OK || (st = check_buffer(z, zb)) != KATA_OK)
+        return st;
+    // S and z are updated in place by different threads: they must not overlap.
+    const char* sp = reinterpret_cast<const char*>(S);
+    const char* zp = reinterpret_cast<const char*>(z);
+    if (sp < zp + zb && zp < sp + sb) return KATA_ERR_INVALID_ARG;
+    return cuda_status(kata::launch_decode_step(dt, q, k, v, o, S, z, (int)BH, p, dv, family, g, stream));
 }
 
 }  // namespace
@@ -289,19 +324,88 @@ kata_status kata_decode_step(const void* q, const void* k, const void* v, void* 
                              int p, int dv, float* S, float* z, cudaStream_t stream) {
     kata_status st = check_shapes(dt, B, H, 1, p, dv);
     if (st != KATA_OK) return st;
-    const int64_t BH = (int64_t)B * H, n = packed(p);
+    return decode_common(q, k, v, o, dt, B, H, p, dv, KATA_LIFT_FULL, 1, S, z, stream);
+}
+
+
+int kata_lift_dim(kata_lift_family family, int p, int g) {
+    if (family != KATA_LIFT_FULL && family != KATA_LIFT_SIGMA && family != KATA_LIFT_MULTI) return -1;
+    return lift_dim(family, p, g);
+}
+
+size_t kata_chunked_block_workspace_bytes(kata_dtype dt, kata_lift_family family, int g, int B, int H, int T, int p,
+                                          int dv, int C) {
+    if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C) || check_lift(family, p, g) != KATA_OK) return 0;
+    if ((int64_t)B * H * T == 0) return 0;
+    return chunked_ws(B, H, T, p, dv, C, lift_dim(family, p, g)).total;
+}
+
+kata_status kata_forward_chunked_block(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B,
+                                       int H, int T, int p, int dv, int C, kata_lift_family family, int g,
+                                       kata_scan_mode mode, const float* S0, const float* z0, float* S_final,
+                                       float* z_final, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if ((st = check_lift(family, p, g)) != KATA_OK) return st;
+    if (!c_ok(C)) return KATA_ERR_UNSUPPORTED;
+    if (mode != KATA_SCAN_SEQUENTIAL && mode != KATA_SCAN_TREE) return KATA_ERR_INVALID_ARG;
+    if ((S0 == nullptr) != (z0 == nullptr)) return KATA_ERR_INVALID_ARG;
+    if ((S_final == nullptr) != (z_final == nullptr)) return KATA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H, n = lift_dim(family, p, g);
     if (BH == 0) return KATA_OK;
-    const size_t qk_bytes = elem_bytes(dt) * BH * p, v_bytes = elem_bytes(dt) * BH * dv;
-    const size_t sb = sizeof(float) * (size_t)(BH * n * dv), zb = sizeof(float) * (size_t)(BH * n);
-    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
-        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
-        (st = check_buffer(S, sb)) != KATA_OK || (st = check_buffer(z, zb)) != KATA_OK)
+    const size_t s_bytes = sizeof(float) * BH * n * dv, z_bytes = sizeof(float) * BH * n;
+    if (S0 && ((st = check_buffer(S0, s_bytes)) != KATA_OK || (st = check_buffer(z0, z_bytes)) != KATA_OK))
         return st;
-    // S and z are updated in place by different threads: they must not overlap.
-    const char* sp = reinterpret_cast<const char*>(S);
-    const char* zp = reinterpret_cast<const char*>(z);
-    if (sp < zp + zb && zp < sp + sb) return KATA_ERR_INVALID_ARG;
-    return cuda_status(kata::launch_decode_step(dt, q, k, v, o, S, z, (int)BH, p, dv, stream));
+    if (S_final &&
+        ((st = check_buffer(S_final, s_bytes)) != KATA_OK || (st = check_buffer(z_final, z_bytes)) != KATA_OK))
+        return st;
+    if (T == 0) {
+        if (S_final == nullptr) return KATA_OK;
+        cudaError_t e = kata::launch_copy_or_zero(S0, S_final, BH * n * dv, stream);
+        if (e == cudaSuccess) e = kata::launch_copy_or_zero(z0, z_final, BH * n, stream);
+        return cuda_status(e);
+    }
+    const size_t qk_bytes = elem_bytes(dt) * BH * T * p, v_bytes = elem_bytes(dt) * BH * T * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
+        return st;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C, n);
+    if (ws == nullptr || ws_bytes < w.total) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
+    const int64_t NC = (T + C - 1) / C;
+    float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
+    float* z_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
+    cudaError_t e = kata::launch_block_states(dt, k, v, S_loc, z_loc, (int)BH, T, p, dv, C, family, g, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, S_loc, S_loc, S0, S_final, BH, NC, n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, z_loc, z_loc, z0, z_final, BH, NC, n, stream);
+    if (e == cudaSuccess)
+        e = kata::launch_block_output(dt, q, k, v, S_loc, z_loc, o, (int)BH, T, p, dv, C, family, g, stream);
+    return cuda_status(e);
+}
+
+kata_status kata_forward_quadratic_block(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B,
+                                         int H, int T, int p, int dv, kata_lift_family family, int g,
+                                         cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if ((st = check_lift(family, p, g)) != KATA_OK) return st;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
+        return st;
+    return cuda_status(kata::launch_block_quadratic(dt, q, k, v, o, B * H, T, p, dv, family, g, stream));
+}
+
+kata_status kata_decode_step_block(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B, int H,
+                                   int p, int dv, kata_lift_family family, int g, float* S, float* z,
+                                   cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, 1, p, dv);
+    if (st != KATA_OK) return st;
+    if ((st = check_lift(family, p, g)) != KATA_OK) return st;
+    return decode_common(q, k, v, o, dt, B, H, p, dv, family, g, S, z, stream);
 }
 
 kata_status kata_get_device_status(cudaStream_t stream) {

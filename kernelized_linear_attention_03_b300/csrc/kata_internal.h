@@ -63,8 +63,22 @@ cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, f
 
 // Recurrent decode step, any dtype: S += psi(kh) v^T, z += psi(kh) in place
 // (S [BH,n,dv], z [BH,n] fp32), o = psi(qh)^T S / psi(qh)^T z [BH,dv].
+// family 0 (g = 1): the full lift; 1 / 2: KATA-Sigma-g / KATA-M-g
+// (block_lift.cuh), n = block_lift_dim(family, p, g).
 cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
-                               float* z, int BH, int p, int dv, cudaStream_t s);
+                               float* z, int BH, int p, int dv, int family, int g, cudaStream_t s);
+
+// Block-lift forwards on CUDA cores (family 1 Sigma-g, 2 M-g; block_lift.cuh),
+// any dtype: per-chunk states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] in the
+// block lift; per-chunk output from their exclusive prefixes; the
+// flash-style quadratic form.
+cudaError_t launch_block_states(int dtype, const void* k, const void* v, float* S_loc, float* z_loc, int BH, int T,
+                                int p, int dv, int C, int family, int g, cudaStream_t s);
+cudaError_t launch_block_output(int dtype, const void* q, const void* k, const void* v, const float* P,
+                                const float* Pz, void* o, int BH, int T, int p, int dv, int C, int family, int g,
+                                cudaStream_t s);
+cudaError_t launch_block_quadratic(int dtype, const void* q, const void* k, const void* v, void* o, int BH, int T,
+                                   int p, int dv, int family, int g, cudaStream_t s);
 
 // dst[i] = src ? src[i] : 0 for i < count (fp32), used for pass-through states.
 cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s);

@@ -137,3 +137,38 @@ def test_decode_argument_errors(lib):
     assert _dec(lib, ptr=MISALIGNED) == kb.KATA_ERR_INVALID_ARG
     # no heads: nothing to do, pointers unused
     assert _dec(lib, B=0) == kb.KATA_OK
+
+
+def test_lift_dims_and_block_workspace(lib):
+    L = kb
+    assert kb.kata_lift_dim(L.KATA_LIFT_SIGMA, 64, 2) == 528
+    assert kb.kata_lift_dim(L.KATA_LIFT_MULTI, 64, 2) == 1056
+    assert kb.kata_lift_dim(L.KATA_LIFT_SIGMA, 16, 4) == 10
+    assert kb.kata_lift_dim(L.KATA_LIFT_FULL, 64, 1) == 2080
+    assert kb.kata_lift_dim(L.KATA_LIFT_FULL, 64, 2) == -1
+    assert kb.kata_lift_dim(L.KATA_LIFT_SIGMA, 64, 3) == -1
+    assert kb.kata_lift_dim(5, 64, 2) == -1
+    # chunk states [BH, NC, n, dv] and [BH, NC, n] fp32, each 256-byte aligned
+    got = kb.kata_chunked_block_workspace_bytes(kb.KATA_FP32, L.KATA_LIFT_MULTI, 2, 1, 2, 100, 16, 16, 32)
+    nc, n = 4, 72
+    assert got == ((2 * nc * n * 16 * 4 + 255) // 256) * 256 + ((2 * nc * n * 4 + 255) // 256) * 256
+    assert kb.kata_chunked_block_workspace_bytes(kb.KATA_FP32, L.KATA_LIFT_SIGMA, 3, 1, 1, 64, 16, 16, 32) == 0
+
+
+def test_block_argument_errors(lib):
+    P = None
+    f = lib.kata_forward_chunked_block
+    args = lambda fam, g, B=1: (P, P, P, P, kb.KATA_FP32, B, 1, 8, 16, 16, 32, fam, g, 0, P, P, P, P, P, 0, P)  # noqa
+    assert f(*args(9, 2)) == kb.KATA_ERR_INVALID_ARG
+    assert f(*args(kb.KATA_LIFT_SIGMA, 0)) == kb.KATA_ERR_INVALID_ARG
+    assert f(*args(kb.KATA_LIFT_SIGMA, 3)) == kb.KATA_ERR_UNSUPPORTED
+    assert f(*args(kb.KATA_LIFT_FULL, 2)) == kb.KATA_ERR_UNSUPPORTED
+    assert f(*args(kb.KATA_LIFT_MULTI, 2)) == kb.KATA_ERR_INVALID_ARG  # null pointers
+    assert f(*args(kb.KATA_LIFT_MULTI, 2, B=0)) == kb.KATA_OK
+    q = lib.kata_forward_quadratic_block
+    assert q(P, P, P, P, kb.KATA_BF16, 1, 1, 8, 16, 16, kb.KATA_LIFT_SIGMA, 32, P) == kb.KATA_ERR_UNSUPPORTED
+    assert q(P, P, P, P, kb.KATA_BF16, 0, 1, 8, 16, 16, kb.KATA_LIFT_SIGMA, 2, P) == kb.KATA_OK
+    d = lib.kata_decode_step_block
+    assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, 4, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
+    assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
+    assert d(P, P, P, P, kb.KATA_BF16, 0, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_OK
