@@ -482,4 +482,79 @@ int kor_forward_recurrent_block(const double* q, const double* k, const double* 
     return 0;
 }
 
+// ---------------------------------------------------------------- backward
+// Gradient of the plain definition.  The pages give no backward algorithm
+// (the training use of the forward is named in the abstract); this is the
+// chain rule through the definition
+//   o_t = N_t / D_t,  N_t = sum_{s<=t} w_ts v_s,  D_t = sum_{s<=t} w_ts,
+//   w_ts = c_ts^2,  c_ts = qh_t . kh_s,  qh = q / ||q||,  kh = k / ||k||.
+// With G_t = dL/do_t:
+//   dL/dv_s  = sum_{t>=s} (w_ts / D_t) G_t
+//   dL/dw_ts = G_t . (v_s - o_t) / D_t
+//   dL/dc_ts = 2 c_ts dL/dw_ts
+//   dL/dqh_t = sum_{s<=t} dL/dc_ts kh_s,   dL/dkh_s = sum_{t>=s} dL/dc_ts qh_t
+//   dL/dq_t  = (dL/dqh_t - (qh_t . dL/dqh_t) qh_t) / ||q_t||   (k likewise).
+// A row with D_t = 0 (its output is fixed at zero) passes no gradient, and a
+// zero q or k vector (where the projection has no derivative) receives none.
+int kor_backward_plain(const double* q, const double* k, const double* v, const double* dO, int B, int H,
+                       int T, int p, int dv, double* dq, double* dk, double* dvv, int nthreads) {
+    const int64_t heads = (int64_t)B * H;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const double* qh = q + bh * T * p;
+        const double* kh = k + bh * T * p;
+        const double* vh = v + bh * T * dv;
+        const double* Gh = dO + bh * T * dv;
+        std::vector<double> qu = normalized_rows(qh, T, p), ku = normalized_rows(kh, T, p);
+        std::vector<double> gq((size_t)T * p, 0.0), gk((size_t)T * p, 0.0), gv((size_t)T * dv, 0.0);
+        std::vector<double> o((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            // forward row t
+            double den = 0.0;
+            std::fill(o.begin(), o.end(), 0.0);
+            for (int s = 0; s <= t; ++s) {
+                const double c = dot(&qu[(size_t)t * p], &ku[(size_t)s * p], p);
+                den += c * c;
+                for (int j = 0; j < dv; ++j) o[j] += c * c * vh[(int64_t)s * dv + j];
+            }
+            if (!(den > 0.0)) continue;
+            for (int j = 0; j < dv; ++j) o[j] /= den;
+            // backward row t
+            const double* G = Gh + (int64_t)t * dv;
+            for (int s = 0; s <= t; ++s) {
+                const double c = dot(&qu[(size_t)t * p], &ku[(size_t)s * p], p);
+                const double w = c * c;
+                double gw = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    gv[(size_t)s * dv + j] += w / den * G[j];
+                    gw += G[j] * (vh[(int64_t)s * dv + j] - o[j]);
+                }
+                gw /= den;
+                const double gc = 2.0 * c * gw;
+                for (int i = 0; i < p; ++i) {
+                    gq[(size_t)t * p + i] += gc * ku[(size_t)s * p + i];
+                    gk[(size_t)s * p + i] += gc * qu[(size_t)t * p + i];
+                }
+            }
+        }
+        // through the unit-sphere projections
+        auto project = [&](const double* x, const double* u, const double* gu, double* gx) {
+            double nrm = 0.0;
+            for (int i = 0; i < p; ++i) nrm += x[i] * x[i];
+            nrm = std::sqrt(nrm);
+            if (!(nrm > 0.0)) {
+                for (int i = 0; i < p; ++i) gx[i] = 0.0;
+                return;
+            }
+            const double ug = dot(u, gu, p);
+            for (int i = 0; i < p; ++i) gx[i] = (gu[i] - ug * u[i]) / nrm;
+        };
+        for (int t = 0; t < T; ++t) {
+            project(qh + (int64_t)t * p, &qu[(size_t)t * p], &gq[(size_t)t * p], dq + (bh * T + t) * p);
+            project(kh + (int64_t)t * p, &ku[(size_t)t * p], &gk[(size_t)t * p], dk + (bh * T + t) * p);
+        }
+        std::copy(gv.begin(), gv.end(), dvv + bh * T * dv);
+    });
+    return 0;
+}
+
 }  // extern "C"

@@ -25,6 +25,9 @@ Parity status of each function (pins live in tests/test_oracle_pins.py):
   forward_plain_block,              pinned (agree with each other; g = 1 is the full
   forward_recurrent_block            forward; Sigma-p running mean; disjoint blocks;
                                      block-permutation behaviour; split calls)
+  backward_plain                    pinned (central finite differences of the
+                                     definition; orthogonality to q and k; value
+                                     shifts; rotations; T = 1; zero vectors)
 """
 import ctypes
 
@@ -72,6 +75,8 @@ def _bind(lib):
     lib.kor_forward_plain_block.restype = i
     lib.kor_forward_recurrent_block.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
     lib.kor_forward_recurrent_block.restype = i
+    lib.kor_backward_plain.argtypes = [_D, _D, _D, _D, i, i, i, i, i, _D, _D, _D, i]
+    lib.kor_backward_plain.restype = i
     return lib
 
 
@@ -252,6 +257,22 @@ def forward_recurrent_block(q, k, v, family, g, S0=None, z0=None, nthreads=0):
     _load().kor_forward_recurrent_block(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, int(family), int(g),
                                         _ptr(S0), _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
     return o, S, z
+
+
+# ---------------------------------------------------------------- backward
+
+def backward_plain(q, k, v, dO, nthreads=0):
+    """Gradients (dq, dk, dv) of L = sum(dO * o) through the plain definition."""
+    q, k, v = _shape4(q, k, v)
+    dO = _f64(dO)
+    if dO.shape != v.shape:
+        raise ValueError("dO must have v's shape [B,H,T,dv]")
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    dq, dk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    _load().kor_backward_plain(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, H, T, p, dv, _ptr(dq), _ptr(dk), _ptr(dvv),
+                               nthreads)
+    return dq, dk, dvv
 
 
 def library_path() -> str:

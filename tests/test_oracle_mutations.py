@@ -58,6 +58,30 @@ BLOCK_MUTATIONS = {
 }
 
 
+# Slips in the backward, caught by the backward pins.
+BACKWARD_MUTATIONS = {
+    "backward_drops_output_term": ("gw += G[j] * (vh[(int64_t)s * dv + j] - o[j]);",
+                                   "gw += G[j] * vh[(int64_t)s * dv + j];"),
+    "backward_missing_factor_two": ("const double gc = 2.0 * c * gw;", "const double gc = c * gw;"),
+    "backward_skips_projection": ("for (int i = 0; i < p; ++i) gx[i] = (gu[i] - ug * u[i]) / nrm;",
+                                  "for (int i = 0; i < p; ++i) gx[i] = gu[i] / nrm;"),
+    "backward_unnormalised_value_weight": ("gv[(size_t)s * dv + j] += w / den * G[j];",
+                                           "gv[(size_t)s * dv + j] += w * G[j];"),
+    "backward_strict_causality": ("for (int s = 0; s <= t; ++s) {\n                const double c = dot(&qu[(size_t)t * p], "
+                                  "&ku[(size_t)s * p], p);\n                const double w = c * c;",
+                                  "for (int s = 0; s < t; ++s) {\n                const double c = dot(&qu[(size_t)t * p], "
+                                  "&ku[(size_t)s * p], p);\n                const double w = c * c;"),
+}
+
+
+def _backward_battery():
+    import tests.test_oracle_backward_pins as bw
+    yield lambda: bw.test_directional_derivatives(33, 5, 2)
+    yield lambda: bw.test_gradients_are_orthogonal_to_q_and_k()
+    yield lambda: bw.test_value_shift_and_value_gradient_sum()
+    yield lambda: bw.test_single_token_and_zero_vectors()
+
+
 def _block_battery():
     import tests.test_oracle_block_pins as bp
     yield lambda: bp.test_state_sizes_at_d64()
@@ -89,10 +113,12 @@ def _battery():
         yield lambda case=case: pins.test_quadratic_recurrent_chunked_agree(*case)
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(BLOCK_MUTATIONS))
+ALL_MUTATIONS = {**MUTATIONS, **BLOCK_MUTATIONS, **BACKWARD_MUTATIONS}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(BLOCK_MUTATIONS) + sorted(BACKWARD_MUTATIONS))
 def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
-    block = name in BLOCK_MUTATIONS
-    old, new = (BLOCK_MUTATIONS if block else MUTATIONS)[name]
+    old, new = ALL_MUTATIONS[name]
     src = open(obuild.SRC).read()
     assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mutated = tmp_path / "mut.cpp"
@@ -103,7 +129,9 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     subprocess.run(cmd, check=True)
     monkeypatch.setattr(km, "_lib", km._bind(ctypes.CDLL(os.fspath(lib))))
     failures = 0
-    for pin in (_block_battery() if block else _battery()):
+    battery = (_block_battery() if name in BLOCK_MUTATIONS
+               else _backward_battery() if name in BACKWARD_MUTATIONS else _battery())
+    for pin in battery:
         try:
             pin()
         except AssertionError:
@@ -115,4 +143,6 @@ def test_unmutated_battery_passes():
     for pin in _battery():
         pin()
     for pin in _block_battery():
+        pin()
+    for pin in _backward_battery():
         pin()
