@@ -41,6 +41,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 SMS = 148
 FP32_LANES_PER_SM = 128
 DECODE_B, DECODE_H = 64, 16  # decode batch: sequences x heads, one new token each
+LIFTS = {"sigma": 1, "multi": 2}  # block-lift families (KATA-Sigma-g, KATA-M-g)
+BLOCK_FORMS = ("chunked_block", "quadratic_block", "decode_block")
 
 
 def load_peaks():
@@ -62,9 +64,33 @@ def flops_forward(w):
     return w.B * w.H * w.T * (4 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
 
 
-def kernel_work(name, w, form="chunked"):
-    """(kind, algorithmic amount per forward call) of a library kernel."""
+def lift_dim(family, p, g):
+    """Width of a block lift: KATA-Sigma-g m(m+1)/2, KATA-M-g g m(m+1)/2 (m = p/g)."""
+    m = p // g
+    return m * (m + 1) // 2 * (1 if family == LIFTS["sigma"] else g)
+
+
+def kernel_work(name, w, form="chunked", lift=None):
+    """(kind, algorithmic amount per forward call) of a library kernel.  `lift`
+    = (family, g) for the block-lift forms."""
     bht = w.B * w.H * w.T
+    if lift is not None:
+        family, g = lift
+        n, m = lift_dim(family, w.p, g), w.p // g
+        pairs = g * g if family == LIFTS["sigma"] else g  # block dot products per score
+        if name == "block_states_simt":
+            return "flop", bht * 2 * n * (w.dv + 1)
+        if name == "block_output_simt":
+            # prefix readout with the normaliser column, and the causal local half with block scores
+            return "flop", bht * (2 * n * (w.dv + 1) + (w.C + 1) * (pairs * m + w.dv))
+        if name == "block_quadratic_simt":
+            return "flop", bht * (w.T + 1) * (pairs * m + w.dv)
+        if name in ("scan_tree", "scan_sequential"):
+            return "byte", 2 * w.B * w.H * w.NC * n * (w.dv + 1) * 4
+        if name == "decode_step_block":
+            elem = 4 if w.dtype == "fp32" else 2
+            return "byte", w.B * w.H * (2 * n * (w.dv + 1) * 4 + (2 * w.p + 2 * w.dv) * elem)
+        return None, 0
     if name in ("chunk_states_simt",):
         return "flop", bht * 2 * w.n * (w.dv + 1)
     if name in ("chunk_output_simt",):
@@ -272,12 +298,13 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     w0 = {x.name.split("_")[0]: x for x in inputs.WORKLOADS}[args.workload]
     w = inputs.Workload(w0.name, w0.B, w0.H, w0.T, w0.p, w0.dv, w0.C, w0.dtype, w0.kind, seed=rank)
-    if args.form == "decode":
+    if args.form in ("decode", "decode_block"):
         # a serving batch of one-token steps with the workload's head shape:
         # 64 sequences x 16 heads, each head's state n x (dv+1) fp32 (above L2 at p >= 32)
         w = inputs.Workload(f"decode_B{DECODE_B}_H{DECODE_H}_p{w0.p}_dv{w0.dv}_{w0.dtype}", DECODE_B, DECODE_H, 1,
                             w0.p, w0.dv, w0.C, w0.dtype, w0.kind, seed=rank)
     mode = kb.KATA_SCAN_TREE if args.scan == "tree" else kb.KATA_SCAN_SEQUENTIAL
+    lift = (LIFTS[args.lift], args.g) if args.form in BLOCK_FORMS else None
     q, k, v = inputs.make(w, dev)
     o = torch.empty_like(v)
     ws_bytes = kb.kata_chunked_workspace_bytes(q.dtype, w.B, w.H, w.T, w.p, w.dv, w.C)
@@ -304,6 +331,25 @@ def run_ours(args, world, rank, local):
 
         def step():
             kb.kata_decode_step(qt, kt, vt, S, z, o=ot, stream=stream)
+    elif args.form == "decode_block":
+        qt, kt, vt = (x[:, :, 0].contiguous() for x in (q, k, v))
+        nl = lift_dim(lift[0], w.p, lift[1])
+        S = torch.zeros((w.B, w.H, nl, w.dv), dtype=torch.float32, device=dev)
+        z = torch.zeros((w.B, w.H, nl), dtype=torch.float32, device=dev)
+        ot = torch.empty_like(vt)
+
+        def step():
+            kb.kata_decode_step_block(qt, kt, vt, S, z, lift[0], lift[1], o=ot, stream=stream)
+    elif args.form == "chunked_block":
+        wsb = torch.empty(max(1, kb.kata_chunked_block_workspace_bytes(q.dtype, lift[0], lift[1], w.B, w.H, w.T,
+                                                                       w.p, w.dv, w.C)),
+                          dtype=torch.uint8, device=dev)
+
+        def step():
+            kb.kata_forward_chunked_block(q, k, v, w.C, lift[0], lift[1], mode, o=o, workspace=wsb, stream=stream)
+    elif args.form == "quadratic_block":
+        def step():
+            kb.kata_forward_quadratic_block(q, k, v, lift[0], lift[1], o=o, stream=stream)
     else:  # scan of given chunk states
         g = torch.Generator(device=dev).manual_seed(rank)
         S_loc = torch.randn((w.B, w.H, w.NC, w.n, w.dv), generator=g, device=dev)
@@ -346,7 +392,7 @@ def run_ours(args, world, rank, local):
     for name, t in trace:
         per.setdefault(name, []).append(t)
     dom = max(per, key=lambda n: sum(per[n]))
-    kind, amount = kernel_work(dom, w, args.form)
+    kind, amount = kernel_work(dom, w, args.form, lift)
     calls_per_step = len(per[dom]) / args.steps
     dom_ms_per_call = sum(per[dom]) / args.steps  # all launches of it in one forward
     if kind == "flop":
@@ -371,12 +417,14 @@ def run_ours(args, world, rank, local):
 
     if args.form != "chunked":
         if rank == 0:
-            line = {"metric": f"KATA {args.form} {w.name}: tokens/s (1 B300)", "value": value, "unit": "tokens/s",
+            label = f"{args.form} {args.lift}{args.g}" if lift else args.form
+            line = {"metric": f"KATA {label} {w.name}: tokens/s (1 B300)", "value": value, "unit": "tokens/s",
                     "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                     "higher_is_better": True, "form": args.form, "roofline": roof, "kernels": kernels,
                     "gpu_launches": len(trace), "clocks": clocks.summary(wall0, wall1),
                     "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "p": w.p, "dv": w.dv, "C": w.C,
-                               "n": w.n, "scan_mode": args.scan}}
+                               "n": lift_dim(lift[0], w.p, lift[1]) if lift else w.n, "scan_mode": args.scan,
+                               "lift": f"{args.lift}{args.g}" if lift else "full"}}
             print(json.dumps(line), flush=True)
         return
 
@@ -467,8 +515,10 @@ def main():
                     help="dram bytes per call of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--form", default="chunked",
-                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode"],
+                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode"] + list(BLOCK_FORMS),
                     help="entry point timed (the contract's line is the chunked forward)")
+    ap.add_argument("--lift", default="sigma", choices=sorted(LIFTS), help="block-lift family of the *_block forms")
+    ap.add_argument("--g", type=int, default=2, help="number of blocks of the *_block forms")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()

@@ -37,3 +37,20 @@ def test_kernel_work_split_and_bytes():
     assert kind == "flop" and quad == 2 * 8 * 2048 * 2049 * 96
     # the segment-state prepass of the forward does no algorithmic work of its own
     assert bench.kernel_work("states_tc", w) == ("flop", 0)
+
+
+def test_block_lift_work_model():
+    # KATA-Sigma-2 at p = 64: n = 528, m = 32, 4 block pairs per score; KATA-M-2: n = 1056, 2 pairs
+    w = W["c4"]
+    bht = w.B * w.H * w.T
+    sig, mul = (bench.LIFTS["sigma"], 2), (bench.LIFTS["multi"], 2)
+    assert bench.lift_dim(sig[0], 64, 2) == 528 and bench.lift_dim(mul[0], 64, 2) == 1056
+    assert bench.kernel_work("block_states_simt", w, "chunked_block", sig) == ("flop", bht * 2 * 528 * 65)
+    assert bench.kernel_work("block_output_simt", w, "chunked_block", sig) == (
+        "flop", bht * (2 * 528 * 65 + 129 * (4 * 32 + 64)))
+    assert bench.kernel_work("block_output_simt", w, "chunked_block", mul) == (
+        "flop", bht * (2 * 1056 * 65 + 129 * (2 * 32 + 64)))
+    assert bench.kernel_work("scan_tree", w, "chunked_block", sig) == ("byte", 2 * 8 * 1024 * 528 * 65 * 4)
+    c2 = W["c2"]
+    assert bench.kernel_work("block_quadratic_simt", c2, "quadratic_block", sig) == (
+        "flop", 2 * 8 * 2048 * 2049 * (4 * 16 + 64))
