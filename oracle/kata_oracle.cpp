@@ -557,4 +557,204 @@ int kor_backward_plain(const double* q, const double* k, const double* v, const 
     return 0;
 }
 
+// ---------------------------------------------------------------- gated prefix
+// The Gated variant ("a Gated prefix adds the learned gate"; its recurrence
+// is in an appendix the pages do not contain).  Reading: one scalar gate
+// gamma_t in [0, 1] per head and token scales the running state before the
+// token's own term is added,
+//   S_t = gamma_t S_{t-1} + psi(kh_t) v_t^T,   z_t = gamma_t z_{t-1} + psi(kh_t),
+// read out as before, o_t = psi(qh_t)^T S_t / psi(qh_t)^T z_t.  gamma = 1 is the
+// ungated forward; gamma_t = 0 forgets everything before t.  The gate is an
+// input, [B, H, T].
+
+// The definition: o_t = sum_{s<=t} d_ts w_ts v_s / sum_{s<=t} d_ts w_ts with
+// w_ts = (qh_t . kh_s)^2 and d_ts = prod_{r=s+1..t} gamma_r (d_tt = 1).
+int kor_forward_plain_gated(const double* q, const double* k, const double* v, const double* gate, int B, int H,
+                            int T, int p, int dv, double* o, int nthreads) {
+    const int64_t heads = (int64_t)B * H;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const double* vh = v + bh * T * dv;
+        const double* gh = gate + bh * T;
+        std::vector<double> qu = normalized_rows(q + bh * T * p, T, p), ku = normalized_rows(k + bh * T * p, T, p);
+        std::vector<double> num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            std::fill(num.begin(), num.end(), 0.0);
+            double den = 0.0, decay = 1.0;
+            for (int s = t; s >= 0; --s) {
+                if (s < t) decay *= gh[s + 1];
+                const double c = dot(&qu[(size_t)t * p], &ku[(size_t)s * p], p);
+                const double w = decay * c * c;
+                den += w;
+                for (int j = 0; j < dv; ++j) num[j] += w * vh[(int64_t)s * dv + j];
+            }
+            for (int j = 0; j < dv; ++j) o[(bh * T + t) * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+    });
+    return 0;
+}
+
+// The gated token recurrence, with optional initial / final state as in
+// kor_forward_recurrent (the initial state is scaled by gamma_0 too).
+int kor_forward_recurrent_gated(const double* q, const double* k, const double* v, const double* gate, int B, int H,
+                                int T, int p, int dv, const double* S0, const double* z0, double* o,
+                                double* S_final, double* z_final, int nthreads) {
+    const int64_t heads = (int64_t)B * H, n = packed_dim_i(p);
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        std::vector<double> S((size_t)(n * dv), 0.0), z((size_t)n, 0.0);
+        if (S0) std::copy(S0 + bh * n * dv, S0 + (bh + 1) * n * dv, S.begin());
+        if (z0) std::copy(z0 + bh * n, z0 + (bh + 1) * n, z.begin());
+        std::vector<double> u((size_t)p), pk((size_t)n), pq((size_t)n), num((size_t)dv);
+        for (int t = 0; t < T; ++t) {
+            const double gam = gate[bh * T + t];
+            const double* vt = v + (bh * T + t) * dv;
+            normalize(k + (bh * T + t) * p, p, u.data());
+            lift(u.data(), p, pk.data());
+            for (int64_t a = 0; a < n; ++a) {
+                for (int j = 0; j < dv; ++j) S[a * dv + j] = gam * S[a * dv + j] + pk[a] * vt[j];
+                z[a] = gam * z[a] + pk[a];
+            }
+            normalize(q + (bh * T + t) * p, p, u.data());
+            lift(u.data(), p, pq.data());
+            std::fill(num.begin(), num.end(), 0.0);
+            for (int64_t a = 0; a < n; ++a)
+                for (int j = 0; j < dv; ++j) num[j] += pq[a] * S[a * dv + j];
+            const double den = dot(pq.data(), z.data(), n);
+            for (int j = 0; j < dv; ++j) o[(bh * T + t) * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+        }
+        if (S_final) std::copy(S.begin(), S.end(), S_final + bh * n * dv);
+        if (z_final) std::copy(z.begin(), z.end(), z_final + bh * n);
+    });
+    return 0;
+}
+
+// Exclusive gated prefix over `nc` items of width `w`: item c carries the
+// pair (a_c, x_c), and prefix_0 = 0, prefix_{c+1} = a_c prefix_c + x_c.  Pairs
+// compose associatively: (a1, x1) then (a2, x2) = (a1 a2, a2 x1 + x2).
+// mode 0: one step per item; mode 1: ceil(log2 nc) rounds, each combining
+// every item with the item 2^d places earlier (Hillis-Steele on the pairs),
+// giving inclusive prefixes that are shifted by one.  Returns the rounds.
+static int gated_exclusive(const double* a, const double* x, int64_t nc, int64_t w, int mode, double* out) {
+    if (mode == 0) {
+        std::vector<double> run((size_t)w, 0.0);
+        for (int64_t c = 0; c < nc; ++c) {
+            for (int64_t e = 0; e < w; ++e) out[c * w + e] = run[e];
+            for (int64_t e = 0; e < w; ++e) run[e] = a[c] * run[e] + x[c * w + e];
+        }
+        return (int)nc;
+    }
+    std::vector<double> ca(a, a + nc), cx(x, x + nc * w), na((size_t)nc), nx((size_t)(nc * w));
+    int rounds = 0;
+    for (int64_t d = 1; d < nc; d <<= 1) {
+        for (int64_t c = 0; c < nc; ++c) {
+            if (c >= d) {
+                // (ca[c-d], cx[c-d]) then (ca[c], cx[c])
+                na[c] = ca[c - d] * ca[c];
+                for (int64_t e = 0; e < w; ++e) nx[c * w + e] = ca[c] * cx[(c - d) * w + e] + cx[c * w + e];
+            } else {
+                na[c] = ca[c];
+                for (int64_t e = 0; e < w; ++e) nx[c * w + e] = cx[c * w + e];
+            }
+        }
+        ca.swap(na);
+        cx.swap(nx);
+        ++rounds;
+    }
+    for (int64_t e = 0; e < w; ++e) out[e] = 0.0;
+    for (int64_t c = 1; c < nc; ++c)
+        for (int64_t e = 0; e < w; ++e) out[c * w + e] = cx[(c - 1) * w + e];
+    return rounds;
+}
+
+int kor_scan_exclusive_gated(const double* a, const double* x, int heads, int nc, int w, int mode, double* out,
+                             int nthreads) {
+    std::vector<int> rounds((size_t)std::max(heads, 1), 0);
+    for_heads(heads, nthreads, [&](int64_t h) {
+        rounds[h] = gated_exclusive(a + h * nc, x + h * (int64_t)nc * w, nc, w, mode, out + h * (int64_t)nc * w);
+    });
+    return heads > 0 ? rounds[0] : 0;
+}
+
+// Gated chunked form.  Chunk c covers tokens [c C, min(c C + C, T)):
+//   local state  S_loc_c = sum_{s in c} (prod_{r=s+1..end_c} gamma_r) psi(kh_s) v_s^T  (z likewise),
+//   chunk decay  a_c = prod_{r in c} gamma_r,
+//   prefix       P_0 = S0, P_{c+1} = a_c P_c + S_loc_c (gated scan, `mode`),
+//   output       num_t = (prod_{r=c C..t} gamma_r) psi(qh_t)^T P_c
+//                        + sum_{s in c, s<=t} (prod_{r=s+1..t} gamma_r) w_ts v_s,  den likewise.
+int kor_forward_chunked_gated(const double* q, const double* k, const double* v, const double* gate, int B, int H,
+                              int T, int p, int dv, int C, int mode, const double* S0, const double* z0, double* o,
+                              double* S_final, double* z_final, int nthreads) {
+    const int64_t heads = (int64_t)B * H, n = packed_dim_i(p), ws = n * dv;
+    const int64_t NC = (T + C - 1) / C;
+    for_heads(heads, nthreads, [&](int64_t bh) {
+        const double* gh = gate + bh * T;
+        // 1. local states and chunk decays; the initial state enters as an
+        //    extra leading item (decay 1) so the scan adds it to every prefix
+        const int64_t items = NC + 1;
+        std::vector<double> a((size_t)items, 1.0), X((size_t)(items * ws), 0.0), Z((size_t)(items * n), 0.0);
+        if (S0) std::copy(S0 + bh * ws, S0 + (bh + 1) * ws, X.begin());
+        if (z0) std::copy(z0 + bh * n, z0 + (bh + 1) * n, Z.begin());
+        std::vector<double> u((size_t)p), pk((size_t)n);
+        for (int64_t c = 0; c < NC; ++c) {
+            const int64_t t0 = c * C, t1 = std::min<int64_t>(t0 + C, T);
+            double* Xc = &X[(size_t)((c + 1) * ws)];
+            double* Zc = &Z[(size_t)((c + 1) * n)];
+            double chunk_decay = 1.0;
+            for (int64_t s = t0; s < t1; ++s) chunk_decay *= gh[s];
+            a[(size_t)(c + 1)] = chunk_decay;
+            for (int64_t s = t0; s < t1; ++s) {
+                double decay = 1.0;  // prod_{r=s+1..t1-1} gamma_r
+                for (int64_t r = s + 1; r < t1; ++r) decay *= gh[r];
+                normalize(k + (bh * T + s) * p, p, u.data());
+                lift(u.data(), p, pk.data());
+                for (int64_t e = 0; e < n; ++e) {
+                    for (int j = 0; j < dv; ++j) Xc[e * dv + j] += decay * pk[e] * v[(bh * T + s) * dv + j];
+                    Zc[e] += decay * pk[e];
+                }
+            }
+        }
+        // 2. gated exclusive prefix over [initial state, chunk 0, ..., chunk NC-1]:
+        //    item c+1's prefix is the state entering chunk c
+        std::vector<double> PX((size_t)(items * ws)), PZ((size_t)(items * n));
+        gated_exclusive(a.data(), X.data(), items, ws, mode, PX.data());
+        gated_exclusive(a.data(), Z.data(), items, n, mode, PZ.data());
+        // 3. per-chunk output
+        std::vector<double> pq((size_t)n), num((size_t)dv), qu((size_t)p), ku((size_t)p);
+        for (int64_t c = 0; c < NC; ++c) {
+            const int64_t t0 = c * C, t1 = std::min<int64_t>(t0 + C, T);
+            const double* Pc = &PX[(size_t)((c + 1) * ws)];
+            const double* Pzc = &PZ[(size_t)((c + 1) * n)];
+            double head_decay = 1.0;  // prod_{r=t0..t} gamma_r
+            for (int64_t t = t0; t < t1; ++t) {
+                head_decay *= gh[t];
+                normalize(q + (bh * T + t) * p, p, qu.data());
+                lift(qu.data(), p, pq.data());
+                std::fill(num.begin(), num.end(), 0.0);
+                for (int64_t e = 0; e < n; ++e)
+                    for (int j = 0; j < dv; ++j) num[j] += head_decay * pq[e] * Pc[e * dv + j];
+                double den = head_decay * dot(pq.data(), Pzc, n);
+                for (int64_t s = t0; s <= t; ++s) {
+                    double decay = 1.0;
+                    for (int64_t r = s + 1; r <= t; ++r) decay *= gh[r];
+                    normalize(k + (bh * T + s) * p, p, ku.data());
+                    const double cc = dot(qu.data(), ku.data(), p);
+                    const double w = decay * cc * cc;
+                    den += w;
+                    for (int j = 0; j < dv; ++j) num[j] += w * v[(bh * T + s) * dv + j];
+                }
+                for (int j = 0; j < dv; ++j) o[(bh * T + t) * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+            }
+        }
+        // 4. final state: the prefix after the last chunk
+        if (S_final || z_final) {
+            std::vector<double> Sf((size_t)ws), zf((size_t)n);
+            const double al = a[(size_t)NC];
+            for (int64_t e = 0; e < ws; ++e) Sf[e] = al * PX[(size_t)(NC * ws + e)] + X[(size_t)(NC * ws + e)];
+            for (int64_t e = 0; e < n; ++e) zf[e] = al * PZ[(size_t)(NC * n + e)] + Z[(size_t)(NC * n + e)];
+            if (S_final) std::copy(Sf.begin(), Sf.end(), S_final + bh * ws);
+            if (z_final) std::copy(zf.begin(), zf.end(), z_final + bh * n);
+        }
+    });
+    return 0;
+}
+
 }  // extern "C"

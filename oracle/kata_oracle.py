@@ -25,6 +25,10 @@ Parity status of each function (pins live in tests/test_oracle_pins.py):
   forward_plain_block,              pinned (agree with each other; g = 1 is the full
   forward_recurrent_block            forward; Sigma-p running mean; disjoint blocks;
                                      block-permutation behaviour; split calls)
+  forward_plain_gated,              pinned (gate 1 is the ungated forward; a zero
+  forward_recurrent_gated,           gate restarts; constant gate with identical
+  forward_chunked_gated,             keys is the moving average; the three forms
+  scan_exclusive_gated               agree; tree = sequential; split calls)
   backward_plain                    pinned (central finite differences of the
                                      definition; orthogonality to q and k; value
                                      shifts; rotations; T = 1; zero vectors)
@@ -77,6 +81,14 @@ def _bind(lib):
     lib.kor_forward_recurrent_block.restype = i
     lib.kor_backward_plain.argtypes = [_D, _D, _D, _D, i, i, i, i, i, _D, _D, _D, i]
     lib.kor_backward_plain.restype = i
+    lib.kor_forward_plain_gated.argtypes = [_D, _D, _D, _D, i, i, i, i, i, _D, i]
+    lib.kor_forward_plain_gated.restype = i
+    lib.kor_forward_recurrent_gated.argtypes = [_D, _D, _D, _D, i, i, i, i, i, _D, _D, _D, _D, _D, i]
+    lib.kor_forward_recurrent_gated.restype = i
+    lib.kor_scan_exclusive_gated.argtypes = [_D, _D, i, i, i, i, _D, i]
+    lib.kor_scan_exclusive_gated.restype = i
+    lib.kor_forward_chunked_gated.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
+    lib.kor_forward_chunked_gated.restype = i
     return lib
 
 
@@ -273,6 +285,73 @@ def backward_plain(q, k, v, dO, nthreads=0):
     _load().kor_backward_plain(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, H, T, p, dv, _ptr(dq), _ptr(dk), _ptr(dvv),
                                nthreads)
     return dq, dk, dvv
+
+
+# ---------------------------------------------------------------- gated prefix
+
+def _gate(gate, q):
+    gate = _f64(gate)
+    if gate.shape != q.shape[:3]:
+        raise ValueError("gate must be [B,H,T]")
+    return gate
+
+
+def forward_plain_gated(q, k, v, gate, nthreads=0):
+    """Definition of the gated forward: weights (qh_t.kh_s)^2 prod_{r=s+1..t} gate_r."""
+    q, k, v = _shape4(q, k, v)
+    gate = _gate(gate, q)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    o = np.empty((B, H, T, dv))
+    _load().kor_forward_plain_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), B, H, T, p, dv, _ptr(o), nthreads)
+    return o
+
+
+def forward_recurrent_gated(q, k, v, gate, S0=None, z0=None, nthreads=0):
+    """Gated token recurrence S_t = gate_t S_{t-1} + psi(kh_t) v_t^T. Returns (o, S, z)."""
+    q, k, v = _shape4(q, k, v)
+    gate = _gate(gate, q)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    n = packed_dim(p)
+    S0 = None if S0 is None else _f64(S0).reshape(B, H, n, dv)
+    z0 = None if z0 is None else _f64(z0).reshape(B, H, n)
+    o = np.empty((B, H, T, dv))
+    S = np.empty((B, H, n, dv))
+    z = np.empty((B, H, n))
+    _load().kor_forward_recurrent_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), B, H, T, p, dv, _ptr(S0), _ptr(z0),
+                                        _ptr(o), _ptr(S), _ptr(z), nthreads)
+    return o, S, z
+
+
+def scan_exclusive_gated(a, x, mode=SCAN_SEQUENTIAL, nthreads=0):
+    """Exclusive gated prefix of items (a [heads, NC], x [heads, NC, W]):
+    prefix_0 = 0, prefix_{c+1} = a_c prefix_c + x_c.  Returns (prefix, rounds)."""
+    a, x = _f64(a), _f64(x)
+    heads, NC, W = x.shape
+    if a.shape != (heads, NC):
+        raise ValueError("a must be [heads, NC]")
+    out = np.empty_like(x)
+    rounds = _load().kor_scan_exclusive_gated(_ptr(a), _ptr(x), heads, NC, W, mode, _ptr(out), nthreads)
+    return out, rounds
+
+
+def forward_chunked_gated(q, k, v, gate, C, mode=SCAN_SEQUENTIAL, S0=None, z0=None, nthreads=0):
+    """Gated chunked form (decayed local states, gated prefix scan, decayed
+    readout plus the local causal part). Returns (o, S_final, z_final)."""
+    q, k, v = _shape4(q, k, v)
+    gate = _gate(gate, q)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    n = packed_dim(p)
+    S0 = None if S0 is None else _f64(S0).reshape(B, H, n, dv)
+    z0 = None if z0 is None else _f64(z0).reshape(B, H, n)
+    o = np.empty((B, H, T, dv))
+    S = np.empty((B, H, n, dv))
+    z = np.empty((B, H, n))
+    _load().kor_forward_chunked_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), B, H, T, p, dv, C, mode, _ptr(S0),
+                                      _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
+    return o, S, z
 
 
 def library_path() -> str:

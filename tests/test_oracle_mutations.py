@@ -74,6 +74,29 @@ BACKWARD_MUTATIONS = {
 }
 
 
+# Slips in the gated prefix, caught by the gated pins.
+GATED_MUTATIONS = {
+    "gated_decay_counts_own_gate": ("if (s < t) decay *= gh[s + 1];", "decay *= gh[s];"),
+    "gated_gate_after_adding": ("S[a * dv + j] = gam * S[a * dv + j] + pk[a] * vt[j];",
+                                "S[a * dv + j] = gam * (S[a * dv + j] + pk[a] * vt[j]);"),
+    "gated_tree_wrong_carry": ("nx[c * w + e] = ca[c] * cx[(c - d) * w + e] + cx[c * w + e];",
+                               "nx[c * w + e] = ca[c - d] * cx[(c - d) * w + e] + cx[c * w + e];"),
+    "gated_readout_skips_first_gate": ("head_decay *= gh[t];", "head_decay *= 1.0;"),
+    "gated_local_decay_off_by_one": ("for (int64_t r = s + 1; r < t1; ++r) decay *= gh[r];",
+                                     "for (int64_t r = s; r < t1; ++r) decay *= gh[r];"),
+}
+
+
+def _gated_battery():
+    import tests.test_oracle_gated_pins as gp
+    yield lambda: gp.test_unit_gate_is_the_ungated_forward()
+    yield lambda: gp.test_zero_gate_restarts_the_sequence(9)
+    yield lambda: gp.test_constant_gate_identical_keys_is_the_moving_average()
+    yield lambda: gp.test_gated_forms_agree(37, 8, 4, 1)
+    yield lambda: gp.test_gated_scan_is_associative(7)
+    yield lambda: gp.test_gated_split_call_with_carried_state(13)
+
+
 def _backward_battery():
     import tests.test_oracle_backward_pins as bw
     yield lambda: bw.test_directional_derivatives(33, 5, 2)
@@ -113,10 +136,11 @@ def _battery():
         yield lambda case=case: pins.test_quadratic_recurrent_chunked_agree(*case)
 
 
-ALL_MUTATIONS = {**MUTATIONS, **BLOCK_MUTATIONS, **BACKWARD_MUTATIONS}
+ALL_MUTATIONS = {**MUTATIONS, **BLOCK_MUTATIONS, **BACKWARD_MUTATIONS, **GATED_MUTATIONS}
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(BLOCK_MUTATIONS) + sorted(BACKWARD_MUTATIONS))
+@pytest.mark.parametrize("name", sorted(MUTATIONS) + sorted(BLOCK_MUTATIONS) + sorted(BACKWARD_MUTATIONS)
+                         + sorted(GATED_MUTATIONS))
 def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     old, new = ALL_MUTATIONS[name]
     src = open(obuild.SRC).read()
@@ -130,7 +154,8 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
     monkeypatch.setattr(km, "_lib", km._bind(ctypes.CDLL(os.fspath(lib))))
     failures = 0
     battery = (_block_battery() if name in BLOCK_MUTATIONS
-               else _backward_battery() if name in BACKWARD_MUTATIONS else _battery())
+               else _backward_battery() if name in BACKWARD_MUTATIONS
+               else _gated_battery() if name in GATED_MUTATIONS else _battery())
     for pin in battery:
         try:
             pin()
@@ -145,4 +170,6 @@ def test_unmutated_battery_passes():
     for pin in _block_battery():
         pin()
     for pin in _backward_battery():
+        pin()
+    for pin in _gated_battery():
         pin()
