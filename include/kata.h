@@ -216,6 +216,28 @@ KATA_API kata_status kata_decode_step_block(const void* q, const void* k, const 
                                             cudaStream_t stream);
 
 /*
+ * Backward: the gradients of L = sum(dO * o) for the forward above (every
+ * form computes the same o), by the chain rule through the definition --
+ * the pages give no backward algorithm:
+ *   dv_s = sum_{t>=s} (w_ts / D_t) dO_t,  w_ts = (qh_t.kh_s)^2, D_t = sum_{s<=t} w_ts
+ *   dc_ts = 2 (qh_t.kh_s) (dO_t.v_s - dO_t.o_t) / D_t
+ *   dq_t, dk_s: sum_s dc_ts kh_s and sum_t dc_ts qh_t taken back through the
+ *   unit-sphere projections (the component along q_t or k_s removed, divided
+ *   by its norm).
+ * A row with a zero denominator passes no gradient; a zero q or k vector
+ * receives none.  q, k, dq, dk [B,H,T,p]; v, dO, dv [B,H,T,dv], all of
+ * `dtype` (gradients in the input dtype, fp32 arithmetic).  workspace: at
+ * least kata_backward_workspace_bytes() bytes, 16-byte aligned.  O(T^2)
+ * work per head (flash-style row and column passes over the causal
+ * triangle).
+ */
+KATA_API size_t kata_backward_workspace_bytes(int B, int H, int T);
+KATA_API kata_status kata_backward(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                                   void* dk, void* dv, kata_dtype dtype, int B, int H, int T, int p,
+                                   int dv_dim, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: KATA_OK, or KATA_ERR_TIMEOUT if a bounded device-side
  * wait expired in an earlier call (that call's outputs are then invalid).

@@ -408,6 +408,34 @@ kata_status kata_decode_step_block(const void* q, const void* k, const void* v, 
     return decode_common(q, k, v, o, dt, B, H, p, dv, family, g, S, z, stream);
 }
 
+size_t kata_backward_workspace_bytes(int B, int H, int T) {
+    if (B < 0 || H < 0 || T < 0) return 0;
+    const int64_t rows = (int64_t)B * H * T;
+    return rows == 0 ? 0 : 2 * round_up(sizeof(float) * (size_t)rows, 256);
+}
+
+kata_status kata_backward(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv,
+                          kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv_dim);
+    if (st != KATA_OK) return st;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv_dim;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(dO, v_bytes)) != KATA_OK ||
+        (st = check_buffer(dq, qk_bytes)) != KATA_OK || (st = check_buffer(dk, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(dv, v_bytes)) != KATA_OK)
+        return st;
+    const size_t need = kata_backward_workspace_bytes(B, H, T);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    float* D_ws = static_cast<float*>(ws);
+    float* delta_ws = reinterpret_cast<float*>(static_cast<char*>(ws) + need / 2);
+    return cuda_status(kata::launch_backward(dt, q, k, v, dO, dq, dk, dv, D_ws, delta_ws, B * H, T, p, dv_dim,
+                                             stream));
+}
+
 kata_status kata_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KATA_ERR_CUDA;
     unsigned int word = kata::quadratic_tc_take_status();

@@ -80,6 +80,13 @@ cudaError_t launch_block_output(int dtype, const void* q, const void* k, const v
 cudaError_t launch_block_quadratic(int dtype, const void* q, const void* k, const void* v, void* o, int BH, int T,
                                    int p, int dv, int family, int g, cudaStream_t s);
 
+// Backward of the forward (CUDA cores, any dtype): dq, dk [BH,T,p] and dv
+// [BH,T,dv] in the input dtype from dO [BH,T,dv]; D_ws and delta_ws are
+// [BH,T] fp32 scratch (row normalisers and dO . o).
+cudaError_t launch_backward(int dtype, const void* q, const void* k, const void* v, const void* dO, void* dq,
+                            void* dk, void* dv, float* D_ws, float* delta_ws, int BH, int T, int p, int dv_dim,
+                            cudaStream_t s);
+
 // dst[i] = src ? src[i] : 0 for i < count (fp32), used for pass-through states.
 cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s);
 

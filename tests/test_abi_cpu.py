@@ -172,3 +172,14 @@ def test_block_argument_errors(lib):
     assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, 4, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
     assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
     assert d(P, P, P, P, kb.KATA_BF16, 0, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_OK
+
+
+def test_backward_workspace_and_argument_errors(lib):
+    assert kb.load().kata_backward_workspace_bytes(1, 2, 100) == 2 * ((2 * 100 * 4 + 255) // 256) * 256
+    assert kb.load().kata_backward_workspace_bytes(0, 2, 100) == 0
+    f = lib.kata_backward
+    P = None
+    assert f(P, P, P, P, P, P, P, 7, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 24, 16, P, 0, P) == kb.KATA_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 0, 16, 16, P, 0, P) == kb.KATA_OK

@@ -1,0 +1,48 @@
+"""GPU parity of the backward (kata_backward) against the fp64 oracle's
+gradient of the plain definition."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kernelized_linear_attention_03_b300 import binding as kb
+from kernelized_linear_attention_03_b300 import inputs
+from tests.parity import f64, head_errors
+
+pytestmark = pytest.mark.gpu
+DNAME = {torch.float32: "fp32", torch.bfloat16: "bf16"}
+# fp32: the gradient sums cancel (dO.v_s - dO.o_t); bf16: output rounding 2^-8 plus that
+GRAD_TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+def _case(B, H, T, p, dv, dtype, seed):
+    q, k, v = inputs.make(inputs.small(B, H, T, p, dv, 32, DNAME[dtype], "raw", seed), "cuda")
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    dO = torch.randn(v.shape, generator=g, dtype=torch.float64).to(dtype).cuda()
+    return q, k, v, dO
+
+
+def _check(q, k, v, dO, dtype):
+    dq, dk, dv = kb.kata_backward(q, k, v, dO)
+    torch.cuda.synchronize()
+    ref = oracle.backward_plain(f64(q), f64(k), f64(v), f64(dO))
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        err = float(head_errors(f64(got), r).max())
+        assert err <= GRAD_TOL[dtype], f"{name}: worst-head relative error {err:.3e}"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 32), (64, 64)])
+@pytest.mark.parametrize("T", [1, 37, 130])
+def test_backward_matches_the_oracle(dtype, p, dv, T):
+    _check(*_case(1, 2, T, p, dv, dtype, seed=T + p + dv), dtype)
+
+
+def test_backward_zero_vectors():
+    q, k, v, dO = _case(1, 1, 20, 16, 16, torch.float32, seed=4)
+    k[0, 0, 3] = 0
+    q[0, 0, 7] = 0
+    dq, dk, dv = kb.kata_backward(q, k, v, dO)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk[0, 0, 3]) == 0 and torch.count_nonzero(dq[0, 0, 7]) == 0
+    _check(q, k, v, dO, torch.float32)
