@@ -216,6 +216,33 @@ KATA_API kata_status kata_decode_step_block(const void* q, const void* k, const 
                                             cudaStream_t stream);
 
 /*
+ * Gated prefix (the Gated variant: "a Gated prefix adds the learned gate";
+ * its recurrence is in an appendix the pages do not contain).  Reading: one
+ * scalar gate per head and token, gate [B,H,T] fp32 (values in [0, 1] keep
+ * every weight nonnegative; others are used as given), scales the running
+ * state before the token's own term is added,
+ *   S_t = gate_t S_{t-1} + psi(kh_t) v_t^T,  z_t = gate_t z_{t-1} + psi(kh_t),
+ * and the readout is unchanged.  A zero gate forgets everything before its
+ * token; all-one gates give kata_forward_chunked.  The chunked form carries
+ * per-chunk decays and a one-step-per-chunk gated prefix.  Other arguments,
+ * states and errors as for kata_forward_chunked (S0 is scaled by gate_0).
+ */
+KATA_API size_t kata_chunked_gated_workspace_bytes(kata_dtype dtype, int B, int H, int T, int p, int dv,
+                                                   int C);
+KATA_API kata_status kata_forward_chunked_gated(const void* q, const void* k, const void* v,
+                                                const float* gate, void* o, kata_dtype dtype, int B,
+                                                int H, int T, int p, int dv, int C, const float* S0,
+                                                const float* z0, float* S_final, float* z_final,
+                                                void* workspace, size_t workspace_bytes,
+                                                cudaStream_t stream);
+
+/* Gated decode step: as kata_decode_step with the state scaled by the head's
+ * gate [B,H] fp32 first (S = gate S + psi(kh) v^T, z likewise). */
+KATA_API kata_status kata_decode_step_gated(const void* q, const void* k, const void* v,
+                                            const float* gate, void* o, kata_dtype dtype, int B, int H,
+                                            int p, int dv, float* S, float* z, cudaStream_t stream);
+
+/*
  * Backward: the gradients of L = sum(dO * o) for the forward above (every
  * form computes the same o), by the chain rule through the definition --
  * the pages give no backward algorithm:

@@ -32,7 +32,8 @@ SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_scan_states", "kata_get_device_status", "kata_trace_start", "kata_trace_stop",
            "kata_trace_get", "kata_forward_chunked_noalloc", "kata_decode_step", "kata_lift_dim",
            "kata_chunked_block_workspace_bytes", "kata_forward_chunked_block", "kata_forward_quadratic_block",
-           "kata_decode_step_block", "kata_backward_workspace_bytes", "kata_backward")
+           "kata_decode_step_block", "kata_backward_workspace_bytes", "kata_backward",
+           "kata_chunked_gated_workspace_bytes", "kata_forward_chunked_gated", "kata_decode_step_gated")
 
 
 class KataError(RuntimeError):
@@ -88,6 +89,12 @@ def load():
     lib.kata_backward_workspace_bytes.restype = Z
     lib.kata_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
     lib.kata_backward.restype = I
+    lib.kata_chunked_gated_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.kata_chunked_gated_workspace_bytes.restype = Z
+    lib.kata_forward_chunked_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, Z, P]
+    lib.kata_forward_chunked_gated.restype = I
+    lib.kata_decode_step_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
+    lib.kata_decode_step_gated.restype = I
     lib.kata_trace_start.argtypes = [I]
     lib.kata_trace_start.restype = I
     lib.kata_trace_stop.argtypes = []
@@ -314,7 +321,45 @@ def kata_decode_step_block(q, k, v, S, z, family, g, o=None, stream=None):
         o = torch.empty_like(v)
     _check(load().kata_decode_step_block(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dtype_code(q), B, H, p, dv,
                                          int(family), int(g), _ptr(S), _ptr(z), _stream(stream)),
-           "kata_decode_step_block", "kata_backward_workspace_bytes", "kata_backward")
+           "kata_decode_step_block", "kata_backward_workspace_bytes", "kata_backward",
+           "kata_chunked_gated_workspace_bytes", "kata_forward_chunked_gated", "kata_decode_step_gated")
+    return o
+
+
+def kata_forward_chunked_gated(q, k, v, gate, C, S0=None, z0=None, o=None, S_final=None, z_final=None,
+                               workspace=None, stream=None):
+    """Gated chunked forward; gate [B,H,T] float32.  Returns o, or (o, S_final,
+    z_final) when state buffers are given."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if gate.shape != (B, H, T) or gate.dtype != torch.float32:
+        raise ValueError("expected a float32 gate [B,H,T]")
+    if o is None:
+        o = torch.empty_like(v)
+    need = int(load().kata_chunked_gated_workspace_bytes(_dtype_code(q), B, H, T, p, dv, int(C)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kata_forward_chunked_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _dtype_code(q), B, H,
+                                             T, p, dv, int(C), _ptr(S0), _ptr(z0), _ptr(S_final), _ptr(z_final),
+                                             _ptr(workspace), ws_bytes, _stream(stream)),
+           "kata_forward_chunked_gated")
+    return o if S_final is None else (o, S_final, z_final)
+
+
+def kata_decode_step_gated(q, k, v, gate, S, z, o=None, stream=None):
+    """Gated decode step; gate [B,H] float32; S, z updated in place.  Returns o."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,p] and v [B,H,dv]")
+    B, H, p = q.shape
+    dv = v.shape[-1]
+    if gate.shape != (B, H) or gate.dtype != torch.float32:
+        raise ValueError("expected a float32 gate [B,H]")
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _dtype_code(q), B, H, p,
+                                         dv, _ptr(S), _ptr(z), _stream(stream)),
+           "kata_decode_step_gated")
     return o
 
 

@@ -65,8 +65,16 @@ cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, f
 // (S [BH,n,dv], z [BH,n] fp32), o = psi(qh)^T S / psi(qh)^T z [BH,dv].
 // family 0 (g = 1): the full lift; 1 / 2: KATA-Sigma-g / KATA-M-g
 // (block_lift.cuh), n = block_lift_dim(family, p, g).
+// gate (or null): [BH] fp32, the gated step S = gate S + psi(kh) v^T (full lift only).
 cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
-                               float* z, int BH, int p, int dv, int family, int g, cudaStream_t s);
+                               float* z, int BH, int p, int dv, int family, int g, const float* gate,
+                               cudaStream_t s);
+
+// Gated chunked forward (CUDA cores, any dtype): gate [BH,T] fp32; X [BH,NC,n,dv],
+// Xz [BH,NC,n], a [BH,NC] fp32 scratch; optional S0/z0 and S_final/z_final.
+cudaError_t launch_chunked_gated(int dtype, const void* q, const void* k, const void* v, const float* gate, void* o,
+                                 float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
+                                 float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s);
 
 // Block-lift forwards on CUDA cores (family 1 Sigma-g, 2 M-g; block_lift.cuh),
 // any dtype: per-chunk states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] in the

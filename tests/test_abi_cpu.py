@@ -183,3 +183,19 @@ def test_backward_workspace_and_argument_errors(lib):
     assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 24, 16, P, 0, P) == kb.KATA_ERR_UNSUPPORTED
     assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
     assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 0, 16, 16, P, 0, P) == kb.KATA_OK
+
+
+def test_gated_argument_errors(lib):
+    P = None
+    f = lib.kata_forward_chunked_gated
+    assert f(P, P, P, P, P, 9, 1, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, 48, P, P, P, P, P, 0, P) == kb.KATA_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, kb.KATA_FP32, 0, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_OK
+    d = lib.kata_decode_step_gated
+    assert d(P, P, P, P, P, kb.KATA_FP32, 1, 1, 16, 16, P, P, P) == kb.KATA_ERR_INVALID_ARG
+    assert d(P, P, P, P, P, kb.KATA_FP32, 0, 1, 16, 16, P, P, P) == kb.KATA_OK
+    # states [BH, NC, n, dv] + [BH, NC, n] + chunk decays [BH, NC], each 256-byte aligned
+    got = lib.kata_chunked_gated_workspace_bytes(kb.KATA_FP32, 1, 2, 100, 16, 16, 32)
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert got == r(2 * 4 * 136 * 16 * 4) + r(2 * 4 * 136 * 4) + r(2 * 4 * 4)
