@@ -253,16 +253,33 @@ KATA_API kata_status kata_decode_step_gated(const void* q, const void* k, const 
  *   by its norm).
  * A row with a zero denominator passes no gradient; a zero q or k vector
  * receives none.  q, k, dq, dk [B,H,T,p]; v, dO, dv [B,H,T,dv], all of
- * `dtype` (gradients in the input dtype, fp32 arithmetic).  workspace: at
- * least kata_backward_workspace_bytes() bytes, 16-byte aligned.  O(T^2)
- * work per head (flash-style row and column passes over the causal
- * triangle).
+ * `dtype` (gradients in the input dtype, fp32 arithmetic).
+ * kata_backward_quadratic: O(T^2) work per head (flash-style row and column
+ * passes over the causal triangle); workspace at least
+ * kata_backward_quadratic_workspace_bytes() bytes, 16-byte aligned.
  */
-KATA_API size_t kata_backward_workspace_bytes(int B, int H, int T);
-KATA_API kata_status kata_backward(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                                   void* dk, void* dv, kata_dtype dtype, int B, int H, int T, int p,
-                                   int dv_dim, void* workspace, size_t workspace_bytes,
-                                   cudaStream_t stream);
+KATA_API size_t kata_backward_quadratic_workspace_bytes(int B, int H, int T);
+KATA_API kata_status kata_backward_quadratic(const void* q, const void* k, const void* v, const void* dO,
+                                             void* dq, void* dk, void* dv, kata_dtype dtype, int B, int H,
+                                             int T, int p, int dv_dim, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The same gradients in O(T) through the chunked form (chunks of 64 tokens,
+ * whatever the forward's C): the forward's exclusive prefix states are
+ * rebuilt; a query-side pass recomputes each row's normaliser D_t and
+ * dO_t . o_t and takes dq from the prefix and the chunk's own keys; the
+ * per-chunk gradient states sum_t psi(qh_t) [dO_t / D_t | -dO_t.o_t / D_t]
+ * are summed over later chunks (a reverse exclusive prefix); a key-side
+ * pass takes dk and dv from them and from the chunk's own later queries.
+ * Arguments as kata_backward_quadratic; workspace: at least
+ * kata_backward_chunked_workspace_bytes() bytes, 256-byte aligned.
+ */
+KATA_API size_t kata_backward_chunked_workspace_bytes(int B, int H, int T, int p, int dv_dim);
+KATA_API kata_status kata_backward_chunked(const void* q, const void* k, const void* v, const void* dO,
+                                           void* dq, void* dk, void* dv, kata_dtype dtype, int B, int H,
+                                           int T, int p, int dv_dim, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of

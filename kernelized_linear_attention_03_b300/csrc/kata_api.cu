@@ -410,15 +410,15 @@ kata_status kata_decode_step_block(const void* q, const void* k, const void* v, 
     return decode_common(q, k, v, o, dt, B, H, p, dv, family, g, S, z, stream);
 }
 
-size_t kata_backward_workspace_bytes(int B, int H, int T) {
+size_t kata_backward_quadratic_workspace_bytes(int B, int H, int T) {
     if (B < 0 || H < 0 || T < 0) return 0;
     const int64_t rows = (int64_t)B * H * T;
     return rows == 0 ? 0 : 2 * round_up(sizeof(float) * (size_t)rows, 256);
 }
 
-kata_status kata_backward(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv,
-                          kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws, size_t ws_bytes,
-                          cudaStream_t stream) {
+kata_status kata_backward_quadratic(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                                    void* dv, kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream) {
     kata_status st = check_shapes(dt, B, H, T, p, dv_dim);
     if (st != KATA_OK) return st;
     const int64_t rows = (int64_t)B * H * T;
@@ -429,7 +429,7 @@ kata_status kata_backward(const void* q, const void* k, const void* v, const voi
         (st = check_buffer(dq, qk_bytes)) != KATA_OK || (st = check_buffer(dk, qk_bytes)) != KATA_OK ||
         (st = check_buffer(dv, v_bytes)) != KATA_OK)
         return st;
-    const size_t need = kata_backward_workspace_bytes(B, H, T);
+    const size_t need = kata_backward_quadratic_workspace_bytes(B, H, T);
     if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
     if ((st = check_buffer(ws, need)) != KATA_OK) return st;
     float* D_ws = static_cast<float*>(ws);
@@ -493,6 +493,41 @@ kata_status kata_forward_chunked_gated(const void* q, const void* k, const void*
     float* a = reinterpret_cast<float*>(static_cast<char*>(ws) + w.total);
     return cuda_status(kata::launch_chunked_gated(dt, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, (int)BH,
                                                   T, p, dv, C, stream));
+}
+
+size_t kata_backward_chunked_workspace_bytes(int B, int H, int T, int p, int dv_dim) {
+    if (B < 0 || H < 0 || T < 0 || !p_ok(p) || !dv_ok(dv_dim)) return 0;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return 0;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv_dim, kata::backward_chunk_len());
+    return w.total + 2 * round_up(sizeof(float) * (size_t)rows, 256);
+}
+
+kata_status kata_backward_chunked(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                                  void* dv, kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv_dim);
+    if (st != KATA_OK) return st;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv_dim;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(dO, v_bytes)) != KATA_OK ||
+        (st = check_buffer(dq, qk_bytes)) != KATA_OK || (st = check_buffer(dk, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(dv, v_bytes)) != KATA_OK)
+        return st;
+    const size_t need = kata_backward_chunked_workspace_bytes(B, H, T, p, dv_dim);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv_dim, kata::backward_chunk_len());
+    char* base = static_cast<char*>(ws);
+    float* S_ws = reinterpret_cast<float*>(base + w.s_off);
+    float* z_ws = reinterpret_cast<float*>(base + w.z_off);
+    float* D_ws = reinterpret_cast<float*>(base + w.total);
+    float* dl_ws = reinterpret_cast<float*>(base + w.total + round_up(sizeof(float) * (size_t)rows, 256));
+    return cuda_status(kata::launch_backward_chunked(dt, q, k, v, dO, dq, dk, dv, S_ws, z_ws, D_ws, dl_ws, (int)(B * H),
+                                                     T, p, dv_dim, stream));
 }
 
 kata_status kata_get_device_status(cudaStream_t stream) {

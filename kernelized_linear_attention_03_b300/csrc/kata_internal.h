@@ -91,6 +91,13 @@ cudaError_t launch_block_quadratic(int dtype, const void* q, const void* k, cons
 // Backward of the forward (CUDA cores, any dtype): dq, dk [BH,T,p] and dv
 // [BH,T,dv] in the input dtype from dO [BH,T,dv]; D_ws and delta_ws are
 // [BH,T] fp32 scratch (row normalisers and dO . o).
+// O(T) backward through the chunked form; S_ws [BH,NC,n,dv], z_ws [BH,NC,n]
+// (NC = ceil(T / backward_chunk_len())), D_ws, delta_ws [BH,T], all fp32.
+int backward_chunk_len();
+cudaError_t launch_backward_chunked(int dtype, const void* q, const void* k, const void* v, const void* dO, void* dq,
+                                    void* dk, void* dv, float* S_ws, float* z_ws, float* D_ws, float* delta_ws, int BH,
+                                    int T, int p, int dv_dim, cudaStream_t s);
+
 cudaError_t launch_backward(int dtype, const void* q, const void* k, const void* v, const void* dO, void* dq,
                             void* dk, void* dv, float* D_ws, float* delta_ws, int BH, int T, int p, int dv_dim,
                             cudaStream_t s);

@@ -175,9 +175,12 @@ def test_block_argument_errors(lib):
 
 
 def test_backward_workspace_and_argument_errors(lib):
-    assert kb.load().kata_backward_workspace_bytes(1, 2, 100) == 2 * ((2 * 100 * 4 + 255) // 256) * 256
-    assert kb.load().kata_backward_workspace_bytes(0, 2, 100) == 0
-    f = lib.kata_backward
+    assert kb.load().kata_backward_quadratic_workspace_bytes(1, 2, 100) == 2 * ((2 * 100 * 4 + 255) // 256) * 256
+    assert kb.load().kata_backward_quadratic_workspace_bytes(0, 2, 100) == 0
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert kb.load().kata_backward_chunked_workspace_bytes(1, 2, 100, 16, 16) == (
+        r(2 * 2 * 136 * 16 * 4) + r(2 * 2 * 136 * 4) + 2 * r(2 * 100 * 4))
+    f = lib.kata_backward_quadratic
     P = None
     assert f(P, P, P, P, P, P, P, 7, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
     assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 24, 16, P, 0, P) == kb.KATA_ERR_UNSUPPORTED

@@ -22,8 +22,8 @@ def _case(B, H, T, p, dv, dtype, seed):
     return q, k, v, dO
 
 
-def _check(q, k, v, dO, dtype):
-    dq, dk, dv = kb.kata_backward(q, k, v, dO)
+def _check(q, k, v, dO, dtype, form="chunked"):
+    dq, dk, dv = kb.kata_backward(q, k, v, dO, form=form)
     torch.cuda.synchronize()
     ref = oracle.backward_plain(f64(q), f64(k), f64(v), f64(dO))
     for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
@@ -34,15 +34,22 @@ def _check(q, k, v, dO, dtype):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 32), (64, 64)])
 @pytest.mark.parametrize("T", [1, 37, 130])
-def test_backward_matches_the_oracle(dtype, p, dv, T):
-    _check(*_case(1, 2, T, p, dv, dtype, seed=T + p + dv), dtype)
+@pytest.mark.parametrize("form", ["chunked", "quadratic"])
+def test_backward_matches_the_oracle(dtype, p, dv, T, form):
+    _check(*_case(1, 2, T, p, dv, dtype, seed=T + p + dv), dtype, form)
 
 
-def test_backward_zero_vectors():
-    q, k, v, dO = _case(1, 1, 20, 16, 16, torch.float32, seed=4)
+@pytest.mark.parametrize("form", ["chunked", "quadratic"])
+def test_backward_zero_vectors(form):
+    q, k, v, dO = _case(1, 1, 90, 16, 16, torch.float32, seed=4)
     k[0, 0, 3] = 0
-    q[0, 0, 7] = 0
-    dq, dk, dv = kb.kata_backward(q, k, v, dO)
+    q[0, 0, 70] = 0
+    dq, dk, dv = kb.kata_backward(q, k, v, dO, form=form)
     torch.cuda.synchronize()
-    assert torch.count_nonzero(dk[0, 0, 3]) == 0 and torch.count_nonzero(dq[0, 0, 7]) == 0
-    _check(q, k, v, dO, torch.float32)
+    assert torch.count_nonzero(dk[0, 0, 3]) == 0 and torch.count_nonzero(dq[0, 0, 70]) == 0
+    _check(q, k, v, dO, torch.float32, form)
+
+
+def test_chunked_backward_long_sequence():
+    """Many backward chunks (the reverse prefix over 33 chunks) on several heads."""
+    _check(*_case(2, 2, 2100, 32, 32, torch.float32, seed=8), torch.float32, "chunked")
