@@ -757,4 +757,52 @@ int kor_forward_chunked_gated(const double* q, const double* k, const double* v,
     return 0;
 }
 
+// ---------------------------------------------------------------- sampled rows
+// The block-lift and gated definitions for selected rows only (row r: head
+// bh[r] = b*H + h, position t[r]), O(t (p + dv)) per row, for checks at sizes
+// where every row would be too slow.  Outputs [nrows, dv].
+int kor_forward_plain_block_rows(const double* q, const double* k, const double* v, int B, int H, int T, int p, int dv,
+                                 int family, int g, const int64_t* bh, const int64_t* t, int64_t nrows, double* out,
+                                 int nthreads) {
+    if (block_dim_i(p, family, g) < 0) return -1;
+    for_heads(nrows, nthreads, [&](int64_t r) {
+        std::vector<double> qu((size_t)p), ku((size_t)p), num((size_t)dv, 0.0);
+        normalize(q + (bh[r] * T + t[r]) * p, p, qu.data());
+        double den = 0.0;
+        for (int64_t s = 0; s <= t[r]; ++s) {
+            normalize(k + (bh[r] * T + s) * p, p, ku.data());
+            const double w = block_kernel(qu.data(), ku.data(), p, family, g);
+            den += w;
+            for (int j = 0; j < dv; ++j) num[j] += w * v[(bh[r] * T + s) * dv + j];
+        }
+        for (int j = 0; j < dv; ++j) out[r * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+    });
+    (void)B;
+    (void)H;
+    return 0;
+}
+
+int kor_forward_plain_gated_rows(const double* q, const double* k, const double* v, const double* gate, int B, int H,
+                                 int T, int p, int dv, const int64_t* bh, const int64_t* t, int64_t nrows, double* out,
+                                 int nthreads) {
+    for_heads(nrows, nthreads, [&](int64_t r) {
+        std::vector<double> qu((size_t)p), ku((size_t)p), num((size_t)dv, 0.0);
+        const double* gh = gate + bh[r] * T;
+        normalize(q + (bh[r] * T + t[r]) * p, p, qu.data());
+        double den = 0.0, decay = 1.0;
+        for (int64_t s = t[r]; s >= 0; --s) {
+            if (s < t[r]) decay *= gh[s + 1];
+            normalize(k + (bh[r] * T + s) * p, p, ku.data());
+            const double c = dot(qu.data(), ku.data(), p);
+            const double w = decay * c * c;
+            den += w;
+            for (int j = 0; j < dv; ++j) num[j] += w * v[(bh[r] * T + s) * dv + j];
+        }
+        for (int j = 0; j < dv; ++j) out[r * dv + j] = den > 0.0 ? num[j] / den : 0.0;
+    });
+    (void)B;
+    (void)H;
+    return 0;
+}
+
 }  // extern "C"

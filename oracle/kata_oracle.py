@@ -25,6 +25,8 @@ Parity status of each function (pins live in tests/test_oracle_pins.py):
   forward_plain_block,              pinned (agree with each other; g = 1 is the full
   forward_recurrent_block            forward; Sigma-p running mean; disjoint blocks;
                                      block-permutation behaviour; split calls)
+  forward_plain_block_rows,         pinned (equal the full-row definitions they
+  forward_plain_gated_rows           sample)
   forward_plain_gated,              pinned (gate 1 is the ungated forward; a zero
   forward_recurrent_gated,           gate restarts; constant gate with identical
   forward_chunked_gated,             keys is the moving average; the three forms
@@ -89,6 +91,10 @@ def _bind(lib):
     lib.kor_scan_exclusive_gated.restype = i
     lib.kor_forward_chunked_gated.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, i, _D, _D, _D, _D, _D, i]
     lib.kor_forward_chunked_gated.restype = i
+    lib.kor_forward_plain_block_rows.argtypes = [_D, _D, _D, i, i, i, i, i, i, i, _I64, _I64, ctypes.c_int64, _D, i]
+    lib.kor_forward_plain_block_rows.restype = i
+    lib.kor_forward_plain_gated_rows.argtypes = [_D, _D, _D, _D, i, i, i, i, i, _I64, _I64, ctypes.c_int64, _D, i]
+    lib.kor_forward_plain_gated_rows.restype = i
     return lib
 
 
@@ -352,6 +358,45 @@ def forward_chunked_gated(q, k, v, gate, C, mode=SCAN_SEQUENTIAL, S0=None, z0=No
     _load().kor_forward_chunked_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), B, H, T, p, dv, C, mode, _ptr(S0),
                                       _ptr(z0), _ptr(o), _ptr(S), _ptr(z), nthreads)
     return o, S, z
+
+
+# ---------------------------------------------------------------- sampled rows
+
+def _rows(q, bh, t):
+    B, H, T = q.shape[:3]
+    bh = np.ascontiguousarray(np.asarray(bh, dtype=np.int64))
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int64))
+    if bh.shape != t.shape or (bh.size and (bh.min() < 0 or bh.max() >= B * H or t.min() < 0 or t.max() >= T)):
+        raise ValueError("row index out of range")
+    return bh, t
+
+
+def forward_plain_block_rows(q, k, v, family, g, bh, t, nthreads=0):
+    """Block-lift definition for rows (bh[r], t[r]). Returns [R, dv]."""
+    q, k, v = _shape4(q, k, v)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    _check_block(p, family, g)
+    bh, t = _rows(q, bh, t)
+    out = np.empty((bh.size, dv))
+    _load().kor_forward_plain_block_rows(_ptr(q), _ptr(k), _ptr(v), B, H, T, p, dv, int(family), int(g),
+                                         bh.ctypes.data_as(_I64), t.ctypes.data_as(_I64), bh.size, _ptr(out),
+                                         nthreads)
+    return out
+
+
+def forward_plain_gated_rows(q, k, v, gate, bh, t, nthreads=0):
+    """Gated definition for rows (bh[r], t[r]). Returns [R, dv]."""
+    q, k, v = _shape4(q, k, v)
+    gate = _gate(gate, q)
+    B, H, T, p = q.shape
+    dv = v.shape[-1]
+    bh, t = _rows(q, bh, t)
+    out = np.empty((bh.size, dv))
+    _load().kor_forward_plain_gated_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), B, H, T, p, dv,
+                                         bh.ctypes.data_as(_I64), t.ctypes.data_as(_I64), bh.size, _ptr(out),
+                                         nthreads)
+    return out
 
 
 def library_path() -> str:

@@ -163,3 +163,12 @@ def test_block_split_call_with_carried_state(fam, T1):
     np.testing.assert_allclose(np.concatenate([o1, o2], axis=2), o_ref, atol=1e-12)
     np.testing.assert_allclose(S2, S_ref, atol=1e-12)
     np.testing.assert_allclose(z2, z_ref, atol=1e-12)
+
+
+def test_sampled_block_rows_equal_the_full_definition():
+    q, k, v = _rand_qkv(2, 2, 40, 8, 3, seed=23)
+    bh = np.array([0, 3, 1, 2, 3])
+    t = np.array([0, 39, 17, 5, 20])
+    for fam in (SIGMA, MULTI):
+        full = oracle.forward_plain_block(q, k, v, fam, 2).reshape(4, 40, 3)
+        np.testing.assert_array_equal(oracle.forward_plain_block_rows(q, k, v, fam, 2, bh, t), full[bh, t])

@@ -116,3 +116,11 @@ def test_gated_outputs_inside_the_hull():
     o = oracle.forward_plain_gated(q, k, v, gate)
     assert np.all(o >= np.minimum.accumulate(v, axis=2) - 1e-12)
     assert np.all(o <= np.maximum.accumulate(v, axis=2) + 1e-12)
+
+
+def test_sampled_gated_rows_equal_the_full_definition():
+    q, k, v, gate = _rand(2, 2, 40, 6, 3, seed=70, lo=0.0)
+    bh = np.array([0, 3, 1, 2, 3])
+    t = np.array([0, 39, 17, 5, 20])
+    full = oracle.forward_plain_gated(q, k, v, gate).reshape(4, 40, 3)
+    np.testing.assert_array_equal(oracle.forward_plain_gated_rows(q, k, v, gate, bh, t), full[bh, t])
