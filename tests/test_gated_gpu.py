@@ -77,3 +77,19 @@ def test_gated_decode_steps(dtype, p, dv):
     torch.cuda.synchronize()
     ref = oracle.forward_plain_gated(f64(q), f64(k), f64(v), f64(gate))
     assert_close(f64(torch.stack(rows, dim=2)), ref, dtype, "gated decode")
+
+
+@pytest.mark.slow
+def test_gated_full_size_sampled_rows():
+    """The 16384-token, 16-head, p = dv = 64 bf16 workload (C = 64) with gates in
+    [0.9, 1], against the oracle's gated definition on sampled rows."""
+    from tests.parity import rows_error, sample_rows
+    w = inputs.WORKLOADS[2]
+    q, k, v = inputs.make(w, "cuda")
+    gate = torch.from_numpy(np.random.default_rng(3).uniform(0.9, 1.0, (w.B, w.H, w.T))).float().cuda()
+    o = kb.kata_forward_chunked_gated(q, k, v, gate, w.C)
+    torch.cuda.synchronize()
+    bh, t = sample_rows(w.B, w.H, w.T, w.C, per_head=6, seed=2)
+    ref = oracle.forward_plain_gated_rows(f64(q), f64(k), f64(v), f64(gate), bh, t)
+    got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
+    assert rows_error(got, ref) <= TOL[torch.bfloat16]
