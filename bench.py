@@ -115,6 +115,20 @@ def kernel_work(name, w, form="chunked", lift=None):
     if name == "states_tc":
         # segment start states: recomputed work, no algorithmic share
         return "flop", 0
+    if name == "backward_query_simt" or name == "backward_key_simt":
+        # prefix readout and its gradient (normaliser column included), two passes over the
+        # causal local half at the backward's 64-token chunks
+        return "flop", bht * (4 * w.n * (w.dv + 1) + 2 * 65 * (w.p + w.dv))
+    if name == "backward_gstates_simt" or name == "gated_states_simt":
+        return "flop", bht * 2 * w.n * (w.dv + 1)
+    if name in ("backward_rows_simt", "backward_cols_simt"):
+        # flash-style backward: two passes over the causal half per query (rows) or key (columns)
+        return "flop", bht * 2 * (w.T + 1) * (w.p + w.dv)
+    if name == "gated_output_simt":
+        return "flop", bht * (2 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
+    if name in ("gated_scan", "backward_reverse_scan"):
+        nc = w.NC if name == "gated_scan" else (w.T + 63) // 64
+        return "byte", 2 * w.B * w.H * nc * w.n * (w.dv + 1) * 4
     if name == "decode_step":
         # state and normaliser read and written once, the token's q, k, v read, o written
         elem = 4 if w.dtype == "fp32" else 2
@@ -340,6 +354,27 @@ def run_ours(args, world, rank, local):
 
         def step():
             kb.kata_decode_step_block(qt, kt, vt, S, z, lift[0], lift[1], o=ot, stream=stream)
+    elif args.form in ("backward", "backward_quadratic"):
+        g = torch.Generator(device=dev).manual_seed(rank)
+        dO = torch.randn(v.shape, generator=g, device=dev).to(v.dtype)
+        dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bform = "chunked" if args.form == "backward" else "quadratic"
+        lib = kb.load()
+        need = (lib.kata_backward_chunked_workspace_bytes(w.B, w.H, w.T, w.p, w.dv) if bform == "chunked"
+                else lib.kata_backward_quadratic_workspace_bytes(w.B, w.H, w.T))
+        wsg = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+
+        def step():
+            kb.kata_backward(q, k, v, dO, dq, dk, dvv, workspace=wsg, stream=stream, form=bform)
+    elif args.form == "gated":
+        g = torch.Generator(device=dev).manual_seed(rank)
+        gate = torch.rand((w.B, w.H, w.T), generator=g, device=dev) * 0.1 + 0.9
+        wsg = torch.empty(max(1, kb.load().kata_chunked_gated_workspace_bytes(kb._dtype_code(q), w.B, w.H, w.T, w.p,
+                                                                               w.dv, w.C)),
+                          dtype=torch.uint8, device=dev)
+
+        def step():
+            kb.kata_forward_chunked_gated(q, k, v, gate, w.C, o=o, workspace=wsg, stream=stream)
     elif args.form == "chunked_block":
         wsb = torch.empty(max(1, kb.kata_chunked_block_workspace_bytes(q.dtype, lift[0], lift[1], w.B, w.H, w.T,
                                                                        w.p, w.dv, w.C)),
@@ -468,6 +503,12 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
     torch.cuda.synchronize()
+    # which kernels one end-to-end step runs (single-head calls may cut each
+    # head into segments: a segment-state prepass and a scan of their totals)
+    kb.kata_trace_start(4096)
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_names = sorted({n for n, _ in kb.kata_trace_stop()})
     barrier(world)
     e0.record(stream)
     for _ in range(e2e_steps):
@@ -476,7 +517,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     e2e = {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "calls": f"one kata_forward_chunked call per head ({nh} calls)", "kernels": e2e_names,
+           "segment_prepass": "states_tc" in e2e_names,
+           "scan_ran": any(n.startswith("scan") for n in e2e_names)}
 
     if rank != 0:
         return
@@ -487,7 +531,9 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16" if not dom.endswith("_simt") else "f32",
         "data": "synthetic: seeded N(0,1) draws, q/k put on the unit sphere",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "p": w.p, "dv": w.dv, "C": w.C,
-                   "n": w.n, "scan_mode": args.scan, "inputs": "bf16",
+                   "n": w.n, "scan_mode_requested": args.scan,
+                   "segment_prepass": "states_tc" in per, "scan_ran": any(n.startswith("scan") for n in per),
+                   "inputs": "bf16",
                    "l2": f"inputs larger than L2 ({(h2d) / 1e6:.0f} MB), no flush",
                    "parallelism": f"replicas x{world}"},
         "algorithmic_tflops": alg_tflops,
@@ -515,7 +561,8 @@ def main():
                     help="dram bytes per call of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--form", default="chunked",
-                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode"] + list(BLOCK_FORMS),
+                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode", "backward",
+                             "backward_quadratic", "gated"] + list(BLOCK_FORMS),
                     help="entry point timed (the contract's line is the chunked forward)")
     ap.add_argument("--lift", default="sigma", choices=sorted(LIFTS), help="block-lift family of the *_block forms")
     ap.add_argument("--g", type=int, default=2, help="number of blocks of the *_block forms")

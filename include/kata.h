@@ -216,6 +216,72 @@ KATA_API kata_status kata_decode_step_block(const void* q, const void* k, const 
                                             cudaStream_t stream);
 
 /*
+ * Gated prefix (the Gated variant: "a Gated prefix adds the learned gate";
+ * its recurrence is in an appendix the pages do not contain).  Reading: one
+ * scalar gate per head and token, gate [B,H,T] fp32 (values in [0, 1] keep
+ * every weight nonnegative; others are used as given), scales the running
+ * state before the token's own term is added,
+ *   S_t = gate_t S_{t-1} + psi(kh_t) v_t^T,  z_t = gate_t z_{t-1} + psi(kh_t),
+ * and the readout is unchanged.  A zero gate forgets everything before its
+ * token; all-one gates give kata_forward_chunked.  The chunked form carries
+ * per-chunk decays and a one-step-per-chunk gated prefix.  Other arguments,
+ * states and errors as for kata_forward_chunked (S0 is scaled by gate_0).
+ */
+KATA_API size_t kata_chunked_gated_workspace_bytes(kata_dtype dtype, int B, int H, int T, int p, int dv,
+                                                   int C);
+KATA_API kata_status kata_forward_chunked_gated(const void* q, const void* k, const void* v,
+                                                const float* gate, void* o, kata_dtype dtype, int B,
+                                                int H, int T, int p, int dv, int C, const float* S0,
+                                                const float* z0, float* S_final, float* z_final,
+                                                void* workspace, size_t workspace_bytes,
+                                                cudaStream_t stream);
+
+/* Gated decode step: as kata_decode_step with the state scaled by the head's
+ * gate [B,H] fp32 first (S = gate S + psi(kh) v^T, z likewise). */
+KATA_API kata_status kata_decode_step_gated(const void* q, const void* k, const void* v,
+                                            const float* gate, void* o, kata_dtype dtype, int B, int H,
+                                            int p, int dv, float* S, float* z, cudaStream_t stream);
+
+/*
+ * Backward: the gradients of L = sum(dO * o) for the forward above (every
+ * form computes the same o), by the chain rule through the definition --
+ * the pages give no backward algorithm:
+ *   dv_s = sum_{t>=s} (w_ts / D_t) dO_t,  w_ts = (qh_t.kh_s)^2, D_t = sum_{s<=t} w_ts
+ *   dc_ts = 2 (qh_t.kh_s) (dO_t.v_s - dO_t.o_t) / D_t
+ *   dq_t, dk_s: sum_s dc_ts kh_s and sum_t dc_ts qh_t taken back through the
+ *   unit-sphere projections (the component along q_t or k_s removed, divided
+ *   by its norm).
+ * A row with a zero denominator passes no gradient; a zero q or k vector
+ * receives none.  q, k, dq, dk [B,H,T,p]; v, dO, dv [B,H,T,dv], all of
+ * `dtype` (gradients in the input dtype, fp32 arithmetic).
+ * kata_backward_quadratic: O(T^2) work per head (flash-style row and column
+ * passes over the causal triangle); workspace at least
+ * kata_backward_quadratic_workspace_bytes() bytes, 16-byte aligned.
+ */
+KATA_API size_t kata_backward_quadratic_workspace_bytes(int B, int H, int T);
+KATA_API kata_status kata_backward_quadratic(const void* q, const void* k, const void* v, const void* dO,
+                                             void* dq, void* dk, void* dv, kata_dtype dtype, int B, int H,
+                                             int T, int p, int dv_dim, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The same gradients in O(T) through the chunked form (chunks of 64 tokens,
+ * whatever the forward's C): the forward's exclusive prefix states are
+ * rebuilt; a query-side pass recomputes each row's normaliser D_t and
+ * dO_t . o_t and takes dq from the prefix and the chunk's own keys; the
+ * per-chunk gradient states sum_t psi(qh_t) [dO_t / D_t | -dO_t.o_t / D_t]
+ * are summed over later chunks (a reverse exclusive prefix); a key-side
+ * pass takes dk and dv from them and from the chunk's own later queries.
+ * Arguments as kata_backward_quadratic; workspace: at least
+ * kata_backward_chunked_workspace_bytes() bytes, 256-byte aligned.
+ */
+KATA_API size_t kata_backward_chunked_workspace_bytes(int B, int H, int T, int p, int dv_dim);
+KATA_API kata_status kata_backward_chunked(const void* q, const void* k, const void* v, const void* dO,
+                                           void* dq, void* dk, void* dv, kata_dtype dtype, int B, int H,
+                                           int T, int p, int dv_dim, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: KATA_OK, or KATA_ERR_TIMEOUT if a bounded device-side
  * wait expired in an earlier call (that call's outputs are then invalid).

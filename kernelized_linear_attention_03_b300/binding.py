@@ -32,7 +32,9 @@ SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_scan_states", "kata_get_device_status", "kata_trace_start", "kata_trace_stop",
            "kata_trace_get", "kata_forward_chunked_noalloc", "kata_decode_step", "kata_lift_dim",
            "kata_chunked_block_workspace_bytes", "kata_forward_chunked_block", "kata_forward_quadratic_block",
-           "kata_decode_step_block")
+           "kata_decode_step_block", "kata_backward_quadratic_workspace_bytes",
+           "kata_backward_quadratic", "kata_backward_chunked_workspace_bytes", "kata_backward_chunked",
+           "kata_chunked_gated_workspace_bytes", "kata_forward_chunked_gated", "kata_decode_step_gated")
 
 
 class KataError(RuntimeError):
@@ -84,6 +86,20 @@ def load():
     lib.kata_forward_quadratic_block.restype = I
     lib.kata_decode_step_block.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P]
     lib.kata_decode_step_block.restype = I
+    lib.kata_backward_quadratic_workspace_bytes.argtypes = [I, I, I]
+    lib.kata_backward_quadratic_workspace_bytes.restype = Z
+    lib.kata_backward_quadratic.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+    lib.kata_backward_quadratic.restype = I
+    lib.kata_backward_chunked_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.kata_backward_chunked_workspace_bytes.restype = Z
+    lib.kata_backward_chunked.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+    lib.kata_backward_chunked.restype = I
+    lib.kata_chunked_gated_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.kata_chunked_gated_workspace_bytes.restype = Z
+    lib.kata_forward_chunked_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, Z, P]
+    lib.kata_forward_chunked_gated.restype = I
+    lib.kata_decode_step_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
+    lib.kata_decode_step_gated.restype = I
     lib.kata_trace_start.argtypes = [I]
     lib.kata_trace_start.restype = I
     lib.kata_trace_stop.argtypes = []
@@ -312,6 +328,69 @@ def kata_decode_step_block(q, k, v, S, z, family, g, o=None, stream=None):
                                          int(family), int(g), _ptr(S), _ptr(z), _stream(stream)),
            "kata_decode_step_block")
     return o
+
+
+def kata_forward_chunked_gated(q, k, v, gate, C, S0=None, z0=None, o=None, S_final=None, z_final=None,
+                               workspace=None, stream=None):
+    """Gated chunked forward; gate [B,H,T] float32.  Returns o, or (o, S_final,
+    z_final) when state buffers are given."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if gate.shape != (B, H, T) or gate.dtype != torch.float32:
+        raise ValueError("expected a float32 gate [B,H,T]")
+    if o is None:
+        o = torch.empty_like(v)
+    need = int(load().kata_chunked_gated_workspace_bytes(_dtype_code(q), B, H, T, p, dv, int(C)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kata_forward_chunked_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _dtype_code(q), B, H,
+                                             T, p, dv, int(C), _ptr(S0), _ptr(z0), _ptr(S_final), _ptr(z_final),
+                                             _ptr(workspace), ws_bytes, _stream(stream)),
+           "kata_forward_chunked_gated")
+    return o if S_final is None else (o, S_final, z_final)
+
+
+def kata_decode_step_gated(q, k, v, gate, S, z, o=None, stream=None):
+    """Gated decode step; gate [B,H] float32; S, z updated in place.  Returns o."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,p] and v [B,H,dv]")
+    B, H, p = q.shape
+    dv = v.shape[-1]
+    if gate.shape != (B, H) or gate.dtype != torch.float32:
+        raise ValueError("expected a float32 gate [B,H]")
+    if o is None:
+        o = torch.empty_like(v)
+    _check(load().kata_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _dtype_code(q), B, H, p,
+                                         dv, _ptr(S), _ptr(z), _stream(stream)),
+           "kata_decode_step_gated")
+    return o
+
+
+def kata_backward(q, k, v, dO, dq=None, dk=None, dv=None, workspace=None, stream=None, form="chunked"):
+    """Gradients (dq, dk, dv) of sum(dO * o) for the forward of (q, k, v),
+    through the chunked form (O(T), default) or the quadratic form."""
+    B, H, T, p, dv_dim = _shapes(q, k, v)
+    if dO.shape != v.shape or dO.dtype != v.dtype:
+        raise ValueError("dO must match v's shape and dtype")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load()
+    if form == "chunked":
+        need, fn = int(lib.kata_backward_chunked_workspace_bytes(B, H, T, p, dv_dim)), lib.kata_backward_chunked
+    elif form == "quadratic":
+        need, fn = int(lib.kata_backward_quadratic_workspace_bytes(B, H, T)), lib.kata_backward_quadratic
+    else:
+        raise ValueError(f"unknown backward form {form!r}")
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _dtype_code(q), B, H, T, p, dv_dim,
+              _ptr(workspace), ws_bytes, _stream(stream)),
+           f"kata_backward_{form}")
+    return dq, dk, dv
 
 
 def kata_get_device_status(stream=None):

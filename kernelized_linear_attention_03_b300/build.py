@@ -8,6 +8,7 @@ import hashlib
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -21,10 +22,11 @@ FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-    "-shared", "-cudart", "shared",
-    "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64"),
     "-I", os.path.join(ROOT, "include"),
 ]
+LINK = ["-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-cudart", "shared",
+        "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64")]
+OBJ = os.path.join(PKG, "_build")
 
 
 def sources():
@@ -39,7 +41,7 @@ def _digest(extra):
         h.update(f.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(FLAGS + extra).encode())
+    h.update(" ".join(FLAGS + LINK + extra).encode())
     return h.hexdigest()
 
 
@@ -51,11 +53,21 @@ def build(force: bool = False, extra=(), verbose: bool = False) -> str:
         with open(STAMP) as f:
             if f.read().strip() == d:
                 return LIB
+    os.makedirs(OBJ, exist_ok=True)
+    objs = [os.path.join(OBJ, os.path.basename(src)[:-3] + ".o") for src in sources()]
+
+    def compile_one(src, obj):
+        cmd = [NVCC] + FLAGS + extra + ["-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd))
+        subprocess.run(cmd, check=True)
+
+    # one nvcc per translation unit, in parallel; then one link
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as pool:
+        for f in [pool.submit(compile_one, s_, o_) for s_, o_ in zip(sources(), objs)]:
+            f.result()
     tmp = LIB + ".tmp"
-    cmd = [NVCC] + FLAGS + extra + sources() + ["-o", tmp]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
+    subprocess.run([NVCC] + LINK + objs + ["-o", tmp], check=True)
     os.replace(tmp, LIB)
     with open(STAMP, "w") as f:
         f.write(d)

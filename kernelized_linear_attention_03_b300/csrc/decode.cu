@@ -28,11 +28,11 @@ constexpr int kDecThreads = 256;
 constexpr int kDecUnroll = 4;  // state rows of a thread in flight at once
 constexpr int kDecMaxSplit = 8;
 
-template <typename Tin, int P, int DV, bool BLOCK>
+template <typename Tin, int P, int DV, bool BLOCK, bool GATED = false>
 __global__ void __launch_bounds__(kDecThreads)
 decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                    Tin* __restrict__ o, float* __restrict__ S, float* __restrict__ z, int family, int g,
-                   int n_block) {
+                   int n_block, const float* __restrict__ gate = nullptr) {
     // full lift: N = p(p+1)/2; block lift (family, g): N = n_block
     const int N = BLOCK ? n_block : P * (P + 1) / 2;
     const int m = BLOCK ? P / g : P, nm = m * (m + 1) / 2;
@@ -63,6 +63,8 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
     const int r0 = split * per, r1 = min(N, r0 + per);
     const int c4 = tid % CPR, rr = tid / CPR;
     const float4 v4 = reinterpret_cast<const float4*>(vv)[c4];
+    // gated step: the state is scaled by the head's gate before the token is added
+    const float gam = GATED ? gate[bh] : 1.f;
     float4* Srow = reinterpret_cast<float4*>(S + bh * (int64_t)N * DV) + c4;
     float* zh = z + bh * (int64_t)N;
 
@@ -128,6 +130,12 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
                     }
                 }
                 float4 t = s[u];
+                if constexpr (GATED) {
+                    t.x *= gam;
+                    t.y *= gam;
+                    t.z *= gam;
+                    t.w *= gam;
+                }
                 t.x = fmaf(fk, v4.x, t.x);
                 t.y = fmaf(fk, v4.y, t.y);
                 t.z = fmaf(fk, v4.z, t.z);
@@ -138,7 +146,7 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
                 acc.z = fmaf(fq, t.z, acc.z);
                 acc.w = fmaf(fq, t.w, acc.w);
                 if (c4 == 0) {
-                    const float zn = zr[u] + fk;
+                    const float zn = (GATED ? gam * zr[u] : zr[u]) + fk;
                     zh[r] = zn;
                     den = fmaf(fq, zn, den);
                 }
@@ -189,7 +197,7 @@ decode_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const T
 
 template <typename Tin, int P, int DV>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH,
-                         int family, int g, cudaStream_t s) {
+                         int family, int g, const float* gate, cudaStream_t s) {
     const bool block = family != kLiftFull;
     const int N = block ? block_lift_dim(family, P, g) : P * (P + 1) / 2;
     if (N <= 0) return cudaErrorInvalidValue;
@@ -213,37 +221,43 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, f
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (block)
+    if (gate)
+        KATA_TRACED("decode_step_gated", s,
+                    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV, false, true>,
+                                           static_cast<const Tin*>(q), static_cast<const Tin*>(k),
+                                           static_cast<const Tin*>(v), static_cast<Tin*>(o), S, z, family, g, N,
+                                           gate));
+    else if (block)
         KATA_TRACED("decode_step_block", s,
                     e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV, true>, static_cast<const Tin*>(q),
                                            static_cast<const Tin*>(k), static_cast<const Tin*>(v),
-                                           static_cast<Tin*>(o), S, z, family, g, N));
+                                           static_cast<Tin*>(o), S, z, family, g, N, nullptr));
     else
         KATA_TRACED("decode_step", s,
                     e = cudaLaunchKernelEx(&cfg, decode_step_kernel<Tin, P, DV, false>, static_cast<const Tin*>(q),
                                            static_cast<const Tin*>(k), static_cast<const Tin*>(v),
-                                           static_cast<Tin*>(o), S, z, family, g, N));
+                                           static_cast<Tin*>(o), S, z, family, g, N, nullptr));
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename Tin, int P>
 cudaError_t by_dv(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH, int dv,
-                  int family, int g, cudaStream_t s) {
+                  int family, int g, const float* gate, cudaStream_t s) {
     switch (dv) {
-        case 16: return launch_typed<Tin, P, 16>(q, k, v, o, S, z, BH, family, g, s);
-        case 32: return launch_typed<Tin, P, 32>(q, k, v, o, S, z, BH, family, g, s);
-        case 64: return launch_typed<Tin, P, 64>(q, k, v, o, S, z, BH, family, g, s);
+        case 16: return launch_typed<Tin, P, 16>(q, k, v, o, S, z, BH, family, g, gate, s);
+        case 32: return launch_typed<Tin, P, 32>(q, k, v, o, S, z, BH, family, g, gate, s);
+        case 64: return launch_typed<Tin, P, 64>(q, k, v, o, S, z, BH, family, g, gate, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <typename Tin>
 cudaError_t by_p(const void* q, const void* k, const void* v, void* o, float* S, float* z, int BH, int p, int dv,
-                 int family, int g, cudaStream_t s) {
+                 int family, int g, const float* gate, cudaStream_t s) {
     switch (p) {
-        case 16: return by_dv<Tin, 16>(q, k, v, o, S, z, BH, dv, family, g, s);
-        case 32: return by_dv<Tin, 32>(q, k, v, o, S, z, BH, dv, family, g, s);
-        case 64: return by_dv<Tin, 64>(q, k, v, o, S, z, BH, dv, family, g, s);
+        case 16: return by_dv<Tin, 16>(q, k, v, o, S, z, BH, dv, family, g, gate, s);
+        case 32: return by_dv<Tin, 32>(q, k, v, o, S, z, BH, dv, family, g, gate, s);
+        case 64: return by_dv<Tin, 64>(q, k, v, o, S, z, BH, dv, family, g, gate, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -251,9 +265,10 @@ cudaError_t by_p(const void* q, const void* k, const void* v, void* o, float* S,
 }  // namespace
 
 cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
-                               float* z, int BH, int p, int dv, int family, int g, cudaStream_t s) {
-    return dtype == 0 ? by_p<float>(q, k, v, o, S, z, BH, p, dv, family, g, s)
-                      : by_p<__nv_bfloat16>(q, k, v, o, S, z, BH, p, dv, family, g, s);
+                               float* z, int BH, int p, int dv, int family, int g, const float* gate,
+                               cudaStream_t s) {
+    return dtype == 0 ? by_p<float>(q, k, v, o, S, z, BH, p, dv, family, g, gate, s)
+                      : by_p<__nv_bfloat16>(q, k, v, o, S, z, BH, p, dv, family, g, gate, s);
 }
 
 }  // namespace kata

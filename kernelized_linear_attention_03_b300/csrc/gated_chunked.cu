@@ -1,0 +1,276 @@
+// Gated chunked forward on CUDA cores (fp32 arithmetic, any input dtype).
+// One scalar gate gamma_t in [0, 1] per head and token scales the running
+// state before the token's own term is added,
+//   S_t = gamma_t S_{t-1} + psi(kh_t) v_t^T,   z_t = gamma_t z_{t-1} + psi(kh_t),
+// and the readout is unchanged.  The three phases of the chunked form carry
+// decays (all as direct products of gates, so a zero gate is exact):
+//   local state  X_c = sum_{s in c} (prod_{r=s+1..end_c} gamma_r) psi(kh_s) v_s^T,
+//   chunk decay  a_c = prod_{r in c} gamma_r,
+//   prefix       P_0 = S0,  P_{c+1} = a_c P_c + X_c   (one step per chunk),
+//   output       num_t = (prod_{r=c C..t} gamma_r) psi(qh_t)^T P_c
+//                        + sum_{s in c, s<=t} (prod_{r=s+1..t} gamma_r) (qh_t.kh_s)^2 v_s,
+//                den_t likewise with 1 for v_s.
+#include "kata_device.cuh"
+#include "kata_internal.h"
+
+namespace kata {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxC = 128;
+constexpr int kRowsPerBlock = 64;
+constexpr int kTile = 32;
+
+// ---------------------------------------------------------------- chunk states
+template <int P, int DV>
+constexpr size_t state_smem_bytes() {
+    return sizeof(float) * (kMaxC * (P + 1) + kMaxC * DV + kMaxC);
+}
+
+// Block (chunk c, tile of 64 packed rows, head bh); also writes the chunk
+// decay a_c (block y = 0, thread 0).
+template <typename Tin, int P, int DV>
+__global__ void __launch_bounds__(kThreads)
+gated_states_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v, const float* __restrict__ gate,
+                    float* __restrict__ X, float* __restrict__ Xz, float* __restrict__ a, int T, int C, int NC) {
+    constexpr int LDP = P + 1, CPT = DV / 4, N = P * (P + 1) / 2;
+    extern __shared__ float smem[];
+    float* Ks = smem;              // [C][LDP] unit keys
+    float* Vs = Ks + kMaxC * LDP;  // [C][DV]
+    float* dec = Vs + kMaxC * DV;  // [C] decay from token s to the chunk's end
+    const int c = blockIdx.x;
+    const int64_t bh = blockIdx.z;
+    const int t0 = c * C, len = min(C, T - t0);
+    load_rows_unit<Tin, P>(k + bh * T * P, t0, len, T, Ks, LDP);
+    load_rows_plain<Tin, DV>(v + bh * T * DV, t0, len, T, Vs, DV);
+    if (threadIdx.x == 0) {
+        const float* g = gate + bh * T + t0;
+        float d = 1.f;
+        for (int s = len - 1; s >= 0; --s) {
+            dec[s] = d;  // prod_{r=s+1..len-1} gamma
+            d *= g[s];
+        }
+        if (blockIdx.y == 0) a[bh * NC + c] = d;  // prod over the whole chunk
+    }
+    __syncthreads();
+
+    const int r = blockIdx.y * kRowsPerBlock + (threadIdx.x >> 2), cg = threadIdx.x & 3;
+    if (r >= N) return;
+    int i, j;
+    unpack_index(r, P, i, j);
+    const float scale = (i == j) ? 1.f : kSqrt2;
+    float acc[CPT];
+#pragma unroll
+    for (int x = 0; x < CPT; ++x) acc[x] = 0.f;
+    float zacc = 0.f;
+    for (int s = 0; s < len; ++s) {
+        const float psi = dec[s] * Ks[s * LDP + i] * Ks[s * LDP + j] * scale;
+        zacc += psi;
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) acc[x] = fmaf(psi, Vs[s * DV + cg * CPT + x], acc[x]);
+    }
+    float* dst = X + ((bh * NC + c) * N + r) * DV + cg * CPT;
+#pragma unroll
+    for (int x = 0; x < CPT; ++x) dst[x] = acc[x];
+    if (cg == 0) Xz[(bh * NC + c) * N + r] = zacc;
+}
+
+// ---------------------------------------------------------------- gated prefix
+// x [heads][NC][W] -> exclusive gated prefix in place: y_c = P_c with P_0 =
+// init (or 0) and P_{c+1} = a_c P_c + x_c; fin (or null) receives P_NC.
+// One thread per column, one step per chunk.
+__global__ void gated_scan_kernel(float* __restrict__ x, const float* __restrict__ a, const float* __restrict__ init,
+                                  float* __restrict__ fin, int64_t heads, int64_t NC, int64_t W) {
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= heads * W) return;
+    const int64_t h = gid / W, e = gid - h * W;
+    float run = init ? init[h * W + e] : 0.f;
+    float* col = x + h * NC * W + e;
+    const float* ah = a + h * NC;
+    for (int64_t c = 0; c < NC; ++c) {
+        const float xc = col[c * W];
+        col[c * W] = run;
+        run = fmaf(ah[c], run, xc);
+    }
+    if (fin) fin[h * W + e] = run;
+}
+
+// ---------------------------------------------------------------- chunk output
+template <int P, int DV>
+constexpr size_t output_smem_bytes() {
+    return sizeof(float) * (2 * kMaxC * (P + 1) + kMaxC * DV + kMaxC * (kTile + 1) + kTile * DV + kTile +
+                            kMaxC * (kTile + 1) + kMaxC) +
+           sizeof(int) * 2 * kTile;
+}
+
+// Block (chunk c, head bh): thread owns token tid/2 and half of the value
+// columns; the local part walks the chunk's keys from the token backwards so
+// the decay is one running product.
+template <typename Tin, int P, int DV>
+__global__ void __launch_bounds__(kThreads)
+gated_output_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+                    const float* __restrict__ gate, const float* __restrict__ Pre, const float* __restrict__ Prez,
+                    Tin* __restrict__ o, int T, int C, int NC) {
+    constexpr int LDP = P + 1, LDT = kTile + 1, CPT = DV / 2, N = P * (P + 1) / 2;
+    extern __shared__ float smem[];
+    float* Qs = smem;              // [C][LDP]
+    float* Ks = Qs + kMaxC * LDP;  // [C][LDP]
+    float* Vs = Ks + kMaxC * LDP;  // [C][DV]
+    float* Ps = Vs + kMaxC * DV;   // [C][LDT] lifted-query tile
+    float* St = Ps + kMaxC * LDT;  // [kTile][DV] prefix state tile
+    float* Zt = St + kTile * DV;   // [kTile]
+    float* Sc = Zt + kTile;        // [C][LDT] local score tile
+    float* gs = Sc + kMaxC * LDT;  // [C] gates of the chunk
+    int* Ii = reinterpret_cast<int*>(gs + kMaxC);
+    int* Jj = Ii + kTile;
+
+    const int c = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * C, len = min(C, T - t0);
+    load_rows_unit<Tin, P>(q + bh * T * P, t0, len, T, Qs, LDP);
+    load_rows_unit<Tin, P>(k + bh * T * P, t0, len, T, Ks, LDP);
+    load_rows_plain<Tin, DV>(v + bh * T * DV, t0, len, T, Vs, DV);
+    for (int s = threadIdx.x; s < kMaxC; s += blockDim.x) gs[s] = s < len ? gate[bh * T + t0 + s] : 0.f;
+
+    const int t = threadIdx.x >> 1, half = threadIdx.x & 1;
+    float acc[CPT];
+#pragma unroll
+    for (int x = 0; x < CPT; ++x) acc[x] = 0.f;
+    float den = 0.f;
+
+    // prefix readout psi(qh_t)^T P_c, scaled afterwards by prod_{r=t0..t} gamma
+    const float* Pc = Pre + (bh * NC + c) * (int64_t)N * DV;
+    const float* Pzc = Prez + (bh * NC + c) * (int64_t)N;
+    for (int a0 = 0; a0 < N; a0 += kTile) {
+        __syncthreads();
+        if (threadIdx.x < kTile) {
+            int i = 0, j = 0;
+            if (a0 + threadIdx.x < N) unpack_index(a0 + threadIdx.x, P, i, j);
+            Ii[threadIdx.x] = i;
+            Jj[threadIdx.x] = j;
+            Zt[threadIdx.x] = a0 + threadIdx.x < N ? Pzc[a0 + threadIdx.x] : 0.f;
+        }
+        for (int e = threadIdx.x; e < kTile * DV; e += blockDim.x) {
+            const int aa = e / DV;
+            St[e] = a0 + aa < N ? Pc[(int64_t)a0 * DV + e] : 0.f;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
+            const int tt = e / kTile, aa = e - tt * kTile;
+            const int i = Ii[aa], j = Jj[aa];
+            const float scale = (i == j) ? 1.f : kSqrt2;
+            Ps[tt * LDT + aa] = a0 + aa < N ? Qs[tt * LDP + i] * Qs[tt * LDP + j] * scale : 0.f;
+        }
+        __syncthreads();
+        if (t < len) {
+            for (int aa = 0; aa < kTile; ++aa) {
+                const float ps = Ps[t * LDT + aa];
+                den = fmaf(ps, Zt[aa], den);
+#pragma unroll
+                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(ps, St[aa * DV + half * CPT + x], acc[x]);
+            }
+        }
+    }
+    if (t < len) {
+        float h = 1.f;
+        for (int r = 0; r <= t; ++r) h *= gs[r];
+        den *= h;
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) acc[x] *= h;
+    }
+    // local part: key tiles from the token's own tile backwards
+    float decay = 1.f;  // prod_{r=s+1..t} gamma for the key s being added
+    const int last_tile = (len - 1) / kTile;
+    for (int tile = last_tile; tile >= 0; --tile) {
+        const int s0 = tile * kTile;
+        __syncthreads();
+        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
+            const int tt = e / kTile, ss = e - tt * kTile, s = s0 + ss;
+            float d = 0.f;
+            if (s < len && s <= tt) {
+#pragma unroll 16
+                for (int i = 0; i < P; ++i) d = fmaf(Qs[tt * LDP + i], Ks[s * LDP + i], d);
+            }
+            Sc[tt * LDT + ss] = d * d;
+        }
+        __syncthreads();
+        if (t < len) {
+            for (int ss = kTile - 1; ss >= 0; --ss) {
+                const int s = s0 + ss;
+                if (s > t || s >= len) continue;
+                if (s < t) decay *= gs[s + 1];
+                const float sc = decay * Sc[t * LDT + ss];
+                den += sc;
+#pragma unroll
+                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(sc, Vs[s * DV + half * CPT + x], acc[x]);
+            }
+        }
+    }
+    if (t < len) {
+        Tin* ot = o + (bh * T + t0 + t) * DV + half * CPT;
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) store_as(ot + x, den > 0.f ? acc[x] / den : 0.f);
+    }
+}
+
+template <typename Tin, int P, int DV>
+cudaError_t gated_typed(const void* q, const void* k, const void* v, const float* gate, void* o, float* X, float* Xz,
+                        float* a, const float* S0, const float* z0, float* S_final, float* z_final, int BH, int T,
+                        int C, cudaStream_t s) {
+    constexpr int N = P * (P + 1) / 2;
+    const int NC = (T + C - 1) / C;
+    {
+        constexpr size_t smem = state_smem_bytes<P, DV>();
+        auto kern = gated_states_kernel<Tin, P, DV>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        KATA_TRACED("gated_states_simt", s,
+                    kern<<<dim3(NC, (N + kRowsPerBlock - 1) / kRowsPerBlock, BH), kThreads, smem, s>>>(
+                        static_cast<const Tin*>(k), static_cast<const Tin*>(v), gate, X, Xz, a, T, C, NC));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    for (int part = 0; part < 2; ++part) {
+        const int64_t W = part == 0 ? (int64_t)N * DV : N;
+        const int64_t threads = (int64_t)BH * W;
+        KATA_TRACED("gated_scan", s,
+                    (gated_scan_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+                        part == 0 ? X : Xz, a, part == 0 ? S0 : z0, part == 0 ? S_final : z_final, BH, NC, W)));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    constexpr size_t smem = output_smem_bytes<P, DV>();
+    auto kern = gated_output_kernel<Tin, P, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    KATA_TRACED("gated_output_simt", s,
+                kern<<<dim3(NC, BH), kThreads, smem, s>>>(static_cast<const Tin*>(q), static_cast<const Tin*>(k),
+                                                          static_cast<const Tin*>(v), gate, X, Xz,
+                                                          static_cast<Tin*>(o), T, C, NC));
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t gated_dispatch(int p, int dv, const void* q, const void* k, const void* v, const float* gate, void* o,
+                           float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
+                           float* z_final, int BH, int T, int C, cudaStream_t s) {
+#define KATA_CASE(P_, DV_)                                                                                      \
+    if (p == P_ && dv == DV_)                                                                                   \
+        return gated_typed<Tin, P_, DV_>(q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH, T, C, s);
+    KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
+    KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
+    KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)
+#undef KATA_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_chunked_gated(int dtype, const void* q, const void* k, const void* v, const float* gate, void* o,
+                                 float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
+                                 float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s) {
+    return dtype == 0 ? gated_dispatch<float>(p, dv, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH, T, C, s)
+                      : gated_dispatch<__nv_bfloat16>(p, dv, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH,
+                                                      T, C, s);
+}
+
+}  // namespace kata

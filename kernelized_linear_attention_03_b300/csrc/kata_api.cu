@@ -138,7 +138,8 @@ kata_status check_lift(kata_lift_family family, int p, int g) {
 
 // Shared body of the decode steps (shapes and lift already checked).
 kata_status decode_common(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B, int H, int p,
-                          int dv, int family, int g, float* S, float* z, cudaStream_t stream) {
+                          int dv, int family, int g, float* S, float* z, cudaStream_t stream,
+                          const float* gate = nullptr) {
     kata_status st = KATA_OK;
     const int64_t BH = (int64_t)B * H, n = lift_dim(family, p, g);
     if (BH == 0) return KATA_OK;
@@ -148,11 +149,12 @@ kata_status decode_common(const void* q, const void* k, const void* v, void* o, 
         (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
         (st = check_buffer(S, sb)) != KATA_OK || (st = check_buffer(z, zb)) != KATA_OK)
         return st;
+    if (gate && (st = check_buffer(gate, sizeof(float) * (size_t)BH)) != KATA_OK) return st;
     // S and z are updated in place by different threads: they must not overlap.
     const char* sp = reinterpret_cast<const char*>(S);
     const char* zp = reinterpret_cast<const char*>(z);
     if (sp < zp + zb && zp < sp + sb) return KATA_ERR_INVALID_ARG;
-    return cuda_status(kata::launch_decode_step(dt, q, k, v, o, S, z, (int)BH, p, dv, family, g, stream));
+    return cuda_status(kata::launch_decode_step(dt, q, k, v, o, S, z, (int)BH, p, dv, family, g, gate, stream));
 }
 
 }  // namespace
@@ -406,6 +408,126 @@ kata_status kata_decode_step_block(const void* q, const void* k, const void* v, 
     if (st != KATA_OK) return st;
     if ((st = check_lift(family, p, g)) != KATA_OK) return st;
     return decode_common(q, k, v, o, dt, B, H, p, dv, family, g, S, z, stream);
+}
+
+size_t kata_backward_quadratic_workspace_bytes(int B, int H, int T) {
+    if (B < 0 || H < 0 || T < 0) return 0;
+    const int64_t rows = (int64_t)B * H * T;
+    return rows == 0 ? 0 : 2 * round_up(sizeof(float) * (size_t)rows, 256);
+}
+
+kata_status kata_backward_quadratic(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                                    void* dv, kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv_dim);
+    if (st != KATA_OK) return st;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv_dim;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(dO, v_bytes)) != KATA_OK ||
+        (st = check_buffer(dq, qk_bytes)) != KATA_OK || (st = check_buffer(dk, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(dv, v_bytes)) != KATA_OK)
+        return st;
+    const size_t need = kata_backward_quadratic_workspace_bytes(B, H, T);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    float* D_ws = static_cast<float*>(ws);
+    float* delta_ws = reinterpret_cast<float*>(static_cast<char*>(ws) + need / 2);
+    return cuda_status(kata::launch_backward(dt, q, k, v, dO, dq, dk, dv, D_ws, delta_ws, B * H, T, p, dv_dim,
+                                             stream));
+}
+
+kata_status kata_decode_step_gated(const void* q, const void* k, const void* v, const float* gate, void* o,
+                                   kata_dtype dt, int B, int H, int p, int dv, float* S, float* z,
+                                   cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, 1, p, dv);
+    if (st != KATA_OK) return st;
+    if ((int64_t)B * H > 0 && gate == nullptr) return KATA_ERR_INVALID_ARG;
+    return decode_common(q, k, v, o, dt, B, H, p, dv, KATA_LIFT_FULL, 1, S, z, stream, gate);
+}
+
+size_t kata_chunked_gated_workspace_bytes(kata_dtype dt, int B, int H, int T, int p, int dv, int C) {
+    if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C)) return 0;
+    const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C;
+    if (BH * T == 0) return 0;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C);
+    return w.total + round_up(sizeof(float) * (size_t)(BH * NC), 256);
+}
+
+kata_status kata_forward_chunked_gated(const void* q, const void* k, const void* v, const float* gate, void* o,
+                                       kata_dtype dt, int B, int H, int T, int p, int dv, int C, const float* S0,
+                                       const float* z0, float* S_final, float* z_final, void* ws, size_t ws_bytes,
+                                       cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if (!c_ok(C)) return KATA_ERR_UNSUPPORTED;
+    if ((S0 == nullptr) != (z0 == nullptr)) return KATA_ERR_INVALID_ARG;
+    if ((S_final == nullptr) != (z_final == nullptr)) return KATA_ERR_INVALID_ARG;
+    const int64_t BH = (int64_t)B * H, n = packed(p);
+    if (BH == 0) return KATA_OK;
+    const size_t s_bytes = sizeof(float) * BH * n * dv, z_bytes = sizeof(float) * BH * n;
+    if (S0 && ((st = check_buffer(S0, s_bytes)) != KATA_OK || (st = check_buffer(z0, z_bytes)) != KATA_OK))
+        return st;
+    if (S_final &&
+        ((st = check_buffer(S_final, s_bytes)) != KATA_OK || (st = check_buffer(z_final, z_bytes)) != KATA_OK))
+        return st;
+    if (T == 0) {
+        if (S_final == nullptr) return KATA_OK;
+        cudaError_t e = kata::launch_copy_or_zero(S0, S_final, BH * n * dv, stream);
+        if (e == cudaSuccess) e = kata::launch_copy_or_zero(z0, z_final, BH * n, stream);
+        return cuda_status(e);
+    }
+    const size_t qk_bytes = elem_bytes(dt) * BH * T * p, v_bytes = elem_bytes(dt) * BH * T * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
+        (st = check_buffer(gate, sizeof(float) * (size_t)(BH * T))) != KATA_OK)
+        return st;
+    const size_t need = kata_chunked_gated_workspace_bytes(dt, B, H, T, p, dv, C);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C);
+    float* X = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
+    float* Xz = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
+    float* a = reinterpret_cast<float*>(static_cast<char*>(ws) + w.total);
+    return cuda_status(kata::launch_chunked_gated(dt, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, (int)BH,
+                                                  T, p, dv, C, stream));
+}
+
+size_t kata_backward_chunked_workspace_bytes(int B, int H, int T, int p, int dv_dim) {
+    if (B < 0 || H < 0 || T < 0 || !p_ok(p) || !dv_ok(dv_dim)) return 0;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return 0;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv_dim, kata::backward_chunk_len());
+    return w.total + 2 * round_up(sizeof(float) * (size_t)rows, 256);
+}
+
+kata_status kata_backward_chunked(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                                  void* dv, kata_dtype dt, int B, int H, int T, int p, int dv_dim, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv_dim);
+    if (st != KATA_OK) return st;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv_dim;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(dO, v_bytes)) != KATA_OK ||
+        (st = check_buffer(dq, qk_bytes)) != KATA_OK || (st = check_buffer(dk, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(dv, v_bytes)) != KATA_OK)
+        return st;
+    const size_t need = kata_backward_chunked_workspace_bytes(B, H, T, p, dv_dim);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    const ChunkedWs w = chunked_ws(B, H, T, p, dv_dim, kata::backward_chunk_len());
+    char* base = static_cast<char*>(ws);
+    float* S_ws = reinterpret_cast<float*>(base + w.s_off);
+    float* z_ws = reinterpret_cast<float*>(base + w.z_off);
+    float* D_ws = reinterpret_cast<float*>(base + w.total);
+    float* dl_ws = reinterpret_cast<float*>(base + w.total + round_up(sizeof(float) * (size_t)rows, 256));
+    return cuda_status(kata::launch_backward_chunked(dt, q, k, v, dO, dq, dk, dv, S_ws, z_ws, D_ws, dl_ws, (int)(B * H),
+                                                     T, p, dv_dim, stream));
 }
 
 kata_status kata_get_device_status(cudaStream_t stream) {

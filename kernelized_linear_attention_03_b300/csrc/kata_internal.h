@@ -65,8 +65,16 @@ cudaError_t launch_scan(int mode, const float* x, float* y, const float* init, f
 // (S [BH,n,dv], z [BH,n] fp32), o = psi(qh)^T S / psi(qh)^T z [BH,dv].
 // family 0 (g = 1): the full lift; 1 / 2: KATA-Sigma-g / KATA-M-g
 // (block_lift.cuh), n = block_lift_dim(family, p, g).
+// gate (or null): [BH] fp32, the gated step S = gate S + psi(kh) v^T (full lift only).
 cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const void* v, void* o, float* S,
-                               float* z, int BH, int p, int dv, int family, int g, cudaStream_t s);
+                               float* z, int BH, int p, int dv, int family, int g, const float* gate,
+                               cudaStream_t s);
+
+// Gated chunked forward (CUDA cores, any dtype): gate [BH,T] fp32; X [BH,NC,n,dv],
+// Xz [BH,NC,n], a [BH,NC] fp32 scratch; optional S0/z0 and S_final/z_final.
+cudaError_t launch_chunked_gated(int dtype, const void* q, const void* k, const void* v, const float* gate, void* o,
+                                 float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
+                                 float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s);
 
 // Block-lift forwards on CUDA cores (family 1 Sigma-g, 2 M-g; block_lift.cuh),
 // any dtype: per-chunk states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] in the
@@ -79,6 +87,20 @@ cudaError_t launch_block_output(int dtype, const void* q, const void* k, const v
                                 cudaStream_t s);
 cudaError_t launch_block_quadratic(int dtype, const void* q, const void* k, const void* v, void* o, int BH, int T,
                                    int p, int dv, int family, int g, cudaStream_t s);
+
+// Backward of the forward (CUDA cores, any dtype): dq, dk [BH,T,p] and dv
+// [BH,T,dv] in the input dtype from dO [BH,T,dv]; D_ws and delta_ws are
+// [BH,T] fp32 scratch (row normalisers and dO . o).
+// O(T) backward through the chunked form; S_ws [BH,NC,n,dv], z_ws [BH,NC,n]
+// (NC = ceil(T / backward_chunk_len())), D_ws, delta_ws [BH,T], all fp32.
+int backward_chunk_len();
+cudaError_t launch_backward_chunked(int dtype, const void* q, const void* k, const void* v, const void* dO, void* dq,
+                                    void* dk, void* dv, float* S_ws, float* z_ws, float* D_ws, float* delta_ws, int BH,
+                                    int T, int p, int dv_dim, cudaStream_t s);
+
+cudaError_t launch_backward(int dtype, const void* q, const void* k, const void* v, const void* dO, void* dq,
+                            void* dk, void* dv, float* D_ws, float* delta_ws, int BH, int T, int p, int dv_dim,
+                            cudaStream_t s);
 
 // dst[i] = src ? src[i] : 0 for i < count (fp32), used for pass-through states.
 cudaError_t launch_copy_or_zero(const float* src, float* dst, int64_t count, cudaStream_t s);

@@ -172,3 +172,33 @@ def test_block_argument_errors(lib):
     assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, 4, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
     assert d(P, P, P, P, kb.KATA_BF16, 1, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_ERR_INVALID_ARG
     assert d(P, P, P, P, kb.KATA_BF16, 0, 1, 16, 16, kb.KATA_LIFT_MULTI, 2, P, P, P) == kb.KATA_OK
+
+
+def test_backward_workspace_and_argument_errors(lib):
+    assert kb.load().kata_backward_quadratic_workspace_bytes(1, 2, 100) == 2 * ((2 * 100 * 4 + 255) // 256) * 256
+    assert kb.load().kata_backward_quadratic_workspace_bytes(0, 2, 100) == 0
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert kb.load().kata_backward_chunked_workspace_bytes(1, 2, 100, 16, 16) == (
+        r(2 * 2 * 136 * 16 * 4) + r(2 * 2 * 136 * 4) + 2 * r(2 * 100 * 4))
+    f = lib.kata_backward_quadratic
+    P = None
+    assert f(P, P, P, P, P, P, P, 7, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 24, 16, P, 0, P) == kb.KATA_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, P, P, kb.KATA_FP32, 1, 1, 0, 16, 16, P, 0, P) == kb.KATA_OK
+
+
+def test_gated_argument_errors(lib):
+    P = None
+    f = lib.kata_forward_chunked_gated
+    assert f(P, P, P, P, P, 9, 1, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, 48, P, P, P, P, P, 0, P) == kb.KATA_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, kb.KATA_FP32, 1, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, kb.KATA_FP32, 0, 1, 8, 16, 16, 32, P, P, P, P, P, 0, P) == kb.KATA_OK
+    d = lib.kata_decode_step_gated
+    assert d(P, P, P, P, P, kb.KATA_FP32, 1, 1, 16, 16, P, P, P) == kb.KATA_ERR_INVALID_ARG
+    assert d(P, P, P, P, P, kb.KATA_FP32, 0, 1, 16, 16, P, P, P) == kb.KATA_OK
+    # states [BH, NC, n, dv] + [BH, NC, n] + chunk decays [BH, NC], each 256-byte aligned
+    got = lib.kata_chunked_gated_workspace_bytes(kb.KATA_FP32, 1, 2, 100, 16, 16, 32)
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert got == r(2 * 4 * 136 * 16 * 4) + r(2 * 4 * 136 * 4) + r(2 * 4 * 4)

@@ -129,3 +129,19 @@ def test_block_argument_errors():
     with pytest.raises(kb.KataError) as e:
         kb.kata_forward_quadratic_block(q, k, v, kb.KATA_LIFT_FULL, 2)
     assert e.value.status == kb.KATA_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_chunked_block_full_size_sampled_rows():
+    """KATA-Sigma-2 on the 131072-token, 8-head, p = dv = 64 bf16 workload (C = 128),
+    against the oracle's definition on sampled rows (first, last, chunk edges,
+    random positions) of every head."""
+    from tests.parity import rows_error, sample_rows
+    w = inputs.WORKLOADS[3]
+    q, k, v = inputs.make(w, "cuda")
+    o = kb.kata_forward_chunked_block(q, k, v, w.C, SIGMA, 2)
+    torch.cuda.synchronize()
+    bh, t = sample_rows(w.B, w.H, w.T, w.C, per_head=6, seed=1)
+    ref = oracle.forward_plain_block_rows(f64(q), f64(k), f64(v), SIGMA, 2, bh, t)
+    got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
+    assert rows_error(got, ref) <= TOL[torch.bfloat16]

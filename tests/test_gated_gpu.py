@@ -1,0 +1,131 @@
+"""GPU parity of the gated prefix (kata_forward_chunked_gated,
+kata_decode_step_gated) against the fp64 oracle's gated forms."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kernelized_linear_attention_03_b300 import binding as kb
+from kernelized_linear_attention_03_b300 import inputs
+from tests.parity import TOL, assert_close, f64
+
+pytestmark = pytest.mark.gpu
+DNAME = {torch.float32: "fp32", torch.bfloat16: "bf16"}
+
+
+def _case(B, H, T, p, dv, dtype, seed, lo=0.5):
+    q, k, v = inputs.make(inputs.small(B, H, T, p, dv, 32, DNAME[dtype], "raw", seed), "cuda")
+    gate = torch.from_numpy(np.random.default_rng(seed).uniform(lo, 1.0, (B, H, T))).float().cuda()
+    return q, k, v, gate
+
+
+def _rel(a, b):
+    return float(np.abs(np.asarray(a) - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 64)])
+@pytest.mark.parametrize("C", [32, 128])
+def test_gated_chunked_matches_the_definition(dtype, p, dv, C):
+    q, k, v, gate = _case(1, 2, 200, p, dv, dtype, seed=p + dv + C)
+    o = kb.kata_forward_chunked_gated(q, k, v, gate, C)
+    torch.cuda.synchronize()
+    ref = oracle.forward_plain_gated(f64(q), f64(k), f64(v), f64(gate))
+    assert_close(f64(o), ref, dtype, "gated chunked")
+
+
+def test_gated_zero_gates_and_unit_gates():
+    q, k, v, gate = _case(1, 2, 150, 32, 32, torch.float32, seed=3)
+    gate[:, :, 40] = 0.0
+    gate[:, :, 97] = 0.0
+    o = kb.kata_forward_chunked_gated(q, k, v, gate, 32)
+    ones = torch.ones_like(gate)
+    o1 = kb.kata_forward_chunked_gated(q, k, v, ones, 64)
+    torch.cuda.synchronize()
+    assert_close(f64(o), oracle.forward_plain_gated(f64(q), f64(k), f64(v), f64(gate)), torch.float32, "zero gates")
+    assert_close(f64(o1), oracle.forward_plain(f64(q), f64(k), f64(v)), torch.float32, "unit gates")
+
+
+def test_gated_states_and_split_calls():
+    dtype, p, dv, C = torch.float32, 16, 32, 32
+    B, H, T1, T2 = 1, 2, 77, 50
+    q, k, v, gate = _case(B, H, T1 + T2, p, dv, dtype, seed=9)
+    n = p * (p + 1) // 2
+    S, z = torch.empty(B, H, n, dv, device="cuda"), torch.empty(B, H, n, device="cuda")
+    S2, z2 = torch.empty_like(S), torch.empty_like(z)
+    part = lambda x, a, b: x[:, :, a:b].contiguous()  # noqa: E731
+    o1, _, _ = kb.kata_forward_chunked_gated(part(q, 0, T1), part(k, 0, T1), part(v, 0, T1), part(gate, 0, T1), C,
+                                             S_final=S, z_final=z)
+    o2, _, _ = kb.kata_forward_chunked_gated(part(q, T1, T1 + T2), part(k, T1, T1 + T2), part(v, T1, T1 + T2),
+                                             part(gate, T1, T1 + T2), C, S0=S, z0=z, S_final=S2, z_final=z2)
+    torch.cuda.synchronize()
+    ref = oracle.forward_plain_gated(f64(q), f64(k), f64(v), f64(gate))
+    assert_close(np.concatenate([f64(o1), f64(o2)], axis=2), ref, dtype, "gated split")
+    _, S_ref, z_ref = oracle.forward_recurrent_gated(f64(q), f64(k), f64(v), f64(gate))
+    assert _rel(f64(S2), S_ref) <= TOL[dtype] and _rel(f64(z2), z_ref) <= TOL[dtype]
+
+
+def _readout_condition(q, k, gate):
+    """kappa_t = tr(Z_t) / (qh_t^T Z_t qh_t) with Z_t = sum_s d_ts kh_s kh_s^T and
+    d_ts = prod_{r=s+1..t} gate_r: the factor by which the recurrent readout's
+    lifted denominator psi(qh_t)^T z_t (a sum of terms of either sign whose
+    magnitudes add up to at most tr(Z_t)) amplifies rounding.  Large when the
+    query is nearly orthogonal to every key the gates have left alive."""
+    qh = q / np.maximum(np.linalg.norm(q, axis=-1, keepdims=True), 1e-300)
+    kh = k / np.maximum(np.linalg.norm(k, axis=-1, keepdims=True), 1e-300)
+    B, H, T, _ = q.shape
+    kappa = np.empty((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                d = np.array([np.prod(gate[b, h, s + 1:t + 1]) for s in range(t + 1)])
+                den = float(np.sum(d * (kh[b, h, :t + 1] @ qh[b, h, t]) ** 2))
+                kappa[b, h, t] = np.sum(d) / max(den, 1e-300)
+    return kappa
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("p,dv", [(16, 16), (64, 64)])
+def test_gated_decode_steps(dtype, p, dv):
+    """Decode steps against the gated definition, row by row: each row may
+    differ by the dtype's tolerance of the head's largest output plus the
+    fp32 rounding of the lifted denominator amplified by the row's
+    condition kappa_t (gates in [0.5, 1] leave few keys alive, and a query
+    nearly orthogonal to all of them has a denominator of 1e-5 or less)."""
+    B, H, T = 2, 3, 20
+    q, k, v, gate = _case(B, H, T, p, dv, dtype, seed=p * dv)
+    n = p * (p + 1) // 2
+    S, z = torch.zeros(B, H, n, dv, device="cuda"), torch.zeros(B, H, n, device="cuda")
+    rows = [kb.kata_decode_step_gated(q[:, :, t].contiguous(), k[:, :, t].contiguous(), v[:, :, t].contiguous(),
+                                      gate[:, :, t].contiguous(), S, z) for t in range(T)]
+    torch.cuda.synchronize()
+    qq, kk, vv, gg = f64(q), f64(k), f64(v), f64(gate)
+    ref = oracle.forward_plain_gated(qq, kk, vv, gg)
+    got = f64(torch.stack(rows, dim=2))
+    kappa = _readout_condition(qq, kk, gg)
+    scale = np.abs(ref).max(axis=(2, 3), keepdims=True)
+    vmax = np.abs(vv).max(axis=(2, 3), keepdims=True)
+    allowed = TOL[dtype] * scale + 16 * np.finfo(np.float32).eps * kappa[..., None] * vmax
+    assert np.all(np.abs(got - ref) <= allowed), "gated decode rows outside the conditioned bound"
+    # rows whose denominator is well conditioned (kappa within ten times its
+    # typical size p for random directions) meet the plain tolerance
+    good = kappa <= 10 * p
+    assert good.mean() > 0.75
+    d = np.where(good[..., None], np.abs(got - ref), 0.0).max(axis=(2, 3), keepdims=True)
+    assert np.all(d <= TOL[dtype] * scale), "well-conditioned gated decode rows"
+
+
+@pytest.mark.slow
+def test_gated_full_size_sampled_rows():
+    """The 16384-token, 16-head, p = dv = 64 bf16 workload (C = 64) with gates in
+    [0.9, 1], against the oracle's gated definition on sampled rows."""
+    from tests.parity import rows_error, sample_rows
+    w = inputs.WORKLOADS[2]
+    q, k, v = inputs.make(w, "cuda")
+    gate = torch.from_numpy(np.random.default_rng(3).uniform(0.9, 1.0, (w.B, w.H, w.T))).float().cuda()
+    o = kb.kata_forward_chunked_gated(q, k, v, gate, w.C)
+    torch.cuda.synchronize()
+    bh, t = sample_rows(w.B, w.H, w.T, w.C, per_head=6, seed=2)
+    ref = oracle.forward_plain_gated_rows(f64(q), f64(k), f64(v), f64(gate), bh, t)
+    got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
+    assert rows_error(got, ref) <= TOL[torch.bfloat16]

@@ -14,7 +14,7 @@ import torch
 import oracle
 from kernelized_linear_attention_03_b300 import binding as kb
 from kernelized_linear_attention_03_b300 import inputs
-from tests.parity import TOL, assert_close, f64, head_errors, rows_error, sample_rows
+from tests.parity import TOL, assert_close, f64, head_errors, row_errors, rows_error, sample_rows
 
 pytestmark = pytest.mark.gpu
 DTYPES = [torch.float32, torch.bfloat16]
@@ -121,15 +121,28 @@ def test_chunked_empty_sequence_passes_state_through():
     assert torch.count_nonzero(Sf) == 0 and torch.count_nonzero(zf) == 0
 
 
-def test_degenerate_zero_query_and_key():
-    q, k, v = _inputs(1, 1, 80, 16, 16, torch.float32, seed=8)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 64)])
+def test_degenerate_zero_query_and_key(dtype, p, dv):
+    """A zero key drops out of every row (its lift is zero); a zero query
+    row has a zero denominator and is written as 0.  Also a query that is
+    zero at t = 0 and a zero key at a chunk edge.  Both forms, both dtypes
+    (the bf16 forms run on the tensor cores)."""
+    T = 300
+    q, k, v = _inputs(1, 2, T, p, dv, dtype, seed=8 + p)
     q[0, 0, 10] = 0.0
+    q[0, 1, 0] = 0.0
     k[0, 0, 5] = 0.0
+    k[0, 1, 128] = 0.0
+    k[0, 1, 0] = 0.0
     ref = oracle.forward_plain(f64(q), f64(k), f64(v))
-    for o in (kb.kata_forward_quadratic(q, k, v), kb.kata_forward_chunked(q, k, v, 32)):
-        torch.cuda.synchronize()
-        assert torch.count_nonzero(o[0, 0, 10]) == 0
-        assert_close(f64(o), ref, torch.float32, "zero rows")
+    for C in (32, 128):
+        for name, o in (("quadratic", kb.kata_forward_quadratic(q, k, v)), ("chunked", kb.kata_forward_chunked(q, k, v, C))):
+            kb.kata_get_device_status()
+            assert torch.count_nonzero(o[0, 0, 10]) == 0, name
+            assert torch.count_nonzero(o[0, 1, 0]) == 0, name
+            assert np.isfinite(f64(o)).all(), name
+            assert_close(f64(o), ref, dtype, f"zero rows {name}")
 
 
 # ---------------------------------------------------------------- chunk states and scans
@@ -227,33 +240,72 @@ def test_workload_c2_quadratic_and_chunked():
 
 
 def _check_sampled(w, q, k, v, o, what):
+    """Sampled rows (32 per head in the last quarter of T among them) against
+    the plain definition, gated per head and row by row; then the convex
+    output gate at every position, with a slack of the row's own size."""
     bh, t = sample_rows(w.B, w.H, w.T, w.C)
     ref = oracle.forward_plain_rows(f64(q), f64(k), f64(v), bh, t)
     got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
     err = rows_error(got, ref)
     assert err <= TOL[torch.bfloat16], f"{what}: sampled-row error {err:.3e}"
-    # convex output gate at every position: o_t within the hull of v_{<=t}
+    per_row = row_errors(got, ref)
+    worst = int(np.argmax(per_row))
+    print(f"{what}: worst per-row error {per_row[worst]:.3e} at head {bh[worst]} t {t[worst]}; "
+          f"worst over the last quarter {per_row[t >= w.T - w.T // 4].max():.3e}")
+    assert per_row[worst] <= TOL[torch.bfloat16], \
+        f"{what}: row t={t[worst]} of head {bh[worst]} has error {per_row[worst]:.3e}"
+    # convex output gate at every position: o_t within the hull of v_{<=t},
+    # up to the tolerance of the row's own largest output
     vf = v.float()
     lo = torch.cummin(vf, dim=2).values
     hi = torch.cummax(vf, dim=2).values
     of = o.float()
-    slack = 4e-3 * vf.abs().amax()
+    slack = TOL[torch.bfloat16] * of.abs().amax(dim=-1, keepdim=True)
     assert bool(((of >= lo - slack) & (of <= hi + slack)).all()), f"{what}: outside the convex hull"
     return err
 
 
+def _traced(fn):
+    """Run fn() under the library's launch trace; return (result, kernel names)."""
+    kb.kata_trace_start(4096)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        names = [name for name, _ in kb.kata_trace_stop()]
+    return out, names
+
+
 def test_workload_c3_sequential_vs_tree_and_chunk_sizes():
+    """The 16-head workload as one call per head: a single head leaves
+    clusters free, so the forward cuts the sequence into segments whose start
+    states come from the selected inter-chunk prefix (sequential or
+    log-depth).  Both modes are checked against the plain definition, and
+    the launch trace shows that they ran different scan kernels."""
     w, (q, k, v) = _workload(2)
-    o_seq = kb.kata_forward_chunked(q, k, v, w.C, kb.KATA_SCAN_SEQUENTIAL)
-    o_tree = kb.kata_forward_chunked(q, k, v, w.C, kb.KATA_SCAN_TREE)
-    _check_sampled(w, q, k, v, o_seq, "c3 sequential")
-    _check_sampled(w, q, k, v, o_tree, "c3 tree")
-    assert head_errors(f64(o_seq), f64(o_tree)).max() <= TOL[torch.bfloat16]
+    outs, scans = {}, {}
+    for mode in (kb.KATA_SCAN_SEQUENTIAL, kb.KATA_SCAN_TREE):
+        o = torch.empty_like(v)
+
+        def run():
+            for h in range(w.H):
+                kb.kata_forward_chunked(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], w.C, mode, o=o[:, h:h + 1])
+            return o
+
+        _, names = _traced(run)
+        scans[mode] = sorted({n for n in names if n.startswith("scan")})
+        assert any(n.startswith("chunk_states") or n.startswith("states") for n in names), names
+        _check_sampled(w, q, k, v, o, f"c3 per-head mode {mode}")
+        outs[mode] = o
+    assert scans[kb.KATA_SCAN_SEQUENTIAL] and scans[kb.KATA_SCAN_TREE]
+    assert scans[kb.KATA_SCAN_SEQUENTIAL] != scans[kb.KATA_SCAN_TREE], scans
+    o_all = kb.kata_forward_chunked(q, k, v, w.C, kb.KATA_SCAN_TREE)
+    _check_sampled(w, q, k, v, o_all, "c3 all heads")
     for C in (32, 128):
         o_c = kb.kata_forward_chunked(q, k, v, C, kb.KATA_SCAN_TREE)
-        assert head_errors(f64(o_c), f64(o_tree)).max() <= TOL[torch.bfloat16]
+        assert head_errors(f64(o_c), f64(o_all)).max() <= TOL[torch.bfloat16]
     oq = kb.kata_forward_quadratic(q, k, v)
-    assert head_errors(f64(oq), f64(o_tree)).max() <= TOL[torch.bfloat16]
+    _check_sampled(w, q, k, v, oq, "c3 quadratic")
 
 
 def test_workload_c4_headline():

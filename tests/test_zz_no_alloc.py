@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from kernelized_linear_attention_03_b300 import binding as kb
 from kernelized_linear_attention_03_b300 import inputs
 from tests.parity import TOL, f64, head_errors
@@ -40,6 +41,9 @@ def test_noalloc_matches_allocating_forward_on_two_calls(dtype):
         kb.kata_get_device_status()
         err = head_errors(f64(o), f64(ref)).max()
         assert err <= TOL[tdt], f"call {call}: {err:.3e}"
+        # and, on its own, what the plain definition gives
+        err = head_errors(f64(o), oracle.forward_plain(f64(q), f64(k), f64(v))).max()
+        assert err <= TOL[tdt], f"call {call}: against the oracle {err:.3e}"
         for a, b in ((S, S_ref), (z, z_ref)):
             rel = float((a - b).abs().max() / b.abs().max())
             assert rel <= TOL[tdt], f"call {call}: state {rel:.3e}"
