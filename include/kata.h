@@ -103,11 +103,10 @@ KATA_API size_t kata_chunked_workspace_bytes(kata_dtype dtype, int B, int H, int
  *   workspace: device scratch of at least kata_chunked_workspace_bytes(),
  *     256-byte aligned; contents on entry are ignored.  The call owns it
  *     until the stream reaches the end of the call.
- * bf16 inputs: the intra-chunk part runs on a second stream of the current
- * device that the library creates once and owns; it is ordered after the
- * work already queued on `stream` (an event) and joined back into `stream`
- * before the call's last kernel, so the call stays stream-ordered on
- * `stream`.
+ * bf16 inputs run on the tensor cores: a first kernel computes every
+ * chunk's local C x C part and the chunk's transposed unit keys into the
+ * workspace, then one fused kernel carries the running state on chip and
+ * writes the outputs.  Every kernel of the call runs on `stream`.
  * Results do not depend on C or mode beyond fp32 rounding.
  */
 KATA_API kata_status kata_forward_chunked(const void* q, const void* k, const void* v, void* o,

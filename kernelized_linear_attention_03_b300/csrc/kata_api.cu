@@ -116,7 +116,7 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
         off = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * G * n), 256);
     }
     pl.ws.i_off = off;
-    pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, dv), 256);
+    pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, p, dv), 256);
     return pl;
 }
 

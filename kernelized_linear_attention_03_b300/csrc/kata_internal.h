@@ -33,13 +33,12 @@ unsigned int states_tc_take_status();
 // cannot be scheduled there); chunked_tc_segment_chunks() the 128-token
 // chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
 // start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
-// `intra` is chunked_tc_intra_bytes() of device scratch (16-byte aligned)
-// for the intra-chunk rows, their normalisers and the inter-chunk
-// denominators; the intra-chunk kernel runs on a second stream of the device
-// that is joined back into `s` before the combine pass.
+// `intra` is chunked_tc_intra_bytes() of device scratch (256-byte aligned)
+// for the intra-chunk rows, their normalisers and the transposed unit keys,
+// which a first kernel writes and the fused kernel reads.
 int chunked_tc_segments(int p, int dv, int BH, int T);
 int chunked_tc_segment_chunks(int T, int G);
-size_t chunked_tc_intra_bytes(int BH, int T, int dv);
+size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv);
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
                               const float* S_start, const float* z_start, int start_groups, float* S_final,
                               float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s);

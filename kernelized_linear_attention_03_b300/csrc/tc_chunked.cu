@@ -12,19 +12,19 @@
 // Q is used as given (its norm cancels between Y and d); Kh are the unit keys.
 //
 // The state of one head (n x dv fp32, n = p(p+1)/2) is spread over a
-// thread-block cluster.  Each "tile CTA" owns two 128-slot tiles of the
-// packed lift; it keeps its state rows in tensor memory (fp32, accumulated
-// by the update MMA) and a bf16 copy in shared memory (B operand of the
-// readout MMA).  Its query lift goes to tensor memory (A operand of the
-// readout), its key lift to shared memory (A operand of the update).  The
+// thread-block cluster.  Each "tile CTA" owns one or two 128-slot tiles of
+// the packed lift; it keeps its state rows in tensor memory (fp32,
+// accumulated by the update MMA) and a bf16 copy in shared memory (B operand
+// of the readout MMA).  Its query lift goes to tensor memory (A operand of
+// the readout), its key lift to shared memory (A operand of the update,
+// built one slot per thread from the chunk's transposed unit keys).  The
 // "extra CTA" owns the last, partly filled tile and Z (the inter-chunk
 // denominator).  Each CTA's partial Y (128 x dv, sent as bf16) is summed in
 // distributed shared memory: tile CTA r owns rows [r*R, r*R + R) of the
 // chunk, receives the partials of those rows from every CTA of the cluster
-// (a ring of RS chunks) and stores their sum and the rows' inter-chunk
-// denominator.  The intra-chunk part of every chunk is computed by a separate
-// kernel on a second stream, beside the clusters (which leave SMs free); a
-// combine pass then adds it and divides.
+// (a ring of RS chunks), adds the rows' intra-chunk part and writes the
+// outputs.  The intra-chunk part of every chunk, and the transposed unit
+// keys the key lift reads, come from a kernel that runs first.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -48,9 +48,9 @@ namespace cg = cooperative_groups;
 __device__ unsigned int g_chunked_tc_status = 0;
 
 
-constexpr int kThreads = 512;  // warpgroups: lift, state epilogue, readout epilogue, MMA
+constexpr int kThreads = 512;  // warpgroups: query lift and readout, state epilogue, key lift, MMA
 // Register split between the warpgroups after launch (setmaxnreg): the MMA
-// warpgroup gives back registers that the lift and state warpgroups take.
+// warpgroup gives back registers that the query warpgroup takes.
 // 128 * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma) must not exceed
 // 512 * (registers per thread at launch); the launcher checks that.
 constexpr uint32_t kRegsLift = 168, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 88;
@@ -67,22 +67,24 @@ struct Cfg {
     static constexpr int n = lift::packed_n(P);
     static constexpr int NT = n / 128;                 // full tiles
     static constexpr int TAIL = n - 128 * NT;          // slots of the last tile (8, 16 or 32)
-    static constexpr int TPC = NT >= 2 ? 2 : 1;        // tiles per tile CTA
+    static constexpr int TPC = P == 64 ? 2 : 1;        // tiles per tile CTA
     static constexpr int NTC = NT / TPC;               // tile CTAs
     static constexpr int CS = NTC + 1;                 // cluster size
     static constexpr int R = kChunk / NTC;             // output rows owned per tile CTA (the extra CTA owns none)
+    // transposed unit keys of a chunk: two 64-token boxes of P rows x 128 bytes
+    static constexpr uint32_t kt_box = P * 128;
+    static constexpr uint32_t kt_bytes = 2 * kt_box;
     // shared memory, in 16 KB atoms from a 1024-byte aligned base
-    //   tile CTA : key lift [0, 2 TPC), V (slot 0), bf16 state [TPC], query/key staging, V (slot 1)
-    //   extra CTA: tail key lift, unit keys [2], bf16 Z, V (slot 0), bf16 tail state, staging [2], V (slot 1)
-    static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 1) * kAtom,
-                              t_stage = (3 * TPC + 1) * kAtom, t_v2 = (3 * TPC + 3) * kAtom;
-    static constexpr uint32_t x_ak = 0, x_kh = 1 * kAtom, x_z16 = 3 * kAtom, x_v = 4 * kAtom,
-                              x_s16 = 5 * kAtom, x_stage = 6 * kAtom, x_v2 = 10 * kAtom;  // extra: V slots x_v, x_v2,
-                                                                                           // unit-key slots x_kh, x_kh + 1
-    // query / key row staging, (Q tile, K tile) per stage, filled by TMA: one
-    // stage in a tile CTA (its lift warps copy the rows out at once), two in
-    // the extra CTA (its MMAs read the queries in place)
-    static constexpr uint32_t atoms = 11, atoms_tile = 3 * TPC + 4;
+    //   tile CTA : key lift [0, 2 TPC) (two 64-token atoms per tile), V x2,
+    //              bf16 state [TPC], query stage, transposed-key stages x2
+    //   extra CTA: tail key lift [0, 2), V x2, bf16 tail state, bf16 Z,
+    //              query stages x2, transposed-key stages x2, one spare atom
+    //              (the M = 128 reads of the Z update run past the last stage)
+    static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 2) * kAtom,
+                              t_q = (3 * TPC + 2) * kAtom, t_kt = (3 * TPC + 3) * kAtom;
+    static constexpr uint32_t x_ak = 0, x_v = 2 * kAtom, x_s16 = 4 * kAtom, x_z16 = 5 * kAtom, x_q = 6 * kAtom,
+                              x_kt = 8 * kAtom;
+    static constexpr uint32_t atoms_tile = 3 * TPC + 5, atoms_extra = 11;
     // partial readouts received by a tile CTA: one part per (source CTA,
     // receive slot) = R rows of bf16 laid out [DV/8][R] x 16 bytes (a warp's
     // store of one column group is contiguous per owner), then R fp32
@@ -91,13 +93,16 @@ struct Cfg {
     static constexpr uint32_t recv_part = part_y + round16(R * 4);
     static constexpr uint32_t recv_buf = CS * recv_part;
     static constexpr uint32_t recv_off = atoms_tile * kAtom;
-    // receive slots (chunks in flight): three where they fit
-    static constexpr int RS = recv_off + 3 * recv_buf + 1024 + 4096 <= 232448 ? 3 : 2;
-    static constexpr uint32_t total = (recv_off + RS * recv_buf) > atoms * kAtom ? recv_off + RS * recv_buf : atoms * kAtom;
+    // receive slots (chunks in flight): three where they fit beside the
+    // static shared memory
+    static constexpr uint32_t kStaticReserve = 1024 + 3072;
+    static constexpr int RS = recv_off + 3 * recv_buf + kStaticReserve <= 232448 ? 3 : 2;
+    static constexpr uint32_t total =
+        (recv_off + RS * recv_buf) > atoms_extra * kAtom ? recv_off + RS * recv_buf : atoms_extra * kAtom;
     static constexpr size_t smem = total + 1024;
     // tensor memory columns, tile CTA
     static constexpr uint32_t tm_s = 0;      // TPC x 64: fp32 state
-    static constexpr uint32_t tm_aq = 128;   // 2 slots x 128: query lift
+    static constexpr uint32_t tm_aq = 128;   // 2 slots x TPC x 64: query lift
     static constexpr uint32_t tm_y = 384;    // 2 slots x 64: partial readout
     // tensor memory columns, extra CTA
     static constexpr uint32_t tx_s = 0;      // tail state
@@ -107,25 +112,51 @@ struct Cfg {
     static constexpr uint32_t tx_z = 448;    // Z
     static_assert(NT % TPC == 0, "tiles must split evenly");
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
-    static_assert(total + 1024 <= 232448, "shared memory");
-    static_assert(atoms_tile <= atoms, "tile CTA layout");
+    static_assert(total + kStaticReserve <= 232448, "shared memory");
     static_assert(R * NTC == kChunk, "owned rows");
+    static_assert(kt_bytes <= kAtom, "transposed-key stage");
 };
 
-// ---------------------------------------------------------------- lifts per tile
-template <int P, int TAU>
-__device__ __forceinline__ void key_tile(const uint32_t (&u)[P / 2], uint8_t* As, int row) {
+// ---------------------------------------------------------------- key lift, one slot per thread
+// Row `row` of a K-major operand tile (two 64-token atoms of 128 rows x 128
+// bytes, 128-byte swizzle) receives the key lift k_i k_j of internal slot
+// `slot` for the 128 tokens of a chunk, from the chunk's transposed unit keys
+// `kts` (row d = dimension d over the tokens, two 64-token boxes of P rows).
+// Consecutive tokens sit side by side in both, so every 16 bytes of the row
+// are one bf16x2 multiply of two 16-byte loads.  Slots past n give zeros.
+template <int P>
+__device__ __forceinline__ void key_row(const uint8_t* kts, int slot, uint8_t* ak, int row) {
+    constexpr int n = lift::packed_n(P);
+    uint8_t* dst0 = ak + (row >> 3) * 1024 + (row & 7) * 128;
+    if (slot >= n) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint4 val;
-        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
-        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
-        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
-        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
-        *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst0 + h * kAtom + (c << 4)) = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    int i = 0, j = 0;
+    lift::slot_coord(P, slot, i, j);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint8_t* bi = kts + h * (P * 128) + i * 128;
+        const uint8_t* bj = kts + h * (P * 128) + j * 128;
+        uint8_t* dst = dst0 + h * kAtom;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 a = *reinterpret_cast<const uint4*>(bi + ((c ^ (i & 7)) << 4));
+            const uint4 b = *reinterpret_cast<const uint4*>(bj + ((c ^ (j & 7)) << 4));
+            uint4 r;
+            r.x = hmul2_bf16(a.x, b.x);
+            r.y = hmul2_bf16(a.y, b.y);
+            r.z = hmul2_bf16(a.z, b.z);
+            r.w = hmul2_bf16(a.w, b.w);
+            *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) = r;
+        }
     }
 }
 
+// ---------------------------------------------------------------- query lifts per tile
 template <int P, int TAU>
 __device__ __forceinline__ void query_tile(const uint32_t (&u)[P / 2], uint32_t taddr) {
 #pragma unroll
@@ -144,34 +175,6 @@ __device__ __forceinline__ void query_dispatch(int tau, const uint32_t (&uq)[P /
             query_tile<P, TAU>(uq, taddr);
         else
             query_dispatch<P, TAU + 1>(tau, uq, taddr);
-    }
-}
-
-template <int P, int TAU = 0>
-__device__ __forceinline__ void key_dispatch(int tau, const uint32_t (&uk)[P / 2], uint8_t* As, int row) {
-    if constexpr (TAU < lift::tiles_of(P)) {
-        if (tau == TAU)
-            key_tile<P, TAU>(uk, As, row);
-        else
-            key_dispatch<P, TAU + 1>(tau, uk, As, row);
-    }
-}
-
-// Key lift of the last (partly filled) tile into its first 64-slot atom, up
-// to the next multiple of 16 slots (slots past n are written as zeros).
-template <int P>
-__device__ __forceinline__ void key_tail(const uint32_t (&u)[P / 2], uint8_t* As, int row) {
-    constexpr int TAU = lift::tiles_of(P) - 1;
-    constexpr int tail = lift::packed_n(P) - 128 * TAU;
-    constexpr int chunks = 2 * ((tail + 15) / 16);
-#pragma unroll
-    for (int c = 0; c < chunks; ++c) {
-        uint4 val;
-        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
-        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
-        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
-        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
-        *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
     }
 }
 
@@ -276,41 +279,46 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
     }
 }
 
+
 // ---------------------------------------------------------------- kernel
 // Warp roles (512 threads, four warpgroups):
-//   warps 0-3   lift:     thread t = token t of the chunk; reads its staged
-//                         query and key rows, puts the key on the unit sphere,
-//                         writes the query lift (tensor memory) and the key
-//                         lift (shared memory; extra CTA: also the unit keys)
+//   warps 0-3   query:    thread t = token t of the chunk; reads its staged
+//                         query row, writes the query lift (tensor memory,
+//                         the A operand of the readout); then, one chunk
+//                         behind, reads lane t of the partial readout and
+//                         sends the row to the tile CTA that owns it
 //   warps 4-7   state:    thread e = tensor-memory lane e; reads the state
 //                         after each update and releases it to the next update,
 //                         refreshes the bf16 copy for the next readout (extra
 //                         CTA: also Z and the rows' inter-chunk denominators)
-//   warps 8-11  readout:  thread e = lane e; reads the partial readout and
-//                         sends each row to the tile CTA that owns it
+//   warps 8-11  key lift: thread e = slot e of each tile; multiplies two rows
+//                         of the chunk's transposed unit keys into row e of
+//                         the update's A operand (shared memory, K-major)
 //   warps 12-15 warp 12 lane 0 issues every tcgen05.mma, warp 13 lane 0 the
-//                         TMA loads; warps 14-15 reduce the owned rows and
-//                         store their numerators and denominators
-// Per chunk the MMAs run update (state += lift(K)^T V) then readout
-// (Y = lift(Q) S), so the next update starts as soon as the state warps have
-// read the state.
+//                         TMA loads; warps 14-15 reduce the owned rows, add
+//                         the intra-chunk part and store the outputs
+// Per chunk the MMAs run update tile by tile (state += lift(K)^T V; each
+// tile's key-lift rows are released as soon as its MMAs are done, so the
+// next chunk's lift of that tile overlaps the rest) and then the readout
+// (Y = lift(Q) S) of the state before the chunk.
 template <int P, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkt,
                   const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
-                  float* __restrict__ den_out, const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
+                  const __nv_bfloat16* __restrict__ y_intra, const float* __restrict__ d_intra,
+                  const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
                   float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV>;
     constexpr int n = K::n;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t lift_full[2], aq_free[2], y_part[2], y_free[2], den_ready[2], v_free[2];
+    __shared__ uint64_t qs_full[2], qs_free[2], kts_full[2], kts_free[2], v_full[2], v_free[2];
+    __shared__ uint64_t klift_full[2], ak_free[2], qlift_full[2], aq_free[2];
+    __shared__ uint64_t y_part[2], y_free[2], den_ready[2];
+    __shared__ uint64_t upd_done, state_read, s16_ready, drain, rd_sync;
     __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
     __shared__ uint64_t local_full[K::RS];  // this CTA's own partial rows written (one arrival per row)
-    __shared__ float dens[2][kChunk];  // extra CTA: denominators of the chunk rows
-    __shared__ uint64_t ak_free, upd_done, state_read, s16_ready, drain;
-    __shared__ uint64_t rd_sync;  // bounded group barrier of the reduce warps
-    __shared__ uint64_t stage_full[2], stage_free[2], v_full[2], kh_free[2];
+    __shared__ float dens[2][kChunk];       // extra CTA: inter-chunk denominators of the chunk rows
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,44 +336,40 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     // bytes of partial rows (and the extra CTA's denominators) other CTAs
     // deliver per chunk
     const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + my_rows * 4;
-    // shared memory of this CTA's role
+    const int nq = extra ? 2 : 1;  // query stages (the extra CTA's MMAs read the queries in place)
     uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
-    // value buffer of chunk kk (two, so the next chunk's values load while the
-    // update, or in the extra CTA the one-chunk-late intra part, reads these)
-    auto v_buf = [&](int kk) { return sm + ((kk & 1) ? (extra ? K::x_v2 : K::t_v2) : (extra ? K::x_v : K::t_v)); };
-    // staging stages and the stage of chunk kk
-    const int nstg = extra ? 2 : 1;
     uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
-    uint8_t* const s_stage = sm + (extra ? K::x_stage : K::t_stage);
-    auto s_kh = [&](int kk) { return sm + K::x_kh + (kk & 1) * kAtom; };
     uint8_t* const s_z16 = sm + K::x_z16;
     uint8_t* const s_recv = sm + K::recv_off;
+    auto v_buf = [&](int kk) { return sm + (extra ? K::x_v : K::t_v) + (kk & 1) * kAtom; };
+    auto q_buf = [&](int s) { return sm + (extra ? K::x_q : K::t_q) + s * kAtom; };
+    auto kt_buf = [&](int s) { return sm + (extra ? K::x_kt : K::t_kt) + s * kAtom; };
 
     if (t == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&lift_full[b], 128);
+            mbar_init(&qs_full[b], 1);
+            // the staged queries are read by the query warps and, in the extra
+            // CTA, by the state warps (after the Q Z product that reads them too)
+            mbar_init(&qs_free[b], extra ? 256 : 128);
+            mbar_init(&kts_full[b], 1);
+            // the staged keys are read by the key-lift warps and, in the extra
+            // CTA, by the Z update (one commit)
+            mbar_init(&kts_free[b], extra ? 129 : 128);
+            mbar_init(&v_full[b], 1);
+            mbar_init(&v_free[b], 1);
+            mbar_init(&klift_full[b], 128);
+            mbar_init(&ak_free[b], 1);
+            mbar_init(&qlift_full[b], 128);
             mbar_init(&aq_free[b], 1);
             mbar_init(&y_part[b], 1);
             mbar_init(&y_free[b], 128);
-
             mbar_init(&den_ready[b], 128);
-            mbar_init(&v_free[b], 1);
         }
-        mbar_init(&rd_sync, 64);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&stage_full[b], 1);
-            // the staged rows are read by the lift warps and, in the extra CTA,
-            // also by the state warps (its Q operand lives there)
-            mbar_init(&stage_free[b], extra ? 256 : 128);
-            mbar_init(&kh_free[b], 1);
-            mbar_init(&v_full[b], 1);
-        }
-        mbar_init(&ak_free, 1);
         mbar_init(&upd_done, 1);
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
         mbar_init(&drain, 1);
-        fence_mbar_init();
+        mbar_init(&rd_sync, 64);
         for (int b = 0; b < K::RS; ++b) {
             mbar_init(&recv_full[b], 1);
             mbar_init(&peer_free[b], K::NTC);  // one arrival per owner
@@ -381,6 +385,12 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
+    // the extra CTA's tail key lift fills rows [0, 32) of its operand tile;
+    // the other rows are read by the tail update's M = 128 MMAs into state
+    // rows nothing reads, and are kept at zero
+    if (extra)
+        for (int i = t; i < 2 * (int)kAtom / 16; i += kThreads)
+            reinterpret_cast<uint4*>(s_ak)[i] = make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -399,14 +409,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, &abort_flag, kWaitNs));
     };
-    // Group barrier of 128 threads on an mbarrier (bounded, unlike bar.sync):
-    // every thread arrives, then waits for the phase of use number `n`.
-    auto group_sync = [&](uint64_t* bar, uint32_t n) {
-        mbar_arrive(bar);
-        return wait(bar, n & 1);
-    };
 
-    // ---- start state of this segment (epilogue warps: lane = slot / dim)
+    // ---- start state of this segment (state warps: lane = slot / dim)
     if (warp >= 4 && warp < 8) {
         const int e = t - 128;
         const int sg = start_groups > 1 ? g : 0;
@@ -444,24 +448,25 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
         }
         tmem_wait_st();
-        fence_proxy_async_smem();
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     cluster.sync();  // barriers initialised and start state in place cluster-wide
     tc_fence_after();
 
     if (warp < 4) {
-        // =============================================================== lift warps
+        // =============================================================== query warps
         regs_inc<kRegsLift>();
-        for (int kk = 0; kk < nk; ++kk) {
+        const int e = t;
+        const int owner = e / K::R, orow = e % K::R;
+        // query lift of chunk kk into its tensor-memory slot (double-buffered:
+        // overlaps the previous chunk's readout)
+        auto lift_q = [&](int kk) -> bool {
             const int slot = kk & 1, use = kk >> 1;
-            const int stg = kk % nstg, stg_use = kk / nstg;
-            // this token's query and key rows (128-byte swizzled, staged by TMA)
-            if (!wait(&stage_full[stg], stg_use & 1)) { fail(); break; }
-            const uint8_t* my_q = s_stage + stg * 2 * kAtom + t * 128;
-            const uint8_t* my_k = my_q + kAtom;
+            const int stg = kk % nq, stg_use = kk / nq;
+            if (!wait(&qs_full[stg], stg_use & 1)) return false;
+            const uint8_t* my_q = q_buf(stg) + t * 128;
             uint32_t uq[P / 2];
-            uint4 kraw[P / 8];
 #pragma unroll
             for (int i = 0; i < P / 8; ++i) {
                 const uint4 a = *reinterpret_cast<const uint4*>(my_q + ((i ^ (t & 7)) << 4));
@@ -469,34 +474,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 uq[4 * i + 1] = a.y;
                 uq[4 * i + 2] = a.z;
                 uq[4 * i + 3] = a.w;
-                kraw[i] = *reinterpret_cast<const uint4*>(my_k + ((i ^ (t & 7)) << 4));
             }
-            mbar_arrive(&stage_free[stg]);
-            // unit key
-            uint32_t uk[P / 2];
-            {
-                float ss = 0.f;
-#pragma unroll
-                for (int i = 0; i < P / 8; ++i) {
-                    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float x = __bfloat162float(ke[j]);
-                        ss = fmaf(x, x, ss);
-                    }
-                }
-                const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
-#pragma unroll
-                for (int i = 0; i < P / 8; ++i) {
-                    const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kraw[i]);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        uk[4 * i + j] = pack_bf16x2(__bfloat162float(ke[2 * j]) * kinv, __bfloat162float(ke[2 * j + 1]) * kinv);
-                }
-            }
-            // query lift -> tensor memory slot (double-buffered: overlaps the
-            // previous chunk's update)
-            if (kk >= 2 && !wait(&aq_free[slot], (use - 1) & 1)) { fail(); break; }
+            mbar_arrive(&qs_free[stg]);
+            if (kk >= 2 && !wait(&aq_free[slot], (use - 1) & 1)) return false;
             tc_fence_after();
             if (!extra) {
 #pragma unroll
@@ -505,62 +485,94 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             } else {
                 query_tail<P>(uq, tm(K::tx_aq + 32 * slot));
             }
-            // key lift -> shared memory (single buffer)
-            if (kk >= 1 && !wait(&ak_free, (kk - 1) & 1)) { fail(); break; }
-            if (!extra) {
-#pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
-                    key_dispatch<P>(rank * K::TPC + tl, uk, s_ak + 2 * tl * kAtom, t);
-            } else {
-                key_tail<P>(uk, s_ak, t);
-                if (kk >= 2 && !wait(&kh_free[slot], (use - 1) & 1)) { fail(); break; }
-#pragma unroll
-                for (int i = 0; i < P / 8; ++i)
-                    *reinterpret_cast<uint4*>(s_kh(kk) + sw128_chunk(t, 8 * i, kChunk)) =
-                        make_uint4(uk[4 * i], uk[4 * i + 1], uk[4 * i + 2], uk[4 * i + 3]);
-            }
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&lift_full[slot]);
+            mbar_arrive(&qlift_full[slot]);
+            return true;
+        };
+        // this lane's partial readout of chunk c0 + kc -> its owner (the extra
+        // CTA adds the row's inter-chunk denominator)
+        auto send = [&](int kc) -> bool {
+            const int slot = kc & 1, use = kc >> 1;
+            const int rs = kc % K::RS, ruse = kc / K::RS;
+            if (!wait(&y_part[slot], use & 1)) return false;
+            tc_fence_after();
+            float den = 0.f;
+            if (extra) {
+                if (!wait(&den_ready[slot], use & 1)) return false;
+                den = dens[slot][e];
+            }
+            uint32_t ypk[DV / 2];
+            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
+            {
+                uint32_t r[DV / 16][16];  // all loads in flight, one wait
+#pragma unroll
+                for (int c = 0; c < DV / 16; ++c) tmem_ld16(tm(ycol + 16 * c), r[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < DV / 16; ++c)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ypk[8 * c + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
+            }
+            tc_fence_before();
+            mbar_arrive(&y_free[slot]);
+            // the owners have consumed what this receive slot held RS chunks ago
+            if (kc >= K::RS && !wait_cluster(&peer_free[rs], (ruse - 1) & 1)) return false;
+            uint8_t* recv = s_recv + rs * K::recv_buf;
+            uint8_t* dst = recv + rank * K::recv_part + orow * 16;
+            if (owner == rank) {
+#pragma unroll
+                for (int i = 0; i < DV / 8; ++i)
+                    *reinterpret_cast<uint4*>(dst + i * K::R * 16) = make_uint4(ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3]);
+                if (extra) *reinterpret_cast<float*>(recv + rank * K::recv_part + K::part_y + orow * 4) = den;
+                mbar_arrive(&local_full[rs]);
+            } else {
+                const uint32_t rdst = cluster_addr(dst, owner);
+                const uint32_t rbar = cluster_addr(&recv_full[rs], owner);
+#pragma unroll
+                for (int i = 0; i < DV / 8; ++i)
+                    st_async_v4_b32(rdst + i * K::R * 16, ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3], rbar);
+                if (extra) st_async_f32(cluster_addr(recv + rank * K::recv_part + K::part_y + orow * 4, owner), den, rbar);
+            }
+            return true;
+        };
+        for (int kk = 0; kk <= nk; ++kk) {
+            if (kk < nk && !lift_q(kk)) { fail(); break; }
+            if (kk >= 1 && !send(kk - 1)) { fail(); break; }
         }
     } else if (warp < 8) {
         // =============================================================== state warps
         regs_inc<kRegsState>();
         const int e = t - 128;
-        bool ok = true;
-        for (int kk = 0; kk < nk && ok; ++kk) {
+        for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
             // state after this chunk's update
             if (!wait(&upd_done, kk & 1)) { fail(); break; }
             tc_fence_after();
             uint32_t sreg[K::TPC][DV / 2];  // bf16 pairs of this lane's state rows
             uint32_t zreg[P / 2];           // extra CTA: bf16 pairs of this lane's Z row
-            float den = 0.f;
-            if (!extra) {
+            const int ntl = extra ? 1 : K::TPC;
 #pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
+            for (int tl = 0; tl < K::TPC; ++tl) {
+                if (tl >= ntl) break;
+                const uint32_t scol = extra ? K::tx_s : K::tm_s + 64 * tl;
 #pragma unroll
-                    for (int c16 = 0; c16 < DV; c16 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(tm(K::tm_s + 64 * tl + c16), r);
-                        tmem_wait_ld();
+                for (int c32 = 0; c32 < DV; c32 += 32) {
+                    uint32_t r[2][16];  // two loads in flight per wait
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            sreg[tl][c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    }
-                tc_fence_before();
-                mbar_arrive(&state_read);
-            } else {
-#pragma unroll
-                for (int c16 = 0; c16 < DV; c16 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tm(K::tx_s + c16), r);
+                    for (int h = 0; h < 2; ++h)
+                        if (c32 + 16 * h < DV) tmem_ld16(tm(scol + c32 + 16 * h), r[h]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        sreg[0][c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    for (int h = 0; h < 2; ++h)
+                        if (c32 + 16 * h < DV)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                sreg[tl][(c32 + 16 * h) / 2 + i] =
+                                    pack_bf16x2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1]));
                 }
+            }
+            if (extra) {
 #pragma unroll
                 for (int c16 = 0; c16 < P; c16 += 16) {
                     uint32_t r[16];
@@ -570,16 +582,17 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     for (int i = 0; i < 8; ++i)
                         zreg[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                 }
-                tc_fence_before();
-                mbar_arrive(&state_read);
             }
+            tc_fence_before();
+            mbar_arrive(&state_read);
             // this chunk's readout is done: its bf16 state copy may be replaced
             if (!wait(&y_part[slot], use & 1)) { fail(); break; }
             tc_fence_after();
+            float den = 0.f;
             if (extra) {
                 // inter-chunk denominator q^T Z q from W = Q Z (Z before this chunk)
                 uint4 qrow[P / 8];
-                const uint8_t* sq = s_stage + slot * 2 * kAtom;  // this chunk's staged queries
+                const uint8_t* sq = q_buf(kk % nq);  // this chunk's staged queries
 #pragma unroll
                 for (int i = 0; i < P / 8; ++i) qrow[i] = *reinterpret_cast<const uint4*>(sq + sw128_chunk(e, 8 * i, kChunk));
                 const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(qrow);
@@ -592,9 +605,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 16; ++i) dint = fmaf(__bfloat162float(qe[c16 + i]), __uint_as_float(w[i]), dint);
                 }
-                den += dint;
+                den = dint;
                 tc_fence_before();
-                mbar_arrive(&stage_free[slot]);  // this chunk's staged queries and W have been read
+                mbar_arrive(&qs_free[kk % nq]);  // this chunk's staged queries and W have been read
             }
             auto write_s16 = [&](const uint32_t (&x)[DV / 2], int tl) {
 #pragma unroll
@@ -602,17 +615,14 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     *reinterpret_cast<uint4*>(s_s16 + tl * kAtom + mn_sw128_chunk(8 * c8, e, kAtom)) =
                         make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
             };
-            if (!extra) {
 #pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl) write_s16(sreg[tl], tl);
-            } else {
-                write_s16(sreg[0], 0);
-                if (e < P) {
+            for (int tl = 0; tl < K::TPC; ++tl)
+                if (tl < ntl) write_s16(sreg[tl], tl);
+            if (extra && e < P) {
 #pragma unroll
-                    for (int c8 = 0; c8 < P / 8; ++c8)
-                        *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, P)) =
-                            make_uint4(zreg[4 * c8], zreg[4 * c8 + 1], zreg[4 * c8 + 2], zreg[4 * c8 + 3]);
-                }
+                for (int c8 = 0; c8 < P / 8; ++c8)
+                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, P)) =
+                        make_uint4(zreg[4 * c8], zreg[4 * c8 + 1], zreg[4 * c8 + 2], zreg[4 * c8 + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -649,71 +659,57 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
         }
     } else if (warp < 12) {
-        // =============================================================== readout warps
+        // =============================================================== key-lift warps
         const int e = t - 256;
-        const int owner = e / K::R, orow = e % K::R;
-        // this lane's partial readout of chunk c0 + kc -> its owner (the extra
-        // CTA adds the row's inter-chunk denominator)
-        auto send = [&](int kc) -> bool {
-            const int slot = kc & 1, use = kc >> 1;
-            const int rs = kc % K::RS, ruse = kc / K::RS;
-            if (!wait(&y_part[slot], use & 1)) return false;
-            tc_fence_after();
-            float den = 0.f;
-            if (extra) {
-                if (!wait(&den_ready[slot], use & 1)) return false;
-                den = dens[slot][e];
+        for (int kk = 0; kk < nk; ++kk) {
+            const int stg = kk & 1, use = kk >> 1;
+            if (!wait(&kts_full[stg], use & 1)) { fail(); break; }
+            const uint8_t* kts = kt_buf(stg);
+            bool ok = true;
+#pragma unroll
+            for (int tl = 0; tl < K::TPC; ++tl) {
+                if (extra && tl > 0) break;
+                if (kk >= 1 && !wait(&ak_free[tl], (kk - 1) & 1)) { ok = false; break; }
+                if (!extra)
+                    key_row<P>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
+                else if (e < 32)
+                    key_row<P>(kts, K::NT * 128 + e, s_ak, e);
+                fence_proxy_async_smem();
+                mbar_arrive(&klift_full[tl]);
             }
-            uint32_t ypk[DV / 2];
-            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
-#pragma unroll
-            for (int c16 = 0; c16 < DV; c16 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tm(ycol + c16), r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ypk[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            }
-            tc_fence_before();
-            mbar_arrive(&y_free[slot]);
-            // the owners have consumed what this receive slot held RS chunks ago
-            if (kc >= K::RS && !wait_cluster(&peer_free[rs], (ruse - 1) & 1)) return false;
-            uint8_t* recv = s_recv + rs * K::recv_buf;
-            uint8_t* dst = recv + rank * K::recv_part + orow * 16;
-            if (owner == rank) {
-#pragma unroll
-                for (int i = 0; i < DV / 8; ++i)
-                    *reinterpret_cast<uint4*>(dst + i * K::R * 16) = make_uint4(ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3]);
-                if (extra) *reinterpret_cast<float*>(recv + rank * K::recv_part + K::part_y + orow * 4) = den;
-                mbar_arrive(&local_full[rs]);
-            } else {
-                const uint32_t rdst = cluster_addr(dst, owner);
-                const uint32_t rbar = cluster_addr(&recv_full[rs], owner);
-#pragma unroll
-                for (int i = 0; i < DV / 8; ++i)
-                    st_async_v4_b32(rdst + i * K::R * 16, ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3], rbar);
-                if (extra) st_async_f32(cluster_addr(recv + rank * K::recv_part + K::part_y + orow * 4, owner), den, rbar);
-            }
-            return true;
-        };
-        for (int kk = 0; kk < nk; ++kk)
-            if (!send(kk)) { fail(); break; }
+            if (!ok) { fail(); break; }
+            mbar_arrive(&kts_free[stg]);
+        }
     } else {
         regs_dec<kRegsMma>();
     }
     if (warp >= 14 && my_rows > 0) {
         // =============================================================== reduce warps
-        // owner side, chunk by chunk as the partial rows land: sum them, store
-        // the rows' inter-chunk numerator and denominator, then hand the
+        // owner side, chunk by chunk as the partial rows land: sum them, add
+        // the intra-chunk rows, divide and store the outputs, then hand the
         // receive slot back to every sender (its next use is RS chunks later)
         constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
         const int er = t - 448;
         const int r0 = rank * K::R;
         const int items = my_rows * (DV / 8);
-        __nv_bfloat16* oh = o + bh * (int64_t)T * DV;
-        float* dh = den_out + bh * (int64_t)T;
+        const int64_t head_row = bh * (int64_t)T;
         for (int kr = 0; kr < nk; ++kr) {
             const int r = kr % K::RS;
+            // this chunk's intra-chunk rows and normalisers (written before this kernel)
+            uint4 yin[kRedIt];
+            float din[kRedIt];
+#pragma unroll
+            for (int it = 0; it < kRedIt; ++it) {
+                const int idx = er + 64 * it;
+                const int lr = idx % my_rows, i = idx / my_rows;
+                const int otok = (c0 + kr) * kChunk + r0 + lr;
+                yin[it] = make_uint4(0, 0, 0, 0);
+                din[it] = 0.f;
+                if (idx < items && otok < T) {
+                    yin[it] = *reinterpret_cast<const uint4*>(y_intra + (head_row + otok) * DV + 8 * i);
+                    din[it] = d_intra[head_row + otok];
+                }
+            }
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs) &&
                                              mbar_wait(&local_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs))) {
                 fail();
@@ -725,7 +721,15 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 const int idx = er + 64 * it;
                 if (idx >= items) break;
                 const int lr = idx % my_rows, i = idx / my_rows;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float acc[8];
+                {
+                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yin[it]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[2 * j] = __low2float(h[j]);
+                        acc[2 * j + 1] = __high2float(h[j]);
+                    }
+                }
 #pragma unroll
                 for (int src = 0; src < K::CS; ++src) {
                     const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
@@ -738,12 +742,11 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
                 const int otok = (c0 + kr) * kChunk + r0 + lr;
                 if (otok < T) {
-                    // the inter-chunk numerator and denominator of the row; the
-                    // combine pass adds the intra-chunk part and divides
-                    *reinterpret_cast<uint4*>(oh + (int64_t)otok * DV + 8 * i) =
-                        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                                   pack_bf16x2(acc[6], acc[7]));
-                    if (i == 0) dh[otok] = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
+                    const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + din[it];
+                    const float inv = d > 0.f ? 1.f / d : 0.f;
+                    *reinterpret_cast<uint4*>(o + (head_row + otok) * DV + 8 * i) =
+                        make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                                   pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
                 }
             }
             mbar_arrive(&rd_sync);
@@ -758,77 +761,88 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (t == 416) {
         // =============================================================== TMA producer
         tma_prefetch_desc(&tmq);
-        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmkt);
         tma_prefetch_desc(&tmv);
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            const int stg = kk % nstg, stg_use = kk / nstg;
+            const int stg = kk % nq, stg_use = kk / nq;
             const int row = (c0 + kk) * kChunk;
-            // query and key rows of chunk kk into its stage
-            if (kk >= nstg && !mbar_wait(&stage_free[stg], (stg_use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            mbar_arrive_expect_tx(&stage_full[stg], 2 * kAtom);
-            tma_load_3d(s_stage + stg * 2 * kAtom, &tmq, 0, row, (int)bh, &stage_full[stg]);
-            tma_load_3d(s_stage + stg * 2 * kAtom + kAtom, &tmk, 0, row, (int)bh, &stage_full[stg]);
+            // transposed unit keys of chunk kk into its stage
+            if (kk >= 2 && !mbar_wait(&kts_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&kts_full[slot], K::kt_bytes);
+            tma_load_3d(kt_buf(slot), &tmkt, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            tma_load_3d(kt_buf(slot) + K::kt_box, &tmkt, 64, (c0 + kk) * P, (int)bh, &kts_full[slot]);
             // value tile of chunk kk into its buffer
             if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             mbar_arrive_expect_tx(&v_full[slot], kAtom);
             tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[slot]);
+            // query rows of chunk kk into its stage
+            if (kk >= nq && !mbar_wait(&qs_free[stg], (stg_use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&qs_full[stg], kAtom);
+            tma_load_3d(q_buf(stg), &tmq, 0, row, (int)bh, &qs_full[stg]);
         }
     }
     if (t == 384) {
         // =============================================================== MMA issuer
         // Every descriptor is built once: one thread issues all MMAs, so the
-        // issue loop carries no descriptor arithmetic beyond one add per
-        // K step (a step moves the start-address field, in 16-byte units).
+        // issue loop carries no descriptor arithmetic beyond adds of
+        // compile-time offsets (a step moves the start-address field, in
+        // 16-byte units).
         constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
-        constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, true, true);
-        constexpr uint32_t id_z = idesc_bf16_f32_major(128, P, true, true);
+        constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, false, true);
+        constexpr uint32_t id_z = idesc_bf16_f32(128, P);
         constexpr uint32_t id_w = idesc_bf16_f32(128, P);
-        constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kAtomD = kAtom >> 4;
-        // key lift (A of the update): tile CTA two 64-slot atoms per tile; the
-        // extra CTA's tail tile one atom that the second M atom aliases (its
-        // rows past the tail are never read)
-        const uint64_t d_ak = sdesc_mnmajor_sw128(smem_u32(s_ak), extra ? 0u : kAtom);
+        constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kAtomD = kAtom >> 4, kBoxD = K::kt_box >> 4;
+        // K step ks of a K-major operand whose 64-element K atoms are `atom` (16-byte units) apart
+        auto kstep = [](uint64_t atom, int ks) { return (uint64_t)(ks >> 2) * atom + (uint64_t)(ks & 3) * kStepK; };
+        const uint64_t d_ak = sdesc_kmajor_sw128(smem_u32(s_ak));
         const uint64_t d_s16 = sdesc_mnmajor_sw128(smem_u32(s_s16), kAtom);
         const uint64_t d_v[2] = {sdesc_mnmajor_sw128(smem_u32(v_buf(0)), kAtom),
                                  sdesc_mnmajor_sw128(smem_u32(v_buf(1)), kAtom)};
-        // extra CTA: unit keys as M (aliased atoms) and as N; staged Q; Z
-        const uint64_t d_khm[2] = {sdesc_mnmajor_sw128(smem_u32(s_kh(0)), 0), sdesc_mnmajor_sw128(smem_u32(s_kh(1)), 0)};
-        const uint64_t d_khn[2] = {sdesc_mnmajor_sw128(smem_u32(s_kh(0)), kAtom),
-                                   sdesc_mnmajor_sw128(smem_u32(s_kh(1)), kAtom)};
-        const uint64_t d_q[2] = {sdesc_kmajor_sw128(smem_u32(s_stage)), sdesc_kmajor_sw128(smem_u32(s_stage + 2 * kAtom))};
+        // extra CTA: staged transposed keys (both operands of the Z update), staged Q, Z
+        const uint64_t d_kt[2] = {sdesc_kmajor_sw128(smem_u32(kt_buf(0))), sdesc_kmajor_sw128(smem_u32(kt_buf(1)))};
+        const uint64_t d_q[2] = {sdesc_kmajor_sw128(smem_u32(q_buf(0))), sdesc_kmajor_sw128(smem_u32(q_buf(extra ? 1 : 0)))};
         const uint64_t d_z16 = sdesc_kmajor_sw128(smem_u32(s_z16));
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            if (!mbar_wait(&lift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
             if (!mbar_wait(&v_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            tc_fence_after();
             const uint64_t dv = d_v[slot];
-            // ---- group U: state updates (extra CTA: tail state and Z)
+            // ---- group U: state updates, tile by tile (extra CTA: tail state and Z)
+            bool ok = true;
             if (!extra) {
 #pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
+                for (int tl = 0; tl < K::TPC; ++tl) {
+                    if (!mbar_wait(&klift_full[tl], kk & 1, &abort_flag, kWaitNs)) { ok = false; break; }
+                    if (tl == 0 && kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + ks * kStepMN, dv + ks * kStepMN, id_upd, 1u);
+                        mma_ss(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                    mma_commit(&ak_free[tl]);
+                }
+                if (!ok) { fail(); break; }
                 mma_commit(&upd_done);
-                mma_commit(&ak_free);
                 mma_commit(&v_free[slot]);
             } else {
+                if (!mbar_wait(&klift_full[0], kk & 1, &abort_flag, kWaitNs) ||
+                    !mbar_wait(&kts_full[slot], use & 1, &abort_flag, kWaitNs) ||
+                    (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs))) { fail(); break; }
+                tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ss(tb + K::tx_s, d_ak + ks * kStepMN, dv + ks * kStepMN, id_upd, 1u);
+                for (int ks = 0; ks < 8; ++ks) mma_ss(tb + K::tx_s, d_ak + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_z, d_khm[slot] + ks * kStepMN, d_khn[slot] + ks * kStepMN, id_z, 1u);
+                    mma_ss(tb + K::tx_z, d_kt[slot] + kstep(kBoxD, ks), d_kt[slot] + kstep(kBoxD, ks), id_z, 1u);
+                mma_commit(&ak_free[0]);
                 mma_commit(&upd_done);
-                mma_commit(&ak_free);
                 mma_commit(&v_free[slot]);
-                mma_commit(&kh_free[slot]);
+                mma_commit(&kts_free[slot]);
             }
             // ---- group R: readout of the state before this chunk
+            if (!mbar_wait(&qlift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
             if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (extra && !mbar_wait(&qs_full[kk % nq], (kk / nq) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
                 const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 128 * slot;
@@ -838,8 +852,6 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     for (int ks = 0; ks < 8; ++ks)
                         mma_ts(dy, aq + 64 * tl + 8 * ks, d_s16 + tl * kAtomD + ks * kStepMN, id_read,
                                (tl > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(&y_part[slot]);
-                mma_commit(&aq_free[slot]);
             } else {
                 const uint32_t dy = tb + K::tx_y + 64 * slot, aq = tb + K::tx_aq + 32 * slot;
 #pragma unroll
@@ -847,10 +859,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     mma_ts(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < P / 16; ++ks)
-                    mma_ss(tb + K::tx_w, d_q[slot] + ks * kStepK, d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
-                mma_commit(&y_part[slot]);
-                mma_commit(&aq_free[slot]);
+                    mma_ss(tb + K::tx_w, d_q[kk % nq] + ks * kStepK, d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
             }
+            mma_commit(&y_part[slot]);
+            mma_commit(&aq_free[slot]);
         }
         // every issued MMA has completed before tensor memory is released
         mma_commit(&drain);
@@ -864,13 +876,16 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
+
 // ---------------------------------------------------------------- intra-chunk part
 // Every chunk on its own (no state): for the 128 queries of a chunk,
 //   P = (Q Kh^T) o (Q Kh^T) o M   (bf16, M the causal mask s <= t)
 //   Y = P V,  d = rowsum(P)       (fp32 accumulation)
 // Y goes out as bf16 rows [BH][T][DV] and d, the rows' intra-chunk
-// normaliser, as fp32 [BH][T]; the fused forward adds both when it combines
-// a chunk's rows.  d sums exactly the rounded weights Y is built from, which
+// normaliser, as fp32 [BH][T]; the fused forward adds both when it writes a
+// chunk's outputs.  The chunk's unit keys also go out transposed, kT
+// [BH][chunks][P][128] bf16 (zeros past T): the fused forward's key lift
+// reads them.  d sums exactly the rounded weights Y is built from, which
 // keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
 // head), 128 columns of tensor memory and 48 KB of shared memory, so several
 // chunks are in flight per SM; thread t owns query / key / value row t.
@@ -878,7 +893,7 @@ template <int P, int DV>
 __global__ void __launch_bounds__(128)
 intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ y_out, float* __restrict__ d_out,
-                int T) {
+                __nv_bfloat16* __restrict__ kt_out, int T) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar, drain;
     __shared__ uint32_t tmem_base;
@@ -931,6 +946,11 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             w.z = pack_bf16x2(__bfloat162float(ke[4]) * kinv, __bfloat162float(ke[5]) * kinv);
             w.w = pack_bf16x2(__bfloat162float(ke[6]) * kinv, __bfloat162float(ke[7]) * kinv);
             *reinterpret_cast<uint4*>(Ks + sw128_chunk(t, 8 * i, kChunk)) = w;
+            // dimensions 8i .. 8i+7 of this token into the transposed keys
+            const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&w);
+            __nv_bfloat16* kt = kt_out + ((bh * gridDim.x + blockIdx.x) * P + 8 * i) * kChunk + t;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) kt[j * kChunk] = we[j];
         }
 #pragma unroll
         for (int i = 0; i < DV / 8; ++i)
@@ -1025,30 +1045,6 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 }
 
 // o = (numerator + intra rows) / (denominator + intra normaliser), in place
-// over the fused kernel's bf16 numerators; thread = 8 columns of one row.
-template <int DV>
-__global__ void __launch_bounds__(256)
-combine_kernel(__nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ y_intra,
-               const float* __restrict__ d_intra, const float* __restrict__ d_inter, int64_t rows) {
-    const int64_t total = rows * (DV / 8);
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = idx / (DV / 8);
-        const uint4 a = reinterpret_cast<const uint4*>(o)[idx];
-        const uint4 b = reinterpret_cast<const uint4*>(y_intra)[idx];
-        const float d = d_inter[row] + d_intra[row];
-        const float inv = d > 0.f ? 1.f / d : 0.f;
-        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
-        uint4 r;
-        uint32_t* w = reinterpret_cast<uint32_t*>(&r);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = pack_bf16x2((__low2float(ha[j]) + __low2float(hb[j])) * inv,
-                               (__high2float(ha[j]) + __high2float(hb[j])) * inv);
-        reinterpret_cast<uint4*>(o)[idx] = r;
-    }
-}
 
 // ---------------------------------------------------------------- host side
 // The register split of the kernel fits in its launch allocation.
@@ -1099,74 +1095,53 @@ int max_clusters() {
     return cached[dev] > 0 ? cached[dev] : 0;
 }
 
-// A second stream of the current device, and two events, for running the
-// intra-chunk kernel beside the fused kernel (created once per device).
-struct AuxStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-    std::mutex mu;  // held across one call's fork ... join, so calls from several host threads do not interleave
+// Workspace of the forward's intra-chunk kernel: bf16 rows [BH][T][dv],
+// fp32 normalisers [BH][T], transposed unit keys [BH][chunks][p][128] bf16.
+struct IntraWs {
+    size_t y_off, d_off, kt_off, total;
 };
-cudaError_t aux_stream(AuxStream** out) {
-    static AuxStream aux[64];
-    static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(mu);
-    AuxStream& a = aux[dev];
-    if (a.s == nullptr) {
-        if ((e = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-    }
-    *out = &a;
-    return cudaSuccess;
+IntraWs intra_ws(int BH, int T, int p, int dv) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t nch = (size_t)(T + kChunk - 1) / kChunk;
+    IntraWs w;
+    w.y_off = 0;
+    w.d_off = up((size_t)BH * T * dv * 2);
+    w.kt_off = w.d_off + up((size_t)BH * T * 4);
+    w.total = w.kt_off + up((size_t)BH * nch * p * kChunk * 2);
+    return w;
 }
 
 template <int P, int DV>
-cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* y_intra, float* d_intra,
-                         float* d_inter, const float* S_start, const float* z_start, int start_groups,
-                         float* S_final, float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
+cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* intra,
+                         const float* S_start, const float* z_start, int start_groups, float* S_final,
+                         float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
     if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
-    AuxStream* aux = nullptr;
-    cudaError_t e = aux_stream(&aux);
-    if (e != cudaSuccess) return e;
-    // the intra-chunk rows of every chunk, on a second stream: the fused
-    // kernel's clusters leave SMs free, and it does not read these rows
+    const IntraWs w = intra_ws(BH, T, P, DV);
+    auto* y_intra = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(intra) + w.y_off);
+    auto* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + w.d_off);
+    auto* kt = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(intra) + w.kt_off);
+    const int nch = (T + kChunk - 1) / kChunk;
+    // the intra-chunk rows and the transposed unit keys of every chunk first
     constexpr size_t intra_smem = 3 * kAtom + 1024;
-    if ((e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)intra_smem)) != cudaSuccess)
-        return e;
+    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)intra_smem);
+    if (e != cudaSuccess) return e;
+    KATA_TRACED("intra_tc", s,
+                (intra_tc_kernel<P, DV><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                    static_cast<const __nv_bfloat16*>(v), y_intra, d_intra, kt, T)));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     if ((e = configure<P, DV>(cfg, attr, G, BH, s)) != cudaSuccess) return e;
-    CUtensorMap tq, tk, tv;
-    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
+    CUtensorMap tq, tkt, tv;
+    if (!rows_map(&tq, q, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
-    std::lock_guard<std::mutex> lk(aux->mu);
-    if ((e = cudaEventRecord(aux->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(aux->s, aux->fork, 0)) != cudaSuccess)
-        return e;
-    // the fused kernel first, so its clusters are placed before the intra CTAs fill the device
     KATA_TRACED("chunked_tc", s,
-                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tk, tv, static_cast<__nv_bfloat16*>(o),
-                                       d_inter, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
+                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tkt, tv, static_cast<__nv_bfloat16*>(o),
+                                       static_cast<const __nv_bfloat16*>(y_intra), static_cast<const float*>(d_intra),
+                                       S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
     if (e != cudaSuccess) return e;
-    const dim3 igrid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)BH);
-    KATA_TRACED("intra_tc", aux->s,
-                (intra_tc_kernel<P, DV><<<igrid, 128, intra_smem, aux->s>>>(
-                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                    static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(y_intra), d_intra, T)));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(aux->join, aux->s)) != cudaSuccess || (e = cudaStreamWaitEvent(s, aux->join, 0)) != cudaSuccess)
-        return e;
-    const int64_t rows = (int64_t)BH * T;
-    const int64_t work = rows * (DV / 8);
-    const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 148 * 16);
-    KATA_TRACED("combine", s,
-                (combine_kernel<DV><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(o),
-                                                             static_cast<const __nv_bfloat16*>(y_intra), d_intra,
-                                                             d_inter, rows)));
     return cudaGetLastError();
 }
 
@@ -1203,21 +1178,14 @@ int chunked_tc_segment_chunks(int T, int G) {
     return (nch + G - 1) / G;
 }
 
-size_t chunked_tc_intra_bytes(int BH, int T, int dv) {
-    return (size_t)BH * (size_t)T * ((size_t)dv * 2 + 8);
-}
+size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv) { return intra_ws(BH, T, p, dv).total; }
 
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
                               const float* S_start, const float* z_start, int start_groups, float* S_final,
                               float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s) {
     const int seg_chunks = chunked_tc_segment_chunks(T, G);
-    // intra-chunk rows: bf16 [BH][T][dv], then fp32 intra-chunk normalisers
-    // [BH][T], then the fused kernel's inter-chunk denominators [BH][T]
-    void* y_intra = intra;
-    float* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + (size_t)BH * T * dv * 2);
-    float* d_inter = d_intra + (size_t)BH * T;
-    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, y_intra, d_intra, d_inter, S_start, z_start, start_groups,
-                                             S_final, z_final, BH, T, seg_chunks, G, s));
+    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, intra, S_start, z_start, start_groups, S_final, z_final, BH, T,
+                                             seg_chunks, G, s));
     return cudaErrorInvalidValue;
 }
 
@@ -1229,4 +1197,3 @@ unsigned int chunked_tc_take_status() {
 }
 
 }  // namespace kata
-
