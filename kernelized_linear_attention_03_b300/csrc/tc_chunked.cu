@@ -159,13 +159,10 @@ __device__ __forceinline__ void key_row(const uint8_t* kts, int slot, uint8_t* a
 // ---------------------------------------------------------------- query lifts per tile
 template <int P, int TAU>
 __device__ __forceinline__ void query_tile(const uint32_t (&u)[P / 2], uint32_t taddr) {
+    uint32_t w[64];  // the tile's 64 words, stored by one tensor-memory instruction
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = lift::lift_word<P, true>(u, 64 * TAU + c0 + i);
-        tmem_st16(taddr + c0, w);
-    }
+    for (int i = 0; i < 64; ++i) w[i] = lift::lift_word<P, true>(u, 64 * TAU + i);
+    tmem_st64(taddr, w);
 }
 
 template <int P, int TAU = 0>
