@@ -90,6 +90,12 @@ def kernel_work(name, w, form="chunked", lift=None):
         if name == "decode_step_block":
             elem = 4 if w.dtype == "fp32" else 2
             return "byte", w.B * w.H * (2 * n * (w.dv + 1) * 4 + (2 * w.p + 2 * w.dv) * elem)
+        if name == "chunked_tc":
+            # the fused KATA-Sigma-g forward: state build and readout with the normaliser column
+            return "flop", bht * 4 * n * (w.dv + 1)
+        if name == "intra_tc":
+            # the causal local half with block scores
+            return "flop", bht * (w.C + 1) * (pairs * m + w.dv)
         return None, 0
     if name in ("chunk_states_simt",):
         return "flop", bht * 2 * w.n * (w.dv + 1)

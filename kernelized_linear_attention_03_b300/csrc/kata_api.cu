@@ -101,12 +101,16 @@ struct TcPlan {
     ChunkedWs ws{0, 0, 0, 0};
 };
 
-TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv) {
+// lg: blocks of the lift (1: the full lift; g > 1: KATA-Sigma-g, whose state
+// has the width of the lift of one block, p/g).  Block lifts run as one
+// segment per head (the segment totals of the prepass use the full lift).
+TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv, int lg = 1) {
     TcPlan pl;
-    if (dt != KATA_BF16) return pl;
-    const int64_t BH = (int64_t)B * H, n = packed(p);
-    const int G = kata::chunked_tc_segments(p, dv, (int)BH, T);
+    if (dt != KATA_BF16 || !kata::chunked_tc_supports(p, dv, lg)) return pl;
+    const int64_t BH = (int64_t)B * H, n = packed(p / lg);
+    int G = kata::chunked_tc_segments(p, dv, lg, (int)BH, T);
     if (G <= 0) return pl;
+    if (lg > 1) G = 1;
     pl.use = true;
     pl.G = G;
     size_t off = 0;
@@ -238,7 +242,7 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         void* intra = static_cast<char*>(ws) + w.i_off;
         if (pl.G == 1)
             return cuda_status(kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, S_final, z_final, (int)BH, T,
-                                                       p, dv, 1, stream));
+                                                       p, dv, 1, 1, stream));
         // segment totals of segments 0..G-2, then exclusive prefixes seeded
         // with the initial state: the start state of every segment
         const int G = pl.G, n32 = (int)n;
@@ -255,7 +259,7 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
         if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
         if (e == cudaSuccess)
-            e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, G,
+            e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, 1, G,
                                         stream);
         return cuda_status(e);
     }
@@ -335,11 +339,19 @@ int kata_lift_dim(kata_lift_family family, int p, int g) {
     return lift_dim(family, p, g);
 }
 
+// bf16 KATA-Sigma-g forwards run on the tensor cores where the fused kernel
+// has the block width; every other block lift on the CUDA cores.
+TcPlan block_tc_plan(kata_dtype dt, kata_lift_family family, int g, int B, int H, int T, int p, int dv) {
+    if (family != KATA_LIFT_SIGMA || g < 2) return TcPlan{};
+    return tc_plan(dt, B, H, T, p, dv, g);
+}
+
 size_t kata_chunked_block_workspace_bytes(kata_dtype dt, kata_lift_family family, int g, int B, int H, int T, int p,
                                           int dv, int C) {
     if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C) || check_lift(family, p, g) != KATA_OK) return 0;
     if ((int64_t)B * H * T == 0) return 0;
-    return chunked_ws(B, H, T, p, dv, C, lift_dim(family, p, g)).total;
+    const TcPlan pl = block_tc_plan(dt, family, g, B, H, T, p, dv);
+    return pl.use ? pl.ws.total : chunked_ws(B, H, T, p, dv, C, lift_dim(family, p, g)).total;
 }
 
 kata_status kata_forward_chunked_block(const void* q, const void* k, const void* v, void* o, kata_dtype dt, int B,
@@ -371,10 +383,14 @@ kata_status kata_forward_chunked_block(const void* q, const void* k, const void*
     if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
         (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK)
         return st;
-    const ChunkedWs w = chunked_ws(B, H, T, p, dv, C, n);
+    const TcPlan pl = block_tc_plan(dt, family, g, B, H, T, p, dv);
+    const ChunkedWs w = pl.use ? pl.ws : chunked_ws(B, H, T, p, dv, C, n);
     if (ws == nullptr || ws_bytes < w.total) return KATA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
     if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
+    if (pl.use)
+        return cuda_status(kata::launch_chunked_tc(q, k, v, o, static_cast<char*>(ws) + w.i_off, S0, z0, 1, S_final,
+                                                   z_final, (int)BH, T, p, dv, g, 1, stream));
     const int64_t NC = (T + C - 1) / C;
     float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
     float* z_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);

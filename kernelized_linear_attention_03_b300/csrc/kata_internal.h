@@ -36,12 +36,15 @@ unsigned int states_tc_take_status();
 // `intra` is chunked_tc_intra_bytes() of device scratch (256-byte aligned)
 // for the intra-chunk rows, their normalisers and the transposed unit keys,
 // which a first kernel writes and the fused kernel reads.
-int chunked_tc_segments(int p, int dv, int BH, int T);
+// lg: blocks of the lift (1: the full lift; 2 or 4: KATA-Sigma-g with
+// blocks of p / lg); chunked_tc_supports() tells which (p, dv, lg) exist.
+bool chunked_tc_supports(int p, int dv, int lg);
+int chunked_tc_segments(int p, int dv, int lg, int BH, int T);
 int chunked_tc_segment_chunks(int T, int G);
 size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv);
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
                               const float* S_start, const float* z_start, int start_groups, float* S_final,
-                              float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s);
+                              float* z_final, int BH, int T, int p, int dv, int lg, int G, cudaStream_t s);
 unsigned int chunked_tc_take_status();
 
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).

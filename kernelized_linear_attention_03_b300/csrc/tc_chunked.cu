@@ -62,12 +62,15 @@ constexpr float kInvSqrt2f = 0.70710678118654752440f;
 
 __host__ __device__ constexpr uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
 
-template <int P, int DV>
+// P: width of q and k; LG: blocks of the lift (1: the full lift; g > 1: the
+// KATA-Sigma-g lift, the sum of the g block lifts of width M = P / g).
+template <int P, int DV, int LG>
 struct Cfg {
-    static constexpr int n = lift::packed_n(P);
+    static constexpr int M = P / LG;                   // width of the lifted blocks
+    static constexpr int n = lift::packed_n(M);
     static constexpr int NT = n / 128;                 // full tiles
     static constexpr int TAIL = n - 128 * NT;          // slots of the last tile (8, 16 or 32)
-    static constexpr int TPC = P == 64 ? 2 : 1;        // tiles per tile CTA
+    static constexpr int TPC = M == 64 ? 2 : 1;        // tiles per tile CTA
     static constexpr int NTC = NT / TPC;               // tile CTAs
     static constexpr int CS = NTC + 1;                 // cluster size
     static constexpr int R = kChunk / NTC;             // output rows owned per tile CTA (the extra CTA owns none)
@@ -119,14 +122,17 @@ struct Cfg {
 
 // ---------------------------------------------------------------- key lift, one slot per thread
 // Row `row` of a K-major operand tile (two 64-token atoms of 128 rows x 128
-// bytes, 128-byte swizzle) receives the key lift k_i k_j of internal slot
-// `slot` for the 128 tokens of a chunk, from the chunk's transposed unit keys
-// `kts` (row d = dimension d over the tokens, two 64-token boxes of P rows).
-// Consecutive tokens sit side by side in both, so every 16 bytes of the row
-// are one bf16x2 multiply of two 16-byte loads.  Slots past n give zeros.
-template <int P>
+// bytes, 128-byte swizzle) receives the key lift of internal slot `slot` for
+// the 128 tokens of a chunk, from the chunk's transposed unit keys `kts` (row
+// d = dimension d over the tokens, two 64-token boxes of P rows): k_i k_j for
+// the full lift, sum_a k_{aM+i} k_{aM+j} over the LG blocks of width M for
+// KATA-Sigma-g.  Consecutive tokens sit side by side in both, so every 16
+// bytes of the row are bf16x2 multiplies of 16-byte loads.  Slots past n
+// give zeros.
+template <int P, int LG>
 __device__ __forceinline__ void key_row(const uint8_t* kts, int slot, uint8_t* ak, int row) {
-    constexpr int n = lift::packed_n(P);
+    constexpr int M = P / LG;
+    constexpr int n = lift::packed_n(M);
     uint8_t* dst0 = ak + (row >> 3) * 1024 + (row & 7) * 128;
     if (slot >= n) {
 #pragma unroll
@@ -136,52 +142,72 @@ __device__ __forceinline__ void key_row(const uint8_t* kts, int slot, uint8_t* a
         return;
     }
     int i = 0, j = 0;
-    lift::slot_coord(P, slot, i, j);
+    lift::slot_coord(M, slot, i, j);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const uint8_t* bi = kts + h * (P * 128) + i * 128;
-        const uint8_t* bj = kts + h * (P * 128) + j * 128;
         uint8_t* dst = dst0 + h * kAtom;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 a = *reinterpret_cast<const uint4*>(bi + ((c ^ (i & 7)) << 4));
-            const uint4 b = *reinterpret_cast<const uint4*>(bj + ((c ^ (j & 7)) << 4));
             uint4 r;
-            r.x = hmul2_bf16(a.x, b.x);
-            r.y = hmul2_bf16(a.y, b.y);
-            r.z = hmul2_bf16(a.z, b.z);
-            r.w = hmul2_bf16(a.w, b.w);
+#pragma unroll
+            for (int blk = 0; blk < LG; ++blk) {
+                const int bi = blk * M + i, bj = blk * M + j;  // rows of this block's two factors
+                const uint4 a = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bi * 128 + ((c ^ (bi & 7)) << 4));
+                const uint4 b = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bj * 128 + ((c ^ (bj & 7)) << 4));
+                if (blk == 0) {
+                    r.x = hmul2_bf16(a.x, b.x);
+                    r.y = hmul2_bf16(a.y, b.y);
+                    r.z = hmul2_bf16(a.z, b.z);
+                    r.w = hmul2_bf16(a.w, b.w);
+                } else {
+                    r.x = hfma2_bf16(a.x, b.x, r.x);
+                    r.y = hfma2_bf16(a.y, b.y, r.y);
+                    r.z = hfma2_bf16(a.z, b.z, r.z);
+                    r.w = hfma2_bf16(a.w, b.w, r.w);
+                }
+            }
             *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) = r;
         }
     }
 }
 
 // ---------------------------------------------------------------- query lifts per tile
-template <int P, int TAU>
+// Query lift word w (slots 2w, 2w+1 of the lift of width M): for KATA-Sigma-g
+// the sum of the LG block lifts (bf16x2 additions).
+template <int P, int LG>
+__device__ __forceinline__ uint32_t query_word(const uint32_t (&u)[P / 2], int w) {
+    constexpr int M = P / LG;
+    uint32_t x = lift::lift_word<M, true>(u, w);
+#pragma unroll
+    for (int blk = 1; blk < LG; ++blk) x = hadd2_bf16(x, lift::lift_word<M, true>(u + blk * (M / 2), w));
+    return x;
+}
+
+template <int P, int LG, int TAU>
 __device__ __forceinline__ void query_tile(const uint32_t (&u)[P / 2], uint32_t taddr) {
     uint32_t w[64];  // the tile's 64 words, stored by one tensor-memory instruction
 #pragma unroll
-    for (int i = 0; i < 64; ++i) w[i] = lift::lift_word<P, true>(u, 64 * TAU + i);
+    for (int i = 0; i < 64; ++i) w[i] = query_word<P, LG>(u, 64 * TAU + i);
     tmem_st64(taddr, w);
 }
 
-template <int P, int TAU = 0>
+template <int P, int LG, int TAU = 0>
 __device__ __forceinline__ void query_dispatch(int tau, const uint32_t (&uq)[P / 2], uint32_t taddr) {
-    if constexpr (TAU < lift::tiles_of(P)) {
+    if constexpr (TAU < lift::tiles_of(P / LG)) {
         if (tau == TAU)
-            query_tile<P, TAU>(uq, taddr);
+            query_tile<P, LG, TAU>(uq, taddr);
         else
-            query_dispatch<P, TAU + 1>(tau, uq, taddr);
+            query_dispatch<P, LG, TAU + 1>(tau, uq, taddr);
     }
 }
 
 // Query lift of the last (partly filled) tile: its first 16 words (32 slots).
-template <int P>
+template <int P, int LG>
 __device__ __forceinline__ void query_tail(const uint32_t (&uq)[P / 2], uint32_t taddr) {
-    constexpr int TAU = lift::tiles_of(P) - 1;
+    constexpr int TAU = lift::tiles_of(P / LG) - 1;
     uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = lift::lift_word<P, true>(uq, 64 * TAU + i);
+    for (int i = 0; i < 16; ++i) w[i] = query_word<P, LG>(uq, 64 * TAU + i);
     tmem_st16(taddr, w);
 }
 
@@ -298,15 +324,15 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 // tile's key-lift rows are released as soon as its MMAs are done, so the
 // next chunk's lift of that tile overlaps the rest) and then the readout
 // (Y = lift(Q) S) of the state before the chunk.
-template <int P, int DV>
+template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkt,
                   const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
                   const __nv_bfloat16* __restrict__ y_intra, const float* __restrict__ d_intra,
                   const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
                   float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
-    using K = Cfg<P, DV>;
-    constexpr int n = K::n;
+    using K = Cfg<P, DV, LG>;
+    constexpr int n = K::n, M = K::M;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qs_full[2], qs_free[2], kts_full[2], kts_free[2], v_full[2], v_free[2];
@@ -416,30 +442,30 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         if (!extra) {
 #pragma unroll
             for (int tl = 0; tl < K::TPC; ++tl)
-                load_state_tile<P, DV>(S0, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), s_s16 + tl * kAtom, e);
+                load_state_tile<M, DV>(S0, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), s_s16 + tl * kAtom, e);
         } else {
-            load_state_tile<P, DV>(S0, K::NT, tm(K::tx_s), s_s16, e);
-            float zr[P];
+            load_state_tile<M, DV>(S0, K::NT, tm(K::tx_s), s_s16, e);
+            float zr[M];
 #pragma unroll
-            for (int j = 0; j < P; ++j) {
+            for (int j = 0; j < M; ++j) {
                 float val = 0.f;
-                if (z0 != nullptr && e < P) {
+                if (z0 != nullptr && e < M) {
                     const int a = e < j ? e : j, b = e < j ? j : e;
-                    val = z0[lift::canonical_index(P, a, b)] * (a == b ? 1.f : kInvSqrt2f);
+                    val = z0[lift::canonical_index(M, a, b)] * (a == b ? 1.f : kInvSqrt2f);
                 }
                 zr[j] = val;
             }
 #pragma unroll
-            for (int c = 0; c < P; c += 16) {
+            for (int c = 0; c < M; c += 16) {
                 uint32_t r[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(zr[c + i]);
                 tmem_st16(tm(K::tx_z + c), r);
             }
-            if (e < P) {
+            if (e < M) {
 #pragma unroll
-                for (int c = 0; c < P / 8; ++c)
-                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c, P)) =
+                for (int c = 0; c < M / 8; ++c)
+                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c, M)) =
                         make_uint4(pack_bf16x2(zr[8 * c], zr[8 * c + 1]), pack_bf16x2(zr[8 * c + 2], zr[8 * c + 3]),
                                    pack_bf16x2(zr[8 * c + 4], zr[8 * c + 5]), pack_bf16x2(zr[8 * c + 6], zr[8 * c + 7]));
             }
@@ -478,9 +504,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (!extra) {
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
-                    query_dispatch<P>(rank * K::TPC + tl, uq, tm(K::tm_aq + 128 * slot + 64 * tl));
+                    query_dispatch<P, LG>(rank * K::TPC + tl, uq, tm(K::tm_aq + 128 * slot + 64 * tl));
             } else {
-                query_tail<P>(uq, tm(K::tx_aq + 32 * slot));
+                query_tail<P, LG>(uq, tm(K::tx_aq + 32 * slot));
             }
             tmem_wait_st();
             tc_fence_before();
@@ -547,7 +573,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (!wait(&upd_done, kk & 1)) { fail(); break; }
             tc_fence_after();
             uint32_t sreg[K::TPC][DV / 2];  // bf16 pairs of this lane's state rows
-            uint32_t zreg[P / 2];           // extra CTA: bf16 pairs of this lane's Z row
+            uint32_t zreg[M / 2];           // extra CTA: bf16 pairs of this lane's Z row
             const int ntl = extra ? 1 : K::TPC;
 #pragma unroll
             for (int tl = 0; tl < K::TPC; ++tl) {
@@ -571,7 +597,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
             if (extra) {
 #pragma unroll
-                for (int c16 = 0; c16 < P; c16 += 16) {
+                for (int c16 = 0; c16 < M; c16 += 16) {
                     uint32_t r[16];
                     tmem_ld16(tm(K::tx_z + c16), r);
                     tmem_wait_ld();
@@ -615,10 +641,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
             for (int tl = 0; tl < K::TPC; ++tl)
                 if (tl < ntl) write_s16(sreg[tl], tl);
-            if (extra && e < P) {
+            if (extra && e < M) {
 #pragma unroll
-                for (int c8 = 0; c8 < P / 8; ++c8)
-                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, P)) =
+                for (int c8 = 0; c8 < M / 8; ++c8)
+                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, M)) =
                         make_uint4(zreg[4 * c8], zreg[4 * c8 + 1], zreg[4 * c8 + 2], zreg[4 * c8 + 3]);
             }
             fence_proxy_async_smem();
@@ -635,23 +661,23 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (!extra) {
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
-                    store_state_tile<P, DV>(S_final + head_s, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), e);
+                    store_state_tile<M, DV>(S_final + head_s, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), e);
             } else {
-                store_state_tile<P, DV>(S_final + head_s, K::NT, tm(K::tx_s), e);
-                uint32_t zr[P];
+                store_state_tile<M, DV>(S_final + head_s, K::NT, tm(K::tx_s), e);
+                uint32_t zr[M];
 #pragma unroll
-                for (int c16 = 0; c16 < P; c16 += 16) {
+                for (int c16 = 0; c16 < M; c16 += 16) {
                     uint32_t r[16];
                     tmem_ld16(tm(K::tx_z + c16), r);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) zr[c16 + i] = r[i];
                 }
                 tmem_wait_ld();
-                if (e < P) {
+                if (e < M) {
 #pragma unroll
-                    for (int j = 0; j < P; ++j)
+                    for (int j = 0; j < M; ++j)
                         if (j >= e)
-                            z_final[head_z + lift::canonical_index(P, e, j)] = __uint_as_float(zr[j]) * (j == e ? 1.f : kSqrt2f);
+                            z_final[head_z + lift::canonical_index(M, e, j)] = __uint_as_float(zr[j]) * (j == e ? 1.f : kSqrt2f);
                 }
             }
         }
@@ -668,9 +694,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 if (extra && tl > 0) break;
                 if (kk >= 1 && !wait(&ak_free[tl], (kk - 1) & 1)) { ok = false; break; }
                 if (!extra)
-                    key_row<P>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
+                    key_row<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
                 else if (e < 32)
-                    key_row<P>(kts, K::NT * 128 + e, s_ak, e);
+                    key_row<P, LG>(kts, K::NT * 128 + e, s_ak, e);
                 fence_proxy_async_smem();
                 mbar_arrive(&klift_full[tl]);
             }
@@ -787,8 +813,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         // 16-byte units).
         constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
         constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, false, true);
-        constexpr uint32_t id_z = idesc_bf16_f32(128, P);
-        constexpr uint32_t id_w = idesc_bf16_f32(128, P);
+        constexpr uint32_t id_z = idesc_bf16_f32(128, M);
+        constexpr uint32_t id_w = idesc_bf16_f32(128, M);
         constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kAtomD = kAtom >> 4, kBoxD = K::kt_box >> 4;
         // K step ks of a K-major operand whose 64-element K atoms are `atom` (16-byte units) apart
         auto kstep = [](uint64_t atom, int ks) { return (uint64_t)(ks >> 2) * atom + (uint64_t)(ks & 3) * kStepK; };
@@ -827,9 +853,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma_ss(tb + K::tx_s, d_ak + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                // Z += sum over the blocks of (rows of the block)^T (rows of the block)
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tb + K::tx_z, d_kt[slot] + kstep(kBoxD, ks), d_kt[slot] + kstep(kBoxD, ks), id_z, 1u);
+                for (int blk = 0; blk < LG; ++blk)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ss(tb + K::tx_z, d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks),
+                               d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks), id_z, 1u);
                 mma_commit(&ak_free[0]);
                 mma_commit(&upd_done);
                 mma_commit(&v_free[slot]);
@@ -854,9 +884,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
                 for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
                     mma_ts(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
+                // W = [Q_0 Z | Q_1 Z | ...], one block of columns per block of the queries
 #pragma unroll
-                for (int ks = 0; ks < P / 16; ++ks)
-                    mma_ss(tb + K::tx_w, d_q[kk % nq] + ks * kStepK, d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
+                for (int blk = 0; blk < LG; ++blk)
+#pragma unroll
+                    for (int ks = 0; ks < M / 16; ++ks)
+                        mma_ss(tb + K::tx_w + blk * M, d_q[kk % nq] + (blk * (M / 16) + ks) * kStepK,
+                               d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
             }
             mma_commit(&y_part[slot]);
             mma_commit(&aq_free[slot]);
@@ -886,7 +920,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 // keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
 // head), 128 columns of tensor memory and 48 KB of shared memory, so several
 // chunks are in flight per SM; thread t owns query / key / value row t.
-template <int P, int DV>
+template <int P, int DV, int LG>
 __global__ void __launch_bounds__(128)
 intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ y_out, float* __restrict__ d_out,
@@ -959,45 +993,106 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     tc_fence_after();
     const uint32_t tb = tmem_base;
     const uint32_t lane0 = (uint32_t)(warp * 32);
-    if (t == 0) {
-        const uint64_t dq = sdesc_kmajor_sw128(smem_u32(Qs)), dk = sdesc_kmajor_sw128(smem_u32(Ks));
-        constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
-#pragma unroll
-        for (int ks = 0; ks < P / 16; ++ks) mma_ss(tb, dq + 2 * ks, dk + 2 * ks, id_sc, ks > 0 ? 1u : 0u);
-        mma_commit(&bar);
-    }
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, kWaitNs));
-    if (!ok) abort_flag = 1;
-    tc_fence_after();
     // P = scores^2 masked, bf16, in place (columns 0..63), and its row sum;
-    // quarters past this warp's rows are all masked
+    // quarters past this warp's rows are all masked.  Full lift: the scores
+    // are (q . kh)^2.  KATA-Sigma-g: sum over the block pairs (a, b) of
+    // (q_a . kh_b)^2, one product per pair into columns 0..127, whose squares
+    // are summed in registers.
     float den = 0.f;
-    if (ok) {
+    bool ok = true;
+    const uint64_t dq = sdesc_kmajor_sw128(smem_u32(Qs)), dk = sdesc_kmajor_sw128(smem_u32(Ks));
+    constexpr uint32_t id_sc = idesc_bf16_f32(128, 128);
+    if constexpr (LG == 1) {
+        // scores (q . kh); P = scores^2
+        if (t == 0) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t pk[16];
-            if (q4 <= warp) {
-                uint32_t sc[32];
-                tmem_ld16(tmem_addr(tb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
-                tmem_ld16(tmem_addr(tb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
-                tmem_wait_ld();
+            for (int ks = 0; ks < P / 16; ++ks) mma_ss(tb, dq + 2 * ks, dk + 2 * ks, id_sc, ks > 0 ? 1u : 0u);
+            mma_commit(&bar);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, kWaitNs));
+        if (!ok) abort_flag = 1;
+        tc_fence_after();
+        if (ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
+                if (q4 <= warp) {
+                    uint32_t sc[32];
+                    tmem_ld16(tmem_addr(tb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                    tmem_ld16(tmem_addr(tb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int col = 32 * q4 + 2 * i;
+                        float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
+                        a = col <= t ? a * a : 0.f;
+                        b = col + 1 <= t ? b * b : 0.f;
+                        pk[i] = pack_bf16x2(a, b);
+                        const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+                        den += __low2float(hp) + __high2float(hp);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                }
+                tmem_st16(tmem_addr(tb, lane0, 16 * q4), pk);
+            }
+            tmem_wait_st();
+        }
+    } else {
+        constexpr int M = P / LG;
+        float acc[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+        // every thread runs every iteration (the block barrier below is reached
+        // by all of them even after a wait gave up)
+        for (int pr = 0; pr < LG * LG; ++pr) {
+            const int a = pr / LG, b = pr % LG;
+            if (t == 0 && ok) {
+#pragma unroll
+                for (int ks = 0; ks < M / 16; ++ks)
+                    mma_ss(tb, dq + 2 * (a * (M / 16) + ks), dk + 2 * (b * (M / 16) + ks), id_sc, ks > 0 ? 1u : 0u);
+                mma_commit(&bar);
+            }
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar, pr & 1, &abort_flag, kWaitNs));
+            if (!ok) abort_flag = 1;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                if (ok && q4 <= warp) {
+                    uint32_t sc[32];
+                    tmem_ld16(tmem_addr(tb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                    tmem_ld16(tmem_addr(tb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = __uint_as_float(sc[i]);
+                        acc[32 * q4 + i] = fmaf(x, x, acc[32 * q4 + i]);
+                    }
+                }
+            }
+            // every lane has read this pair's scores before the next pair overwrites them
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+        if (ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int col = 32 * q4 + 2 * i;
-                    float a = __uint_as_float(sc[2 * i]), b = __uint_as_float(sc[2 * i + 1]);
-                    a = col <= t ? a * a : 0.f;
-                    b = col + 1 <= t ? b * b : 0.f;
-                    pk[i] = pack_bf16x2(a, b);
+                    const float x0 = (q4 <= warp && col <= t) ? acc[col] : 0.f;
+                    const float x1 = (q4 <= warp && col + 1 <= t) ? acc[col + 1] : 0.f;
+                    pk[i] = pack_bf16x2(x0, x1);
                     const __nv_bfloat162 hp = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
                     den += __low2float(hp) + __high2float(hp);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                tmem_st16(tmem_addr(tb, lane0, 16 * q4), pk);
             }
-            tmem_st16(tmem_addr(tb, lane0, 16 * q4), pk);
+            tmem_wait_st();
         }
-        tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
@@ -1010,7 +1105,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         for (int ks = 0; ks < 8; ++ks) mma_ts(tb + 64, tb + 8 * ks, dv + ks * (2048 >> 4), id_pv, ks > 0 ? 1u : 0u);
         mma_commit(&bar);
     }
-    ok = !abort_flag && __all_sync(0xffffffffu, mbar_wait(&bar, 1, &abort_flag, kWaitNs));
+    ok = !abort_flag && __all_sync(0xffffffffu, mbar_wait(&bar, (LG * LG) & 1, &abort_flag, kWaitNs));
     tc_fence_after();
     if (ok) {
         uint32_t y[DV];
@@ -1045,17 +1140,17 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 
 // ---------------------------------------------------------------- host side
 // The register split of the kernel fits in its launch allocation.
-template <int P, int DV>
+template <int P, int DV, int LG>
 bool register_split_fits() {
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, chunked_tc_kernel<P, DV>) != cudaSuccess) return false;
+    if (cudaFuncGetAttributes(&fa, chunked_tc_kernel<P, DV, LG>) != cudaSuccess) return false;
     return (uint32_t)kThreads * (uint32_t)fa.numRegs >= 128u * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma);
 }
 
-template <int P, int DV>
+template <int P, int DV, int LG>
 cudaError_t configure(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int G, int BH, cudaStream_t s) {
-    using K = Cfg<P, DV>;
-    auto kern = chunked_tc_kernel<P, DV>;
+    using K = Cfg<P, DV, LG>;
+    auto kern = chunked_tc_kernel<P, DV, LG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
     if (e == cudaSuccess && K::CS > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -1073,7 +1168,7 @@ cudaError_t configure(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int G,
     return cudaSuccess;
 }
 
-template <int P, int DV>
+template <int P, int DV, int LG>
 int max_clusters() {
     static int cached[64] = {};
     int dev = 0;
@@ -1082,8 +1177,8 @@ int max_clusters() {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
         int m = 0;
-        if (!register_split_fits<P, DV>() || configure<P, DV>(cfg, attr, 1, 1, 0) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&m, chunked_tc_kernel<P, DV>, &cfg) != cudaSuccess) {
+        if (!register_split_fits<P, DV, LG>() || configure<P, DV, LG>(cfg, attr, 1, 1, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&m, chunked_tc_kernel<P, DV, LG>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
@@ -1108,11 +1203,11 @@ IntraWs intra_ws(int BH, int T, int p, int dv) {
     return w;
 }
 
-template <int P, int DV>
+template <int P, int DV, int LG>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* intra,
                          const float* S_start, const float* z_start, int start_groups, float* S_final,
                          float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
-    if (!register_split_fits<P, DV>()) return cudaErrorInvalidConfiguration;
+    if (!register_split_fits<P, DV, LG>()) return cudaErrorInvalidConfiguration;
     const IntraWs w = intra_ws(BH, T, P, DV);
     auto* y_intra = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(intra) + w.y_off);
     auto* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + w.d_off);
@@ -1120,22 +1215,22 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
     const int nch = (T + kChunk - 1) / kChunk;
     // the intra-chunk rows and the transposed unit keys of every chunk first
     constexpr size_t intra_smem = 3 * kAtom + 1024;
-    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)intra_smem);
     if (e != cudaSuccess) return e;
     KATA_TRACED("intra_tc", s,
-                (intra_tc_kernel<P, DV><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
+                (intra_tc_kernel<P, DV, LG><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                     static_cast<const __nv_bfloat16*>(v), y_intra, d_intra, kt, T)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    if ((e = configure<P, DV>(cfg, attr, G, BH, s)) != cudaSuccess) return e;
+    if ((e = configure<P, DV, LG>(cfg, attr, G, BH, s)) != cudaSuccess) return e;
     CUtensorMap tq, tkt, tv;
     if (!rows_map(&tq, q, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
     KATA_TRACED("chunked_tc", s,
-                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV>, tq, tkt, tv, static_cast<__nv_bfloat16*>(o),
+                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV, LG>, tq, tkt, tv, static_cast<__nv_bfloat16*>(o),
                                        static_cast<const __nv_bfloat16*>(y_intra), static_cast<const float*>(d_intra),
                                        S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
     if (e != cudaSuccess) return e;
@@ -1144,23 +1239,35 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
 
 }  // namespace
 
-#define KATA_DISPATCH(...)                                              \
-    do {                                                                 \
-        if (p == 16 && dv == 16) { constexpr int P = 16, DV = 16; __VA_ARGS__; } \
-        if (p == 16 && dv == 32) { constexpr int P = 16, DV = 32; __VA_ARGS__; } \
-        if (p == 16 && dv == 64) { constexpr int P = 16, DV = 64; __VA_ARGS__; } \
-        if (p == 32 && dv == 16) { constexpr int P = 32, DV = 16; __VA_ARGS__; } \
-        if (p == 32 && dv == 32) { constexpr int P = 32, DV = 32; __VA_ARGS__; } \
-        if (p == 32 && dv == 64) { constexpr int P = 32, DV = 64; __VA_ARGS__; } \
-        if (p == 64 && dv == 16) { constexpr int P = 64, DV = 16; __VA_ARGS__; } \
-        if (p == 64 && dv == 32) { constexpr int P = 64, DV = 32; __VA_ARGS__; } \
-        if (p == 64 && dv == 64) { constexpr int P = 64, DV = 64; __VA_ARGS__; } \
+// (p, dv, lift blocks): the full lift (1 block) at p = 16, 32, 64 and the
+// KATA-Sigma-g lift with blocks of 16 or 32 (p = 32 with g = 2; p = 64 with
+// g = 2 or 4).
+#define KATA_DISPATCH_DV(P_, LG_, ...)                                                   \
+    do {                                                                                 \
+        if (dv == 16) { constexpr int P = P_, DV = 16, LG = LG_; __VA_ARGS__; }          \
+        if (dv == 32) { constexpr int P = P_, DV = 32, LG = LG_; __VA_ARGS__; }          \
+        if (dv == 64) { constexpr int P = P_, DV = 64, LG = LG_; __VA_ARGS__; }          \
+    } while (0)
+#define KATA_DISPATCH(...)                                                   \
+    do {                                                                     \
+        if (p == 16 && lg == 1) KATA_DISPATCH_DV(16, 1, __VA_ARGS__);        \
+        if (p == 32 && lg == 1) KATA_DISPATCH_DV(32, 1, __VA_ARGS__);        \
+        if (p == 64 && lg == 1) KATA_DISPATCH_DV(64, 1, __VA_ARGS__);        \
+        if (p == 32 && lg == 2) KATA_DISPATCH_DV(32, 2, __VA_ARGS__);        \
+        if (p == 64 && lg == 2) KATA_DISPATCH_DV(64, 2, __VA_ARGS__);        \
+        if (p == 64 && lg == 4) KATA_DISPATCH_DV(64, 4, __VA_ARGS__);        \
     } while (0)
 
-int chunked_tc_segments(int p, int dv, int BH, int T) {
+bool chunked_tc_supports(int p, int dv, int lg) {
+    bool ok = false;
+    KATA_DISPATCH(ok = true);
+    return ok;
+}
+
+int chunked_tc_segments(int p, int dv, int lg, int BH, int T) {
     const int nch = (T + kChunk - 1) / kChunk;
     int m = 0;
-    KATA_DISPATCH(m = max_clusters<P, DV>());
+    KATA_DISPATCH(m = max_clusters<P, DV, LG>());
     if (m <= 0) return 0;
     if (nch <= 0) return 1;
     int G = m / (BH > 0 ? BH : 1);
@@ -1179,9 +1286,9 @@ size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv) { return intra_ws(BH
 
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
                               const float* S_start, const float* z_start, int start_groups, float* S_final,
-                              float* z_final, int BH, int T, int p, int dv, int G, cudaStream_t s) {
+                              float* z_final, int BH, int T, int p, int dv, int lg, int G, cudaStream_t s) {
     const int seg_chunks = chunked_tc_segment_chunks(T, G);
-    KATA_DISPATCH(return launch_typed<P, DV>(q, k, v, o, intra, S_start, z_start, start_groups, S_final, z_final, BH, T,
+    KATA_DISPATCH(return launch_typed<P, DV, LG>(q, k, v, o, intra, S_start, z_start, start_groups, S_final, z_final, BH, T,
                                              seg_chunks, G, s));
     return cudaErrorInvalidValue;
 }

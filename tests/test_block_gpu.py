@@ -131,17 +131,82 @@ def test_block_argument_errors():
     assert e.value.status == kb.KATA_ERR_UNSUPPORTED
 
 
+# ---------------------------------------------------------------- KATA-Sigma-g on the tensor cores
+# bf16 KATA-Sigma-g with blocks of 16 or 32 runs on the fused tensor-core
+# forward (the lift of one block sets the state's width; the key and query
+# lifts sum the g block lifts, Z sums the g block Gram matrices, and the
+# intra-chunk scores sum the squares of every block pair's dot products).
+
+def _traced(fn):
+    kb.kata_trace_start(1024)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        names = {name for name, _ in kb.kata_trace_stop()}
+    return out, names
+
+
+TC_SIGMA = [(2, 64, 64), (2, 64, 16), (4, 64, 32), (2, 32, 64)]
+
+
+@pytest.mark.parametrize("g,p,dv", TC_SIGMA)
+@pytest.mark.parametrize("T", [1, 127, 129, 600])
+def test_sigma_tensor_core_forward(g, p, dv, T):
+    q, k, v = _tokens(1, 3, T, p, dv, torch.bfloat16, seed=7 * g + p + T)
+    o, names = _traced(lambda: kb.kata_forward_chunked_block(q, k, v, 128, SIGMA, g))
+    assert "chunked_tc" in names and "intra_tc" in names, names
+    assert_close(f64(o), oracle.forward_plain_block(f64(q), f64(k), f64(v), SIGMA, g), torch.bfloat16,
+                 "Sigma tensor cores")
+
+
+@pytest.mark.parametrize("g,p,dv", TC_SIGMA[:2])
+def test_sigma_tensor_core_states_and_split_calls(g, p, dv):
+    """The carried state of the tensor-core path (KATA-Sigma-g packing, sqrt(2)
+    off the diagonal) continues a forward and matches the oracle's recurrence."""
+    B, H, T1, T2 = 1, 2, 300, 222
+    q, k, v = _tokens(B, H, T1 + T2, p, dv, torch.bfloat16, seed=5 + g)
+    n = kb.kata_lift_dim(SIGMA, p, g)
+    S, z = torch.empty(B, H, n, dv, device="cuda"), torch.empty(B, H, n, device="cuda")
+    S2, z2 = torch.empty_like(S), torch.empty_like(z)
+    part = lambda x, a, b: x[:, :, a:b].contiguous()  # noqa: E731
+    o1, _, _ = kb.kata_forward_chunked_block(part(q, 0, T1), part(k, 0, T1), part(v, 0, T1), 64, SIGMA, g,
+                                             S_final=S, z_final=z)
+    o2, _, _ = kb.kata_forward_chunked_block(part(q, T1, T1 + T2), part(k, T1, T1 + T2), part(v, T1, T1 + T2), 64,
+                                             SIGMA, g, S0=S, z0=z, S_final=S2, z_final=z2)
+    torch.cuda.synchronize()
+    ref = oracle.forward_plain_block(f64(q), f64(k), f64(v), SIGMA, g)
+    assert_close(np.concatenate([f64(o1), f64(o2)], axis=2), ref, torch.bfloat16, "Sigma split")
+    _, S_ref, z_ref = oracle.forward_recurrent_block(f64(q), f64(k), f64(v), SIGMA, g)
+    assert _rel(f64(S2), S_ref) <= TOL[torch.bfloat16] and _rel(f64(z2), z_ref) <= TOL[torch.bfloat16]
+
+
+def test_sigma_tensor_core_zero_vectors():
+    q, k, v = _tokens(1, 2, 260, 64, 64, torch.bfloat16, seed=3)
+    q[0, 0, 7] = 0
+    k[0, 1, 0] = 0
+    k[0, 0, 128] = 0
+    o = kb.kata_forward_chunked_block(q, k, v, 128, SIGMA, 2)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(o[0, 0, 7]) == 0
+    assert_close(f64(o), oracle.forward_plain_block(f64(q), f64(k), f64(v), SIGMA, 2), torch.bfloat16, "zero")
+
+
 @pytest.mark.slow
 def test_chunked_block_full_size_sampled_rows():
-    """KATA-Sigma-2 on the 131072-token, 8-head, p = dv = 64 bf16 workload (C = 128),
-    against the oracle's definition on sampled rows (first, last, chunk edges,
-    random positions) of every head."""
-    from tests.parity import rows_error, sample_rows
+    """KATA-Sigma-2 on the 131072-token, 8-head, p = dv = 64 bf16 workload (C = 128)
+    -- the fused tensor-core forward -- against the oracle's definition on
+    sampled rows (first, last, chunk edges, random and late positions) of every
+    head, gated per head and row by row."""
+    from tests.parity import row_errors, rows_error, sample_rows
     w = inputs.WORKLOADS[3]
     q, k, v = inputs.make(w, "cuda")
-    o = kb.kata_forward_chunked_block(q, k, v, w.C, SIGMA, 2)
-    torch.cuda.synchronize()
+    o, names = _traced(lambda: kb.kata_forward_chunked_block(q, k, v, w.C, SIGMA, 2))
+    assert "chunked_tc" in names
     bh, t = sample_rows(w.B, w.H, w.T, w.C, per_head=6, seed=1)
     ref = oracle.forward_plain_block_rows(f64(q), f64(k), f64(v), SIGMA, 2, bh, t)
     got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
     assert rows_error(got, ref) <= TOL[torch.bfloat16]
+    per_row = row_errors(got, ref)
+    print(f"Sigma-2 full size: worst per-row error {per_row.max():.3e}")
+    assert per_row.max() <= TOL[torch.bfloat16]
