@@ -805,11 +805,14 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             tma_load_3d(q_buf(stg), &tmq, 0, row, (int)bh, &qs_full[stg]);
         }
     }
-    if (t == 384) {
+    if (warp == 12) {
         // =============================================================== MMA issuer
-        // Every descriptor is built once: one thread issues all MMAs, so the
-        // issue loop carries no descriptor arithmetic beyond adds of
-        // compile-time offsets (a step moves the start-address field, in
+        // The whole warp runs the issue loop (waits, descriptors) and one
+        // elected lane issues each instruction: the operands stay warp-uniform,
+        // which keeps the issue of back-to-back MMAs as cheap as a loop of
+        // constants (a single lane in a divergent branch issues them at about
+        // two thirds of that rate).  Every descriptor is built once; the loop
+        // adds compile-time offsets (a step moves the start-address field, in
         // 16-byte units).
         constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
         constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, false, true);
@@ -828,48 +831,48 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         const uint64_t d_z16 = sdesc_kmajor_sw128(smem_u32(s_z16));
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            if (!mbar_wait(&v_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!wait(&v_full[slot], use & 1)) { fail(); break; }
             const uint64_t dv = d_v[slot];
             // ---- group U: state updates, tile by tile (extra CTA: tail state and Z)
             bool ok = true;
             if (!extra) {
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl) {
-                    if (!mbar_wait(&klift_full[tl], kk & 1, &abort_flag, kWaitNs)) { ok = false; break; }
-                    if (tl == 0 && kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs)) { ok = false; break; }
+                    if (!wait(&klift_full[tl], kk & 1)) { ok = false; break; }
+                    if (tl == 0 && kk >= 1 && !wait(&state_read, (kk - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
-                    mma_commit(&ak_free[tl]);
+                        mma_ss_w(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                    mma_commit_w(&ak_free[tl]);
                 }
                 if (!ok) { fail(); break; }
-                mma_commit(&upd_done);
-                mma_commit(&v_free[slot]);
+                mma_commit_w(&upd_done);
+                mma_commit_w(&v_free[slot]);
             } else {
-                if (!mbar_wait(&klift_full[0], kk & 1, &abort_flag, kWaitNs) ||
-                    !mbar_wait(&kts_full[slot], use & 1, &abort_flag, kWaitNs) ||
-                    (kk >= 1 && !mbar_wait(&state_read, (kk - 1) & 1, &abort_flag, kWaitNs))) { fail(); break; }
+                if (!wait(&klift_full[0], kk & 1) ||
+                    !wait(&kts_full[slot], use & 1) ||
+                    (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ss(tb + K::tx_s, d_ak + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                for (int ks = 0; ks < 8; ++ks) mma_ss_w(tb + K::tx_s, d_ak + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
                 // Z += sum over the blocks of (rows of the block)^T (rows of the block)
 #pragma unroll
                 for (int blk = 0; blk < LG; ++blk)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tb + K::tx_z, d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks),
+                        mma_ss_w(tb + K::tx_z, d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks),
                                d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks), id_z, 1u);
-                mma_commit(&ak_free[0]);
-                mma_commit(&upd_done);
-                mma_commit(&v_free[slot]);
-                mma_commit(&kts_free[slot]);
+                mma_commit_w(&ak_free[0]);
+                mma_commit_w(&upd_done);
+                mma_commit_w(&v_free[slot]);
+                mma_commit_w(&kts_free[slot]);
             }
             // ---- group R: readout of the state before this chunk
-            if (!mbar_wait(&qlift_full[slot], use & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (kk >= 1 && !mbar_wait(&s16_ready, (kk - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (kk >= 2 && !mbar_wait(&y_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            if (extra && !mbar_wait(&qs_full[kk % nq], (kk / nq) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            if (!wait(&qlift_full[slot], use & 1)) { fail(); break; }
+            if (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1)) { fail(); break; }
+            if (kk >= 2 && !wait(&y_free[slot], (use - 1) & 1)) { fail(); break; }
+            if (extra && !wait(&qs_full[kk % nq], (kk / nq) & 1)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
                 const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 128 * slot;
@@ -877,26 +880,26 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 for (int tl = 0; tl < K::TPC; ++tl)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(dy, aq + 64 * tl + 8 * ks, d_s16 + tl * kAtomD + ks * kStepMN, id_read,
+                        mma_ts_w(dy, aq + 64 * tl + 8 * ks, d_s16 + tl * kAtomD + ks * kStepMN, id_read,
                                (tl > 0 || ks > 0) ? 1u : 0u);
             } else {
                 const uint32_t dy = tb + K::tx_y + 64 * slot, aq = tb + K::tx_aq + 32 * slot;
 #pragma unroll
                 for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
-                    mma_ts(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
+                    mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
                 // W = [Q_0 Z | Q_1 Z | ...], one block of columns per block of the queries
 #pragma unroll
                 for (int blk = 0; blk < LG; ++blk)
 #pragma unroll
                     for (int ks = 0; ks < M / 16; ++ks)
-                        mma_ss(tb + K::tx_w + blk * M, d_q[kk % nq] + (blk * (M / 16) + ks) * kStepK,
+                        mma_ss_w(tb + K::tx_w + blk * M, d_q[kk % nq] + (blk * (M / 16) + ks) * kStepK,
                                d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
             }
-            mma_commit(&y_part[slot]);
-            mma_commit(&aq_free[slot]);
+            mma_commit_w(&y_part[slot]);
+            mma_commit_w(&aq_free[slot]);
         }
         // every issued MMA has completed before tensor memory is released
-        mma_commit(&drain);
+        mma_commit_w(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
     }
 

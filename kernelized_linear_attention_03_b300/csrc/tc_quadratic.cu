@@ -138,28 +138,29 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_wait_quiet(&k_full[j % kStages], (j / kStages) & 1, kWaitNs);
             mbar_wait_quiet(&v_full[j % kStages], (j / kStages) & 1, kWaitNs);
         }
-    } else if (t == 32) {
+    } else if (warp == 1) {
         // =============================================================== MMA issuer
+        // (the whole warp runs the loop; one elected lane issues each instruction)
         constexpr uint32_t id_s = idesc_bf16_f32(kTile, kTile);
         constexpr uint32_t id_o = idesc_bf16_f32_major(kTile, kNV, false, true);
         // scores of query tile g against key tile j (P in place of S afterwards)
         auto issue_s = [&](int g, int j) -> bool {
             const int st = j % kStages;
-            if (!mbar_wait(&k_ready[st], (j / kStages) & 1, &abort_flag, kWaitNs)) return false;
+            if (!wait(&k_ready[st], (j / kStages) & 1)) return false;
             tc_fence_after();
             const uint64_t d_q = sdesc_kmajor_sw128(smem_u32(sm + kQOff + g * kAtom));
             const uint64_t d_k = sdesc_kmajor_sw128(smem_u32(sm + kKOff + st * kAtom));
 #pragma unroll
             for (int ks = 0; ks < P / 16; ++ks)
-                mma_ss(tb + kTmS + 128 * g, d_q + 2 * ks, d_k + 2 * ks, id_s, ks > 0 ? 1u : 0u);
-            mma_commit(&s_full[g]);
+                mma_ss_w(tb + kTmS + 128 * g, d_q + 2 * ks, d_k + 2 * ks, id_s, ks > 0 ? 1u : 0u);
+            mma_commit_w(&s_full[g]);
             return true;
         };
         // O_g += P_g [V_j | 1]; then the next scores of tile g (they overwrite P_g)
         auto issue_o = [&](int g, int j) -> bool {
             const int st = j % kStages;
-            if (!mbar_wait(&p_full[g], j & 1, &abort_flag, kWaitNs) ||
-                !mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag, kWaitNs))
+            if (!wait(&p_full[g], j & 1) ||
+                !wait(&v_full[st], (j / kStages) & 1))
                 return false;
             tc_fence_after();
             // B = [value tile | ones]: two MN atoms, the ones atom kOnesOff - value stage bytes away
@@ -167,20 +168,20 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const uint64_t d_v = sdesc_mnmajor_sw128(vaddr, (uint32_t)(kOnesOff - (kVOff + st * kAtom)));
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ts(tb + kTmO + 128 * g, tb + kTmS + 128 * g + 8 * ks, d_v + ks * (2048 >> 4), id_o,
+                mma_ts_w(tb + kTmO + 128 * g, tb + kTmS + 128 * g + 8 * ks, d_v + ks * (2048 >> 4), id_o,
                        (j > 0 || ks > 0) ? 1u : 0u);
             if (j + 1 <= last[g]) return issue_s(g, j + 1);
             return true;
         };
-        bool ok = mbar_wait(&q_full, 0, &abort_flag, kWaitNs) && issue_s(0, 0) && (!has_b || issue_s(1, 0));
+        bool ok = wait(&q_full, 0) && issue_s(0, 0) && (!has_b || issue_s(1, 0));
         for (int j = 0; ok && j < nj; ++j) {
             if (j <= last[0] && !issue_o(0, j)) { ok = false; break; }
             if (j <= last[1] && !issue_o(1, j)) { ok = false; break; }
-            mma_commit(&kv_free[j % kStages]);  // both tiles' products with key / value tile j are issued
+            mma_commit_w(&kv_free[j % kStages]);  // both tiles' products with key / value tile j are issued
         }
         if (!ok) fail();
-        mma_commit(&o_done);
-        mma_commit(&drain);
+        mma_commit_w(&o_done);
+        mma_commit_w(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
     } else if (warp >= 12) {
         // =============================================================== key normalisation

@@ -166,8 +166,9 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             mbar_wait_quiet(&k_full[i % kStages], (i / kStages) & 1, kWaitNs);
             mbar_wait_quiet(&v_full[i % kStages], (i / kStages) & 1, kWaitNs);
         }
-    } else if (t == 32) {
+    } else if (warp == 1) {
         // =============================================================== MMA issuer
+        // (the whole warp runs the loop; one elected lane issues each instruction)
         constexpr uint32_t idesc = idesc_bf16_f32_major(128, kNB, true, true);
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
@@ -176,9 +177,9 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             block(i, b0, b1, seg);
             const int sl = seg - seg0, acb = sl & 1;
             const bool first = b0 == seg * L, last = b1 == min(T, (seg + 1) * L);
-            if (!mbar_wait(&a_full[ab], (i >> 1) & 1, &abort_flag, kWaitNs) ||
-                !mbar_wait(&v_full[st], (i / kStages) & 1, &abort_flag, kWaitNs) ||
-                (first && sl >= 2 && !mbar_wait(&acc_free[acb], ((sl - 2) >> 1) & 1, &abort_flag, kWaitNs))) {
+            if (!wait(&a_full[ab], (i >> 1) & 1) ||
+                !wait(&v_full[st], (i / kStages) & 1) ||
+                (first && sl >= 2 && !wait(&acc_free[acb], ((sl - 2) >> 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -188,14 +189,14 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
                                                      (uint32_t)(kOnesOff - (kVOff + st * kAtom)));
             const int steps = (b1 - b0 + 15) / 16;
             for (int ks = 0; ks < steps; ++ks)
-                mma_ss(tb + 128 * acb, d_a + ks * (2048 >> 4), d_b + ks * (2048 >> 4), idesc,
+                mma_ss_w(tb + 128 * acb, d_a + ks * (2048 >> 4), d_b + ks * (2048 >> 4), idesc,
                        (first && ks == 0) ? 0u : 1u);
-            mma_commit(&a_free[ab]);
-            mma_commit(&kv_free[st]);
-            if (last) mma_commit(&acc_full[acb]);
+            mma_commit_w(&a_free[ab]);
+            mma_commit_w(&kv_free[st]);
+            if (last) mma_commit_w(&acc_full[acb]);
         }
         if (!ok) fail();
-        mma_commit(&drain);
+        mma_commit_w(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
     } else if (warp >= 4 && warp < 8) {
         // =============================================================== lift warps
