@@ -16,8 +16,9 @@
 // the packed lift; it keeps its state rows in tensor memory (fp32,
 // accumulated by the update MMA) and a bf16 copy in shared memory (B operand
 // of the readout MMA).  Its query lift goes to tensor memory (A operand of
-// the readout), its key lift to shared memory (A operand of the update,
-// built one slot per thread from the chunk's transposed unit keys).  The
+// the readout), its key lift (A operand of the update, built one slot per
+// thread from the chunk's transposed unit keys) to tensor memory as well
+// where the columns allow (one tile per CTA), else to shared memory.  The
 // "extra CTA" owns the last, partly filled tile and Z (the inter-chunk
 // denominator).  Each CTA's partial Y (128 x dv, sent as bf16) is summed in
 // distributed shared memory: tile CTA r owns rows [r*R, r*R + R) of the
@@ -53,7 +54,7 @@ constexpr int kThreads = 512;  // warpgroups: query lift and readout, state epil
 // warpgroup gives back registers that the query warpgroup takes.
 // 128 * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma) must not exceed
 // 512 * (registers per thread at launch); the launcher checks that.
-constexpr uint32_t kRegsLift = 168, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 88;
+constexpr uint32_t kRegsLift = 152, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 104;
 constexpr int kChunk = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes
@@ -77,17 +78,21 @@ struct Cfg {
     // transposed unit keys of a chunk: two 64-token boxes of P rows x 128 bytes
     static constexpr uint32_t kt_box = P * 128;
     static constexpr uint32_t kt_bytes = 2 * kt_box;
+    // the tile CTA's key lift: tensor memory with one tile per CTA, shared
+    // memory with two (their state, query lift double buffer and partial
+    // readouts leave no columns for it)
+    static constexpr bool AKT = TPC == 1;
     // shared memory, in 16 KB atoms from a 1024-byte aligned base
-    //   tile CTA : key lift [0, 2 TPC) (two 64-token atoms per tile), V x2,
+    //   tile CTA : [key lift, two 64-token atoms per tile, unless AKT], V x2,
     //              bf16 state [TPC], query stage, transposed-key stages x2
-    //   extra CTA: tail key lift [0, 2), V x2, bf16 tail state, bf16 Z,
-    //              query stages x2, transposed-key stages x2, one spare atom
-    //              (the M = 128 reads of the Z update run past the last stage)
-    static constexpr uint32_t t_ak = 0, t_v = (2 * TPC) * kAtom, t_s16 = (2 * TPC + 2) * kAtom,
-                              t_q = (3 * TPC + 2) * kAtom, t_kt = (3 * TPC + 3) * kAtom;
-    static constexpr uint32_t x_ak = 0, x_v = 2 * kAtom, x_s16 = 4 * kAtom, x_z16 = 5 * kAtom, x_q = 6 * kAtom,
-                              x_kt = 8 * kAtom;
-    static constexpr uint32_t atoms_tile = 3 * TPC + 5, atoms_extra = 11;
+    //   extra CTA: V x2, bf16 tail state, bf16 Z, query stages x2,
+    //              transposed-key stages x2, one spare atom (the M = 128
+    //              reads of the Z update run past the last stage)
+    static constexpr uint32_t ak_atoms = AKT ? 0 : 2 * TPC;
+    static constexpr uint32_t t_ak = 0, t_v = ak_atoms * kAtom, t_s16 = t_v + 2 * kAtom, t_q = t_s16 + TPC * kAtom,
+                              t_kt = t_q + kAtom;
+    static constexpr uint32_t x_v = 0, x_s16 = 2 * kAtom, x_z16 = 3 * kAtom, x_q = 4 * kAtom, x_kt = 6 * kAtom;
+    static constexpr uint32_t atoms_tile = ak_atoms + TPC + 5, atoms_extra = 9;
     // partial readouts received by a tile CTA: one part per (source CTA,
     // receive slot) = R rows of bf16 laid out [DV/8][R] x 16 bytes (a warp's
     // store of one column group is contiguous per owner), then R fp32
@@ -96,78 +101,110 @@ struct Cfg {
     static constexpr uint32_t recv_part = part_y + round16(R * 4);
     static constexpr uint32_t recv_buf = CS * recv_part;
     static constexpr uint32_t recv_off = atoms_tile * kAtom;
-    // receive slots (chunks in flight): three where they fit beside the
-    // static shared memory
+    // the owned rows' intra-chunk part, staged by a bulk copy per chunk: R
+    // rows of bf16, then R fp32 normalisers
+    static constexpr uint32_t intra_slot = R * DV * 2 + round16(R * 4);
+    // receive slots (chunks in flight, each with its intra-chunk stage):
+    // three where they fit beside the static shared memory
     static constexpr uint32_t kStaticReserve = 1024 + 3072;
-    static constexpr int RS = recv_off + 3 * recv_buf + kStaticReserve <= 232448 ? 3 : 2;
-    static constexpr uint32_t total =
-        (recv_off + RS * recv_buf) > atoms_extra * kAtom ? recv_off + RS * recv_buf : atoms_extra * kAtom;
+    static constexpr int RS = recv_off + 3 * (recv_buf + intra_slot) + kStaticReserve <= 232448 ? 3 : 2;
+    static constexpr uint32_t intra_off = recv_off + RS * recv_buf;
+    static constexpr uint32_t tile_end = intra_off + RS * intra_slot;
+    static constexpr uint32_t total = tile_end > atoms_extra * kAtom ? tile_end : atoms_extra * kAtom;
     static constexpr size_t smem = total + 1024;
     // tensor memory columns, tile CTA
-    static constexpr uint32_t tm_s = 0;      // TPC x 64: fp32 state
-    static constexpr uint32_t tm_aq = 128;   // 2 slots x TPC x 64: query lift
-    static constexpr uint32_t tm_y = 384;    // 2 slots x 64: partial readout
+    static constexpr uint32_t tm_s = 0;                                // TPC x 64: fp32 state
+    static constexpr uint32_t tm_ak = 64 * TPC;                        // AKT: 64, key lift (bf16 pairs of tokens)
+    static constexpr uint32_t tm_aq = AKT ? 128 * TPC : 64 * TPC;      // 2 slots x TPC x 64: query lift
+    static constexpr uint32_t tm_y = tm_aq + 128 * TPC;                // 2 slots x 64: partial readout
     // tensor memory columns, extra CTA
     static constexpr uint32_t tx_s = 0;      // tail state
     static constexpr uint32_t tx_aq = 64;    // 2 slots x 32: tail query lift
     static constexpr uint32_t tx_y = 128;    // 2 slots x 64: partial readout
+    static constexpr uint32_t tx_ak = 256;   // 64: tail key lift (lanes past the tail hold zeros)
     static constexpr uint32_t tx_w = 384;    // Q Z
     static constexpr uint32_t tx_z = 448;    // Z
     static_assert(NT % TPC == 0, "tiles must split evenly");
+    static_assert(tm_y + 128 <= 512, "tensor memory columns");
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(total + kStaticReserve <= 232448, "shared memory");
     static_assert(R * NTC == kChunk, "owned rows");
     static_assert(kt_bytes <= kAtom, "transposed-key stage");
+    static_assert((R * DV * 2) % 16 == 0 && (R * 4) % 16 == 0 && intra_off % 16 == 0, "bulk copy sizes");
 };
 
 // ---------------------------------------------------------------- key lift, one slot per thread
-// Row `row` of a K-major operand tile (two 64-token atoms of 128 rows x 128
-// bytes, 128-byte swizzle) receives the key lift of internal slot `slot` for
-// the 128 tokens of a chunk, from the chunk's transposed unit keys `kts` (row
-// d = dimension d over the tokens, two 64-token boxes of P rows): k_i k_j for
-// the full lift, sum_a k_{aM+i} k_{aM+j} over the LG blocks of width M for
-// KATA-Sigma-g.  Consecutive tokens sit side by side in both, so every 16
-// bytes of the row are bf16x2 multiplies of 16-byte loads.  Slots past n
+// The key lift of internal slot (i, j) for the 128 tokens of a chunk comes
+// from the chunk's transposed unit keys `kts` (row d = dimension d over the
+// tokens, two 64-token boxes of P rows, 128-byte swizzle): k_i k_j for the
+// full lift, sum_a k_{aM+i} k_{aM+j} over the LG blocks of width M for
+// KATA-Sigma-g.  Consecutive tokens sit side by side in both, so the 16
+// bytes of tokens [64h + 8c, 64h + 8c + 8) are four bf16x2 multiplies of two
+// 16-byte loads.
+template <int P, int LG>
+__device__ __forceinline__ uint4 key_words(const uint8_t* kts, int i, int j, int h, int c) {
+    constexpr int M = P / LG;
+    uint4 r;
+#pragma unroll
+    for (int blk = 0; blk < LG; ++blk) {
+        const int bi = blk * M + i, bj = blk * M + j;  // rows of this block's two factors
+        const uint4 a = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bi * 128 + ((c ^ (bi & 7)) << 4));
+        const uint4 b = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bj * 128 + ((c ^ (bj & 7)) << 4));
+        if (blk == 0) {
+            r.x = hmul2_bf16(a.x, b.x);
+            r.y = hmul2_bf16(a.y, b.y);
+            r.z = hmul2_bf16(a.z, b.z);
+            r.w = hmul2_bf16(a.w, b.w);
+        } else {
+            r.x = hfma2_bf16(a.x, b.x, r.x);
+            r.y = hfma2_bf16(a.y, b.y, r.y);
+            r.z = hfma2_bf16(a.z, b.z, r.z);
+            r.w = hfma2_bf16(a.w, b.w, r.w);
+        }
+    }
+    return r;
+}
+
+// Row `row` of a K-major shared-memory operand tile (two 64-token atoms of
+// 128 rows x 128 bytes, 128-byte swizzle) receives the key lift of slot
+// `slot`; slots past n give zeros.
+template <int P, int LG>
+__device__ __forceinline__ void key_row_smem(const uint8_t* kts, int slot, uint8_t* ak, int row) {
+    constexpr int n = lift::packed_n(P / LG);
+    uint8_t* dst0 = ak + (row >> 3) * 1024 + (row & 7) * 128;
+    const bool live = slot < n;
+    int i = 0, j = 0;
+    if (live) lift::slot_coord(P / LG, slot, i, j);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst0 + h * kAtom + ((c ^ (row & 7)) << 4)) =
+                live ? key_words<P, LG>(kts, i, j, h, c) : make_uint4(0, 0, 0, 0);
+}
+
+// Lane `slot % 128` of a tensor-memory operand (64 columns, column c = the
+// bf16 pair of tokens 2c, 2c+1) receives the key lift of slot `slot`, a
+// quarter of the chunk (32 tokens) per tensor-memory store; slots past n
 // give zeros.
 template <int P, int LG>
-__device__ __forceinline__ void key_row(const uint8_t* kts, int slot, uint8_t* ak, int row) {
-    constexpr int M = P / LG;
-    constexpr int n = lift::packed_n(M);
-    uint8_t* dst0 = ak + (row >> 3) * 1024 + (row & 7) * 128;
-    if (slot >= n) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst0 + h * kAtom + (c << 4)) = make_uint4(0, 0, 0, 0);
-        return;
-    }
+__device__ __forceinline__ void key_row_tmem(const uint8_t* kts, int slot, uint32_t taddr) {
+    constexpr int n = lift::packed_n(P / LG);
+    const bool live = slot < n;
     int i = 0, j = 0;
-    lift::slot_coord(M, slot, i, j);
+    if (live) lift::slot_coord(P / LG, slot, i, j);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint8_t* dst = dst0 + h * kAtom;
+    for (int qt = 0; qt < 4; ++qt) {
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 r;
-#pragma unroll
-            for (int blk = 0; blk < LG; ++blk) {
-                const int bi = blk * M + i, bj = blk * M + j;  // rows of this block's two factors
-                const uint4 a = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bi * 128 + ((c ^ (bi & 7)) << 4));
-                const uint4 b = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bj * 128 + ((c ^ (bj & 7)) << 4));
-                if (blk == 0) {
-                    r.x = hmul2_bf16(a.x, b.x);
-                    r.y = hmul2_bf16(a.y, b.y);
-                    r.z = hmul2_bf16(a.z, b.z);
-                    r.w = hmul2_bf16(a.w, b.w);
-                } else {
-                    r.x = hfma2_bf16(a.x, b.x, r.x);
-                    r.y = hfma2_bf16(a.y, b.y, r.y);
-                    r.z = hfma2_bf16(a.z, b.z, r.z);
-                    r.w = hfma2_bf16(a.w, b.w, r.w);
-                }
-            }
-            *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) = r;
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint4 r = live ? key_words<P, LG>(kts, i, j, qt >> 1, (qt & 1) * 4 + cc) : make_uint4(0, 0, 0, 0);
+            w[4 * cc] = r.x;
+            w[4 * cc + 1] = r.y;
+            w[4 * cc + 2] = r.z;
+            w[4 * cc + 3] = r.w;
         }
+        tmem_st16(taddr + 16 * qt, w);
     }
 }
 
@@ -341,6 +378,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     __shared__ uint64_t upd_done, state_read, s16_ready, drain, rd_sync;
     __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
     __shared__ uint64_t local_full[K::RS];  // this CTA's own partial rows written (one arrival per row)
+    __shared__ uint64_t intra_full[K::RS];  // the owned rows' intra-chunk part staged
     __shared__ float dens[2][kChunk];       // extra CTA: inter-chunk denominators of the chunk rows
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -360,7 +398,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     // deliver per chunk
     const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + my_rows * 4;
     const int nq = extra ? 2 : 1;  // query stages (the extra CTA's MMAs read the queries in place)
-    uint8_t* const s_ak = sm + (extra ? K::x_ak : K::t_ak);
+    uint8_t* const s_ak = sm + K::t_ak;  // tile CTA key lift, when it lives in shared memory
     uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
     uint8_t* const s_z16 = sm + K::x_z16;
     uint8_t* const s_recv = sm + K::recv_off;
@@ -397,6 +435,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             mbar_init(&recv_full[b], 1);
             mbar_init(&peer_free[b], K::NTC);  // one arrival per owner
             mbar_init(&local_full[b], my_rows > 0 ? my_rows : 1);
+            mbar_init(&intra_full[b], 1);
         }
         fence_mbar_init();
         // the first RS chunks' partial rows may arrive as soon as the cluster starts
@@ -408,12 +447,6 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
-    // the extra CTA's tail key lift fills rows [0, 32) of its operand tile;
-    // the other rows are read by the tail update's M = 128 MMAs into state
-    // rows nothing reads, and are kept at zero
-    if (extra)
-        for (int i = t; i < 2 * (int)kAtom / 16; i += kThreads)
-            reinterpret_cast<uint4*>(s_ak)[i] = make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -472,6 +505,17 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         }
         tmem_wait_st();
     }
+    // the extra CTA's tail key lift fills lanes [0, 32) of its operand; the
+    // other lanes are read by the tail update's M = 128 MMAs into state rows
+    // nothing reads, and are kept at zero
+    if (extra && warp >= 9 && warp < 12) {
+        uint32_t zw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) zw[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) tmem_st16(tm(K::tx_ak + c), zw);
+        tmem_wait_st();
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     cluster.sync();  // barriers initialised and start state in place cluster-wide
@@ -504,7 +548,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (!extra) {
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
-                    query_dispatch<P, LG>(rank * K::TPC + tl, uq, tm(K::tm_aq + 128 * slot + 64 * tl));
+                    query_dispatch<P, LG>(rank * K::TPC + tl, uq, tm(K::tm_aq + 64 * K::TPC * slot + 64 * tl));
             } else {
                 query_tail<P, LG>(uq, tm(K::tx_aq + 32 * slot));
             }
@@ -689,15 +733,22 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (!wait(&kts_full[stg], use & 1)) { fail(); break; }
             const uint8_t* kts = kt_buf(stg);
             bool ok = true;
+            const int ntl = extra ? 1 : K::TPC;
 #pragma unroll
             for (int tl = 0; tl < K::TPC; ++tl) {
-                if (extra && tl > 0) break;
+                if (tl >= ntl) break;
                 if (kk >= 1 && !wait(&ak_free[tl], (kk - 1) & 1)) { ok = false; break; }
-                if (!extra)
-                    key_row<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
-                else if (e < 32)
-                    key_row<P, LG>(kts, K::NT * 128 + e, s_ak, e);
+                tc_fence_after();
+                if (extra) {
+                    if (warp == 8) key_row_tmem<P, LG>(kts, K::NT * 128 + e, tm(K::tx_ak));
+                } else if constexpr (K::AKT) {
+                    key_row_tmem<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, tm(K::tm_ak + 64 * tl));
+                } else {
+                    key_row_smem<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
+                }
                 fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(&klift_full[tl]);
             }
             if (!ok) { fail(); break; }
@@ -708,78 +759,97 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     }
     if (warp >= 14 && my_rows > 0) {
         // =============================================================== reduce warps
-        // owner side, chunk by chunk as the partial rows land: sum them, add
-        // the intra-chunk rows, divide and store the outputs, then hand the
-        // receive slot back to every sender (its next use is RS chunks later)
+        // owner side, chunk by chunk as the partial rows land: sum them and
+        // the intra-chunk rows (staged by a bulk copy RS chunks ahead), hand
+        // the receive slot back to every sender (its next use is RS chunks
+        // later), then divide and store the outputs
         constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
+        constexpr uint32_t kIntraY = K::R * DV * 2, kIntraBytes = kIntraY + K::R * 4;
         const int er = t - 448;
         const int r0 = rank * K::R;
         const int items = my_rows * (DV / 8);
-        const int64_t head_row = bh * (int64_t)T;
+        const int64_t head_row = bh * (int64_t)T;                // output rows
+        const int64_t head_prow = bh * (int64_t)NCH * kChunk;    // intra-chunk rows: whole chunks per head
+        uint8_t* const s_intra = sm + K::intra_off;
+        int staged = 0, consumed = 0;  // bulk copies issued / waited for
+        auto stage_intra = [&](int kr) {
+            ++staged;
+            const int r = kr % K::RS;
+            const int64_t row = head_prow + (int64_t)(c0 + kr) * kChunk + r0;
+            uint8_t* dst = s_intra + r * K::intra_slot;
+            mbar_arrive_expect_tx(&intra_full[r], kIntraBytes);
+            bulk_load(dst, y_intra + row * DV, kIntraY, &intra_full[r]);
+            bulk_load(dst + kIntraY, d_intra + row, K::R * 4, &intra_full[r]);
+        };
+        if (er == 0)
+            for (int kr = 0; kr < K::RS && kr < nk; ++kr) stage_intra(kr);
         for (int kr = 0; kr < nk; ++kr) {
             const int r = kr % K::RS;
-            // this chunk's intra-chunk rows and normalisers (written before this kernel)
-            uint4 yin[kRedIt];
-            float din[kRedIt];
-#pragma unroll
-            for (int it = 0; it < kRedIt; ++it) {
-                const int idx = er + 64 * it;
-                const int lr = idx % my_rows, i = idx / my_rows;
-                const int otok = (c0 + kr) * kChunk + r0 + lr;
-                yin[it] = make_uint4(0, 0, 0, 0);
-                din[it] = 0.f;
-                if (idx < items && otok < T) {
-                    yin[it] = *reinterpret_cast<const uint4*>(y_intra + (head_row + otok) * DV + 8 * i);
-                    din[it] = d_intra[head_row + otok];
-                }
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs) &&
-                                             mbar_wait(&local_full[r], (kr / K::RS) & 1, &abort_flag, kWaitNs))) {
+            const uint32_t par = (kr / K::RS) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], par, &abort_flag, kWaitNs) &&
+                                             mbar_wait(&local_full[r], par, &abort_flag, kWaitNs) &&
+                                             mbar_wait(&intra_full[r], par, &abort_flag, kWaitNs))) {
                 fail();
                 break;
             }
+            consumed = kr + 1;
             const uint8_t* recv = s_recv + r * K::recv_buf;
+            const uint8_t* sin = s_intra + r * K::intra_slot;
+            float acc[kRedIt][8], den[kRedIt];
 #pragma unroll
             for (int it = 0; it < kRedIt; ++it) {
                 const int idx = er + 64 * it;
-                if (idx >= items) break;
                 const int lr = idx % my_rows, i = idx / my_rows;
-                float acc[8];
-                {
-                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&yin[it]);
+                if (idx >= items) continue;
+                const uint4 yin = *reinterpret_cast<const uint4*>(sin + lr * (DV * 2) + i * 16);
+                const __nv_bfloat162* hy = reinterpret_cast<const __nv_bfloat162*>(&yin);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[2 * j] = __low2float(h[j]);
-                        acc[2 * j + 1] = __high2float(h[j]);
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    acc[it][2 * j] = __low2float(hy[j]);
+                    acc[it][2 * j + 1] = __high2float(hy[j]);
                 }
+                den[it] = *reinterpret_cast<const float*>(sin + kIntraY + lr * 4);
 #pragma unroll
                 for (int src = 0; src < K::CS; ++src) {
                     const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
                     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        acc[2 * j] += __low2float(h[j]);
-                        acc[2 * j + 1] += __high2float(h[j]);
+                        acc[it][2 * j] += __low2float(h[j]);
+                        acc[it][2 * j + 1] += __high2float(h[j]);
                     }
                 }
-                const int otok = (c0 + kr) * kChunk + r0 + lr;
-                if (otok < T) {
-                    const float d = *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4) + din[it];
-                    const float inv = d > 0.f ? 1.f / d : 0.f;
-                    *reinterpret_cast<uint4*>(o + (head_row + otok) * DV + 8 * i) =
-                        make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
-                                   pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
-                }
+                den[it] += *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
             }
+            // every reader of slot r is past its last read once rd_sync completes
             mbar_arrive(&rd_sync);
             if (!__all_sync(0xffffffffu, mbar_wait(&rd_sync, kr & 1, &abort_flag, kWaitNs))) {
                 fail();
                 break;
             }
-            if (er == 0 && kr + K::RS < nk) mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
-            if (er < K::CS) mbar_arrive_remote(cluster_addr(&peer_free[r], er));
+            if (er == 0 && kr + K::RS < nk) {
+                mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
+                fence_proxy_async_smem();
+                stage_intra(kr + K::RS);
+            }
+            if (er < K::CS) mbar_arrive_remote_relaxed(cluster_addr(&peer_free[r], er));
+#pragma unroll
+            for (int it = 0; it < kRedIt; ++it) {
+                const int idx = er + 64 * it;
+                const int lr = idx % my_rows, i = idx / my_rows;
+                const int otok = (c0 + kr) * kChunk + r0 + lr;
+                if (idx < items && otok < T) {
+                    const float inv = den[it] > 0.f ? 1.f / den[it] : 0.f;
+                    const float* a = acc[it];
+                    *reinterpret_cast<uint4*>(o + (head_row + otok) * DV + 8 * i) =
+                        make_uint4(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv),
+                                   pack_bf16x2(a[4] * inv, a[5] * inv), pack_bf16x2(a[6] * inv, a[7] * inv));
+                }
+            }
         }
+        // no bulk copy may still be landing in shared memory when the CTA exits
+        if (er == 0)
+            for (int kr = consumed; kr < staged; ++kr) mbar_wait_quiet(&intra_full[kr % K::RS], (kr / K::RS) & 1, kWaitNs);
     }
     if (t == 416) {
         // =============================================================== TMA producer
@@ -842,8 +912,13 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     if (tl == 0 && kk >= 1 && !wait(&state_read, (kk - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ss_w(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        if constexpr (K::AKT)
+                            mma_ts_w(tb + K::tm_s + 64 * tl, tb + K::tm_ak + 64 * tl + 8 * ks, dv + ks * kStepMN, id_upd, 1u);
+                        else
+                            mma_ss_w(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN,
+                                     id_upd, 1u);
+                    }
                     mma_commit_w(&ak_free[tl]);
                 }
                 if (!ok) { fail(); break; }
@@ -855,7 +930,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ss_w(tb + K::tx_s, d_ak + kstep(kAtomD, ks), dv + ks * kStepMN, id_upd, 1u);
+                for (int ks = 0; ks < 8; ++ks) mma_ts_w(tb + K::tx_s, tb + K::tx_ak + 8 * ks, dv + ks * kStepMN, id_upd, 1u);
                 // Z += sum over the blocks of (rows of the block)^T (rows of the block)
 #pragma unroll
                 for (int blk = 0; blk < LG; ++blk)
@@ -875,7 +950,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (extra && !wait(&qs_full[kk % nq], (kk / nq) & 1)) { fail(); break; }
             tc_fence_after();
             if (!extra) {
-                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 128 * slot;
+                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 64 * K::TPC * slot;
 #pragma unroll
                 for (int tl = 0; tl < K::TPC; ++tl)
 #pragma unroll
@@ -915,9 +990,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 // Every chunk on its own (no state): for the 128 queries of a chunk,
 //   P = (Q Kh^T) o (Q Kh^T) o M   (bf16, M the causal mask s <= t)
 //   Y = P V,  d = rowsum(P)       (fp32 accumulation)
-// Y goes out as bf16 rows [BH][T][DV] and d, the rows' intra-chunk
-// normaliser, as fp32 [BH][T]; the fused forward adds both when it writes a
-// chunk's outputs.  The chunk's unit keys also go out transposed, kT
+// Y goes out as bf16 rows [BH][Tc][DV] and d, the rows' intra-chunk
+// normaliser, as fp32 [BH][Tc] (Tc = T rounded up to whole chunks; rows past
+// T are not written); the fused forward adds both when it writes a chunk's
+// outputs.  The chunk's unit keys also go out transposed, kT
 // [BH][chunks][P][128] bf16 (zeros past T): the fused forward's key lift
 // reads them.  d sums exactly the rounded weights Y is built from, which
 // keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
@@ -941,6 +1017,8 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     const int row = blockIdx.x * kChunk + t;
     const bool valid = row < T;
     const int64_t grow = bh * T + (valid ? row : 0);
+    // y and d rows: T rounded up to whole chunks per head
+    const int64_t prow = bh * (int64_t)(gridDim.x * kChunk) + row;
     if (t == 0) {
         mbar_init(&bar, 1);
         mbar_init(&drain, 1);
@@ -1116,14 +1194,14 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         for (int c = 0; c < DV; c += 16) tmem_ld16(tmem_addr(tb, lane0, 64 + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
         tmem_wait_ld();
         if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(y_out + grow * DV);
+            uint4* dst = reinterpret_cast<uint4*>(y_out + prow * DV);
 #pragma unroll
             for (int i = 0; i < DV / 8; ++i)
                 dst[i] = make_uint4(pack_bf16x2(__uint_as_float(y[8 * i]), __uint_as_float(y[8 * i + 1])),
                                     pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
                                     pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
                                     pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
-            d_out[grow] = den;
+            d_out[prow] = den;
         }
     } else if (t == 0) {
         atomicOr(&g_chunked_tc_status, kStatusTimeout);
@@ -1200,8 +1278,8 @@ IntraWs intra_ws(int BH, int T, int p, int dv) {
     const size_t nch = (size_t)(T + kChunk - 1) / kChunk;
     IntraWs w;
     w.y_off = 0;
-    w.d_off = up((size_t)BH * T * dv * 2);
-    w.kt_off = w.d_off + up((size_t)BH * T * 4);
+    w.d_off = up((size_t)BH * nch * kChunk * dv * 2);
+    w.kt_off = w.d_off + up((size_t)BH * nch * kChunk * 4);
     w.total = w.kt_off + up((size_t)BH * nch * p * kChunk * 2);
     return w;
 }

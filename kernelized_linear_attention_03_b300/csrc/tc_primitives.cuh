@@ -81,15 +81,20 @@ constexpr uint32_t kSleepHintNs = 20000;
 // Wait for the phase with the given parity to complete, for at most
 // `budget_ns` of wall time; also gives up as soon as *abort is non-zero.
 // Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t budget_ns) {
-    if (mbar_test(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            uint64_t budget_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_test_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t budget_ns) {
+    if (mbar_test(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, budget_ns);
 }
 
 // Wait without an abort flag, for at most `budget_ns` (used on the way out of
@@ -128,16 +133,21 @@ __device__ __forceinline__ bool mbar_test_cluster_sleep(uint64_t* bar, uint32_t 
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t budget_ns) {
-    if (*abort) return false;
-    if (mbar_test_cluster(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                    uint64_t budget_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_test_cluster_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > budget_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t budget_ns) {
+    if (*abort) return false;
+    if (mbar_test_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_slow(bar, parity, abort, budget_ns);
 }
 
 // Shared::cluster address of `p` (a shared variable of this CTA) in the CTA
@@ -151,6 +161,15 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
 // Arrive (release at cluster scope) on a barrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr)
+                 : "memory");
+}
+
+// Arrive on a barrier of another CTA without release semantics: for a
+// hand-back whose caller has already ordered its own accesses (an acquire of
+// a CTA barrier that every reader arrived on after its last read), so the
+// arrive need not wait for this thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr)
                  : "memory");
 }
 
@@ -222,6 +241,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, in
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory; the barrier counts the
+// bytes when they land.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 
