@@ -104,8 +104,10 @@ KATA_API size_t kata_chunked_workspace_bytes(kata_dtype dtype, int B, int H, int
  *     256-byte aligned; contents on entry are ignored.  The call owns it
  *     until the stream reaches the end of the call.
  * bf16 inputs run on the tensor cores: a first kernel computes every
- * chunk's local C x C part and the chunk's transposed unit keys into the
- * workspace, then one fused kernel carries the running state on chip and
+ * chunk's local C x C part (into fp32 accumulation rows of the workspace)
+ * and the chunk's transposed unit keys, then a state kernel carries each
+ * 128-slot tile of the running state on chip and adds the tile's share of
+ * every readout to the accumulation rows, and a last pass divides and
  * writes the outputs.  Every kernel of the call runs on `stream`.
  * Results do not depend on C or mode beyond fp32 rounding.
  */

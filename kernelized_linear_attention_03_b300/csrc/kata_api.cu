@@ -92,8 +92,8 @@ ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C, int64_t n_lift =
     return w;
 }
 
-// bf16 inputs take the fused tensor-core forward when its cluster can be
-// scheduled on the current device; its workspace holds one start state per
+// bf16 inputs take the tensor-core forward when its kernels can run on the
+// current device; its workspace holds one start state per
 // segment when the sequence is cut into G > 1 segments.
 struct TcPlan {
     bool use = false;

@@ -27,15 +27,16 @@ cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* 
                              int p, int dv, int L, int NS, int NS_out, int prefix, cudaStream_t s);
 unsigned int states_tc_take_status();
 
-// Fused chunked forward on the tensor cores (bf16), one cluster per (head,
-// segment).  chunked_tc_segments() gives the number of segments G the
-// sequence is cut into on the current device (0 if the kernel's cluster
-// cannot be scheduled there); chunked_tc_segment_chunks() the 128-token
+// Chunked forward on the tensor cores (bf16): one CTA per (head, segment,
+// 128-slot tile of the lift).  chunked_tc_segments() gives the number of
+// segments G the sequence is cut into on the current device (0 if the
+// kernel cannot run there); chunked_tc_segment_chunks() the 128-token
 // chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
 // start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
 // `intra` is chunked_tc_intra_bytes() of device scratch (256-byte aligned)
-// for the intra-chunk rows, their normalisers and the transposed unit keys,
-// which a first kernel writes and the fused kernel reads.
+// for the fp32 accumulation rows of the numerators and denominators and
+// the transposed unit keys: the intra-chunk kernel initialises them, the
+// state kernel adds to them, a last pass divides.
 // lg: blocks of the lift (1: the full lift; 2 or 4: KATA-Sigma-g with
 // blocks of p / lg); chunked_tc_supports() tells which (p, dv, lg) exist.
 bool chunked_tc_supports(int p, int dv, int lg);

@@ -1,7 +1,7 @@
 // Exact O(T) chunked-state KATA forward on the tcgen05 tensor cores (bf16
-// inputs, fp32 accumulation): the chunked-scan paragraph's decomposition
-// fused into one kernel per (head, segment), with the running state kept on
-// chip instead of being written to memory per chunk.
+// inputs, fp32 accumulation): the chunked-scan paragraph's decomposition with
+// the running state kept on chip instead of being written to memory per
+// chunk.
 //
 // Per chunk of 128 tokens, with S the state before the chunk, Z = sum k k^T
 // over the same tokens (the p x p form of the normaliser z: psi(q)^T z =
@@ -11,22 +11,18 @@
 //   o = Y / d;   S += psiK(Kh)^T V;   Z += Kh^T Kh
 // Q is used as given (its norm cancels between Y and d); Kh are the unit keys.
 //
-// The state of one head (n x dv fp32, n = p(p+1)/2) is spread over a
-// thread-block cluster.  Each "tile CTA" owns one or two 128-slot tiles of
-// the packed lift; it keeps its state rows in tensor memory (fp32,
-// accumulated by the update MMA) and a bf16 copy in shared memory (B operand
-// of the readout MMA).  Its query lift goes to tensor memory (A operand of
-// the readout), its key lift (A operand of the update, built one slot per
-// thread from the chunk's transposed unit keys) to tensor memory as well
-// where the columns allow (one tile per CTA), else to shared memory.  The
-// "extra CTA" owns the last, partly filled tile and Z (the inter-chunk
-// denominator).  Each CTA's partial Y (128 x dv, sent as bf16) is summed in
-// distributed shared memory: tile CTA r owns rows [r*R, r*R + R) of the
-// chunk, receives the partials of those rows from every CTA of the cluster
-// (a ring of RS chunks), adds the rows' intra-chunk part and writes the
-// outputs.  The intra-chunk part of every chunk, and the transposed unit
-// keys the key lift reads, come from a kernel that runs first.
-#include <cooperative_groups.h>
+// Three kernels.  The intra-chunk kernel computes every chunk's local part
+// (the masked squared scores times V, and their row sums) into fp32
+// accumulation rows Y[BH][Tc][dv], d[BH][Tc], and the chunk's unit keys
+// transposed for the key lift.  The state kernel then runs one CTA per
+// (head, segment, 128-slot tile of the packed lift): the CTA keeps its tile
+// of the state (128 x dv fp32) in tensor memory and a bf16 copy in shared
+// memory, lifts the chunk's keys and queries for its slots into tensor
+// memory, updates its state rows and adds its partial readout psiQ(Q) S_tile
+// to Y with a TMA reduce-add.  One more CTA per (head, segment) keeps Z and
+// adds the inter-chunk denominators to d.  The CTAs of a head
+// share nothing but the accumulation rows, so they need no cluster and fill
+// the GPU independently.  A last pass writes o = Y / d.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,24 +40,20 @@ namespace kata {
 namespace {
 
 using namespace tc;
-namespace cg = cooperative_groups;
 
 __device__ unsigned int g_chunked_tc_status = 0;
 
-
-constexpr int kThreads = 512;  // warpgroups: query lift and readout, state epilogue, key lift, MMA
+constexpr int kThreads = 512;  // warpgroups: query lift and output, state epilogue, key lift, MMA and loads
 // Register split between the warpgroups after launch (setmaxnreg): the MMA
 // warpgroup gives back registers that the query warpgroup takes.
 // 128 * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma) must not exceed
 // 512 * (registers per thread at launch); the launcher checks that.
-constexpr uint32_t kRegsLift = 152, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 104;
+constexpr uint32_t kRegsLift = 168, kRegsState = 128, kRegsLaunch = 128, kRegsMma = 88;
 constexpr int kChunk = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes
 constexpr float kSqrt2f = 1.41421356237309504880f;
 constexpr float kInvSqrt2f = 0.70710678118654752440f;
-
-__host__ __device__ constexpr uint32_t round16(uint32_t x) { return (x + 15u) & ~15u; }
 
 // P: width of q and k; LG: blocks of the lift (1: the full lift; g > 1: the
 // KATA-Sigma-g lift, the sum of the g block lifts of width M = P / g).
@@ -71,66 +63,35 @@ struct Cfg {
     static constexpr int n = lift::packed_n(M);
     static constexpr int NT = n / 128;                 // full tiles
     static constexpr int TAIL = n - 128 * NT;          // slots of the last tile (8, 16 or 32)
-    static constexpr int TPC = M == 64 ? 2 : 1;        // tiles per tile CTA
-    static constexpr int NTC = NT / TPC;               // tile CTAs
-    static constexpr int CS = NTC + 1;                 // cluster size
-    static constexpr int R = kChunk / NTC;             // output rows owned per tile CTA (the extra CTA owns none)
+    static constexpr int CS = NT + 2;                  // CTAs per head and segment: one per tile, one for Z
     // transposed unit keys of a chunk: two 64-token boxes of P rows x 128 bytes
     static constexpr uint32_t kt_box = P * 128;
     static constexpr uint32_t kt_bytes = 2 * kt_box;
-    // the tile CTA's key lift: tensor memory with one tile per CTA, shared
-    // memory with two (their state, query lift double buffer and partial
-    // readouts leave no columns for it)
-    static constexpr bool AKT = TPC == 1;
-    // shared memory, in 16 KB atoms from a 1024-byte aligned base
-    //   tile CTA : [key lift, two 64-token atoms per tile, unless AKT], V x2,
-    //              bf16 state [TPC], query stage, transposed-key stages x2
-    //   extra CTA: V x2, bf16 tail state, bf16 Z, query stages x2,
-    //              transposed-key stages x2, one spare atom (the M = 128
-    //              reads of the Z update run past the last stage)
-    static constexpr uint32_t ak_atoms = AKT ? 0 : 2 * TPC;
-    static constexpr uint32_t t_ak = 0, t_v = ak_atoms * kAtom, t_s16 = t_v + 2 * kAtom, t_q = t_s16 + TPC * kAtom,
-                              t_kt = t_q + kAtom;
-    static constexpr uint32_t x_v = 0, x_s16 = 2 * kAtom, x_z16 = 3 * kAtom, x_q = 4 * kAtom, x_kt = 6 * kAtom;
-    static constexpr uint32_t atoms_tile = ak_atoms + TPC + 5, atoms_extra = 9;
-    // partial readouts received by a tile CTA: one part per (source CTA,
-    // receive slot) = R rows of bf16 laid out [DV/8][R] x 16 bytes (a warp's
-    // store of one column group is contiguous per owner), then R fp32
-    // denominators (extra CTA's part only)
-    static constexpr uint32_t part_y = R * DV * 2;
-    static constexpr uint32_t recv_part = part_y + round16(R * 4);
-    static constexpr uint32_t recv_buf = CS * recv_part;
-    static constexpr uint32_t recv_off = atoms_tile * kAtom;
-    // the owned rows' intra-chunk part, staged by a bulk copy per chunk: R
-    // rows of bf16, then R fp32 normalisers
-    static constexpr uint32_t intra_slot = R * DV * 2 + round16(R * 4);
-    // receive slots (chunks in flight, each with its intra-chunk stage):
-    // three where they fit beside the static shared memory
-    static constexpr uint32_t kStaticReserve = 1024 + 3072;
-    static constexpr int RS = recv_off + 3 * (recv_buf + intra_slot) + kStaticReserve <= 232448 ? 3 : 2;
-    static constexpr uint32_t intra_off = recv_off + RS * recv_buf;
-    static constexpr uint32_t tile_end = intra_off + RS * intra_slot;
-    static constexpr uint32_t total = tile_end > atoms_extra * kAtom ? tile_end : atoms_extra * kAtom;
+    // partial readout staged for the reduce-add: YH boxes of 128 rows x YW
+    // fp32 columns (128-byte rows for YW = 32)
+    static constexpr int YW = DV < 32 ? DV : 32;
+    static constexpr int YH = DV / YW;
+    static constexpr uint32_t y_box = 128 * YW * 4;
+    static constexpr uint32_t y_stage = YH * y_box;
+    // shared memory, in 16 KB atoms from a 1024-byte aligned base: V x2,
+    // bf16 state, query stages x2, bf16 Z (normaliser CTA), transposed-key
+    // stages x2, one spare atom (the M = 128 reads of the Z update run past
+    // the last stage), then two partial-readout stages
+    static constexpr uint32_t o_v = 0, o_s16 = 2 * kAtom, o_q = 3 * kAtom, o_z16 = 5 * kAtom, o_kt = 6 * kAtom,
+                              o_y = 9 * kAtom;
+    static constexpr uint32_t total = o_y + 2 * y_stage;
     static constexpr size_t smem = total + 1024;
-    // tensor memory columns, tile CTA
-    static constexpr uint32_t tm_s = 0;                                // TPC x 64: fp32 state
-    static constexpr uint32_t tm_ak = 64 * TPC;                        // AKT: 64, key lift (bf16 pairs of tokens)
-    static constexpr uint32_t tm_aq = AKT ? 128 * TPC : 64 * TPC;      // 2 slots x TPC x 64: query lift
-    static constexpr uint32_t tm_y = tm_aq + 128 * TPC;                // 2 slots x 64: partial readout
-    // tensor memory columns, extra CTA
-    static constexpr uint32_t tx_s = 0;      // tail state
-    static constexpr uint32_t tx_aq = 64;    // 2 slots x 32: tail query lift
-    static constexpr uint32_t tx_y = 128;    // 2 slots x 64: partial readout
-    static constexpr uint32_t tx_ak = 256;   // 64: tail key lift (lanes past the tail hold zeros)
-    static constexpr uint32_t tx_w = 384;    // Q Z
-    static constexpr uint32_t tx_z = 448;    // Z
-    static_assert(NT % TPC == 0, "tiles must split evenly");
-    static_assert(tm_y + 128 <= 512, "tensor memory columns");
+    // tensor memory columns
+    static constexpr uint32_t tm_s = 0;      // 64: fp32 state tile
+    static constexpr uint32_t tm_ak = 64;    // 64: key lift (bf16 pairs of tokens); the last tile's lanes past the tail hold zeros
+    static constexpr uint32_t tm_aq = 128;   // 2 slots x 64: query lift (bf16 pairs of slots)
+    static constexpr uint32_t tm_y = 256;    // 2 slots x 64: partial readout
+    static constexpr uint32_t tm_w = 384;    // normaliser CTA: Q Z
+    static constexpr uint32_t tm_z = 448;    // normaliser CTA: Z
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
-    static_assert(total + kStaticReserve <= 232448, "shared memory");
-    static_assert(R * NTC == kChunk, "owned rows");
+    static_assert(total + 4096 <= 232448, "shared memory");
     static_assert(kt_bytes <= kAtom, "transposed-key stage");
-    static_assert((R * DV * 2) % 16 == 0 && (R * 4) % 16 == 0 && intra_off % 16 == 0, "bulk copy sizes");
+    static_assert(DV % YW == 0 && DV <= 64, "value width");
 };
 
 // ---------------------------------------------------------------- key lift, one slot per thread
@@ -163,24 +124,6 @@ __device__ __forceinline__ uint4 key_words(const uint8_t* kts, int i, int j, int
         }
     }
     return r;
-}
-
-// Row `row` of a K-major shared-memory operand tile (two 64-token atoms of
-// 128 rows x 128 bytes, 128-byte swizzle) receives the key lift of slot
-// `slot`; slots past n give zeros.
-template <int P, int LG>
-__device__ __forceinline__ void key_row_smem(const uint8_t* kts, int slot, uint8_t* ak, int row) {
-    constexpr int n = lift::packed_n(P / LG);
-    uint8_t* dst0 = ak + (row >> 3) * 1024 + (row & 7) * 128;
-    const bool live = slot < n;
-    int i = 0, j = 0;
-    if (live) lift::slot_coord(P / LG, slot, i, j);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(dst0 + h * kAtom + ((c ^ (row & 7)) << 4)) =
-                live ? key_words<P, LG>(kts, i, j, h, c) : make_uint4(0, 0, 0, 0);
 }
 
 // Lane `slot % 128` of a tensor-memory operand (64 columns, column c = the
@@ -291,28 +234,6 @@ __device__ __forceinline__ void load_state_tile(const float* S_start, int tau, u
     }
 }
 
-// Refresh the bf16 copy of lane t of a state tile from tensor memory.
-template <int DV>
-__device__ __forceinline__ void refresh_state_tile(uint32_t taddr, uint8_t* S16, int t) {
-#pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + c0, r);
-        tmem_wait_ld();
-        uint4 a, b;
-        a.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
-        a.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
-        a.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
-        a.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-        b.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
-        b.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
-        b.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
-        b.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
-        *reinterpret_cast<uint4*>(S16 + mn_sw128_chunk(c0, t, kAtom)) = a;
-        *reinterpret_cast<uint4*>(S16 + mn_sw128_chunk(c0 + 8, t, kAtom)) = b;
-    }
-}
-
 // Write lane t of a state tile to the C ABI's packed order (sqrt(2) restored).
 template <int P, int DV>
 __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t taddr, int t) {
@@ -340,107 +261,90 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 }
 
 
-// ---------------------------------------------------------------- kernel
-// Warp roles (512 threads, four warpgroups):
-//   warps 0-3   query:    thread t = token t of the chunk; reads its staged
-//                         query row, writes the query lift (tensor memory,
-//                         the A operand of the readout); then, one chunk
-//                         behind, reads lane t of the partial readout and
-//                         sends the row to the tile CTA that owns it
-//   warps 4-7   state:    thread e = tensor-memory lane e; reads the state
-//                         after each update and releases it to the next update,
-//                         refreshes the bf16 copy for the next readout (extra
-//                         CTA: also Z and the rows' inter-chunk denominators)
-//   warps 8-11  key lift: thread e = slot e of each tile; multiplies two rows
-//                         of the chunk's transposed unit keys into row e of
-//                         the update's A operand (shared memory, K-major)
-//   warps 12-15 warp 12 lane 0 issues every tcgen05.mma, warp 13 lane 0 the
-//                         TMA loads; warps 14-15 reduce the owned rows, add
-//                         the intra-chunk part and store the outputs
-// Per chunk the MMAs run update tile by tile (state += lift(K)^T V; each
-// tile's key-lift rows are released as soon as its MMAs are done, so the
-// next chunk's lift of that tile overlaps the rest) and then the readout
-// (Y = lift(Q) S) of the state before the chunk.
+// ---------------------------------------------------------------- state kernel
+// CTA kinds, by tile index tau: tau < NT a full 128-slot tile of the lift;
+// tau = NT the last, partly filled tile (TAIL slots); tau = NT + 1 the
+// normaliser CTA, which keeps Z and adds the inter-chunk denominators
+// q^T Z q to d (no state tile).
+// Warp roles (512 threads, four warpgroups); thread e of a warpgroup is
+// tensor-memory lane e:
+//   warps 0-3   query:    lane = token; lifts its staged query row for this
+//                         CTA's slots into tensor memory (A operand of the
+//                         readout); one chunk behind, reads the token's
+//                         partial readout, stages it in shared memory and
+//                         (one thread) adds the chunk's rows to Y by TMA
+//   warps 4-7   state:    lane = slot; after each update reads the state row
+//                         and releases it to the next update, then refreshes
+//                         the bf16 copy the next readout reads (normaliser
+//                         CTA: the same for Z, and the denominators)
+//   warps 8-11  key lift: lane = slot; multiplies two rows of the chunk's
+//                         transposed unit keys into the update's A operand
+//   warp 12     MMA:      per chunk the update (state += lift(K)^T V) and the
+//                         readout (Y = lift(Q) S) of the state before the
+//                         chunk (normaliser CTA: Z += Kh^T Kh and W = Q Z); the
+//                         whole warp runs the loop, one elected lane issues
+//   warp 13     loads:    lane 0 issues the TMA loads (transposed keys, values,
+//                         queries)
 template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkt,
-                  const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
-                  const __nv_bfloat16* __restrict__ y_intra, const float* __restrict__ d_intra,
-                  const float* __restrict__ S_start, const float* __restrict__ z_start, int start_groups,
-                  float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmy,
+                  float* __restrict__ dacc, const float* __restrict__ S_start, const float* __restrict__ z_start,
+                  int start_groups, float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV, LG>;
     constexpr int n = K::n, M = K::M;
-    cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qs_full[2], qs_free[2], kts_full[2], kts_free[2], v_full[2], v_free[2];
-    __shared__ uint64_t klift_full[2], ak_free[2], qlift_full[2], aq_free[2];
-    __shared__ uint64_t y_part[2], y_free[2], den_ready[2];
-    __shared__ uint64_t upd_done, state_read, s16_ready, drain, rd_sync;
-    __shared__ uint64_t recv_full[K::RS], peer_free[K::RS];
-    __shared__ uint64_t local_full[K::RS];  // this CTA's own partial rows written (one arrival per row)
-    __shared__ uint64_t intra_full[K::RS];  // the owned rows' intra-chunk part staged
-    __shared__ float dens[2][kChunk];       // extra CTA: inter-chunk denominators of the chunk rows
+    __shared__ uint64_t qlift_full[2], aq_free[2], y_part[2], y_free[2], ys_full[2], ys_free[2];
+    __shared__ uint64_t klift_full, ak_free, upd_done, state_read, s16_ready, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int t = threadIdx.x, warp = t >> 5;
-    const int rank = (int)cluster.block_rank();
-    const bool extra = rank == K::NTC;
-    const int g = blockIdx.x / K::CS;
+    const int tau = blockIdx.x % K::CS;  // tile of the packed lift (NT + 1: the normaliser CTA)
+    const int g = blockIdx.x / K::CS;    // segment
     const int G = gridDim.x / K::CS;
+    const bool tail = tau == K::NT;      // the last, partly filled tile
+    const bool zc = tau == K::NT + 1;    // Z and the denominators
     const int64_t bh = blockIdx.y;
     const int NCH = (T + kChunk - 1) / kChunk;
+    const int64_t head_prow = bh * (int64_t)NCH * kChunk;  // accumulation rows: whole chunks per head
     const int c0 = g * seg_chunks, c1 = min(NCH, c0 + seg_chunks);
     const int nk = c1 - c0;
-    const int my_rows = extra ? 0 : K::R;
-    // bytes of partial rows (and the extra CTA's denominators) other CTAs
-    // deliver per chunk
-    const uint32_t rx_bytes = (K::CS - 1) * my_rows * DV * 2 + my_rows * 4;
-    const int nq = extra ? 2 : 1;  // query stages (the extra CTA's MMAs read the queries in place)
-    uint8_t* const s_ak = sm + K::t_ak;  // tile CTA key lift, when it lives in shared memory
-    uint8_t* const s_s16 = sm + (extra ? K::x_s16 : K::t_s16);
-    uint8_t* const s_z16 = sm + K::x_z16;
-    uint8_t* const s_recv = sm + K::recv_off;
-    auto v_buf = [&](int kk) { return sm + (extra ? K::x_v : K::t_v) + (kk & 1) * kAtom; };
-    auto q_buf = [&](int s) { return sm + (extra ? K::x_q : K::t_q) + s * kAtom; };
-    auto kt_buf = [&](int s) { return sm + (extra ? K::x_kt : K::t_kt) + s * kAtom; };
+    uint8_t* const s_s16 = sm + K::o_s16;
+    uint8_t* const s_z16 = sm + K::o_z16;
+    auto v_buf = [&](int kk) { return sm + K::o_v + (kk & 1) * kAtom; };
+    auto q_buf = [&](int kk) { return sm + K::o_q + (kk & 1) * kAtom; };
+    auto kt_buf = [&](int kk) { return sm + K::o_kt + (kk & 1) * kAtom; };
+    auto y_buf = [&](int kk) { return sm + K::o_y + (kk & 1) * K::y_stage; };
 
     if (t == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&qs_full[b], 1);
-            // the staged queries are read by the query warps and, in the extra
-            // CTA, by the state warps (after the Q Z product that reads them too)
-            mbar_init(&qs_free[b], extra ? 256 : 128);
+            // the staged queries are read by the query warps (tiles) or by the
+            // state warps after the Q Z product that reads them too (normaliser)
+            mbar_init(&qs_free[b], 128);
             mbar_init(&kts_full[b], 1);
-            // the staged keys are read by the key-lift warps and, in the extra
-            // CTA, by the Z update (one commit)
-            mbar_init(&kts_free[b], extra ? 129 : 128);
+            // the staged keys are read by the key-lift warps (tiles) or by the
+            // Z update (normaliser, one commit)
+            mbar_init(&kts_free[b], zc ? 1 : 128);
             mbar_init(&v_full[b], 1);
             mbar_init(&v_free[b], 1);
-            mbar_init(&klift_full[b], 128);
-            mbar_init(&ak_free[b], 1);
             mbar_init(&qlift_full[b], 128);
             mbar_init(&aq_free[b], 1);
             mbar_init(&y_part[b], 1);
             mbar_init(&y_free[b], 128);
-            mbar_init(&den_ready[b], 128);
+            mbar_init(&ys_full[b], 128);
+            mbar_init(&ys_free[b], 1);
         }
+        mbar_init(&klift_full, 128);
+        mbar_init(&ak_free, 1);
         mbar_init(&upd_done, 1);
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
         mbar_init(&drain, 1);
-        mbar_init(&rd_sync, 64);
-        for (int b = 0; b < K::RS; ++b) {
-            mbar_init(&recv_full[b], 1);
-            mbar_init(&peer_free[b], K::NTC);  // one arrival per owner
-            mbar_init(&local_full[b], my_rows > 0 ? my_rows : 1);
-            mbar_init(&intra_full[b], 1);
-        }
         fence_mbar_init();
-        // the first RS chunks' partial rows may arrive as soon as the cluster starts
-        if (my_rows > 0)
-            for (int b = 0; b < K::RS && b < nk; ++b) mbar_arrive_expect_tx(&recv_full[b], rx_bytes);
         abort_flag = 0;
     }
     if (warp == 0) {
@@ -462,22 +366,16 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag, kWaitNs));
     };
-    auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, &abort_flag, kWaitNs));
-    };
 
-    // ---- start state of this segment (state warps: lane = slot / dim)
+    // ---- start state of this segment (state warps: lane = slot / dimension)
     if (warp >= 4 && warp < 8) {
         const int e = t - 128;
         const int sg = start_groups > 1 ? g : 0;
-        const float* S0 = S_start ? S_start + (bh * start_groups + sg) * (int64_t)n * DV : nullptr;
-        const float* z0 = z_start ? z_start + (bh * start_groups + sg) * (int64_t)n : nullptr;
-        if (!extra) {
-#pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl)
-                load_state_tile<M, DV>(S0, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), s_s16 + tl * kAtom, e);
+        if (!zc) {
+            const float* S0 = S_start ? S_start + (bh * start_groups + sg) * (int64_t)n * DV : nullptr;
+            load_state_tile<M, DV>(S0, tau, tm(K::tm_s), s_s16, e);
         } else {
-            load_state_tile<M, DV>(S0, K::NT, tm(K::tx_s), s_s16, e);
+            const float* z0 = z_start ? z_start + (bh * start_groups + sg) * (int64_t)n : nullptr;
             float zr[M];
 #pragma unroll
             for (int j = 0; j < M; ++j) {
@@ -493,7 +391,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 uint32_t r[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(zr[c + i]);
-                tmem_st16(tm(K::tx_z + c), r);
+                tmem_st16(tm(K::tm_z + c), r);
             }
             if (e < M) {
 #pragma unroll
@@ -505,34 +403,32 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         }
         tmem_wait_st();
     }
-    // the extra CTA's tail key lift fills lanes [0, 32) of its operand; the
-    // other lanes are read by the tail update's M = 128 MMAs into state rows
-    // nothing reads, and are kept at zero
-    if (extra && warp >= 9 && warp < 12) {
+    // the last tile's key lift fills lanes [0, 32) of its operand; the other
+    // lanes are read by its M = 128 update into state rows nothing reads, and
+    // are kept at zero
+    if (tail && warp >= 9 && warp < 12) {
         uint32_t zw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) zw[i] = 0u;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_st16(tm(K::tx_ak + c), zw);
+        for (int c = 0; c < 64; c += 16) tmem_st16(tm(K::tm_ak + c), zw);
         tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    cluster.sync();  // barriers initialised and start state in place cluster-wide
+    __syncthreads();  // barriers initialised and start state in place
     tc_fence_after();
 
     if (warp < 4) {
         // =============================================================== query warps
         regs_inc<kRegsLift>();
         const int e = t;
-        const int owner = e / K::R, orow = e % K::R;
         // query lift of chunk kk into its tensor-memory slot (double-buffered:
         // overlaps the previous chunk's readout)
         auto lift_q = [&](int kk) -> bool {
             const int slot = kk & 1, use = kk >> 1;
-            const int stg = kk % nq, stg_use = kk / nq;
-            if (!wait(&qs_full[stg], stg_use & 1)) return false;
-            const uint8_t* my_q = q_buf(stg) + t * 128;
+            if (!wait(&qs_full[slot], use & 1)) return false;
+            const uint8_t* my_q = q_buf(kk) + t * 128;
             uint32_t uq[P / 2];
 #pragma unroll
             for (int i = 0; i < P / 8; ++i) {
@@ -542,70 +438,66 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 uq[4 * i + 2] = a.z;
                 uq[4 * i + 3] = a.w;
             }
-            mbar_arrive(&qs_free[stg]);
+            mbar_arrive(&qs_free[slot]);
             if (kk >= 2 && !wait(&aq_free[slot], (use - 1) & 1)) return false;
             tc_fence_after();
-            if (!extra) {
-#pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
-                    query_dispatch<P, LG>(rank * K::TPC + tl, uq, tm(K::tm_aq + 64 * K::TPC * slot + 64 * tl));
-            } else {
-                query_tail<P, LG>(uq, tm(K::tx_aq + 32 * slot));
-            }
+            if (!tail)
+                query_dispatch<P, LG>(tau, uq, tm(K::tm_aq + 64 * slot));
+            else
+                query_tail<P, LG>(uq, tm(K::tm_aq + 64 * slot));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&qlift_full[slot]);
             return true;
         };
-        // this lane's partial readout of chunk c0 + kc -> its owner (the extra
-        // CTA adds the row's inter-chunk denominator)
-        auto send = [&](int kc) -> bool {
+        // this lane's partial readout of chunk c0 + kc -> the stage; thread 0
+        // adds the stage to the chunk's accumulation rows
+        auto out = [&](int kc) -> bool {
             const int slot = kc & 1, use = kc >> 1;
-            const int rs = kc % K::RS, ruse = kc / K::RS;
             if (!wait(&y_part[slot], use & 1)) return false;
             tc_fence_after();
-            float den = 0.f;
-            if (extra) {
-                if (!wait(&den_ready[slot], use & 1)) return false;
-                den = dens[slot][e];
-            }
-            uint32_t ypk[DV / 2];
-            const uint32_t ycol = (extra ? K::tx_y : K::tm_y) + 64 * slot;
-            {
-                uint32_t r[DV / 16][16];  // all loads in flight, one wait
+            uint32_t y[DV];
 #pragma unroll
-                for (int c = 0; c < DV / 16; ++c) tmem_ld16(tm(ycol + 16 * c), r[c]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < DV / 16; ++c)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) ypk[8 * c + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1]));
-            }
+            for (int c = 0; c < DV; c += 16) tmem_ld16(tm(K::tm_y + 64 * slot + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&y_free[slot]);
-            // the owners have consumed what this receive slot held RS chunks ago
-            if (kc >= K::RS && !wait_cluster(&peer_free[rs], (ruse - 1) & 1)) return false;
-            uint8_t* recv = s_recv + rs * K::recv_buf;
-            uint8_t* dst = recv + rank * K::recv_part + orow * 16;
-            if (owner == rank) {
+            // the stage's previous contents (chunk kc - 2) have been read by the TMA
+            if (kc >= 2 && !wait(&ys_free[slot], (use - 1) & 1)) return false;
+            uint8_t* stg = y_buf(kc);
 #pragma unroll
-                for (int i = 0; i < DV / 8; ++i)
-                    *reinterpret_cast<uint4*>(dst + i * K::R * 16) = make_uint4(ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3]);
-                if (extra) *reinterpret_cast<float*>(recv + rank * K::recv_part + K::part_y + orow * 4) = den;
-                mbar_arrive(&local_full[rs]);
-            } else {
-                const uint32_t rdst = cluster_addr(dst, owner);
-                const uint32_t rbar = cluster_addr(&recv_full[rs], owner);
+            for (int hh = 0; hh < K::YH; ++hh) {
 #pragma unroll
-                for (int i = 0; i < DV / 8; ++i)
-                    st_async_v4_b32(rdst + i * K::R * 16, ypk[4 * i], ypk[4 * i + 1], ypk[4 * i + 2], ypk[4 * i + 3], rbar);
-                if (extra) st_async_f32(cluster_addr(recv + rank * K::recv_part + K::part_y + orow * 4, owner), den, rbar);
+                for (int c = 0; c < K::YW / 4; ++c) {
+                    const uint32_t off = K::YW == 32 ? (uint32_t)e * 128u + ((uint32_t)(c ^ (e & 7)) << 4)
+                                                     : (uint32_t)e * (K::YW * 4) + (uint32_t)c * 16u;
+                    *reinterpret_cast<uint4*>(stg + hh * K::y_box + off) =
+                        make_uint4(y[hh * K::YW + 4 * c], y[hh * K::YW + 4 * c + 1], y[hh * K::YW + 4 * c + 2],
+                                   y[hh * K::YW + 4 * c + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&ys_full[slot]);
+            if (t == 0) {
+                if (!mbar_wait(&ys_full[slot], use & 1, &abort_flag, kWaitNs)) return false;
+                const int row0 = (c0 + kc) * kChunk;
+#pragma unroll
+                for (int hh = 0; hh < K::YH; ++hh)
+                    tma_reduce_add_3d(&tmy, hh * K::YW, row0, (int)bh, stg + hh * K::y_box);
+                bulk_commit();
+                // the previous chunk's stage has been read: it may be rewritten
+                bulk_wait_read<1>();
+                if (kc >= 1) mbar_arrive(&ys_free[(kc - 1) & 1]);
             }
             return true;
         };
-        for (int kk = 0; kk <= nk; ++kk) {
-            if (kk < nk && !lift_q(kk)) { fail(); break; }
-            if (kk >= 1 && !send(kk - 1)) { fail(); break; }
+        if (!zc) {
+            for (int kk = 0; kk <= nk; ++kk) {
+                if (kk < nk && !lift_q(kk)) { fail(); break; }
+                if (kk >= 1 && !out(kk - 1)) { fail(); break; }
+            }
+            // no reduce-add may still be reading shared memory when the CTA exits
+            if (t == 0) bulk_wait<0>();
         }
     } else if (warp < 8) {
         // =============================================================== state warps
@@ -613,53 +505,50 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         const int e = t - 128;
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            // state after this chunk's update
+            // state (Z) after this chunk's update
             if (!wait(&upd_done, kk & 1)) { fail(); break; }
             tc_fence_after();
-            uint32_t sreg[K::TPC][DV / 2];  // bf16 pairs of this lane's state rows
-            uint32_t zreg[M / 2];           // extra CTA: bf16 pairs of this lane's Z row
-            const int ntl = extra ? 1 : K::TPC;
-#pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl) {
-                if (tl >= ntl) break;
-                const uint32_t scol = extra ? K::tx_s : K::tm_s + 64 * tl;
+            uint32_t sreg[(M > DV ? M : DV) / 2];  // bf16 pairs of this lane's state (Z) row
+            if (!zc) {
 #pragma unroll
                 for (int c32 = 0; c32 < DV; c32 += 32) {
                     uint32_t r[2][16];  // two loads in flight per wait
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        if (c32 + 16 * h < DV) tmem_ld16(tm(scol + c32 + 16 * h), r[h]);
+                        if (c32 + 16 * h < DV) tmem_ld16(tm(K::tm_s + c32 + 16 * h), r[h]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         if (c32 + 16 * h < DV)
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                sreg[tl][(c32 + 16 * h) / 2 + i] =
-                                    pack_bf16x2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1]));
+                                sreg[(c32 + 16 * h) / 2 + i] = pack_bf16x2(__uint_as_float(r[h][2 * i]), __uint_as_float(r[h][2 * i + 1]));
                 }
-            }
-            if (extra) {
+            } else {
 #pragma unroll
                 for (int c16 = 0; c16 < M; c16 += 16) {
                     uint32_t r[16];
-                    tmem_ld16(tm(K::tx_z + c16), r);
+                    tmem_ld16(tm(K::tm_z + c16), r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        zreg[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        sreg[c16 / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                 }
             }
             tc_fence_before();
             mbar_arrive(&state_read);
-            // this chunk's readout is done: its bf16 state copy may be replaced
+            // this chunk's readout (W) is done: its bf16 state (Z) copy may be replaced
             if (!wait(&y_part[slot], use & 1)) { fail(); break; }
             tc_fence_after();
-            float den = 0.f;
-            if (extra) {
+            if (!zc) {
+#pragma unroll
+                for (int c8 = 0; c8 < DV / 8; ++c8)
+                    *reinterpret_cast<uint4*>(s_s16 + mn_sw128_chunk(8 * c8, e, kAtom)) =
+                        make_uint4(sreg[4 * c8], sreg[4 * c8 + 1], sreg[4 * c8 + 2], sreg[4 * c8 + 3]);
+            } else {
                 // inter-chunk denominator q^T Z q from W = Q Z (Z before this chunk)
                 uint4 qrow[P / 8];
-                const uint8_t* sq = q_buf(kk % nq);  // this chunk's staged queries
+                const uint8_t* sq = q_buf(kk);  // this chunk's staged queries
 #pragma unroll
                 for (int i = 0; i < P / 8; ++i) qrow[i] = *reinterpret_cast<const uint4*>(sq + sw128_chunk(e, 8 * i, kChunk));
                 const __nv_bfloat16* qe = reinterpret_cast<const __nv_bfloat16*>(qrow);
@@ -667,52 +556,36 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
                 for (int c16 = 0; c16 < P; c16 += 16) {
                     uint32_t w[16];
-                    tmem_ld16(tm(K::tx_w + c16), w);
+                    tmem_ld16(tm(K::tm_w + c16), w);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) dint = fmaf(__bfloat162float(qe[c16 + i]), __uint_as_float(w[i]), dint);
                 }
-                den = dint;
                 tc_fence_before();
-                mbar_arrive(&qs_free[kk % nq]);  // this chunk's staged queries and W have been read
-            }
-            auto write_s16 = [&](const uint32_t (&x)[DV / 2], int tl) {
+                mbar_arrive(&qs_free[slot]);  // this chunk's staged queries and W have been read
+                atomicAdd(dacc + head_prow + (int64_t)(c0 + kk) * kChunk + e, dint);
+                if (e < M) {
 #pragma unroll
-                for (int c8 = 0; c8 < DV / 8; ++c8)
-                    *reinterpret_cast<uint4*>(s_s16 + tl * kAtom + mn_sw128_chunk(8 * c8, e, kAtom)) =
-                        make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
-            };
-#pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl)
-                if (tl < ntl) write_s16(sreg[tl], tl);
-            if (extra && e < M) {
-#pragma unroll
-                for (int c8 = 0; c8 < M / 8; ++c8)
-                    *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, M)) =
-                        make_uint4(zreg[4 * c8], zreg[4 * c8 + 1], zreg[4 * c8 + 2], zreg[4 * c8 + 3]);
+                    for (int c8 = 0; c8 < M / 8; ++c8)
+                        *reinterpret_cast<uint4*>(s_z16 + sw128_chunk(e, 8 * c8, M)) =
+                            make_uint4(sreg[4 * c8], sreg[4 * c8 + 1], sreg[4 * c8 + 2], sreg[4 * c8 + 3]);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s16_ready);
-            if (extra) {
-                dens[slot][e] = den;
-                mbar_arrive(&den_ready[slot]);
-            }
         }
         // final state of the last segment
         if (S_final != nullptr && g == G - 1 && !abort_flag) {
             const int64_t head_s = bh * (int64_t)n * DV, head_z = bh * (int64_t)n;
-            if (!extra) {
-#pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
-                    store_state_tile<M, DV>(S_final + head_s, rank * K::TPC + tl, tm(K::tm_s + 64 * tl), e);
+            if (!zc) {
+                store_state_tile<M, DV>(S_final + head_s, tau, tm(K::tm_s), e);
             } else {
-                store_state_tile<M, DV>(S_final + head_s, K::NT, tm(K::tx_s), e);
                 uint32_t zr[M];
 #pragma unroll
                 for (int c16 = 0; c16 < M; c16 += 16) {
                     uint32_t r[16];
-                    tmem_ld16(tm(K::tx_z + c16), r);
+                    tmem_ld16(tm(K::tm_z + c16), r);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) zr[c16 + i] = r[i];
                 }
@@ -728,151 +601,46 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     } else if (warp < 12) {
         // =============================================================== key-lift warps
         const int e = t - 256;
-        for (int kk = 0; kk < nk; ++kk) {
-            const int stg = kk & 1, use = kk >> 1;
-            if (!wait(&kts_full[stg], use & 1)) { fail(); break; }
-            const uint8_t* kts = kt_buf(stg);
-            bool ok = true;
-            const int ntl = extra ? 1 : K::TPC;
-#pragma unroll
-            for (int tl = 0; tl < K::TPC; ++tl) {
-                if (tl >= ntl) break;
-                if (kk >= 1 && !wait(&ak_free[tl], (kk - 1) & 1)) { ok = false; break; }
+        if (!zc) {
+            for (int kk = 0; kk < nk; ++kk) {
+                const int stg = kk & 1, use = kk >> 1;
+                if (!wait(&kts_full[stg], use & 1)) { fail(); break; }
+                if (kk >= 1 && !wait(&ak_free, (kk - 1) & 1)) { fail(); break; }
                 tc_fence_after();
-                if (extra) {
-                    if (warp == 8) key_row_tmem<P, LG>(kts, K::NT * 128 + e, tm(K::tx_ak));
-                } else if constexpr (K::AKT) {
-                    key_row_tmem<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, tm(K::tm_ak + 64 * tl));
-                } else {
-                    key_row_smem<P, LG>(kts, (rank * K::TPC + tl) * 128 + e, s_ak + 2 * tl * kAtom, e);
-                }
-                fence_proxy_async_smem();
+                if (!tail || warp == 8) key_row_tmem<P, LG>(kt_buf(kk), tau * 128 + e, tm(K::tm_ak));
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&klift_full[tl]);
+                mbar_arrive(&klift_full);
+                mbar_arrive(&kts_free[stg]);
             }
-            if (!ok) { fail(); break; }
-            mbar_arrive(&kts_free[stg]);
         }
     } else {
         regs_dec<kRegsMma>();
-    }
-    if (warp >= 14 && my_rows > 0) {
-        // =============================================================== reduce warps
-        // owner side, chunk by chunk as the partial rows land: sum them and
-        // the intra-chunk rows (staged by a bulk copy RS chunks ahead), hand
-        // the receive slot back to every sender (its next use is RS chunks
-        // later), then divide and store the outputs
-        constexpr int kRedIt = (K::R * (DV / 8) + 63) / 64;
-        constexpr uint32_t kIntraY = K::R * DV * 2, kIntraBytes = kIntraY + K::R * 4;
-        const int er = t - 448;
-        const int r0 = rank * K::R;
-        const int items = my_rows * (DV / 8);
-        const int64_t head_row = bh * (int64_t)T;                // output rows
-        const int64_t head_prow = bh * (int64_t)NCH * kChunk;    // intra-chunk rows: whole chunks per head
-        uint8_t* const s_intra = sm + K::intra_off;
-        int staged = 0, consumed = 0;  // bulk copies issued / waited for
-        auto stage_intra = [&](int kr) {
-            ++staged;
-            const int r = kr % K::RS;
-            const int64_t row = head_prow + (int64_t)(c0 + kr) * kChunk + r0;
-            uint8_t* dst = s_intra + r * K::intra_slot;
-            mbar_arrive_expect_tx(&intra_full[r], kIntraBytes);
-            bulk_load(dst, y_intra + row * DV, kIntraY, &intra_full[r]);
-            bulk_load(dst + kIntraY, d_intra + row, K::R * 4, &intra_full[r]);
-        };
-        if (er == 0)
-            for (int kr = 0; kr < K::RS && kr < nk; ++kr) stage_intra(kr);
-        for (int kr = 0; kr < nk; ++kr) {
-            const int r = kr % K::RS;
-            const uint32_t par = (kr / K::RS) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&recv_full[r], par, &abort_flag, kWaitNs) &&
-                                             mbar_wait(&local_full[r], par, &abort_flag, kWaitNs) &&
-                                             mbar_wait(&intra_full[r], par, &abort_flag, kWaitNs))) {
-                fail();
-                break;
-            }
-            consumed = kr + 1;
-            const uint8_t* recv = s_recv + r * K::recv_buf;
-            const uint8_t* sin = s_intra + r * K::intra_slot;
-            float acc[kRedIt][8], den[kRedIt];
-#pragma unroll
-            for (int it = 0; it < kRedIt; ++it) {
-                const int idx = er + 64 * it;
-                const int lr = idx % my_rows, i = idx / my_rows;
-                if (idx >= items) continue;
-                const uint4 yin = *reinterpret_cast<const uint4*>(sin + lr * (DV * 2) + i * 16);
-                const __nv_bfloat162* hy = reinterpret_cast<const __nv_bfloat162*>(&yin);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc[it][2 * j] = __low2float(hy[j]);
-                    acc[it][2 * j + 1] = __high2float(hy[j]);
-                }
-                den[it] = *reinterpret_cast<const float*>(sin + kIntraY + lr * 4);
-#pragma unroll
-                for (int src = 0; src < K::CS; ++src) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(recv + src * K::recv_part + (i * K::R + lr) * 16);
-                    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[it][2 * j] += __low2float(h[j]);
-                        acc[it][2 * j + 1] += __high2float(h[j]);
-                    }
-                }
-                den[it] += *reinterpret_cast<const float*>(recv + K::NTC * K::recv_part + K::part_y + lr * 4);
-            }
-            // every reader of slot r is past its last read once rd_sync completes
-            mbar_arrive(&rd_sync);
-            if (!__all_sync(0xffffffffu, mbar_wait(&rd_sync, kr & 1, &abort_flag, kWaitNs))) {
-                fail();
-                break;
-            }
-            if (er == 0 && kr + K::RS < nk) {
-                mbar_arrive_expect_tx(&recv_full[r], rx_bytes);
-                fence_proxy_async_smem();
-                stage_intra(kr + K::RS);
-            }
-            if (er < K::CS) mbar_arrive_remote_relaxed(cluster_addr(&peer_free[r], er));
-#pragma unroll
-            for (int it = 0; it < kRedIt; ++it) {
-                const int idx = er + 64 * it;
-                const int lr = idx % my_rows, i = idx / my_rows;
-                const int otok = (c0 + kr) * kChunk + r0 + lr;
-                if (idx < items && otok < T) {
-                    const float inv = den[it] > 0.f ? 1.f / den[it] : 0.f;
-                    const float* a = acc[it];
-                    *reinterpret_cast<uint4*>(o + (head_row + otok) * DV + 8 * i) =
-                        make_uint4(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv),
-                                   pack_bf16x2(a[4] * inv, a[5] * inv), pack_bf16x2(a[6] * inv, a[7] * inv));
-                }
-            }
-        }
-        // no bulk copy may still be landing in shared memory when the CTA exits
-        if (er == 0)
-            for (int kr = consumed; kr < staged; ++kr) mbar_wait_quiet(&intra_full[kr % K::RS], (kr / K::RS) & 1, kWaitNs);
     }
     if (t == 416) {
         // =============================================================== TMA producer
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmkt);
         tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmy);
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            const int stg = kk % nq, stg_use = kk / nq;
             const int row = (c0 + kk) * kChunk;
             // transposed unit keys of chunk kk into its stage
             if (kk >= 2 && !mbar_wait(&kts_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             mbar_arrive_expect_tx(&kts_full[slot], K::kt_bytes);
-            tma_load_3d(kt_buf(slot), &tmkt, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
-            tma_load_3d(kt_buf(slot) + K::kt_box, &tmkt, 64, (c0 + kk) * P, (int)bh, &kts_full[slot]);
-            // value tile of chunk kk into its buffer
-            if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            mbar_arrive_expect_tx(&v_full[slot], kAtom);
-            tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[slot]);
+            tma_load_3d(kt_buf(kk), &tmkt, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            tma_load_3d(kt_buf(kk) + K::kt_box, &tmkt, 64, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            // value tile of chunk kk into its buffer (state tiles only)
+            if (!zc) {
+                if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+                mbar_arrive_expect_tx(&v_full[slot], kAtom);
+                tma_load_3d(v_buf(kk), &tmv, 0, row, (int)bh, &v_full[slot]);
+            }
             // query rows of chunk kk into its stage
-            if (kk >= nq && !mbar_wait(&qs_free[stg], (stg_use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            mbar_arrive_expect_tx(&qs_full[stg], kAtom);
-            tma_load_3d(q_buf(stg), &tmq, 0, row, (int)bh, &qs_full[stg]);
+            if (kk >= 2 && !mbar_wait(&qs_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+            mbar_arrive_expect_tx(&qs_full[slot], kAtom);
+            tma_load_3d(q_buf(kk), &tmq, 0, row, (int)bh, &qs_full[slot]);
         }
     }
     if (warp == 12) {
@@ -884,94 +652,82 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         // two thirds of that rate).  Every descriptor is built once; the loop
         // adds compile-time offsets (a step moves the start-address field, in
         // 16-byte units).
-        constexpr uint32_t id_read = idesc_bf16_f32_major(128, DV, false, true);
-        constexpr uint32_t id_upd = idesc_bf16_f32_major(128, DV, false, true);
+        constexpr uint32_t id_mn = idesc_bf16_f32_major(128, DV, false, true);
         constexpr uint32_t id_z = idesc_bf16_f32(128, M);
         constexpr uint32_t id_w = idesc_bf16_f32(128, M);
-        constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kAtomD = kAtom >> 4, kBoxD = K::kt_box >> 4;
+        constexpr uint64_t kStepMN = 2048 >> 4, kStepK = 32 >> 4, kBoxD = K::kt_box >> 4;
         // K step ks of a K-major operand whose 64-element K atoms are `atom` (16-byte units) apart
         auto kstep = [](uint64_t atom, int ks) { return (uint64_t)(ks >> 2) * atom + (uint64_t)(ks & 3) * kStepK; };
-        const uint64_t d_ak = sdesc_kmajor_sw128(smem_u32(s_ak));
         const uint64_t d_s16 = sdesc_mnmajor_sw128(smem_u32(s_s16), kAtom);
         const uint64_t d_v[2] = {sdesc_mnmajor_sw128(smem_u32(v_buf(0)), kAtom),
                                  sdesc_mnmajor_sw128(smem_u32(v_buf(1)), kAtom)};
-        // extra CTA: staged transposed keys (both operands of the Z update), staged Q, Z
+        // normaliser CTA: staged transposed keys (both operands of the Z update), staged Q, Z
         const uint64_t d_kt[2] = {sdesc_kmajor_sw128(smem_u32(kt_buf(0))), sdesc_kmajor_sw128(smem_u32(kt_buf(1)))};
-        const uint64_t d_q[2] = {sdesc_kmajor_sw128(smem_u32(q_buf(0))), sdesc_kmajor_sw128(smem_u32(q_buf(extra ? 1 : 0)))};
+        const uint64_t d_q[2] = {sdesc_kmajor_sw128(smem_u32(q_buf(0))), sdesc_kmajor_sw128(smem_u32(q_buf(1)))};
         const uint64_t d_z16 = sdesc_kmajor_sw128(smem_u32(s_z16));
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
-            if (!wait(&v_full[slot], use & 1)) { fail(); break; }
-            const uint64_t dv = d_v[slot];
-            // ---- group U: state updates, tile by tile (extra CTA: tail state and Z)
-            bool ok = true;
-            if (!extra) {
-#pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl) {
-                    if (!wait(&klift_full[tl], kk & 1)) { ok = false; break; }
-                    if (tl == 0 && kk >= 1 && !wait(&state_read, (kk - 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        if constexpr (K::AKT)
-                            mma_ts_w(tb + K::tm_s + 64 * tl, tb + K::tm_ak + 64 * tl + 8 * ks, dv + ks * kStepMN, id_upd, 1u);
-                        else
-                            mma_ss_w(tb + K::tm_s + 64 * tl, d_ak + 2 * tl * kAtomD + kstep(kAtomD, ks), dv + ks * kStepMN,
-                                     id_upd, 1u);
-                    }
-                    mma_commit_w(&ak_free[tl]);
+            if (!zc) {
+                if (!wait(&v_full[slot], use & 1) || !wait(&klift_full, kk & 1) ||
+                    (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
+                    fail();
+                    break;
                 }
-                if (!ok) { fail(); break; }
+                tc_fence_after();
+                // ---- update: state += lift(K)^T V
+                const uint64_t dv = d_v[slot];
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) mma_ts_w(tb + K::tm_s, tb + K::tm_ak + 8 * ks, dv + ks * kStepMN, id_mn, 1u);
+                mma_commit_w(&ak_free);
                 mma_commit_w(&upd_done);
                 mma_commit_w(&v_free[slot]);
-            } else {
-                if (!wait(&klift_full[0], kk & 1) ||
-                    !wait(&kts_full[slot], use & 1) ||
-                    (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) { fail(); break; }
+                // ---- readout of the state before this chunk
+                if (!wait(&qlift_full[slot], use & 1) || (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1)) ||
+                    (kk >= 2 && !wait(&y_free[slot], (use - 1) & 1))) {
+                    fail();
+                    break;
+                }
                 tc_fence_after();
+                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 64 * slot;
+                if (!tail) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ts_w(tb + K::tx_s, tb + K::tx_ak + 8 * ks, dv + ks * kStepMN, id_upd, 1u);
-                // Z += sum over the blocks of (rows of the block)^T (rows of the block)
+                    for (int ks = 0; ks < 8; ++ks) mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
+                        mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                }
+                mma_commit_w(&y_part[slot]);
+                mma_commit_w(&aq_free[slot]);
+            } else {
+                if (!wait(&kts_full[slot], use & 1) || (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                // ---- Z += sum over the blocks of Kh_b^T Kh_b
 #pragma unroll
                 for (int blk = 0; blk < LG; ++blk)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss_w(tb + K::tx_z, d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks),
-                               d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks), id_z, 1u);
-                mma_commit_w(&ak_free[0]);
-                mma_commit_w(&upd_done);
-                mma_commit_w(&v_free[slot]);
+                        mma_ss_w(tb + K::tm_z, d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks),
+                                 d_kt[slot] + (uint64_t)(blk * M * 8) + kstep(kBoxD, ks), id_z, 1u);
                 mma_commit_w(&kts_free[slot]);
-            }
-            // ---- group R: readout of the state before this chunk
-            if (!wait(&qlift_full[slot], use & 1)) { fail(); break; }
-            if (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1)) { fail(); break; }
-            if (kk >= 2 && !wait(&y_free[slot], (use - 1) & 1)) { fail(); break; }
-            if (extra && !wait(&qs_full[kk % nq], (kk / nq) & 1)) { fail(); break; }
-            tc_fence_after();
-            if (!extra) {
-                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 64 * K::TPC * slot;
-#pragma unroll
-                for (int tl = 0; tl < K::TPC; ++tl)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts_w(dy, aq + 64 * tl + 8 * ks, d_s16 + tl * kAtomD + ks * kStepMN, id_read,
-                               (tl > 0 || ks > 0) ? 1u : 0u);
-            } else {
-                const uint32_t dy = tb + K::tx_y + 64 * slot, aq = tb + K::tx_aq + 32 * slot;
-#pragma unroll
-                for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
-                    mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_read, ks > 0 ? 1u : 0u);
-                // W = [Q_0 Z | Q_1 Z | ...], one block of columns per block of the queries
+                mma_commit_w(&upd_done);
+                // ---- W = [Q_0 Z | Q_1 Z | ...] with Z before this chunk, one block of columns per block of the queries
+                if (!wait(&qs_full[slot], use & 1) || (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1))) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int blk = 0; blk < LG; ++blk)
 #pragma unroll
                     for (int ks = 0; ks < M / 16; ++ks)
-                        mma_ss_w(tb + K::tx_w + blk * M, d_q[kk % nq] + (blk * (M / 16) + ks) * kStepK,
-                               d_z16 + ks * kStepK, id_w, ks > 0 ? 1u : 0u);
+                        mma_ss_w(tb + K::tm_w + blk * M, d_q[slot] + (blk * (M / 16) + ks) * kStepK, d_z16 + ks * kStepK,
+                                 id_w, ks > 0 ? 1u : 0u);
+                mma_commit_w(&y_part[slot]);
             }
-            mma_commit_w(&y_part[slot]);
-            mma_commit_w(&aq_free[slot]);
         }
         // every issued MMA has completed before tensor memory is released
         mma_commit_w(&drain);
@@ -980,9 +736,31 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 
     tc_fence_before();
     __syncwarp();
-    cluster.sync();
+    __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+// ---------------------------------------------------------------- output
+// o = Y / d for the rows t < T (0 where d = 0); one thread per 8 columns.
+template <int DV>
+__global__ void __launch_bounds__(256)
+normalize_kernel(const float* __restrict__ yacc, const float* __restrict__ dacc, __nv_bfloat16* __restrict__ o, int T,
+                 int Tc, int64_t BH) {
+    constexpr int per = DV / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BH * T * per) return;
+    const int64_t row = i / per;
+    const int c = (int)(i % per);
+    const int64_t bh = row / T, tt = row % T;
+    const int64_t arow = bh * Tc + tt;
+    const float4 a = *reinterpret_cast<const float4*>(yacc + arow * DV + 8 * c);
+    const float4 b = *reinterpret_cast<const float4*>(yacc + arow * DV + 8 * c + 4);
+    const float d = dacc[arow];
+    const float inv = d > 0.f ? 1.f / d : 0.f;
+    *reinterpret_cast<uint4*>(o + row * DV + 8 * c) =
+        make_uint4(pack_bf16x2(a.x * inv, a.y * inv), pack_bf16x2(a.z * inv, a.w * inv), pack_bf16x2(b.x * inv, b.y * inv),
+                   pack_bf16x2(b.z * inv, b.w * inv));
 }
 
 
@@ -990,10 +768,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 // Every chunk on its own (no state): for the 128 queries of a chunk,
 //   P = (Q Kh^T) o (Q Kh^T) o M   (bf16, M the causal mask s <= t)
 //   Y = P V,  d = rowsum(P)       (fp32 accumulation)
-// Y goes out as bf16 rows [BH][Tc][DV] and d, the rows' intra-chunk
-// normaliser, as fp32 [BH][Tc] (Tc = T rounded up to whole chunks; rows past
-// T are not written); the fused forward adds both when it writes a chunk's
-// outputs.  The chunk's unit keys also go out transposed, kT
+// Y and d, the rows' intra-chunk normaliser, initialise the forward's fp32
+// accumulation rows [BH][Tc][DV] and [BH][Tc] (Tc = T rounded up to whole
+// chunks; rows past T are not written): the state kernel adds the
+// inter-chunk parts to them.  The chunk's unit keys also go out transposed, kT
 // [BH][chunks][P][128] bf16 (zeros past T): the fused forward's key lift
 // reads them.  d sums exactly the rounded weights Y is built from, which
 // keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
@@ -1002,7 +780,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 template <int P, int DV, int LG>
 __global__ void __launch_bounds__(128)
 intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ y_out, float* __restrict__ d_out,
+                const __nv_bfloat16* __restrict__ v, float* __restrict__ y_out, float* __restrict__ d_out,
                 __nv_bfloat16* __restrict__ kt_out, int T) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar, drain;
@@ -1196,11 +974,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(y_out + prow * DV);
 #pragma unroll
-            for (int i = 0; i < DV / 8; ++i)
-                dst[i] = make_uint4(pack_bf16x2(__uint_as_float(y[8 * i]), __uint_as_float(y[8 * i + 1])),
-                                    pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
-                                    pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
-                                    pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
+            for (int i = 0; i < DV / 4; ++i) dst[i] = make_uint4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
             d_out[prow] = den;
         }
     } else if (t == 0) {
@@ -1228,48 +1002,33 @@ bool register_split_fits() {
     return (uint32_t)kThreads * (uint32_t)fa.numRegs >= 128u * (kRegsLift + kRegsState + kRegsLaunch + kRegsMma);
 }
 
+// CTAs of the state kernel resident at once on the current device (one per
+// SM when it fits), 0 if the kernel cannot run there.
 template <int P, int DV, int LG>
-cudaError_t configure(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int G, int BH, cudaStream_t s) {
-    using K = Cfg<P, DV, LG>;
-    auto kern = chunked_tc_kernel<P, DV, LG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem);
-    if (e == cudaSuccess && K::CS > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    cfg = cudaLaunchConfig_t{};
-    cfg.gridDim = dim3(K::CS * G, BH, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = K::smem;
-    cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = K::CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaSuccess;
-}
-
-template <int P, int DV, int LG>
-int max_clusters() {
+int resident_ctas() {
     static int cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] == 0) {
-        cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
-        int m = 0;
-        if (!register_split_fits<P, DV, LG>() || configure<P, DV, LG>(cfg, attr, 1, 1, 0) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&m, chunked_tc_kernel<P, DV, LG>, &cfg) != cudaSuccess) {
+        using K = Cfg<P, DV, LG>;
+        int per_sm = 0, sms = 0;
+        if (!register_split_fits<P, DV, LG>() ||
+            cudaFuncSetAttribute(chunked_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunked_tc_kernel<P, DV, LG>, kThreads, K::smem) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
-        cached[dev] = m > 0 ? m : -1;
+        cached[dev] = per_sm * sms > 0 ? per_sm * sms : -1;
     }
     return cached[dev] > 0 ? cached[dev] : 0;
 }
 
-// Workspace of the forward's intra-chunk kernel: bf16 rows [BH][T][dv],
-// fp32 normalisers [BH][T], transposed unit keys [BH][chunks][p][128] bf16.
+// Workspace of the forward: fp32 accumulation rows Y [BH][Tc][dv] and d
+// [BH][Tc] (Tc = T rounded up to whole chunks), transposed unit keys
+// [BH][chunks][p][128] bf16.
 struct IntraWs {
     size_t y_off, d_off, kt_off, total;
 };
@@ -1278,7 +1037,7 @@ IntraWs intra_ws(int BH, int T, int p, int dv) {
     const size_t nch = (size_t)(T + kChunk - 1) / kChunk;
     IntraWs w;
     w.y_off = 0;
-    w.d_off = up((size_t)BH * nch * kChunk * dv * 2);
+    w.d_off = up((size_t)BH * nch * kChunk * dv * 4);
     w.kt_off = w.d_off + up((size_t)BH * nch * kChunk * 4);
     w.total = w.kt_off + up((size_t)BH * nch * p * kChunk * 2);
     return w;
@@ -1288,13 +1047,15 @@ template <int P, int DV, int LG>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* intra,
                          const float* S_start, const float* z_start, int start_groups, float* S_final,
                          float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
+    using K = Cfg<P, DV, LG>;
     if (!register_split_fits<P, DV, LG>()) return cudaErrorInvalidConfiguration;
     const IntraWs w = intra_ws(BH, T, P, DV);
-    auto* y_intra = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(intra) + w.y_off);
-    auto* d_intra = reinterpret_cast<float*>(static_cast<char*>(intra) + w.d_off);
+    auto* yacc = reinterpret_cast<float*>(static_cast<char*>(intra) + w.y_off);
+    auto* dacc = reinterpret_cast<float*>(static_cast<char*>(intra) + w.d_off);
     auto* kt = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(intra) + w.kt_off);
     const int nch = (T + kChunk - 1) / kChunk;
-    // the intra-chunk rows and the transposed unit keys of every chunk first
+    // the intra-chunk part (initialises the accumulation rows) and the
+    // transposed unit keys of every chunk first
     constexpr size_t intra_smem = 3 * kAtom + 1024;
     cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)intra_smem);
@@ -1302,19 +1063,24 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
     KATA_TRACED("intra_tc", s,
                 (intra_tc_kernel<P, DV, LG><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                    static_cast<const __nv_bfloat16*>(v), y_intra, d_intra, kt, T)));
+                    static_cast<const __nv_bfloat16*>(v), yacc, dacc, kt, T)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    if ((e = configure<P, DV, LG>(cfg, attr, G, BH, s)) != cudaSuccess) return e;
-    CUtensorMap tq, tkt, tv;
-    if (!rows_map(&tq, q, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) || !rows_map(&tv, v, DV, T, BH))
+    CUtensorMap tq, tkt, tv, ty;
+    if (!rows_map(&tq, q, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) || !rows_map(&tv, v, DV, T, BH) ||
+        !acc_map(&ty, yacc, DV, K::YW, nch * kChunk, BH))
         return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(chunked_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)K::smem)) != cudaSuccess)
+        return e;
     KATA_TRACED("chunked_tc", s,
-                e = cudaLaunchKernelEx(&cfg, chunked_tc_kernel<P, DV, LG>, tq, tkt, tv, static_cast<__nv_bfloat16*>(o),
-                                       static_cast<const __nv_bfloat16*>(y_intra), static_cast<const float*>(d_intra),
-                                       S_start, z_start, start_groups, S_final, z_final, T, seg_chunks));
-    if (e != cudaSuccess) return e;
+                (chunked_tc_kernel<P, DV, LG><<<dim3((unsigned)(K::CS * G), (unsigned)BH), kThreads, K::smem, s>>>(
+                    tq, tkt, tv, ty, dacc, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks)));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t items = (int64_t)BH * T * (DV / 8);
+    if (items > 0)
+        KATA_TRACED("normalize", s,
+                    (normalize_kernel<DV><<<(unsigned)((items + 255) / 256), 256, 0, s>>>(
+                        yacc, dacc, static_cast<__nv_bfloat16*>(o), T, nch * kChunk, (int64_t)BH)));
     return cudaGetLastError();
 }
 
@@ -1347,11 +1113,12 @@ bool chunked_tc_supports(int p, int dv, int lg) {
 
 int chunked_tc_segments(int p, int dv, int lg, int BH, int T) {
     const int nch = (T + kChunk - 1) / kChunk;
-    int m = 0;
-    KATA_DISPATCH(m = max_clusters<P, DV, LG>());
+    int m = 0, cs = 1;
+    KATA_DISPATCH(m = resident_ctas<P, DV, LG>(); cs = Cfg<P, DV, LG>::CS);
     if (m <= 0) return 0;
     if (nch <= 0) return 1;
-    int G = m / (BH > 0 ? BH : 1);
+    // as many segments per head as keep every resident CTA busy in one wave
+    int G = (m / cs) / (BH > 0 ? BH : 1);
     if (G < 1) G = 1;
     if (G > nch) G = nch;
     const int per = (nch + G - 1) / G;

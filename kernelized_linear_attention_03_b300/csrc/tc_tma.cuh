@@ -1,5 +1,6 @@
-// Host side of the TMA tile loads: tensor maps of the bf16 [BH][T][cols]
-// arrays the tensor-core kernels stream in 128-row boxes.
+// Host side of the TMA tile copies: tensor maps of the bf16 [BH][T][cols]
+// arrays the tensor-core kernels stream in 128-row boxes, and of the fp32
+// accumulation rows they reduce into.
 #pragma once
 
 #include <cuda.h>
@@ -56,6 +57,21 @@ inline bool kt_map(CUtensorMap* m, const void* base, int P, int chunks, int BH) 
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of an fp32 [BH][Tc][cols] accumulation array written by boxes
+// of 128 rows x w columns (w = 32: 128-byte rows, 128-byte swizzle; w = 16:
+// 64-byte rows, no swizzle); cols is a multiple of w.
+inline bool acc_map(CUtensorMap* m, const void* base, int cols, int w, int Tc, int BH) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)Tc, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)Tc * cols * 4};
+    cuuint32_t box[3] = {(cuuint32_t)w, 128u, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, w == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc
