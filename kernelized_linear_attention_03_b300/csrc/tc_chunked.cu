@@ -302,12 +302,14 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int t = threadIdx.x, warp = t >> 5;
-    const int tau = blockIdx.x % K::CS;  // tile of the packed lift (NT + 1: the normaliser CTA)
-    const int g = blockIdx.x / K::CS;    // segment
-    const int G = gridDim.x / K::CS;
+    // grid: x = head, y = (segment, tile): neighbouring CTAs (which share an
+    // SM pair and its instruction fetch) run the same tile of different heads
+    const int tau = blockIdx.y % K::CS;  // tile of the packed lift (NT + 1: the normaliser CTA)
+    const int g = blockIdx.y / K::CS;    // segment
+    const int G = gridDim.y / K::CS;
     const bool tail = tau == K::NT;      // the last, partly filled tile
     const bool zc = tau == K::NT + 1;    // Z and the denominators
-    const int64_t bh = blockIdx.y;
+    const int64_t bh = blockIdx.x;
     const int NCH = (T + kChunk - 1) / kChunk;
     const int64_t head_prow = bh * (int64_t)NCH * kChunk;  // accumulation rows: whole chunks per head
     const int c0 = g * seg_chunks, c1 = min(NCH, c0 + seg_chunks);
@@ -1073,7 +1075,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
                                   (int)K::smem)) != cudaSuccess)
         return e;
     KATA_TRACED("chunked_tc", s,
-                (chunked_tc_kernel<P, DV, LG><<<dim3((unsigned)(K::CS * G), (unsigned)BH), kThreads, K::smem, s>>>(
+                (chunked_tc_kernel<P, DV, LG><<<dim3((unsigned)BH, (unsigned)(K::CS * G)), kThreads, K::smem, s>>>(
                     tq, tkt, tv, ty, dacc, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t items = (int64_t)BH * T * (DV / 8);
