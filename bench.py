@@ -70,6 +70,14 @@ def lift_dim(family, p, g):
     return m * (m + 1) // 2 * (1 if family == LIFTS["sigma"] else g)
 
 
+# DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum + dram__bytes_write.sum from
+# one ncu pass with --clock-control none) for the configurations they were captured on; the summary
+# under profiles/ gives the command.  An entry is dropped whenever its kernel changes.
+MEASURED_TRAFFIC = {
+    ("chunked", "c4_T131072_p64_bf16", "chunked_tc"): 1.48e9 + 474.67e6,
+}
+
+
 def kernel_work(name, w, form="chunked", lift=None):
     """(kind, algorithmic amount per forward call) of a library kernel.  `lift`
     = (family, g) for the block-lift forms."""
@@ -112,9 +120,9 @@ def kernel_work(name, w, form="chunked", lift=None):
     if name == "chunked_tc":
         # the fused forward: state build and readout with the normaliser column
         return "flop", bht * 4 * w.n * (w.dv + 1)
-    if name == "combine":
-        # numerators, intra rows and both normalisers read, o written
-        return "byte", bht * (w.dv * 2 * 3 + 8)
+    if name == "normalize":
+        # fp32 numerator rows and denominators read, o written
+        return "byte", bht * (w.dv * 4 + 4 + w.dv * 2)
     if name == "intra_tc":
         # the causal intra-chunk half of the forward
         return "flop", bht * (w.C + 1) * (w.p + w.dv)
@@ -448,7 +456,9 @@ def run_ours(args, world, rank, local):
         achieved = amount / (dom_ms_per_call / 1e3) / 1e9
         peak, bound, unit = peaks["hbm_gbs"], "hbm", "GB/s"
     roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": args.traffic, "peak_source": peaks["source"],
+            "frac": achieved / peak,
+            "traffic": args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get((args.form, w.name, dom)),
+            "peak_source": peaks["source"],
             "launches_per_step": calls_per_step,
             "ms_per_step_in_kernel": dom_ms_per_call,
             "share_of_step": dom_ms_per_call / ms}
