@@ -83,12 +83,16 @@ struct Cfg {
     static constexpr size_t smem = total + 1024;
     // tensor memory columns
     static constexpr uint32_t tm_s = 0;      // 64: fp32 state tile
-    static constexpr uint32_t tm_ak = 64;    // 64: key lift (bf16 pairs of tokens); the last tile's lanes past the tail hold zeros
-    static constexpr uint32_t tm_aq = 128;   // 2 slots x 64: query lift (bf16 pairs of slots)
-    static constexpr uint32_t tm_y = 256;    // 2 slots x 64: partial readout
-    static constexpr uint32_t tm_w = 384;    // normaliser CTA: Q Z
+    // key-lift buffers: two for the block lifts (measured 10% faster at p = 64, g = 2), one for
+    // the full lift (the second one measured 3% slower there)
+    static constexpr int AKB = LG > 1 ? 2 : 1;
+    static constexpr uint32_t tm_ak = 64;    // AKB slots x 64: key lift (bf16 pairs of tokens); the last tile's lanes past the tail hold zeros
+    static constexpr uint32_t tm_aq = 64 + 64 * AKB;  // 2 slots x 64: query lift (bf16 pairs of slots)
+    static constexpr uint32_t tm_y = tm_aq + 128;    // 2 slots x 64: partial readout
+    static constexpr uint32_t tm_w = 384;    // normaliser CTA (which has no tile): Q Z
     static constexpr uint32_t tm_z = 448;    // normaliser CTA: Z
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
+    static_assert(tm_y + 128 <= 512, "tensor memory columns");
     static_assert(total + 4096 <= 232448, "shared memory");
     static_assert(kt_bytes <= kAtom, "transposed-key stage");
     static_assert(DV % YW == 0 && DV <= 64, "value width");
@@ -296,7 +300,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qs_full[2], qs_free[2], kts_full[2], kts_free[2], v_full[2], v_free[2];
     __shared__ uint64_t qlift_full[2], aq_free[2], y_part[2], y_free[2], ys_full[2], ys_free[2];
-    __shared__ uint64_t klift_full, ak_free, upd_done, state_read, s16_ready, drain;
+    __shared__ uint64_t klift_full[2], ak_free[2], upd_done, state_read, s16_ready, drain;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -340,8 +344,10 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             mbar_init(&ys_full[b], 128);
             mbar_init(&ys_free[b], 1);
         }
-        mbar_init(&klift_full, 128);
-        mbar_init(&ak_free, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&klift_full[b], 128);
+            mbar_init(&ak_free[b], 1);
+        }
         mbar_init(&upd_done, 1);
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
@@ -413,7 +419,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
         for (int i = 0; i < 16; ++i) zw[i] = 0u;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_st16(tm(K::tm_ak + c), zw);
+        for (int c = 0; c < 64 * K::AKB; c += 16) tmem_st16(tm(K::tm_ak + c), zw);
         tmem_wait_st();
     }
     fence_proxy_async_smem();
@@ -607,12 +613,14 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             for (int kk = 0; kk < nk; ++kk) {
                 const int stg = kk & 1, use = kk >> 1;
                 if (!wait(&kts_full[stg], use & 1)) { fail(); break; }
-                if (kk >= 1 && !wait(&ak_free, (kk - 1) & 1)) { fail(); break; }
+                // the key-lift buffer's previous chunk (kk - AKB) has been read by its update
+                const int ab = kk % K::AKB, ause = kk / K::AKB;
+                if (kk >= K::AKB && !wait(&ak_free[ab], (ause - 1) & 1)) { fail(); break; }
                 tc_fence_after();
-                if (!tail || warp == 8) key_row_tmem<P, LG>(kt_buf(kk), tau * 128 + e, tm(K::tm_ak));
+                if (!tail || warp == 8) key_row_tmem<P, LG>(kt_buf(kk), tau * 128 + e, tm(K::tm_ak + 64 * ab));
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&klift_full);
+                mbar_arrive(&klift_full[ab]);
                 mbar_arrive(&kts_free[stg]);
             }
         }
@@ -670,7 +678,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
             if (!zc) {
-                if (!wait(&v_full[slot], use & 1) || !wait(&klift_full, kk & 1) ||
+                const int ab = kk % K::AKB, ause = kk / K::AKB;
+                if (!wait(&v_full[slot], use & 1) || !wait(&klift_full[ab], ause & 1) ||
                     (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
                     fail();
                     break;
@@ -679,8 +688,9 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // ---- update: state += lift(K)^T V
                 const uint64_t dv = d_v[slot];
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ts_w(tb + K::tm_s, tb + K::tm_ak + 8 * ks, dv + ks * kStepMN, id_mn, 1u);
-                mma_commit_w(&ak_free);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts_w(tb + K::tm_s, tb + K::tm_ak + 64 * ab + 8 * ks, dv + ks * kStepMN, id_mn, 1u);
+                mma_commit_w(&ak_free[ab]);
                 mma_commit_w(&upd_done);
                 mma_commit_w(&v_free[slot]);
                 // ---- readout of the state before this chunk
@@ -781,27 +791,30 @@ normalize_kernel(const float* __restrict__ yacc, const float* __restrict__ dacc,
 // chunks are in flight per SM; thread t owns query / key / value row t.
 template <int P, int DV, int LG>
 __global__ void __launch_bounds__(128)
-intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                const __nv_bfloat16* __restrict__ v, float* __restrict__ y_out, float* __restrict__ d_out,
-                __nv_bfloat16* __restrict__ kt_out, int T) {
+intra_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkt,
+                const __grid_constant__ CUtensorMap tmy, float* __restrict__ d_out, int T) {
+    constexpr int YW = DV < 32 ? DV : 32, YH = DV / YW;  // fp32 output boxes of 128 rows x YW columns
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar, drain;
+    __shared__ uint64_t bar, drain, ld_full;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* Qs = sm;              // K-major, 128 rows x 128 B
-    uint8_t* Ks = sm + kAtom;      // unit keys, K-major
-    uint8_t* Vs = sm + 2 * kAtom;  // V, MN-major
+    uint8_t* Qs = sm;              // K-major, 128 rows x 128 B (TMA, zeros past T and past P)
+    uint8_t* Ks = sm + kAtom;      // keys, normalised in place: unit keys, K-major
+    uint8_t* Vs = sm + 2 * kAtom;  // V, MN-major (TMA)
+    uint8_t* KTs = sm + 3 * kAtom; // transposed unit keys: two boxes of P rows x 64 tokens (128-byte swizzle)
+    uint8_t* Ys = sm;              // fp32 rows for the output boxes (over Q and K once the scores are read)
     const int t = threadIdx.x, warp = t >> 5;
     const int64_t bh = blockIdx.y;
     const int row = blockIdx.x * kChunk + t;
     const bool valid = row < T;
-    const int64_t grow = bh * T + (valid ? row : 0);
     // y and d rows: T rounded up to whole chunks per head
     const int64_t prow = bh * (int64_t)(gridDim.x * kChunk) + row;
     if (t == 0) {
         mbar_init(&bar, 1);
         mbar_init(&drain, 1);
+        mbar_init(&ld_full, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -809,18 +822,22 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         tmem_alloc(&tmem_base, 128);
         tmem_relinquish();
     }
-    // rows -> shared memory (zeros past T)
-    {
-        const uint4* gq = reinterpret_cast<const uint4*>(q + grow * P);
-        const uint4* gk = reinterpret_cast<const uint4*>(k + grow * P);
-        const uint4* gv = reinterpret_cast<const uint4*>(v + grow * DV);
+    __syncthreads();
+    // q, k, v rows of the chunk by TMA (rows past T read as zeros)
+    if (t == 0) {
+        mbar_arrive_expect_tx(&ld_full, 3 * kAtom);
+        tma_load_3d(Qs, &tmq, 0, blockIdx.x * kChunk, (int)bh, &ld_full);
+        tma_load_3d(Ks, &tmk, 0, blockIdx.x * kChunk, (int)bh, &ld_full);
+        tma_load_3d(Vs, &tmv, 0, blockIdx.x * kChunk, (int)bh, &ld_full);
+    }
+    const bool loaded = __all_sync(0xffffffffu, mbar_wait(&ld_full, 0, &abort_flag, kWaitNs));
+    // thread t normalises key row t in place and writes it transposed into the staging boxes
+    if (loaded) {
         uint4 kr[P / 8];
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < P / 8; ++i) {
-            const uint4 a = valid ? gq[i] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(Qs + sw128_chunk(t, 8 * i, kChunk)) = a;
-            kr[i] = valid ? gk[i] : make_uint4(0, 0, 0, 0);
+            kr[i] = *reinterpret_cast<const uint4*>(Ks + sw128_chunk(t, 8 * i, kChunk));
             const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -829,6 +846,7 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             }
         }
         const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        uint8_t* kt_box = KTs + (t >> 6) * (P * 128);
 #pragma unroll
         for (int i = 0; i < P / 8; ++i) {
             const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
@@ -838,15 +856,26 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             w.z = pack_bf16x2(__bfloat162float(ke[4]) * kinv, __bfloat162float(ke[5]) * kinv);
             w.w = pack_bf16x2(__bfloat162float(ke[6]) * kinv, __bfloat162float(ke[7]) * kinv);
             *reinterpret_cast<uint4*>(Ks + sw128_chunk(t, 8 * i, kChunk)) = w;
-            // dimensions 8i .. 8i+7 of this token into the transposed keys
-            const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&w);
-            __nv_bfloat16* kt = kt_out + ((bh * gridDim.x + blockIdx.x) * P + 8 * i) * kChunk + t;
+            // dimensions 8i .. 8i+7 of this token: rows of the transposed box, token column t % 64
+            const uint16_t* we = reinterpret_cast<const uint16_t*>(&w);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) kt[j * kChunk] = we[j];
+            for (int j = 0; j < 8; ++j) {
+                const int d = 8 * i + j;
+                *reinterpret_cast<uint16_t*>(kt_box + d * 128 + ((((t & 63) >> 3) ^ (d & 7)) << 4) + (t & 7) * 2) = we[j];
+            }
         }
-#pragma unroll
-        for (int i = 0; i < DV / 8; ++i)
-            *reinterpret_cast<uint4*>(Vs + mn_sw128_chunk(8 * i, t, kAtom)) = valid ? gv[i] : make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    // the transposed unit keys of the chunk out by TMA (read before the CTA exits)
+    if (t == 0 && loaded) {
+        tma_store_3d(&tmkt, 0, blockIdx.x * P, (int)bh, KTs);
+        tma_store_3d(&tmkt, 64, blockIdx.x * P, (int)bh, KTs + P * 128);
+        bulk_commit();
+    }
+    if (!loaded && t == 0) {
+        abort_flag = 1;
+        atomicOr(&g_chunked_tc_status, kStatusTimeout);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -969,21 +998,37 @@ intra_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     ok = !abort_flag && __all_sync(0xffffffffu, mbar_wait(&bar, (LG * LG) & 1, &abort_flag, kWaitNs));
     tc_fence_after();
     if (ok) {
+        // row t of Y into the output boxes (over the query and key tiles, whose
+        // products are done), the normaliser straight out
         uint32_t y[DV];
 #pragma unroll
         for (int c = 0; c < DV; c += 16) tmem_ld16(tmem_addr(tb, lane0, 64 + c), *reinterpret_cast<uint32_t(*)[16]>(y + c));
         tmem_wait_ld();
-        if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(y_out + prow * DV);
 #pragma unroll
-            for (int i = 0; i < DV / 4; ++i) dst[i] = make_uint4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-            d_out[prow] = den;
-        }
+        for (int hh = 0; hh < YH; ++hh)
+#pragma unroll
+            for (int c = 0; c < YW / 4; ++c) {
+                const uint32_t off = YW == 32 ? (uint32_t)t * 128u + ((uint32_t)(c ^ (t & 7)) << 4)
+                                              : (uint32_t)t * (YW * 4) + (uint32_t)c * 16u;
+                *reinterpret_cast<uint4*>(Ys + hh * (128 * YW * 4) + off) =
+                    make_uint4(y[hh * YW + 4 * c], y[hh * YW + 4 * c + 1], y[hh * YW + 4 * c + 2], y[hh * YW + 4 * c + 3]);
+            }
+        if (valid) d_out[prow] = den;
     } else if (t == 0) {
         atomicOr(&g_chunked_tc_status, kStatusTimeout);
     }
-    // every issued MMA has completed before the tensor memory is released
+    fence_proxy_async_smem();
+    __syncthreads();
     if (t == 0) {
+        if (ok) {
+#pragma unroll
+            for (int hh = 0; hh < YH; ++hh)
+                tma_store_3d(&tmy, hh * YW, blockIdx.x * kChunk, (int)bh, Ys + hh * (128 * YW * 4));
+            bulk_commit();
+        }
+        // no store may still be reading shared memory when the CTA exits
+        bulk_wait_read<0>();
+        // every issued MMA has completed before the tensor memory is released
         mma_commit(&drain);
         mbar_wait_quiet(&drain, 0, kWaitNs);
     }
@@ -1058,19 +1103,18 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
     const int nch = (T + kChunk - 1) / kChunk;
     // the intra-chunk part (initialises the accumulation rows) and the
     // transposed unit keys of every chunk first
-    constexpr size_t intra_smem = 3 * kAtom + 1024;
+    CUtensorMap tq, tk, tkt, tv, ty;
+    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) ||
+        !rows_map(&tv, v, DV, T, BH) || !acc_map(&ty, yacc, DV, K::YW, nch * kChunk, BH))
+        return cudaErrorInvalidValue;
+    constexpr size_t intra_smem = 4 * kAtom + 1024;
     cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)intra_smem);
     if (e != cudaSuccess) return e;
     KATA_TRACED("intra_tc", s,
                 (intra_tc_kernel<P, DV, LG><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
-                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                    static_cast<const __nv_bfloat16*>(v), yacc, dacc, kt, T)));
+                    tq, tk, tv, tkt, ty, dacc, T)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    CUtensorMap tq, tkt, tv, ty;
-    if (!rows_map(&tq, q, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) || !rows_map(&tv, v, DV, T, BH) ||
-        !acc_map(&ty, yacc, DV, K::YW, nch * kChunk, BH))
-        return cudaErrorInvalidValue;
     if ((e = cudaFuncSetAttribute(chunked_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)K::smem)) != cudaSuccess)
         return e;

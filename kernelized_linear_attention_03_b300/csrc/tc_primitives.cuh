@@ -266,6 +266,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, int x, int y
         : "memory");
 }
 
+// TMA: 3-D tiled store of a shared-memory box into global memory, tracked as
+// a bulk group of this thread.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, const void* smem_src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's bulk groups are still reading their
