@@ -52,6 +52,10 @@ constexpr uint32_t kRegsLift = 168, kRegsState = 128, kRegsLaunch = 128, kRegsMm
 constexpr int kChunk = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kAtom = 128 * 128;  // 128 rows x 128 bytes
+// transposed unit keys of a chunk in memory: P rows of 128 tokens (bf16) and
+// a 16-byte pad
+constexpr int kKtCols = kChunk + 8;
+constexpr uint32_t kKtRow = kKtCols * 2;
 constexpr float kSqrt2f = 1.41421356237309504880f;
 constexpr float kInvSqrt2f = 0.70710678118654752440f;
 
@@ -64,9 +68,12 @@ struct Cfg {
     static constexpr int NT = n / 128;                 // full tiles
     static constexpr int TAIL = n - 128 * NT;          // slots of the last tile (8, 16 or 32)
     static constexpr int CS = NT + 2;                  // CTAs per head and segment: one per tile, one for Z
-    // transposed unit keys of a chunk: two 64-token boxes of P rows x 128 bytes
+    // transposed unit keys of a chunk: in a tile CTA one bulk copy of the
+    // padded rows (P x kKtRow bytes); in the normaliser CTA two 64-token boxes
+    // of P rows x 128 bytes (128-byte swizzle, the MMA operand layout)
     static constexpr uint32_t kt_box = P * 128;
     static constexpr uint32_t kt_bytes = 2 * kt_box;
+    static constexpr uint32_t kt_rows_bytes = P * kKtRow;
     // partial readout staged for the reduce-add: YH boxes of 128 rows x YW
     // fp32 columns (128-byte rows for YW = 32)
     static constexpr int YW = DV < 32 ? DV : 32;
@@ -75,8 +82,9 @@ struct Cfg {
     static constexpr uint32_t y_stage = YH * y_box;
     // shared memory, in 16 KB atoms from a 1024-byte aligned base: V x2,
     // bf16 state, query stages x2, bf16 Z (normaliser CTA), transposed-key
-    // stages x2, one spare atom (the M = 128 reads of the Z update run past
-    // the last stage), then two partial-readout stages
+    // stages (three atoms: two padded stages in a tile CTA; two swizzled
+    // stages and a spare atom in the normaliser CTA, whose M = 128 reads of
+    // the Z update run past the last stage), then two partial-readout stages
     static constexpr uint32_t o_v = 0, o_s16 = 2 * kAtom, o_q = 3 * kAtom, o_z16 = 5 * kAtom, o_kt = 6 * kAtom,
                               o_y = 9 * kAtom;
     static constexpr uint32_t total = o_y + 2 * y_stage;
@@ -94,27 +102,38 @@ struct Cfg {
     static_assert(TAIL > 0 && TAIL <= 32, "tail tile");
     static_assert(tm_y + 128 <= 512, "tensor memory columns");
     static_assert(total + 4096 <= 232448, "shared memory");
-    static_assert(kt_bytes <= kAtom, "transposed-key stage");
+    static_assert(kt_bytes <= kAtom && 2 * kt_rows_bytes <= 3 * kAtom, "transposed-key stages");
     static_assert(DV % YW == 0 && DV <= 64, "value width");
 };
 
 // ---------------------------------------------------------------- key lift, one slot per thread
 // The key lift of internal slot (i, j) for the 128 tokens of a chunk comes
 // from the chunk's transposed unit keys `kts` (row d = dimension d over the
-// tokens, two 64-token boxes of P rows, 128-byte swizzle): k_i k_j for the
+// tokens, kKtRow bytes apart: 128 tokens and a 16-byte pad, so that rows
+// d, d+1, ... start in consecutive 16-byte bank groups and a warp reading one
+// 16-byte piece of 32 consecutive rows is conflict-free): k_i k_j for the
 // full lift, sum_a k_{aM+i} k_{aM+j} over the LG blocks of width M for
-// KATA-Sigma-g.  Consecutive tokens sit side by side in both, so the 16
-// bytes of tokens [64h + 8c, 64h + 8c + 8) are four bf16x2 multiplies of two
-// 16-byte loads.
-template <int P, int LG>
-__device__ __forceinline__ uint4 key_words(const uint8_t* kts, int i, int j, int h, int c) {
-    constexpr int M = P / LG;
+// KATA-Sigma-g.  Consecutive tokens sit side by side in both rows, so the 16
+// bytes of tokens [8g, 8g + 8) are four bf16x2 multiplies of two 16-byte
+// loads at compile-time offsets from the two rows.
+// 16 bytes at shared address a + OFF.
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4 + %5];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(a), "n"(OFF)
+                 : "memory");
+    return r;
+}
+
+template <int LG, int G>
+__device__ __forceinline__ uint4 key_words(const uint32_t (&ri)[LG], const uint32_t (&rj)[LG]) {
     uint4 r;
 #pragma unroll
     for (int blk = 0; blk < LG; ++blk) {
-        const int bi = blk * M + i, bj = blk * M + j;  // rows of this block's two factors
-        const uint4 a = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bi * 128 + ((c ^ (bi & 7)) << 4));
-        const uint4 b = *reinterpret_cast<const uint4*>(kts + h * (P * 128) + bj * 128 + ((c ^ (bj & 7)) << 4));
+        const uint4 a = lds128<16 * G>(ri[blk]);
+        const uint4 b = lds128<16 * G>(rj[blk]);
         if (blk == 0) {
             r.x = hmul2_bf16(a.x, b.x);
             r.y = hmul2_bf16(a.y, b.y);
@@ -136,22 +155,45 @@ __device__ __forceinline__ uint4 key_words(const uint8_t* kts, int i, int j, int
 // give zeros.
 template <int P, int LG>
 __device__ __forceinline__ void key_row_tmem(const uint8_t* kts, int slot, uint32_t taddr) {
-    constexpr int n = lift::packed_n(P / LG);
+    constexpr int M = P / LG;
+    constexpr int n = lift::packed_n(M);
     const bool live = slot < n;
     int i = 0, j = 0;
-    if (live) lift::slot_coord(P / LG, slot, i, j);
+    if (live) lift::slot_coord(M, slot, i, j);
+    uint32_t ri[LG], rj[LG];  // shared addresses of the factor rows
 #pragma unroll
+    for (int blk = 0; blk < LG; ++blk) {
+        ri[blk] = smem_u32(kts) + (uint32_t)(blk * M + i) * kKtRow;
+        rj[blk] = smem_u32(kts) + (uint32_t)(blk * M + j) * kKtRow;
+    }
+    // one quarter (32 tokens) at a time: a rolled loop keeps the loads of one
+    // quarter in flight, within the warpgroup's registers
+#pragma unroll 1
     for (int qt = 0; qt < 4; ++qt) {
         uint32_t w[16];
+        uint4 r[4];
+        if (live) {
+            r[0] = key_words<LG, 0>(ri, rj);
+            r[1] = key_words<LG, 1>(ri, rj);
+            r[2] = key_words<LG, 2>(ri, rj);
+            r[3] = key_words<LG, 3>(ri, rj);
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) r[cc] = make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-            const uint4 r = live ? key_words<P, LG>(kts, i, j, qt >> 1, (qt & 1) * 4 + cc) : make_uint4(0, 0, 0, 0);
-            w[4 * cc] = r.x;
-            w[4 * cc + 1] = r.y;
-            w[4 * cc + 2] = r.z;
-            w[4 * cc + 3] = r.w;
+            w[4 * cc] = r[cc].x;
+            w[4 * cc + 1] = r[cc].y;
+            w[4 * cc + 2] = r[cc].z;
+            w[4 * cc + 3] = r[cc].w;
         }
         tmem_st16(taddr + 16 * qt, w);
+#pragma unroll
+        for (int blk = 0; blk < LG; ++blk) {
+            ri[blk] += 64;
+            rj[blk] += 64;
+        }
     }
 }
 
@@ -293,7 +335,8 @@ template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkt,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmy,
-                  float* __restrict__ dacc, const float* __restrict__ S_start, const float* __restrict__ z_start,
+                  const __grid_constant__ CUtensorMap tmktr, float* __restrict__ dacc,
+                  const float* __restrict__ S_start, const float* __restrict__ z_start,
                   int start_groups, float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
     using K = Cfg<P, DV, LG>;
     constexpr int n = K::n, M = K::M;
@@ -322,7 +365,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     uint8_t* const s_z16 = sm + K::o_z16;
     auto v_buf = [&](int kk) { return sm + K::o_v + (kk & 1) * kAtom; };
     auto q_buf = [&](int kk) { return sm + K::o_q + (kk & 1) * kAtom; };
-    auto kt_buf = [&](int kk) { return sm + K::o_kt + (kk & 1) * kAtom; };
+    // transposed-key stage of chunk kk: padded rows (tile CTAs) or swizzled boxes (normaliser)
+    auto kt_buf = [&](int kk) { return sm + K::o_kt + (kk & 1) * (zc ? kAtom : K::kt_rows_bytes); };
     auto y_buf = [&](int kk) { return sm + K::o_y + (kk & 1) * K::y_stage; };
 
     if (t == 0) {
@@ -631,6 +675,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         // =============================================================== TMA producer
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmkt);
+        tma_prefetch_desc(&tmktr);
         tma_prefetch_desc(&tmv);
         tma_prefetch_desc(&tmy);
         for (int kk = 0; kk < nk; ++kk) {
@@ -638,9 +683,14 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             const int row = (c0 + kk) * kChunk;
             // transposed unit keys of chunk kk into its stage
             if (kk >= 2 && !mbar_wait(&kts_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
-            mbar_arrive_expect_tx(&kts_full[slot], K::kt_bytes);
-            tma_load_3d(kt_buf(kk), &tmkt, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
-            tma_load_3d(kt_buf(kk) + K::kt_box, &tmkt, 64, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            if (!zc) {
+                mbar_arrive_expect_tx(&kts_full[slot], K::kt_rows_bytes);
+                tma_load_3d(kt_buf(kk), &tmktr, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            } else {
+                mbar_arrive_expect_tx(&kts_full[slot], K::kt_bytes);
+                tma_load_3d(kt_buf(kk), &tmkt, 0, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+                tma_load_3d(kt_buf(kk) + K::kt_box, &tmkt, 64, (c0 + kk) * P, (int)bh, &kts_full[slot]);
+            }
             // value tile of chunk kk into its buffer (state tiles only)
             if (!zc) {
                 if (kk >= 2 && !mbar_wait(&v_free[slot], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
@@ -784,15 +834,16 @@ normalize_kernel(const float* __restrict__ yacc, const float* __restrict__ dacc,
 // accumulation rows [BH][Tc][DV] and [BH][Tc] (Tc = T rounded up to whole
 // chunks; rows past T are not written): the state kernel adds the
 // inter-chunk parts to them.  The chunk's unit keys also go out transposed, kT
-// [BH][chunks][P][128] bf16 (zeros past T): the fused forward's key lift
-// reads them.  d sums exactly the rounded weights Y is built from, which
-// keeps the intra-chunk weights a convex combination.  One CTA per (chunk,
-// head), 128 columns of tensor memory and 48 KB of shared memory, so several
-// chunks are in flight per SM; thread t owns query / key / value row t.
+// [BH][chunks][P][kKtCols] bf16 (128 tokens, zeros past T, and a pad): the
+// state kernel's key lift reads them.  d sums exactly the rounded weights Y
+// is built from, which keeps the intra-chunk weights a convex combination.
+// One CTA per (chunk, head), 128 columns of tensor memory and about 66 KB of
+// shared memory, so several chunks are in flight per SM; thread t owns query
+// / key / value row t.
 template <int P, int DV, int LG>
 __global__ void __launch_bounds__(128)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmkt,
+                const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ kt_out,
                 const __grid_constant__ CUtensorMap tmy, float* __restrict__ d_out, int T) {
     constexpr int YW = DV < 32 ? DV : 32, YH = DV / YW;  // fp32 output boxes of 128 rows x YW columns
     extern __shared__ uint8_t smem_raw[];
@@ -803,7 +854,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     uint8_t* Qs = sm;              // K-major, 128 rows x 128 B (TMA, zeros past T and past P)
     uint8_t* Ks = sm + kAtom;      // keys, normalised in place: unit keys, K-major
     uint8_t* Vs = sm + 2 * kAtom;  // V, MN-major (TMA)
-    uint8_t* KTs = sm + 3 * kAtom; // transposed unit keys: two boxes of P rows x 64 tokens (128-byte swizzle)
+    uint8_t* KTs = sm + 3 * kAtom; // transposed unit keys: P rows of kKtRow bytes
     uint8_t* Ys = sm;              // fp32 rows for the output boxes (over Q and K once the scores are read)
     const int t = threadIdx.x, warp = t >> 5;
     const int64_t bh = blockIdx.y;
@@ -846,7 +897,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             }
         }
         const float kinv = ss > 0.f ? rsqrtf(ss) : 0.f;
-        uint8_t* kt_box = KTs + (t >> 6) * (P * 128);
+        // the pad of row t (never read; written so that the copy out is defined)
+        if (t < P) *reinterpret_cast<uint4*>(KTs + t * kKtRow + 2 * kChunk) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int i = 0; i < P / 8; ++i) {
             const __nv_bfloat16* ke = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
@@ -856,21 +908,17 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             w.z = pack_bf16x2(__bfloat162float(ke[4]) * kinv, __bfloat162float(ke[5]) * kinv);
             w.w = pack_bf16x2(__bfloat162float(ke[6]) * kinv, __bfloat162float(ke[7]) * kinv);
             *reinterpret_cast<uint4*>(Ks + sw128_chunk(t, 8 * i, kChunk)) = w;
-            // dimensions 8i .. 8i+7 of this token: rows of the transposed box, token column t % 64
+            // dimensions 8i .. 8i+7 of this token: rows of the transposed keys, column t
             const uint16_t* we = reinterpret_cast<const uint16_t*>(&w);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int d = 8 * i + j;
-                *reinterpret_cast<uint16_t*>(kt_box + d * 128 + ((((t & 63) >> 3) ^ (d & 7)) << 4) + (t & 7) * 2) = we[j];
-            }
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint16_t*>(KTs + (8 * i + j) * kKtRow + t * 2) = we[j];
         }
     }
     fence_proxy_async_smem();
     __syncthreads();
-    // the transposed unit keys of the chunk out by TMA (read before the CTA exits)
+    // the transposed unit keys of the chunk out in one bulk copy (read before the CTA exits)
     if (t == 0 && loaded) {
-        tma_store_3d(&tmkt, 0, blockIdx.x * P, (int)bh, KTs);
-        tma_store_3d(&tmkt, 64, blockIdx.x * P, (int)bh, KTs + P * 128);
+        bulk_store(kt_out + ((int64_t)bh * gridDim.x + blockIdx.x) * (P * kKtCols), KTs, P * kKtRow);
         bulk_commit();
     }
     if (!loaded && t == 0) {
@@ -1086,7 +1134,7 @@ IntraWs intra_ws(int BH, int T, int p, int dv) {
     w.y_off = 0;
     w.d_off = up((size_t)BH * nch * kChunk * dv * 4);
     w.kt_off = w.d_off + up((size_t)BH * nch * kChunk * 4);
-    w.total = w.kt_off + up((size_t)BH * nch * p * kChunk * 2);
+    w.total = w.kt_off + up((size_t)BH * nch * p * kKtCols * 2);
     return w;
 }
 
@@ -1103,24 +1151,24 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
     const int nch = (T + kChunk - 1) / kChunk;
     // the intra-chunk part (initialises the accumulation rows) and the
     // transposed unit keys of every chunk first
-    CUtensorMap tq, tk, tkt, tv, ty;
-    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH) ||
+    CUtensorMap tq, tk, tkt, tktr, tv, ty;
+    if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !kt_map(&tkt, kt, P, nch, BH, kKtCols) || !kt_rows_map(&tktr, kt, P, nch, BH, kKtCols) ||
         !rows_map(&tv, v, DV, T, BH) || !acc_map(&ty, yacc, DV, K::YW, nch * kChunk, BH))
         return cudaErrorInvalidValue;
-    constexpr size_t intra_smem = 4 * kAtom + 1024;
+    constexpr size_t intra_smem = 3 * kAtom + P * kKtRow + 1024;
     cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)intra_smem);
     if (e != cudaSuccess) return e;
     KATA_TRACED("intra_tc", s,
                 (intra_tc_kernel<P, DV, LG><<<dim3((unsigned)nch, (unsigned)BH), 128, intra_smem, s>>>(
-                    tq, tk, tv, tkt, ty, dacc, T)));
+                    tq, tk, tv, kt, ty, dacc, T)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(chunked_tc_kernel<P, DV, LG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)K::smem)) != cudaSuccess)
         return e;
     KATA_TRACED("chunked_tc", s,
                 (chunked_tc_kernel<P, DV, LG><<<dim3((unsigned)BH, (unsigned)(K::CS * G)), kThreads, K::smem, s>>>(
-                    tq, tkt, tv, ty, dacc, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks)));
+                    tq, tkt, tv, ty, tktr, dacc, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t items = (int64_t)BH * T * (DV / 8);
     if (items > 0)

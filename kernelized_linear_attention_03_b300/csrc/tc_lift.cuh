@@ -62,9 +62,23 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return r;
 }
 
+// bf16 pair (u_a, u_b) of the vector u (P/2 packed words; a, b compile-time
+// after unrolling): an aligned pair is the word itself, a repeated element one
+// byte permute (shared by every word that repeats it), anything else a
+// permute of two words.
+__device__ __forceinline__ uint32_t u_pair(const uint32_t* u, int a, int b) {
+    if ((a & 1) == 0 && b == a + 1) return u[a >> 1];
+    if (a == b) return __byte_perm(u[a >> 1], 0u, (a & 1) ? 0x3232u : 0x1010u);
+    return bf16_pair(u, a, u, b);
+}
+
 // Packed bf16x2 word holding the lift at slots (2w, 2w+1) of the vector u
 // (P/2 packed words).  QUERY applies the query's factor 2 to off-diagonal
-// slots (exact in bf16).  Slots at or past n give 0.
+// slots (exact in bf16).  Slots at or past n give 0.  The word is the product
+// of two pairs, (u_i0, u_i1) and (u_j0, u_j1); in every tile of the slot order
+// one of them repeats a single element over a run of words, and the factor
+// goes onto that one, so that it is computed once per run and each word costs
+// one multiply.
 template <int P, bool QUERY>
 __device__ __forceinline__ uint32_t lift_word(const uint32_t* u, int w) {
     constexpr int n = packed_n(P);
@@ -78,12 +92,17 @@ __device__ __forceinline__ uint32_t lift_word(const uint32_t* u, int w) {
         i1 = i0;
         j1 = j0;
     }
-    uint32_t x = bf16_pair(u, i0, u, i1);
+    uint32_t x = u_pair(u, i0, i1);
+    uint32_t y = u_pair(u, j0, j1);
     if (QUERY) {
         const uint32_t f = (i0 < j0 ? 0x4000u : 0x3F80u) | ((i1 < j1 ? 0x4000u : 0x3F80u) << 16);  // (2|1, 2|1)
-        if (f != 0x3F803F80u) x = bf16x2_mul(x, f);
+        if (f != 0x3F803F80u) {
+            if (i0 == i1 || j0 != j1)
+                x = bf16x2_mul(x, f);
+            else
+                y = bf16x2_mul(y, f);
+        }
     }
-    const uint32_t y = bf16_pair(u, j0, u, j1);
     const uint32_t r = bf16x2_mul(x, y);
     return s1 < n ? r : (r & 0xFFFFu);
 }

@@ -44,18 +44,34 @@ inline bool rows_map(CUtensorMap* m, const void* base, int cols, int T, int BH) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor map of transposed keys, bf16 [BH][chunks][P][128] (row d of a
-// chunk = dimension d over its 128 tokens), read as boxes of P rows x 64
-// tokens (128-byte rows, 128-byte swizzle): two boxes per chunk.
-inline bool kt_map(CUtensorMap* m, const void* base, int P, int chunks, int BH) {
+// Tensor map of transposed keys, bf16 [BH][chunks][P][row] (row d of a chunk
+// = dimension d over its 128 tokens, then `row` - 128 pad elements), read as
+// boxes of P rows x 64 tokens (128-byte rows, 128-byte swizzle): two boxes
+// per chunk.
+inline bool kt_map(CUtensorMap* m, const void* base, int P, int chunks, int BH, int row) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)chunks * P, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {256, (cuuint64_t)chunks * P * 256};
+    cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)chunks * P, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)row * 2, (cuuint64_t)chunks * P * row * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)P, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same transposed keys read as one box per chunk: P rows x `row`
+// elements, no swizzle (the rows land in shared memory `row` * 2 bytes apart,
+// pad included).
+inline bool kt_rows_map(CUtensorMap* m, const void* base, int P, int chunks, int BH, int row) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)chunks * P, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)row * 2, (cuuint64_t)chunks * P * row * 2};
+    cuuint32_t box[3] = {(cuuint32_t)row, (cuuint32_t)P, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
