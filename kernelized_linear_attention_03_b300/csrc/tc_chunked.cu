@@ -91,9 +91,10 @@ struct Cfg {
     static constexpr size_t smem = total + 1024;
     // tensor memory columns
     static constexpr uint32_t tm_s = 0;      // 64: fp32 state tile
-    // key-lift buffers: two for the block lifts (measured 10% faster at p = 64, g = 2), one for
-    // the full lift (the second one measured 3% slower there)
-    static constexpr int AKB = LG > 1 ? 2 : 1;
+    // key-lift buffers: two, so that the lift of the next chunk overlaps this
+    // chunk's update (with the readouts issued by a warp of their own: 2-4%
+    // faster than one buffer at p = 64)
+    static constexpr int AKB = 2;
     static constexpr uint32_t tm_ak = 64;    // AKB slots x 64: key lift (bf16 pairs of tokens); the last tile's lanes past the tail hold zeros
     static constexpr uint32_t tm_aq = 64 + 64 * AKB;  // 2 slots x 64: query lift (bf16 pairs of slots)
     static constexpr uint32_t tm_y = tm_aq + 128;    // 2 slots x 64: partial readout
@@ -325,12 +326,13 @@ __device__ __forceinline__ void store_state_tile(float* S_out, int tau, uint32_t
 //                         CTA: the same for Z, and the denominators)
 //   warps 8-11  key lift: lane = slot; multiplies two rows of the chunk's
 //                         transposed unit keys into the update's A operand
-//   warp 12     MMA:      per chunk the update (state += lift(K)^T V) and the
-//                         readout (Y = lift(Q) S) of the state before the
-//                         chunk (normaliser CTA: Z += Kh^T Kh and W = Q Z); the
+//   warp 12     MMA:      per chunk the update (state += lift(K)^T V)
+//                         (normaliser CTA: Z += Kh^T Kh and W = Q Z); the
 //                         whole warp runs the loop, one elected lane issues
 //   warp 13     loads:    lane 0 issues the TMA loads (transposed keys, values,
 //                         queries)
+//   warp 14     MMA:      per chunk the readout (Y = lift(Q) S) of the state
+//                         before the chunk (tile CTAs)
 template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkt,
@@ -343,7 +345,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qs_full[2], qs_free[2], kts_full[2], kts_free[2], v_full[2], v_free[2];
     __shared__ uint64_t qlift_full[2], aq_free[2], y_part[2], y_free[2], ys_full[2], ys_free[2];
-    __shared__ uint64_t klift_full[2], ak_free[2], upd_done, state_read, s16_ready, drain;
+    __shared__ uint64_t klift_full[2], ak_free[2], upd_done, state_read, s16_ready, drain, drain2;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -396,6 +398,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         mbar_init(&state_read, 128);
         mbar_init(&s16_ready, 128);
         mbar_init(&drain, 1);
+        mbar_init(&drain2, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -703,8 +706,11 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             tma_load_3d(q_buf(kk), &tmq, 0, row, (int)bh, &qs_full[slot]);
         }
     }
-    if (warp == 12) {
-        // =============================================================== MMA issuer
+    if (warp == 12 || (warp == 14 && !zc)) {
+        // =============================================================== MMA issuers
+        // Tile CTAs: warp 12 issues the updates, warp 14 the readouts (the two
+        // chains share no operand, and neither issuer's waits hold up the
+        // other's MMAs); the normaliser CTA: warp 12 issues both of its products.
         // The whole warp runs the issue loop (waits, descriptors) and one
         // elected lane issues each instruction: the operands stay warp-uniform,
         // which keeps the issue of back-to-back MMAs as cheap as a loop of
@@ -728,39 +734,43 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         for (int kk = 0; kk < nk; ++kk) {
             const int slot = kk & 1, use = kk >> 1;
             if (!zc) {
-                const int ab = kk % K::AKB, ause = kk / K::AKB;
-                if (!wait(&v_full[slot], use & 1) || !wait(&klift_full[ab], ause & 1) ||
-                    (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
-                    fail();
-                    break;
-                }
-                tc_fence_after();
-                // ---- update: state += lift(K)^T V
-                const uint64_t dv = d_v[slot];
+                if (warp == 12) {
+                    const int ab = kk % K::AKB, ause = kk / K::AKB;
+                    if (!wait(&v_full[slot], use & 1) || !wait(&klift_full[ab], ause & 1) ||
+                        (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
+                        fail();
+                        break;
+                    }
+                    tc_fence_after();
+                    // ---- update: state += lift(K)^T V
+                    const uint64_t dv = d_v[slot];
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts_w(tb + K::tm_s, tb + K::tm_ak + 64 * ab + 8 * ks, dv + ks * kStepMN, id_mn, 1u);
-                mma_commit_w(&ak_free[ab]);
-                mma_commit_w(&upd_done);
-                mma_commit_w(&v_free[slot]);
-                // ---- readout of the state before this chunk
-                if (!wait(&qlift_full[slot], use & 1) || (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1)) ||
-                    (kk >= 2 && !wait(&y_free[slot], (use - 1) & 1))) {
-                    fail();
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 64 * slot;
-                if (!tail) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts_w(tb + K::tm_s, tb + K::tm_ak + 64 * ab + 8 * ks, dv + ks * kStepMN, id_mn, 1u);
+                    mma_commit_w(&ak_free[ab]);
+                    mma_commit_w(&upd_done);
+                    mma_commit_w(&v_free[slot]);
                 } else {
+                    // ---- readout of the state before this chunk
+                    if (!wait(&qlift_full[slot], use & 1) || (kk >= 1 && !wait(&s16_ready, (kk - 1) & 1)) ||
+                        (kk >= 2 && !wait(&y_free[slot], (use - 1) & 1))) {
+                        fail();
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dy = tb + K::tm_y + 64 * slot, aq = tb + K::tm_aq + 64 * slot;
+                    if (!tail) {
 #pragma unroll
-                    for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
-                        mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < (K::TAIL + 15) / 16; ++ks)
+                            mma_ts_w(dy, aq + 8 * ks, d_s16 + ks * kStepMN, id_mn, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit_w(&y_part[slot]);
+                    mma_commit_w(&aq_free[slot]);
                 }
-                mma_commit_w(&y_part[slot]);
-                mma_commit_w(&aq_free[slot]);
             } else {
                 if (!wait(&kts_full[slot], use & 1) || (kk >= 1 && !wait(&state_read, (kk - 1) & 1))) {
                     fail();
@@ -792,8 +802,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
         }
         // every issued MMA has completed before tensor memory is released
-        mma_commit_w(&drain);
-        mbar_wait_quiet(&drain, 0, kWaitNs);
+        mma_commit_w(warp == 12 ? &drain : &drain2);
+        mbar_wait_quiet(warp == 12 ? &drain : &drain2, 0, kWaitNs);
     }
 
     tc_fence_before();
