@@ -2,14 +2,18 @@
 // order they keep internally (the rank-one lift paragraph after Eq. 8; the
 // packed width n = p(p+1)/2 of Eq. 8).
 //
-// Internal slot order.  With h = p/2, the n coordinates (i <= j) of the
-// upper triangle are laid out as
-//   slots [0, h*h)   "rectangle":  s = r*h + l            -> (i, j) = (r, h + l)
-//   slots [h*h, n)   "triangles":  s = h*h + r*h + l, r in [0, h]:
-//                       l >= r -> (r, l)          (upper-left triangle)
-//                       l <  r -> (h + l, h-1+r)  (lower-right triangle)
-// so that two consecutive slots (l even) nearly always share one factor and
-// take the other from an aligned pair of u: one bf16x2 multiply per pair.
+// Internal slot order.  With h = p/2, the n = h(2h+1) coordinates (i <= j)
+// of the upper triangle are laid out as 2h+1 rows of h slots, slot s in row
+// R = s / h at column l = s % h.  Even rows R = 2r < 2h are the "rectangle"
+// (r, h + l); odd rows R = 2r + 1 and the last row R = 2h (r = h) fold the
+// two triangles together:
+//   l >= r -> (r, l)          (upper-left triangle)
+//   l <  r -> (h + l, h-1+r)  (lower-right triangle)
+// Two consecutive slots (l even) nearly always share one factor and take the
+// other from an aligned pair of u: one bf16x2 multiply per pair.  Rectangle
+// and fold rows alternate so that every 128-slot tile of the tensor-core
+// kernels (a run of whole rows for p >= 16) holds as many of each: the fold
+// rows' lift costs a little more, and the slowest tile sets the pace.
 //
 // Internal scaling.  Keys are lifted without the sqrt(2) of the packed
 // Frobenius form: psiK(k)_(i,j) = k_i k_j.  Queries carry the whole factor 2
@@ -31,11 +35,12 @@ __host__ __device__ constexpr int tiles_of(int P) { return (packed_n(P) + 127) /
 // Coordinates (i, j), i <= j, of internal slot s < n.
 __host__ __device__ constexpr void slot_coord(int P, int s, int& i, int& j) {
     const int h = P / 2;
-    if (s < h * h) {
-        i = s / h;
-        j = h + s % h;
+    const int R = s / h, l = s % h;
+    if (R < 2 * h && (R & 1) == 0) {
+        i = R / 2;
+        j = h + l;
     } else {
-        const int q = s - h * h, r = q / h, l = q % h;
+        const int r = R < 2 * h ? R / 2 : h;
         if (l >= r) {
             i = r;
             j = l;
