@@ -102,15 +102,13 @@ struct TcPlan {
 };
 
 // lg: blocks of the lift (1: the full lift; g > 1: KATA-Sigma-g, whose state
-// has the width of the lift of one block, p/g).  Block lifts run as one
-// segment per head (the segment totals of the prepass use the full lift).
+// has the width of the lift of one block, p/g).
 TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv, int lg = 1) {
     TcPlan pl;
     if (dt != KATA_BF16 || !kata::chunked_tc_supports(p, dv, lg)) return pl;
     const int64_t BH = (int64_t)B * H, n = packed(p / lg);
     int G = kata::chunked_tc_segments(p, dv, lg, (int)BH, T);
     if (G <= 0) return pl;
-    if (lg > 1) G = 1;
     pl.use = true;
     pl.G = G;
     size_t off = 0;
@@ -122,6 +120,38 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv, int lg = 1) {
     pl.ws.i_off = off;
     pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, p, dv), 256);
     return pl;
+}
+
+// The tensor-core forward of a plan: one launch of the fused kernels when the
+// sequence is one segment per head; otherwise the segment totals of segments
+// 0..G-2 (chunk-state kernel), their exclusive prefixes seeded with the
+// initial state (the start state of every segment), then the fused kernels
+// with a start state per segment.  lg: blocks of the lift.
+cudaError_t launch_tc_forward(const TcPlan& pl, const void* q, const void* k, const void* v, void* o, void* ws,
+                              const float* S0, const float* z0, float* S_final, float* z_final, int64_t BH, int T,
+                              int p, int dv, int lg, kata_scan_mode mode, cudaStream_t stream) {
+    const ChunkedWs& w = pl.ws;
+    void* intra = static_cast<char*>(ws) + w.i_off;
+    if (pl.G == 1)
+        return kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, S_final, z_final, (int)BH, T, p, dv, lg, 1,
+                                       stream);
+    const int G = pl.G;
+    const int64_t n = packed(p / lg);
+    const int L = kata::chunked_tc_segment_chunks(T, G) * 128;
+    float* Sg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
+    float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
+    cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, 0, lg, stream);
+    if (e == cudaSuccess)
+        e = cudaMemset2DAsync(Sg + (size_t)(G - 1) * n * dv, sizeof(float) * (size_t)G * n * dv, 0,
+                              sizeof(float) * (size_t)n * dv, (size_t)BH, stream);
+    if (e == cudaSuccess)
+        e = cudaMemset2DAsync(zg + (size_t)(G - 1) * n, sizeof(float) * (size_t)G * n, 0, sizeof(float) * (size_t)n,
+                              (size_t)BH, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
+    if (e == cudaSuccess)
+        e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, lg, G, stream);
+    return e;
 }
 
 // Width of a lift (full, Sigma-g, M-g); -1 if (family, g) does not fit p.
@@ -238,31 +268,8 @@ kata_status kata_forward_chunked(const void* q, const void* k, const void* v, vo
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
         if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
     }
-    if (pl.use) {
-        void* intra = static_cast<char*>(ws) + w.i_off;
-        if (pl.G == 1)
-            return cuda_status(kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, S_final, z_final, (int)BH, T,
-                                                       p, dv, 1, 1, stream));
-        // segment totals of segments 0..G-2, then exclusive prefixes seeded
-        // with the initial state: the start state of every segment
-        const int G = pl.G, n32 = (int)n;
-        const int L = kata::chunked_tc_segment_chunks(T, G) * 128;
-        float* Sg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
-        float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
-        cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, 0, stream);
-        if (e == cudaSuccess)
-            e = cudaMemset2DAsync(Sg + (size_t)(G - 1) * n32 * dv, sizeof(float) * (size_t)G * n32 * dv, 0,
-                                  sizeof(float) * (size_t)n32 * dv, (size_t)BH, stream);
-        if (e == cudaSuccess)
-            e = cudaMemset2DAsync(zg + (size_t)(G - 1) * n32, sizeof(float) * (size_t)G * n32, 0,
-                                  sizeof(float) * (size_t)n32, (size_t)BH, stream);
-        if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
-        if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
-        if (e == cudaSuccess)
-            e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, 1, G,
-                                        stream);
-        return cuda_status(e);
-    }
+    if (pl.use)
+        return cuda_status(launch_tc_forward(pl, q, k, v, o, ws, S0, z0, S_final, z_final, BH, T, p, dv, 1, mode, stream));
 
     const int64_t NC = (T + C - 1) / C;
     float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
@@ -293,9 +300,9 @@ kata_status kata_chunk_state_scan(const void* k, const void* v, kata_dtype dt, i
     // order as it goes and writes the exclusive prefixes directly (one pass)
     if (dt == KATA_BF16 && mode == KATA_SCAN_SEQUENTIAL)
         return cuda_status(
-            kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 1, stream));
+            kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 1, 1, stream));
     cudaError_t e = dt == KATA_BF16
-                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 0, stream)
+                        ? kata::launch_states_tc(k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, (int)NC, (int)NC, 0, 1, stream)
                         : kata::launch_chunk_states_simt(dt, k, v, S_prefix, z_prefix, (int)BH, T, p, dv, C, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, S_prefix, S_prefix, nullptr, nullptr, BH, NC, n * dv, stream);
     if (e == cudaSuccess) e = kata::launch_scan(mode, z_prefix, z_prefix, nullptr, nullptr, BH, NC, n, stream);
@@ -389,8 +396,7 @@ kata_status kata_forward_chunked_block(const void* q, const void* k, const void*
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
     if ((st = check_buffer(ws, w.total)) != KATA_OK) return st;
     if (pl.use)
-        return cuda_status(kata::launch_chunked_tc(q, k, v, o, static_cast<char*>(ws) + w.i_off, S0, z0, 1, S_final,
-                                                   z_final, (int)BH, T, p, dv, g, 1, stream));
+        return cuda_status(launch_tc_forward(pl, q, k, v, o, ws, S0, z0, S_final, z_final, BH, T, p, dv, g, mode, stream));
     const int64_t NC = (T + C - 1) / C;
     float* S_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
     float* z_loc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);

@@ -21,10 +21,11 @@ unsigned int quadratic_tc_take_status();
 
 // Segment states on the tensor cores (bf16 k, v): for each head and each
 // of the first NS segments of L tokens, into S_out [BH, NS_out, n, dv] and
-// z_out [BH, NS_out, n] (fp32, sqrt(2)-packed order).  NS <= NS_out and
-// NS <= ceil(T / L).
+// z_out [BH, NS_out, n] (fp32, sqrt(2)-packed order), for the full lift
+// (lg = 1) or KATA-Sigma-g (lg = g > 1, n the lift width of one block).
+// NS <= NS_out and NS <= ceil(T / L).
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, int prefix, cudaStream_t s);
+                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s);
 unsigned int states_tc_take_status();
 
 // Chunked forward on the tensor cores (bf16): one CTA per (head, segment,

@@ -49,32 +49,64 @@ constexpr uint32_t kAOff = 0, kKOff = 4 * kAtom, kVOff = (4 + kStages) * kAtom,
 constexpr uint32_t kOutRow = 64 * 4 + 16;
 constexpr size_t kSmem = kOutOff + 128 * kOutRow + 1024;
 
+// Key lift word w (slots 2w, 2w+1) of the lift of width M = P / LG: the full
+// lift (LG = 1) or KATA-Sigma-g, the sum of the LG block lifts (products
+// accumulated by bf16x2 multiply-adds in block order, as the fused forward's
+// key lift does).
+template <int P, int LG>
+__device__ __forceinline__ uint32_t key_word(const uint32_t (&u)[P / 2], int w) {
+    constexpr int M = P / LG;
+    if constexpr (LG == 1) {
+        return lift::lift_word<M, false>(u, w);
+    } else {
+        constexpr int n = lift::packed_n(M);
+        const int s0 = 2 * w, s1 = 2 * w + 1;
+        if (s0 >= n) return 0u;
+        int i0 = 0, j0 = 0, i1 = 0, j1 = 0;
+        lift::slot_coord(M, s0, i0, j0);
+        if (s1 < n) {
+            lift::slot_coord(M, s1, i1, j1);
+        } else {
+            i1 = i0;
+            j1 = j0;
+        }
+        uint32_t r = 0u;
+#pragma unroll
+        for (int blk = 0; blk < LG; ++blk) {
+            const uint32_t* ub = u + blk * (M / 2);
+            const uint32_t x = lift::u_pair(ub, i0, i1), y = lift::u_pair(ub, j0, j1);
+            r = blk == 0 ? hmul2_bf16(x, y) : hfma2_bf16(x, y, r);
+        }
+        return s1 < n ? r : (r & 0xFFFFu);
+    }
+}
+
 // Lifted key coordinates of tile TAU for this thread's token into row `row`
 // of the token-major A tile.
-template <int P, int TAU>
+template <int P, int LG, int TAU>
 __device__ __forceinline__ void key_tile_to_smem(const uint32_t (&u)[P / 2], uint8_t* As, int row) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         uint4 val;
-        val.x = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 0);
-        val.y = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 1);
-        val.z = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 2);
-        val.w = lift::lift_word<P, false>(u, 64 * TAU + 4 * c + 3);
+        val.x = key_word<P, LG>(u, 64 * TAU + 4 * c + 0);
+        val.y = key_word<P, LG>(u, 64 * TAU + 4 * c + 1);
+        val.z = key_word<P, LG>(u, 64 * TAU + 4 * c + 2);
+        val.w = key_word<P, LG>(u, 64 * TAU + 4 * c + 3);
         *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
     }
 }
 
-template <int P, int TAU = 0>
+template <int P, int LG, int TAU = 0>
 __device__ __forceinline__ void key_tile_dispatch(int tau, const uint32_t (&u)[P / 2], uint8_t* As, int row) {
-    if constexpr (TAU < lift::tiles_of(P)) {
+    if constexpr (TAU < lift::tiles_of(P / LG)) {
         if (tau == TAU)
-            key_tile_to_smem<P, TAU>(u, As, row);
+            key_tile_to_smem<P, LG, TAU>(u, As, row);
         else
-            key_tile_dispatch<P, TAU + 1>(tau, u, As, row);
+            key_tile_dispatch<P, LG, TAU + 1>(tau, u, As, row);
     }
 }
 
-template <int P, int DV>
+template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS, int NS_out,
@@ -84,7 +116,8 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     // segment order in the epilogue's registers, instead of the segment's own total
     // T: tokens per head; segments 0..NS-1 of L tokens (L a multiple of 128,
     // or L <= 128) are computed into rows of a [BH, NS_out, n] layout.
-    constexpr int n = lift::packed_n(P);
+    constexpr int M = P / LG;  // width of the lifted blocks (P for the full lift)
+    constexpr int n = lift::packed_n(M);
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t k_full[kStages], v_full[kStages], kv_free[kStages], a_full[2], a_free[2];
     __shared__ uint64_t acc_full[2], acc_free[2], drain;
@@ -232,7 +265,7 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
                         u[4 * c + j] = pack_bf16x2(__bfloat162float(e[2 * j]) * inv, __bfloat162float(e[2 * j + 1]) * inv);
                 }
             }
-            key_tile_dispatch<P>(tau, u, sm + kAOff + 2 * ab * kAtom, lt);
+            key_tile_dispatch<P, LG>(tau, u, sm + kAOff + 2 * ab * kAtom, lt);
             fence_proxy_async_smem();
             mbar_arrive(&a_full[ab]);
         }
@@ -245,9 +278,9 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const uint32_t lane0 = (uint32_t)((warp & 3) * 32);
         const int slot = tau * 128 + e;
         int ci = 0, cj = 0;
-        if (slot < n) lift::slot_coord(P, slot, ci, cj);
+        if (slot < n) lift::slot_coord(M, slot, ci, cj);
         const float f = ci < cj ? kSqrt2f : 1.f;
-        const int my_canon = slot < n ? lift::canonical_index(P, ci, cj) : -1;
+        const int my_canon = slot < n ? lift::canonical_index(M, ci, cj) : -1;
         uint8_t* stage = sm + kOutOff;
         float run[DV + 1];  // running sum of the segment totals (prefix mode)
 #pragma unroll
@@ -258,31 +291,37 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             if (!wait(&acc_full[acb], (sl >> 1) & 1)) { fail(); break; }
             tc_fence_after();
             const int64_t base = (bh * NS_out + seg) * (int64_t)n;
-            // 16 columns at a time: out = the segment's total, or (prefix mode)
-            // the sum before it, into the staging row
+            // 32 columns per tensor-memory wait (the last wait also brings the
+            // ones column, z): out = the segment's total, or (prefix mode) the
+            // sum before it, into the staging row
             __syncwarp();  // this warp's previous rows have left the staging
+            uint32_t zr = 0;
 #pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tmem_addr(tb + 128 * acb, lane0, c0), r);
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+                uint32_t r[2][16];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    if (c0 + 16 * hh < DV) tmem_ld16(tmem_addr(tb + 128 * acb, lane0, c0 + 16 * hh), r[hh]);
+                if (c0 + 32 >= DV) zr = tmem_ld1(tmem_addr(tb + 128 * acb, lane0, 64));  // the ones column: z
                 tmem_wait_ld();
-                float out[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float tot = __uint_as_float(r[i]);
-                    out[i] = prefix ? run[c0 + i] : tot;
-                    run[c0 + i] += tot;
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (c0 + 16 * hh >= DV) continue;
+                    float out[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float tot = __uint_as_float(r[hh][i]);
+                        out[i] = prefix ? run[c0 + 16 * hh + i] : tot;
+                        run[c0 + 16 * hh + i] += tot;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<float4*>(stage + e * kOutRow + 4 * (c0 + 16 * hh + 4 * c)) =
+                            make_float4(f * out[4 * c], f * out[4 * c + 1], f * out[4 * c + 2], f * out[4 * c + 3]);
                 }
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4*>(stage + e * kOutRow + 4 * (c0 + 4 * c)) =
-                        make_float4(f * out[4 * c], f * out[4 * c + 1], f * out[4 * c + 2], f * out[4 * c + 3]);
             }
             {
-                uint32_t r[16];
-                tmem_ld16(tmem_addr(tb + 128 * acb, lane0, 64), r);  // the ones column: z
-                tmem_wait_ld();
-                const float tot = __uint_as_float(r[0]);
+                const float tot = __uint_as_float(zr);
                 const float zo = prefix ? run[DV] : tot;
                 run[DV] += tot;
                 if (slot < n) z_out[base + my_canon] = f * zo;
@@ -290,15 +329,27 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             tc_fence_before();
             mbar_arrive(&acc_free[acb]);
             __syncwarp();
-            for (int rr = 0; rr < 32; ++rr) {
-                const int canon = __shfl_sync(0xffffffffu, my_canon, rr);
-                if (canon < 0) continue;
-                const uint8_t* src = stage + (32 * ew + rr) * kOutRow;
-                float* dst = S_out + (base + canon) * DV;
-                if (DV == 64) {
-                    reinterpret_cast<float2*>(dst)[lane] = *reinterpret_cast<const float2*>(src + 8 * lane);
-                } else if (lane < DV) {
-                    dst[lane] = *reinterpret_cast<const float*>(src + 4 * lane);
+            if (DV == 64) {
+                // two rows per store instruction (16 bytes a lane), unrolled so
+                // that the staging loads and the stores of several rows are in
+                // flight at once
+                const int half = lane >> 4, c16 = lane & 15;
+#pragma unroll 4
+                for (int rr = 0; rr < 32; rr += 2) {
+                    const int row = rr + half;
+                    const int canon = __shfl_sync(0xffffffffu, my_canon, row);
+                    if (canon >= 0) {
+                        const float4 val = *reinterpret_cast<const float4*>(stage + (32 * ew + row) * kOutRow + 16 * c16);
+                        *reinterpret_cast<float4*>(S_out + (base + canon) * DV + 4 * c16) = val;
+                    }
+                }
+            } else {
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int canon = __shfl_sync(0xffffffffu, my_canon, rr);
+                    if (canon < 0) continue;
+                    const uint8_t* src = stage + (32 * ew + rr) * kOutRow;
+                    float* dst = S_out + (base + canon) * DV;
+                    if (lane < DV) dst[lane] = *reinterpret_cast<const float*>(src + 4 * lane);
                 }
             }
         }
@@ -309,15 +360,15 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     if (warp == 0) tmem_dealloc(tb, 256);
 }
 
-template <int P, int DV>
+template <int P, int DV, int LG>
 cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_out, int BH, int T, int L,
                          int NS, int NS_out, int prefix, cudaStream_t s) {
-    auto kern = states_tc_kernel<P, DV>;
+    auto kern = states_tc_kernel<P, DV, LG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     CUtensorMap tk, tv;
     if (!rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH)) return cudaErrorInvalidValue;
-    const int tiles = lift::tiles_of(P);
+    const int tiles = lift::tiles_of(P / LG);
     // about two CTAs per SM in total, each a run of segments
     const int64_t units = (int64_t)tiles * BH;
     int groups = prefix ? 1 : (int)((2 * 148) / (units > 0 ? units : 1));
@@ -332,13 +383,18 @@ cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_ou
 }  // namespace
 
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, int prefix, cudaStream_t s) {
+                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s) {
     if (NS <= 0) return cudaSuccess;
-#define KATA_CASE(P_, DV_) \
-    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, prefix, s);
-    KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
-    KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
-    KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)
+#define KATA_CASE(P_, DV_, LG_)                  \
+    if (p == P_ && dv == DV_ && lg == LG_) \
+        return launch_typed<P_, DV_, LG_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, prefix, s);
+    KATA_CASE(16, 16, 1) KATA_CASE(16, 32, 1) KATA_CASE(16, 64, 1)
+    KATA_CASE(32, 16, 1) KATA_CASE(32, 32, 1) KATA_CASE(32, 64, 1)
+    KATA_CASE(64, 16, 1) KATA_CASE(64, 32, 1) KATA_CASE(64, 64, 1)
+    // KATA-Sigma-g: the block widths of the fused forward (p = 32, g = 2; p = 64, g = 2 or 4)
+    KATA_CASE(32, 16, 2) KATA_CASE(32, 32, 2) KATA_CASE(32, 64, 2)
+    KATA_CASE(64, 16, 2) KATA_CASE(64, 32, 2) KATA_CASE(64, 64, 2)
+    KATA_CASE(64, 16, 4) KATA_CASE(64, 32, 4) KATA_CASE(64, 64, 4)
 #undef KATA_CASE
     return cudaErrorInvalidValue;
 }

@@ -156,6 +156,11 @@ def test_sigma_tensor_core_forward(g, p, dv, T):
     q, k, v = _tokens(1, 3, T, p, dv, torch.bfloat16, seed=7 * g + p + T)
     o, names = _traced(lambda: kb.kata_forward_chunked_block(q, k, v, 128, SIGMA, g))
     assert "chunked_tc" in names and "intra_tc" in names, names
+    # three heads leave CTAs free, so a sequence of more than one 128-token
+    # chunk is cut into segments whose start states come from the chunk-state
+    # kernel's segment totals (block lift) and the scan
+    if T > 128:
+        assert "states_tc" in names, names
     assert_close(f64(o), oracle.forward_plain_block(f64(q), f64(k), f64(v), SIGMA, g), torch.bfloat16,
                  "Sigma tensor cores")
 
