@@ -78,21 +78,59 @@ gated_states_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v, const 
 // ---------------------------------------------------------------- gated prefix
 // x [heads][NC][W] -> exclusive gated prefix in place: y_c = P_c with P_0 =
 // init (or 0) and P_{c+1} = a_c P_c + x_c; fin (or null) receives P_NC.
-// One thread per column, one step per chunk.
+// One thread per VEC consecutive columns, one step per chunk; the values of
+// kBatch chunks are loaded before any of them is overwritten, so that the
+// loads of a batch are in flight together (each step's store would otherwise
+// hold back the next chunk's load).
+constexpr int kBatch = 8;
+
+template <int VEC>
 __global__ void gated_scan_kernel(float* __restrict__ x, const float* __restrict__ a, const float* __restrict__ init,
                                   float* __restrict__ fin, int64_t heads, int64_t NC, int64_t W) {
+    const int64_t per_head = W / VEC;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= heads * W) return;
-    const int64_t h = gid / W, e = gid - h * W;
-    float run = init ? init[h * W + e] : 0.f;
+    if (gid >= heads * per_head) return;
+    const int64_t h = gid / per_head, e = (gid - h * per_head) * VEC;
+    float run[VEC];
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) run[u] = init ? init[h * W + e + u] : 0.f;
     float* col = x + h * NC * W + e;
     const float* ah = a + h * NC;
-    for (int64_t c = 0; c < NC; ++c) {
-        const float xc = col[c * W];
-        col[c * W] = run;
-        run = fmaf(ah[c], run, xc);
+    for (int64_t c0 = 0; c0 < NC; c0 += kBatch) {
+        float xv[kBatch][VEC], av[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const bool live = c0 + b < NC;
+            av[b] = live ? ah[c0 + b] : 0.f;
+            if (VEC == 4) {
+                const float4 t = live ? *reinterpret_cast<const float4*>(col + (c0 + b) * W) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[b][0] = t.x;
+                xv[b][VEC > 1 ? 1 : 0] = t.y;
+                xv[b][VEC > 2 ? 2 : 0] = t.z;
+                xv[b][VEC > 3 ? 3 : 0] = t.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) xv[b][u] = live ? col[(c0 + b) * W + u] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (c0 + b >= NC) break;
+            if (VEC == 4) {
+                *reinterpret_cast<float4*>(col + (c0 + b) * W) =
+                    make_float4(run[0], run[VEC > 1 ? 1 : 0], run[VEC > 2 ? 2 : 0], run[VEC > 3 ? 3 : 0]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) col[(c0 + b) * W + u] = run[u];
+            }
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) run[u] = fmaf(av[b], run[u], xv[b][u]);
+        }
     }
-    if (fin) fin[h * W + e] = run;
+    if (fin) {
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) fin[h * W + e + u] = run[u];
+    }
 }
 
 // ---------------------------------------------------------------- chunk output
@@ -231,10 +269,19 @@ cudaError_t gated_typed(const void* q, const void* k, const void* v, const float
     }
     for (int part = 0; part < 2; ++part) {
         const int64_t W = part == 0 ? (int64_t)N * DV : N;
-        const int64_t threads = (int64_t)BH * W;
-        KATA_TRACED("gated_scan", s,
-                    (gated_scan_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-                        part == 0 ? X : Xz, a, part == 0 ? S0 : z0, part == 0 ? S_final : z_final, BH, NC, W)));
+        float* xs = part == 0 ? X : Xz;
+        const float* init = part == 0 ? S0 : z0;
+        float* fin = part == 0 ? S_final : z_final;
+        auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+        if (W % 4 == 0 && a16(xs)) {
+            const int64_t threads = (int64_t)BH * (W / 4);
+            KATA_TRACED("gated_scan", s,
+                        (gated_scan_kernel<4><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xs, a, init, fin, BH, NC, W)));
+        } else {
+            const int64_t threads = (int64_t)BH * W;
+            KATA_TRACED("gated_scan", s,
+                        (gated_scan_kernel<1><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xs, a, init, fin, BH, NC, W)));
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
