@@ -111,7 +111,7 @@ def kernel_work(name, w, form="chunked", lift=None):
         return "flop", bht * (2 * w.n * (w.dv + 1) + (w.C + 1) * (w.p + w.dv))
     if name in ("scan_tree", "scan_sequential"):
         return "byte", 2 * w.B * w.H * w.NC * w.n * (w.dv + 1) * 4
-    if name == "quadratic_tc" or name == "quadratic_simt":
+    if name in ("quadratic_tc", "quadratic_simt", "quadratic_gated_tc"):
         # causal half of the flash-style form: (T+1)(p+dv) per head-token
         return "flop", bht * (w.T + 1) * (w.p + w.dv)
     if name == "states_tc" and form == "chunk_state_scan":
@@ -143,6 +143,9 @@ def kernel_work(name, w, form="chunked", lift=None):
     if name in ("gated_scan", "backward_reverse_scan"):
         nc = w.NC if name == "gated_scan" else (w.T + 63) // 64
         return "byte", 2 * w.B * w.H * nc * w.n * (w.dv + 1) * 4
+    if name == "gate_prefix":
+        # the gates read, the per-token log-gate sums and last zero gates written
+        return "byte", bht * 12
     if name == "decode_step":
         # state and normaliser read and written once, the token's q, k, v read, o written
         elem = 4 if w.dtype == "fp32" else 2
@@ -380,6 +383,14 @@ def run_ours(args, world, rank, local):
 
         def step():
             kb.kata_backward(q, k, v, dO, dq, dk, dvv, workspace=wsg, stream=stream, form=bform)
+    elif args.form == "quadratic_gated":
+        g = torch.Generator(device=dev).manual_seed(rank)
+        gate = torch.rand((w.B, w.H, w.T), generator=g, device=dev) * 0.1 + 0.9
+        wsq = torch.empty(max(1, kb.load().kata_quadratic_gated_workspace_bytes(kb._dtype_code(q), w.B, w.H, w.T)),
+                          dtype=torch.uint8, device=dev)
+
+        def step():
+            kb.kata_forward_quadratic_gated(q, k, v, gate, o=o, workspace=wsq, stream=stream)
     elif args.form == "gated":
         g = torch.Generator(device=dev).manual_seed(rank)
         gate = torch.rand((w.B, w.H, w.T), generator=g, device=dev) * 0.1 + 0.9
@@ -577,7 +588,7 @@ def main():
                     help="dram bytes per call of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--form", default="chunked",
-                    choices=["chunked", "quadratic", "scan", "chunk_state_scan", "decode", "backward",
+                    choices=["chunked", "quadratic", "quadratic_gated", "scan", "chunk_state_scan", "decode", "backward",
                              "backward_quadratic", "gated"] + list(BLOCK_FORMS),
                     help="entry point timed (the contract's line is the chunked forward)")
     ap.add_argument("--lift", default="sigma", choices=sorted(LIFTS), help="block-lift family of the *_block forms")

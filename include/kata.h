@@ -237,6 +237,23 @@ KATA_API kata_status kata_forward_chunked_gated(const void* q, const void* k, co
                                                 void* workspace, size_t workspace_bytes,
                                                 cudaStream_t stream);
 
+/*
+ * Gated prefix, flash-style form: the same output as kata_forward_chunked_gated
+ * by the O(T^2) route of kata_forward_quadratic, each weight
+ * (qh_t.kh_s)^2 carrying the decay prod_{r=s+1..t} gate_r (the gated readout
+ * written out over all earlier tokens).  bf16 only (KATA_ERR_UNSUPPORTED for
+ * fp32 inputs); gates in [0, 1] (a zero gate forgets everything before its
+ * token; values outside [0, 1] are not supported by this form).  The decays
+ * are taken from per-token sums of log gates (fp64, stored fp32) in the
+ * workspace: at least kata_quadratic_gated_workspace_bytes() bytes, 256-byte
+ * aligned.  q, k, v, o, gate and errors as kata_forward_chunked_gated.
+ */
+KATA_API size_t kata_quadratic_gated_workspace_bytes(kata_dtype dtype, int B, int H, int T);
+KATA_API kata_status kata_forward_quadratic_gated(const void* q, const void* k, const void* v,
+                                                  const float* gate, void* o, kata_dtype dtype, int B,
+                                                  int H, int T, int p, int dv, void* workspace,
+                                                  size_t workspace_bytes, cudaStream_t stream);
+
 /* Gated decode step: as kata_decode_step with the state scaled by the head's
  * gate [B,H] fp32 first (S = gate S + psi(kh) v^T, z likewise). */
 KATA_API kata_status kata_decode_step_gated(const void* q, const void* k, const void* v,

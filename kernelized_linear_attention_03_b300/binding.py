@@ -34,7 +34,8 @@ SYMBOLS = ("kata_packed_dim", "kata_status_string", "kata_forward_quadratic",
            "kata_chunked_block_workspace_bytes", "kata_forward_chunked_block", "kata_forward_quadratic_block",
            "kata_decode_step_block", "kata_backward_quadratic_workspace_bytes",
            "kata_backward_quadratic", "kata_backward_chunked_workspace_bytes", "kata_backward_chunked",
-           "kata_chunked_gated_workspace_bytes", "kata_forward_chunked_gated", "kata_decode_step_gated")
+           "kata_chunked_gated_workspace_bytes", "kata_forward_chunked_gated", "kata_decode_step_gated",
+           "kata_quadratic_gated_workspace_bytes", "kata_forward_quadratic_gated")
 
 
 class KataError(RuntimeError):
@@ -98,6 +99,10 @@ def load():
     lib.kata_chunked_gated_workspace_bytes.restype = Z
     lib.kata_forward_chunked_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, Z, P]
     lib.kata_forward_chunked_gated.restype = I
+    lib.kata_quadratic_gated_workspace_bytes.argtypes = [I, I, I, I]
+    lib.kata_quadratic_gated_workspace_bytes.restype = Z
+    lib.kata_forward_quadratic_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+    lib.kata_forward_quadratic_gated.restype = I
     lib.kata_decode_step_gated.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
     lib.kata_decode_step_gated.restype = I
     lib.kata_trace_start.argtypes = [I]
@@ -349,6 +354,25 @@ def kata_forward_chunked_gated(q, k, v, gate, C, S0=None, z0=None, o=None, S_fin
                                              _ptr(workspace), ws_bytes, _stream(stream)),
            "kata_forward_chunked_gated")
     return o if S_final is None else (o, S_final, z_final)
+
+
+def kata_forward_quadratic_gated(q, k, v, gate, o=None, workspace=None, stream=None):
+    """Gated flash-style forward (bf16, gates in [0, 1]); gate [B,H,T] float32.
+    Returns o."""
+    B, H, T, p, dv = _shapes(q, k, v)
+    if gate.shape != (B, H, T) or gate.dtype != torch.float32:
+        raise ValueError("expected a float32 gate [B,H,T]")
+    if o is None:
+        o = torch.empty_like(v)
+    need = int(load().kata_quadratic_gated_workspace_bytes(_dtype_code(q), B, H, T))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _used_on(workspace, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().kata_forward_quadratic_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _dtype_code(q), B, H,
+                                               T, p, dv, _ptr(workspace), ws_bytes, _stream(stream)),
+           "kata_forward_quadratic_gated")
+    return o
 
 
 def kata_decode_step_gated(q, k, v, gate, S, z, o=None, stream=None):

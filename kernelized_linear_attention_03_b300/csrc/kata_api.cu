@@ -225,6 +225,32 @@ kata_status kata_forward_quadratic(const void* q, const void* k, const void* v, 
     return cuda_status(kata::launch_quadratic_simt(dt, q, k, v, o, B * H, T, p, dv, stream));
 }
 
+size_t kata_quadratic_gated_workspace_bytes(kata_dtype dt, int B, int H, int T) {
+    if (dt != KATA_BF16 || B < 0 || H < 0 || T < 0) return 0;
+    if ((int64_t)B * H * T == 0) return 0;
+    return kata::quadratic_gated_tc_workspace(B * H, T);
+}
+
+kata_status kata_forward_quadratic_gated(const void* q, const void* k, const void* v, const float* gate, void* o,
+                                         kata_dtype dt, int B, int H, int T, int p, int dv, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream) {
+    kata_status st = check_shapes(dt, B, H, T, p, dv);
+    if (st != KATA_OK) return st;
+    if (dt != KATA_BF16) return KATA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return KATA_OK;
+    const size_t qk_bytes = elem_bytes(dt) * rows * p, v_bytes = elem_bytes(dt) * rows * dv;
+    if ((st = check_buffer(q, qk_bytes)) != KATA_OK || (st = check_buffer(k, qk_bytes)) != KATA_OK ||
+        (st = check_buffer(v, v_bytes)) != KATA_OK || (st = check_buffer(o, v_bytes)) != KATA_OK ||
+        (st = check_buffer(gate, sizeof(float) * rows)) != KATA_OK)
+        return st;
+    const size_t need = kata::quadratic_gated_tc_workspace(B * H, T);
+    if (ws == nullptr || ws_bytes < need) return KATA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KATA_ERR_INVALID_ARG;
+    if ((st = check_buffer(ws, need)) != KATA_OK) return st;
+    return cuda_status(kata::launch_quadratic_gated_tc(q, k, v, gate, o, ws, B * H, T, p, dv, stream));
+}
+
 size_t kata_chunked_workspace_bytes(kata_dtype dt, int B, int H, int T, int p, int dv, int C) {
     if (check_shapes(dt, B, H, T, p, dv) != KATA_OK || !c_ok(C)) return 0;
     if ((int64_t)B * H * T == 0) return 0;

@@ -17,6 +17,12 @@ cudaError_t launch_quadratic_simt(int dtype, const void* q, const void* k, const
 cudaError_t launch_quadratic_tc(const void* q, const void* k, const void* v, void* o, int BH, int T,
                                 int p, int dv, cudaStream_t s);
 // Read and clear the device status word of the tensor-core quadratic kernel.
+// Gated flash-style form (bf16): per-token log-gate sums and last zero gates
+// into ws (quadratic_gated_tc_workspace bytes, 256-byte aligned), then the
+// tensor-core kernel with the decays in its weights.
+size_t quadratic_gated_tc_workspace(int BH, int T);
+cudaError_t launch_quadratic_gated_tc(const void* q, const void* k, const void* v, const float* gate, void* o,
+                                      void* ws, int BH, int T, int p, int dv, cudaStream_t s);
 unsigned int quadratic_tc_take_status();
 
 // Segment states on the tensor cores (bf16 k, v): for each head and each

@@ -12,6 +12,18 @@
 // denominator alike and cancels.  Scores of unit keys with a fixed query are
 // bounded, so no running maximum or rescale is needed.
 //
+// Gated form (GATED): every weight also carries the decay of the gates after
+// its key, G(t, s) = prod_{r=s+1..t} gamma_r.  With L_t the sum of log gamma_r
+// since the last zero gate z_t <= t (both from gate_prefix_kernel),
+// G(t, s) = [z_t <= s] exp(L_t - L_s).  A factor of a whole row cancels between
+// numerator and denominator, so when the CTA's query rows share their last
+// zero gate (none inside its tiles) and their decay is moderate (L at the
+// first row minus L at the last below kSpanMax), each weight takes the key's
+// factor exp(R - L_s) alone, R = L at the CTA's last row (at most 1 for gates
+// in [0, 1]; 0 for keys before the zero gate): the key warps scale each unit
+// key by the square root of its factor, and the scores and their squares are
+// then those of the ungated form.  Other CTAs take exp(L_t - L_s) per weight.
+//
 // Pipeline (one CTA per pair of query tiles A = 2m, B = 2m + 1, sharing
 // every key / value tile they both need; 512 threads):
 //   warp 0 lane 0   TMA: both query tiles once, key and value tiles into a
@@ -27,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kata_internal.h"
 #include "tc_primitives.cuh"
@@ -45,19 +58,86 @@ constexpr int kStages = 4;        // key / value ring
 constexpr uint32_t kAtom = 128 * 128;
 constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value slots, the ones column, pad
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every device-side wait
+constexpr float kSpanMax = 80.f;  // decay span of a query tile (natural log) below which its weights take key factors
+constexpr float kLog2e = 1.44269504088896340736f;
 
 // shared memory, 16 KB atoms from a 1024-byte aligned base: Q_A, Q_B,
 // K[kStages], V[kStages], the ones atom (last, so every value stage reaches
 // it with a positive atom stride)
 constexpr uint32_t kQOff = 0, kKOff = 2 * kAtom, kVOff = (2 + kStages) * kAtom, kOnesOff = (2 + 2 * kStages) * kAtom;
+// gated form, after the ones atom: per key stage, L_s of the tile's keys (fp32)
+constexpr uint32_t kGateOff = (3 + 2 * kStages) * kAtom, kGateStage = kTile * 4;
 constexpr size_t kSmem = (3 + 2 * kStages) * kAtom + 1024;
+constexpr size_t kSmemGated = kSmem + kStages * kGateStage;
 // tensor memory: scores (then squared weights, in place) and O per query tile
 constexpr uint32_t kTmS = 0, kTmO = 256;  // tile g: S at 128 g, O at 256 + 128 g
 
-template <int P, int DV>
+// Per head, for every token t: L_t = sum of log gamma_r over r in (z_t, t]
+// (fp32 logs summed in fp64) and z_t, the position of the last zero gate at or
+// before t (-1 if none).  One block of kPrefixThreads per head: each thread
+// takes a run of consecutive tokens, the runs' (sum, last zero) pairs are
+// combined by a scan (a later zero restarts the sum), then every thread walks
+// its run again from its prefix.
+constexpr int kPrefixThreads = 1024;
+
+__global__ void __launch_bounds__(kPrefixThreads)
+gate_prefix_kernel(const float* __restrict__ gate, float* __restrict__ Lc, int* __restrict__ zid, int T) {
+    __shared__ double ssum[kPrefixThreads];
+    __shared__ int szero[kPrefixThreads];
+    const int t = threadIdx.x;
+    const int64_t base = (int64_t)blockIdx.x * T;
+    const int run = (T + kPrefixThreads - 1) / kPrefixThreads;
+    const int a = min(T, t * run), b = min(T, a + run);
+    double sum = 0.0;
+    int zero = -1;
+    for (int r = a; r < b; ++r) {
+        const float gm = gate[base + r];
+        if (gm == 0.f) {
+            zero = r;
+            sum = 0.0;
+        } else {
+            sum += (double)logf(gm);
+        }
+    }
+    ssum[t] = sum;
+    szero[t] = zero;
+    __syncthreads();
+    // inclusive scan of the runs: (s1, z1) then (s2, z2) -> z2 >= 0 ? (s2, z2) : (s1 + s2, z1)
+    for (int d = 1; d < kPrefixThreads; d <<= 1) {
+        double ps = 0.0;
+        int pz = -1;
+        const bool has = t >= d;
+        if (has) {
+            ps = ssum[t - d];
+            pz = szero[t - d];
+        }
+        __syncthreads();
+        if (has && szero[t] < 0) {
+            ssum[t] = ps + ssum[t];
+            szero[t] = pz;
+        }
+        __syncthreads();
+    }
+    double cur = t > 0 ? ssum[t - 1] : 0.0;
+    int cz = t > 0 ? szero[t - 1] : -1;
+    for (int r = a; r < b; ++r) {
+        const float gm = gate[base + r];
+        if (gm == 0.f) {
+            cz = r;
+            cur = 0.0;
+        } else {
+            cur += (double)logf(gm);
+        }
+        Lc[base + r] = (float)cur;
+        zid[base + r] = cz;
+    }
+}
+
+template <int P, int DV, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int T) {
+                    const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int T,
+                    const float* __restrict__ Lc, const int* __restrict__ zid) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_ready[kStages], kv_free[kStages];
     __shared__ uint64_t s_full[2], p_full[2], o_done, drain;
@@ -73,6 +153,18 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const bool has_b = qb < ntiles;
     const int last[2] = {qa, has_b ? qb : -1};  // last key tile of each query tile
     const int nj = has_b ? qb + 1 : qa + 1;     // key tiles loaded
+    // gated form: whether the weights of this CTA's rows take key factors, the
+    // reference R and the rows' common last zero gate
+    bool gfast = false;
+    float gref = 0.f;
+    int gzero = -1;
+    if (GATED) {
+        const int r0 = qa * kTile, r1 = min(T, nj * kTile) - 1;
+        const float l0 = Lc[bh * T + r0], l1 = Lc[bh * T + r1];
+        gref = l1;
+        gzero = zid[bh * T + r1];
+        gfast = gzero < r0 && l0 - l1 < kSpanMax && l0 - l1 >= 0.f;
+    }
 
     if (t == 0) {
         mbar_init(&q_full, 1);
@@ -186,8 +278,16 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     } else if (warp >= 12) {
         // =============================================================== key normalisation
         const int r = t - 384;
+        // gated form: L of this thread's key in the next tile, loaded one tile
+        // ahead so that its latency overlaps the wait for the tile
+        float lk_next = (GATED && r < T) ? Lc[bh * T + r] : 0.f;
         for (int j = 0; j < nj; ++j) {
             const int st = j % kStages;
+            const float lk = lk_next;
+            if (GATED) {
+                const int nk = (j + 1) * kTile + r;
+                lk_next = (j + 1 < nj && nk < T) ? Lc[bh * T + nk] : 0.f;
+            }
             if (!wait(&k_full[st], (j / kStages) & 1)) { fail(); break; }
             uint8_t* kb = sm + kKOff + st * kAtom;
             uint4 raw[P / 8];
@@ -202,7 +302,14 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     ss = fmaf(x, x, ss);
                 }
             }
-            const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+            if (GATED) {
+                // the key's L (exact weights), or the unit key scaled by the
+                // square root of its factor (0 before the zero gate and past T)
+                const int key = j * kTile + r;
+                reinterpret_cast<float*>(sm + kGateOff + st * kGateStage)[r] = lk;
+                if (gfast) inv = (key < T && key >= gzero) ? inv * exp2f(0.5f * (gref - lk) * kLog2e) : 0.f;
+            }
 #pragma unroll
             for (int c = 0; c < P / 8; ++c) {
                 const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw[c]);
@@ -223,40 +330,73 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const int wq = (warp & 3);        // this warp's rows are 32 wq .. 32 wq + 31
         const uint32_t lane0 = (uint32_t)(wq * 32);
         const uint32_t sb = tb + kTmS + 128 * g;
-        for (int j = 0; j <= last[g]; ++j) {
-            if (!wait(&s_full[g], j & 1)) { fail(); break; }
-            tc_fence_after();
-            const bool diag = j == last[g];  // keys past the query are masked only on the diagonal tile
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t pk[16];
-                if (!diag || q4 <= wq) {
-                    uint32_t sc[32];
-                    tmem_ld16(tmem_addr(sb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
-                    tmem_ld16(tmem_addr(sb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int col = 32 * q4 + 2 * i;
-                        float a = __uint_as_float(sc[2 * i]), c = __uint_as_float(sc[2 * i + 1]);
-                        a *= a;
-                        c *= c;
-                        if (diag) {
-                            a = col <= e ? a : 0.f;
-                            c = col + 1 <= e ? c : 0.f;
-                        }
-                        pk[i] = pack_bf16x2(a, c);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
-                }
-                tmem_st16(tmem_addr(sb, lane0, 16 * q4), pk);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[g]);
+        // gated form: this row's L and last zero gate (exact weights)
+        float lrow = 0.f;
+        int zrow = -1;
+        if (GATED) {
+            const int row = min(T - 1, last[g] * kTile + e);
+            lrow = Lc[bh * T + row];
+            zrow = zid[bh * T + row];
         }
+        // P of key tile j in place of its scores; EXACT: every weight with its
+        // own decay exp(L_t - L_s) (gated CTAs outside the key-factor range),
+        // otherwise the squares as they are (the ungated form, and gated CTAs
+        // whose key factors are already in the unit keys).  Two compiled loops,
+        // chosen once per CTA, so the squaring of the common case stays lean.
+        auto square = [&](auto exact_tag) -> bool {
+            constexpr bool EXACT = decltype(exact_tag)::value;
+            for (int j = 0; j <= last[g]; ++j) {
+                if (!wait(&s_full[g], j & 1)) return false;
+                // the key tile's L values are in shared memory (its staging completed before the scores' MMA)
+                if (EXACT && !wait(&k_ready[j % kStages], (j / kStages) & 1)) return false;
+                tc_fence_after();
+                const bool diag = j == last[g];  // keys past the query are masked only on the diagonal tile
+                const float* gs = reinterpret_cast<const float*>(sm + kGateOff + (j % kStages) * kGateStage);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[16];
+                    if (!diag || q4 <= wq) {
+                        uint32_t sc[32];
+                        tmem_ld16(tmem_addr(sb, lane0, 32 * q4), *reinterpret_cast<uint32_t(*)[16]>(sc));
+                        tmem_ld16(tmem_addr(sb, lane0, 32 * q4 + 16), *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int col = 32 * q4 + 2 * i;
+                            float a = __uint_as_float(sc[2 * i]), c = __uint_as_float(sc[2 * i + 1]);
+                            a *= a;
+                            c *= c;
+                            if (EXACT) {
+                                const float2 lk = *reinterpret_cast<const float2*>(gs + col);
+                                const int key = j * kTile + col;
+                                a = zrow <= key ? a * exp2f((lrow - lk.x) * kLog2e) : 0.f;
+                                c = zrow <= key + 1 ? c * exp2f((lrow - lk.y) * kLog2e) : 0.f;
+                            }
+                            if (diag) {
+                                a = col <= e ? a : 0.f;
+                                c = col + 1 <= e ? c : 0.f;
+                            }
+                            pk[i] = pack_bf16x2(a, c);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                    }
+                    tmem_st16(tmem_addr(sb, lane0, 16 * q4), pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[g]);
+            }
+            return true;
+        };
+        bool sq_ok;
+        if constexpr (GATED) {
+            sq_ok = gfast ? square(std::false_type{}) : square(std::true_type{});
+        } else {
+            sq_ok = square(std::false_type{});
+        }
+        if (!sq_ok) fail();
         // ---- o = O[:, :DV] / O[:, 64]
         const bool ok = wait(&o_done, 0) && !abort_flag;
         tc_fence_after();
@@ -291,18 +431,19 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
-template <int P, int DV>
-cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, int BH, int T,
-                         cudaStream_t s) {
-    auto kern = quadratic_tc_kernel<P, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+template <int P, int DV, bool GATED>
+cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, int BH, int T, const float* Lc,
+                         const int* zid, cudaStream_t s) {
+    auto kern = quadratic_tc_kernel<P, DV, GATED>;
+    const size_t smem = GATED ? kSmemGated : kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
     dim3 grid(((T + kTile - 1) / kTile + 1) / 2, BH);
-    KATA_TRACED("quadratic_tc", s,
-                kern<<<grid, kThreads, kSmem, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), T));
+    KATA_TRACED(GATED ? "quadratic_gated_tc" : "quadratic_tc", s,
+                kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), T, Lc, zid));
     return cudaGetLastError();
 }
 
@@ -311,7 +452,29 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, i
 cudaError_t launch_quadratic_tc(const void* q, const void* k, const void* v, void* o, int BH, int T,
                                 int p, int dv, cudaStream_t s) {
 #define KATA_CASE(P_, DV_) \
-    if (p == P_ && dv == DV_) return launch_typed<P_, DV_>(q, k, v, o, BH, T, s);
+    if (p == P_ && dv == DV_) return launch_typed<P_, DV_, false>(q, k, v, o, BH, T, nullptr, nullptr, s);
+    KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
+    KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
+    KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)
+#undef KATA_CASE
+    return cudaErrorInvalidValue;
+}
+
+size_t quadratic_gated_tc_workspace(int BH, int T) {
+    const size_t n = (size_t)BH * T;
+    return ((n * sizeof(float) + 255) / 256) * 256 + ((n * sizeof(int) + 255) / 256) * 256;
+}
+
+cudaError_t launch_quadratic_gated_tc(const void* q, const void* k, const void* v, const float* gate, void* o,
+                                      void* ws, int BH, int T, int p, int dv, cudaStream_t s) {
+    const size_t n = (size_t)BH * T;
+    float* Lc = static_cast<float*>(ws);
+    int* zid = reinterpret_cast<int*>(static_cast<char*>(ws) + ((n * sizeof(float) + 255) / 256) * 256);
+    KATA_TRACED("gate_prefix", s, (gate_prefix_kernel<<<(unsigned)BH, kPrefixThreads, 0, s>>>(gate, Lc, zid, T)));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+#define KATA_CASE(P_, DV_) \
+    if (p == P_ && dv == DV_) return launch_typed<P_, DV_, true>(q, k, v, o, BH, T, Lc, zid, s);
     KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
     KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
     KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)

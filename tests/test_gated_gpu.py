@@ -129,3 +129,129 @@ def test_gated_full_size_sampled_rows():
     ref = oracle.forward_plain_gated_rows(f64(q), f64(k), f64(v), f64(gate), bh, t)
     got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
     assert rows_error(got, ref) <= TOL[torch.bfloat16]
+
+
+# ---------------------------------------------------------------- gated flash-style form (tensor cores)
+
+def _traced_names(fn):
+    kb.kata_trace_start(4096)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        names = {name for name, _ in kb.kata_trace_stop()}
+    return out, names
+
+
+def _decays(gate):
+    """d[b, h, t, s] = prod_{r=s+1..t} gate_r for s <= t (0 above the diagonal)."""
+    B, H, T = gate.shape
+    d = np.zeros((B, H, T, T))
+    for t in range(T):
+        d[:, :, t, t] = 1.0
+        if t:
+            d[:, :, t, :t] = np.flip(np.cumprod(np.flip(gate[:, :, 1:t + 1], axis=-1), axis=-1), axis=-1)
+    return d
+
+
+def _check_gated_rows(q, k, v, gate, o, p, what, min_good=0.9):
+    """Rows against the oracle's gated definition at the bf16 tolerance where
+    the readout is well conditioned, and every row inside the hull of the
+    values its weights can reach.  The condition kappa_t = sum_s d_ts /
+    sum_s d_ts (qh_t.kh_s)^2 (1 for a query parallel to every live key, about p
+    for random directions) is the factor by which the rounding of the unit
+    keys to bf16 is amplified in the ratio of the weights: a query nearly
+    orthogonal to the few keys the gates leave alive has a large kappa, and its
+    output is only bound by the convex hull (nonnegative weights)."""
+    qq, kk, vv, gg = f64(q), f64(k), f64(v), f64(gate)
+    ref = oracle.forward_plain_gated(qq, kk, vv, gg)
+    got = f64(o)
+    qh = qq / np.maximum(np.linalg.norm(qq, axis=-1, keepdims=True), 1e-300)
+    kh = kk / np.maximum(np.linalg.norm(kk, axis=-1, keepdims=True), 1e-300)
+    d = _decays(gg)
+    cos2 = np.einsum("bhtp,bhsp->bhts", qh, kh) ** 2
+    kappa = d.sum(-1) / np.maximum((d * cos2).sum(-1), 1e-300)
+    good = kappa <= 10 * p
+    # (most rows are well conditioned: a check that would pass vacuously is not one)
+    assert good.size < 50 or good.mean() > min_good, f"{what}: {good.mean():.2f} of the rows well conditioned"
+    scale = np.abs(ref).max(axis=(2, 3), keepdims=True)
+    err = np.abs(got - ref)
+    worst = float(np.where(good[..., None], err / scale, 0.0).max())
+    assert worst <= TOL[torch.bfloat16], f"{what}: well-conditioned rows {worst:.3e}"
+    # convex hull: the values at or after the last zero gate up to t (what a
+    # nonnegative weight can reach), with the output's bf16 rounding as slack
+    # (the live keys of row t are the window [a_t, t]: d_ts only shrinks with
+    # distance, and a zero gate ends it)
+    first = np.argmax(d > 0, axis=-1)
+    B, H, T, _ = vv.shape
+    slack = 1e-2 * np.abs(vv).max()
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                win = vv[b, h, first[b, h, t]:t + 1]
+                assert np.all(got[b, h, t] >= win.min(axis=0) - slack) and np.all(got[b, h, t] <= win.max(axis=0) + slack), \
+                    f"{what}: row {t} of head {h} outside the convex hull"
+
+
+@pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 64), (64, 32)])
+@pytest.mark.parametrize("T", [1, 127, 300, 600])
+def test_gated_quadratic_matches_the_definition(p, dv, T):
+    """Gates in [0.5, 1]: every query tile's decay is moderate, so its weights
+    take the keys' factors; against the oracle's gated definition."""
+    q, k, v, gate = _case(1, 3, T, p, dv, torch.bfloat16, seed=11 * p + dv + T)
+    o, names = _traced_names(lambda: kb.kata_forward_quadratic_gated(q, k, v, gate))
+    kb.kata_get_device_status()
+    assert "quadratic_gated_tc" in names and "gate_prefix" in names, names
+    _check_gated_rows(q, k, v, gate, o, p, "gated quadratic")
+
+
+@pytest.mark.parametrize("p,dv", [(32, 32), (64, 64)])
+def test_gated_quadratic_strong_decay_and_zero_gates(p, dv):
+    """Gates in [0.015, 0.3] (a query tile's decay far past the key-factor
+    range, so every weight takes its own exponential) and zero gates inside
+    query tiles and on a tile edge; against the oracle."""
+    q, k, v, gate = _case(1, 2, 420, p, dv, torch.bfloat16, seed=p + 5, lo=0.05)
+    gate = gate * 0.3
+    gate[0, 0, 40] = 0.0
+    gate[0, 0, 128] = 0.0
+    gate[0, 1, 300] = 0.0
+    o = kb.kata_forward_quadratic_gated(q, k, v, gate)
+    kb.kata_get_device_status()
+    assert np.isfinite(f64(o)).all()
+    # (with one to three keys alive per row, fewer rows are well conditioned)
+    _check_gated_rows(q, k, v, gate, o, p, "gated quadratic, strong decay and zero gates", min_good=0.75)
+
+
+def test_gated_quadratic_unit_gates_are_the_ungated_form():
+    """All gates 1: every decay factor is exactly 1, so the gated kernel's
+    weights and output are those of the ungated flash-style form, bit for bit."""
+    q, k, v, gate = _case(2, 2, 333, 64, 64, torch.bfloat16, seed=21)
+    gate = torch.ones_like(gate)
+    o = kb.kata_forward_quadratic_gated(q, k, v, gate)
+    ref = kb.kata_forward_quadratic(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref)
+
+
+def test_gated_quadratic_refuses_fp32():
+    q, k, v, gate = _case(1, 1, 64, 16, 16, torch.float32, seed=1)
+    with pytest.raises(kb.KataError):
+        kb.kata_forward_quadratic_gated(q, k, v, gate)
+
+
+@pytest.mark.slow
+def test_gated_quadratic_full_size_sampled_rows():
+    """The 16384-token, 16-head, p = dv = 64 bf16 workload with gates in [0.9, 1]
+    through the gated flash-style form, against the oracle's gated definition on
+    sampled rows (32 per head in the last quarter), gated per head and row by row."""
+    from tests.parity import row_errors, rows_error, sample_rows
+    w = inputs.WORKLOADS[2]
+    q, k, v = inputs.make(w, "cuda")
+    gate = torch.from_numpy(np.random.default_rng(3).uniform(0.9, 1.0, (w.B, w.H, w.T))).float().cuda()
+    o = kb.kata_forward_quadratic_gated(q, k, v, gate)
+    kb.kata_get_device_status()
+    bh, t = sample_rows(w.B, w.H, w.T, w.C, per_head=6, seed=2)
+    ref = oracle.forward_plain_gated_rows(f64(q), f64(k), f64(v), f64(gate), bh, t)
+    got = f64(o).reshape(w.B * w.H, w.T, w.dv)[bh, t]
+    assert rows_error(got, ref) <= TOL[torch.bfloat16]
+    assert row_errors(got, ref).max() <= TOL[torch.bfloat16]
