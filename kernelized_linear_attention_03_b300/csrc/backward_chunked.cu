@@ -295,16 +295,51 @@ cbwd_gstates_kernel(const Tin* __restrict__ q, const Tin* __restrict__ dO, const
 }
 
 // Reverse exclusive prefix over the chunk axis, in place: x_c <- sum_{c' > c} x_c'.
+// One thread per VEC consecutive columns; the values of kRevBatch chunks are
+// loaded before any of them is overwritten, so that a batch's loads are in
+// flight together (each step's store would otherwise hold back the next load).
+constexpr int kRevBatch = 8;
+
+template <int VEC>
 __global__ void reverse_exclusive_kernel(float* __restrict__ x, int64_t heads, int64_t NC, int64_t W) {
+    const int64_t per_head = W / VEC;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= heads * W) return;
-    const int64_t h = gid / W, e = gid - h * W;
+    if (gid >= heads * per_head) return;
+    const int64_t h = gid / per_head, e = (gid - h * per_head) * VEC;
     float* col = x + h * NC * W + e;
-    float run = 0.f;
-    for (int64_t c = NC - 1; c >= 0; --c) {
-        const float xc = col[c * W];
-        col[c * W] = run;
-        run += xc;
+    float run[VEC];
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) run[u] = 0.f;
+    for (int64_t c1 = NC - 1; c1 >= 0; c1 -= kRevBatch) {
+        float xv[kRevBatch][VEC];
+#pragma unroll
+        for (int b = 0; b < kRevBatch; ++b) {
+            const int64_t c = c1 - b;
+            if (VEC == 4) {
+                const float4 t = c >= 0 ? *reinterpret_cast<const float4*>(col + c * W) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[b][0] = t.x;
+                xv[b][VEC > 1 ? 1 : 0] = t.y;
+                xv[b][VEC > 2 ? 2 : 0] = t.z;
+                xv[b][VEC > 3 ? 3 : 0] = t.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) xv[b][u] = c >= 0 ? col[c * W + u] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kRevBatch; ++b) {
+            const int64_t c = c1 - b;
+            if (c < 0) break;
+            if (VEC == 4) {
+                *reinterpret_cast<float4*>(col + c * W) =
+                    make_float4(run[0], run[VEC > 1 ? 1 : 0], run[VEC > 2 ? 2 : 0], run[VEC > 3 ? 3 : 0]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) col[c * W + u] = run[u];
+            }
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) run[u] += xv[b][u];
+        }
     }
 }
 
@@ -478,10 +513,17 @@ cudaError_t typed(const void* q, const void* k, const void* v, const void* dO, v
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     for (int part = 0; part < 2; ++part) {
-        const int64_t W = part == 0 ? (int64_t)N * DV : N, threads = (int64_t)BH * W;
-        KATA_TRACED("backward_reverse_scan", s,
-                    (reverse_exclusive_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(part == 0 ? S : z, BH,
-                                                                                                 NC, W)));
+        const int64_t W = part == 0 ? (int64_t)N * DV : N;
+        float* xs = part == 0 ? S : z;
+        if (W % 4 == 0 && (reinterpret_cast<uintptr_t>(xs) & 15u) == 0) {
+            const int64_t threads = (int64_t)BH * (W / 4);
+            KATA_TRACED("backward_reverse_scan", s,
+                        (reverse_exclusive_kernel<4><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xs, BH, NC, W)));
+        } else {
+            const int64_t threads = (int64_t)BH * W;
+            KATA_TRACED("backward_reverse_scan", s,
+                        (reverse_exclusive_kernel<1><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(xs, BH, NC, W)));
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     constexpr size_t smem = sizeof(float) * key_smem_floats<P, DV>();

@@ -94,10 +94,14 @@ ChunkedWs chunked_ws(int B, int H, int T, int p, int dv, int C, int64_t n_lift =
 
 // bf16 inputs take the tensor-core forward when its kernels can run on the
 // current device; its workspace holds one start state per
-// segment when the sequence is cut into G > 1 segments.
+// segment when the sequence is cut into G > 1 segments.  The segment totals
+// are built over `sub` equal parts of each segment (more CTAs for the
+// chunk-state kernel when few heads leave most of the GPU to it); their
+// exclusive prefix at every sub-th part is a segment's start state.
 struct TcPlan {
     bool use = false;
     int G = 1;
+    int sub = 1;
     ChunkedWs ws{0, 0, 0, 0};
 };
 
@@ -113,9 +117,20 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv, int lg = 1) {
     pl.G = G;
     size_t off = 0;
     if (G > 1) {
+        // parts per segment: about two chunk-state CTAs per SM (148 SMs), a
+        // divisor of the segment's chunks so that parts tile the segments
+        const int seg_chunks = kata::chunked_tc_segment_chunks(T, G);
+        const int64_t units = ((n + 127) / 128) * BH * (G - 1);
+        const int want = (int)((2 * 148 + units - 1) / units);
+        for (int d = want < seg_chunks ? want : seg_chunks; d >= 1; --d)
+            if (seg_chunks % d == 0) {
+                pl.sub = d;
+                break;
+            }
+        const int64_t entries = (int64_t)G * pl.sub;
         pl.ws.s_off = 0;
-        pl.ws.z_off = round_up(sizeof(float) * (size_t)(BH * G * n * dv), 256);
-        off = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * G * n), 256);
+        pl.ws.z_off = round_up(sizeof(float) * (size_t)(BH * entries * n * dv), 256);
+        off = pl.ws.z_off + round_up(sizeof(float) * (size_t)(BH * entries * n), 256);
     }
     pl.ws.i_off = off;
     pl.ws.total = off + round_up(kata::chunked_tc_intra_bytes((int)BH, T, p, dv), 256);
@@ -123,34 +138,37 @@ TcPlan tc_plan(kata_dtype dt, int B, int H, int T, int p, int dv, int lg = 1) {
 }
 
 // The tensor-core forward of a plan: one launch of the fused kernels when the
-// sequence is one segment per head; otherwise the segment totals of segments
-// 0..G-2 (chunk-state kernel), their exclusive prefixes seeded with the
-// initial state (the start state of every segment), then the fused kernels
-// with a start state per segment.  lg: blocks of the lift.
+// sequence is one segment per head; otherwise the totals of the parts of
+// segments 0..G-2 (chunk-state kernel), their exclusive prefixes seeded with
+// the initial state (at every sub-th part: the start state of a segment),
+// then the fused kernels with a start state per segment.  lg: blocks of the
+// lift.
 cudaError_t launch_tc_forward(const TcPlan& pl, const void* q, const void* k, const void* v, void* o, void* ws,
                               const float* S0, const float* z0, float* S_final, float* z_final, int64_t BH, int T,
                               int p, int dv, int lg, kata_scan_mode mode, cudaStream_t stream) {
     const ChunkedWs& w = pl.ws;
     void* intra = static_cast<char*>(ws) + w.i_off;
     if (pl.G == 1)
-        return kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, S_final, z_final, (int)BH, T, p, dv, lg, 1,
+        return kata::launch_chunked_tc(q, k, v, o, intra, S0, z0, 1, 1, S_final, z_final, (int)BH, T, p, dv, lg, 1,
                                        stream);
-    const int G = pl.G;
+    const int G = pl.G, sub = pl.sub, E = G * sub;  // E prefix entries per head
     const int64_t n = packed(p / lg);
-    const int L = kata::chunked_tc_segment_chunks(T, G) * 128;
+    const int L = kata::chunked_tc_segment_chunks(T, G) * 128 / sub;  // tokens per part
     float* Sg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
     float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
-    cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, G - 1, G, 0, lg, stream);
+    cudaError_t e = kata::launch_states_tc(k, v, Sg, zg, (int)BH, T, p, dv, L, E - sub, E, 0, lg, stream);
+    // the last segment's parts are not summed: zero them, so the scan reads defined values
     if (e == cudaSuccess)
-        e = cudaMemset2DAsync(Sg + (size_t)(G - 1) * n * dv, sizeof(float) * (size_t)G * n * dv, 0,
-                              sizeof(float) * (size_t)n * dv, (size_t)BH, stream);
+        e = cudaMemset2DAsync(Sg + (size_t)(E - sub) * n * dv, sizeof(float) * (size_t)E * n * dv, 0,
+                              sizeof(float) * (size_t)sub * n * dv, (size_t)BH, stream);
     if (e == cudaSuccess)
-        e = cudaMemset2DAsync(zg + (size_t)(G - 1) * n, sizeof(float) * (size_t)G * n, 0, sizeof(float) * (size_t)n,
-                              (size_t)BH, stream);
-    if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, G, n * dv, stream);
-    if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, G, n, stream);
+        e = cudaMemset2DAsync(zg + (size_t)(E - sub) * n, sizeof(float) * (size_t)E * n, 0,
+                              sizeof(float) * (size_t)sub * n, (size_t)BH, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, Sg, Sg, S0, nullptr, BH, E, n * dv, stream);
+    if (e == cudaSuccess) e = kata::launch_scan(mode, zg, zg, z0, nullptr, BH, E, n, stream);
     if (e == cudaSuccess)
-        e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, G, S_final, z_final, (int)BH, T, p, dv, lg, G, stream);
+        e = kata::launch_chunked_tc(q, k, v, o, intra, Sg, zg, E, sub, S_final, z_final, (int)BH, T, p, dv, lg, G,
+                                    stream);
     return e;
 }
 

@@ -39,7 +39,8 @@ unsigned int states_tc_take_status();
 // segments G the sequence is cut into on the current device (0 if the
 // kernel cannot run there); chunked_tc_segment_chunks() the 128-token
 // chunks per segment.  S_start/z_start: [BH, start_groups, n, dv] / [.., n]
-// start states (sqrt(2)-packed order; NULL = zero; start_groups is G or 1).
+// start states (sqrt(2)-packed order; NULL = zero); segment g starts from
+// entry g * start_stride (start_groups 1: every segment from entry 0).
 // `intra` is chunked_tc_intra_bytes() of device scratch (256-byte aligned)
 // for the fp32 accumulation rows of the numerators and denominators and
 // the transposed unit keys: the intra-chunk kernel initialises them, the
@@ -51,8 +52,9 @@ int chunked_tc_segments(int p, int dv, int lg, int BH, int T);
 int chunked_tc_segment_chunks(int T, int G);
 size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv);
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
-                              const float* S_start, const float* z_start, int start_groups, float* S_final,
-                              float* z_final, int BH, int T, int p, int dv, int lg, int G, cudaStream_t s);
+                              const float* S_start, const float* z_start, int start_groups, int start_stride,
+                              float* S_final, float* z_final, int BH, int T, int p, int dv, int lg, int G,
+                              cudaStream_t s);
 unsigned int chunked_tc_take_status();
 
 // Per-chunk local states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] (fp32, SIMT).

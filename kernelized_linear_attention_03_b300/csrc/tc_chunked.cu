@@ -339,7 +339,8 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmy,
                   const __grid_constant__ CUtensorMap tmktr, float* __restrict__ dacc,
                   const float* __restrict__ S_start, const float* __restrict__ z_start,
-                  int start_groups, float* __restrict__ S_final, float* __restrict__ z_final, int T, int seg_chunks) {
+                  int start_groups, int start_stride, float* __restrict__ S_final, float* __restrict__ z_final, int T,
+                  int seg_chunks) {
     using K = Cfg<P, DV, LG>;
     constexpr int n = K::n, M = K::M;
     extern __shared__ uint8_t smem_raw[];
@@ -425,7 +426,7 @@ chunked_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     // ---- start state of this segment (state warps: lane = slot / dimension)
     if (warp >= 4 && warp < 8) {
         const int e = t - 128;
-        const int sg = start_groups > 1 ? g : 0;
+        const int sg = start_groups > 1 ? g * start_stride : 0;  // this segment's start state
         if (!zc) {
             const float* S0 = S_start ? S_start + (bh * start_groups + sg) * (int64_t)n * DV : nullptr;
             load_state_tile<M, DV>(S0, tau, tm(K::tm_s), s_s16, e);
@@ -1150,8 +1151,8 @@ IntraWs intra_ws(int BH, int T, int p, int dv) {
 
 template <int P, int DV, int LG>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, void* intra,
-                         const float* S_start, const float* z_start, int start_groups, float* S_final,
-                         float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
+                         const float* S_start, const float* z_start, int start_groups, int start_stride,
+                         float* S_final, float* z_final, int BH, int T, int seg_chunks, int G, cudaStream_t s) {
     using K = Cfg<P, DV, LG>;
     if (!register_split_fits<P, DV, LG>()) return cudaErrorInvalidConfiguration;
     const IntraWs w = intra_ws(BH, T, P, DV);
@@ -1178,7 +1179,8 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, v
         return e;
     KATA_TRACED("chunked_tc", s,
                 (chunked_tc_kernel<P, DV, LG><<<dim3((unsigned)BH, (unsigned)(K::CS * G)), kThreads, K::smem, s>>>(
-                    tq, tkt, tv, ty, tktr, dacc, S_start, z_start, start_groups, S_final, z_final, T, seg_chunks)));
+                    tq, tkt, tv, ty, tktr, dacc, S_start, z_start, start_groups, start_stride, S_final, z_final, T,
+                    seg_chunks)));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t items = (int64_t)BH * T * (DV / 8);
     if (items > 0)
@@ -1237,11 +1239,12 @@ int chunked_tc_segment_chunks(int T, int G) {
 size_t chunked_tc_intra_bytes(int BH, int T, int p, int dv) { return intra_ws(BH, T, p, dv).total; }
 
 cudaError_t launch_chunked_tc(const void* q, const void* k, const void* v, void* o, void* intra,
-                              const float* S_start, const float* z_start, int start_groups, float* S_final,
-                              float* z_final, int BH, int T, int p, int dv, int lg, int G, cudaStream_t s) {
+                              const float* S_start, const float* z_start, int start_groups, int start_stride,
+                              float* S_final, float* z_final, int BH, int T, int p, int dv, int lg, int G,
+                              cudaStream_t s) {
     const int seg_chunks = chunked_tc_segment_chunks(T, G);
-    KATA_DISPATCH(return launch_typed<P, DV, LG>(q, k, v, o, intra, S_start, z_start, start_groups, S_final, z_final, BH, T,
-                                             seg_chunks, G, s));
+    KATA_DISPATCH(return launch_typed<P, DV, LG>(q, k, v, o, intra, S_start, z_start, start_groups, start_stride, S_final,
+                                                 z_final, BH, T, seg_chunks, G, s));
     return cudaErrorInvalidValue;
 }
 

@@ -103,6 +103,56 @@ def test_chunked_initial_state_and_split_call(dtype):
     assert _state_err(S1, S_ref) <= _state_tol(dtype)
 
 
+def _traced_kernels(fn):
+    kb.kata_trace_start(4096)
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        names = [name for name, _ in kb.kata_trace_stop()]
+    return out, names
+
+
+def test_segmented_forward_with_parts_and_initial_state():
+    """One head of 4096 tokens leaves most CTAs free, so the bf16 forward is cut
+    into segments whose start states are exclusive prefixes over parts of the
+    segments (the chunk-state kernel builds two parts per segment here),
+    seeded with the initial state: the full lift and KATA-Sigma-2 against the
+    oracle, the output and the carried state."""
+    T1, T = 300, 300 + 4096
+    q, k, v = _inputs(1, 1, T, 64, 64, torch.bfloat16, seed=31)
+    qq, kk, vv = f64(q), f64(k), f64(v)
+    part = lambda x, a, b: x[:, :, a:b].contiguous()  # noqa: E731
+    # the full lift
+    n = kb.kata_packed_dim(64)
+    S1, z1 = torch.empty(1, 1, n, 64, device="cuda"), torch.empty(1, 1, n, device="cuda")
+    o1, _, _ = kb.kata_forward_chunked(part(q, 0, T1), part(k, 0, T1), part(v, 0, T1), 128, S_final=S1, z_final=z1)
+    S2, z2 = torch.empty_like(S1), torch.empty_like(z1)
+    (o2, _, _), names = _traced_kernels(lambda: kb.kata_forward_chunked(
+        part(q, T1, T), part(k, T1, T), part(v, T1, T), 128, S0=S1, z0=z1, S_final=S2, z_final=z2))
+    assert names.count("states_tc") == 1 and "chunked_tc" in names, names
+    ref = oracle.forward_plain(qq, kk, vv)
+    assert_close(np.concatenate([f64(o1), f64(o2)], axis=2), ref, torch.bfloat16, "segments with parts")
+    _, S_ref, z_ref = oracle.forward_recurrent(qq, kk, vv)
+    assert _state_err(S2, S_ref) <= _state_tol(torch.bfloat16)
+    assert _state_err(z2, z_ref) <= _state_tol(torch.bfloat16)
+    # KATA-Sigma-2
+    nb = kb.kata_lift_dim(kb.KATA_LIFT_SIGMA, 64, 2)
+    B1, y1 = torch.empty(1, 1, nb, 64, device="cuda"), torch.empty(1, 1, nb, device="cuda")
+    p1, _, _ = kb.kata_forward_chunked_block(part(q, 0, T1), part(k, 0, T1), part(v, 0, T1), 128, kb.KATA_LIFT_SIGMA, 2,
+                                             S_final=B1, z_final=y1)
+    B2, y2 = torch.empty_like(B1), torch.empty_like(y1)
+    (p2, _, _), names = _traced_kernels(lambda: kb.kata_forward_chunked_block(
+        part(q, T1, T), part(k, T1, T), part(v, T1, T), 128, kb.KATA_LIFT_SIGMA, 2, S0=B1, z0=y1, S_final=B2,
+        z_final=y2))
+    assert names.count("states_tc") == 1, names
+    refb = oracle.forward_plain_block(qq, kk, vv, oracle.LIFT_SIGMA, 2)
+    assert_close(np.concatenate([f64(p1), f64(p2)], axis=2), refb, torch.bfloat16, "Sigma-2 segments with parts")
+    _, B_ref, y_ref = oracle.forward_recurrent_block(qq, kk, vv, oracle.LIFT_SIGMA, 2)
+    assert _state_err(B2, B_ref) <= _state_tol(torch.bfloat16)
+    assert _state_err(y2, y_ref) <= _state_tol(torch.bfloat16)
+
+
 def test_chunked_empty_sequence_passes_state_through():
     S0 = torch.randn(1, 3, 136, 16, device="cuda")
     z0 = torch.rand(1, 3, 136, device="cuda")
