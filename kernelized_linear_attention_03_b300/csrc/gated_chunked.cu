@@ -10,6 +10,8 @@
 //   output       num_t = (prod_{r=c C..t} gamma_r) psi(qh_t)^T P_c
 //                        + sum_{s in c, s<=t} (prod_{r=s+1..t} gamma_r) (qh_t.kh_s)^2 v_s,
 //                den_t likewise with 1 for v_s.
+#include <type_traits>
+
 #include "kata_device.cuh"
 #include "kata_internal.h"
 
@@ -133,6 +135,42 @@ __global__ void gated_scan_kernel(float* __restrict__ x, const float* __restrict
     }
 }
 
+// ---------------------------------------------------------------- decays for the tensor-core chunk states
+// One warp per (chunk c, head bh): dec[t] = prod_{r=t+1..end_c} gamma_r for the
+// chunk's tokens and a[c] = prod over the chunk (fp32 products; a zero gate
+// gives exact zeros).  Each lane takes up to kMaxC / 32 consecutive tokens; the
+// lanes' products are combined by a suffix product across the warp.
+__global__ void __launch_bounds__(32)
+gate_decay_kernel(const float* __restrict__ gate, float* __restrict__ dec, float* __restrict__ a, int T, int C, int NC) {
+    constexpr int kPer = kMaxC / 32;
+    const int c = blockIdx.x, lane = threadIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int t0 = c * C, len = min(C, T - t0), per = (C + 31) / 32;
+    float gl[kPer];
+    float tot = 1.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = lane * per + i;
+        gl[i] = (i < per && s < len) ? gate[bh * T + t0 + s] : 1.f;
+        tot *= gl[i];
+    }
+    float incl = tot;  // product of this lane's gates and every later lane's
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float later = __shfl_down_sync(0xffffffffu, incl, d);
+        if (lane + d < 32) incl *= later;
+    }
+    float run = __shfl_down_sync(0xffffffffu, incl, 1);
+    if (lane == 31) run = 1.f;
+#pragma unroll
+    for (int i = kPer - 1; i >= 0; --i) {
+        const int s = lane * per + i;
+        if (i < per && s < len) dec[bh * T + t0 + s] = run;
+        run *= gl[i];
+    }
+    if (lane == 0) a[bh * NC + c] = incl;
+}
+
 // ---------------------------------------------------------------- chunk output
 template <int P, int DV>
 constexpr size_t output_smem_bytes() {
@@ -253,11 +291,18 @@ gated_output_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const 
 
 template <typename Tin, int P, int DV>
 cudaError_t gated_typed(const void* q, const void* k, const void* v, const float* gate, void* o, float* X, float* Xz,
-                        float* a, const float* S0, const float* z0, float* S_final, float* z_final, int BH, int T,
-                        int C, cudaStream_t s) {
+                        float* a, float* dec, const float* S0, const float* z0, float* S_final, float* z_final, int BH,
+                        int T, int C, cudaStream_t s) {
     constexpr int N = P * (P + 1) / 2;
     const int NC = (T + C - 1) / C;
-    {
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        // bf16: the chunk states on the tensor cores (the chunk-state kernel,
+        // each token's key lift weighted by its decay to the chunk's end)
+        KATA_TRACED("gate_decay", s, (gate_decay_kernel<<<dim3(NC, BH), 32, 0, s>>>(gate, dec, a, T, C, NC)));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if ((e = launch_states_tc(k, v, X, Xz, BH, T, P, DV, C, NC, NC, 0, 1, s, dec)) != cudaSuccess) return e;
+    } else {
         constexpr size_t smem = state_smem_bytes<P, DV>();
         auto kern = gated_states_kernel<Tin, P, DV>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -298,11 +343,11 @@ cudaError_t gated_typed(const void* q, const void* k, const void* v, const float
 
 template <typename Tin>
 cudaError_t gated_dispatch(int p, int dv, const void* q, const void* k, const void* v, const float* gate, void* o,
-                           float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
+                           float* X, float* Xz, float* a, float* dec, const float* S0, const float* z0, float* S_final,
                            float* z_final, int BH, int T, int C, cudaStream_t s) {
 #define KATA_CASE(P_, DV_)                                                                                      \
     if (p == P_ && dv == DV_)                                                                                   \
-        return gated_typed<Tin, P_, DV_>(q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH, T, C, s);
+        return gated_typed<Tin, P_, DV_>(q, k, v, gate, o, X, Xz, a, dec, S0, z0, S_final, z_final, BH, T, C, s);
     KATA_CASE(16, 16) KATA_CASE(16, 32) KATA_CASE(16, 64)
     KATA_CASE(32, 16) KATA_CASE(32, 32) KATA_CASE(32, 64)
     KATA_CASE(64, 16) KATA_CASE(64, 32) KATA_CASE(64, 64)
@@ -313,11 +358,12 @@ cudaError_t gated_dispatch(int p, int dv, const void* q, const void* k, const vo
 }  // namespace
 
 cudaError_t launch_chunked_gated(int dtype, const void* q, const void* k, const void* v, const float* gate, void* o,
-                                 float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
-                                 float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s) {
-    return dtype == 0 ? gated_dispatch<float>(p, dv, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH, T, C, s)
-                      : gated_dispatch<__nv_bfloat16>(p, dv, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, BH,
-                                                      T, C, s);
+                                 float* X, float* Xz, float* a, float* dec, const float* S0, const float* z0,
+                                 float* S_final, float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s) {
+    return dtype == 0 ? gated_dispatch<float>(p, dv, q, k, v, gate, o, X, Xz, a, dec, S0, z0, S_final, z_final, BH, T,
+                                              C, s)
+                      : gated_dispatch<__nv_bfloat16>(p, dv, q, k, v, gate, o, X, Xz, a, dec, S0, z0, S_final, z_final,
+                                                      BH, T, C, s);
 }
 
 }  // namespace kata

@@ -518,7 +518,8 @@ size_t kata_chunked_gated_workspace_bytes(kata_dtype dt, int B, int H, int T, in
     const int64_t BH = (int64_t)B * H, NC = (T + C - 1) / C;
     if (BH * T == 0) return 0;
     const ChunkedWs w = chunked_ws(B, H, T, p, dv, C);
-    return w.total + round_up(sizeof(float) * (size_t)(BH * NC), 256);
+    // chunk decays a [BH,NC], then the per-token decays dec [BH,T]
+    return w.total + round_up(sizeof(float) * (size_t)(BH * NC), 256) + round_up(sizeof(float) * (size_t)(BH * T), 256);
 }
 
 kata_status kata_forward_chunked_gated(const void* q, const void* k, const void* v, const float* gate, void* o,
@@ -557,8 +558,10 @@ kata_status kata_forward_chunked_gated(const void* q, const void* k, const void*
     float* X = reinterpret_cast<float*>(static_cast<char*>(ws) + w.s_off);
     float* Xz = reinterpret_cast<float*>(static_cast<char*>(ws) + w.z_off);
     float* a = reinterpret_cast<float*>(static_cast<char*>(ws) + w.total);
-    return cuda_status(kata::launch_chunked_gated(dt, q, k, v, gate, o, X, Xz, a, S0, z0, S_final, z_final, (int)BH,
-                                                  T, p, dv, C, stream));
+    float* dec = reinterpret_cast<float*>(static_cast<char*>(ws) + w.total +
+                                          round_up(sizeof(float) * (size_t)(BH * ((T + C - 1) / C)), 256));
+    return cuda_status(kata::launch_chunked_gated(dt, q, k, v, gate, o, X, Xz, a, dec, S0, z0, S_final, z_final,
+                                                  (int)BH, T, p, dv, C, stream));
 }
 
 size_t kata_backward_chunked_workspace_bytes(int B, int H, int T, int p, int dv_dim) {

@@ -29,9 +29,11 @@ unsigned int quadratic_tc_take_status();
 // of the first NS segments of L tokens, into S_out [BH, NS_out, n, dv] and
 // z_out [BH, NS_out, n] (fp32, sqrt(2)-packed order), for the full lift
 // (lg = 1) or KATA-Sigma-g (lg = g > 1, n the lift width of one block).
-// NS <= NS_out and NS <= ceil(T / L).
+// NS <= NS_out and NS <= ceil(T / L).  dec (or null; lg = 1 only): [BH, T]
+// fp32, a weight on each token's key lift (the gated form's decays).
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s);
+                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s,
+                             const float* dec = nullptr);
 unsigned int states_tc_take_status();
 
 // Chunked forward on the tensor cores (bf16): one CTA per (head, segment,
@@ -82,11 +84,12 @@ cudaError_t launch_decode_step(int dtype, const void* q, const void* k, const vo
                                float* z, int BH, int p, int dv, int family, int g, const float* gate,
                                cudaStream_t s);
 
-// Gated chunked forward (CUDA cores, any dtype): gate [BH,T] fp32; X [BH,NC,n,dv],
-// Xz [BH,NC,n], a [BH,NC] fp32 scratch; optional S0/z0 and S_final/z_final.
+// Gated chunked forward (any dtype; bf16 chunk states on the tensor cores):
+// gate [BH,T] fp32; X [BH,NC,n,dv], Xz [BH,NC,n], a [BH,NC], dec [BH,T] fp32
+// scratch; optional S0/z0 and S_final/z_final.
 cudaError_t launch_chunked_gated(int dtype, const void* q, const void* k, const void* v, const float* gate, void* o,
-                                 float* X, float* Xz, float* a, const float* S0, const float* z0, float* S_final,
-                                 float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s);
+                                 float* X, float* Xz, float* a, float* dec, const float* S0, const float* z0,
+                                 float* S_final, float* z_final, int BH, int T, int p, int dv, int C, cudaStream_t s);
 
 // Block-lift forwards on CUDA cores (family 1 Sigma-g, 2 M-g; block_lift.cuh),
 // any dtype: per-chunk states S_loc [BH,NC,n,dv], z_loc [BH,NC,n] in the

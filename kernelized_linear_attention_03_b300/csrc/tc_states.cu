@@ -83,8 +83,9 @@ __device__ __forceinline__ uint32_t key_word(const uint32_t (&u)[P / 2], int w) 
 
 // Lifted key coordinates of tile TAU for this thread's token into row `row`
 // of the token-major A tile.
-template <int P, int LG, int TAU>
-__device__ __forceinline__ void key_tile_to_smem(const uint32_t (&u)[P / 2], uint8_t* As, int row) {
+// SCALE: every word times the bf16 pair dd (a per-token weight of the lift).
+template <int P, int LG, int TAU, bool SCALE>
+__device__ __forceinline__ void key_tile_to_smem(const uint32_t (&u)[P / 2], uint8_t* As, int row, uint32_t dd) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         uint4 val;
@@ -92,17 +93,24 @@ __device__ __forceinline__ void key_tile_to_smem(const uint32_t (&u)[P / 2], uin
         val.y = key_word<P, LG>(u, 64 * TAU + 4 * c + 1);
         val.z = key_word<P, LG>(u, 64 * TAU + 4 * c + 2);
         val.w = key_word<P, LG>(u, 64 * TAU + 4 * c + 3);
+        if (SCALE) {
+            val.x = hmul2_bf16(val.x, dd);
+            val.y = hmul2_bf16(val.y, dd);
+            val.z = hmul2_bf16(val.z, dd);
+            val.w = hmul2_bf16(val.w, dd);
+        }
         *reinterpret_cast<uint4*>(As + mn_sw128_chunk(8 * c, row, kAtom)) = val;
     }
 }
 
-template <int P, int LG, int TAU = 0>
-__device__ __forceinline__ void key_tile_dispatch(int tau, const uint32_t (&u)[P / 2], uint8_t* As, int row) {
+template <int P, int LG, bool SCALE, int TAU = 0>
+__device__ __forceinline__ void key_tile_dispatch(int tau, const uint32_t (&u)[P / 2], uint8_t* As, int row,
+                                                  uint32_t dd) {
     if constexpr (TAU < lift::tiles_of(P / LG)) {
         if (tau == TAU)
-            key_tile_to_smem<P, LG, TAU>(u, As, row);
+            key_tile_to_smem<P, LG, TAU, SCALE>(u, As, row, dd);
         else
-            key_tile_dispatch<P, LG, TAU + 1>(tau, u, As, row);
+            key_tile_dispatch<P, LG, SCALE, TAU + 1>(tau, u, As, row, dd);
     }
 }
 
@@ -110,7 +118,9 @@ template <int P, int DV, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  float* __restrict__ S_out, float* __restrict__ z_out, int T, int L, int NS, int NS_out,
-                 int segs_per_cta, int prefix) {
+                 int segs_per_cta, int prefix, const float* __restrict__ dec) {
+    // dec (or null; full lift only): a weight per token, the key lift of token
+    // t taken times dec[bh][t] (the gated form's decay to its chunk's end)
     // prefix != 0 (one CTA per tile and head, all segments): each segment's
     // row is the exclusive running sum of the segments before it, summed in
     // segment order in the epilogue's registers, instead of the segment's own total
@@ -265,7 +275,16 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
                         u[4 * c + j] = pack_bf16x2(__bfloat162float(e[2 * j]) * inv, __bfloat162float(e[2 * j + 1]) * inv);
                 }
             }
-            key_tile_dispatch<P, LG>(tau, u, sm + kAOff + 2 * ab * kAtom, lt);
+            if constexpr (LG == 1) {
+                if (dec != nullptr) {
+                    const float w = valid ? dec[bh * (int64_t)T + b0 + lt] : 0.f;
+                    key_tile_dispatch<P, LG, true>(tau, u, sm + kAOff + 2 * ab * kAtom, lt, pack_bf16x2(w, w));
+                } else {
+                    key_tile_dispatch<P, LG, false>(tau, u, sm + kAOff + 2 * ab * kAtom, lt, 0u);
+                }
+            } else {
+                key_tile_dispatch<P, LG, false>(tau, u, sm + kAOff + 2 * ab * kAtom, lt, 0u);
+            }
             fence_proxy_async_smem();
             mbar_arrive(&a_full[ab]);
         }
@@ -362,7 +381,7 @@ states_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 
 template <int P, int DV, int LG>
 cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_out, int BH, int T, int L,
-                         int NS, int NS_out, int prefix, cudaStream_t s) {
+                         int NS, int NS_out, int prefix, const float* dec, cudaStream_t s) {
     auto kern = states_tc_kernel<P, DV, LG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
@@ -376,18 +395,21 @@ cudaError_t launch_typed(const void* k, const void* v, float* S_out, float* z_ou
     const int per = (NS + groups - 1) / groups;
     groups = (NS + per - 1) / per;
     dim3 grid(tiles, groups, BH);
-    KATA_TRACED("states_tc", s, kern<<<grid, kThreads, kSmem, s>>>(tk, tv, S_out, z_out, T, L, NS, NS_out, per, prefix));
+    KATA_TRACED("states_tc", s,
+                kern<<<grid, kThreads, kSmem, s>>>(tk, tv, S_out, z_out, T, L, NS, NS_out, per, prefix, dec));
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_states_tc(const void* k, const void* v, float* S_out, float* z_out, int BH, int T,
-                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s) {
+                             int p, int dv, int L, int NS, int NS_out, int prefix, int lg, cudaStream_t s,
+                             const float* dec) {
     if (NS <= 0) return cudaSuccess;
+    if (dec != nullptr && lg != 1) return cudaErrorInvalidValue;
 #define KATA_CASE(P_, DV_, LG_)                  \
     if (p == P_ && dv == DV_ && lg == LG_) \
-        return launch_typed<P_, DV_, LG_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, prefix, s);
+        return launch_typed<P_, DV_, LG_>(k, v, S_out, z_out, BH, T, L, NS, NS_out, prefix, dec, s);
     KATA_CASE(16, 16, 1) KATA_CASE(16, 32, 1) KATA_CASE(16, 64, 1)
     KATA_CASE(32, 16, 1) KATA_CASE(32, 32, 1) KATA_CASE(32, 64, 1)
     KATA_CASE(64, 16, 1) KATA_CASE(64, 32, 1) KATA_CASE(64, 64, 1)

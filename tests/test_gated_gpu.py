@@ -30,6 +30,11 @@ def test_gated_chunked_matches_the_definition(dtype, p, dv, C):
     q, k, v, gate = _case(1, 2, 200, p, dv, dtype, seed=p + dv + C)
     o = kb.kata_forward_chunked_gated(q, k, v, gate, C)
     torch.cuda.synchronize()
+    if dtype == torch.bfloat16:
+        # bf16 chunk states are sums of bf16 unit-key lifts: rows held to the
+        # tolerance where the readout is well conditioned, all rows to the hull
+        _check_gated_rows(q, k, v, gate, o, p, "gated chunked")
+        return
     ref = oracle.forward_plain_gated(f64(q), f64(k), f64(v), f64(gate))
     assert_close(f64(o), ref, dtype, "gated chunked")
 
@@ -191,6 +196,34 @@ def _check_gated_rows(q, k, v, gate, o, p, what, min_good=0.9):
                 win = vv[b, h, first[b, h, t]:t + 1]
                 assert np.all(got[b, h, t] >= win.min(axis=0) - slack) and np.all(got[b, h, t] <= win.max(axis=0) + slack), \
                     f"{what}: row {t} of head {h} outside the convex hull"
+
+
+@pytest.mark.parametrize("p,dv,C", [(32, 32, 32), (64, 64, 64), (16, 64, 128)])
+def test_gated_chunked_bf16_states_on_tensor_cores(p, dv, C):
+    """bf16 chunk states from the tensor-core chunk-state kernel, each token's
+    key lift weighted by its decay to its chunk's end (gate_decay): zero gates
+    inside a chunk and on a chunk's last and first tokens, ragged tails, and a
+    second call that carries the state; outputs and the final state against
+    the oracle's gated definition and recurrence."""
+    B, H, T1, T2 = 1, 2, 3 * C + 5, 2 * C - 3
+    q, k, v, gate = _case(B, H, T1 + T2, p, dv, torch.bfloat16, seed=3 * p + C)
+    gate[0, 0, C // 2] = 0.0
+    gate[0, 1, C - 1] = 0.0
+    gate[0, 1, 2 * C] = 0.0
+    n = p * (p + 1) // 2
+    S, z = torch.empty(B, H, n, dv, device="cuda"), torch.empty(B, H, n, device="cuda")
+    S2, z2 = torch.empty_like(S), torch.empty_like(z)
+    part = lambda x, a, b: x[:, :, a:b].contiguous()  # noqa: E731
+    (o1, _, _), names = _traced_names(lambda: kb.kata_forward_chunked_gated(
+        part(q, 0, T1), part(k, 0, T1), part(v, 0, T1), part(gate, 0, T1), C, S_final=S, z_final=z))
+    assert {"gate_decay", "states_tc"} <= names and "gated_states_simt" not in names, names
+    o2, _, _ = kb.kata_forward_chunked_gated(part(q, T1, T1 + T2), part(k, T1, T1 + T2), part(v, T1, T1 + T2),
+                                             part(gate, T1, T1 + T2), C, S0=S, z0=z, S_final=S2, z_final=z2)
+    kb.kata_get_device_status()
+    o = torch.cat([o1, o2], dim=2)
+    _check_gated_rows(q, k, v, gate, o, p, "gated chunked, tensor-core states", min_good=0.75)
+    _, S_ref, z_ref = oracle.forward_recurrent_gated(f64(q), f64(k), f64(v), f64(gate))
+    assert _rel(f64(S2), S_ref) <= TOL[torch.bfloat16] and _rel(f64(z2), z_ref) <= TOL[torch.bfloat16]
 
 
 @pytest.mark.parametrize("p,dv", [(16, 16), (32, 64), (64, 64), (64, 32)])
