@@ -158,6 +158,13 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
     return r;
 }
 
+// Every thread of every CTA of the cluster: arrive (release) and wait
+// (acquire) on the cluster barrier; the non-aligned forms, so a warp need not
+// be converged.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Arrive (release at cluster scope) on a barrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr)

@@ -36,7 +36,16 @@
 //   warps 8-11      squaring group of query tile B (and its o at the end)
 //   warps 12-15     put the keys of each staged tile on the unit sphere, in
 //                   place (thread = key row)
+//
+// Short sequences (two CTAs a pair fit in one wave): clusters of two CTAs split a pair's
+// key tiles, rank 0 taking tiles 0..m and rank 1 the rest (2m + 2 and 2m + 1
+// tile products).  The weights need no running maximum, so the two partial
+// sums of O simply add: rank 1 leaves its O (numerators and denominator,
+// fp32) in its own shared memory, and rank 0 adds it through distributed
+// shared memory before the division.
 #include <cuda_bf16.h>
+
+#include <cooperative_groups.h>
 
 #include <cstdint>
 #include <type_traits>
@@ -60,6 +69,7 @@ constexpr uint32_t kNV = 80;      // B columns of the value product: 64 value sl
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every device-side wait
 constexpr float kSpanMax = 80.f;  // decay span of a query tile (natural log) below which its weights take key factors
 constexpr float kLog2e = 1.44269504088896340736f;
+constexpr int64_t kSplitMax = 148;  // CTAs of the split grid (two per pair) up to which pairs are split: one wave
 
 // shared memory, 16 KB atoms from a 1024-byte aligned base: Q_A, Q_B,
 // K[kStages], V[kStages], the ones atom (last, so every value stage reaches
@@ -137,7 +147,7 @@ template <int P, int DV, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int T,
-                    const float* __restrict__ Lc, const int* __restrict__ zid) {
+                    const float* __restrict__ Lc, const int* __restrict__ zid, int split) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_ready[kStages], kv_free[kStages];
     __shared__ uint64_t s_full[2], p_full[2], o_done, drain;
@@ -146,20 +156,28 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int t = threadIdx.x, warp = t >> 5;
-    const int m = gridDim.x - 1 - blockIdx.x;  // heaviest pairs first
+    // heaviest pairs first; with split, the two CTAs of a cluster take parts
+    // 0 and 1 of one pair's key tiles
+    const int part = split ? (int)(blockIdx.x & 1) : 0;
+    const int m = (split ? (int)(gridDim.x >> 1) - 1 - (int)(blockIdx.x >> 1) : (int)gridDim.x - 1 - (int)blockIdx.x);
     const int64_t bh = blockIdx.y;
     const int ntiles = (T + kTile - 1) / kTile;
     const int qa = 2 * m, qb = 2 * m + 1;
     const bool has_b = qb < ntiles;
-    const int last[2] = {qa, has_b ? qb : -1};  // last key tile of each query tile
-    const int nj = has_b ? qb + 1 : qa + 1;     // key tiles loaded
+    // last key tile of query tile g (its diagonal; -1: no tile B)
+    auto last = [&](int g) { return g ? (has_b ? qb : -1) : qa; };
+    const int nj_all = has_b ? qb + 1 : qa + 1;
+    // key tiles [j0, j1) of this CTA; query tile g takes j0 .. jend(g) of them
+    const int j0 = split && part == 1 ? m + 1 : 0, j1 = split && part == 0 ? m + 1 : nj_all;
+    const int nj = j1 - j0;
+    auto jend = [&](int g) { return min(last(g), j1 - 1); };
     // gated form: whether the weights of this CTA's rows take key factors, the
     // reference R and the rows' common last zero gate
     bool gfast = false;
     float gref = 0.f;
     int gzero = -1;
     if (GATED) {
-        const int r0 = qa * kTile, r1 = min(T, nj * kTile) - 1;
+        const int r0 = qa * kTile, r1 = min(T, nj_all * kTile) - 1;
         const float l0 = Lc[bh * T + r0], l1 = Lc[bh * T + r1];
         gref = l1;
         gzero = zid[bh * T + r1];
@@ -215,14 +233,14 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_load_3d(sm + kQOff, &tmq, 0, qa * kTile, (int)bh, &q_full);
         if (has_b) tma_load_3d(sm + kQOff + kAtom, &tmq, 0, qb * kTile, (int)bh, &q_full);
         int issued = 0;
-        for (int j = 0; j < nj; ++j) {
-            const int st = j % kStages, use = j / kStages;
-            if (j >= kStages && !mbar_wait(&kv_free[st], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
+        for (int jl = 0; jl < nj; ++jl) {
+            const int st = jl % kStages, use = jl / kStages, j = j0 + jl;
+            if (jl >= kStages && !mbar_wait(&kv_free[st], (use - 1) & 1, &abort_flag, kWaitNs)) { fail(); break; }
             mbar_arrive_expect_tx(&k_full[st], kAtom);
             tma_load_3d(sm + kKOff + st * kAtom, &tmk, 0, j * kTile, (int)bh, &k_full[st]);
             mbar_arrive_expect_tx(&v_full[st], kAtom);
             tma_load_3d(sm + kVOff + st * kAtom, &tmv, 0, j * kTile, (int)bh, &v_full[st]);
-            issued = j + 1;
+            issued = jl + 1;
         }
         // no copy may still be landing in shared memory when the CTA exits
         mbar_wait_quiet(&q_full, 0, kWaitNs);
@@ -237,8 +255,8 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         constexpr uint32_t id_o = idesc_bf16_f32_major(kTile, kNV, false, true);
         // scores of query tile g against key tile j (P in place of S afterwards)
         auto issue_s = [&](int g, int j) -> bool {
-            const int st = j % kStages;
-            if (!wait(&k_ready[st], (j / kStages) & 1)) return false;
+            const int jl = j - j0, st = jl % kStages;
+            if (!wait(&k_ready[st], (jl / kStages) & 1)) return false;
             tc_fence_after();
             const uint64_t d_q = sdesc_kmajor_sw128(smem_u32(sm + kQOff + g * kAtom));
             const uint64_t d_k = sdesc_kmajor_sw128(smem_u32(sm + kKOff + st * kAtom));
@@ -250,9 +268,9 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         };
         // O_g += P_g [V_j | 1]; then the next scores of tile g (they overwrite P_g)
         auto issue_o = [&](int g, int j) -> bool {
-            const int st = j % kStages;
-            if (!wait(&p_full[g], j & 1) ||
-                !wait(&v_full[st], (j / kStages) & 1))
+            const int jl = j - j0, st = jl % kStages;
+            if (!wait(&p_full[g], jl & 1) ||
+                !wait(&v_full[st], (jl / kStages) & 1))
                 return false;
             tc_fence_after();
             // B = [value tile | ones]: two MN atoms, the ones atom kOnesOff - value stage bytes away
@@ -261,15 +279,15 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks)
                 mma_ts_w(tb + kTmO + 128 * g, tb + kTmS + 128 * g + 8 * ks, d_v + ks * (2048 >> 4), id_o,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-            if (j + 1 <= last[g]) return issue_s(g, j + 1);
+                       (j > j0 || ks > 0) ? 1u : 0u);
+            if (j + 1 <= jend(g)) return issue_s(g, j + 1);
             return true;
         };
-        bool ok = wait(&q_full, 0) && issue_s(0, 0) && (!has_b || issue_s(1, 0));
-        for (int j = 0; ok && j < nj; ++j) {
-            if (j <= last[0] && !issue_o(0, j)) { ok = false; break; }
-            if (j <= last[1] && !issue_o(1, j)) { ok = false; break; }
-            mma_commit_w(&kv_free[j % kStages]);  // both tiles' products with key / value tile j are issued
+        bool ok = wait(&q_full, 0) && (jend(0) < j0 || issue_s(0, j0)) && (jend(1) < j0 || issue_s(1, j0));
+        for (int j = j0; ok && j < j1; ++j) {
+            if (j <= jend(0) && !issue_o(0, j)) { ok = false; break; }
+            if (j <= jend(1) && !issue_o(1, j)) { ok = false; break; }
+            mma_commit_w(&kv_free[(j - j0) % kStages]);  // both tiles' products with key / value tile j are issued
         }
         if (!ok) fail();
         mma_commit_w(&o_done);
@@ -280,15 +298,15 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const int r = t - 384;
         // gated form: L of this thread's key in the next tile, loaded one tile
         // ahead so that its latency overlaps the wait for the tile
-        float lk_next = (GATED && r < T) ? Lc[bh * T + r] : 0.f;
-        for (int j = 0; j < nj; ++j) {
-            const int st = j % kStages;
+        float lk_next = (GATED && j0 * kTile + r < T) ? Lc[bh * T + j0 * kTile + r] : 0.f;
+        for (int j = j0; j < j1; ++j) {
+            const int jl = j - j0, st = jl % kStages;
             const float lk = lk_next;
             if (GATED) {
                 const int nk = (j + 1) * kTile + r;
-                lk_next = (j + 1 < nj && nk < T) ? Lc[bh * T + nk] : 0.f;
+                lk_next = (j + 1 < j1 && nk < T) ? Lc[bh * T + nk] : 0.f;
             }
-            if (!wait(&k_full[st], (j / kStages) & 1)) { fail(); break; }
+            if (!wait(&k_full[st], (jl / kStages) & 1)) { fail(); break; }
             uint8_t* kb = sm + kKOff + st * kAtom;
             uint4 raw[P / 8];
             float ss = 0.f;
@@ -334,7 +352,7 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         float lrow = 0.f;
         int zrow = -1;
         if (GATED) {
-            const int row = min(T - 1, last[g] * kTile + e);
+            const int row = min(T - 1, last(g) * kTile + e);
             lrow = Lc[bh * T + row];
             zrow = zid[bh * T + row];
         }
@@ -345,13 +363,14 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // chosen once per CTA, so the squaring of the common case stays lean.
         auto square = [&](auto exact_tag) -> bool {
             constexpr bool EXACT = decltype(exact_tag)::value;
-            for (int j = 0; j <= last[g]; ++j) {
-                if (!wait(&s_full[g], j & 1)) return false;
+            for (int j = j0; j <= jend(g); ++j) {
+                const int jl = j - j0;
+                if (!wait(&s_full[g], jl & 1)) return false;
                 // the key tile's L values are in shared memory (its staging completed before the scores' MMA)
-                if (EXACT && !wait(&k_ready[j % kStages], (j / kStages) & 1)) return false;
+                if (EXACT && !wait(&k_ready[jl % kStages], (jl / kStages) & 1)) return false;
                 tc_fence_after();
-                const bool diag = j == last[g];  // keys past the query are masked only on the diagonal tile
-                const float* gs = reinterpret_cast<const float*>(sm + kGateOff + (j % kStages) * kGateStage);
+                const bool diag = j == last(g);  // keys past the query are masked only on the diagonal tile
+                const float* gs = reinterpret_cast<const float*>(sm + kGateOff + (jl % kStages) * kGateStage);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t pk[16];
@@ -397,11 +416,11 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             sq_ok = square(std::false_type{});
         }
         if (!sq_ok) fail();
-        // ---- o = O[:, :DV] / O[:, 64]
+        // ---- o = O[:, :DV] / O[:, 64] (split: after the exchange below)
         const bool ok = wait(&o_done, 0) && !abort_flag;
         tc_fence_after();
         const int qi = (g == 0 ? qa : qb) * kTile + e;
-        if (ok && last[g] >= 0) {
+        if (!split && ok && last(g) >= 0) {
             const uint32_t ob = tb + kTmO + 128 * g;
             uint32_t r[16];
             tmem_ld16(tmem_addr(ob, lane0, 64), r);
@@ -428,6 +447,65 @@ quadratic_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (split) {
+        // every copy has landed and every MMA completed (the producer and the
+        // MMA warp waited for them): the stage memory is free for the exchange,
+        // x[g][c][row] = O_g[row][c] of rank 1 (c = DV: the denominator)
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        float* x = reinterpret_cast<float*>(sm);
+        const bool sq = warp >= 4 && warp < 12;
+        const int g = warp >= 8 ? 1 : 0, e = t & 127;
+        const uint32_t lane0 = (uint32_t)((warp & 3) * 32), ob = tb + kTmO + 128 * g;
+        const bool live = !abort_flag && jend(g) >= j0;  // this tile has products in this CTA
+        if (sq && part == 1) {
+            uint32_t r[16];
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 16) {
+                if (live) {
+                    tmem_ld16(tmem_addr(ob, lane0, c0), r);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[(g * (DV + 1) + c0 + i) * kTile + e] = live ? __uint_as_float(r[i]) : 0.f;
+            }
+            if (live) {
+                tmem_ld16(tmem_addr(ob, lane0, 64), r);
+                tmem_wait_ld();
+            }
+            x[(g * (DV + 1) + DV) * kTile + e] = live ? __uint_as_float(r[0]) : 0.f;
+        }
+        cluster_barrier();
+        const int qi = (g == 0 ? qa : qb) * kTile + e;
+        // (the tensor-memory loads are warp-wide: rows past T load and skip the store)
+        if (sq && part == 0 && live) {
+            const float* xr = cluster.map_shared_rank(x, 1);
+            uint32_t r[16];
+            tmem_ld16(tmem_addr(ob, lane0, 64), r);
+            tmem_wait_ld();
+            const float den = __uint_as_float(r[0]) + xr[(g * (DV + 1) + DV) * kTile + e];
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 16) {
+                tmem_ld16(tmem_addr(ob, lane0, c0), r);
+                tmem_wait_ld();
+                uint4 out[2];
+                uint32_t* w = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float a = __uint_as_float(r[2 * i]) + xr[(g * (DV + 1) + c0 + 2 * i) * kTile + e];
+                    const float b = __uint_as_float(r[2 * i + 1]) + xr[(g * (DV + 1) + c0 + 2 * i + 1) * kTile + e];
+                    w[i] = pack_bf16x2(a * inv, b * inv);
+                }
+                if (qi < T) {
+                    __nv_bfloat16* dst = o + (bh * T + qi) * (int64_t)DV + c0;
+                    reinterpret_cast<uint4*>(dst)[0] = out[0];
+                    reinterpret_cast<uint4*>(dst)[1] = out[1];
+                }
+            }
+        }
+        cluster_barrier();  // rank 1's shared memory stays until rank 0 has read it
+    }
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
@@ -441,9 +519,25 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, void* o, i
     CUtensorMap tq, tk, tv;
     if (!rows_map(&tq, q, P, T, BH) || !rows_map(&tk, k, P, T, BH) || !rows_map(&tv, v, DV, T, BH))
         return cudaErrorInvalidValue;
-    dim3 grid(((T + kTile - 1) / kTile + 1) / 2, BH);
+    const int ntiles = (T + kTile - 1) / kTile, pairs = (ntiles + 1) / 2;
+    // when even two CTAs a pair fit in one wave, split each pair's key tiles
+    // over a cluster of two (a second wave costs more than the split saves)
+    const int split = ntiles >= 2 && 2 * (int64_t)pairs * BH <= kSplitMax ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pairs * (1 + split)), (unsigned)BH, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1 + split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split ? 1 : 0;
     KATA_TRACED(GATED ? "quadratic_gated_tc" : "quadratic_tc", s,
-                kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o), T, Lc, zid));
+                (e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, static_cast<__nv_bfloat16*>(o), T, Lc, zid, split)));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

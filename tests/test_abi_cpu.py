@@ -198,7 +198,7 @@ def test_gated_argument_errors(lib):
     d = lib.kata_decode_step_gated
     assert d(P, P, P, P, P, kb.KATA_FP32, 1, 1, 16, 16, P, P, P) == kb.KATA_ERR_INVALID_ARG
     assert d(P, P, P, P, P, kb.KATA_FP32, 0, 1, 16, 16, P, P, P) == kb.KATA_OK
-    # states [BH, NC, n, dv] + [BH, NC, n] + chunk decays [BH, NC], each 256-byte aligned
+    # states [BH, NC, n, dv] + [BH, NC, n] + chunk decays [BH, NC] + token decays [BH, T], each 256-byte aligned
     got = lib.kata_chunked_gated_workspace_bytes(kb.KATA_FP32, 1, 2, 100, 16, 16, 32)
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    assert got == r(2 * 4 * 136 * 16 * 4) + r(2 * 4 * 136 * 4) + r(2 * 4 * 4)
+    assert got == r(2 * 4 * 136 * 16 * 4) + r(2 * 4 * 136 * 4) + r(2 * 4 * 4) + r(2 * 100 * 4)

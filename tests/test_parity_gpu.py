@@ -54,6 +54,20 @@ def test_quadratic_tile_hint_does_not_change_results(C):
     assert_close(f64(o), oracle.forward_plain(f64(q), f64(k), f64(v)), torch.bfloat16, "quadratic")
 
 
+@pytest.mark.parametrize("B,H", [(1, 2), (4, 10)])
+@pytest.mark.parametrize("T", [129, 600, 1000])
+def test_quadratic_key_split_and_whole_pairs(B, H, T):
+    """bf16 flash-style form where two CTAs a pair of query tiles fit in one
+    wave (two heads, and 40 heads of 129 tokens: each pair's key tiles split
+    over a cluster of two CTAs whose partial sums add) and where they do not
+    (40 heads of 600 or 1000 tokens: one CTA a pair); 129 tokens puts one key
+    tile in each part, 600 an odd tile count (a last pair with one query tile)."""
+    q, k, v = _inputs(B, H, T, 64, 64, torch.bfloat16, seed=B * H + T)
+    o = kb.kata_forward_quadratic(q, k, v)
+    kb.kata_get_device_status()
+    assert_close(f64(o), oracle.forward_plain(f64(q), f64(k), f64(v)), torch.bfloat16, "quadratic, key split")
+
+
 # ---------------------------------------------------------------- chunked form
 
 @pytest.mark.parametrize("dtype", DTYPES)
