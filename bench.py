@@ -126,6 +126,9 @@ def kernel_work(name, w, form="chunked", lift=None):
     if name == "intra_tc":
         # the causal intra-chunk half of the forward
         return "flop", bht * (w.C + 1) * (w.p + w.dv)
+    if name == "states_tc" and form == "gated":
+        # the gated form's chunk states (each key lift weighted by its decay)
+        return "flop", bht * 2 * w.n * (w.dv + 1)
     if name == "states_tc":
         # segment start states: recomputed work, no algorithmic share
         return "flop", 0
@@ -143,6 +146,9 @@ def kernel_work(name, w, form="chunked", lift=None):
     if name in ("gated_scan", "backward_reverse_scan"):
         nc = w.NC if name == "gated_scan" else (w.T + 63) // 64
         return "byte", 2 * w.B * w.H * nc * w.n * (w.dv + 1) * 4
+    if name == "gate_decay":
+        # the gates read, each token's decay to its chunk's end written
+        return "byte", bht * 8
     if name == "gate_prefix":
         # the gates read, the per-token log-gate sums and last zero gates written
         return "byte", bht * 12

@@ -37,6 +37,11 @@ def test_kernel_work_split_and_bytes():
     assert kind == "flop" and quad == 2 * 8 * 2048 * 2049 * 96
     # the segment-state prepass of the forward does no algorithmic work of its own
     assert bench.kernel_work("states_tc", w) == ("flop", 0)
+    # the gated form's chunk states are its own work; its decays one read and one write a token
+    c3 = W["c3"]
+    bht3 = c3.B * c3.H * c3.T
+    assert bench.kernel_work("states_tc", c3, "gated") == ("flop", bht3 * 2 * 2080 * 65)
+    assert bench.kernel_work("gate_decay", c3, "gated") == ("byte", bht3 * 8)
 
 
 def test_block_lift_work_model():
