@@ -21,7 +21,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxC = 128;
 constexpr int kRowsPerBlock = 64;
-constexpr int kTile = 32;
 
 // ---------------------------------------------------------------- chunk states
 template <int P, int DV>
@@ -172,121 +171,199 @@ gate_decay_kernel(const float* __restrict__ gate, float* __restrict__ dec, float
 }
 
 // ---------------------------------------------------------------- chunk output
+constexpr int kSlotTile = 64;  // packed rows of the prefix state per pass
+constexpr int kKeyTile = 32;   // keys of the chunk per pass of the local part
+
 template <int P, int DV>
-constexpr size_t output_smem_bytes() {
-    return sizeof(float) * (2 * kMaxC * (P + 1) + kMaxC * DV + kMaxC * (kTile + 1) + kTile * DV + kTile +
-                            kMaxC * (kTile + 1) + kMaxC) +
-           sizeof(int) * 2 * kTile;
+__host__ __device__ constexpr int output_union_floats() {
+    constexpr int LDP = P + 1, LDT = kMaxC + 4;
+    constexpr int readout = kSlotTile * LDT + kSlotTile * DV + kSlotTile;
+    constexpr int local = kKeyTile * LDP + kKeyTile * DV + kKeyTile * LDT;
+    return readout > local ? readout : local;
 }
 
-// Block (chunk c, head bh): thread owns token tid/2 and half of the value
-// columns; the local part walks the chunk's keys from the token backwards so
-// the decay is one running product.
+template <int P, int DV>
+constexpr size_t output_smem_bytes() {
+    return sizeof(float) * ((size_t)kMaxC * (P + 1) + kMaxC + output_union_floats<P, DV>()) +
+           sizeof(int) * 2 * kSlotTile;
+}
+
+// Block (chunk c, head bh), kThreads threads: thread (tg, cg) holds tokens
+// 4 tg .. 4 tg + 3 (and the same of KT - 1 further token groups when one
+// pass of the block does not cover the chunk) times value columns
+// 4 cg .. 4 cg + 3 in registers.
+//   prefix readout  per tile of kSlotTile packed rows: the chunk's query
+//                   lifts (rows x tokens) and the prefix state rows in shared
+//                   memory, each thread accumulating its 4 x 4 products (two
+//                   16-byte loads per 16 multiply-adds); then scaled by the
+//                   decay from the chunk's start, prod_{r=cC..t} gamma_r
+//   local part      per tile of kKeyTile keys: the decayed squared scores
+//                   prod_{r=s+1..t} gamma_r (qh_t.kh_s)^2 (keys x tokens) and
+//                   the values, accumulated the same way
+// Each (token, column) sum runs over the packed rows, then over the keys, in
+// order.  The denominators' products are shared out over the CG threads of a
+// token group (thread cg takes rows cg, cg + CG, ...) and summed by shuffles
+// at the end.
 template <typename Tin, int P, int DV>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 gated_output_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                     const float* __restrict__ gate, const float* __restrict__ Pre, const float* __restrict__ Prez,
                     Tin* __restrict__ o, int T, int C, int NC) {
-    constexpr int LDP = P + 1, LDT = kTile + 1, CPT = DV / 2, N = P * (P + 1) / 2;
+    constexpr int LDP = P + 1, LDT = kMaxC + 4, N = P * (P + 1) / 2;
+    constexpr int CG = DV / 4, TGT = kThreads / CG, KT = (kMaxC / 4 + TGT - 1) / TGT;
+    static_assert(kSlotTile % CG == 0 && kKeyTile % CG == 0 && CG <= 32, "column groups");
     extern __shared__ float smem[];
-    float* Qs = smem;              // [C][LDP]
-    float* Ks = Qs + kMaxC * LDP;  // [C][LDP]
-    float* Vs = Ks + kMaxC * LDP;  // [C][DV]
-    float* Ps = Vs + kMaxC * DV;   // [C][LDT] lifted-query tile
-    float* St = Ps + kMaxC * LDT;  // [kTile][DV] prefix state tile
-    float* Zt = St + kTile * DV;   // [kTile]
-    float* Sc = Zt + kTile;        // [C][LDT] local score tile
-    float* gs = Sc + kMaxC * LDT;  // [C] gates of the chunk
-    int* Ii = reinterpret_cast<int*>(gs + kMaxC);
-    int* Jj = Ii + kTile;
+    float* Qs = smem;              // [C][LDP] unit queries
+    float* gs = Qs + kMaxC * LDP;  // [C] gates of the chunk
+    float* Ru = gs + kMaxC;        // the readout's and the local part's tiles share this
+    float* Pt = Ru;                                // [kSlotTile][LDT] query lifts, row-major by packed row
+    float* St = Pt + kSlotTile * LDT;              // [kSlotTile][DV] prefix state rows
+    float* Zt = St + kSlotTile * DV;               // [kSlotTile] prefix normaliser rows
+    float* Ks = Ru;                                // [kKeyTile][LDP] unit keys
+    float* Vs = Ks + kKeyTile * LDP;               // [kKeyTile][DV]
+    float* Sc = Vs + kKeyTile * DV;                // [kKeyTile][LDT] decayed squared scores, by key
+    int* Ii = reinterpret_cast<int*>(Ru + output_union_floats<P, DV>());
+    int* Jj = Ii + kSlotTile;
 
     const int c = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int t0 = c * C, len = min(C, T - t0);
+    const int ngroups = (len + 3) / 4, nt = 4 * ngroups;
     load_rows_unit<Tin, P>(q + bh * T * P, t0, len, T, Qs, LDP);
-    load_rows_unit<Tin, P>(k + bh * T * P, t0, len, T, Ks, LDP);
-    load_rows_plain<Tin, DV>(v + bh * T * DV, t0, len, T, Vs, DV);
     for (int s = threadIdx.x; s < kMaxC; s += blockDim.x) gs[s] = s < len ? gate[bh * T + t0 + s] : 0.f;
 
-    const int t = threadIdx.x >> 1, half = threadIdx.x & 1;
-    float acc[CPT];
+    const int cg = threadIdx.x % CG, tg0 = threadIdx.x / CG;
+    float acc[KT][4][4], den[KT][4];
 #pragma unroll
-    for (int x = 0; x < CPT; ++x) acc[x] = 0.f;
-    float den = 0.f;
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            den[kt][i] = 0.f;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[kt][i][x] = 0.f;
+        }
+    // the 4 x 4 products of row `row` of A (tokens) and B (columns): 16 multiply-adds per token group
+    auto accumulate = [&](const float* A, const float* B, int row) {
+        const float4 b = *reinterpret_cast<const float4*>(B + row * DV + 4 * cg);
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            const int tg = tg0 + kt * TGT;
+            if (tg < ngroups) {
+                const float4 a = *reinterpret_cast<const float4*>(A + row * LDT + 4 * tg);
+                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[kt][i][x] = fmaf(av[i], bv[x], acc[kt][i][x]);
+            }
+        }
+    };
+    // this thread's share of the denominator: row `row` of A times w
+    auto accumulate_den = [&](const float* A, int row, float w) {
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            const int tg = tg0 + kt * TGT;
+            if (tg < ngroups) {
+                const float4 a = *reinterpret_cast<const float4*>(A + row * LDT + 4 * tg);
+                den[kt][0] = fmaf(a.x, w, den[kt][0]);
+                den[kt][1] = fmaf(a.y, w, den[kt][1]);
+                den[kt][2] = fmaf(a.z, w, den[kt][2]);
+                den[kt][3] = fmaf(a.w, w, den[kt][3]);
+            }
+        }
+    };
 
-    // prefix readout psi(qh_t)^T P_c, scaled afterwards by prod_{r=t0..t} gamma
+    // prefix readout psi(qh_t)^T P_c
     const float* Pc = Pre + (bh * NC + c) * (int64_t)N * DV;
     const float* Pzc = Prez + (bh * NC + c) * (int64_t)N;
-    for (int a0 = 0; a0 < N; a0 += kTile) {
-        __syncthreads();
-        if (threadIdx.x < kTile) {
+    for (int a0 = 0; a0 < N; a0 += kSlotTile) {
+        __syncthreads();  // the previous tile's readers are done
+        if (threadIdx.x < kSlotTile) {
+            const int a = a0 + threadIdx.x;
             int i = 0, j = 0;
-            if (a0 + threadIdx.x < N) unpack_index(a0 + threadIdx.x, P, i, j);
+            if (a < N) unpack_index(a, P, i, j);
             Ii[threadIdx.x] = i;
             Jj[threadIdx.x] = j;
-            Zt[threadIdx.x] = a0 + threadIdx.x < N ? Pzc[a0 + threadIdx.x] : 0.f;
+            Zt[threadIdx.x] = a < N ? Pzc[a] : 0.f;
         }
-        for (int e = threadIdx.x; e < kTile * DV; e += blockDim.x) {
-            const int aa = e / DV;
-            St[e] = a0 + aa < N ? Pc[(int64_t)a0 * DV + e] : 0.f;
+        for (int e = threadIdx.x; e < kSlotTile * (DV / 4); e += blockDim.x) {
+            const int aa = e / (DV / 4);
+            const float4 val = a0 + aa < N ? *reinterpret_cast<const float4*>(Pc + (int64_t)a0 * DV + 4 * e)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(St + 4 * e) = val;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
-            const int tt = e / kTile, aa = e - tt * kTile;
+        for (int e = threadIdx.x; e < kSlotTile * nt; e += blockDim.x) {
+            const int aa = e / nt, tt = e - aa * nt;
             const int i = Ii[aa], j = Jj[aa];
             const float scale = (i == j) ? 1.f : kSqrt2;
-            Ps[tt * LDT + aa] = a0 + aa < N ? Qs[tt * LDP + i] * Qs[tt * LDP + j] * scale : 0.f;
+            Pt[aa * LDT + tt] = (tt < len && a0 + aa < N) ? Qs[tt * LDP + i] * Qs[tt * LDP + j] * scale : 0.f;
         }
         __syncthreads();
-        if (t < len) {
-            for (int aa = 0; aa < kTile; ++aa) {
-                const float ps = Ps[t * LDT + aa];
-                den = fmaf(ps, Zt[aa], den);
+        for (int r0 = 0; r0 < kSlotTile; r0 += CG) {
+            accumulate_den(Pt, r0 + cg, Zt[r0 + cg]);
 #pragma unroll
-                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(ps, St[aa * DV + half * CPT + x], acc[x]);
+            for (int u = 0; u < CG; ++u) accumulate(Pt, St, r0 + u);
+        }
+    }
+    // scaled by prod_{r=cC..t} gamma_r
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 4 * (tg0 + kt * TGT) + i;
+            if (t < len) {
+                float h = 1.f;
+                for (int r = 0; r <= t; ++r) h *= gs[r];
+                den[kt][i] *= h;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) acc[kt][i][x] *= h;
             }
         }
-    }
-    if (t < len) {
-        float h = 1.f;
-        for (int r = 0; r <= t; ++r) h *= gs[r];
-        den *= h;
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) acc[x] *= h;
-    }
-    // local part: key tiles from the token's own tile backwards
-    float decay = 1.f;  // prod_{r=s+1..t} gamma for the key s being added
-    const int last_tile = (len - 1) / kTile;
-    for (int tile = last_tile; tile >= 0; --tile) {
-        const int s0 = tile * kTile;
+    // local part: sum_{s in c, s <= t} prod_{r=s+1..t} gamma_r (qh_t.kh_s)^2 [v_s | 1]
+    for (int s0 = 0; s0 < len; s0 += kKeyTile) {
+        __syncthreads();  // the previous tile's readers are done
+        load_rows_unit<Tin, P>(k + bh * T * P, t0 + s0, kKeyTile, T, Ks, LDP);
+        load_rows_plain<Tin, DV>(v + bh * T * DV, t0 + s0, kKeyTile, T, Vs, DV);
         __syncthreads();
-        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
-            const int tt = e / kTile, ss = e - tt * kTile, s = s0 + ss;
-            float d = 0.f;
-            if (s < len && s <= tt) {
+        for (int e = threadIdx.x; e < kKeyTile * nt; e += blockDim.x) {
+            const int ss = e / nt, tt = e - ss * nt, s = s0 + ss;
+            float val = 0.f;
+            if (tt < len && s <= tt) {
+                float d = 0.f;
 #pragma unroll 16
-                for (int i = 0; i < P; ++i) d = fmaf(Qs[tt * LDP + i], Ks[s * LDP + i], d);
+                for (int i = 0; i < P; ++i) d = fmaf(Qs[tt * LDP + i], Ks[ss * LDP + i], d);
+                float decay = 1.f;
+                for (int r = tt; r > s; --r) decay *= gs[r];
+                val = decay * (d * d);
             }
-            Sc[tt * LDT + ss] = d * d;
+            Sc[ss * LDT + tt] = val;
         }
         __syncthreads();
-        if (t < len) {
-            for (int ss = kTile - 1; ss >= 0; --ss) {
-                const int s = s0 + ss;
-                if (s > t || s >= len) continue;
-                if (s < t) decay *= gs[s + 1];
-                const float sc = decay * Sc[t * LDT + ss];
-                den += sc;
+        for (int r0 = 0; r0 < kKeyTile; r0 += CG) {
+            accumulate_den(Sc, r0 + cg, 1.f);
 #pragma unroll
-                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(sc, Vs[s * DV + half * CPT + x], acc[x]);
-            }
+            for (int u = 0; u < CG; ++u) accumulate(Sc, Vs, r0 + u);
         }
     }
-    if (t < len) {
-        Tin* ot = o + (bh * T + t0 + t) * DV + half * CPT;
+    // denominators: the CG threads of a token group are neighbouring lanes
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) store_as(ot + x, den > 0.f ? acc[x] / den : 0.f);
-    }
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int off = 1; off < CG; off <<= 1) den[kt][i] += __shfl_xor_sync(0xffffffffu, den[kt][i], off);
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 4 * (tg0 + kt * TGT) + i;
+            if (t < len) {
+                Tin* ot = o + (bh * T + t0 + t) * DV + 4 * cg;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) store_as(ot + x, den[kt][i] > 0.f ? acc[kt][i][x] / den[kt][i] : 0.f);
+            }
+        }
 }
 
 template <typename Tin, int P, int DV>
