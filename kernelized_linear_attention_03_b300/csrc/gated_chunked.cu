@@ -14,6 +14,7 @@
 
 #include "kata_device.cuh"
 #include "kata_internal.h"
+#include "tc_primitives.cuh"
 
 namespace kata {
 namespace {
@@ -177,7 +178,7 @@ constexpr int kKeyTile = 32;   // keys of the chunk per pass of the local part
 template <int P, int DV>
 __host__ __device__ constexpr int output_union_floats() {
     constexpr int LDP = P + 1, LDT = kMaxC + 4;
-    constexpr int readout = kSlotTile * LDT + kSlotTile * DV + kSlotTile;
+    constexpr int readout = kSlotTile * LDT + 2 * (kSlotTile * DV + kSlotTile);
     constexpr int local = kKeyTile * LDP + kKeyTile * DV + kKeyTile * LDT;
     return readout > local ? readout : local;
 }
@@ -194,9 +195,11 @@ constexpr size_t output_smem_bytes() {
 // 4 cg .. 4 cg + 3 in registers.
 //   prefix readout  per tile of kSlotTile packed rows: the chunk's query
 //                   lifts (rows x tokens) and the prefix state rows in shared
-//                   memory, each thread accumulating its 4 x 4 products (two
-//                   16-byte loads per 16 multiply-adds); then scaled by the
-//                   decay from the chunk's start, prod_{r=cC..t} gamma_r
+//                   memory (the next tile's rows copied asynchronously into a
+//                   second buffer meanwhile), each thread accumulating its
+//                   4 x 4 products (two 16-byte loads per 16 multiply-adds);
+//                   then scaled by the decay from the chunk's start,
+//                   prod_{r=cC..t} gamma_r
 //   local part      per tile of kKeyTile keys: the decayed squared scores
 //                   prod_{r=s+1..t} gamma_r (qh_t.kh_s)^2 (keys x tokens) and
 //                   the values, accumulated the same way
@@ -217,8 +220,8 @@ gated_output_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const 
     float* gs = Qs + kMaxC * LDP;  // [C] gates of the chunk
     float* Ru = gs + kMaxC;        // the readout's and the local part's tiles share this
     float* Pt = Ru;                                // [kSlotTile][LDT] query lifts, row-major by packed row
-    float* St = Pt + kSlotTile * LDT;              // [kSlotTile][DV] prefix state rows
-    float* Zt = St + kSlotTile * DV;               // [kSlotTile] prefix normaliser rows
+    float* Sb = Pt + kSlotTile * LDT;              // two buffers of [kSlotTile][DV] prefix state rows
+    float* Zb = Sb + 2 * kSlotTile * DV;           // and of [kSlotTile] prefix normaliser rows
     float* Ks = Ru;                                // [kKeyTile][LDP] unit keys
     float* Vs = Ks + kKeyTile * LDP;               // [kKeyTile][DV]
     float* Sc = Vs + kKeyTile * DV;                // [kKeyTile][LDT] decayed squared scores, by key
@@ -276,36 +279,64 @@ gated_output_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const 
     // prefix readout psi(qh_t)^T P_c
     const float* Pc = Pre + (bh * NC + c) * (int64_t)N * DV;
     const float* Pzc = Prez + (bh * NC + c) * (int64_t)N;
-    for (int a0 = 0; a0 < N; a0 += kSlotTile) {
-        __syncthreads();  // the previous tile's readers are done
-        if (threadIdx.x < kSlotTile) {
-            const int a = a0 + threadIdx.x;
-            int i = 0, j = 0;
-            if (a < N) unpack_index(a, P, i, j);
-            Ii[threadIdx.x] = i;
-            Jj[threadIdx.x] = j;
-            Zt[threadIdx.x] = a < N ? Pzc[a] : 0.f;
-        }
+    // packed rows a0 .. a0 + kSlotTile - 1 of the prefix state into buffer b (rows past N zero-filled)
+    auto copy_tile = [&](int a0, int b) {
+        float* St = Sb + b * kSlotTile * DV;
         for (int e = threadIdx.x; e < kSlotTile * (DV / 4); e += blockDim.x) {
-            const int aa = e / (DV / 4);
-            const float4 val = a0 + aa < N ? *reinterpret_cast<const float4*>(Pc + (int64_t)a0 * DV + 4 * e)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(St + 4 * e) = val;
+            const bool in = a0 + e / (DV / 4) < N;
+            tc::cp_async16(St + 4 * e, in ? Pc + (int64_t)a0 * DV + 4 * e : Pc, in ? 16u : 0u);
         }
-        __syncthreads();
+        for (int e = threadIdx.x; e < kSlotTile / 4; e += blockDim.x) {
+            const bool in = a0 + 4 * e < N;  // N - a0 rows are left; a partial vector is read as scalars below
+            if (in && a0 + 4 * e + 4 <= N)
+                tc::cp_async16(Zb + b * kSlotTile + 4 * e, Pzc + a0 + 4 * e, 16u);
+            else
+                for (int u = 0; u < 4; ++u) Zb[b * kSlotTile + 4 * e + u] = a0 + 4 * e + u < N ? Pzc[a0 + 4 * e + u] : 0.f;
+        }
+        tc::cp_async_commit();
+    };
+    // the chunk's query lifts of packed rows a0 .. into Pt; (aa, tt) from e by
+    // shifts when the token count is a power of two (every full chunk)
+    auto lift_tile = [&](int a0, auto pow2) {
+        constexpr bool POW2 = decltype(pow2)::value;
+        const int sh = __ffs(nt) - 1;
         for (int e = threadIdx.x; e < kSlotTile * nt; e += blockDim.x) {
-            const int aa = e / nt, tt = e - aa * nt;
+            const int aa = POW2 ? e >> sh : e / nt, tt = POW2 ? e & (nt - 1) : e - aa * nt;
             const int i = Ii[aa], j = Jj[aa];
             const float scale = (i == j) ? 1.f : kSqrt2;
             Pt[aa * LDT + tt] = (tt < len && a0 + aa < N) ? Qs[tt * LDP + i] * Qs[tt * LDP + j] * scale : 0.f;
         }
+    };
+    const bool pow2 = (nt & (nt - 1)) == 0;
+    copy_tile(0, 0);
+    for (int a0 = 0, b = 0; a0 < N; a0 += kSlotTile, b ^= 1) {
+        __syncthreads();  // the previous tile's readers are done (with Pt and with buffer b ^ 1)
+        if (a0 + kSlotTile < N)
+            copy_tile(a0 + kSlotTile, b ^ 1);
+        else
+            tc::cp_async_commit();  // (an empty group keeps the count of groups in flight fixed)
+        if (threadIdx.x < kSlotTile) {
+            int i = 0, j = 0;
+            if (a0 + threadIdx.x < N) unpack_index(a0 + threadIdx.x, P, i, j);
+            Ii[threadIdx.x] = i;
+            Jj[threadIdx.x] = j;
+        }
+        tc::cp_async_wait<1>();  // this thread's copies of tile b have landed
+        __syncthreads();         // everyone's, and the row indices
+        if (pow2)
+            lift_tile(a0, std::true_type{});
+        else
+            lift_tile(a0, std::false_type{});
         __syncthreads();
+        const float* St = Sb + b * kSlotTile * DV;
+        const float* Zt = Zb + b * kSlotTile;
         for (int r0 = 0; r0 < kSlotTile; r0 += CG) {
             accumulate_den(Pt, r0 + cg, Zt[r0 + cg]);
 #pragma unroll
             for (int u = 0; u < CG; ++u) accumulate(Pt, St, r0 + u);
         }
     }
+    tc::cp_async_wait<0>();
     // scaled by prod_{r=cC..t} gamma_r
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt)
