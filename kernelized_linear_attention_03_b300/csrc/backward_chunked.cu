@@ -486,10 +486,17 @@ cudaError_t typed(const void* q, const void* k, const void* v, const void* dO, v
     constexpr int N = P * (P + 1) / 2;
     const int NC = (T + kBC - 1) / kBC;
     const int dtype = sizeof(Tin) == 4 ? 0 : 1;
-    // forward prefix states at the backward's chunk length
-    cudaError_t e = launch_chunk_states_simt(dtype, k, v, S, z, BH, T, P, DV, kBC, s);
-    if (e == cudaSuccess) e = launch_scan(0, S, S, nullptr, nullptr, BH, NC, (int64_t)N * DV, s);
-    if (e == cudaSuccess) e = launch_scan(0, z, z, nullptr, nullptr, BH, NC, N, s);
+    // forward prefix states at the backward's chunk length (bf16: the
+    // tensor-core chunk-state kernel writes every chunk's exclusive prefix in
+    // one pass, as the forward's own states are built)
+    cudaError_t e;
+    if (dtype == 1) {
+        e = launch_states_tc(k, v, S, z, BH, T, P, DV, kBC, NC, NC, 1, 1, s);
+    } else {
+        e = launch_chunk_states_simt(dtype, k, v, S, z, BH, T, P, DV, kBC, s);
+        if (e == cudaSuccess) e = launch_scan(0, S, S, nullptr, nullptr, BH, NC, (int64_t)N * DV, s);
+        if (e == cudaSuccess) e = launch_scan(0, z, z, nullptr, nullptr, BH, NC, N, s);
+    }
     if (e != cudaSuccess) return e;
     {
         constexpr size_t smem = sizeof(float) * query_smem_floats<P, DV>();

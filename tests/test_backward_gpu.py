@@ -82,3 +82,16 @@ def test_backward_zero_vectors(form):
 def test_chunked_backward_long_sequence():
     """Many backward chunks (the reverse prefix over 33 chunks) on several heads."""
     _check(*_case(2, 2, 2100, 32, 32, torch.float32, seed=8), torch.float32, "chunked")
+
+
+def test_chunked_backward_bf16_prefix_states_on_tensor_cores():
+    """bf16: the forward's prefix states at the backward's 64-token chunks come
+    from the tensor-core chunk-state kernel in prefix mode (every chunk's
+    exclusive prefix in one pass, no scan); 33 chunks on several heads, a
+    ragged last chunk, against the oracle's gradients."""
+    kb.kata_trace_start(4096)
+    try:
+        _check(*_case(2, 2, 2100, 32, 32, torch.bfloat16, seed=8), torch.bfloat16, "chunked")
+    finally:
+        names = {name for name, _ in kb.kata_trace_stop()}
+    assert "states_tc" in names and "chunk_states_simt" not in names, names
