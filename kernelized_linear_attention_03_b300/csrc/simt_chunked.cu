@@ -7,6 +7,7 @@
 // kata_chunk_state_scan.
 #include "kata_device.cuh"
 #include "kata_internal.h"
+#include "simt_output.cuh"
 
 namespace kata {
 namespace {
@@ -60,111 +61,6 @@ chunk_states_simt_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
     if (cg == 0) z_loc[(bh * NC + c) * N + a] = zacc;
 }
 
-// ---------------------------------------------------------------- chunk output
-// Block (chunk c, head bh): thread owns token t = tid/2 of the chunk and half
-// of the value columns.  The prefix readout walks the packed rows in tiles of
-// 32 (lifted queries and state rows staged in shared memory); the local part
-// walks the chunk's keys in tiles of 32 with squared masked scores.
-constexpr int kTile = 32;
-
-template <int P, int DV>
-constexpr size_t output_smem_bytes() {
-    return sizeof(float) * (2 * kMaxC * (P + 1) + kMaxC * DV + kMaxC * (kTile + 1) + kTile * DV +
-                            kTile + kMaxC * (kTile + 1)) +
-           sizeof(int) * 2 * kTile;
-}
-
-template <typename Tin, int P, int DV>
-__global__ void __launch_bounds__(kThreads)
-chunk_output_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
-                         const Tin* __restrict__ v, const float* __restrict__ Pre,
-                         const float* __restrict__ Prez, Tin* __restrict__ o, int T, int C, int NC) {
-    constexpr int LDP = P + 1, LDT = kTile + 1, CPT = DV / 2, N = P * (P + 1) / 2;
-    extern __shared__ float smem[];
-    float* Qs = smem;                    // [C][LDP]
-    float* Ks = Qs + kMaxC * LDP;        // [C][LDP]
-    float* Vs = Ks + kMaxC * LDP;        // [C][DV]
-    float* Ps = Vs + kMaxC * DV;         // [C][LDT] lifted-query tile
-    float* St = Ps + kMaxC * LDT;        // [kTile][DV] prefix state tile
-    float* Zt = St + kTile * DV;         // [kTile]
-    float* Sc = Zt + kTile;              // [C][LDT] local score tile
-    int* Ii = reinterpret_cast<int*>(Sc + kMaxC * LDT);
-    int* Jj = Ii + kTile;
-
-    const int c = blockIdx.x;
-    const int64_t bh = blockIdx.y;
-    const int t0 = c * C, len = min(C, T - t0);
-    load_rows_unit<Tin, P>(q + bh * T * P, t0, len, T, Qs, LDP);
-    load_rows_unit<Tin, P>(k + bh * T * P, t0, len, T, Ks, LDP);
-    load_rows_plain<Tin, DV>(v + bh * T * DV, t0, len, T, Vs, DV);
-
-    const int t = threadIdx.x >> 1, half = threadIdx.x & 1;
-    float acc[CPT];
-#pragma unroll
-    for (int m = 0; m < CPT; ++m) acc[m] = 0.f;
-    float den = 0.f;
-
-    const float* Pc = Pre + (bh * NC + c) * (int64_t)N * DV;
-    const float* Pzc = Prez + (bh * NC + c) * (int64_t)N;
-    for (int a0 = 0; a0 < N; a0 += kTile) {
-        __syncthreads();
-        if (threadIdx.x < kTile) {
-            int i = 0, j = 0;
-            if (a0 + threadIdx.x < N) unpack_index(a0 + threadIdx.x, P, i, j);
-            Ii[threadIdx.x] = i;
-            Jj[threadIdx.x] = j;
-            Zt[threadIdx.x] = a0 + threadIdx.x < N ? Pzc[a0 + threadIdx.x] : 0.f;
-        }
-        for (int e = threadIdx.x; e < kTile * DV; e += blockDim.x) {
-            const int aa = e / DV;
-            St[e] = a0 + aa < N ? Pc[(int64_t)a0 * DV + e] : 0.f;
-        }
-        __syncthreads();
-        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
-            const int tt = e / kTile, aa = e - tt * kTile;
-            const int i = Ii[aa], j = Jj[aa];
-            const float scale = (i == j) ? 1.f : kSqrt2;
-            Ps[tt * LDT + aa] = a0 + aa < N ? Qs[tt * LDP + i] * Qs[tt * LDP + j] * scale : 0.f;
-        }
-        __syncthreads();
-        if (t < len) {
-            for (int aa = 0; aa < kTile; ++aa) {
-                const float ps = Ps[t * LDT + aa];
-                den = fmaf(ps, Zt[aa], den);
-#pragma unroll
-                for (int m = 0; m < CPT; ++m) acc[m] = fmaf(ps, St[aa * DV + half * CPT + m], acc[m]);
-            }
-        }
-    }
-    for (int s0 = 0; s0 < len; s0 += kTile) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < len * kTile; e += blockDim.x) {
-            const int tt = e / kTile, ss = e - tt * kTile, s = s0 + ss;
-            float d = 0.f;
-            if (s < len) {
-#pragma unroll 16
-                for (int i = 0; i < P; ++i) d = fmaf(Qs[tt * LDP + i], Ks[s * LDP + i], d);
-            }
-            Sc[tt * LDT + ss] = (s <= tt && s < len) ? d * d : 0.f;
-        }
-        __syncthreads();
-        if (t < len) {
-            for (int ss = 0; ss < kTile && s0 + ss < len; ++ss) {
-                const float sc = Sc[t * LDT + ss];
-                den += sc;
-#pragma unroll
-                for (int m = 0; m < CPT; ++m)
-                    acc[m] = fmaf(sc, Vs[(s0 + ss) * DV + half * CPT + m], acc[m]);
-            }
-        }
-    }
-    if (t < len) {
-        Tin* ot = o + (bh * T + t0 + t) * DV + half * CPT;
-#pragma unroll
-        for (int m = 0; m < CPT; ++m) store_as(ot + m, den > 0.f ? acc[m] / den : 0.f);
-    }
-}
-
 template <typename Tin, int P, int DV>
 cudaError_t states_typed(const void* k, const void* v, float* S, float* z, int BH, int T, int C,
                          cudaStream_t s) {
@@ -184,16 +80,16 @@ cudaError_t states_typed(const void* k, const void* v, float* S, float* z, int B
 template <typename Tin, int P, int DV>
 cudaError_t output_typed(const void* q, const void* k, const void* v, const float* Pre,
                          const float* Prez, void* o, int BH, int T, int C, cudaStream_t s) {
-    constexpr size_t smem = output_smem_bytes<P, DV>();
-    auto kern = chunk_output_simt_kernel<Tin, P, DV>;
+    constexpr size_t smem = chunk_out::output_smem_bytes<P, DV>();
+    auto kern = chunk_out::chunk_output_kernel<Tin, P, DV, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int NC = (T + C - 1) / C;
     dim3 grid(NC, BH);
     KATA_TRACED("chunk_output_simt", s,
-                kern<<<grid, kThreads, smem, s>>>(static_cast<const Tin*>(q), static_cast<const Tin*>(k),
-                                                  static_cast<const Tin*>(v), Pre, Prez,
-                                                  static_cast<Tin*>(o), T, C, NC));
+                kern<<<grid, chunk_out::kThreads, smem, s>>>(static_cast<const Tin*>(q), static_cast<const Tin*>(k),
+                                                             static_cast<const Tin*>(v), nullptr, Pre, Prez,
+                                                             static_cast<Tin*>(o), T, C, NC));
     return cudaGetLastError();
 }
 
