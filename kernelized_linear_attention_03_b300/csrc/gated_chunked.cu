@@ -1,4 +1,5 @@
-// Gated chunked forward on CUDA cores (fp32 arithmetic, any input dtype).
+// Gated chunked forward (fp32 accumulation, any input dtype; for bf16 inputs
+// the local states run on the tensor cores, the rest on CUDA cores).
 // One scalar gate gamma_t in [0, 1] per head and token scales the running
 // state before the token's own term is added,
 //   S_t = gamma_t S_{t-1} + psi(kh_t) v_t^T,   z_t = gamma_t z_{t-1} + psi(kh_t),
@@ -10,6 +11,9 @@
 //   output       num_t = (prod_{r=c C..t} gamma_r) psi(qh_t)^T P_c
 //                        + sum_{s in c, s<=t} (prod_{r=s+1..t} gamma_r) (qh_t.kh_s)^2 v_s,
 //                den_t likewise with 1 for v_s.
+// Local states: bf16, the tensor-core chunk-state kernel with each token's key
+// lift weighted by its decay to the chunk's end (gate_decay_kernel); fp32, a
+// CUDA-core kernel.  Output: the register-tiled kernel of simt_output.cuh.
 #include <type_traits>
 
 #include "kata_device.cuh"
